@@ -1,0 +1,331 @@
+"""Pins for the oracle against facts that do not come from the oracle itself.
+
+Each test checks the plain C reference against something fixed by the pages or by
+mathematics: a hand-derived stream, the correctly rounded sum (math.fsum), the Gaussian
+escape-rate argmin the window rule stands for, the constant re-derived with mpmath, the
+closed-form size and "about 11 bits per value" (ZipCCL, "Key idea and contribution"), and
+exhaustive round trips.  A plausible mistake in the oracle -- a wrong shift, a dropped
+rounding, an off-by-one window, a transposed section -- fails at least one of them.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from lossless_bf16_compression_gb300 import workloads
+
+CHUNK = 4096
+
+
+def pad16(v):
+    return (v + 15) // 16 * 16
+
+
+def bf16_to_float(bits):
+    """Exact Python floats of BF16 bit patterns (through fp32, which holds them exactly)."""
+    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+    with np.errstate(invalid="ignore"):
+        return b.view(np.float32).astype(np.float64)
+
+
+def closed_form_size(x, e0):
+    """Stream length from the size formula, with escapes counted by a per-chunk histogram."""
+    n = x.size
+    N = (n + CHUNK - 1) // CHUNK
+    E = (x.astype(np.int64) >> 7) & 0xFF
+    escape = (E < e0) | (E > e0 + 6)
+    total = pad16(32 + 8 * (N + 1))
+    for c in range(N):
+        m = min(CHUNK, n - c * CHUNK)
+        k = int(escape[c * CHUNK:c * CHUNK + m].sum())
+        total += 16 + pad16((3 * m + 7) // 8) + pad16(m) + pad16(3 * k)
+    return total
+
+
+# ----------------------------------------------------------------------------- golden
+
+
+def test_golden_stream_matches_hand_derivation(golden_tiny):
+    e0, values, stream = golden_tiny
+    got = oracle.compress(values, e0)
+    assert got.tobytes() == stream.tobytes()
+    st, back = oracle.decompress(stream, values.size)
+    assert st == oracle.OK
+    assert np.array_equal(back, values)
+
+
+# ----------------------------------------------------------------------------- window rule
+
+
+def _derive_c2_mpmath():
+    mp = pytest.importorskip("mpmath")
+    mp.mp.dps = 40
+    f = lambda t: mp.erf(t / mp.sqrt(2)) + mp.erfc(128 * t / mp.sqrt(2))  # noqa: E731
+    u = mp.findroot(lambda u: f(u) - f(2 * u), 0.019)
+    return mp, (2 * u) ** 2
+
+
+def test_window_constant_rederived():
+    """c = 2u with f(u) = f(2u): the switching point between adjacent 7-binade windows."""
+    mp, c2 = _derive_c2_mpmath()
+    assert oracle.window_constant() == float(c2)
+
+
+def _gaussian_escape_rate(mp, e0, sigma):
+    lo = mp.mpf(2) ** (e0 - 127)
+    hi = mp.mpf(2) ** (e0 - 120)
+    s = mp.mpf(sigma) * mp.sqrt(2)
+    return mp.erf(lo / s) + mp.erfc(hi / s)
+
+
+def test_window_is_gaussian_escape_argmin():
+    """For a tensor whose RMS is sigma (a constant tensor), e0 must be the integer base whose
+    7-binade window has the fewest expected escapes under N(0, sigma^2)."""
+    mp, _ = _derive_c2_mpmath()
+    mp.mp.dps = 30
+    checked = 0
+    for bits in range(0x3000, 0x5000, 7):  # sigma from about 5e-10 to 3e9
+        sigma = float(bf16_to_float([bits])[0])
+        rates = {e: _gaussian_escape_rate(mp, e, sigma) for e in range(0, 250)
+                 if abs(e - (math.log2(sigma) + 122.3)) < 4}
+        best = min(rates, key=lambda e: rates[e])
+        second = sorted(rates.values())[1]
+        if abs(second - rates[best]) < 1e-9 * rates[best]:
+            continue  # a tie: both windows are optimal
+        x = np.full(3, bits, dtype=np.uint16)
+        assert oracle.choose_e0(x) == best, hex(bits)
+        checked += 1
+    assert checked > 1000
+
+
+def test_constant_tensors_follow_log2_rule():
+    """Every positive finite BF16 constant: e0 = clamp(floor(log2(|v| c)) + 127, 0, 249)."""
+    mp, c2 = _derive_c2_mpmath()
+    c = mp.sqrt(c2)
+    for bits in range(1, 0x7F80):
+        v = mp.mpf(float(bf16_to_float([bits])[0]))
+        t = mp.log(v * c, 2)
+        if abs(t - mp.nint(t)) < 1e-12:
+            continue
+        want = min(249, max(0, int(mp.floor(t)) + 127))
+        x = np.array([bits, bits | 0x8000], dtype=np.uint16)  # sign does not matter
+        assert oracle.choose_e0(x) == want, hex(bits)
+
+
+def test_special_cases():
+    assert oracle.choose_e0(np.zeros(0, np.uint16)) == 0
+    assert oracle.choose_e0(np.zeros(1000, np.uint16)) == 0
+    assert oracle.choose_e0(np.full(10, 0x8000, np.uint16)) == 0  # -0.0
+    assert oracle.choose_e0(np.array([0x7F80, 0xFF80, 0x7FC0], np.uint16)) == 0  # no finite value
+    assert oracle.choose_e0(np.full(10, 0x3F80, np.uint16)) == 122  # 1.0: window 122..128
+    # a non-finite value changes neither the sum nor the count
+    x = np.full(10, 0x3F80, np.uint16)
+    assert oracle.choose_e0(np.concatenate([x, [0x7FC0, 0xFF80]]).astype(np.uint16)) == 122
+
+
+# ----------------------------------------------------------------------------- exact sum
+
+
+def _fsum_reference(bits):
+    v = bf16_to_float(bits)
+    fin = np.isfinite(v)
+    return math.fsum((v[fin] * v[fin]).tolist()), int(fin.sum())
+
+
+@pytest.mark.parametrize("case", ["gauss", "patterns", "tiny", "huge", "mixed", "weight_1m"])
+def test_sum_of_squares_is_correctly_rounded(case):
+    rng = np.random.default_rng(11)
+    if case == "gauss":
+        x = workloads.fp32_to_bf16_bits(rng.standard_normal(300_000).astype(np.float32))
+    elif case == "patterns":
+        x = workloads.random_patterns(300_000, 12)
+    elif case == "tiny":  # subnormals and the smallest normals only
+        x = rng.integers(0, 0x0200, 50_000).astype(np.uint16)
+    elif case == "huge":  # the largest finite values
+        x = rng.integers(0x7E00, 0x7F80, 50_000).astype(np.uint16)
+    elif case == "mixed":  # one huge value among many tiny ones: the sum must not lose either
+        x = rng.integers(0x0001, 0x0080, 200_000).astype(np.uint16)
+        x[::50_000] = 0x7F7F
+    else:
+        x = workloads.weight_1m()
+    S_d, n_f = oracle.sum_squares(x)
+    want_S, want_nf = _fsum_reference(x)
+    assert n_f == want_nf
+    assert S_d == want_S
+
+
+def test_sum_tie_rounds_to_even():
+    # 128 squares of 2^23 sum to 2^53, where the fp64 spacing is 2; adding squares of 1.0
+    # lands exactly halfway between two neighbours, so the rounding must pick the even one.
+    one = 0x3F80  # 1.0 -> square 1
+    big = 0x4B00  # 2^23 -> square 2^46
+    x = np.array([big] * 128 + [one], dtype=np.uint16)  # 2^53 + 1: a tie between 2^53 and 2^53+2
+    S_d, _ = oracle.sum_squares(x)
+    assert S_d == 2.0 ** 53  # ties to even
+    x = np.array([big] * 128 + [one, one, one], dtype=np.uint16)  # 2^53 + 3: tie -> 2^53 + 4
+    S_d, _ = oracle.sum_squares(x)
+    assert S_d == 2.0 ** 53 + 4
+    assert S_d == math.fsum([2.0 ** 46] * 128 + [1.0] * 3)
+
+
+# ----------------------------------------------------------------------------- size
+
+
+@pytest.mark.parametrize("n", [0, 1, 7, 8, 9, 15, 16, 17, 43, 171, 4095, 4096, 4097, 4139, 8191, 12288, 12345])
+def test_size_closed_form_around_chunk_edges(n):
+    rng = np.random.default_rng(n)
+    x = workloads.fp32_to_bf16_bits(rng.standard_normal(n).astype(np.float32))
+    mask = rng.random(n) < 0.1
+    x[mask] = rng.integers(0, 1 << 16, int(mask.sum())).astype(np.uint16)
+    for e0 in (-1, 0, 100, 122, 249):
+        s = oracle.compress(x, e0)
+        used = s[7] if e0 == -1 else e0
+        assert len(s) == closed_form_size(x, int(used))
+        st, back = oracle.decompress(s, n)
+        assert st == oracle.OK and np.array_equal(back, x)
+
+
+def test_about_eleven_bits_per_value():
+    """No escapes: 16 -> about 11 bits per value, about 31% less volume (the page's ideal)."""
+    rng = np.random.default_rng(5)
+    n = 1 << 20
+    e0 = 122
+    exps = rng.integers(e0, e0 + 7, n)
+    x = ((rng.integers(0, 2, n) << 15) | (exps << 7) | rng.integers(0, 128, n)).astype(np.uint16)
+    s = oracle.compress(x, e0)
+    bits_per_value = 8 * len(s) / n
+    assert 11.0 <= bits_per_value < 11.05
+    assert abs((1 - len(s) / (2 * n)) - 0.31) < 0.005
+    assert len(s) == closed_form_size(x, e0)
+
+
+def test_worst_case_matches_max_stream_bytes():
+    for n in (1, 4096, 4097, 10000):
+        x = np.zeros(n, np.uint16)  # exponent 0 is outside every window with e0 >= 1
+        s = oracle.compress(x, 5)
+        assert len(s) == oracle.max_stream_bytes(n)
+
+
+# ----------------------------------------------------------------------------- round trips
+
+
+def test_all_patterns_round_trip_every_base():
+    x = workloads.all_patterns()
+    for e0 in [-1] + list(range(250)):
+        s = oracle.compress(x, e0)
+        used = int(s[7])
+        if e0 >= 0:
+            assert used == e0
+        assert len(s) == closed_form_size(x, used)
+        st, back = oracle.decompress(s, x.size)
+        assert st == oracle.OK
+        assert np.array_equal(back, x)
+
+
+def test_every_pattern_as_single_value():
+    x = workloads.all_patterns()
+    for b in x:
+        one = np.array([b], np.uint16)
+        s = oracle.compress(one)
+        E = (int(b) >> 7) & 0xFF
+        k = 0 if s[7] <= E <= s[7] + 6 else 1
+        assert len(s) == 48 + 16 + 16 + 16 + 16 * k
+        st, back = oracle.decompress(s, 1)
+        assert st == oracle.OK and back[0] == b
+
+
+_ALPHABET = np.array(
+    [0x0000, 0x8000, 0x0001, 0x807F, 0x0080, 0x00FF, 0x3C00, 0x3D00, 0x3D80, 0x3E00, 0x3E80,
+     0x3F00, 0x3F80, 0xBF80, 0x4000, 0x4080, 0x4100, 0x4180, 0x4200, 0x4280, 0x4300, 0x4380,
+     0x7F00, 0x7F7F, 0xFF7F, 0x7F80, 0xFF80, 0x7FC0, 0xFFC1, 0x7F81, 0x3FFF, 0xBFFF, 0x0100,
+     0x1000, 0x2000, 0x3000, 0x3800, 0x3A00, 0x3B00, 0x3B80, 0x3C80, 0x3E7F, 0x3EFF, 0x3F7F,
+     0x407F, 0x40FF, 0x417F, 0x41FF, 0x427F, 0x42FF, 0x437F, 0x4400, 0x4500, 0x5000, 0x6000,
+     0x7000, 0x7E00, 0xC000, 0xC100, 0xC300, 0xC400, 0xBE00, 0xBD00, 0x3D40],
+    dtype=np.uint16)
+
+
+def test_brute_force_pairs():
+    """Every 2-value tensor over a 64-pattern alphabet, under several bases."""
+    assert len(set(_ALPHABET.tolist())) == 64
+    bases = [-1, 0, 1, 60, 120, 121, 122, 123, 124, 125, 126, 127, 248, 249]
+    for a in _ALPHABET:
+        for b in _ALPHABET:
+            x = np.array([a, b], np.uint16)
+            for e0 in bases:
+                s = oracle.compress(x, e0)
+                assert len(s) == closed_form_size(x, int(s[7]))
+                st, back = oracle.decompress(s, 2)
+                assert st == oracle.OK and np.array_equal(back, x)
+
+
+def test_brute_force_triples():
+    alpha = _ALPHABET[::4]
+    assert alpha.size == 16
+    for a in alpha:
+        for b in alpha:
+            for c in alpha:
+                x = np.array([a, b, c], np.uint16)
+                for e0 in (-1, 0, 122, 249):
+                    s = oracle.compress(x, e0)
+                    assert len(s) == closed_form_size(x, int(s[7]))
+                    st, back = oracle.decompress(s, 3)
+                    assert st == oracle.OK and np.array_equal(back, x)
+
+
+# ----------------------------------------------------------------------------- canonical form
+
+
+def _bijection_under_flips(stream, n):
+    accepted = 0
+    for pos in range(len(stream)):
+        for bit in range(8):
+            t = stream.copy()
+            t[pos] ^= 1 << bit
+            st, back = oracle.decompress(t, n)
+            if st == oracle.OK:
+                # an accepted stream must be exactly what the encoder writes for its content
+                assert oracle.compress(back, int(t[7])).tobytes() == t.tobytes(), (pos, bit)
+                accepted += 1
+    return accepted
+
+
+def test_decoder_accepts_only_canonical_streams(golden_tiny):
+    e0, values, stream = golden_tiny
+    accepted = _bijection_under_flips(stream, values.size)
+    assert accepted > 0  # flips of sign/mantissa bits or in-window codes stay valid
+    rng = np.random.default_rng(3)
+    x = workloads.fp32_to_bf16_bits(rng.standard_normal(37).astype(np.float32))
+    _bijection_under_flips(oracle.compress(x), x.size)
+
+
+def test_decoder_rejections(golden_tiny):
+    e0, values, stream = golden_tiny
+    assert oracle.decompress(stream, 6)[0] == oracle.ERR_SIZE_MISMATCH
+    assert oracle.decompress(stream[:-16], 5)[0] == oracle.ERR_CORRUPT  # truncated
+    t = stream.copy(); t[0] = 0  # magic  # noqa: E702
+    assert oracle.decompress(t, 5)[0] == oracle.ERR_CORRUPT
+    t = stream.copy(); t[7] = 250  # base out of range  # noqa: E702
+    assert oracle.decompress(t, 5)[0] == oracle.ERR_CORRUPT
+    t = stream.copy(); t[16 * 6 + 6] = 1  # nonzero escape padding (after 2+2+1+1 bytes)  # noqa: E702
+    assert oracle.decompress(t, 5)[0] == oracle.ERR_CORRUPT
+    t = stream.copy(); t[16 * 6 + 4] = 130  # escape exponent inside the window  # noqa: E702
+    assert oracle.decompress(t, 5)[0] == oracle.ERR_CORRUPT
+
+
+# ----------------------------------------------------------------------------- statistics
+
+
+def test_gaussian_escape_rate_matches_model():
+    """N(0,1): window 122..128, so escapes are |x| < 2^-5 or |x| >= 4."""
+    x = workloads.sweep(20)
+    s = oracle.compress(x)
+    assert s[7] == 122
+    rec = int.from_bytes(s[32:40].tobytes(), "little")
+    N = 256
+    k = sum(int.from_bytes(s[o:o + 4].tobytes(), "little")
+            for o in [int.from_bytes(s[32 + 8 * c:40 + 8 * c].tobytes(), "little") for c in range(N)])
+    assert rec == pad16(32 + 8 * (N + 1))
+    p = math.erf(2.0 ** -5 / math.sqrt(2)) + math.erfc(4.0 / math.sqrt(2))
+    n = x.size
+    assert abs(k - p * n) < 5 * math.sqrt(n * p * (1 - p))
