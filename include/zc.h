@@ -1,0 +1,144 @@
+/*
+ * zc.h -- C ABI of the GB300 lossless BF16 exponent codec.
+ *
+ * The operation is the exponent coding of "ZipCCL: Efficient Lossless Data Compression of
+ * Communication Collectives for Accelerating LLM Training" (SIGCOMM scribe notes), section
+ * "Key idea and contribution", first technique: the frequent-exponent window is taken
+ * directly from the tensor's standard deviation (no histogram, no sort), in-window exponents
+ * are stored in 3 bits instead of 8, out-of-window exponents keep their full 8 bits in a
+ * separate list so that reconstruction is exact, and sign and mantissa travel unchanged --
+ * about 11 bits per value instead of 16.  The second technique of the same section
+ * ("GPU-optimized compression and decompression kernels": communication-aware layout,
+ * aligned global and shared memory access, data movement pipelined with compute) is what the
+ * kernels behind these calls implement for sm_103a.
+ *
+ * Stream format "ZCB1" (little-endian, every section zero-padded to a multiple of 16 bytes):
+ *   header   32 B   "ZCB1", u16 version = 1, u8 log2(chunk) = 12, u8 e0, u64 n, u64 N,
+ *                   u64 total_bytes                      (N = ceil(n / 4096) chunks)
+ *   offsets  u64[N+1], absolute byte offset of each chunk record; offsets[N] = total_bytes
+ *   records  at pad16(32 + 8 (N+1)), in chunk order, back to back.  A record of m values
+ *            with k escapes is: u32 k, u32 m, u64 0; 3-bit codes, code i at bits [3i, 3i+3)
+ *            least significant bit first (pad16(ceil(3m/8)) B); one sign|mantissa byte per
+ *            value, (x >> 8 & 0x80) | (x & 0x7F) (pad16(m) B); u16 positions then u8 full
+ *            exponents of the escapes in ascending position order (pad16(3k) B).
+ *   Code c < 7 means exponent e0 + c; code 7 means "escape".  e0 is in [0, 249].
+ * A full chunk without escapes costs 5648 B for 4096 values: 11.03 bits per value.
+ *
+ * All entry points are host functions.  Pointers called "device" may be any address the GPU
+ * can dereference (cudaMalloc, managed, or mapped pinned memory).  Every call is
+ * asynchronous in the order of `stream` and never synchronizes, except where stated.
+ */
+#ifndef ZC_H
+#define ZC_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;
+typedef struct CUstream_st* cudaStream_t; /* the CUDA runtime's own stream handle type */
+
+/* ------------------------------------------------------------------ status codes */
+#define ZC_OK 0
+#define ZC_ERR_INVALID_ARG 1   /* null pointer, base outside [0,249] and not ZC_BASE_AUTO,
+                                  n > ZC_MAX_N, overlapping buffers                        */
+#define ZC_ERR_MISALIGNED 2    /* in/out not 16-byte aligned, out_bytes not 8-byte aligned  */
+#define ZC_ERR_CUDA 3          /* a CUDA runtime call or a launch failed                    */
+#define ZC_ERR_CORRUPT 4       /* device-side: the stream is not one the encoder writes     */
+#define ZC_ERR_SIZE_MISMATCH 5 /* device-side: the stream holds a different n               */
+#define ZC_ERR_TIMEOUT 6       /* device-side: a bounded wait inside a kernel ran out       */
+
+#define ZC_BASE_AUTO (-1)               /* choose the window base from the data */
+#define ZC_MAX_N ((size_t)1 << 40)      /* largest supported number of values   */
+#define ZC_CHUNK_VALUES 4096
+
+/* ------------------------------------------------------------------ sizes */
+
+/* Bytes the caller must provide at `out` for zc_compress of n values: the worst-case stream
+ * (every value escaping, 17,936 B per full chunk, plus header and offset table) followed by
+ * the call's workspace (look-back state, 8 B per chunk, and a 16.25 KiB control block).
+ * Pure host function; makes no CUDA call.  Returns 0 when n > ZC_MAX_N. */
+size_t zc_max_compressed_bytes(size_t n);
+
+/* Worst-case stream length alone (no workspace).  Pure host function. */
+size_t zc_max_stream_bytes(size_t n);
+
+/* ------------------------------------------------------------------ compress */
+
+/* Compress n BF16 values (raw bit patterns) into one "ZCB1" stream.
+ *   in            device, n x u16, 16-byte aligned, read only.
+ *   n             number of values, 0 <= n <= ZC_MAX_N.  n = 0 gives a 48-byte stream.
+ *   base_or_auto  ZC_BASE_AUTO: e0 = floor(log2(sigma * c)) + 127 clamped to [0, 249], with
+ *                 sigma the root mean square of the finite values and c^2 =
+ *                 0x1.79a1e790e0f01p-10 (the window with the fewest expected escapes for a
+ *                 Gaussian; "determines the frequent exponent range directly from the tensor
+ *                 standard deviation").  0..249: use that e0.  The stream depends only on
+ *                 (input bits, e0): both modes give identical bytes for the same e0.
+ *   out           device, zc_max_compressed_bytes(n) bytes, 16-byte aligned, must not overlap
+ *                 `in`.  The stream is written from out[0]; the bytes past *out_bytes,
+ *                 including the workspace tail, are unspecified afterwards.  The library keeps
+ *                 no per-call state outside `out`, so calls on different streams with
+ *                 different buffers may run concurrently.
+ *   out_bytes     receives the stream length.  Device, managed or pinned host memory is
+ *                 written by the last kernel (asynchronously).  Pageable host memory is also
+ *                 accepted: the call then copies the length back and synchronizes `stream`.
+ * The chosen e0 is byte 7 of the stream.  Returns ZC_OK or a host-side error code
+ * (ZC_ERR_INVALID_ARG, ZC_ERR_MISALIGNED, ZC_ERR_CUDA); device-side errors
+ * (ZC_ERR_TIMEOUT) are reported through zc_status. */
+int zc_compress(const void* in, size_t n, int base_or_auto, void* out, size_t* out_bytes,
+                cudaStream_t stream);
+
+/* ------------------------------------------------------------------ decompress */
+
+/* Decompress a "ZCB1" stream back into n BF16 bit patterns (the exact input of compress).
+ *   in      device, 16-byte aligned; must hold the stream's total_bytes (header bytes 24..31)
+ *           readable bytes.  The kernel checks every offset and size against the header, the
+ *           largest stream n values can produce and each record's own sizes, and reads only
+ *           inside [0, total_bytes).
+ *   out     device, n x u16, 16-byte aligned, must not overlap `in`.
+ *   n       the number of values the caller expects; a stream holding another n sets
+ *           ZC_ERR_SIZE_MISMATCH.
+ * Any stream the encoder could not have written (bad magic, version, base, offsets, sizes,
+ * escape positions or exponents, nonzero padding) sets ZC_ERR_CORRUPT; `out` is then
+ * unspecified.  Device-side errors are read with zc_status. */
+int zc_decompress(const void* in, void* out, size_t n, cudaStream_t stream);
+
+/* ------------------------------------------------------------------ status */
+
+/* Synchronize `stream`, then return the first device-side error recorded on the current
+ * device since the last reset (ZC_OK if none).  The status word is shared by all streams of
+ * the device; reset != 0 clears it.  Returns ZC_ERR_CUDA if the synchronization fails. */
+int zc_status(cudaStream_t stream, int reset);
+
+/* ------------------------------------------------------------------ kernel timing */
+
+#define ZC_KERNEL_STATS 1
+#define ZC_KERNEL_ENCODE 2
+#define ZC_KERNEL_DECODE 3
+
+/* enable != 0: bracket every kernel the library launches from now on with CUDA events on the
+ * kernel's own stream.  enable == 0: stop recording.  Returns ZC_OK or ZC_ERR_CUDA. */
+int zc_timing_enable(int enable);
+
+/* Wait for the recorded events, write up to `max` (kernel id, milliseconds) pairs, oldest
+ * first, drop them from the record and return how many were written (negative ZC_ERR_CUDA on
+ * failure).  Records beyond `max` are dropped too. */
+int zc_timing_collect(int* kernel_ids, float* ms, int max);
+
+/* ------------------------------------------------------------------ test hook */
+
+/* zc_compress with a planted stall, for testing the bounded waits: chunk `stalled_chunk`
+ * never publishes its look-back state, so the next chunk's wait runs out after about
+ * `spin_limit` polls and the call reports ZC_ERR_TIMEOUT through zc_status instead of
+ * hanging.  The stream written is then incomplete.  No counterpart on the pages. */
+int zc_compress_stall_test(const void* in, size_t n, int base_or_auto, void* out,
+                           size_t* out_bytes, cudaStream_t stream, size_t stalled_chunk,
+                           unsigned spin_limit);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ZC_H */

@@ -1,0 +1,219 @@
+// zc_api.cu -- the C ABI: argument checks, workspace set-up, launches, status and timing.
+//
+// Call sequence of zc_compress (ZipCCL SIGCOMM scribe notes, "Key idea and contribution":
+// window from the standard deviation, 3-bit codes, separate full exponents):
+//   1. clear the workspace in the tail of `out` (one memset on `stream`);
+//   2. statistics kernel (auto mode only): sum of squares, non-finite count, e0;
+//   3. encode kernel: codes, sign|mantissa plane, escapes, look-back scan, records.
+// zc_decompress is one decode kernel.  No call synchronizes except zc_status, and
+// zc_compress when `out_bytes` is pageable host memory.
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "zc_common.cuh"
+
+namespace zc {
+namespace {
+
+__device__ int g_status;  // first device-side error since the last reset, per device
+
+constexpr int kMaxDevices = 64;
+constexpr unsigned kDefaultSpinLimit = 1u << 20;
+
+std::mutex g_mutex;
+DeviceInfo g_devices[kMaxDevices];
+bool g_device_ready[kMaxDevices];
+
+struct TimingRecord {
+  int kernel;
+  cudaEvent_t start, stop;
+};
+bool g_timing = false;
+std::vector<TimingRecord> g_records;
+std::vector<cudaEvent_t> g_event_pool;
+TimingRecord g_open;
+bool g_open_valid = false;
+
+cudaEvent_t take_event() {
+  if (!g_event_pool.empty()) {
+    cudaEvent_t e = g_event_pool.back();
+    g_event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return na && nb && x < y + nb && y < x + na;
+}
+
+}  // namespace
+
+cudaError_t device_info(DeviceInfo* info) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (!g_device_ready[dev]) {
+    DeviceInfo d{};
+    err = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev);
+    if (err != cudaSuccess) return err;
+    err = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status), g_status);
+    if (err != cudaSuccess) return err;
+    g_devices[dev] = d;
+    g_device_ready[dev] = true;
+  }
+  *info = g_devices[dev];
+  return cudaSuccess;
+}
+
+void timing_begin(int kernel_id, cudaStream_t stream) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (!g_timing) return;
+  g_open.kernel = kernel_id;
+  g_open.start = take_event();
+  g_open.stop = take_event();
+  g_open_valid = g_open.start && g_open.stop;
+  if (g_open_valid) cudaEventRecord(g_open.start, stream);
+}
+
+void timing_end(cudaStream_t stream) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (!g_timing || !g_open_valid) return;
+  cudaEventRecord(g_open.stop, stream);
+  g_records.push_back(g_open);
+  g_open_valid = false;
+}
+
+}  // namespace zc
+
+using namespace zc;
+
+namespace {
+
+int compress_impl(const void* in, size_t n, int base, void* out, size_t* out_bytes, cudaStream_t stream,
+                  uint64_t stall_chunk, unsigned spin_limit) {
+  if (n > ZC_MAX_N || base < ZC_BASE_AUTO || base > kE0Max) return ZC_ERR_INVALID_ARG;
+  if (out == nullptr || out_bytes == nullptr || (n > 0 && in == nullptr)) return ZC_ERR_INVALID_ARG;
+  if (!aligned(in, 16) || !aligned(out, 16) || !aligned(out_bytes, 8)) return ZC_ERR_MISALIGNED;
+  const size_t cap = zc_max_compressed_bytes(n);
+  if (overlap(in, 2 * n, out, cap)) return ZC_ERR_INVALID_ARG;
+
+  DeviceInfo dev;
+  if (device_info(&dev) != cudaSuccess) return ZC_ERR_CUDA;
+
+  // Where the kernel writes the length: any device-visible address, else the control block.
+  cudaPointerAttributes attr;
+  if (cudaPointerGetAttributes(&attr, out_bytes) != cudaSuccess) {
+    cudaGetLastError();
+    return ZC_ERR_CUDA;
+  }
+  unsigned long long* len_ptr = nullptr;
+  const bool pageable = attr.type == cudaMemoryTypeUnregistered || attr.devicePointer == nullptr;
+  if (!pageable) len_ptr = static_cast<unsigned long long*>(attr.devicePointer);
+
+  uint8_t* o = static_cast<uint8_t*>(out);
+  const uint64_t ws = workspace_offset(n);
+  if (cudaMemsetAsync(o + ws, 0, workspace_bytes(n), stream) != cudaSuccess) return ZC_ERR_CUDA;
+  const uint16_t* x = static_cast<const uint16_t*>(in);
+  if (n > 0 && base == ZC_BASE_AUTO) {
+    if (launch_stats(x, n, o, dev, stream) != cudaSuccess) return ZC_ERR_CUDA;
+  }
+  if (launch_encode(x, n, base, o, len_ptr, dev, stream, stall_chunk, spin_limit) != cudaSuccess)
+    return ZC_ERR_CUDA;
+  if (pageable) {
+    unsigned long long total = 0;
+    const Control* ctrl = reinterpret_cast<const Control*>(o + ws);
+    if (cudaMemcpyAsync(&total, &ctrl->total, sizeof total, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+      return ZC_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return ZC_ERR_CUDA;
+    *out_bytes = static_cast<size_t>(total);
+  }
+  return ZC_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t zc_max_stream_bytes(size_t n) {
+  if (n > ZC_MAX_N) return 0;
+  return static_cast<size_t>(max_stream_bytes(n));
+}
+
+size_t zc_max_compressed_bytes(size_t n) {
+  if (n > ZC_MAX_N) return 0;
+  return static_cast<size_t>(workspace_offset(n) + workspace_bytes(n));
+}
+
+int zc_compress(const void* in, size_t n, int base_or_auto, void* out, size_t* out_bytes, cudaStream_t stream) {
+  return compress_impl(in, n, base_or_auto, out, out_bytes, stream, ~uint64_t(0), kDefaultSpinLimit);
+}
+
+int zc_compress_stall_test(const void* in, size_t n, int base_or_auto, void* out, size_t* out_bytes,
+                           cudaStream_t stream, size_t stalled_chunk, unsigned spin_limit) {
+  return compress_impl(in, n, base_or_auto, out, out_bytes, stream, stalled_chunk, spin_limit);
+}
+
+int zc_decompress(const void* in, void* out, size_t n, cudaStream_t stream) {
+  if (n > ZC_MAX_N || in == nullptr || (n > 0 && out == nullptr)) return ZC_ERR_INVALID_ARG;
+  if (!aligned(in, 16) || !aligned(out, 16)) return ZC_ERR_MISALIGNED;
+  if (overlap(in, kHeaderBytes, out, 2 * n)) return ZC_ERR_INVALID_ARG;
+  DeviceInfo dev;
+  if (device_info(&dev) != cudaSuccess) return ZC_ERR_CUDA;
+  if (launch_decode(static_cast<const uint8_t*>(in), static_cast<uint16_t*>(out), n, dev, stream) != cudaSuccess)
+    return ZC_ERR_CUDA;
+  return ZC_OK;
+}
+
+int zc_status(cudaStream_t stream, int reset) {
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return ZC_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_status, sizeof v) != cudaSuccess) return ZC_ERR_CUDA;
+  if (reset) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_status, &zero, sizeof zero) != cudaSuccess) return ZC_ERR_CUDA;
+  }
+  return v;
+}
+
+int zc_timing_enable(int enable) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  g_timing = enable != 0;
+  return ZC_OK;
+}
+
+int zc_timing_collect(int* kernel_ids, float* ms, int max) {
+  std::vector<TimingRecord> recs;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    recs.swap(g_records);
+  }
+  int written = 0;
+  int result = 0;
+  for (const TimingRecord& r : recs) {
+    float t = 0.f;
+    if (cudaEventSynchronize(r.stop) != cudaSuccess || cudaEventElapsedTime(&t, r.start, r.stop) != cudaSuccess)
+      result = -ZC_ERR_CUDA;
+    if (written < max && kernel_ids && ms) {
+      kernel_ids[written] = r.kernel;
+      ms[written] = t;
+      ++written;
+    }
+  }
+  std::lock_guard<std::mutex> lock(g_mutex);
+  for (const TimingRecord& r : recs) {
+    g_event_pool.push_back(r.start);
+    g_event_pool.push_back(r.stop);
+  }
+  return result < 0 ? result : written;
+}
+
+}  // extern "C"

@@ -1,0 +1,290 @@
+// zc_common.cuh -- layout arithmetic, workspace, PTX wrappers and the block scan shared by the
+// sm_103a kernels of the lossless BF16 exponent codec.
+//
+// Method: ZipCCL (SIGCOMM scribe notes), "Key idea and contribution": exponent coding with a
+// window taken from the standard deviation (first technique) and GPU kernels with a
+// communication-aware layout, aligned global/shared memory access and data movement pipelined
+// with compute (second technique).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "zc.h"
+
+namespace zc {
+
+// ------------------------------------------------------------------ stream layout ("ZCB1")
+
+constexpr int kChunk = 4096;                       // values per chunk record
+constexpr int kHeaderBytes = 32;                   // stream header
+constexpr int kRecordHeaderBytes = 16;             // u32 k, u32 m, u64 reserved
+constexpr int kFullCodeBytes = 3 * kChunk / 8;     // 1536: 3-bit codes of a full chunk
+constexpr int kMaxRecordBytes = kRecordHeaderBytes + kFullCodeBytes + kChunk + 3 * kChunk;  // 17936
+constexpr int kE0Max = 249;
+constexpr unsigned long long kMagicWord =          // bytes 0..6 of the header: "ZCB1", v1, 12
+    0x5Aull | (0x43ull << 8) | (0x42ull << 16) | (0x31ull << 24) | (1ull << 32) | (12ull << 48);
+
+__host__ __device__ inline uint64_t pad16(uint64_t v) { return (v + 15u) & ~uint64_t(15); }
+__host__ __device__ inline uint64_t num_chunks(uint64_t n) { return (n + kChunk - 1) / kChunk; }
+__host__ __device__ inline uint64_t records_base(uint64_t n) {
+  return pad16(kHeaderBytes + 8 * (num_chunks(n) + 1));
+}
+__host__ __device__ inline uint64_t code_section_bytes(uint64_t m) { return pad16((3 * m + 7) / 8); }
+__host__ __device__ inline uint64_t record_bytes(uint64_t m, uint64_t k) {
+  return kRecordHeaderBytes + code_section_bytes(m) + pad16(m) + pad16(3 * k);
+}
+// Values in chunk c of an n-value tensor (c < num_chunks(n)).
+__host__ __device__ inline unsigned chunk_values(uint64_t n, uint64_t c) {
+  const uint64_t left = n - c * kChunk;
+  return left < static_cast<uint64_t>(kChunk) ? static_cast<unsigned>(left) : static_cast<unsigned>(kChunk);
+}
+__host__ __device__ inline uint64_t max_stream_bytes(uint64_t n) {
+  const uint64_t full = n / kChunk, rem = n % kChunk;
+  return records_base(n) + full * kMaxRecordBytes + (rem ? record_bytes(rem, rem) : 0);
+}
+
+// ------------------------------------------------------------------ workspace (tail of `out`)
+//
+// [ws + 0,    ws + 256)            Control block
+// [ws + 256,  ws + 256 + 16 KiB)   per-CTA partials of the statistics pass
+// [ws + 16640, ...)                look-back state, one u64 per chunk
+constexpr int kStatsMaxCtas = 1024;
+constexpr uint64_t kWsControlBytes = 256;
+constexpr uint64_t kWsPartialsBytes = 16ull * kStatsMaxCtas;
+
+struct Control {
+  unsigned encode_ticket;   // next chunk to hand out (encoder)
+  unsigned stats_done;      // CTAs of the statistics pass that have finished
+  int e0;                   // window base chosen by the statistics pass
+  unsigned exact_path;      // 1 when the statistics pass needed its exact fallback
+  unsigned long long total; // stream length, for the pageable out_bytes path
+};
+
+struct StatsPartial {
+  double sum;               // fp64 sum of block sums of squares
+  unsigned long long nonfinite;
+};
+
+__host__ __device__ inline uint64_t workspace_offset(uint64_t n) {
+  return (max_stream_bytes(n) + 255) & ~uint64_t(255);
+}
+__host__ __device__ inline uint64_t workspace_bytes(uint64_t n) {
+  return kWsControlBytes + kWsPartialsBytes + 8 * num_chunks(n);
+}
+
+// Look-back state word: bits 62..63 status, bits 0..61 value.
+constexpr unsigned long long kFlagAggregate = 1ull << 62;   // value = this chunk's record size
+constexpr unsigned long long kFlagInclusive = 2ull << 62;   // value = sizes up to and including it
+constexpr unsigned long long kFlagValueMask = (1ull << 62) - 1;
+
+// ------------------------------------------------------------------ errors
+
+__device__ __forceinline__ void set_error(int* status, int code) { atomicCAS(status, 0, code); }
+
+__device__ __forceinline__ int read_status(const int* status) {
+  int v;
+  asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(status) : "memory");
+  return v;
+}
+
+// ------------------------------------------------------------------ PTX wrappers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, unsigned count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, unsigned bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, unsigned parity) {
+  unsigned ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait on an mbarrier phase; false when the limit ran out.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, unsigned parity, unsigned limit) {
+  for (unsigned i = 0; i < limit; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+
+// Bulk (non-tensor) async copies: 16-byte aligned addresses, size a multiple of 16.
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, unsigned bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(smem_dst)),
+      "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void bulk_store(void* gdst, const void* smem_src, unsigned bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),
+               "r"(smem_u32(smem_src)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+template <int N>
+__device__ __forceinline__ void bulk_wait_all() {
+  asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+// Make this thread's generic-proxy shared-memory writes visible to the async (bulk copy) proxy.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+// Packed 16-bit lane arithmetic (two BF16 values per 32-bit word).
+__device__ __forceinline__ uint32_t add_u16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("add.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t min_u16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("min.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
+// ------------------------------------------------------------------ value-level helpers
+
+// a[i] for a runtime i without local-memory indexing.
+__device__ __forceinline__ uint32_t pick4(const uint32_t (&a)[4], unsigned i) {
+  return i < 2 ? (i == 0 ? a[0] : a[1]) : (i == 2 ? a[2] : a[3]);
+}
+
+// Codes of two BF16 values (halves of w): e - e0 when 0 <= e - e0 <= 6, else 7.
+// neg_e0x2 holds (65536 - e0) in both halves, so the add wraps out-of-window values high.
+__device__ __forceinline__ uint32_t codes_x2(uint32_t w, uint32_t neg_e0x2) {
+  const uint32_t e2 = (w >> 7) & 0x00FF00FFu;
+  return min_u16x2(add_u16x2(e2, neg_e0x2), 0x00070007u);
+}
+
+// Sign|mantissa bytes of the four values in (w0, w1): (x >> 8 & 0x80) | (x & 0x7F).
+__device__ __forceinline__ uint32_t sign_mantissa_x4(uint32_t w0, uint32_t w1) {
+  const uint32_t lo = prmt(w0, w1, 0x6420);  // low byte of each value
+  const uint32_t hi = prmt(w0, w1, 0x7531);  // high byte of each value
+  return (hi & 0x80808080u) | (lo & 0x7F7F7F7Fu);
+}
+
+// Natural-order escape mask (bit j = value j) of the 8 codes in c2[0..3].
+__device__ __forceinline__ uint32_t escape_mask8(const uint32_t (&c2)[4]) {
+  uint32_t mask = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t e = (c2[i] + 0x00010001u) & 0x00080008u;  // bit 3 / bit 19 set where code == 7
+    mask |= (((e >> 3) | (e >> 18)) & 3u) << (2 * i);
+  }
+  return mask;
+}
+
+// 24-bit little-endian bitstream of 8 codes: code j at bits [3j, 3j+3).
+__device__ __forceinline__ uint32_t pack_codes8(const uint32_t (&c2)[4]) {
+  uint32_t v = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) v |= ((c2[i] | (c2[i] >> 13)) & 0x3Fu) << (6 * i);
+  return v;
+}
+
+// ------------------------------------------------------------------ block scan (128 threads)
+//
+// Chunk value v = 1024 q + 8 t + j is held by thread t (slice q = 0..3, j = 0..7).  In
+// ascending position order the escapes are ordered by (q, t, j).  Given each thread's
+// per-slice counts, return each slice's first rank and the chunk total.  `scratch` holds
+// 8 words of shared memory.  Contains one __syncthreads.
+constexpr int kChunkThreads = 128;
+
+__device__ __forceinline__ unsigned chunk_ranks(const unsigned (&cnt)[4], unsigned (&base)[4],
+                                                unsigned* scratch) {
+  const unsigned lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  unsigned p0 = cnt[0] | (cnt[1] << 16), p1 = cnt[2] | (cnt[3] << 16);
+  const unsigned own0 = p0, own1 = p1;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned a = __shfl_up_sync(0xFFFFFFFFu, p0, o);
+    const unsigned b = __shfl_up_sync(0xFFFFFFFFu, p1, o);
+    if (lane >= (unsigned)o) {
+      p0 += a;
+      p1 += b;
+    }
+  }
+  if (lane == 31) {
+    scratch[2 * warp] = p0;
+    scratch[2 * warp + 1] = p1;
+  }
+  __syncthreads();
+  const unsigned ex0 = p0 - own0, ex1 = p1 - own1;
+  unsigned before[4] = {0, 0, 0, 0}, total[4] = {0, 0, 0, 0};
+#pragma unroll
+  for (int w = 0; w < kChunkThreads / 32; ++w) {
+    const unsigned s0 = scratch[2 * w], s1 = scratch[2 * w + 1];
+    const unsigned t[4] = {s0 & 0xFFFFu, s0 >> 16, s1 & 0xFFFFu, s1 >> 16};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      total[q] += t[q];
+      if ((unsigned)w < warp) before[q] += t[q];
+    }
+  }
+  const unsigned ex[4] = {ex0 & 0xFFFFu, ex0 >> 16, ex1 & 0xFFFFu, ex1 >> 16};
+  unsigned run = 0;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    base[q] = run + before[q] + ex[q];
+    run += total[q];
+  }
+  return run;
+}
+
+// ------------------------------------------------------------------ launchers (host side)
+
+struct DeviceInfo {
+  int sm_count;
+  int* status;  // device address of the library's status word on this device
+};
+
+cudaError_t device_info(DeviceInfo* info);  // defined in zc_api.cu
+
+void timing_begin(int kernel_id, cudaStream_t stream);  // no-ops unless timing is enabled
+void timing_end(cudaStream_t stream);
+
+cudaError_t launch_stats(const uint16_t* in, uint64_t n, uint8_t* out, const DeviceInfo& dev,
+                         cudaStream_t stream);
+cudaError_t launch_encode(const uint16_t* in, uint64_t n, int base, uint8_t* out,
+                          unsigned long long* out_bytes, const DeviceInfo& dev, cudaStream_t stream,
+                          uint64_t stall_chunk, unsigned spin_limit);
+cudaError_t launch_decode(const uint8_t* in, uint16_t* out, uint64_t n, const DeviceInfo& dev,
+                          cudaStream_t stream);
+
+}  // namespace zc

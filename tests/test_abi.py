@@ -1,0 +1,83 @@
+"""The C ABI library without a GPU: it builds for sm_103a, loads, exports every entry point
+include/zc.h declares, and its pure host functions and host-side argument checks behave."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import oracle
+from lossless_bf16_compression_gb300 import binding as zc
+from lossless_bf16_compression_gb300 import build as zbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    zbuild.build()
+    return zc.lib()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "zc.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:size_t|int|void)\s+(zc_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 8
+    for name in names:
+        assert hasattr(lib, name), name
+    assert sorted(zc.exported_symbols()) == names
+
+
+def test_max_stream_bytes_matches_oracle(lib):
+    for n in [0, 1, 7, 8, 4095, 4096, 4097, 10 ** 6, 58_720_256, 117_440_512, 268_435_456, 1 << 29]:
+        assert zc.zc_max_stream_bytes(n) == oracle.max_stream_bytes(n)
+        N = (n + 4095) // 4096
+        assert zc.zc_max_compressed_bytes(n) >= zc.zc_max_stream_bytes(n) + 8 * N
+
+
+def test_max_stream_bytes_closed_form_large(lib):
+    n = (1 << 40) - 3
+    N = (n + 4095) // 4096
+    rem = n % 4096
+    pad16 = lambda v: (v + 15) // 16 * 16  # noqa: E731
+    want = pad16(32 + 8 * (N + 1)) + (n // 4096) * 17936 + 16 + pad16((3 * rem + 7) // 8) + pad16(rem) + pad16(3 * rem)
+    assert zc.zc_max_stream_bytes(n) == want
+
+
+def test_sizes_beyond_limit(lib):
+    assert zc.zc_max_stream_bytes((1 << 40) + 1) == 0
+    assert zc.zc_max_compressed_bytes((1 << 40) + 1) == 0
+
+
+def test_host_argument_checks(lib):
+    A = 1 << 20  # an aligned fake address; never dereferenced by these calls
+    out_len = ctypes.c_uint64()
+    p_len = ctypes.addressof(out_len)
+    assert zc.zc_compress(0, 10, -1, A, p_len, 0) == zc.ZC_ERR_INVALID_ARG       # null input
+    assert zc.zc_compress(A, 10, -1, 0, p_len, 0) == zc.ZC_ERR_INVALID_ARG       # null output
+    assert zc.zc_compress(A, 10, -1, A * 4, 0, 0) == zc.ZC_ERR_INVALID_ARG       # null length
+    assert zc.zc_compress(A, 10, 250, A * 4, p_len, 0) == zc.ZC_ERR_INVALID_ARG  # base too big
+    assert zc.zc_compress(A, 10, -2, A * 4, p_len, 0) == zc.ZC_ERR_INVALID_ARG
+    assert zc.zc_compress(A, (1 << 40) + 1, -1, A * 4, p_len, 0) == zc.ZC_ERR_INVALID_ARG
+    assert zc.zc_compress(A + 2, 10, -1, A * 4, p_len, 0) == zc.ZC_ERR_MISALIGNED
+    assert zc.zc_compress(A, 10, -1, A * 4 + 8, p_len, 0) == zc.ZC_ERR_MISALIGNED
+    assert zc.zc_compress(A, 10, -1, A * 4, p_len + 4, 0) == zc.ZC_ERR_MISALIGNED
+    assert zc.zc_compress(A, 100, -1, A + 64, p_len, 0) == zc.ZC_ERR_INVALID_ARG  # overlap
+    assert zc.zc_decompress(0, A, 10, 0) == zc.ZC_ERR_INVALID_ARG
+    assert zc.zc_decompress(A, 0, 10, 0) == zc.ZC_ERR_INVALID_ARG
+    assert zc.zc_decompress(A + 8, A * 4, 10, 0) == zc.ZC_ERR_MISALIGNED
+    assert zc.zc_decompress(A, A + 16, 100, 0) == zc.ZC_ERR_INVALID_ARG          # overlap
+
+
+@pytest.mark.skipif(os.path.exists("/dev/nvidia0"), reason="checks the no-GPU failure path")
+def test_no_gpu_fails_loudly(lib):
+    A = 1 << 20
+    out_len = ctypes.c_uint64()
+    # valid arguments reach the CUDA runtime, which reports that there is no device
+    assert zc.zc_compress(A, 10, -1, A * 4, ctypes.addressof(out_len), 0) == zc.ZC_ERR_CUDA
+    assert zc.zc_decompress(A, A * 4, 10, 0) == zc.ZC_ERR_CUDA

@@ -1,0 +1,178 @@
+"""Device-side error detection, without faulting the GPU.
+
+Corrupt streams are made on the host; the decoder must report them through zc_status (and
+agree with the oracle on which streams are invalid) while reading only inside the buffer.
+The look-back wait is made to run out by a chunk that never publishes; the call must report
+ZC_ERR_TIMEOUT and leave the context usable.  Canary bytes around every buffer must survive.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+
+import oracle
+from lossless_bf16_compression_gb300 import binding as zc
+from lossless_bf16_compression_gb300 import workloads
+
+from gpu_helpers import gpu_decompress_bytes, require_gpu, to_device
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+N_VALUES = 3 * 4096 + 100
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    require_gpu()
+
+
+@pytest.fixture(scope="module")
+def sample():
+    rng = np.random.default_rng(42)
+    x = workloads.fp32_to_bf16_bits((rng.standard_normal(N_VALUES) * 0.02).astype(np.float32))
+    x[rng.choice(N_VALUES, 300, replace=False)] = workloads.random_patterns(300, 43)
+    return x, oracle.compress(x)
+
+
+def u64_at(s, off, v):
+    t = s.copy()
+    t[off:off + 8] = np.frombuffer(np.uint64(v).tobytes(), np.uint8)
+    return t
+
+
+def oracle_status(stream, n, capacity):
+    buf = np.zeros(capacity, np.uint8)
+    buf[:stream.size] = stream
+    return oracle.decompress(buf, n)
+
+
+def record_offset(s, c):
+    return int(s[32 + 8 * c:40 + 8 * c].view(np.uint64)[0])
+
+
+def targeted_mutations(s):
+    off0, off3 = record_offset(s, 0), record_offset(s, 3)
+    k0 = int(s[off0:off0 + 4].view(np.uint32)[0])
+    esc0 = off0 + 16 + 1536 + 4096
+    muts = {
+        "magic": (0, 0x00),
+        "version": (4, 2),
+        "log2_chunk": (6, 11),
+        "base_250": (7, 250),
+        "N": (16, 5),
+        "total_bytes": (24, s[24] ^ 0x10),
+        "offset_0": (32, s[32] ^ 0x10),
+        "offset_1_misaligned": (40, s[40] ^ 0x01),
+        "record_k": (off0, s[off0] ^ 0x01),
+        "record_m": (off0 + 4, s[off0 + 4] ^ 0x01),
+        "record_reserved": (off0 + 9, 1),
+        "escape_position": (esc0, s[esc0] ^ 0x01),
+        "escape_exponent_in_window": (esc0 + 2 * k0, s[7]),
+        "escape_padding": (esc0 + 3 * k0 + (1 if (3 * k0) % 16 else 0), 0x55),
+        "last_codes_padding": (off3 + 16 + (3 * 100 + 7) // 8 + 1, 0x80),
+        "last_byte_plane_padding": (off3 + 16 + 48 + 100 + 1, 0x01),
+    }
+    out = {}
+    for name, (pos, val) in muts.items():
+        t = s.copy()
+        t[pos] = np.uint8(val)
+        out[name] = t
+    out["n_mismatch"] = u64_at(s, 8, N_VALUES + 1)
+    out["table_end"] = u64_at(s, 32 + 8 * 4, int(s[24:32].view(np.uint64)[0]) + 16)
+    return out
+
+
+def test_targeted_corruptions_are_reported(sample):
+    x, s = sample
+    cap = zc.zc_max_compressed_bytes(N_VALUES)
+    for name, t in targeted_mutations(s).items():
+        ost, _ = oracle_status(t, N_VALUES, cap)
+        assert ost != oracle.OK, f"{name}: the oracle accepts it, the mutation is not a corruption"
+        st, _ = gpu_decompress_bytes(t, N_VALUES, cap)
+        want = zc.ZC_ERR_SIZE_MISMATCH if ost == oracle.ERR_SIZE_MISMATCH else zc.ZC_ERR_CORRUPT
+        assert st == want, f"{name}: status {zc.ERROR_NAMES.get(st, st)}"
+
+
+def test_random_bit_flips_match_oracle_verdict(sample):
+    x, s = sample
+    cap = zc.zc_max_compressed_bytes(N_VALUES)
+    rng = np.random.default_rng(5)
+    accepted = rejected = 0
+    for _ in range(400):
+        t = s.copy()
+        pos = int(rng.integers(0, s.size))
+        t[pos] ^= np.uint8(1 << int(rng.integers(0, 8)))
+        ost, ovals = oracle_status(t, N_VALUES, cap)
+        st, gvals = gpu_decompress_bytes(t, N_VALUES, cap)
+        if ost == oracle.OK:
+            assert st == zc.ZC_OK, f"flip at {pos}: GPU rejects a valid stream"
+            assert np.array_equal(gvals, ovals), f"flip at {pos}: different values"
+            accepted += 1
+        else:
+            assert st != zc.ZC_OK, f"flip at {pos}: GPU accepts an invalid stream"
+            rejected += 1
+    assert accepted > 50 and rejected > 50
+
+
+def test_valid_stream_and_wrong_n(sample):
+    x, s = sample
+    cap = zc.zc_max_compressed_bytes(N_VALUES)
+    st, vals = gpu_decompress_bytes(s, N_VALUES, cap)
+    assert st == zc.ZC_OK and np.array_equal(vals, x)
+    st, _ = gpu_decompress_bytes(s, N_VALUES - 1, cap)
+    assert st == zc.ZC_ERR_SIZE_MISMATCH
+
+
+def test_empty_stream():
+    s = oracle.compress(np.zeros(0, np.uint16))
+    st, _ = gpu_decompress_bytes(s, 0, 64)
+    assert st == zc.ZC_OK
+    st, _ = gpu_decompress_bytes(u64_at(s, 24, 64), 0, 128)
+    assert st == zc.ZC_ERR_CORRUPT
+
+
+@pytest.mark.parametrize("stalled", [0, 1, 17])
+def test_lookback_wait_is_bounded(stalled):
+    x = workloads.sweep(18)  # 64 chunks
+    xd = to_device(x)
+    cap = zc.zc_max_compressed_bytes(x.size)
+    out = torch.empty(cap, dtype=torch.uint8, device="cuda")
+    ob = torch.zeros(1, dtype=torch.int64, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    zc.status(reset=True)
+    assert zc.zc_compress_stall_test(xd.data_ptr(), x.size, -1, out.data_ptr(), ob.data_ptr(), s,
+                                     stalled, 2000) == zc.ZC_OK
+    assert zc.zc_status(s, 1) == zc.ZC_ERR_TIMEOUT
+    # the context is still usable: a normal call afterwards is exact
+    out2, ob2 = zc.compress(xd)
+    back = zc.decompress(out2, x.size)
+    assert zc.status(reset=True) == zc.ZC_OK
+    assert np.array_equal(back.cpu().numpy().view(np.uint16), x)
+    assert out2[:int(ob2.item())].cpu().numpy().tobytes() == oracle.compress(x).tobytes()
+
+
+def test_guard_bands():
+    """4 KiB of 0xA5 before and after the input, the output and the decoded buffer."""
+    G = 4096
+    rng = np.random.default_rng(77)
+    for n in (1, 4097, 3 * 4096 + 5, 70_001):
+        x = workloads.random_patterns(n, int(rng.integers(1 << 30)))
+        cap = zc.zc_max_compressed_bytes(n)
+        inb = torch.full((G + 2 * n + G,), 0xA5, dtype=torch.uint8, device="cuda")
+        inb[G:G + 2 * n] = torch.from_numpy(x.view(np.uint8).copy())
+        outb = torch.full((G + cap + G,), 0xA5, dtype=torch.uint8, device="cuda")
+        decb = torch.full((G + 2 * n + 16 + G,), 0xA5, dtype=torch.uint8, device="cuda")
+        ob = torch.zeros(1, dtype=torch.int64, device="cuda")
+        s = torch.cuda.current_stream().cuda_stream
+        zc.status(reset=True)
+        assert zc.zc_compress(inb.data_ptr() + G, n, -1, outb.data_ptr() + G, ob.data_ptr(), s) == zc.ZC_OK
+        assert zc.zc_decompress(outb.data_ptr() + G, decb.data_ptr() + G, n, s) == zc.ZC_OK
+        assert zc.zc_status(s, 1) == zc.ZC_OK
+        for buf, lo, hi in ((inb, G, G + 2 * n), (outb, G, G + cap), (decb, G, G + 2 * n)):
+            h = buf.cpu().numpy()
+            assert np.all(h[:lo] == 0xA5) and np.all(h[hi:] == 0xA5), "a guard band was written"
+        got = decb[G:G + 2 * n].cpu().numpy().view(np.uint16)
+        assert np.array_equal(got, x)
+        total = int(ob.item())
+        assert outb[G:G + total].cpu().numpy().tobytes() == oracle.compress(x).tobytes()
