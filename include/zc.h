@@ -12,17 +12,20 @@
  * aligned global and shared memory access, data movement pipelined with compute) is what the
  * kernels behind these calls implement for sm_103a.
  *
- * Stream format "ZCB1" (little-endian, every section zero-padded to a multiple of 16 bytes):
- *   header   32 B   "ZCB1", u16 version = 1, u8 log2(chunk) = 12, u8 e0, u64 n, u64 N,
+ * Stream format "ZCB1", version 2 (little-endian, every section zero-padded to 16 bytes):
+ *   header    32 B  "ZCB1", u16 version = 2, u8 log2(chunk) = 12, u8 e0, u64 n, u64 N,
  *                   u64 total_bytes                      (N = ceil(n / 4096) chunks)
- *   offsets  u64[N+1], absolute byte offset of each chunk record; offsets[N] = total_bytes
- *   records  at pad16(32 + 8 (N+1)), in chunk order, back to back.  A record of m values
- *            with k escapes is: u32 k, u32 m, u64 0; 3-bit codes, code i at bits [3i, 3i+3)
- *            least significant bit first (pad16(ceil(3m/8)) B); one sign|mantissa byte per
- *            value, (x >> 8 & 0x80) | (x & 0x7F) (pad16(m) B); u16 positions then u8 full
- *            exponents of the escapes in ascending position order (pad16(3k) B).
+ *   offsets   u64[N+1]: absolute byte offset of each chunk's escape list; offsets[N] =
+ *             total_bytes.  Zero padding to R0 = pad16(32 + 8 (N+1)).
+ *   fixed     for chunk c (m values), at R0 + 5632 c: 3-bit codes, code i at bits [3i, 3i+3)
+ *             least significant bit first (pad16(ceil(3m/8)) B), then one sign|mantissa byte
+ *             per value, (x >> 8 & 0x80) | (x & 0x7F) (pad16(m) B).  The place of every fixed
+ *             part follows from n alone ("communication-aware layout": it can be sent before
+ *             any size is exchanged).
+ *   escapes   after the last fixed part, in chunk order: for a chunk with k escapes, u16
+ *             positions then u8 full exponents in ascending position order (pad16(3k) B).
  *   Code c < 7 means exponent e0 + c; code 7 means "escape".  e0 is in [0, 249].
- * A full chunk without escapes costs 5648 B for 4096 values: 11.03 bits per value.
+ * A full chunk without escapes costs 5632 B for 4096 values: 11 bits per value.
  *
  * All entry points are host functions.  Pointers called "device" may be any address the GPU
  * can dereference (cudaMalloc, managed, or mapped pinned memory).  Every call is
@@ -57,8 +60,8 @@ typedef struct CUstream_st* cudaStream_t; /* the CUDA runtime's own stream handl
 /* ------------------------------------------------------------------ sizes */
 
 /* Bytes the caller must provide at `out` for zc_compress of n values: the worst-case stream
- * (every value escaping, 17,936 B per full chunk, plus header and offset table) followed by
- * the call's workspace (look-back state, 8 B per chunk, and a 16.25 KiB control block).
+ * (every value escaping, 17,920 B per full chunk, plus header and offset table) followed by
+ * the call's workspace (scan state, 8 B per chunk, and a 16.25 KiB control block).
  * Pure host function; makes no CUDA call.  Returns 0 when n > ZC_MAX_N. */
 size_t zc_max_compressed_bytes(size_t n);
 
@@ -129,10 +132,10 @@ int zc_timing_collect(int* kernel_ids, float* ms, int max);
 
 /* ------------------------------------------------------------------ test hook */
 
-/* zc_compress with a planted stall, for testing the bounded waits: chunk `stalled_chunk`
- * never publishes its look-back state, so the next chunk's wait runs out after about
- * `spin_limit` polls and the call reports ZC_ERR_TIMEOUT through zc_status instead of
- * hanging.  The stream written is then incomplete.  No counterpart on the pages. */
+/* zc_compress with a planted stall, for testing the bounded waits: chunk `stalled_chunk` never
+ * publishes its escape-list size, so the device-wide scan cannot pass it; the waits for it run
+ * out after about `spin_limit` polls and the call reports ZC_ERR_TIMEOUT through zc_status
+ * instead of hanging.  The stream written is then incomplete.  No counterpart on the pages. */
 int zc_compress_stall_test(const void* in, size_t n, int base_or_auto, void* out,
                            size_t* out_bytes, cudaStream_t stream, size_t stalled_chunk,
                            unsigned spin_limit);

@@ -14,34 +14,45 @@
 
 namespace zc {
 
-// ------------------------------------------------------------------ stream layout ("ZCB1")
-
-constexpr int kChunk = 4096;                       // values per chunk record
+// ------------------------------------------------------------------ stream layout ("ZCB1" v2)
+//
+// header (32 B) | u64 escape offsets [N+1] | zero pad to 16 | fixed parts | escape lists
+// The fixed part of chunk c (3-bit codes, then the sign|mantissa plane) starts at
+// records_base(n) + c * kFullFixedBytes, so its place follows from n alone; only the escape
+// lists (u16 positions, u8 exponents, zero pad) are placed by the scan.
+constexpr int kChunk = 4096;                       // values per chunk
 constexpr int kHeaderBytes = 32;                   // stream header
-constexpr int kRecordHeaderBytes = 16;             // u32 k, u32 m, u64 reserved
 constexpr int kFullCodeBytes = 3 * kChunk / 8;     // 1536: 3-bit codes of a full chunk
-constexpr int kMaxRecordBytes = kRecordHeaderBytes + kFullCodeBytes + kChunk + 3 * kChunk;  // 17936
+constexpr int kFullFixedBytes = kFullCodeBytes + kChunk;  // 5632: fixed part of a full chunk
+constexpr int kMaxEscapeBytes = 3 * kChunk;        // 12288: every value escapes
 constexpr int kE0Max = 249;
-constexpr unsigned long long kMagicWord =          // bytes 0..6 of the header: "ZCB1", v1, 12
-    0x5Aull | (0x43ull << 8) | (0x42ull << 16) | (0x31ull << 24) | (1ull << 32) | (12ull << 48);
+constexpr unsigned long long kMagicWord =          // bytes 0..6 of the header: "ZCB1", v2, 12
+    0x5Aull | (0x43ull << 8) | (0x42ull << 16) | (0x31ull << 24) | (2ull << 32) | (12ull << 48);
 
 __host__ __device__ inline uint64_t pad16(uint64_t v) { return (v + 15u) & ~uint64_t(15); }
 __host__ __device__ inline uint64_t num_chunks(uint64_t n) { return (n + kChunk - 1) / kChunk; }
-__host__ __device__ inline uint64_t records_base(uint64_t n) {
-  return pad16(kHeaderBytes + 8 * (num_chunks(n) + 1));
-}
-__host__ __device__ inline uint64_t code_section_bytes(uint64_t m) { return pad16((3 * m + 7) / 8); }
-__host__ __device__ inline uint64_t record_bytes(uint64_t m, uint64_t k) {
-  return kRecordHeaderBytes + code_section_bytes(m) + pad16(m) + pad16(3 * k);
-}
 // Values in chunk c of an n-value tensor (c < num_chunks(n)).
 __host__ __device__ inline unsigned chunk_values(uint64_t n, uint64_t c) {
   const uint64_t left = n - c * kChunk;
   return left < static_cast<uint64_t>(kChunk) ? static_cast<unsigned>(left) : static_cast<unsigned>(kChunk);
 }
+// Start of the fixed region.
+__host__ __device__ inline uint64_t records_base(uint64_t n) {
+  return pad16(kHeaderBytes + 8 * (num_chunks(n) + 1));
+}
+__host__ __device__ inline uint64_t code_section_bytes(uint64_t m) { return pad16((3 * m + 7) / 8); }
+__host__ __device__ inline uint64_t fixed_bytes(uint64_t m) { return code_section_bytes(m) + pad16(m); }
+__host__ __device__ inline uint64_t fixed_offset(uint64_t n, uint64_t c) {
+  return records_base(n) + c * static_cast<uint64_t>(kFullFixedBytes);
+}
+// Start of the escape region, right after the last fixed part.
+__host__ __device__ inline uint64_t escape_base(uint64_t n) {
+  const uint64_t N = num_chunks(n);
+  return N ? fixed_offset(n, N - 1) + fixed_bytes(chunk_values(n, N - 1)) : records_base(n);
+}
 __host__ __device__ inline uint64_t max_stream_bytes(uint64_t n) {
-  const uint64_t full = n / kChunk, rem = n % kChunk;
-  return records_base(n) + full * kMaxRecordBytes + (rem ? record_bytes(rem, rem) : 0);
+  const uint64_t rem = n % kChunk;
+  return escape_base(n) + (n / kChunk) * kMaxEscapeBytes + pad16(3 * rem);
 }
 
 // ------------------------------------------------------------------ workspace (tail of `out`)
@@ -199,17 +210,6 @@ __device__ __forceinline__ uint32_t sign_mantissa_x4(uint32_t w0, uint32_t w1) {
   return (hi & 0x80808080u) | (lo & 0x7F7F7F7Fu);
 }
 
-// Natural-order escape mask (bit j = value j) of the 8 codes in c2[0..3].
-__device__ __forceinline__ uint32_t escape_mask8(const uint32_t (&c2)[4]) {
-  uint32_t mask = 0;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint32_t e = (c2[i] + 0x00010001u) & 0x00080008u;  // bit 3 / bit 19 set where code == 7
-    mask |= (((e >> 3) | (e >> 18)) & 3u) << (2 * i);
-  }
-  return mask;
-}
-
 // 24-bit little-endian bitstream of 8 codes: code j at bits [3j, 3j+3).
 __device__ __forceinline__ uint32_t pack_codes8(const uint32_t (&c2)[4]) {
   uint32_t v = 0;
@@ -218,16 +218,38 @@ __device__ __forceinline__ uint32_t pack_codes8(const uint32_t (&c2)[4]) {
   return v;
 }
 
+// Write a warp's 32 consecutive 24-bit code groups (lane L's group at byte 3 L of `dst`) as 24
+// aligned 32-bit words, skipping words at or past `limit` bytes.  All lanes must call it.
+__device__ __forceinline__ void store_code_groups(uint8_t* dst, uint32_t bits, unsigned limit) {
+  const unsigned lane = threadIdx.x & 31;
+  const unsigned w = lane < 24 ? lane : 23;
+  const unsigned l0 = (4 * w) / 3, off = 32 * w - 24 * l0;  // off in {0, 8, 16}
+  const uint32_t a = __shfl_sync(0xFFFFFFFFu, bits, l0);
+  const uint32_t b = __shfl_sync(0xFFFFFFFFu, bits, l0 + 1);
+  const uint32_t word = (a >> off) | (b << (24 - off));
+  if (lane < 24 && 4 * lane < limit) reinterpret_cast<uint32_t*>(dst)[lane] = word;
+}
+
 // ------------------------------------------------------------------ block scan (128 threads)
-//
-// Chunk value v = 1024 q + 8 t + j is held by thread t (slice q = 0..3, j = 0..7).  In
-// ascending position order the escapes are ordered by (q, t, j).  Given each thread's
-// per-slice counts, return each slice's first rank and the chunk total.  `scratch` holds
-// 8 words of shared memory.  Contains one __syncthreads.
 constexpr int kChunkThreads = 128;
 
-__device__ __forceinline__ unsigned chunk_ranks(const unsigned (&cnt)[4], unsigned (&base)[4],
-                                                unsigned* scratch) {
+// Barrier over the CTA's first 128 threads only (named barrier 1), for kernels that run an
+// extra warp on other work.
+__device__ __forceinline__ void bar_chunk() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ bool bar_chunk_or(bool v) {
+  unsigned r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.or.pred p, 1, 128, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<unsigned>(v))
+      : "memory");
+  return r != 0;
+}
+
+template <bool kNamedBarrier>
+__device__ __forceinline__ unsigned chunk_ranks_impl(const unsigned (&cnt)[4], unsigned (&base)[4],
+                                                     unsigned* scratch) {
   const unsigned lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   unsigned p0 = cnt[0] | (cnt[1] << 16), p1 = cnt[2] | (cnt[3] << 16);
   const unsigned own0 = p0, own1 = p1;
@@ -244,7 +266,7 @@ __device__ __forceinline__ unsigned chunk_ranks(const unsigned (&cnt)[4], unsign
     scratch[2 * warp] = p0;
     scratch[2 * warp + 1] = p1;
   }
-  __syncthreads();
+  if (kNamedBarrier) bar_chunk(); else __syncthreads();
   const unsigned ex0 = p0 - own0, ex1 = p1 - own1;
   unsigned before[4] = {0, 0, 0, 0}, total[4] = {0, 0, 0, 0};
 #pragma unroll
@@ -265,6 +287,50 @@ __device__ __forceinline__ unsigned chunk_ranks(const unsigned (&cnt)[4], unsign
     run += total[q];
   }
   return run;
+}
+
+// 256 threads, 2 slices: chunk value v = 2048 q + 8 t + j is held by thread t (q = 0..1,
+// j = 0..7), escapes ordered by (q, t, j).  Same contract as below; `scratch` holds 8 words;
+// one barrier over the first 256 threads (named barrier 1).
+__device__ __forceinline__ unsigned chunk_ranks_256(const unsigned (&cnt)[2], unsigned (&base)[2],
+                                                    unsigned* scratch) {
+  const unsigned lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  unsigned p0 = cnt[0] | (cnt[1] << 16);
+  const unsigned own = p0;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned a = __shfl_up_sync(0xFFFFFFFFu, p0, o);
+    if (lane >= (unsigned)o) p0 += a;
+  }
+  if (lane == 31) scratch[warp] = p0;
+  asm volatile("bar.sync 1, 256;" ::: "memory");
+  const unsigned ex = p0 - own;
+  unsigned before0 = 0, before1 = 0, total0 = 0, total1 = 0;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    const unsigned t = scratch[w];
+    total0 += t & 0xFFFFu;
+    total1 += t >> 16;
+    if ((unsigned)w < warp) {
+      before0 += t & 0xFFFFu;
+      before1 += t >> 16;
+    }
+  }
+  base[0] = before0 + (ex & 0xFFFFu);
+  base[1] = total0 + before1 + (ex >> 16);
+  return total0 + total1;
+}
+
+// Chunk value v = 1024 q + 8 t + j is held by thread t (slice q = 0..3, j = 0..7).  In
+// ascending position order the escapes are ordered by (q, t, j).  Given each thread's
+// per-slice counts, return each slice's first rank and the chunk total.  `scratch` holds
+// 8 words of shared memory.  Contains one barrier over the chunk's 128 threads.
+__device__ __forceinline__ unsigned chunk_ranks(const unsigned (&cnt)[4], unsigned (&base)[4], unsigned* scratch) {
+  return chunk_ranks_impl<false>(cnt, base, scratch);
+}
+__device__ __forceinline__ unsigned chunk_ranks_named(const unsigned (&cnt)[4], unsigned (&base)[4],
+                                                      unsigned* scratch) {
+  return chunk_ranks_impl<true>(cnt, base, scratch);
 }
 
 // ------------------------------------------------------------------ launchers (host side)

@@ -6,20 +6,23 @@
 // reconstruction is exact (first technique); decompression kernels with aligned global and
 // shared memory access (second technique).
 //
-// GB300 design.  One 128-thread CTA per chunk, many CTAs per SM: the chunk-offset table makes
-// every record independently addressable, so there is no inter-CTA dependency.  A thread holds
-// 4 slices of 8 values; per slice it reads its 24 code bits (two aligned 32-bit loads and a
-// funnel shift) and 8 sign|mantissa bytes, builds two values per 32-bit word, and writes one
-// coalesced 16-byte store.  Escapes get their rank from the same block scan the encoder uses,
-// which also checks every stored position and exponent.  Every offset and size is checked
-// against the header and the record's own header before it is used, so a corrupt stream sets
-// an error instead of steering a read outside [0, total_bytes).
+// GB300 design.  One 128-thread CTA per chunk, many CTAs per SM: fixed parts sit at places that
+// follow from n and the offset table locates every escape list, so there is no inter-CTA
+// dependency.  Warp 0 reads the header and the chunk's two escape offsets in one round trip and
+// checks them; the fixed part (5,632 B) and the escape list (at most 12,288 B) then arrive in
+// shared memory by two bulk async copies (TMA engine, one mbarrier).  A thread holds 4 slices of 8 values; per slice it takes its 24 code bits and 8
+// sign|mantissa bytes from shared memory, builds two values per 32-bit word with one imad and
+// one lop3, and writes one coalesced 16-byte store.  Escapes get their rank from the same block
+// scan the encoder uses, which also checks every stored position and exponent.  Every offset
+// and size is checked before it is used, so a corrupt stream sets an error instead of steering
+// a read outside [0, total_bytes).
 #include "zc_common.cuh"
 
 namespace zc {
 namespace {
 
 constexpr int kThreads = kChunkThreads;  // 128
+constexpr unsigned kWaitLimit = 1u << 22;   // mbarrier polls before giving up
 
 struct DecodeParams {
   const uint8_t* in;
@@ -29,67 +32,81 @@ struct DecodeParams {
   int* status;
 };
 
-__global__ void __launch_bounds__(kThreads) decode_kernel(DecodeParams p) {
-  __shared__ unsigned scan[8];
-  __shared__ int hdr_ok;
-  __shared__ int e0_s;
-  __shared__ unsigned k_s;
-  __shared__ unsigned long long off_s;
+struct __align__(128) DecodeSmem {
+  uint4 fixed[kFullFixedBytes / 16];
+  uint4 esc[kMaxEscapeBytes / 16];
+  uint64_t mbar;
+  unsigned scan[8];
+  int ok;
+  int e0;
+  unsigned esc_bytes;
+};
 
-  const unsigned tid = threadIdx.x;
+__global__ void __launch_bounds__(kThreads) decode_kernel(DecodeParams p) {
+  __shared__ DecodeSmem S;
+  const unsigned tid = threadIdx.x, lane = tid & 31;
   const uint64_t c = blockIdx.x;
   const uint64_t first = c * kChunk;
   const unsigned m = c < p.N ? chunk_values(p.n, c) : 0;
 
-  if (tid == 0) {
+  if (tid < 32) {
+    // lanes 0..6 fetch header words, the chunk's two escape offsets and the table's zero pad
     const unsigned long long* w = reinterpret_cast<const unsigned long long*>(p.in);
-    const unsigned long long h0 = w[0], h1 = w[1], h2 = w[2], total = w[3];
-    const unsigned long long off0 = w[4 + c];
-    const unsigned long long off1 = c < p.N ? w[5 + c] : 0;
-    const uint64_t R0 = records_base(p.n);
-    int bad = 0;
-    const int e0 = static_cast<int>(h0 >> 56);
-    if ((h0 & 0x00FFFFFFFFFFFFFFull) != kMagicWord || e0 > kE0Max) bad = ZC_ERR_CORRUPT;
-    else if (h1 != p.n) bad = ZC_ERR_SIZE_MISMATCH;
-    else if (h2 != p.N || total < R0 || total > max_stream_bytes(p.n)) bad = ZC_ERR_CORRUPT;
-    if (!bad && (c == 0 || c == p.N - 1 || p.N == 0)) {
-      // the table's zero pad, and the ends of the table
-      if (kHeaderBytes + 8 * (p.N + 1) < R0 && w[5 + p.N] != 0) bad = ZC_ERR_CORRUPT;
-      if (c == 0 && off0 != R0) bad = ZC_ERR_CORRUPT;
-      if (p.N == 0 && total != R0) bad = ZC_ERR_CORRUPT;
-      if (p.N > 0 && c == p.N - 1 && off1 != total) bad = ZC_ERR_CORRUPT;
-    }
-    unsigned k = 0;
-    if (!bad && c < p.N) {
-      if (off0 < R0 || off1 > total || off1 <= off0 || ((off0 | off1) & 15) ||
-          off1 - off0 > static_cast<unsigned long long>(kMaxRecordBytes)) {
+    const uint64_t R0 = records_base(p.n), E0 = escape_base(p.n);
+    const bool has_pad = kHeaderBytes + 8 * (p.N + 1) < R0;
+    unsigned long long v = 0;
+    if (lane < 4) v = w[lane];
+    else if (lane == 4) v = w[4 + c];
+    else if (lane == 5 && c < p.N) v = w[5 + c];
+    else if (lane == 6 && has_pad && (c == 0 || c + 1 >= p.N)) v = w[5 + p.N];
+    const unsigned long long h0 = __shfl_sync(0xFFFFFFFFu, v, 0), h1 = __shfl_sync(0xFFFFFFFFu, v, 1);
+    const unsigned long long h2 = __shfl_sync(0xFFFFFFFFu, v, 2), total = __shfl_sync(0xFFFFFFFFu, v, 3);
+    const unsigned long long off0 = __shfl_sync(0xFFFFFFFFu, v, 4), off1 = __shfl_sync(0xFFFFFFFFu, v, 5);
+    const unsigned long long pad = __shfl_sync(0xFFFFFFFFu, v, 6);
+    if (lane == 0) {
+      int bad = 0;
+      const int e0 = static_cast<int>(h0 >> 56);
+      if ((h0 & 0x00FFFFFFFFFFFFFFull) != kMagicWord || e0 > kE0Max) bad = ZC_ERR_CORRUPT;
+      else if (h1 != p.n) bad = ZC_ERR_SIZE_MISMATCH;
+      else if (h2 != p.N || total < E0 || total > max_stream_bytes(p.n) || pad != 0) bad = ZC_ERR_CORRUPT;
+      else if ((c == 0 && off0 != E0) || (p.N == 0 && total != E0) || (p.N > 0 && c == p.N - 1 && off1 != total))
         bad = ZC_ERR_CORRUPT;
-      } else {
-        const uint4 rh = *reinterpret_cast<const uint4*>(p.in + off0);
-        k = rh.x;
-        if (rh.y != m || k > m || rh.z != 0 || rh.w != 0 || off1 - off0 != record_bytes(m, k))
-          bad = ZC_ERR_CORRUPT;
+      else if (c < p.N && (off0 < E0 || off1 > total || off1 < off0 || ((off0 | off1) & 15) ||
+                           off1 - off0 > pad16(3ull * m)))
+        bad = ZC_ERR_CORRUPT;
+      if (bad) set_error(p.status, bad);
+      S.ok = !bad && c < p.N;
+      S.e0 = e0;
+      S.esc_bytes = static_cast<unsigned>(off1 - off0);
+      if (S.ok) {
+        const unsigned fbytes = static_cast<unsigned>(fixed_bytes(m));
+        mbar_init(&S.mbar, 1);
+        fence_mbar_init();
+        mbar_arrive_expect_tx(&S.mbar, fbytes + S.esc_bytes);
+        bulk_load(S.fixed, p.in + fixed_offset(p.n, c), fbytes, &S.mbar);
+        if (S.esc_bytes) bulk_load(S.esc, p.in + off0, S.esc_bytes, &S.mbar);
       }
     }
-    if (bad) set_error(p.status, bad);
-    hdr_ok = !bad;
-    e0_s = e0;
-    k_s = k;
-    off_s = off0;
   }
   __syncthreads();
-  if (!hdr_ok || c >= p.N) return;
+  if (!S.ok) return;
+  // every thread polls; the CTA acts on one shared answer
+  if (__syncthreads_or(!mbar_wait(&S.mbar, 0, kWaitLimit))) {
+    if (tid == 0) {
+      set_error(p.status, ZC_ERR_TIMEOUT);
+      mbar_wait(&S.mbar, 0, kWaitLimit);  // never leave a copy in flight
+    }
+    return;
+  }
 
-  const int e0 = e0_s;
-  const unsigned k = k_s;
+  const int e0 = S.e0;
   const bool full = m == kChunk;
   const unsigned cbytes = full ? kFullCodeBytes : static_cast<unsigned>(code_section_bytes(m));
   const unsigned smbytes = full ? kChunk : static_cast<unsigned>(pad16(m));
-  const uint8_t* rec = p.in + off_s;
-  const uint8_t* codes = rec + kRecordHeaderBytes;
+  const uint8_t* codes = reinterpret_cast<const uint8_t*>(S.fixed);
   const uint8_t* smp = codes + cbytes;
-  const uint8_t* esc = smp + smbytes;
-  const uint32_t e0x2 = static_cast<uint32_t>(e0) * 0x00010001u;
+  const uint8_t* esc = reinterpret_cast<const uint8_t*>(S.esc);
+  const uint32_t e0_field = static_cast<uint32_t>(e0) * (128u * 0x00010001u);  // e0 << 7 in both halves
 
   uint32_t x[4][4];
   unsigned cnt[4], msk[4];
@@ -103,40 +120,39 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeParams p) {
     if (!full && v0 >= m) continue;
     const unsigned b = 3 * g;
     const uint32_t* cw = reinterpret_cast<const uint32_t*>(codes + (b & ~3u));
-    const uint32_t bits = __funnelshift_r(__ldg(cw), __ldg(cw + 1), 8 * (b & 3));
-    const uint2 sm = __ldg(reinterpret_cast<const uint2*>(smp + v0));
-    uint32_t c2[4];
+    const uint32_t bits = __funnelshift_r(cw[0], cw[1], 8 * (b & 3));
+    const uint2 sm = *reinterpret_cast<const uint2*>(smp + v0);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      c2[i] = ((bits >> (6 * i)) & 7u) | (((bits >> (6 * i + 3)) & 7u) << 16);
+      // codes of values 2i, 2i+1 -> (c + e0) << 7 in the two halves
+      const uint32_t v = (bits >> (6 * i)) & 0x3Fu;
+      const uint32_t efield = (v & 0x38u) * (0x1FFFu << 7) + v * 128u + e0_field;
+      // sign|mantissa bytes -> halves with the sign replicated over bits 7..15
       const uint32_t sw = i < 2 ? sm.x : sm.y;
       const unsigned lo = (2 * i) & 3;
-      const uint32_t s2 = prmt(sw, 0u, lo | (4u << 4) | ((lo + 1) << 8) | (4u << 12));  // two bytes -> halves
-      const uint32_t sign_mant = ((s2 << 8) & 0x80008000u) | (s2 & 0x007F007Fu);
-      x[q][i] = sign_mant | (((c2[i] + e0x2) & 0x00FF00FFu) << 7);
+      const uint32_t s2 = prmt(sw, 0u, lo | ((8u | lo) << 4) | ((lo + 1) << 8) | ((8u | (lo + 1)) << 12));
+      x[q][i] = (s2 & 0x807F807Fu) | (efield & 0x7F807F80u);
     }
-    msk[q] = escape_mask8(c2);
-    if (!full && v0 + 8 > m) msk[q] &= (1u << (m - v0)) - 1u;  // padding codes are checked below
-    cnt[q] = __popc(msk[q]);
+    // code 7 = all three bits set: one bit per value at positions 3j
+    uint32_t e = bits & (bits >> 1) & (bits >> 2) & 0x249249u;
+    if (!full && v0 + 8 > m) e &= (1u << (3 * (m - v0))) - 1u;  // padding codes are checked below
+    msk[q] = e;
+    cnt[q] = __popc(e);
   }
 
   unsigned base[4];
-  const unsigned total = chunk_ranks(cnt, base, scan);
-  bool corrupt = total != k;
+  const unsigned k = chunk_ranks(cnt, base, S.scan);  // the escape count follows from the codes
+  bool corrupt = pad16(3ull * k) != S.esc_bytes;
 
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     unsigned mk = msk[q], r = base[q];
     const unsigned v0 = 1024 * q + 8 * tid;
     while (mk) {
-      const int j = __ffs(mk) - 1;
+      const int j = (__ffs(mk) - 1) / 3;
       mk &= mk - 1;
-      if (r >= k) {
-        corrupt = true;
-        break;
-      }
-      const unsigned pos = __ldg(reinterpret_cast<const uint16_t*>(esc) + r);
-      const unsigned E = __ldg(esc + 2 * k + r);
+      const unsigned pos = reinterpret_cast<const uint16_t*>(esc)[r];
+      const unsigned E = esc[2 * k + r];
       if (pos != v0 + j || (E >= static_cast<unsigned>(e0) && E <= static_cast<unsigned>(e0) + 6)) corrupt = true;
       const unsigned sh = 16 * (j & 1);
       const uint32_t clear = ~(0xFFu << (sh + 7));
@@ -150,23 +166,24 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeParams p) {
     }
   }
 
+  uint16_t* dst = p.out + first;
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     const unsigned v0 = 1024 * q + 8 * tid;
     if (full || v0 + 8 <= m) {
-      *reinterpret_cast<uint4*>(p.out + first + v0) = make_uint4(x[q][0], x[q][1], x[q][2], x[q][3]);
+      *reinterpret_cast<uint4*>(dst + v0) = make_uint4(x[q][0], x[q][1], x[q][2], x[q][3]);
     } else if (v0 < m) {
-      for (unsigned j = 0; v0 + j < m; ++j)
-        p.out[first + v0 + j] = static_cast<uint16_t>(pick4(x[q], j >> 1) >> (16 * (j & 1)));
+      for (unsigned j = 0; v0 + j < m; ++j) dst[v0 + j] = static_cast<uint16_t>(pick4(x[q], j >> 1) >> (16 * (j & 1)));
     }
   }
 
-  if (tid == 0) {  // zero padding: escapes always, codes and bytes of a partial chunk
-    for (unsigned b = 3 * k; b < pad16(3ull * k); ++b) corrupt |= esc[b] != 0;
-    if (!full) {
-      for (unsigned b = m; b < smbytes; ++b) corrupt |= smp[b] != 0;
-      for (unsigned bit = 3 * m; bit < 8 * cbytes; ++bit) corrupt |= ((codes[bit >> 3] >> (bit & 7)) & 1u) != 0;
-    }
+  // zero padding: the escape list always, code bits and sign|mantissa bytes of a partial chunk
+  const unsigned epad = corrupt ? 0u : S.esc_bytes - 3 * k;  // < 16
+  if (tid < epad) corrupt |= esc[3 * k + tid] != 0;
+  if (!full) {
+    if (tid < smbytes - m) corrupt |= smp[m + tid] != 0;
+    const unsigned bit = 3 * m + tid;  // at most 127 padding bits
+    if (bit < 8 * cbytes) corrupt |= ((codes[bit >> 3] >> (bit & 7)) & 1u) != 0;
   }
   if (corrupt) set_error(p.status, ZC_ERR_CORRUPT);
 }

@@ -7,24 +7,35 @@
 // kernels use a communication-aware layout, aligned global/shared memory access and pipeline
 // data movement with compression compute (second technique).
 //
-// GB300 design.  A persistent grid of 128-thread CTAs, several per SM.  Each CTA takes chunks
-// from an atomic ticket, so chunk order follows execution order and every predecessor of a
-// chunk belongs to a running CTA.  Input chunks (8 KiB) arrive by bulk async copy (TMA engine,
-// mbarrier completion) two stages ahead; a thread holds 4 slices of 8 values, codes two values
-// per 32-bit word with packed 16-bit arithmetic, and writes the record into shared memory.
-// The record's stream offset comes from a decoupled look-back over per-chunk state words read
-// 32 at a time by one warp (Merrill & Garland, single-pass parallel prefix scan); every wait
-// is bounded.  The finished record leaves shared memory in one bulk async store, so the
-// compaction costs no extra pass over HBM.
+// GB300 design.  A persistent grid, three CTAs per SM, each with eight coding warps.  Chunks
+// are handed out by an atomic ticket (ticket order = chunk order).  Inputs (8 KiB per chunk)
+// arrive by bulk async copies (TMA engine, mbarrier completion) three stages ahead; a thread
+// holds 2 slices of 8 values and codes two values per 32-bit word with packed 16-bit
+// arithmetic.  The fixed part of a chunk has a place that follows from n, so it goes straight
+// from registers to HBM: 8-byte stores of sign|mantissa bytes and, per warp, 24 coalesced
+// 32-bit words of codes assembled with two shuffles.  Only the escape list waits for the
+// device-wide scan: each chunk publishes its list size in a per-chunk state word as soon as
+// its escape count is known, and a ninth warp in CTA 0 (the scanner) walks the state words in
+// order, 512 per round trip, turning every run of published sizes into inclusive offsets with
+// a warp scan (a chained scan with one scanner, after Merrill & Garland's single-pass scan).
+// Escape lists wait in a ring buffer in shared memory, where a waiting list costs only its own
+// bytes, so coding never waits for the scan; thread 0 writes resolved lists out with bulk
+// async stores and blocks only when the ring is full.  Every wait is bounded.
 #include "zc_common.cuh"
 
 namespace zc {
 namespace {
 
-constexpr int kThreads = kChunkThreads;  // 128
-constexpr int kStages = 2;
+constexpr int kCoders = 256;               // coding threads: 2 slices of 8 values each
+constexpr int kThreads = kCoders + 32;     // + one warp (the scanner in CTA 0)
+constexpr int kCtasPerSm = 3;
+constexpr int kStages = 3;                 // input chunks in flight per CTA
 constexpr unsigned kInBytes = 2 * kChunk;
+constexpr unsigned kRingBytes = 32 * 1024; // escape-list ring per CTA
+constexpr int kQueue = 64;                 // escape lists waiting, at most
+constexpr int kPeek = 4;                   // waiting lists whose state is read ahead per chunk
 constexpr unsigned kWaitLimit = 1u << 22;  // mbarrier polls before giving up
+constexpr int kScanPerLane = 16;           // state words per lane per scanner round trip
 
 struct EncodeParams {
   const uint16_t* in;
@@ -42,23 +53,39 @@ struct EncodeParams {
 
 struct __align__(128) EncodeSmem {
   uint4 xin[kStages][kInBytes / 16];
-  uint4 rec[kStages][kMaxRecordBytes / 16];
+  uint4 ring[kRingBytes / 16];
   uint64_t mbar[kStages];
   unsigned ticket[kStages];
+  // escape lists in the ring, oldest first (written by thread 0)
+  unsigned long long q_chunk[kQueue];
+  unsigned q_off[kQueue];
+  unsigned q_size[kQueue];
+  unsigned q_front, q_count;
+  unsigned long long peek_state[kPeek], peek_chunk[kPeek];
   unsigned scan[8];
-  unsigned long long rec_off;
-  int publish;  // look-back succeeded: store the record
-  int abort;
+  unsigned esc_off;  // ring offset of the list being written
+  int abort;         // written by thread 0 only, between the rank barrier and [E]
+  int load_fail;     // a bounded wait for an input copy ran out
   int e0;
 };
 
-__device__ void issue_load(EncodeSmem& S, int s, unsigned c, const EncodeParams& p) {
-  const uint64_t first = static_cast<uint64_t>(c) * kChunk;
+// Thread 0's ring bookkeeping: lists occupy [tail, head), wrapping at the end of the ring.
+struct Ring {
+  unsigned head = 0;          // where the newest list ends
+  unsigned used = 0;          // bytes held by waiting lists and by lists still being read out
+  unsigned unread_bytes = 0;  // bytes of written-out lists whose bulk store may still be reading
+  unsigned unread_off = 0;    // the oldest such list
+};
+
+__device__ __forceinline__ void bar_coders() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+// Thread 0: start the bulk copy of chunk c into stage s (a ragged tail, < 16 bytes, by plain loads).
+__device__ void issue_load(EncodeSmem& S, int s, uint64_t c, const EncodeParams& p) {
+  const uint64_t first = c * kChunk;
   const unsigned m = chunk_values(p.n, c);
   const unsigned bytes = 2 * m, bulk = bytes & ~15u;
   uint8_t* dst = reinterpret_cast<uint8_t*>(S.xin[s]);
-  for (unsigned b = bulk; b < bytes; b += 2)  // ragged tail of the last chunk: < 16 bytes
-    *reinterpret_cast<uint16_t*>(dst + b) = p.in[first + b / 2];
+  for (unsigned b = bulk; b < bytes; b += 2) *reinterpret_cast<uint16_t*>(dst + b) = p.in[first + b / 2];
   if (bulk) {
     fence_proxy_async_smem();
     mbar_arrive_expect_tx(&S.mbar[s], bulk);
@@ -68,55 +95,172 @@ __device__ void issue_load(EncodeSmem& S, int s, unsigned c, const EncodeParams&
   }
 }
 
-// Warp 0: publish this chunk's size and find the sum of all earlier record sizes.
-__device__ bool look_back(const EncodeParams& p, unsigned c, unsigned long long size,
-                          unsigned long long* exclusive) {
+// The scanner (warp 8 of CTA 0): resolve chunks in order.  Each round reads the next 512 state
+// words; the published sizes before the first unpublished one become inclusive offsets.
+__device__ __noinline__ void scanner(unsigned long long* flags, uint64_t N, int* status, unsigned spin_limit) {
   const unsigned lane = threadIdx.x & 31;
-  if (lane == 0) st_relaxed_u64(&p.flags[c], (c == 0 ? kFlagInclusive : kFlagAggregate) | size);
-  unsigned long long excl = 0;
-  if (c > 0) {
-    long long hi = static_cast<long long>(c) - 1;
-    unsigned spins = 0, backoff = 32;
-    for (;;) {
-      const long long idx = hi - static_cast<long long>(lane);
-      const unsigned long long f = idx >= 0 ? ld_relaxed_u64(&p.flags[idx]) : kFlagInclusive;
-      const unsigned st = static_cast<unsigned>(f >> 62);
-      const unsigned incl = __ballot_sync(0xFFFFFFFFu, st == 2);
-      const unsigned zero = __ballot_sync(0xFFFFFFFFu, st == 0);
-      const int first = incl ? __ffs(incl) - 1 : 31;
-      const unsigned window = first == 31 ? 0xFFFFFFFFu : ((2u << first) - 1u);
-      if (zero & window) {  // a predecessor in the window has not published yet
-        int bad = lane == 0 ? read_status(p.status) : 0;
-        bad = __shfl_sync(0xFFFFFFFFu, bad, 0);
-        if (++spins > p.spin_limit || bad != 0) return false;
-        __nanosleep(backoff);
-        backoff = backoff < 1024 ? backoff * 2 : 1024;
-        continue;
-      }
-      unsigned long long v = static_cast<int>(lane) <= first ? (f & kFlagValueMask) : 0ull;
+  uint64_t frontier = 0;
+  unsigned long long prefix = 0;
+  unsigned spins = 0, backoff = 32;
+  while (frontier < N) {
+    unsigned long long f[kScanPerLane];
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-      excl += v;
-      if (incl) break;
-      hi -= 32;
-      spins = 0;
-      backoff = 32;
+    for (int j = 0; j < kScanPerLane; ++j) {
+      const uint64_t idx = frontier + kScanPerLane * lane + j;
+      f[j] = idx < N ? ld_relaxed_u64(&flags[idx]) : 0ull;
     }
-    if (lane == 0) st_relaxed_u64(&p.flags[c], kFlagInclusive | (excl + size));
+    unsigned mine = 32 * kScanPerLane;  // first unpublished position held by this lane
+#pragma unroll
+    for (int j = kScanPerLane - 1; j >= 0; --j)
+      if ((f[j] >> 62) == 0) mine = kScanPerLane * lane + j;
+    const unsigned ready = __reduce_min_sync(0xFFFFFFFFu, mine);
+    if (ready == 0) {
+      int bad = lane == 0 ? read_status(status) : 0;
+      bad = __shfl_sync(0xFFFFFFFFu, bad, 0);
+      if (bad != 0) return;
+      if (++spins > spin_limit) {
+        if (lane == 0) set_error(status, ZC_ERR_TIMEOUT);
+        return;
+      }
+      __nanosleep(backoff);
+      backoff = backoff < 256 ? backoff * 2 : 256;
+      continue;
+    }
+    spins = 0;
+    backoff = 32;
+    unsigned long long own = 0;
+#pragma unroll
+    for (int j = 0; j < kScanPerLane; ++j)
+      if (kScanPerLane * lane + j < ready) own += f[j] & kFlagValueMask;
+    unsigned long long run = own;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const unsigned long long t = __shfl_up_sync(0xFFFFFFFFu, run, o);
+      if (lane >= static_cast<unsigned>(o)) run += t;
+    }
+    unsigned long long acc = prefix + (run - own);
+#pragma unroll
+    for (int j = 0; j < kScanPerLane; ++j) {
+      const unsigned q = kScanPerLane * lane + j;
+      if (q < ready) {
+        acc += f[j] & kFlagValueMask;
+        st_relaxed_u64(&flags[frontier + q], kFlagInclusive | acc);
+      }
+    }
+    prefix += __shfl_sync(0xFFFFFFFFu, run, 31);
+    frontier += ready;
   }
-  *exclusive = excl;
+}
+
+// Thread 0: write out the oldest waiting escape list, whose state word reads `f` (resolved),
+// and fill in its table entry (and the header fields that belong to the first and last chunk).
+__device__ void retire_front(EncodeSmem& S, Ring& R, const EncodeParams& p, int e0, unsigned long long f) {
+  const unsigned i = S.q_front;
+  const unsigned long long c = S.q_chunk[i];
+  const unsigned size = S.q_size[i];
+  const unsigned long long off = escape_base(p.n) + (f & kFlagValueMask) - size;
+  if (size) {
+    bulk_store(p.out + off, reinterpret_cast<const uint8_t*>(S.ring) + S.q_off[i], size);
+    bulk_commit();
+    if (R.unread_bytes == 0) R.unread_off = S.q_off[i];
+    R.unread_bytes += size;
+  }
+  unsigned long long* table = reinterpret_cast<unsigned long long*>(p.out + kHeaderBytes);
+  table[c] = off;
+  if (c == 0) {
+    unsigned long long* hdr = reinterpret_cast<unsigned long long*>(p.out);
+    hdr[0] = kMagicWord | (static_cast<unsigned long long>(e0) << 56);
+    hdr[1] = p.n;
+    hdr[2] = p.N;
+    if (kHeaderBytes + 8 * (p.N + 1) < records_base(p.n)) table[p.N + 1] = 0;  // zero pad
+  }
+  if (c == p.N - 1) {
+    const unsigned long long total = off + size;
+    table[p.N] = total;
+    reinterpret_cast<unsigned long long*>(p.out)[3] = total;
+    p.ctrl->total = total;
+    if (p.out_bytes) *p.out_bytes = total;
+  }
+  S.q_front = (S.q_front + 1) % kQueue;
+  --S.q_count;
+}
+
+// Thread 0: wait (bounded) until the oldest waiting list is resolved, then write it out.
+__device__ bool retire_front_blocking(EncodeSmem& S, Ring& R, const EncodeParams& p, int e0) {
+  const unsigned long long* flag = &p.flags[S.q_chunk[S.q_front]];
+  unsigned long long f = ld_relaxed_u64(flag);
+  unsigned spins = 0, backoff = 64;
+  while ((f >> 62) != 2) {
+    if (read_status(p.status) != 0) return false;
+    if (++spins > p.spin_limit) {
+      set_error(p.status, ZC_ERR_TIMEOUT);
+      return false;
+    }
+    __nanosleep(backoff);
+    backoff = backoff < 512 ? backoff * 2 : 512;
+    f = ld_relaxed_u64(flag);
+  }
+  retire_front(S, R, p, e0, f);
   return true;
 }
 
-__global__ void __launch_bounds__(kThreads) encode_kernel(EncodeParams p) {
+// Thread 0: room for `need` bytes (a multiple of 16, at most kMaxEscapeBytes) in the ring and
+// a free queue slot, writing out resolved lists as needed.  False after a failed wait.
+__device__ bool ring_alloc(EncodeSmem& S, Ring& R, const EncodeParams& p, int e0, unsigned need, unsigned* where) {
+  for (;;) {
+    if (S.q_count < kQueue) {
+      if (need == 0) {
+        *where = R.head;
+        return true;
+      }
+      if (R.used == 0) {  // nothing held: start over at the beginning
+        R.head = 0;
+        *where = 0;
+        return true;
+      }
+      const unsigned tail = R.unread_bytes ? R.unread_off : (S.q_count ? S.q_off[S.q_front] : R.head);
+      if (R.head > tail) {  // in use: [tail, head)
+        if (kRingBytes - R.head >= need) {
+          *where = R.head;
+          return true;
+        }
+        if (tail >= need) {
+          *where = 0;
+          return true;
+        }
+      } else if (tail - R.head >= need) {  // wrapped: in use [tail, end) and [0, head)
+        *where = R.head;
+        return true;
+      }
+    }
+    if (R.unread_bytes) {  // let the bulk stores finish reading; their space is then free
+      bulk_wait_read<0>();
+      R.used -= R.unread_bytes;
+      R.unread_bytes = 0;
+      continue;
+    }
+    if (S.q_count == 0 || !retire_front_blocking(S, R, p, e0)) return false;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) encode_kernel(EncodeParams p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   EncodeSmem& S = *reinterpret_cast<EncodeSmem*>(smem_raw);
-  const unsigned tid = threadIdx.x, warp = tid >> 5;
-  // Thread 0's bookkeeping, bit s for stage s: a load is in flight; parity of its next wait.
-  unsigned pending = 0, parity = 0;
+  const unsigned tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid >= kCoders) {  // the ninth warp: CTA 0 runs the scanner, the others leave
+    if (blockIdx.x == 0) scanner(p.flags, p.N, p.status, p.spin_limit);
+    return;
+  }
+  Ring R;                                // thread 0 only
+  unsigned pending = 0, parity = 0;      // thread 0: loads in flight per stage, next wait parity
+  unsigned next_ticket = 0;              // thread 0: the ticket for the next free stage
+  unsigned long long peek = 0, peek_chunk = ~0ull;  // lanes 0..kPeek-1 of warp 0
 
   if (tid == 0) {
     S.abort = 0;
+    S.load_fail = 0;
+    S.q_front = 0;
+    S.q_count = 0;
     S.e0 = p.base >= 0 ? p.base : __ldcg(&p.ctrl->e0);
     for (int s = 0; s < kStages; ++s) mbar_init(&S.mbar[s], 1);
     fence_mbar_init();
@@ -128,55 +272,59 @@ __global__ void __launch_bounds__(kThreads) encode_kernel(EncodeParams p) {
         pending |= 1u << s;
       }
     }
+    next_ticket = atomicAdd(&p.ctrl->encode_ticket, 1u);
   }
-  __syncthreads();
+  bar_coders();
   const int e0 = S.e0;
   const uint32_t neg_e0x2 = ((0x10000u - static_cast<unsigned>(e0)) & 0xFFFFu) * 0x00010001u;
+  const uint64_t R0 = records_base(p.n);
 
   for (unsigned it = 0;; ++it) {
-    const int s = it & 1;
-    if (tid == 0 && it >= 2) bulk_wait_read<1>();  // the store that last used rec[s] has read it
-    __syncthreads();                                 // [A]
-    const unsigned c = S.ticket[s];
-    if (c >= p.N || S.abort) break;
-
-    if (!mbar_wait(&S.mbar[s], (it >> 1) & 1, kWaitLimit)) {
+    const int s = it % kStages;
+    const unsigned c = S.ticket[s];  // set at least one barrier ago
+    if (c >= p.N) break;
+    if (!mbar_wait(&S.mbar[s], (it / kStages) & 1, kWaitLimit)) {
       set_error(p.status, ZC_ERR_TIMEOUT);
-      S.abort = 1;
+      S.load_fail = 1;  // acted on by thread 0 before [E]
     }
     if (tid == 0) {
       pending &= ~(1u << s);
       parity ^= 1u << s;
     }
-    uint4 xq[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) xq[q] = S.xin[s][128 * q + tid];
-    __syncthreads();  // [B] xin[s] is free again
-    if (S.abort) break;
+    const uint4 xq0 = S.xin[s][tid], xq1 = S.xin[s][256 + tid];
+    bar_coders();  // [B] stage s is free again
     if (tid == 0) {
-      const unsigned nc = atomicAdd(&p.ctrl->encode_ticket, 1u);
-      S.ticket[s] = nc;
-      if (nc < p.N) {
-        issue_load(S, s, nc, p);
+      // The next ticket was taken a chunk ago, so its round trip is already over; the one
+      // after it is taken now and used a chunk later.
+      S.ticket[s] = next_ticket;
+      if (next_ticket < p.N) {
+        issue_load(S, s, next_ticket, p);
         pending |= 1u << s;
+        next_ticket = atomicAdd(&p.ctrl->encode_ticket, 1u);
+      }
+    }
+    if (warp == 0 && lane < kPeek) {  // read ahead the state of the oldest waiting lists
+      peek_chunk = ~0ull;
+      if (lane < S.q_count) {
+        peek_chunk = S.q_chunk[(S.q_front + lane) % kQueue];
+        peek = ld_relaxed_u64(&p.flags[peek_chunk]);
       }
     }
 
-    // ---- code the chunk into rec[s]
+    // ---- code the chunk: the fixed part goes straight to its place in the stream
     const unsigned m = chunk_values(p.n, c);
     const bool full = m == kChunk;
     const unsigned cbytes = full ? kFullCodeBytes : static_cast<unsigned>(code_section_bytes(m));
     const unsigned smbytes = full ? kChunk : static_cast<unsigned>(pad16(m));
-    uint8_t* rec = reinterpret_cast<uint8_t*>(S.rec[s]);
-    uint8_t* codes = rec + kRecordHeaderBytes;
-    uint8_t* smp = codes + cbytes;
+    uint8_t* fixed = p.out + R0 + c * static_cast<uint64_t>(kFullFixedBytes);
 
-    unsigned cnt[4], msk[4];
-    uint32_t words[4][4];
+    unsigned cnt[2], msk[2];
+    uint32_t words[2][4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      uint32_t w[4] = {xq[q].x, xq[q].y, xq[q].z, xq[q].w};
-      const unsigned v0 = 1024 * q + 8 * tid;
+    for (int q = 0; q < 2; ++q) {
+      const uint4 xv = q ? xq1 : xq0;
+      uint32_t w[4] = {xv.x, xv.y, xv.z, xv.w};
+      const unsigned v0 = 2048 * q + 8 * tid;
       uint32_t c2[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) c2[i] = codes_x2(w[i], neg_e0x2);
@@ -189,83 +337,79 @@ __global__ void __launch_bounds__(kThreads) encode_kernel(EncodeParams p) {
         }
       }
       const uint2 smv = make_uint2(sign_mantissa_x4(w[0], w[1]), sign_mantissa_x4(w[2], w[3]));
-      if (full || v0 < smbytes) *reinterpret_cast<uint2*>(smp + v0) = smv;
+      if (full || v0 < smbytes) *reinterpret_cast<uint2*>(fixed + cbytes + v0) = smv;
       const uint32_t bits = pack_codes8(c2);
-      const unsigned b0 = 3 * (128 * q + tid);
-#pragma unroll
-      for (int b = 0; b < 3; ++b)
-        if (full || b0 + b < cbytes) codes[b0 + b] = static_cast<uint8_t>(bits >> (8 * b));
-      msk[q] = escape_mask8(c2);
+      const unsigned wbase = 3 * (256 * q + 32 * warp);  // this warp's 96 code bytes
+      store_code_groups(fixed + wbase, bits, cbytes > wbase ? cbytes - wbase : 0);
+      msk[q] = bits & (bits >> 1) & (bits >> 2) & 0x249249u;  // code 7: bit 3j for value j
       cnt[q] = __popc(msk[q]);
 #pragma unroll
       for (int i = 0; i < 4; ++i) words[q][i] = w[i];
     }
 
-    unsigned base[4];
-    const unsigned k = chunk_ranks(cnt, base, S.scan);  // contains [C]
-    const unsigned long long size = kRecordHeaderBytes + cbytes + smbytes + pad16(3ull * k);
-    uint8_t* esc = smp + smbytes;
-
-    if (warp == 0) {
-      unsigned long long excl = 0;
-      bool ok = false;
-      if (c != p.stall_chunk) {
-        ok = look_back(p, c, size, &excl);
-        if (!ok && tid == 0) set_error(p.status, ZC_ERR_TIMEOUT);
-      }
-      if (tid == 0) {
-        S.rec_off = records_base(p.n) + excl;
-        S.publish = ok;
-        if (!ok) S.abort = 1;
-      }
+    unsigned base[2];
+    const unsigned k = chunk_ranks_256(cnt, base, S.scan);
+    const unsigned esc_bytes = static_cast<unsigned>(pad16(3ull * k));
+    if (warp == 0 && lane < kPeek) {
+      S.peek_state[lane] = peek;
+      S.peek_chunk[lane] = peek_chunk;
     }
-    if (tid == kThreads - 1) {
-      *reinterpret_cast<uint4*>(rec) = make_uint4(k, m, 0u, 0u);
-      for (unsigned b = 3 * k; b < pad16(3ull * k); ++b) esc[b] = 0;
+    __syncwarp();
+    if (tid == 0) {
+      if (c != p.stall_chunk) st_relaxed_u64(&p.flags[c], kFlagAggregate | esc_bytes);  // publish early
+      for (int i = 0; i < kPeek && S.q_count > 0; ++i) {  // write out lists already resolved
+        if (S.peek_chunk[i] != S.q_chunk[S.q_front] || (S.peek_state[i] >> 62) != 2) break;
+        retire_front(S, R, p, e0, S.peek_state[i]);
+      }
+      unsigned where = 0;
+      if (S.load_fail || c == p.stall_chunk || !ring_alloc(S, R, p, e0, esc_bytes, &where)) {
+        S.abort = 1;  // (the stall test hook: this list is never resolved)
+        where = 0;
+      }
+      S.esc_off = where;
     }
+    bar_coders();  // [E] the list has a place in the ring
+    uint8_t* esc = reinterpret_cast<uint8_t*>(S.ring) + S.esc_off;
+    if (!S.abort) {
+      if (tid == kCoders - 1)
+        for (unsigned b = 3 * k; b < esc_bytes; ++b) esc[b] = 0;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      unsigned r = base[q];
-      unsigned mk = msk[q];
-      while (mk) {
-        const int j = __ffs(mk) - 1;
-        mk &= mk - 1;
-        const unsigned E = (pick4(words[q], j >> 1) >> (16 * (j & 1) + 7)) & 0xFFu;
-        *reinterpret_cast<uint16_t*>(esc + 2 * r) = static_cast<uint16_t>(1024 * q + 8 * tid + j);
-        esc[2 * k + r] = static_cast<uint8_t>(E);
-        ++r;
+      for (int q = 0; q < 2; ++q) {
+        unsigned r = base[q];
+        unsigned mk = msk[q];
+        while (mk) {
+          const int j = (__ffs(mk) - 1) / 3;
+          mk &= mk - 1;
+          const unsigned E = (pick4(words[q], j >> 1) >> (16 * (j & 1) + 7)) & 0xFFu;
+          *reinterpret_cast<uint16_t*>(esc + 2 * r) = static_cast<uint16_t>(2048 * q + 8 * tid + j);
+          esc[2 * k + r] = static_cast<uint8_t>(E);
+          ++r;
+        }
+      }
+      fence_proxy_async_smem();
+    }
+    bar_coders();  // [C] the list is complete in the ring
+    if (S.abort) break;
+    if (tid == 0) {
+      const unsigned qi = (S.q_front + S.q_count) % kQueue;
+      S.q_chunk[qi] = c;
+      S.q_off[qi] = S.esc_off;
+      S.q_size[qi] = esc_bytes;
+      ++S.q_count;
+      if (esc_bytes) {
+        R.head = S.esc_off + esc_bytes;
+        R.used += esc_bytes;
       }
     }
-    fence_proxy_async_smem();
-    __syncthreads();  // [D] record complete, offset known
-
-    if (tid == 0 && S.publish) {
-      const unsigned long long off = S.rec_off;
-      bulk_store(p.out + off, rec, static_cast<unsigned>(size));
-      unsigned long long* table = reinterpret_cast<unsigned long long*>(p.out + kHeaderBytes);
-      table[c] = off;
-      if (c == 0) {
-        unsigned long long* hdr = reinterpret_cast<unsigned long long*>(p.out);
-        hdr[0] = kMagicWord | (static_cast<unsigned long long>(e0) << 56);
-        hdr[1] = p.n;
-        hdr[2] = p.N;
-        if (kHeaderBytes + 8 * (p.N + 1) < records_base(p.n)) table[p.N + 1] = 0;  // zero pad
-      }
-      if (c == p.N - 1) {
-        const unsigned long long total = off + size;
-        table[p.N] = total;
-        reinterpret_cast<unsigned long long*>(p.out)[3] = total;
-        p.ctrl->total = total;
-        if (p.out_bytes) *p.out_bytes = total;
-      }
-    }
-    if (tid == 0) bulk_commit();  // one group per iteration, possibly empty
   }
 
   if (tid == 0) {
+    if (!S.abort) {
+      while (S.q_count > 0)
+        if (!retire_front_blocking(S, R, p, e0)) break;
+    }
     bulk_wait_all<0>();
-    // After an abort, loads may still be in flight into this CTA's shared memory.
-    for (int s = 0; s < kStages; ++s)
+    for (int s = 0; s < kStages; ++s)  // never leave a copy in flight
       if (pending & (1u << s)) mbar_wait(&S.mbar[s], (parity >> s) & 1u, kWaitLimit);
   }
 }
@@ -315,8 +459,7 @@ cudaError_t launch_encode(const uint16_t* in, uint64_t n, int base, uint8_t* out
   int per_sm = 0;
   err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, encode_kernel, kThreads, smem);
   if (err != cudaSuccess) return err;
-  if (per_sm < 1) per_sm = 1;
-  uint64_t grid = static_cast<uint64_t>(per_sm) * dev.sm_count;
+  uint64_t grid = static_cast<uint64_t>(per_sm > 0 ? per_sm : 1) * dev.sm_count;
   if (grid > p.N) grid = p.N;
   timing_begin(ZC_KERNEL_ENCODE, stream);
   encode_kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(p);

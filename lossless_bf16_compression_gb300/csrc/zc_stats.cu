@@ -21,6 +21,7 @@ namespace zc {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kCtasPerSm = 4;
 constexpr int kWarps = kThreads / 32;
 constexpr int kVecPerLane = 8;               // 8 x 16 B = 64 values per lane per block
 constexpr int kVecPerWarpBlock = 32 * kVecPerLane;
@@ -49,7 +50,7 @@ __device__ int select_e0(double S, unsigned long long n_f) {
 // Careful block sum for 64 values (32 words): skips Inf/NaN, and scales every square by
 // 4^-(Emax'-E') relative to the largest exponent present, so no fp32 overflow or underflow
 // matters.  Returns the fp64 value of the block sum and adds the non-finite count.
-__device__ double careful_block(const uint32_t (&w)[32], unsigned* nonfinite) {
+__device__ __forceinline__ double careful_block(const uint32_t (&w)[32], unsigned* nonfinite) {
   int emax = 0;
   unsigned nf = 0;
 #pragma unroll
@@ -80,8 +81,35 @@ __device__ double careful_block(const uint32_t (&w)[32], unsigned* nonfinite) {
   return static_cast<double>(s) * scale;
 }
 
+// The careful path for one lane's block (vectors wb + 32 j + lane), reloaded from memory so that
+// the fast path's registers never have to be spilled to call it.
+__device__ __noinline__ double careful_block_at(const uint4* in, uint64_t wb, uint64_t nv, unsigned lane,
+                                                unsigned* nonfinite) {
+  uint32_t w[32];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint64_t idx = wb + 32 * j + lane;
+    const uint4 v = idx < nv ? __ldg(in + idx) : make_uint4(0, 0, 0, 0);
+    w[4 * j] = v.x;
+    w[4 * j + 1] = v.y;
+    w[4 * j + 2] = v.z;
+    w[4 * j + 3] = v.w;
+  }
+  return careful_block(w, nonfinite);
+}
+
+// The last n % 8 values, zero-padded (a zero adds nothing and is not counted as non-finite).
+__device__ __noinline__ double tail_block(const uint16_t* tail, unsigned count, unsigned* nonfinite) {
+  uint32_t w[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) w[i] = 0;
+  for (unsigned i = 0; i < count; ++i) w[i >> 1] |= static_cast<uint32_t>(tail[i]) << (16 * (i & 1));
+  return careful_block(w, nonfinite);
+}
+
 // Fast block sum: the squares of 64 values in four fp32 FFMA chains.
-__device__ __forceinline__ void block_sum(const uint32_t (&w)[32], double* acc, unsigned* nonfinite) {
+__device__ __forceinline__ void block_sum(const uint32_t (&w)[32], const uint4* in, uint64_t wb, uint64_t nv,
+                                          unsigned lane, double* acc, unsigned* nonfinite) {
   float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
   for (int i = 0; i < 32; i += 2) {
@@ -98,7 +126,7 @@ __device__ __forceinline__ void block_sum(const uint32_t (&w)[32], double* acc, 
   if (blk >= 0x1p-100f && blk < 0x1p120f) {
     *acc += static_cast<double>(blk);
   } else {
-    *acc += careful_block(w, nonfinite);
+    *acc += careful_block_at(in, wb, nv, lane, nonfinite);
   }
 }
 
@@ -112,7 +140,7 @@ struct StatsParams {
 
 // Exact fallback, run by the last CTA alone: per-exponent integer sums of sig^2, then the
 // 576-bit integer sum_E T_E 2^(2E-2) (= S 2^266), rounded once to fp64, nearest-even.
-__device__ double exact_sum_of_squares(const uint16_t* x, uint64_t n, unsigned long long* bins) {
+__device__ __noinline__ double exact_sum_of_squares(const uint16_t* x, uint64_t n, unsigned long long* bins) {
   const unsigned warp = threadIdx.x >> 5;
   for (int i = threadIdx.x; i < kWarps * 256; i += kThreads) bins[i] = 0;
   __syncthreads();
@@ -180,7 +208,7 @@ __device__ double exact_sum_of_squares(const uint16_t* x, uint64_t n, unsigned l
   return result;
 }
 
-__global__ void __launch_bounds__(kThreads) stats_kernel(StatsParams p) {
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) stats_kernel(StatsParams p) {
   __shared__ double red_sum[kWarps];
   __shared__ unsigned long long red_nf[kWarps];
   __shared__ unsigned long long bins[kWarps * 256];
@@ -206,17 +234,10 @@ __global__ void __launch_bounds__(kThreads) stats_kernel(StatsParams p) {
       w[4 * j + 2] = v.z;
       w[4 * j + 3] = v.w;
     }
-    block_sum(w, &acc, &nonfinite);
+    block_sum(w, p.in, wb, nv, lane, &acc, &nonfinite);
   }
-  // The last n % 8 values (zero-padded: a zero adds nothing and is not counted as non-finite).
-  if (blockIdx.x == 0 && threadIdx.x == 0 && (p.n & 7)) {
-    uint32_t w[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) w[i] = 0;
-    const uint16_t* tail = reinterpret_cast<const uint16_t*>(p.in) + (nv << 3);
-    for (int i = 0; i < static_cast<int>(p.n & 7); ++i) w[i >> 1] |= static_cast<uint32_t>(tail[i]) << (16 * (i & 1));
-    acc += careful_block(w, &nonfinite);
-  }
+  if (blockIdx.x == 0 && threadIdx.x == 0 && (p.n & 7))
+    acc += tail_block(reinterpret_cast<const uint16_t*>(p.in) + (nv << 3), static_cast<unsigned>(p.n & 7), &nonfinite);
 
   // CTA reduction in a fixed order.
   unsigned long long nf = nonfinite;
@@ -313,7 +334,10 @@ cudaError_t launch_stats(const uint16_t* in, uint64_t n, uint8_t* out, const Dev
   p.status = dev.status;
   const uint64_t nv = n >> 3;
   const uint64_t blocks_needed = (nv + kVecPerWarpBlock * kWarps - 1) / (kVecPerWarpBlock * kWarps);
-  uint64_t grid = static_cast<uint64_t>(dev.sm_count) * 4;
+  int per_sm = 0;
+  cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, stats_kernel, kThreads, 0);
+  if (err != cudaSuccess) return err;
+  uint64_t grid = static_cast<uint64_t>(per_sm > 0 ? per_sm : 1) * dev.sm_count;  // one wave
   if (grid > blocks_needed) grid = blocks_needed;
   if (grid < 1) grid = 1;
   if (grid > kStatsMaxCtas) grid = kStatsMaxCtas;

@@ -22,8 +22,13 @@
  *       f(u) = f(2u) for f(t) = P(|Z| < t) + P(|Z| >= 128 t), Z ~ N(0,1).  For a Gaussian
  *       of standard deviation sigma this picks the 7-binade window with the fewest expected
  *       escapes.  It is evaluated as floor(ilogb(q*c^2)/2) + 127.
- *   R5  byte layout ("ZCB1"): 32-byte header, u64 chunk-offset table, then one record per
- *       4096-value chunk; every section padded with zeros to 16 bytes; little-endian.
+ *   R5  byte layout ("ZCB1", version 2), read from the "communication-aware data layout" of
+ *       the second technique and the compress / exchange sizes / send workflow (Figure 5(b),
+ *       Design-1): every chunk's fixed-size part (3-bit codes, then the sign|mantissa plane) sits
+ *       at an offset that follows from n alone, so it can be sent before any size is known;
+ *       only the variable escape lists are compacted, behind a table of their offsets.
+ *       32-byte header, u64 escape-offset table, fixed parts in chunk order, escape lists in
+ *       chunk order; every section padded with zeros to 16 bytes; little-endian.
  */
 #include "zc_oracle.h"
 
@@ -33,8 +38,7 @@
 
 #define CHUNK 4096u
 #define HEADER_BYTES 32u
-#define RECORD_HEADER_BYTES 16u
-#define FORMAT_VERSION 1u
+#define FORMAT_VERSION 2u
 #define LOG2_CHUNK 12u
 #define E0_MAX 249
 #define WINDOW 7
@@ -50,18 +54,10 @@ static void put_u16(uint8_t* p, uint16_t v) {
   p[0] = (uint8_t)(v & 0xFFu);
   p[1] = (uint8_t)(v >> 8);
 }
-static void put_u32(uint8_t* p, uint32_t v) {
-  for (int i = 0; i < 4; ++i) p[i] = (uint8_t)(v >> (8 * i));
-}
 static void put_u64(uint8_t* p, uint64_t v) {
   for (int i = 0; i < 8; ++i) p[i] = (uint8_t)(v >> (8 * i));
 }
 static uint16_t get_u16(const uint8_t* p) { return (uint16_t)(p[0] | (p[1] << 8)); }
-static uint32_t get_u32(const uint8_t* p) {
-  uint32_t v = 0;
-  for (int i = 3; i >= 0; --i) v = (v << 8) | p[i];
-  return v;
-}
 static uint64_t get_u64(const uint8_t* p) {
   uint64_t v = 0;
   for (int i = 7; i >= 0; --i) v = (v << 8) | p[i];
@@ -78,22 +74,32 @@ static unsigned bf16_sign(uint16_t x) { return (x >> 15) & 1u; }
 
 uint64_t zco_num_chunks(uint64_t n) { return (n + CHUNK - 1) / CHUNK; }
 
+static uint64_t chunk_len(uint64_t n, uint64_t c) { return n - c * CHUNK < CHUNK ? n - c * CHUNK : CHUNK; }
+
+/* Start of the fixed region: after the header and the N+1 escape offsets. */
 uint64_t zco_records_base(uint64_t n) {
   return pad16(HEADER_BYTES + 8u * (zco_num_chunks(n) + 1u));
 }
 
-/* Record = 16-byte record header + 3-bit code section + sign/mantissa plane + escape list. */
-uint64_t zco_record_bytes(uint64_t m, uint64_t k) {
-  return RECORD_HEADER_BYTES + pad16((3u * m + 7u) / 8u) + pad16(m) + pad16(3u * k);
+/* Fixed part of a chunk of m values: 3-bit code section, then the sign|mantissa plane. */
+static uint64_t fixed_bytes(uint64_t m) { return pad16((3u * m + 7u) / 8u) + pad16(m); }
+
+/* Bytes a chunk of m values with k escapes contributes: its fixed part and its escape list. */
+uint64_t zco_record_bytes(uint64_t m, uint64_t k) { return fixed_bytes(m) + pad16(3u * k); }
+
+/* Where chunk c's fixed part starts: every earlier chunk is full. */
+static uint64_t fixed_offset(uint64_t n, uint64_t c) { return zco_records_base(n) + c * fixed_bytes(CHUNK); }
+
+/* Start of the escape region: after every fixed part. */
+static uint64_t escape_base(uint64_t n) {
+  uint64_t N = zco_num_chunks(n);
+  return N ? fixed_offset(n, N - 1) + fixed_bytes(chunk_len(n, N - 1)) : zco_records_base(n);
 }
 
 uint64_t zco_max_stream_bytes(uint64_t n) {
-  uint64_t total = zco_records_base(n);
+  uint64_t total = escape_base(n);
   uint64_t N = zco_num_chunks(n);
-  for (uint64_t c = 0; c < N; ++c) {
-    uint64_t m = n - c * CHUNK < CHUNK ? n - c * CHUNK : CHUNK;
-    total += zco_record_bytes(m, m); /* worst case: every value escapes */
-  }
+  for (uint64_t c = 0; c < N; ++c) total += pad16(3u * chunk_len(n, c)); /* every value escapes */
   return total;
 }
 
@@ -213,15 +219,13 @@ int64_t zco_compress(const uint16_t* x, uint64_t n, int base_or_auto, uint8_t* o
   int e0 = base_or_auto == -1 ? zco_choose_e0(x, n) : base_or_auto;
 
   uint64_t N = zco_num_chunks(n);
-  uint64_t base = zco_records_base(n);
 
-  /* First pass: record sizes, so that the capacity check happens before any write. */
-  uint64_t total = base;
+  /* First pass: escape-list sizes, so that the capacity check happens before any write. */
+  uint64_t total = escape_base(n);
   for (uint64_t c = 0; c < N; ++c) {
-    uint64_t m = n - c * CHUNK < CHUNK ? n - c * CHUNK : CHUNK;
-    uint64_t k = 0;
+    uint64_t m = chunk_len(n, c), k = 0;
     for (uint64_t i = 0; i < m; ++i) k += exponent_code(bf16_exponent(x[c * CHUNK + i]), e0) == 7u;
-    total += zco_record_bytes(m, k);
+    total += pad16(3u * k);
   }
   if (out == NULL || total > cap) return -ZCO_ERR_CAPACITY;
   memset(out, 0, (size_t)total);
@@ -238,24 +242,17 @@ int64_t zco_compress(const uint16_t* x, uint64_t n, int base_or_auto, uint8_t* o
   put_u64(out + 16, N);
   put_u64(out + 24, total);
 
-  /* Records, in chunk order, each at the offset the table names. */
-  uint64_t pos = base;
+  uint64_t esc_pos = escape_base(n);
   for (uint64_t c = 0; c < N; ++c) {
     const uint16_t* xc = x + c * CHUNK;
-    uint64_t m = n - c * CHUNK < CHUNK ? n - c * CHUNK : CHUNK;
-    put_u64(out + HEADER_BYTES + 8u * c, pos);
-
-    uint8_t* rec = out + pos;
-    uint64_t code_bytes = pad16((3u * m + 7u) / 8u);
-    uint8_t* codes = rec + RECORD_HEADER_BYTES;
-    uint8_t* sm = codes + code_bytes;
-    uint8_t* esc = sm + pad16(m);
+    uint64_t m = chunk_len(n, c);
+    uint8_t* codes = out + fixed_offset(n, c);
+    uint8_t* sm = codes + pad16((3u * m + 7u) / 8u);
+    uint8_t* esc = out + esc_pos;
+    put_u64(out + HEADER_BYTES + 8u * c, esc_pos);
 
     uint64_t k = 0;
     for (uint64_t i = 0; i < m; ++i) k += exponent_code(bf16_exponent(xc[i]), e0) == 7u;
-    put_u32(rec, (uint32_t)k);
-    put_u32(rec + 4, (uint32_t)m);
-    /* rec[8..15] reserved, zero */
 
     uint64_t r = 0;
     for (uint64_t i = 0; i < m; ++i) {
@@ -270,9 +267,9 @@ int64_t zco_compress(const uint16_t* x, uint64_t n, int base_or_auto, uint8_t* o
         r += 1;
       }
     }
-    pos += zco_record_bytes(m, k);
+    esc_pos += pad16(3u * k);
   }
-  put_u64(out + HEADER_BYTES + 8u * N, pos);
+  put_u64(out + HEADER_BYTES + 8u * N, esc_pos);
   return (int64_t)total;
 }
 
@@ -296,25 +293,23 @@ int zco_decompress(const uint8_t* in, uint64_t in_bytes, uint16_t* out, uint64_t
   if (get_u64(in + 16) != N) return ZCO_ERR_CORRUPT;
   uint64_t total = get_u64(in + 24);
   uint64_t base = zco_records_base(n);
-  if (total > in_bytes || total > zco_max_stream_bytes(n) || total < base) return ZCO_ERR_CORRUPT;
+  if (total > in_bytes || total > zco_max_stream_bytes(n) || total < escape_base(n)) return ZCO_ERR_CORRUPT;
   if (!all_zero(in + HEADER_BYTES + 8u * (N + 1), base - (HEADER_BYTES + 8u * (N + 1))))
     return ZCO_ERR_CORRUPT;
 
-  uint64_t pos = base;
+  uint64_t esc_pos = escape_base(n);
   for (uint64_t c = 0; c < N; ++c) {
-    uint64_t m = n - c * CHUNK < CHUNK ? n - c * CHUNK : CHUNK;
-    if (get_u64(in + HEADER_BYTES + 8u * c) != pos) return ZCO_ERR_CORRUPT;
-    if (pos + RECORD_HEADER_BYTES > total) return ZCO_ERR_CORRUPT;
-    const uint8_t* rec = in + pos;
-    uint64_t k = get_u32(rec);
-    if (get_u32(rec + 4) != m || k > m || !all_zero(rec + 8, 8)) return ZCO_ERR_CORRUPT;
-    uint64_t size = zco_record_bytes(m, k);
-    if (size > total - pos) return ZCO_ERR_CORRUPT;
-
+    uint64_t m = chunk_len(n, c);
+    if (get_u64(in + HEADER_BYTES + 8u * c) != esc_pos) return ZCO_ERR_CORRUPT;
+    const uint8_t* codes = in + fixed_offset(n, c);
     uint64_t code_bytes = pad16((3u * m + 7u) / 8u);
-    const uint8_t* codes = rec + RECORD_HEADER_BYTES;
     const uint8_t* sm = codes + code_bytes;
-    const uint8_t* esc = sm + pad16(m);
+
+    uint64_t k = 0; /* the escape count follows from the codes */
+    for (uint64_t i = 0; i < m; ++i)
+      k += (get_bit(codes, 3u * i) & get_bit(codes, 3u * i + 1) & get_bit(codes, 3u * i + 2));
+    if (esc_pos + pad16(3u * k) > total) return ZCO_ERR_CORRUPT;
+    const uint8_t* esc = in + esc_pos;
 
     uint64_t r = 0;
     for (uint64_t i = 0; i < m; ++i) {
@@ -324,7 +319,6 @@ int zco_decompress(const uint8_t* in, uint64_t in_bytes, uint16_t* out, uint64_t
       if (code < 7u) {
         E = (unsigned)e0 + code;
       } else {
-        if (r >= k) return ZCO_ERR_CORRUPT;
         if (get_u16(esc + 2u * r) != i) return ZCO_ERR_CORRUPT; /* positions ascending, exact */
         E = esc[2u * k + r];
         if (exponent_code(E, e0) != 7u) return ZCO_ERR_CORRUPT; /* an escape must lie outside */
@@ -332,13 +326,12 @@ int zco_decompress(const uint8_t* in, uint64_t in_bytes, uint16_t* out, uint64_t
       }
       out[c * CHUNK + i] = (uint16_t)(((unsigned)(sm[i] >> 7) << 15) | (E << 7) | (sm[i] & 0x7Fu));
     }
-    if (r != k) return ZCO_ERR_CORRUPT;
     for (uint64_t b = 3u * m; b < 8u * code_bytes; ++b)
       if (get_bit(codes, b)) return ZCO_ERR_CORRUPT;
     if (!all_zero(sm + m, pad16(m) - m)) return ZCO_ERR_CORRUPT;
     if (!all_zero(esc + 3u * k, pad16(3u * k) - 3u * k)) return ZCO_ERR_CORRUPT;
-    pos += size;
+    esc_pos += pad16(3u * k);
   }
-  if (get_u64(in + HEADER_BYTES + 8u * N) != pos || pos != total) return ZCO_ERR_CORRUPT;
+  if (get_u64(in + HEADER_BYTES + 8u * N) != esc_pos || esc_pos != total) return ZCO_ERR_CORRUPT;
   return ZCO_OK;
 }

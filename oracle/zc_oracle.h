@@ -40,7 +40,9 @@ extern "C" {
 #define ZCO_ERR_SIZE_MISMATCH 5
 #define ZCO_ERR_CAPACITY 7
 
-/* Layout helpers (pure). */
+/* Layout helpers (pure).  records_base: start of the fixed-part region (after the header and
+ * the escape-offset table); record_bytes: what a chunk of m values with k escapes adds to the
+ * stream (its fixed part plus its escape list). */
 uint64_t zco_num_chunks(uint64_t n);
 uint64_t zco_records_base(uint64_t n);
 uint64_t zco_record_bytes(uint64_t m, uint64_t k);

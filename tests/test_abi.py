@@ -45,7 +45,8 @@ def test_max_stream_bytes_closed_form_large(lib):
     N = (n + 4095) // 4096
     rem = n % 4096
     pad16 = lambda v: (v + 15) // 16 * 16  # noqa: E731
-    want = pad16(32 + 8 * (N + 1)) + (n // 4096) * 17936 + 16 + pad16((3 * rem + 7) // 8) + pad16(rem) + pad16(3 * rem)
+    # header + table, then per chunk the fixed part and a full escape list (every value escapes)
+    want = pad16(32 + 8 * (N + 1)) + (n // 4096) * (5632 + 12288) + pad16((3 * rem + 7) // 8) + pad16(rem) + pad16(3 * rem)
     assert zc.zc_max_stream_bytes(n) == want
 
 

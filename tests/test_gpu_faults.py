@@ -47,46 +47,51 @@ def oracle_status(stream, n, capacity):
     return oracle.decompress(buf, n)
 
 
-def record_offset(s, c):
+def escape_offset(s, c):
     return int(s[32 + 8 * c:40 + 8 * c].view(np.uint64)[0])
 
 
-def targeted_mutations(s):
-    off0, off3 = record_offset(s, 0), record_offset(s, 3)
-    k0 = int(s[off0:off0 + 4].view(np.uint32)[0])
-    esc0 = off0 + 16 + 1536 + 4096
+def targeted_mutations(s, x):
+    pad16 = lambda v: (v + 15) // 16 * 16  # noqa: E731
+    N = (N_VALUES + 4095) // 4096
+    R0 = pad16(32 + 8 * (N + 1))
+    e0 = int(s[7])
+    E = (x[:4096].astype(np.int64) >> 7) & 0xFF
+    k0 = int(((E < e0) | (E > e0 + 6)).sum())
+    esc0 = escape_offset(s, 0)
+    last = R0 + (N - 1) * 5632  # fixed part of the last chunk (100 values)
     muts = {
         "magic": (0, 0x00),
-        "version": (4, 2),
+        "version": (4, 1),
         "log2_chunk": (6, 11),
         "base_250": (7, 250),
         "N": (16, 5),
         "total_bytes": (24, s[24] ^ 0x10),
         "offset_0": (32, s[32] ^ 0x10),
         "offset_1_misaligned": (40, s[40] ^ 0x01),
-        "record_k": (off0, s[off0] ^ 0x01),
-        "record_m": (off0 + 4, s[off0 + 4] ^ 0x01),
-        "record_reserved": (off0 + 9, 1),
         "escape_position": (esc0, s[esc0] ^ 0x01),
-        "escape_exponent_in_window": (esc0 + 2 * k0, s[7]),
-        "escape_padding": (esc0 + 3 * k0 + (1 if (3 * k0) % 16 else 0), 0x55),
-        "last_codes_padding": (off3 + 16 + (3 * 100 + 7) // 8 + 1, 0x80),
-        "last_byte_plane_padding": (off3 + 16 + 48 + 100 + 1, 0x01),
+        "escape_exponent_in_window": (esc0 + 2 * k0, e0),
+        "last_codes_padding": (last + (3 * 100 + 7) // 8 + 1, 0x80),
+        "last_byte_plane_padding": (last + 48 + 100 + 1, 0x01),
     }
+    if (3 * k0) % 16:
+        muts["escape_padding"] = (esc0 + 3 * k0 + 1, 0x55)
+    if not (E[0] < e0 or E[0] > e0 + 6):  # value 0's code is in bits 0..2 of the first code byte
+        muts["code_to_escape"] = (R0, s[R0] | 0x07)
     out = {}
     for name, (pos, val) in muts.items():
         t = s.copy()
         t[pos] = np.uint8(val)
         out[name] = t
     out["n_mismatch"] = u64_at(s, 8, N_VALUES + 1)
-    out["table_end"] = u64_at(s, 32 + 8 * 4, int(s[24:32].view(np.uint64)[0]) + 16)
+    out["table_end"] = u64_at(s, 32 + 8 * N, int(s[24:32].view(np.uint64)[0]) + 16)
     return out
 
 
 def test_targeted_corruptions_are_reported(sample):
     x, s = sample
     cap = zc.zc_max_compressed_bytes(N_VALUES)
-    for name, t in targeted_mutations(s).items():
+    for name, t in targeted_mutations(s, x).items():
         ost, _ = oracle_status(t, N_VALUES, cap)
         assert ost != oracle.OK, f"{name}: the oracle accepts it, the mutation is not a corruption"
         st, _ = gpu_decompress_bytes(t, N_VALUES, cap)

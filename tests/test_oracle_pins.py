@@ -39,7 +39,7 @@ def closed_form_size(x, e0):
     for c in range(N):
         m = min(CHUNK, n - c * CHUNK)
         k = int(escape[c * CHUNK:c * CHUNK + m].sum())
-        total += 16 + pad16((3 * m + 7) // 8) + pad16(m) + pad16(3 * k)
+        total += pad16((3 * m + 7) // 8) + pad16(m) + pad16(3 * k)
     return total
 
 
@@ -187,7 +187,8 @@ def test_size_closed_form_around_chunk_edges(n):
 
 
 def test_about_eleven_bits_per_value():
-    """No escapes: 16 -> about 11 bits per value, about 31% less volume (the page's ideal)."""
+    """No escapes: 16 -> about 11 bits per value, about 31% less volume (the page's ideal):
+    3 code bits + 8 sign|mantissa bits per value, plus the header and offset table."""
     rng = np.random.default_rng(5)
     n = 1 << 20
     e0 = 122
@@ -195,7 +196,7 @@ def test_about_eleven_bits_per_value():
     x = ((rng.integers(0, 2, n) << 15) | (exps << 7) | rng.integers(0, 128, n)).astype(np.uint16)
     s = oracle.compress(x, e0)
     bits_per_value = 8 * len(s) / n
-    assert 11.0 <= bits_per_value < 11.05
+    assert 11.0 <= bits_per_value < 11.02  # 3 + 8 bits, plus 8 table bytes per 4096 values
     assert abs((1 - len(s) / (2 * n)) - 0.31) < 0.005
     assert len(s) == closed_form_size(x, e0)
 
@@ -230,7 +231,7 @@ def test_every_pattern_as_single_value():
         s = oracle.compress(one)
         E = (int(b) >> 7) & 0xFF
         k = 0 if s[7] <= E <= s[7] + 6 else 1
-        assert len(s) == 48 + 16 + 16 + 16 + 16 * k
+        assert len(s) == 48 + 16 + 16 + 16 * k  # header+table, codes, byte plane, escapes
         st, back = oracle.decompress(s, 1)
         assert st == oracle.OK and back[0] == b
 
@@ -307,13 +308,28 @@ def test_decoder_rejections(golden_tiny):
     assert oracle.decompress(t, 5)[0] == oracle.ERR_CORRUPT
     t = stream.copy(); t[7] = 250  # base out of range  # noqa: E702
     assert oracle.decompress(t, 5)[0] == oracle.ERR_CORRUPT
-    t = stream.copy(); t[16 * 6 + 6] = 1  # nonzero escape padding (after 2+2+1+1 bytes)  # noqa: E702
+    t = stream.copy(); t[80 + 6] = 1  # nonzero escape padding (after 2+2+1+1 bytes)  # noqa: E702
     assert oracle.decompress(t, 5)[0] == oracle.ERR_CORRUPT
-    t = stream.copy(); t[16 * 6 + 4] = 130  # escape exponent inside the window  # noqa: E702
+    t = stream.copy(); t[80 + 4] = 130  # escape exponent inside the window  # noqa: E702
+    assert oracle.decompress(t, 5)[0] == oracle.ERR_CORRUPT
+    t = stream.copy(); t[48] |= 0x07  # code 0 -> 7: one more escape than the list holds  # noqa: E702
     assert oracle.decompress(t, 5)[0] == oracle.ERR_CORRUPT
 
 
 # ----------------------------------------------------------------------------- statistics
+
+
+def stream_escape_count(s, n):
+    """Escapes in a stream, counted from the 3-bit codes of its fixed parts."""
+    N = (n + CHUNK - 1) // CHUNK
+    base = pad16(32 + 8 * (N + 1))
+    k = 0
+    for c in range(N):
+        m = min(CHUNK, n - c * CHUNK)
+        codes = s[base + 5632 * c: base + 5632 * c + (3 * m + 7) // 8]
+        bits = np.unpackbits(codes, bitorder="little")[:3 * m].reshape(m, 3)
+        k += int(np.all(bits == 1, axis=1).sum())
+    return k
 
 
 def test_gaussian_escape_rate_matches_model():
@@ -321,11 +337,7 @@ def test_gaussian_escape_rate_matches_model():
     x = workloads.sweep(20)
     s = oracle.compress(x)
     assert s[7] == 122
-    rec = int.from_bytes(s[32:40].tobytes(), "little")
-    N = 256
-    k = sum(int.from_bytes(s[o:o + 4].tobytes(), "little")
-            for o in [int.from_bytes(s[32 + 8 * c:40 + 8 * c].tobytes(), "little") for c in range(N)])
-    assert rec == pad16(32 + 8 * (N + 1))
+    k = stream_escape_count(s, x.size)
     p = math.erf(2.0 ** -5 / math.sqrt(2)) + math.erfc(4.0 / math.sqrt(2))
     n = x.size
     assert abs(k - p * n) < 5 * math.sqrt(n * p * (1 - p))
