@@ -289,36 +289,60 @@ __device__ __forceinline__ unsigned chunk_ranks_impl(const unsigned (&cnt)[4], u
   return run;
 }
 
-// 256 threads, 2 slices: chunk value v = 2048 q + 8 t + j is held by thread t (q = 0..1,
-// j = 0..7), escapes ordered by (q, t, j).  Same contract as below; `scratch` holds 8 words;
-// one barrier over the first 256 threads (named barrier 1).
-__device__ __forceinline__ unsigned chunk_ranks_256(const unsigned (&cnt)[2], unsigned (&base)[2],
-                                                    unsigned* scratch) {
+// kT threads, kS = 4096 / (8 kT) slices: chunk value v = 8 kT q + 8 t + j is held by thread t
+// (q = 0..kS-1, j = 0..7); escapes are ordered by (q, t, j).  Given each thread's per-slice
+// escape counts, return each slice's first rank and the chunk total.  Counts travel two to a
+// word (16-bit fields), so the cross-warp sums are plain adds.  Uses named barrier 1 over the
+// CTA's first kT threads; `scratch` holds kT / 32 * kS / 2 words (a multiple of 4).
+template <int kT>
+__device__ __forceinline__ unsigned chunk_ranks_bar1(const unsigned (&cnt)[kChunk / (8 * kT)],
+                                                     unsigned (&base)[kChunk / (8 * kT)], unsigned* scratch) {
+  constexpr int kS = kChunk / (8 * kT), kP = kS / 2, kW = kT / 32, kWords = kW * kP;
+  static_assert(kS % 2 == 0 && kWords % 4 == 0, "two counters per word, whole 16-byte reads");
   const unsigned lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  unsigned p0 = cnt[0] | (cnt[1] << 16);
-  const unsigned own = p0;
+  unsigned pk[kP], own[kP];
+#pragma unroll
+  for (int i = 0; i < kP; ++i) own[i] = pk[i] = cnt[2 * i] | (cnt[2 * i + 1] << 16);
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const unsigned a = __shfl_up_sync(0xFFFFFFFFu, p0, o);
-    if (lane >= (unsigned)o) p0 += a;
-  }
-  if (lane == 31) scratch[warp] = p0;
-  asm volatile("bar.sync 1, 256;" ::: "memory");
-  const unsigned ex = p0 - own;
-  unsigned before0 = 0, before1 = 0, total0 = 0, total1 = 0;
 #pragma unroll
-  for (int w = 0; w < 8; ++w) {
-    const unsigned t = scratch[w];
-    total0 += t & 0xFFFFu;
-    total1 += t >> 16;
-    if ((unsigned)w < warp) {
-      before0 += t & 0xFFFFu;
-      before1 += t >> 16;
+    for (int i = 0; i < kP; ++i) {
+      const unsigned t = __shfl_up_sync(0xFFFFFFFFu, pk[i], o);
+      if (lane >= (unsigned)o) pk[i] += t;
     }
   }
-  base[0] = before0 + (ex & 0xFFFFu);
-  base[1] = total0 + before1 + (ex >> 16);
-  return total0 + total1;
+  if (lane == 31) {
+#pragma unroll
+    for (int i = 0; i < kP; ++i) scratch[kW * i + warp] = pk[i];  // pair-major: [pair][warp]
+  }
+  asm volatile("bar.sync 1, %0;" ::"n"(kT) : "memory");
+  unsigned tot[kP], bef[kP];
+#pragma unroll
+  for (int i = 0; i < kP; ++i) {
+    tot[i] = 0;
+    bef[i] = 0;
+  }
+#pragma unroll
+  for (int v = 0; v < kWords / 4; ++v) {
+    const uint4 t4 = reinterpret_cast<const uint4*>(scratch)[v];
+    const unsigned t[4] = {t4.x, t4.y, t4.z, t4.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int i = (4 * v + e) / kW, w = (4 * v + e) % kW;
+      tot[i] += t[e];
+      bef[i] += (unsigned)w < warp ? t[e] : 0u;
+    }
+  }
+  unsigned run = 0;
+#pragma unroll
+  for (int i = 0; i < kP; ++i) {
+    const unsigned ex = pk[i] - own[i] + bef[i];  // both fields: ranks before this thread, in this warp pair
+    base[2 * i] = run + (ex & 0xFFFFu);
+    run += tot[i] & 0xFFFFu;
+    base[2 * i + 1] = run + (ex >> 16);
+    run += tot[i] >> 16;
+  }
+  return run;
 }
 
 // Chunk value v = 1024 q + 8 t + j is held by thread t (slice q = 0..3, j = 0..7).  In

@@ -10,10 +10,12 @@
 // follow from n and the offset table locates every escape list, so there is no inter-CTA
 // dependency.  Warp 0 reads the header and the chunk's two escape offsets in one round trip and
 // checks them; the fixed part (5,632 B) and the escape list (at most 12,288 B) then arrive in
-// shared memory by two bulk async copies (TMA engine, one mbarrier).  A thread holds 4 slices of 8 values; per slice it takes its 24 code bits and 8
-// sign|mantissa bytes from shared memory, builds two values per 32-bit word with one imad and
-// one lop3, and writes one coalesced 16-byte store.  Escapes get their rank from the same block
-// scan the encoder uses, which also checks every stored position and exponent.  Every offset
+// shared memory by two bulk async copies (TMA engine, one mbarrier).  A thread holds 4 slices
+// of 8 values; per slice it takes its 24 code bits and 8 sign|mantissa bytes from shared
+// memory, builds two values per 32-bit word with a few integer ops, and writes one coalesced
+// 16-byte store, escaped values with a placeholder exponent.  Then the threads walk the escape
+// list together, one entry each, check it against the codes and patch the value, so escape
+// work is proportional to the number of escapes rather than to the busiest lane.  Every offset
 // and size is checked before it is used, so a corrupt stream sets an error instead of steering
 // a read outside [0, total_bytes).
 #include "zc_common.cuh"
@@ -36,7 +38,7 @@ struct __align__(128) DecodeSmem {
   uint4 fixed[kFullFixedBytes / 16];
   uint4 esc[kMaxEscapeBytes / 16];
   uint64_t mbar;
-  unsigned scan[8];
+  unsigned escapes;  // code-7 count of the chunk, summed by the warps
   int ok;
   int e0;
   unsigned esc_bytes;
@@ -77,6 +79,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeParams p) {
       if (bad) set_error(p.status, bad);
       S.ok = !bad && c < p.N;
       S.e0 = e0;
+      S.escapes = 0;
       S.esc_bytes = static_cast<unsigned>(off1 - off0);
       if (S.ok) {
         const unsigned fbytes = static_cast<unsigned>(fixed_bytes(m));
@@ -107,21 +110,19 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeParams p) {
   const uint8_t* smp = codes + cbytes;
   const uint8_t* esc = reinterpret_cast<const uint8_t*>(S.esc);
   const uint32_t e0_field = static_cast<uint32_t>(e0) * (128u * 0x00010001u);  // e0 << 7 in both halves
+  uint16_t* dst = p.out + first;
 
-  uint32_t x[4][4];
-  unsigned cnt[4], msk[4];
+  // Every value as if in the window (an escape gets a placeholder exponent, patched below).
+  unsigned mine = 0;  // this thread's code-7 count
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     const unsigned g = 128 * q + tid, v0 = 8 * g;
-    cnt[q] = 0;
-    msk[q] = 0;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) x[q][i] = 0;
     if (!full && v0 >= m) continue;
     const unsigned b = 3 * g;
     const uint32_t* cw = reinterpret_cast<const uint32_t*>(codes + (b & ~3u));
     const uint32_t bits = __funnelshift_r(cw[0], cw[1], 8 * (b & 3));
     const uint2 sm = *reinterpret_cast<const uint2*>(smp + v0);
+    uint32_t x[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       // codes of values 2i, 2i+1 -> (c + e0) << 7 in the two halves
@@ -131,49 +132,40 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeParams p) {
       const uint32_t sw = i < 2 ? sm.x : sm.y;
       const unsigned lo = (2 * i) & 3;
       const uint32_t s2 = prmt(sw, 0u, lo | ((8u | lo) << 4) | ((lo + 1) << 8) | ((8u | (lo + 1)) << 12));
-      x[q][i] = (s2 & 0x807F807Fu) | (efield & 0x7F807F80u);
+      x[i] = (s2 & 0x807F807Fu) | (efield & 0x7F807F80u);
     }
-    // code 7 = all three bits set: one bit per value at positions 3j
-    uint32_t e = bits & (bits >> 1) & (bits >> 2) & 0x249249u;
-    if (!full && v0 + 8 > m) e &= (1u << (3 * (m - v0))) - 1u;  // padding codes are checked below
-    msk[q] = e;
-    cnt[q] = __popc(e);
-  }
-
-  unsigned base[4];
-  const unsigned k = chunk_ranks(cnt, base, S.scan);  // the escape count follows from the codes
-  bool corrupt = pad16(3ull * k) != S.esc_bytes;
-
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    unsigned mk = msk[q], r = base[q];
-    const unsigned v0 = 1024 * q + 8 * tid;
-    while (mk) {
-      const int j = (__ffs(mk) - 1) / 3;
-      mk &= mk - 1;
-      const unsigned pos = reinterpret_cast<const uint16_t*>(esc)[r];
-      const unsigned E = esc[2 * k + r];
-      if (pos != v0 + j || (E >= static_cast<unsigned>(e0) && E <= static_cast<unsigned>(e0) + 6)) corrupt = true;
-      const unsigned sh = 16 * (j & 1);
-      const uint32_t clear = ~(0xFFu << (sh + 7));
-      const uint32_t v = (pick4(x[q], j >> 1) & clear) | (E << (sh + 7));
-      const unsigned wi = j >> 1;
-      x[q][0] = wi == 0 ? v : x[q][0];
-      x[q][1] = wi == 1 ? v : x[q][1];
-      x[q][2] = wi == 2 ? v : x[q][2];
-      x[q][3] = wi == 3 ? v : x[q][3];
-      ++r;
-    }
-  }
-
-  uint16_t* dst = p.out + first;
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const unsigned v0 = 1024 * q + 8 * tid;
+    uint32_t e = bits & (bits >> 1) & (bits >> 2) & 0x249249u;  // code 7: bit 3j for value j
     if (full || v0 + 8 <= m) {
-      *reinterpret_cast<uint4*>(dst + v0) = make_uint4(x[q][0], x[q][1], x[q][2], x[q][3]);
-    } else if (v0 < m) {
-      for (unsigned j = 0; v0 + j < m; ++j) dst[v0 + j] = static_cast<uint16_t>(pick4(x[q], j >> 1) >> (16 * (j & 1)));
+      *reinterpret_cast<uint4*>(dst + v0) = make_uint4(x[0], x[1], x[2], x[3]);
+    } else {
+      e &= (1u << (3 * (m - v0))) - 1u;  // padding codes are checked below
+      for (unsigned j = 0; v0 + j < m; ++j) dst[v0 + j] = static_cast<uint16_t>(pick4(x, j >> 1) >> (16 * (j & 1)));
+    }
+    mine += __popc(e);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mine += __shfl_xor_sync(0xFFFFFFFFu, mine, o);
+  if (lane == 0) atomicAdd(&S.escapes, mine);
+  __syncthreads();  // every placeholder is written and the chunk's escape count is known
+
+  // Escapes: entry i of the list patches value pos[i].  Positions strictly increasing, below m,
+  // each holding code 7, with as many entries as code-7 values: the list names exactly the
+  // escaped values, so the stream is canonical.
+  const unsigned k = S.escapes;
+  bool corrupt = pad16(3ull * k) != S.esc_bytes;
+  if (!corrupt) {
+    const uint16_t* pos_list = reinterpret_cast<const uint16_t*>(esc);
+    for (unsigned i = tid; i < k; i += kThreads) {
+      const unsigned pos = pos_list[i], E = esc[2 * k + i];
+      const unsigned pb = 3 * pos;
+      const unsigned code = pos < m ? ((codes[pb >> 3] | (codes[(pb >> 3) + 1] << 8)) >> (pb & 7)) & 7u : 0u;
+      if (code != 7u || (i > 0 && pos <= pos_list[i - 1]) ||
+          (E >= static_cast<unsigned>(e0) && E <= static_cast<unsigned>(e0) + 6)) {
+        corrupt = true;
+        continue;
+      }
+      const unsigned sm = smp[pos];
+      dst[pos] = static_cast<uint16_t>(((sm & 0x80u) << 8) | (E << 7) | (sm & 0x7Fu));
     }
   }
 

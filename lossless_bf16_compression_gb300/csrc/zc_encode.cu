@@ -26,7 +26,8 @@
 namespace zc {
 namespace {
 
-constexpr int kCoders = 256;               // coding threads: 2 slices of 8 values each
+constexpr int kCoders = 256;               // coding threads
+constexpr int kSlices = kChunk / (8 * kCoders);  // slices of 8 values per coding thread
 constexpr int kThreads = kCoders + 32;     // + one warp (the scanner in CTA 0)
 constexpr int kCtasPerSm = 3;
 constexpr int kStages = 3;                 // input chunks in flight per CTA
@@ -62,7 +63,7 @@ struct __align__(128) EncodeSmem {
   unsigned q_size[kQueue];
   unsigned q_front, q_count;
   unsigned long long peek_state[kPeek], peek_chunk[kPeek];
-  unsigned scan[8];
+  __align__(16) unsigned scan[kCoders / 32 * kSlices / 2];
   unsigned esc_off;  // ring offset of the list being written
   int abort;         // written by thread 0 only, between the rank barrier and [E]
   int load_fail;     // a bounded wait for an input copy ran out
@@ -77,7 +78,7 @@ struct Ring {
   unsigned unread_off = 0;    // the oldest such list
 };
 
-__device__ __forceinline__ void bar_coders() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+__device__ __forceinline__ void bar_coders() { asm volatile("bar.sync 1, %0;" ::"n"(kCoders) : "memory"); }
 
 // Thread 0: start the bulk copy of chunk c into stage s (a ragged tail, < 16 bytes, by plain loads).
 __device__ void issue_load(EncodeSmem& S, int s, uint64_t c, const EncodeParams& p) {
@@ -291,18 +292,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) encode_kernel(EncodePara
       pending &= ~(1u << s);
       parity ^= 1u << s;
     }
-    const uint4 xq0 = S.xin[s][tid], xq1 = S.xin[s][256 + tid];
-    bar_coders();  // [B] stage s is free again
-    if (tid == 0) {
-      // The next ticket was taken a chunk ago, so its round trip is already over; the one
-      // after it is taken now and used a chunk later.
-      S.ticket[s] = next_ticket;
-      if (next_ticket < p.N) {
-        issue_load(S, s, next_ticket, p);
-        pending |= 1u << s;
-        next_ticket = atomicAdd(&p.ctrl->encode_ticket, 1u);
-      }
-    }
     if (warp == 0 && lane < kPeek) {  // read ahead the state of the oldest waiting lists
       peek_chunk = ~0ull;
       if (lane < S.q_count) {
@@ -318,13 +307,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) encode_kernel(EncodePara
     const unsigned smbytes = full ? kChunk : static_cast<unsigned>(pad16(m));
     uint8_t* fixed = p.out + R0 + c * static_cast<uint64_t>(kFullFixedBytes);
 
-    unsigned cnt[2], msk[2];
-    uint32_t words[2][4];
+    unsigned cnt[kSlices], msk[kSlices];
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      const uint4 xv = q ? xq1 : xq0;
+    for (int q = 0; q < kSlices; ++q) {
+      const uint4 xv = S.xin[s][kCoders * q + tid];
       uint32_t w[4] = {xv.x, xv.y, xv.z, xv.w};
-      const unsigned v0 = 2048 * q + 8 * tid;
+      const unsigned v0 = 8 * kCoders * q + 8 * tid;
       uint32_t c2[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) c2[i] = codes_x2(w[i], neg_e0x2);
@@ -339,16 +327,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) encode_kernel(EncodePara
       const uint2 smv = make_uint2(sign_mantissa_x4(w[0], w[1]), sign_mantissa_x4(w[2], w[3]));
       if (full || v0 < smbytes) *reinterpret_cast<uint2*>(fixed + cbytes + v0) = smv;
       const uint32_t bits = pack_codes8(c2);
-      const unsigned wbase = 3 * (256 * q + 32 * warp);  // this warp's 96 code bytes
+      const unsigned wbase = 3 * (kCoders * q + 32 * warp);  // this warp's 96 code bytes
       store_code_groups(fixed + wbase, bits, cbytes > wbase ? cbytes - wbase : 0);
       msk[q] = bits & (bits >> 1) & (bits >> 2) & 0x249249u;  // code 7: bit 3j for value j
       cnt[q] = __popc(msk[q]);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) words[q][i] = w[i];
     }
 
-    unsigned base[2];
-    const unsigned k = chunk_ranks_256(cnt, base, S.scan);
+    unsigned base[kSlices];
+    const unsigned k = chunk_ranks_bar1<kCoders>(cnt, base, S.scan);
     const unsigned esc_bytes = static_cast<unsigned>(pad16(3ull * k));
     if (warp == 0 && lane < kPeek) {
       S.peek_state[lane] = peek;
@@ -370,25 +356,28 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) encode_kernel(EncodePara
     }
     bar_coders();  // [E] the list has a place in the ring
     uint8_t* esc = reinterpret_cast<uint8_t*>(S.ring) + S.esc_off;
-    if (!S.abort) {
-      if (tid == kCoders - 1)
-        for (unsigned b = 3 * k; b < esc_bytes; ++b) esc[b] = 0;
+    const bool go = !S.abort;
+    if (go) {  // positions, in rank order
 #pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        unsigned r = base[q];
-        unsigned mk = msk[q];
+      for (int q = 0; q < kSlices; ++q) {
+        unsigned r = base[q], mk = msk[q];
+        const unsigned v0 = 8 * kCoders * q + 8 * tid;
         while (mk) {
-          const int j = (__ffs(mk) - 1) / 3;
+          const unsigned j = ((__ffs(mk) - 1) * 11u) >> 5;  // bit 3j -> j, exact for j < 8
           mk &= mk - 1;
-          const unsigned E = (pick4(words[q], j >> 1) >> (16 * (j & 1) + 7)) & 0xFFu;
-          *reinterpret_cast<uint16_t*>(esc + 2 * r) = static_cast<uint16_t>(2048 * q + 8 * tid + j);
-          esc[2 * k + r] = static_cast<uint8_t>(E);
-          ++r;
+          reinterpret_cast<uint16_t*>(esc)[r++] = static_cast<uint16_t>(v0 + j);
         }
       }
+    }
+    bar_coders();  // [F] every position is in place
+    if (go) {  // exponents, one list entry per thread, read back from the staged input
+      const uint16_t* xin16 = reinterpret_cast<const uint16_t*>(S.xin[s]);
+      for (unsigned i = tid; i < k; i += kCoders)
+        esc[2 * k + i] = static_cast<uint8_t>(xin16[reinterpret_cast<const uint16_t*>(esc)[i]] >> 7);
+      if (tid < esc_bytes - 3 * k) esc[3 * k + tid] = 0;  // zero padding, < 16 bytes
       fence_proxy_async_smem();
     }
-    bar_coders();  // [C] the list is complete in the ring
+    bar_coders();  // [C] the list is complete in the ring; stage s is free again
     if (S.abort) break;
     if (tid == 0) {
       const unsigned qi = (S.q_front + S.q_count) % kQueue;
@@ -399,6 +388,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) encode_kernel(EncodePara
       if (esc_bytes) {
         R.head = S.esc_off + esc_bytes;
         R.used += esc_bytes;
+      }
+      // The next ticket was taken a chunk ago, so its round trip is already over; the one
+      // after it is taken now and used a chunk later.
+      S.ticket[s] = next_ticket;
+      if (next_ticket < p.N) {
+        issue_load(S, s, next_ticket, p);
+        pending |= 1u << s;
+        next_ticket = atomicAdd(&p.ctrl->encode_ticket, 1u);
       }
     }
   }
