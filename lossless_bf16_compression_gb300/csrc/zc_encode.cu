@@ -7,20 +7,21 @@
 // kernels use a communication-aware layout, aligned global/shared memory access and pipeline
 // data movement with compression compute (second technique).
 //
-// GB300 design.  A persistent grid, three CTAs per SM, each with eight coding warps.  Chunks
-// are handed out by an atomic ticket (ticket order = chunk order).  Inputs (8 KiB per chunk)
-// arrive by bulk async copies (TMA engine, mbarrier completion) three stages ahead; a thread
-// holds 2 slices of 8 values and codes two values per 32-bit word with packed 16-bit
-// arithmetic.  The fixed part of a chunk has a place that follows from n, so it goes straight
-// from registers to HBM: 8-byte stores of sign|mantissa bytes and, per warp, 24 coalesced
-// 32-bit words of codes assembled with two shuffles.  Only the escape list waits for the
-// device-wide scan: each chunk publishes its list size in a per-chunk state word as soon as
-// its escape count is known, and a ninth warp in CTA 0 (the scanner) walks the state words in
-// order, 512 per round trip, turning every run of published sizes into inclusive offsets with
-// a warp scan (a chained scan with one scanner, after Merrill & Garland's single-pass scan).
-// Escape lists wait in a ring buffer in shared memory, where a waiting list costs only its own
-// bytes, so coding never waits for the scan; thread 0 writes resolved lists out with bulk
-// async stores and blocks only when the ring is full.  Every wait is bounded.
+// GB300 design.  A persistent grid, three CTAs per SM.  Block 0 is the scanner; every other
+// block has eight coding warps and one retiring warp.  Chunks are handed out by an atomic
+// ticket (ticket order = chunk order).  Inputs (8 KiB per chunk) arrive by bulk async copies
+// (TMA engine, mbarrier completion) three stages ahead; a coding thread holds 2 slices of 8
+// values and codes two values per 32-bit word with packed 16-bit arithmetic.  The fixed part of
+// a chunk has a place that follows from n, so it goes straight from registers to HBM: 8-byte
+// stores of sign|mantissa bytes and, per warp, 24 coalesced 32-bit words of codes assembled
+// with two shuffles.  Only the escape list waits for the device-wide scan: each chunk publishes
+// its list size in a per-chunk state word as soon as its escape count is known, and the
+// scanner walks the state words in order, 512 per round trip, turning every run of published
+// sizes into inclusive offsets with a warp scan (a chained scan with one scanner, after Merrill
+// & Garland's single-pass scan).  Escape lists wait in a ring buffer in shared memory, where a
+// waiting list costs only its own bytes; the retiring warp polls up to 32 waiting lists per
+// round trip and writes resolved ones out with bulk async stores, so coding never waits for
+// the scan unless the ring is full.  Every wait is bounded.
 #include "zc_common.cuh"
 
 namespace zc {
@@ -28,13 +29,12 @@ namespace {
 
 constexpr int kCoders = 256;               // coding threads
 constexpr int kSlices = kChunk / (8 * kCoders);  // slices of 8 values per coding thread
-constexpr int kThreads = kCoders + 32;     // + one warp (the scanner in CTA 0)
+constexpr int kThreads = kCoders + 32;     // + the retiring warp (the scanner in block 0)
 constexpr int kCtasPerSm = 3;
 constexpr int kStages = 3;                 // input chunks in flight per CTA
 constexpr unsigned kInBytes = 2 * kChunk;
 constexpr unsigned kRingBytes = 32 * 1024; // escape-list ring per CTA
-constexpr int kQueue = 64;                 // escape lists waiting, at most
-constexpr int kPeek = 4;                   // waiting lists whose state is read ahead per chunk
+constexpr unsigned kQueue = 64;            // escape lists waiting, at most
 constexpr unsigned kWaitLimit = 1u << 22;  // mbarrier polls before giving up
 constexpr int kScanPerLane = 16;           // state words per lane per scanner round trip
 
@@ -57,30 +57,25 @@ struct __align__(128) EncodeSmem {
   uint4 ring[kRingBytes / 16];
   uint64_t mbar[kStages];
   unsigned ticket[kStages];
-  // escape lists in the ring, oldest first (written by thread 0)
+  // Escape lists in the ring, a single-producer (coding thread 0) single-consumer (retiring
+  // warp) queue.  Entry i (mod kQueue): chunk, ring offset, size, bytes skipped before it.
   unsigned long long q_chunk[kQueue];
-  unsigned q_off[kQueue];
-  unsigned q_size[kQueue];
-  unsigned q_front, q_count;
-  unsigned long long peek_state[kPeek], peek_chunk[kPeek];
+  unsigned q_off[kQueue], q_size[kQueue], q_gap[kQueue];
+  volatile unsigned q_pushed;   // entries made (producer)
+  volatile unsigned q_retired;  // entries written out and read back from the ring (consumer)
+  volatile unsigned freed;      // ring bytes given back, gaps included (consumer)
+  volatile int coders_done;     // no more entries will come
   __align__(16) unsigned scan[kCoders / 32 * kSlices / 2];
   unsigned esc_off;  // ring offset of the list being written
-  int abort;         // written by thread 0 only, between the rank barrier and [E]
+  int abort;         // written by coding thread 0 only, between the rank barrier and [E]
   int load_fail;     // a bounded wait for an input copy ran out
   int e0;
 };
 
-// Thread 0's ring bookkeeping: lists occupy [tail, head), wrapping at the end of the ring.
-struct Ring {
-  unsigned head = 0;          // where the newest list ends
-  unsigned used = 0;          // bytes held by waiting lists and by lists still being read out
-  unsigned unread_bytes = 0;  // bytes of written-out lists whose bulk store may still be reading
-  unsigned unread_off = 0;    // the oldest such list
-};
-
 __device__ __forceinline__ void bar_coders() { asm volatile("bar.sync 1, %0;" ::"n"(kCoders) : "memory"); }
 
-// Thread 0: start the bulk copy of chunk c into stage s (a ragged tail, < 16 bytes, by plain loads).
+// Coding thread 0: start the bulk copy of chunk c into stage s (a ragged tail, < 16 bytes, by
+// plain loads).
 __device__ void issue_load(EncodeSmem& S, int s, uint64_t c, const EncodeParams& p) {
   const uint64_t first = c * kChunk;
   const unsigned m = chunk_values(p.n, c);
@@ -96,8 +91,8 @@ __device__ void issue_load(EncodeSmem& S, int s, uint64_t c, const EncodeParams&
   }
 }
 
-// The scanner (warp 8 of CTA 0): resolve chunks in order.  Each round reads the next 512 state
-// words; the published sizes before the first unpublished one become inclusive offsets.
+// The scanner (block 0): resolve chunks in order.  Each round reads the next 512 state words;
+// the published sizes before the first unpublished one become inclusive offsets.
 __device__ __noinline__ void scanner(unsigned long long* flags, uint64_t N, int* status, unsigned spin_limit) {
   const unsigned lane = threadIdx.x & 31;
   uint64_t frontier = 0;
@@ -153,45 +148,101 @@ __device__ __noinline__ void scanner(unsigned long long* flags, uint64_t N, int*
   }
 }
 
-// Thread 0: write out the oldest waiting escape list, whose state word reads `f` (resolved),
-// and fill in its table entry (and the header fields that belong to the first and last chunk).
-__device__ void retire_front(EncodeSmem& S, Ring& R, const EncodeParams& p, int e0, unsigned long long f) {
-  const unsigned i = S.q_front;
-  const unsigned long long c = S.q_chunk[i];
-  const unsigned size = S.q_size[i];
-  const unsigned long long off = escape_base(p.n) + (f & kFlagValueMask) - size;
-  if (size) {
-    bulk_store(p.out + off, reinterpret_cast<const uint8_t*>(S.ring) + S.q_off[i], size);
-    bulk_commit();
-    if (R.unread_bytes == 0) R.unread_off = S.q_off[i];
-    R.unread_bytes += size;
-  }
+// The retiring warp: write escape lists out in chunk order as the scanner resolves them, fill in
+// the offset table (and the header fields that belong to the first and last chunk), and give
+// ring space back once each bulk store has read its bytes.
+__device__ void retirer(EncodeSmem& S, const EncodeParams& p) {
+  const unsigned lane = threadIdx.x & 31;
+  const uint64_t E0 = escape_base(p.n);
   unsigned long long* table = reinterpret_cast<unsigned long long*>(p.out + kHeaderBytes);
-  table[c] = off;
-  if (c == 0) {
-    unsigned long long* hdr = reinterpret_cast<unsigned long long*>(p.out);
-    hdr[0] = kMagicWord | (static_cast<unsigned long long>(e0) << 56);
-    hdr[1] = p.n;
-    hdr[2] = p.N;
-    if (kHeaderBytes + 8 * (p.N + 1) < records_base(p.n)) table[p.N + 1] = 0;  // zero pad
+  unsigned retired = 0, freed = 0, spins = 0, backoff = 64;
+  for (;;) {
+    const unsigned pushed = S.q_pushed;
+    const unsigned avail = pushed - retired;
+    if (avail == 0) {
+      if (S.coders_done) {  // the producer bumps q_pushed before it sets coders_done
+        __threadfence_block();
+        if (S.q_pushed == retired) break;
+        continue;
+      }
+      if (++spins > p.spin_limit || read_status(p.status) != 0) break;
+      __nanosleep(backoff);
+      backoff = backoff < 512 ? backoff * 2 : 512;
+      continue;
+    }
+    __threadfence_block();  // the entries below were written before q_pushed was bumped
+    const unsigned i = (retired + lane) % kQueue;
+    const bool mine = lane < avail;
+    const unsigned long long f = mine ? ld_relaxed_u64(&p.flags[S.q_chunk[i]]) : 0ull;
+    const unsigned resolved = __ballot_sync(0xFFFFFFFFu, mine && (f >> 62) == 2);
+    const unsigned run = __ffs(~resolved) ? __ffs(~resolved) - 1 : 32;  // leading resolved entries
+    if (run == 0) {
+      int bad = lane == 0 ? read_status(p.status) : 0;
+      bad = __shfl_sync(0xFFFFFFFFu, bad, 0);
+      if (bad != 0 || ++spins > p.spin_limit) break;
+      __nanosleep(backoff);
+      backoff = backoff < 512 ? backoff * 2 : 512;
+      continue;
+    }
+    spins = 0;
+    backoff = 64;
+    unsigned give_back = 0;
+    if (lane < run) {
+      const unsigned long long c = S.q_chunk[i];
+      const unsigned size = S.q_size[i];
+      const unsigned long long off = E0 + (f & kFlagValueMask) - size;
+      if (size) {
+        bulk_store(p.out + off, reinterpret_cast<const uint8_t*>(S.ring) + S.q_off[i], size);
+        bulk_commit();
+      }
+      table[c] = off;
+      if (c == 0) {
+        unsigned long long* hdr = reinterpret_cast<unsigned long long*>(p.out);
+        hdr[0] = kMagicWord | (static_cast<unsigned long long>(S.e0) << 56);
+        hdr[1] = p.n;
+        hdr[2] = p.N;
+        if (kHeaderBytes + 8 * (p.N + 1) < records_base(p.n)) table[p.N + 1] = 0;  // zero pad
+      }
+      if (c == p.N - 1) {
+        const unsigned long long total = off + size;
+        table[p.N] = total;
+        reinterpret_cast<unsigned long long*>(p.out)[3] = total;
+        p.ctrl->total = total;
+        if (p.out_bytes) *p.out_bytes = total;
+      }
+      give_back = S.q_gap[i] + size;
+      bulk_wait_read<0>();  // this lane's stores have read their bytes
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) give_back += __shfl_xor_sync(0xFFFFFFFFu, give_back, o);
+    retired += run;
+    freed += give_back;
+    if (lane == 0) {
+      S.freed = freed;
+      S.q_retired = retired;
+    }
+    __syncwarp();
   }
-  if (c == p.N - 1) {
-    const unsigned long long total = off + size;
-    table[p.N] = total;
-    reinterpret_cast<unsigned long long*>(p.out)[3] = total;
-    p.ctrl->total = total;
-    if (p.out_bytes) *p.out_bytes = total;
-  }
-  S.q_front = (S.q_front + 1) % kQueue;
-  --S.q_count;
+  bulk_wait_all<0>();
 }
 
-// Thread 0: wait (bounded) until the oldest waiting list is resolved, then write it out.
-__device__ bool retire_front_blocking(EncodeSmem& S, Ring& R, const EncodeParams& p, int e0) {
-  const unsigned long long* flag = &p.flags[S.q_chunk[S.q_front]];
-  unsigned long long f = ld_relaxed_u64(flag);
+// Coding thread 0's side of the ring: room for `need` bytes (a multiple of 16, at most
+// kMaxEscapeBytes) and a free queue slot.  Waits (bounded) for the retiring warp when the ring
+// is full.  False after a failed wait.
+struct Producer {
+  unsigned pushed = 0;  // entries made
+  unsigned made = 0;    // ring bytes handed out, gaps included
+  unsigned head = 0;    // ring offset where the next list may start
+};
+
+__device__ bool ring_alloc(EncodeSmem& S, Producer& P, const EncodeParams& p, unsigned need, unsigned* where,
+                           unsigned* gap) {
+  // head is the ring offset of `made`; a list that ended exactly at the end leaves it at
+  // kRingBytes, which is offset 0.  With head below kRingBytes, where + need <= kRingBytes.
+  if (P.head >= kRingBytes) P.head = 0;
+  const unsigned skip = (need && P.head + need > kRingBytes) ? kRingBytes - P.head : 0u;
   unsigned spins = 0, backoff = 64;
-  while ((f >> 62) != 2) {
+  while (P.pushed - S.q_retired >= kQueue || P.made + skip + need - S.freed > kRingBytes) {
     if (read_status(p.status) != 0) return false;
     if (++spins > p.spin_limit) {
       set_error(p.status, ZC_ERR_TIMEOUT);
@@ -199,70 +250,41 @@ __device__ bool retire_front_blocking(EncodeSmem& S, Ring& R, const EncodeParams
     }
     __nanosleep(backoff);
     backoff = backoff < 512 ? backoff * 2 : 512;
-    f = ld_relaxed_u64(flag);
   }
-  retire_front(S, R, p, e0, f);
+  *gap = skip;
+  *where = skip ? 0u : P.head;
+  P.made += skip + need;
+  P.head = *where + need;
   return true;
-}
-
-// Thread 0: room for `need` bytes (a multiple of 16, at most kMaxEscapeBytes) in the ring and
-// a free queue slot, writing out resolved lists as needed.  False after a failed wait.
-__device__ bool ring_alloc(EncodeSmem& S, Ring& R, const EncodeParams& p, int e0, unsigned need, unsigned* where) {
-  for (;;) {
-    if (S.q_count < kQueue) {
-      if (need == 0) {
-        *where = R.head;
-        return true;
-      }
-      if (R.used == 0) {  // nothing held: start over at the beginning
-        R.head = 0;
-        *where = 0;
-        return true;
-      }
-      const unsigned tail = R.unread_bytes ? R.unread_off : (S.q_count ? S.q_off[S.q_front] : R.head);
-      if (R.head > tail) {  // in use: [tail, head)
-        if (kRingBytes - R.head >= need) {
-          *where = R.head;
-          return true;
-        }
-        if (tail >= need) {
-          *where = 0;
-          return true;
-        }
-      } else if (tail - R.head >= need) {  // wrapped: in use [tail, end) and [0, head)
-        *where = R.head;
-        return true;
-      }
-    }
-    if (R.unread_bytes) {  // let the bulk stores finish reading; their space is then free
-      bulk_wait_read<0>();
-      R.used -= R.unread_bytes;
-      R.unread_bytes = 0;
-      continue;
-    }
-    if (S.q_count == 0 || !retire_front_blocking(S, R, p, e0)) return false;
-  }
 }
 
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) encode_kernel(EncodeParams p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   EncodeSmem& S = *reinterpret_cast<EncodeSmem*>(smem_raw);
-  const unsigned tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (tid >= kCoders) {  // the ninth warp: CTA 0 runs the scanner, the others leave
-    if (blockIdx.x == 0) scanner(p.flags, p.N, p.status, p.spin_limit);
+  const unsigned tid = threadIdx.x, warp = tid >> 5;
+  if (blockIdx.x == 0) {  // block 0: the scanner
+    if (warp == kCoders / 32) scanner(p.flags, p.N, p.status, p.spin_limit);
     return;
   }
-  Ring R;                                // thread 0 only
-  unsigned pending = 0, parity = 0;      // thread 0: loads in flight per stage, next wait parity
-  unsigned next_ticket = 0;              // thread 0: the ticket for the next free stage
-  unsigned long long peek = 0, peek_chunk = ~0ull;  // lanes 0..kPeek-1 of warp 0
-
   if (tid == 0) {
+    S.q_pushed = 0;
+    S.q_retired = 0;
+    S.freed = 0;
+    S.coders_done = 0;
     S.abort = 0;
     S.load_fail = 0;
-    S.q_front = 0;
-    S.q_count = 0;
     S.e0 = p.base >= 0 ? p.base : __ldcg(&p.ctrl->e0);
+  }
+  __syncthreads();
+  if (warp == kCoders / 32) {  // the retiring warp
+    retirer(S, p);
+    return;
+  }
+
+  Producer P;                            // coding thread 0 only
+  unsigned pending = 0, parity = 0;      // coding thread 0: loads in flight per stage, next parity
+  unsigned next_ticket = 0;              // coding thread 0: the ticket for the next free stage
+  if (tid == 0) {
     for (int s = 0; s < kStages; ++s) mbar_init(&S.mbar[s], 1);
     fence_mbar_init();
     for (int s = 0; s < kStages; ++s) {
@@ -291,13 +313,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) encode_kernel(EncodePara
     if (tid == 0) {
       pending &= ~(1u << s);
       parity ^= 1u << s;
-    }
-    if (warp == 0 && lane < kPeek) {  // read ahead the state of the oldest waiting lists
-      peek_chunk = ~0ull;
-      if (lane < S.q_count) {
-        peek_chunk = S.q_chunk[(S.q_front + lane) % kQueue];
-        peek = ld_relaxed_u64(&p.flags[peek_chunk]);
-      }
     }
 
     // ---- code the chunk: the fixed part goes straight to its place in the stream
@@ -336,59 +351,45 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) encode_kernel(EncodePara
     unsigned base[kSlices];
     const unsigned k = chunk_ranks_bar1<kCoders>(cnt, base, S.scan);
     const unsigned esc_bytes = static_cast<unsigned>(pad16(3ull * k));
-    if (warp == 0 && lane < kPeek) {
-      S.peek_state[lane] = peek;
-      S.peek_chunk[lane] = peek_chunk;
-    }
-    __syncwarp();
+    unsigned gap = 0;
     if (tid == 0) {
       if (c != p.stall_chunk) st_relaxed_u64(&p.flags[c], kFlagAggregate | esc_bytes);  // publish early
-      for (int i = 0; i < kPeek && S.q_count > 0; ++i) {  // write out lists already resolved
-        if (S.peek_chunk[i] != S.q_chunk[S.q_front] || (S.peek_state[i] >> 62) != 2) break;
-        retire_front(S, R, p, e0, S.peek_state[i]);
-      }
       unsigned where = 0;
-      if (S.load_fail || c == p.stall_chunk || !ring_alloc(S, R, p, e0, esc_bytes, &where)) {
+      if (S.load_fail || c == p.stall_chunk || !ring_alloc(S, P, p, esc_bytes, &where, &gap)) {
         S.abort = 1;  // (the stall test hook: this list is never resolved)
         where = 0;
       }
       S.esc_off = where;
     }
     bar_coders();  // [E] the list has a place in the ring
-    uint8_t* esc = reinterpret_cast<uint8_t*>(S.ring) + S.esc_off;
-    const bool go = !S.abort;
-    if (go) {  // positions, in rank order
+    if (!S.abort) {  // positions and exponents, in rank order
+      uint8_t* esc = reinterpret_cast<uint8_t*>(S.ring) + S.esc_off;
+      const uint16_t* xin16 = reinterpret_cast<const uint16_t*>(S.xin[s]);
 #pragma unroll
       for (int q = 0; q < kSlices; ++q) {
         unsigned r = base[q], mk = msk[q];
         const unsigned v0 = 8 * kCoders * q + 8 * tid;
         while (mk) {
-          const unsigned j = ((__ffs(mk) - 1) * 11u) >> 5;  // bit 3j -> j, exact for j < 8
+          const unsigned pos = v0 + (((__ffs(mk) - 1) * 11u) >> 5);  // bit 3j -> j, exact for j < 8
           mk &= mk - 1;
-          reinterpret_cast<uint16_t*>(esc)[r++] = static_cast<uint16_t>(v0 + j);
+          reinterpret_cast<uint16_t*>(esc)[r] = static_cast<uint16_t>(pos);
+          esc[2 * k + r] = static_cast<uint8_t>(xin16[pos] >> 7);
+          ++r;
         }
       }
-    }
-    bar_coders();  // [F] every position is in place
-    if (go) {  // exponents, one list entry per thread, read back from the staged input
-      const uint16_t* xin16 = reinterpret_cast<const uint16_t*>(S.xin[s]);
-      for (unsigned i = tid; i < k; i += kCoders)
-        esc[2 * k + i] = static_cast<uint8_t>(xin16[reinterpret_cast<const uint16_t*>(esc)[i]] >> 7);
       if (tid < esc_bytes - 3 * k) esc[3 * k + tid] = 0;  // zero padding, < 16 bytes
       fence_proxy_async_smem();
     }
     bar_coders();  // [C] the list is complete in the ring; stage s is free again
     if (S.abort) break;
     if (tid == 0) {
-      const unsigned qi = (S.q_front + S.q_count) % kQueue;
+      const unsigned qi = P.pushed % kQueue;
       S.q_chunk[qi] = c;
       S.q_off[qi] = S.esc_off;
       S.q_size[qi] = esc_bytes;
-      ++S.q_count;
-      if (esc_bytes) {
-        R.head = S.esc_off + esc_bytes;
-        R.used += esc_bytes;
-      }
+      S.q_gap[qi] = gap;
+      __threadfence_block();
+      S.q_pushed = ++P.pushed;
       // The next ticket was taken a chunk ago, so its round trip is already over; the one
       // after it is taken now and used a chunk later.
       S.ticket[s] = next_ticket;
@@ -401,11 +402,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) encode_kernel(EncodePara
   }
 
   if (tid == 0) {
-    if (!S.abort) {
-      while (S.q_count > 0)
-        if (!retire_front_blocking(S, R, p, e0)) break;
-    }
-    bulk_wait_all<0>();
+    __threadfence_block();
+    S.coders_done = 1;  // the retiring warp drains the queue and leaves
     for (int s = 0; s < kStages; ++s)  // never leave a copy in flight
       if (pending & (1u << s)) mbar_wait(&S.mbar[s], (parity >> s) & 1u, kWaitLimit);
   }
@@ -457,7 +455,8 @@ cudaError_t launch_encode(const uint16_t* in, uint64_t n, int base, uint8_t* out
   err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, encode_kernel, kThreads, smem);
   if (err != cudaSuccess) return err;
   uint64_t grid = static_cast<uint64_t>(per_sm > 0 ? per_sm : 1) * dev.sm_count;
-  if (grid > p.N) grid = p.N;
+  if (grid > p.N + 1) grid = p.N + 1;  // block 0 scans, the others code
+  if (grid < 2) grid = 2;
   timing_begin(ZC_KERNEL_ENCODE, stream);
   encode_kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(p);
   timing_end(stream);
