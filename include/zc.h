@@ -130,6 +130,30 @@ int zc_timing_enable(int enable);
  * failure).  Records beyond `max` are dropped too. */
 int zc_timing_collect(int* kernel_ids, float* ms, int max);
 
+/* ------------------------------------------------------------------ compress without allocation */
+
+/* Largest n zc_compress_static_scratch accepts: its workspace must fit a fixed 2 MiB array. */
+#define ZC_STATIC_SCRATCH_MAX_N ((size_t)1065222144)
+
+/* zc_compress for callers that cannot allocate device memory, such as a communication layer
+ * whose send buffers are registered once at exactly the worst-case stream size and that may
+ * not call cudaMalloc on its progress path.  The paper has no counterpart: it is an interface
+ * for such callers.
+ * Arguments, stream and results are those of zc_compress, except:
+ *   - `out` needs only zc_max_stream_bytes(n) bytes: the call's workspace lives in a
+ *     file-scope 2 MiB device array of the library instead of the tail of `out`.  That array
+ *     exists on every GPU that loads the library until the process exits.
+ *   - n > ZC_STATIC_SCRATCH_MAX_N returns ZC_ERR_INVALID_ARG.
+ *   - The call allocates nothing (no cudaMalloc, no cudaFree, no allocating library call).
+ *   - All calls on a device share the array; calls whose work overlaps on the GPU (for
+ *     example on two streams running at the same time) corrupt each other, so order them
+ *     (one stream, or events).  Each call clears the part of the array that must start at
+ *     zero before its kernels run.
+ *   - The first call on a device looks up the array's device address (once per device, with
+ *     that device current); make that first call before any stream capture. */
+int zc_compress_static_scratch(const void* in, size_t n, int base_or_auto, void* out, size_t* out_bytes,
+                               cudaStream_t stream);
+
 /* ------------------------------------------------------------------ test hook */
 
 /* zc_compress with a planted stall, for testing the bounded waits: chunk `stalled_chunk` never

@@ -21,6 +21,7 @@ ZC_ERR_CORRUPT = 4
 ZC_ERR_SIZE_MISMATCH = 5
 ZC_ERR_TIMEOUT = 6
 ZC_BASE_AUTO = -1
+ZC_STATIC_SCRATCH_MAX_N = 1065222144
 ZC_CHUNK_VALUES = 4096
 ZC_KERNEL_STATS = 1
 ZC_KERNEL_ENCODE = 2
@@ -46,6 +47,8 @@ _SIG = {
     "zc_status": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int]),
     "zc_timing_enable": (ctypes.c_int, [ctypes.c_int]),
     "zc_timing_collect": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]),
+    "zc_compress_static_scratch": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p,
+                                                  ctypes.c_void_p, ctypes.c_void_p]),
     "zc_compress_stall_test": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int,
                                               ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                               ctypes.c_size_t, ctypes.c_uint]),
@@ -117,6 +120,11 @@ def zc_timing_collect(max_records: int = 4096) -> list[tuple[int, float]]:
     if k < 0:
         raise ZcError(-k, "zc_timing_collect")
     return [(ids[i], ms[i]) for i in range(k)]
+
+
+def zc_compress_static_scratch(in_ptr: int, n: int, base_or_auto: int, out_ptr: int, out_bytes_ptr: int,
+                               stream: int) -> int:
+    return int(lib().zc_compress_static_scratch(in_ptr, n, base_or_auto, out_ptr, out_bytes_ptr, stream))
 
 
 def zc_compress_stall_test(in_ptr: int, n: int, base_or_auto: int, out_ptr: int, out_bytes_ptr: int,

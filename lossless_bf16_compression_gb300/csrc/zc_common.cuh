@@ -29,8 +29,8 @@ constexpr int kE0Max = 249;
 constexpr unsigned long long kMagicWord =          // bytes 0..6 of the header: "ZCB1", v2, 12
     0x5Aull | (0x43ull << 8) | (0x42ull << 16) | (0x31ull << 24) | (2ull << 32) | (12ull << 48);
 
-__host__ __device__ inline uint64_t pad16(uint64_t v) { return (v + 15u) & ~uint64_t(15); }
-__host__ __device__ inline uint64_t num_chunks(uint64_t n) { return (n + kChunk - 1) / kChunk; }
+__host__ __device__ constexpr uint64_t pad16(uint64_t v) { return (v + 15u) & ~uint64_t(15); }
+__host__ __device__ constexpr uint64_t num_chunks(uint64_t n) { return (n + kChunk - 1) / kChunk; }
 // Values in chunk c of an n-value tensor (c < num_chunks(n)).
 __host__ __device__ inline unsigned chunk_values(uint64_t n, uint64_t c) {
   const uint64_t left = n - c * kChunk;
@@ -80,7 +80,7 @@ struct StatsPartial {
 __host__ __device__ inline uint64_t workspace_offset(uint64_t n) {
   return (max_stream_bytes(n) + 255) & ~uint64_t(255);
 }
-__host__ __device__ inline uint64_t workspace_bytes(uint64_t n) {
+__host__ __device__ constexpr uint64_t workspace_bytes(uint64_t n) {
   return kWsControlBytes + kWsPartialsBytes + 8 * num_chunks(n);
 }
 
@@ -376,5 +376,10 @@ cudaError_t launch_encode(const uint16_t* in, uint64_t n, int base, uint8_t* out
                           uint64_t stall_chunk, unsigned spin_limit);
 cudaError_t launch_decode(const uint8_t* in, uint16_t* out, uint64_t n, const DeviceInfo& dev,
                           cudaStream_t stream);
+// The same statistics and encode launches with the workspace at `ws` (workspace_bytes(n) bytes)
+// instead of the tail of `out`.
+cudaError_t launch_stats_ws(const uint16_t* in, uint64_t n, uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream);
+cudaError_t launch_encode_ws(const uint16_t* in, uint64_t n, int base, uint8_t* out, unsigned long long* out_bytes,
+                             uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream);
 
 }  // namespace zc

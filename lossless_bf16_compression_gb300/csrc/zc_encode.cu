@@ -463,4 +463,39 @@ cudaError_t launch_encode(const uint16_t* in, uint64_t n, int base, uint8_t* out
   return cudaGetLastError();
 }
 
+// Same launch with the workspace at `ws` instead of the tail of `out`.
+cudaError_t launch_encode_ws(const uint16_t* in, uint64_t n, int base, uint8_t* out, unsigned long long* out_bytes,
+                             uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream) {
+  Control* ctrl = reinterpret_cast<Control*>(ws);
+  if (n == 0) {
+    empty_stream_kernel<<<1, 1, 0, stream>>>(out, base, ctrl, out_bytes);
+    return cudaGetLastError();
+  }
+  EncodeParams p;
+  p.in = in;
+  p.n = n;
+  p.N = num_chunks(n);
+  p.out = out;
+  p.ctrl = ctrl;
+  p.flags = reinterpret_cast<unsigned long long*>(ws + kWsControlBytes + kWsPartialsBytes);
+  p.out_bytes = out_bytes;
+  p.base = base;
+  p.status = dev.status;
+  p.stall_chunk = ~uint64_t(0);
+  p.spin_limit = 1u << 20;
+  const int smem = static_cast<int>(sizeof(EncodeSmem));
+  cudaError_t err = cudaFuncSetAttribute(encode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (err != cudaSuccess) return err;
+  int per_sm = 0;
+  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, encode_kernel, kThreads, smem);
+  if (err != cudaSuccess) return err;
+  uint64_t grid = static_cast<uint64_t>(per_sm > 0 ? per_sm : 1) * dev.sm_count;
+  if (grid > p.N + 1) grid = p.N + 1;  // block 0 scans, the others code
+  if (grid < 2) grid = 2;
+  timing_begin(ZC_KERNEL_ENCODE, stream);
+  encode_kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(p);
+  timing_end(stream);
+  return cudaGetLastError();
+}
+
 }  // namespace zc

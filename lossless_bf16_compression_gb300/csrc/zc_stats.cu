@@ -347,4 +347,27 @@ cudaError_t launch_stats(const uint16_t* in, uint64_t n, uint8_t* out, const Dev
   return cudaGetLastError();
 }
 
+// Same launch with the workspace at `ws` instead of the tail of `out`.
+cudaError_t launch_stats_ws(const uint16_t* in, uint64_t n, uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream) {
+  StatsParams p;
+  p.in = reinterpret_cast<const uint4*>(in);
+  p.n = n;
+  p.ctrl = reinterpret_cast<Control*>(ws);
+  p.partials = reinterpret_cast<StatsPartial*>(ws + kWsControlBytes);
+  p.status = dev.status;
+  const uint64_t nv = n >> 3;
+  const uint64_t blocks_needed = (nv + kVecPerWarpBlock * kWarps - 1) / (kVecPerWarpBlock * kWarps);
+  int per_sm = 0;
+  cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, stats_kernel, kThreads, 0);
+  if (err != cudaSuccess) return err;
+  uint64_t grid = static_cast<uint64_t>(per_sm > 0 ? per_sm : 1) * dev.sm_count;
+  if (grid > blocks_needed) grid = blocks_needed;
+  if (grid < 1) grid = 1;
+  if (grid > kStatsMaxCtas) grid = kStatsMaxCtas;
+  timing_begin(ZC_KERNEL_STATS, stream);
+  stats_kernel<<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(p);
+  timing_end(stream);
+  return cudaGetLastError();
+}
+
 }  // namespace zc
