@@ -1,5 +1,5 @@
 // zc_encode.cu -- chunked encoder: 3-bit exponent codes, sign|mantissa byte plane, escape
-// compaction, and a single-pass device-wide scan that places every chunk record in one
+// compaction, and a single-pass device-wide scan that places every escape list in one
 // contiguous stream behind a chunk-offset table.
 //
 // Method: ZipCCL (SIGCOMM scribe notes), "Key idea and contribution": in-window exponents are
@@ -16,11 +16,11 @@
 // stores of sign|mantissa bytes and, per warp, 24 coalesced 32-bit words of codes assembled
 // with two shuffles.  Only the escape list waits for the device-wide scan: each chunk publishes
 // its list size in a per-chunk state word as soon as its escape count is known, and the
-// scanner walks the state words in order, 512 per round trip, turning every run of published
-// sizes into inclusive offsets with a warp scan (a chained scan with one scanner, after Merrill
-// & Garland's single-pass scan).  Escape lists wait in a ring buffer in shared memory, where a
-// waiting list costs only its own bytes; the retiring warp polls up to 32 waiting lists per
-// round trip and writes resolved ones out with bulk async stores, so coding never waits for
+// scanner's eight warps walk the state words in order, 2048 per round trip, turning every run
+// of published sizes into inclusive offsets (a chained scan with one scanning block, after
+// Merrill & Garland's single-pass scan).  Escape lists wait in a ring buffer in shared memory,
+// where a waiting list costs only its own bytes; the retiring warp polls up to 32 waiting lists
+// per round trip and copies resolved ones out with 16-byte stores, so coding never waits for
 // the scan unless the ring is full.  Every wait is bounded.
 #include "zc_common.cuh"
 
@@ -36,7 +36,9 @@ constexpr unsigned kInBytes = 2 * kChunk;
 constexpr unsigned kRingBytes = 32 * 1024; // escape-list ring per CTA
 constexpr unsigned kQueue = 64;            // escape lists waiting, at most
 constexpr unsigned kWaitLimit = 1u << 22;  // mbarrier polls before giving up
-constexpr int kScanPerLane = 16;           // state words per lane per scanner round trip
+constexpr int kScanPerLane = 8;            // state words per scanner lane per round trip
+constexpr int kCoderWarps = kCoders / 32;
+constexpr unsigned kScanPerWarp = 32 * kScanPerLane;
 
 struct EncodeParams {
   const uint16_t* in;
@@ -69,6 +71,10 @@ struct __align__(128) EncodeSmem {
   unsigned esc_off;  // ring offset of the list being written
   int abort;         // written by coding thread 0 only, between the rank barrier and [E]
   int load_fail;     // a bounded wait for an input copy ran out
+  // scanner (block 0): per round parity, each warp's ready count and sum, and the status word
+  unsigned long long scan_sum[2][kCoderWarps];
+  unsigned scan_ready[2][kCoderWarps];
+  int scan_bad[2];
   int e0;
 };
 
@@ -91,39 +97,31 @@ __device__ void issue_load(EncodeSmem& S, int s, uint64_t c, const EncodeParams&
   }
 }
 
-// The scanner (block 0): resolve chunks in order.  Each round reads the next 512 state words;
-// the published sizes before the first unpublished one become inclusive offsets.
-__device__ __noinline__ void scanner(unsigned long long* flags, uint64_t N, int* status, unsigned spin_limit) {
-  const unsigned lane = threadIdx.x & 31;
+// The scanner (block 0, warps 0..7): resolve chunks in order.  Each round, warp w reads state
+// words frontier + 256 w .. + 255; the published sizes before the first unpublished word (over
+// all warps, in order) become inclusive offsets.  One barrier per round exchanges the warps'
+// ready counts and sums (double-buffered by round parity, so one barrier suffices).
+__device__ __noinline__ void scanner(EncodeSmem& S, unsigned long long* flags, uint64_t N, int* status,
+                                     unsigned spin_limit) {
+  const unsigned lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint64_t frontier = 0;
   unsigned long long prefix = 0;
   unsigned spins = 0, backoff = 32;
-  while (frontier < N) {
+  for (unsigned round = 0; frontier < N; ++round) {
+    const unsigned b = round & 1;
+    const uint64_t wbase = frontier + static_cast<uint64_t>(kScanPerWarp) * warp;
+    const int bad = warp == 0 && lane == 0 ? read_status(status) : 0;  // in flight with the flags
     unsigned long long f[kScanPerLane];
 #pragma unroll
     for (int j = 0; j < kScanPerLane; ++j) {
-      const uint64_t idx = frontier + kScanPerLane * lane + j;
+      const uint64_t idx = wbase + kScanPerLane * lane + j;
       f[j] = idx < N ? ld_relaxed_u64(&flags[idx]) : 0ull;
     }
-    unsigned mine = 32 * kScanPerLane;  // first unpublished position held by this lane
+    unsigned mine = kScanPerWarp;  // first unpublished position held by this lane
 #pragma unroll
     for (int j = kScanPerLane - 1; j >= 0; --j)
       if ((f[j] >> 62) == 0) mine = kScanPerLane * lane + j;
     const unsigned ready = __reduce_min_sync(0xFFFFFFFFu, mine);
-    if (ready == 0) {
-      int bad = lane == 0 ? read_status(status) : 0;
-      bad = __shfl_sync(0xFFFFFFFFu, bad, 0);
-      if (bad != 0) return;
-      if (++spins > spin_limit) {
-        if (lane == 0) set_error(status, ZC_ERR_TIMEOUT);
-        return;
-      }
-      __nanosleep(backoff);
-      backoff = backoff < 256 ? backoff * 2 : 256;
-      continue;
-    }
-    spins = 0;
-    backoff = 32;
     unsigned long long own = 0;
 #pragma unroll
     for (int j = 0; j < kScanPerLane; ++j)
@@ -134,38 +132,81 @@ __device__ __noinline__ void scanner(unsigned long long* flags, uint64_t N, int*
       const unsigned long long t = __shfl_up_sync(0xFFFFFFFFu, run, o);
       if (lane >= static_cast<unsigned>(o)) run += t;
     }
-    unsigned long long acc = prefix + (run - own);
+    if (lane == 31) {
+      S.scan_ready[b][warp] = ready;
+      S.scan_sum[b][warp] = run;
+    }
+    if (warp == 0 && lane == 0) S.scan_bad[b] = bad;
+    bar_coders();
+    // Lanes 0..7 hold the eight warps' results; warps before the first partly ready one are
+    // whole, and that one contributes its ready part.
+    const unsigned r8 = lane < kCoderWarps ? S.scan_ready[b][lane] : 0u;
+    const unsigned long long s8 = lane < kCoderWarps ? S.scan_sum[b][lane] : 0ull;
+    const unsigned whole = __ballot_sync(0xFFFFFFFFu, lane < kCoderWarps && r8 == kScanPerWarp);
+    const unsigned first_partial = __ffs(~whole) - 1;  // kCoderWarps when all are whole
+    const unsigned tail_ready = __shfl_sync(0xFFFFFFFFu, r8, first_partial & 31);
+    const uint64_t total_ready = static_cast<uint64_t>(kScanPerWarp) * first_partial +
+                                 (first_partial < static_cast<unsigned>(kCoderWarps) ? tail_ready : 0u);
+    const unsigned long long use = lane <= first_partial ? s8 : 0ull;  // sums that count
+    unsigned long long before = lane < warp ? use : 0ull, total = use;
 #pragma unroll
-    for (int j = 0; j < kScanPerLane; ++j) {
-      const unsigned q = kScanPerLane * lane + j;
-      if (q < ready) {
-        acc += f[j] & kFlagValueMask;
-        st_relaxed_u64(&flags[frontier + q], kFlagInclusive | acc);
+    for (int o = 16; o > 0; o >>= 1) {
+      before += __shfl_xor_sync(0xFFFFFFFFu, before, o);
+      total += __shfl_xor_sync(0xFFFFFFFFu, total, o);
+    }
+    if (total_ready == 0) {
+      if (S.scan_bad[b] != 0) return;
+      if (++spins > spin_limit) {
+        if (warp == 0 && lane == 0) set_error(status, ZC_ERR_TIMEOUT);
+        return;
+      }
+      __nanosleep(backoff);
+      backoff = backoff < 256 ? backoff * 2 : 256;
+      continue;
+    }
+    spins = 0;
+    backoff = 32;
+    if (warp <= first_partial) {
+      unsigned long long acc = prefix + before + (run - own);
+#pragma unroll
+      for (int j = 0; j < kScanPerLane; ++j) {
+        const unsigned q = kScanPerLane * lane + j;
+        if (q < ready) {
+          acc += f[j] & kFlagValueMask;
+          st_relaxed_u64(&flags[wbase + q], kFlagInclusive | acc);
+        }
       }
     }
-    prefix += __shfl_sync(0xFFFFFFFFu, run, 31);
-    frontier += ready;
+    prefix += total;
+    frontier += total_ready;
   }
 }
 
-// The retiring warp: write escape lists out in chunk order as the scanner resolves them, fill in
+// The retiring warp: copy escape lists out in chunk order as the scanner resolves them, fill in
 // the offset table (and the header fields that belong to the first and last chunk), and give
-// ring space back once each bulk store has read its bytes.
+// the ring space back.  Lists and their places are 16-byte aligned, so the whole warp copies
+// each one with 16-byte loads and stores: plain stores, so the coding threads need no proxy
+// fence before handing a list over.  Every value that steers the warp is made uniform over its
+// lanes: each lane reads it itself and the warp takes the minimum (or any / all).
 __device__ void retirer(EncodeSmem& S, const EncodeParams& p) {
   const unsigned lane = threadIdx.x & 31;
   const uint64_t E0 = escape_base(p.n);
   unsigned long long* table = reinterpret_cast<unsigned long long*>(p.out + kHeaderBytes);
   unsigned retired = 0, freed = 0, spins = 0, backoff = 64;
   for (;;) {
-    const unsigned pushed = S.q_pushed;
+    const unsigned pushed = __reduce_min_sync(0xFFFFFFFFu, S.q_pushed);
     const unsigned avail = pushed - retired;
     if (avail == 0) {
-      if (S.coders_done) {  // the producer bumps q_pushed before it sets coders_done
+      if (__all_sync(0xFFFFFFFFu, S.coders_done != 0)) {  // q_pushed was bumped before coders_done
         __threadfence_block();
-        if (S.q_pushed == retired) break;
+        if (__reduce_min_sync(0xFFFFFFFFu, S.q_pushed) == retired) break;
         continue;
       }
-      if (++spins > p.spin_limit || read_status(p.status) != 0) break;
+      if (__any_sync(0xFFFFFFFFu, read_status(p.status) != 0)) break;
+      if (++spins > p.spin_limit) {
+        if (lane == 0) set_error(p.status, ZC_ERR_TIMEOUT);
+        break;
+      }
       __nanosleep(backoff);
       backoff = backoff < 512 ? backoff * 2 : 512;
       continue;
@@ -179,22 +220,30 @@ __device__ void retirer(EncodeSmem& S, const EncodeParams& p) {
     if (run == 0) {
       int bad = lane == 0 ? read_status(p.status) : 0;
       bad = __shfl_sync(0xFFFFFFFFu, bad, 0);
-      if (bad != 0 || ++spins > p.spin_limit) break;
+      if (bad != 0) break;
+      if (++spins > p.spin_limit) {
+        if (lane == 0) set_error(p.status, ZC_ERR_TIMEOUT);
+        break;
+      }
       __nanosleep(backoff);
       backoff = backoff < 512 ? backoff * 2 : 512;
       continue;
     }
     spins = 0;
     backoff = 64;
+    for (unsigned t = 0; t < run; ++t) {  // the lists, in order, each by the whole warp
+      const unsigned long long ft = __shfl_sync(0xFFFFFFFFu, f, t);
+      const unsigned it = (retired + t) % kQueue;
+      const unsigned size = S.q_size[it];
+      const uint4* src = S.ring + S.q_off[it] / 16;
+      uint4* dst = reinterpret_cast<uint4*>(p.out + E0 + (ft & kFlagValueMask) - size);
+      for (unsigned v = lane; v < size / 16; v += 32) dst[v] = src[v];
+    }
     unsigned give_back = 0;
     if (lane < run) {
       const unsigned long long c = S.q_chunk[i];
       const unsigned size = S.q_size[i];
       const unsigned long long off = E0 + (f & kFlagValueMask) - size;
-      if (size) {
-        bulk_store(p.out + off, reinterpret_cast<const uint8_t*>(S.ring) + S.q_off[i], size);
-        bulk_commit();
-      }
       table[c] = off;
       if (c == 0) {
         unsigned long long* hdr = reinterpret_cast<unsigned long long*>(p.out);
@@ -211,19 +260,19 @@ __device__ void retirer(EncodeSmem& S, const EncodeParams& p) {
         if (p.out_bytes) *p.out_bytes = total;
       }
       give_back = S.q_gap[i] + size;
-      bulk_wait_read<0>();  // this lane's stores have read their bytes
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) give_back += __shfl_xor_sync(0xFFFFFFFFu, give_back, o);
     retired += run;
     freed += give_back;
+    __syncwarp();
     if (lane == 0) {
+      __threadfence_block();  // the copies have read the ring before it is handed back
       S.freed = freed;
       S.q_retired = retired;
     }
     __syncwarp();
   }
-  bulk_wait_all<0>();
 }
 
 // Coding thread 0's side of the ring: room for `need` bytes (a multiple of 16, at most
@@ -263,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) encode_kernel(EncodePara
   EncodeSmem& S = *reinterpret_cast<EncodeSmem*>(smem_raw);
   const unsigned tid = threadIdx.x, warp = tid >> 5;
   if (blockIdx.x == 0) {  // block 0: the scanner
-    if (warp == kCoders / 32) scanner(p.flags, p.N, p.status, p.spin_limit);
+    if (warp < kCoderWarps) scanner(S, p.flags, p.N, p.status, p.spin_limit);
     return;
   }
   if (tid == 0) {
@@ -378,7 +427,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) encode_kernel(EncodePara
         }
       }
       if (tid < esc_bytes - 3 * k) esc[3 * k + tid] = 0;  // zero padding, < 16 bytes
-      fence_proxy_async_smem();
     }
     bar_coders();  // [C] the list is complete in the ring; stage s is free again
     if (S.abort) break;
