@@ -7,10 +7,12 @@
 // kernels use a communication-aware layout, aligned global/shared memory access and pipeline
 // data movement with compression compute (second technique).
 //
-// GB300 design.  A persistent grid, three CTAs per SM.  Block 0 is the scanner; every other
+// GB300 design.  A persistent grid, four CTAs per SM.  Block 0 is the scanner; every other
 // block has eight coding warps and one retiring warp.  Chunks are handed out by an atomic
 // ticket (ticket order = chunk order).  Inputs (8 KiB per chunk) arrive by bulk async copies
-// (TMA engine, mbarrier completion) three stages ahead; a coding thread holds 2 slices of 8
+// (TMA engine, mbarrier completion) into two stages, so the next chunk's copy is in flight
+// while a chunk is coded (with four CTAs per SM, deeper pipelines measured slower: every stage
+// holds a ticket, and held tickets lengthen the tail); a coding thread holds 2 slices of 8
 // values and codes two values per 32-bit word with packed 16-bit arithmetic.  The fixed part of
 // a chunk has a place that follows from n, so it goes straight from registers to HBM: 8-byte
 // stores of sign|mantissa bytes and, per warp, 24 coalesced 32-bit words of codes assembled
@@ -30,11 +32,12 @@ namespace {
 constexpr int kCoders = 256;               // coding threads
 constexpr int kSlices = kChunk / (8 * kCoders);  // slices of 8 values per coding thread
 constexpr int kThreads = kCoders + 32;     // + the retiring warp (the scanner in block 0)
-constexpr int kCtasPerSm = 3;
-constexpr int kStages = 3;                 // input chunks in flight per CTA
+constexpr int kCtasPerSm = 4;
+constexpr int kStages = 2;                 // input chunks in flight per CTA
 constexpr unsigned kInBytes = 2 * kChunk;
 constexpr unsigned kRingBytes = 32 * 1024; // escape-list ring per CTA
 constexpr unsigned kQueue = 64;            // escape lists waiting, at most
+constexpr unsigned kCoopMin = 6;           // escapes per lane from which a warp writes them together
 constexpr unsigned kWaitLimit = 1u << 22;  // mbarrier polls before giving up
 constexpr int kScanPerLane = 8;            // state words per scanner lane per round trip
 constexpr int kCoderWarps = kCoders / 32;
@@ -68,6 +71,9 @@ struct __align__(128) EncodeSmem {
   volatile unsigned freed;      // ring bytes given back, gaps included (consumer)
   volatile int coders_done;     // no more entries will come
   __align__(16) unsigned scan[kCoders / 32 * kSlices / 2];
+  // Per coding warp: the warp's escapes of one slice in rank order, each as its value's offset in
+  // the warp's 256 values of that slice.
+  uint8_t esc_at[kCoderWarps][256];
   unsigned esc_off;  // ring offset of the list being written
   int abort;         // written by coding thread 0 only, between the rank barrier and [E]
   int load_fail;     // a bounded wait for an input copy ran out
@@ -77,6 +83,24 @@ struct __align__(128) EncodeSmem {
   int scan_bad[2];
   int e0;
 };
+
+// Shared-memory accesses by 32-bit shared-window address.
+__device__ __forceinline__ void sts_u8(uint32_t a, unsigned v) {
+  asm volatile("st.shared.u8 [%0], %1;" ::"r"(a), "h"(static_cast<unsigned short>(v)) : "memory");
+}
+__device__ __forceinline__ void sts_u16(uint32_t a, unsigned v) {
+  asm volatile("st.shared.u16 [%0], %1;" ::"r"(a), "h"(static_cast<unsigned short>(v)) : "memory");
+}
+__device__ __forceinline__ unsigned lds_u8(uint32_t a) {
+  unsigned short v;
+  asm volatile("ld.shared.u8 %0, [%1];" : "=h"(v) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ unsigned lds_u16(uint32_t a) {
+  unsigned short v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a) : "memory");
+  return v;
+}
 
 __device__ __forceinline__ void bar_coders() { asm volatile("bar.sync 1, %0;" ::"n"(kCoders) : "memory"); }
 
@@ -310,7 +334,7 @@ __device__ bool ring_alloc(EncodeSmem& S, Producer& P, const EncodeParams& p, un
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) encode_kernel(EncodeParams p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   EncodeSmem& S = *reinterpret_cast<EncodeSmem*>(smem_raw);
-  const unsigned tid = threadIdx.x, warp = tid >> 5;
+  const unsigned tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (blockIdx.x == 0) {  // block 0: the scanner
     if (warp < kCoderWarps) scanner(S, p.flags, p.N, p.status, p.spin_limit);
     return;
@@ -411,22 +435,49 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) encode_kernel(EncodePara
       S.esc_off = where;
     }
     bar_coders();  // [E] the list has a place in the ring
-    if (!S.abort) {  // positions and exponents, in rank order
-      uint8_t* esc = reinterpret_cast<uint8_t*>(S.ring) + S.esc_off;
-      const uint16_t* xin16 = reinterpret_cast<const uint16_t*>(S.xin[s]);
+    if (!S.abort) {  // positions and exponents, in rank order (S.abort is the same for all)
+      // Two ways to write a warp's escapes of one slice, chosen by the most escapes any of its
+      // lanes holds (M).  Sparse (M < kCoopMin): each lane writes its own, M passes.  Dense:
+      // each lane enters its escapes' offsets (within the warp's 256 values of the slice) in the
+      // warp's table, a short loop with no loads; then lane x writes the warp's x-th escape, so
+      // one pass covers 32 escapes with consecutive stores.  Shared memory is addressed with
+      // 32-bit shared-window addresses throughout.
+      const uint32_t esc = smem_u32(S.ring) + S.esc_off;
+      const uint32_t xin = smem_u32(S.xin[s]);
 #pragma unroll
       for (int q = 0; q < kSlices; ++q) {
-        unsigned r = base[q], mk = msk[q];
-        const unsigned v0 = 8 * kCoders * q + 8 * tid;
-        while (mk) {
-          const unsigned pos = v0 + (((__ffs(mk) - 1) * 11u) >> 5);  // bit 3j -> j, exact for j < 8
-          mk &= mk - 1;
-          reinterpret_cast<uint16_t*>(esc)[r] = static_cast<uint16_t>(pos);
-          esc[2 * k + r] = static_cast<uint8_t>(xin16[pos] >> 7);
-          ++r;
+        const unsigned first = 8 * kCoders * q + 256 * warp;  // the warp's values in slice q
+        unsigned mk = msk[q];
+        if (__reduce_max_sync(0xFFFFFFFFu, cnt[q]) < kCoopMin) {
+          unsigned r = base[q];
+          while (mk) {
+            const unsigned pos = first + 8 * lane + (((__ffs(mk) - 1) * 11u) >> 5);  // bit 3j -> j
+            mk &= mk - 1;
+            sts_u16(esc + 2 * r, pos);
+            sts_u8(esc + 2 * k + r, lds_u16(xin + 2 * pos) >> 7);
+            ++r;
+          }
+        } else {
+          const unsigned wfirst = __shfl_sync(0xFFFFFFFFu, base[q], 0);  // lane 0: the warp's first rank
+          const unsigned wcnt = __shfl_sync(0xFFFFFFFFu, base[q] + cnt[q], 31) - wfirst;
+          const uint32_t at = smem_u32(&S.esc_at[warp][0]);
+          unsigned r = base[q] - wfirst;
+          while (mk) {
+            const unsigned j = ((__ffs(mk) - 1) * 11u) >> 5;  // bit 3j -> j, exact for j < 8
+            mk &= mk - 1;
+            sts_u8(at + r++, 8 * lane + j);
+          }
+          __syncwarp();
+          for (unsigned x = lane; x < wcnt; x += 32) {
+            const unsigned pos = first + lds_u8(at + x);
+            const unsigned rr = wfirst + x;
+            sts_u16(esc + 2 * rr, pos);
+            sts_u8(esc + 2 * k + rr, lds_u16(xin + 2 * pos) >> 7);
+          }
+          __syncwarp();  // the table is reused by the next slice
         }
       }
-      if (tid < esc_bytes - 3 * k) esc[3 * k + tid] = 0;  // zero padding, < 16 bytes
+      if (tid < esc_bytes - 3 * k) sts_u8(esc + 3 * k + tid, 0);  // zero padding, < 16 bytes
     }
     bar_coders();  // [C] the list is complete in the ring; stage s is free again
     if (S.abort) break;
