@@ -8,8 +8,8 @@
  * are stored in 3 bits instead of 8, out-of-window exponents keep their full 8 bits in a
  * separate list so that reconstruction is exact, and sign and mantissa travel unchanged --
  * about 11 bits per value instead of 16.  The second technique of the same section
- * ("GPU-optimized compression and decompression kernels": communication-aware layout,
- * aligned global and shared memory access, data movement pipelined with compute) is what the
+ * (kernels tuned for the GPU: a layout shaped by the communication, aligned global and shared
+ * memory access, data movement pipelined with compute) is what the
  * kernels behind these calls implement for sm_103a.
  *
  * Stream format "ZCB1", version 2 (little-endian, every section zero-padded to 16 bytes):
@@ -20,8 +20,8 @@
  *   fixed     for chunk c (m values), at R0 + 5632 c: 3-bit codes, code i at bits [3i, 3i+3)
  *             least significant bit first (pad16(ceil(3m/8)) B), then one sign|mantissa byte
  *             per value, (x >> 8 & 0x80) | (x & 0x7F) (pad16(m) B).  The place of every fixed
- *             part follows from n alone ("communication-aware layout": it can be sent before
- *             any size is exchanged).
+ *             part follows from n alone (a layout shaped by the communication: it can be sent
+ *             before any size is exchanged).
  *   escapes   after the last fixed part, in chunk order: for a chunk with k escapes, u16
  *             positions then u8 full exponents in ascending position order (pad16(3k) B).
  *   Code c < 7 means exponent e0 + c; code 7 means "escape".  e0 is in [0, 249].
@@ -76,8 +76,8 @@ size_t zc_max_stream_bytes(size_t n);
  *   base_or_auto  ZC_BASE_AUTO: e0 = floor(log2(sigma * c)) + 127 clamped to [0, 249], with
  *                 sigma the root mean square of the finite values and c^2 =
  *                 0x1.79a1e790e0f01p-10 (the window with the fewest expected escapes for a
- *                 Gaussian; "determines the frequent exponent range directly from the tensor
- *                 standard deviation").  0..249: use that e0.  The stream depends only on
+ *                 Gaussian: the window comes from the standard deviation alone, with no
+ *                 histogram or sort).  0..249: use that e0.  The stream depends only on
  *                 (input bits, e0): both modes give identical bytes for the same e0.
  *   out           device, zc_max_compressed_bytes(n) bytes, 16-byte aligned, must not overlap
  *                 `in`.  The stream is written from out[0]; the bytes past *out_bytes,

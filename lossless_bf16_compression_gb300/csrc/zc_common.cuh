@@ -3,7 +3,7 @@
 //
 // Method: ZipCCL (SIGCOMM scribe notes), "Key idea and contribution": exponent coding with a
 // window taken from the standard deviation (first technique) and GPU kernels with a
-// communication-aware layout, aligned global/shared memory access and data movement pipelined
+// layout shaped by the communication, aligned global/shared memory access and data movement pipelined
 // with compute (second technique).
 #pragma once
 

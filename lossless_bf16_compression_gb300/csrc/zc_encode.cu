@@ -3,9 +3,9 @@
 // contiguous stream behind a chunk-offset table.
 //
 // Method: ZipCCL (SIGCOMM scribe notes), "Key idea and contribution": in-window exponents are
-// coded in 3 bits, out-of-window exponents are kept whole "separately" (first technique); the
-// kernels use a communication-aware layout, aligned global/shared memory access and pipeline
-// data movement with compression compute (second technique).
+// coded in 3 bits, out-of-window exponents are kept whole in a list of their own (first
+// technique); the kernels lay data out for the communication step, align their global and
+// shared memory accesses, and overlap data movement with the coding (second technique).
 //
 // GB300 design.  A persistent grid, four CTAs per SM.  Block 0 is the scanner; every other
 // block has eight coding warps and one retiring warp.  Chunks are handed out by an atomic

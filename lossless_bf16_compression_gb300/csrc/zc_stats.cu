@@ -1,9 +1,9 @@
 // zc_stats.cu -- statistics pass: sum of squares of the finite values, count of the
 // non-finite ones, and the window base e0 derived from them.
 //
-// Method: ZipCCL (SIGCOMM scribe notes), "Key idea and contribution", first technique: "the
-// frequent exponent range directly from the tensor standard deviation", with no histogram and
-// no sort.  e0 = floor(log2(sigma * c)) + 127 clamped to [0, 249], sigma^2 = S / n_f, where S is
+// Method: ZipCCL (SIGCOMM scribe notes), "Key idea and contribution", first technique: the
+// window of frequent exponents is taken from the tensor's standard deviation alone, with no
+// histogram and no sort.  e0 = floor(log2(sigma * c)) + 127 clamped to [0, 249], sigma^2 = S / n_f, where S is
 // the exact sum of squares rounded once to fp64 and c^2 = 0x1.79a1e790e0f01p-10 (the base
 // whose 7-binade window has the fewest expected escapes under a Gaussian).
 //
