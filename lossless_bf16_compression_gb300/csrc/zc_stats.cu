@@ -9,8 +9,11 @@
 //
 // GB300 design.  The pass is HBM-bound (it reads 2n bytes), and GB300's fp64 rate is far below
 // what one fp64 operation per value would need, so values are summed in fp32 blocks of 64 with
-// four FFMA chains, and only block sums go to fp64.  Every block sum carries a relative error
-// below 2^-18 (at most 17 roundings, or 64 on the careful path), so the grid total S_est
+// four FFMA chains, and only block sums go to fp64.  A block whose plain fp32 sum leaves the
+// safe range is redone with its values scaled by a power of two from its largest magnitude,
+// so no bit pattern of the BF16 range overflows or loses the block's sum to underflow; only
+// blocks holding Inf or NaN take a careful path that skips them.  Every block sum carries a relative error below 2^-18 (at most 17 roundings, or
+// 64 on the careful path), so the grid total S_est
 // satisfies |S_est - S| < 2^-17 S.  The last CTA evaluates the rule at S_est (1 -+ 2^-16),
 // rounded outward; when both ends give the same e0 (all but ~4e-5 of random tensors) that e0
 // is exactly the one the correctly rounded S gives, because the rule is monotone in S.
@@ -81,10 +84,29 @@ __device__ __forceinline__ double careful_block(const uint32_t (&w)[32], unsigne
   return static_cast<double>(s) * scale;
 }
 
-// The careful path for one lane's block (vectors wb + 32 j + lane), reloaded from memory so that
-// the fast path's registers never have to be spilled to call it.
-__device__ __noinline__ double careful_block_at(const uint4* in, uint64_t wb, uint64_t nv, unsigned lane,
-                                                unsigned* nonfinite) {
+// The last n % 8 values, zero-padded (a zero adds nothing and is not counted as non-finite).
+__device__ __noinline__ double tail_block(const uint16_t* tail, unsigned count, unsigned* nonfinite) {
+  uint32_t w[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) w[i] = 0;
+  for (unsigned i = 0; i < count; ++i) w[i >> 1] |= static_cast<uint32_t>(tail[i]) << (16 * (i & 1));
+  return careful_block(w, nonfinite);
+}
+
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// A block whose plain fp32 sum may have overflowed, lost precision to underflow or met Inf/NaN,
+// reloaded from memory (so that the fast path's registers need not survive the call).  Every
+// value is scaled by a power of two taken from the block's largest magnitude, so that no square
+// overflows and the largest lies in [2^-16, 16).  Bit patterns with the sign cleared order like
+// magnitudes, so one packed 16-bit max finds the largest.  Blocks holding Inf or NaN take the
+// careful path.
+__device__ __noinline__ double scaled_block_at(const uint4* in, uint64_t wb, uint64_t nv, unsigned lane,
+                                               unsigned* nonfinite) {
   uint32_t w[32];
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
@@ -95,16 +117,31 @@ __device__ __noinline__ double careful_block_at(const uint4* in, uint64_t wb, ui
     w[4 * j + 2] = v.z;
     w[4 * j + 3] = v.w;
   }
-  return careful_block(w, nonfinite);
-}
-
-// The last n % 8 values, zero-padded (a zero adds nothing and is not counted as non-finite).
-__device__ __noinline__ double tail_block(const uint16_t* tail, unsigned count, unsigned* nonfinite) {
-  uint32_t w[32];
+  uint32_t mx = 0;
 #pragma unroll
-  for (int i = 0; i < 32; ++i) w[i] = 0;
-  for (unsigned i = 0; i < count; ++i) w[i >> 1] |= static_cast<uint32_t>(tail[i]) << (16 * (i & 1));
-  return careful_block(w, nonfinite);
+  for (int i = 0; i < 32; ++i) mx = max_u16x2(mx, w[i] & 0x7FFF7FFFu);
+  const unsigned m = max(mx & 0xFFFFu, mx >> 16);
+  if (m >= 0x7F80u) return careful_block(w, nonfinite);  // Inf or NaN in the block
+  if (m == 0) return 0.0;                                  // zeros only
+  // The largest value lies in [2^(E-127), 2^(E-126)), E its biased exponent (1 for subnormals,
+  // whose largest is at least 2^-133).  Scale by 2^(126-Es), Es = min(E, 252), a normal float:
+  // the scaled values stay below 4 and the largest is at least 2^-8.  A scaled value loses bits
+  // only below 2^-142, so every square the sum keeps is exact, and what underflows is under
+  // 2^-120 of the block sum.
+  const int Es = min(max(static_cast<int>(m >> 7), 1), 252);
+  const float sc = __int_as_float((253 - Es) << 23);
+  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; i += 2) {
+    const float l0 = __uint_as_float(w[i] << 16) * sc, h0 = __uint_as_float(w[i] & 0xFFFF0000u) * sc;
+    const float l1 = __uint_as_float(w[i + 1] << 16) * sc, h1 = __uint_as_float(w[i + 1] & 0xFFFF0000u) * sc;
+    a0 = fmaf(l0, l0, a0);
+    a1 = fmaf(h0, h0, a1);
+    a2 = fmaf(l1, l1, a2);
+    a3 = fmaf(h1, h1, a3);
+  }
+  const float blk = (a0 + a1) + (a2 + a3);
+  return static_cast<double>(blk) * __longlong_as_double(static_cast<long long>(1023 + 2 * Es - 252) << 52);
 }
 
 // Fast block sum: the squares of 64 values in four fp32 FFMA chains.
@@ -122,11 +159,11 @@ __device__ __forceinline__ void block_sum(const uint32_t (&w)[32], const uint4* 
   }
   const float blk = (a0 + a1) + (a2 + a3);
   // NaN/Inf inputs, fp32 overflow and blocks that may have lost precision to subnormal
-  // partial sums all fail this test and take the careful path.
+  // partial sums all fail this test and are redone scaled.
   if (blk >= 0x1p-100f && blk < 0x1p120f) {
     *acc += static_cast<double>(blk);
   } else {
-    *acc += careful_block_at(in, wb, nv, lane, nonfinite);
+    *acc += scaled_block_at(in, wb, nv, lane, nonfinite);
   }
 }
 
