@@ -7,18 +7,20 @@
 // technique); the kernels lay data out for the communication step, align their global and
 // shared memory accesses, and overlap data movement with the coding (second technique).
 //
-// GB300 design.  A persistent grid, four CTAs per SM.  Block 0 is the scanner; every other
-// block has eight coding warps and one retiring warp.  Chunks are handed out by an atomic
+// GB300 design.  A persistent grid, five CTAs per SM.  Block 0 is the scanner; every other
+// block has four coding warps and one retiring warp, so that each chunk's fixed costs (waits,
+// ranks, barriers) are paid by 128 threads and five chunks are in flight per SM (measured
+// faster than eight coding warps at four CTAs per SM).  Chunks are handed out by an atomic
 // ticket (ticket order = chunk order).  Inputs (8 KiB per chunk) arrive by bulk async copies
 // (TMA engine, mbarrier completion) into two stages, so the next chunk's copy is in flight
-// while a chunk is coded (with four CTAs per SM, deeper pipelines measured slower: every stage
-// holds a ticket, and held tickets lengthen the tail); a coding thread holds 2 slices of 8
-// values and codes two values per 32-bit word with packed 16-bit arithmetic.  The fixed part of
+// while a chunk is coded (deeper pipelines measured slower: every stage holds a ticket, and
+// held tickets lengthen the tail); a coding thread holds 4 slices of 8 values and codes two
+// values per 32-bit word with packed 16-bit arithmetic.  The fixed part of
 // a chunk has a place that follows from n, so it goes straight from registers to HBM: 8-byte
 // stores of sign|mantissa bytes and, per warp, 24 coalesced 32-bit words of codes assembled
 // with two shuffles.  Only the escape list waits for the device-wide scan: each chunk publishes
 // its list size in a per-chunk state word as soon as its escape count is known, and the
-// scanner's eight warps walk the state words in order, 2048 per round trip, turning every run
+// scanner's four warps walk the state words in order, 1024 per round trip, turning every run
 // of published sizes into inclusive offsets (a chained scan with one scanning block, after
 // Merrill & Garland's single-pass scan).  Escape lists wait in a ring buffer in shared memory,
 // where a waiting list costs only its own bytes; the retiring warp polls up to 32 waiting lists
@@ -29,13 +31,13 @@
 namespace zc {
 namespace {
 
-constexpr int kCoders = 256;               // coding threads
+constexpr int kCoders = 128;               // coding threads
 constexpr int kSlices = kChunk / (8 * kCoders);  // slices of 8 values per coding thread
 constexpr int kThreads = kCoders + 32;     // + the retiring warp (the scanner in block 0)
-constexpr int kCtasPerSm = 4;
+constexpr int kCtasPerSm = 5;
 constexpr int kStages = 2;                 // input chunks in flight per CTA
 constexpr unsigned kInBytes = 2 * kChunk;
-constexpr unsigned kRingBytes = 32 * 1024; // escape-list ring per CTA
+constexpr unsigned kRingBytes = 24 * 1024; // escape-list ring per CTA (two worst-case lists)
 constexpr unsigned kQueue = 64;            // escape lists waiting, at most
 constexpr unsigned kCoopMin = 6;           // escapes per lane from which a warp writes them together
 constexpr unsigned kWaitLimit = 1u << 22;  // mbarrier polls before giving up
@@ -121,7 +123,7 @@ __device__ void issue_load(EncodeSmem& S, int s, uint64_t c, const EncodeParams&
   }
 }
 
-// The scanner (block 0, warps 0..7): resolve chunks in order.  Each round, warp w reads state
+// The scanner (block 0, its kCoderWarps first warps): resolve chunks in order.  Each round, warp w reads state
 // words frontier + 256 w .. + 255; the published sizes before the first unpublished word (over
 // all warps, in order) become inclusive offsets.  One barrier per round exchanges the warps'
 // ready counts and sums (double-buffered by round parity, so one barrier suffices).
@@ -162,7 +164,7 @@ __device__ __noinline__ void scanner(EncodeSmem& S, unsigned long long* flags, u
     }
     if (warp == 0 && lane == 0) S.scan_bad[b] = bad;
     bar_coders();
-    // Lanes 0..7 hold the eight warps' results; warps before the first partly ready one are
+    // Lanes below kCoderWarps hold the warps' results; warps before the first partly ready one are
     // whole, and that one contributes its ready part.
     const unsigned r8 = lane < kCoderWarps ? S.scan_ready[b][lane] : 0u;
     const unsigned long long s8 = lane < kCoderWarps ? S.scan_sum[b][lane] : 0ull;
