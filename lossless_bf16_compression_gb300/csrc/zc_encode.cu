@@ -39,7 +39,8 @@ constexpr int kStages = 2;                 // input chunks in flight per CTA
 constexpr unsigned kInBytes = 2 * kChunk;
 constexpr unsigned kRingBytes = 24 * 1024; // escape-list ring per CTA (two worst-case lists)
 constexpr unsigned kQueue = 64;            // escape lists waiting, at most
-constexpr unsigned kCoopMin = 6;           // escapes per lane from which a warp writes them together
+constexpr unsigned kCombinedMax = 16;      // escapes per lane from which a warp writes them together
+static_assert(kSlices == 4, "the combined escape mask holds four slices of 8");
 constexpr unsigned kWaitLimit = 1u << 22;  // mbarrier polls before giving up
 constexpr int kScanPerLane = 8;            // state words per scanner lane per round trip
 constexpr int kCoderWarps = kCoders / 32;
@@ -85,6 +86,13 @@ struct __align__(128) EncodeSmem {
   int scan_bad[2];
   int e0;
 };
+
+// The 8 code-7 flags of a slice (bit 3j for value j) as bits 0..7.
+__device__ __forceinline__ unsigned compact8(unsigned m) {
+  m = (m | (m >> 2)) & 0x0C30C3u;
+  m = (m | (m >> 4)) & 0x00F00Fu;
+  return (m | (m >> 8)) & 0xFFu;
+}
 
 // Shared-memory accesses by 32-bit shared-window address.
 __device__ __forceinline__ void sts_u8(uint32_t a, unsigned v) {
@@ -438,28 +446,40 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) encode_kernel(EncodePara
     }
     bar_coders();  // [E] the list has a place in the ring
     if (!S.abort) {  // positions and exponents, in rank order (S.abort is the same for all)
-      // Two ways to write a warp's escapes of one slice, chosen by the most escapes any of its
-      // lanes holds (M).  Sparse (M < kCoopMin): each lane writes its own, M passes.  Dense:
-      // each lane enters its escapes' offsets (within the warp's 256 values of the slice) in the
-      // warp's table, a short loop with no loads; then lane x writes the warp's x-th escape, so
-      // one pass covers 32 escapes with consecutive stores.  Shared memory is addressed with
-      // 32-bit shared-window addresses throughout.
+      // Two ways to write a warp's escapes, chosen by the most escapes any of its lanes holds
+      // over all its slices (M).  Sparse (M < kCombinedMax): each lane walks one mask of all its
+      // slices, M passes in all.  Dense, per slice: each lane enters its escapes' offsets (within
+      // the warp's 256 values of the slice) in the warp's table, a short loop with no loads;
+      // then lane x writes the warp's x-th escape, so one pass covers 32 escapes with
+      // consecutive stores.  Shared memory is addressed with 32-bit shared-window addresses.
       const uint32_t esc = smem_u32(S.ring) + S.esc_off;
       const uint32_t xin = smem_u32(S.xin[s]);
+      unsigned mine = 0;
 #pragma unroll
-      for (int q = 0; q < kSlices; ++q) {
-        const unsigned first = 8 * kCoders * q + 256 * warp;  // the warp's values in slice q
-        unsigned mk = msk[q];
-        if (__reduce_max_sync(0xFFFFFFFFu, cnt[q]) < kCoopMin) {
-          unsigned r = base[q];
-          while (mk) {
-            const unsigned pos = first + 8 * lane + (((__ffs(mk) - 1) * 11u) >> 5);  // bit 3j -> j
-            mk &= mk - 1;
-            sts_u16(esc + 2 * r, pos);
-            sts_u8(esc + 2 * k + r, lds_u16(xin + 2 * pos) >> 7);
-            ++r;
-          }
-        } else {
+      for (int q = 0; q < kSlices; ++q) mine += cnt[q];
+      if (__reduce_max_sync(0xFFFFFFFFu, mine) < kCombinedMax) {
+        unsigned m32 = 0, adj[kSlices], before = 0;  // rank of a lane's t-th escape: adj[q] + t
+#pragma unroll
+        for (int q = 0; q < kSlices; ++q) {
+          m32 |= compact8(msk[q]) << (8 * q);
+          adj[q] = base[q] - before;
+          before += cnt[q];
+        }
+        unsigned t = 0;
+        while (m32) {
+          const unsigned b = __ffs(m32) - 1;
+          m32 &= m32 - 1;
+          const unsigned q = b >> 3;
+          const unsigned pos = 8 * kCoders * q + 8 * tid + (b & 7);
+          const unsigned r = pick4(adj, q) + t++;
+          sts_u16(esc + 2 * r, pos);
+          sts_u8(esc + 2 * k + r, lds_u16(xin + 2 * pos) >> 7);
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < kSlices; ++q) {
+          const unsigned first = 8 * kCoders * q + 256 * warp;  // the warp's values in slice q
+          unsigned mk = msk[q];
           const unsigned wfirst = __shfl_sync(0xFFFFFFFFu, base[q], 0);  // lane 0: the warp's first rank
           const unsigned wcnt = __shfl_sync(0xFFFFFFFFu, base[q] + cnt[q], 31) - wfirst;
           const uint32_t at = smem_u32(&S.esc_at[warp][0]);
