@@ -77,9 +77,6 @@ struct __align__(128) EncodeSmem {
   // Per coding warp: the warp's escapes of one slice in rank order, each as its value's offset in
   // the warp's 256 values of that slice.
   uint8_t esc_at[kCoderWarps][256];
-  unsigned esc_off;  // ring offset of the list being written
-  int abort;         // written by coding thread 0 only, between the rank barrier and [E]
-  int load_fail;     // a bounded wait for an input copy ran out
   // scanner (block 0): per round parity, each warp's ready count and sum, and the status word
   unsigned long long scan_sum[2][kCoderWarps];
   unsigned scan_ready[2][kCoderWarps];
@@ -309,23 +306,28 @@ __device__ void retirer(EncodeSmem& S, const EncodeParams& p) {
   }
 }
 
-// Coding thread 0's side of the ring: room for `need` bytes (a multiple of 16, at most
-// kMaxEscapeBytes) and a free queue slot.  Waits (bounded) for the retiring warp when the ring
-// is full.  False after a failed wait.
-struct Producer {
+// The ring as every coding thread tracks it (the same in all of them, so each can place the
+// next list itself): `need` bytes (a multiple of 16, at most kMaxEscapeBytes) at `where`, after
+// skipping `gap` bytes at the end.
+struct Ring {
   unsigned pushed = 0;  // entries made
   unsigned made = 0;    // ring bytes handed out, gaps included
   unsigned head = 0;    // ring offset where the next list may start
 };
 
-__device__ bool ring_alloc(EncodeSmem& S, Producer& P, const EncodeParams& p, unsigned need, unsigned* where,
-                           unsigned* gap) {
+__device__ __forceinline__ void ring_place(Ring& R, unsigned need, unsigned* where, unsigned* gap) {
   // head is the ring offset of `made`; a list that ended exactly at the end leaves it at
   // kRingBytes, which is offset 0.  With head below kRingBytes, where + need <= kRingBytes.
-  if (P.head >= kRingBytes) P.head = 0;
-  const unsigned skip = (need && P.head + need > kRingBytes) ? kRingBytes - P.head : 0u;
+  if (R.head >= kRingBytes) R.head = 0;
+  *gap = (need && R.head + need > kRingBytes) ? kRingBytes - R.head : 0u;
+  *where = *gap ? 0u : R.head;
+}
+
+// Wait (bounded) until the retiring warp has freed room for `bytes` more ring bytes and a queue
+// slot.  False after an error or a timeout.
+__device__ bool ring_room(const EncodeSmem& S, const Ring& R, unsigned bytes, const EncodeParams& p) {
   unsigned spins = 0, backoff = 64;
-  while (P.pushed - S.q_retired >= kQueue || P.made + skip + need - S.freed > kRingBytes) {
+  while (R.pushed - S.q_retired >= kQueue || R.made + bytes - S.freed > kRingBytes) {
     if (read_status(p.status) != 0) return false;
     if (++spins > p.spin_limit) {
       set_error(p.status, ZC_ERR_TIMEOUT);
@@ -334,11 +336,18 @@ __device__ bool ring_alloc(EncodeSmem& S, Producer& P, const EncodeParams& p, un
     __nanosleep(backoff);
     backoff = backoff < 512 ? backoff * 2 : 512;
   }
-  *gap = skip;
-  *where = skip ? 0u : P.head;
-  P.made += skip + need;
-  P.head = *where + need;
   return true;
+}
+
+__device__ __forceinline__ bool bar_coders_or(bool v) {
+  unsigned r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.or.pred p, 1, %2, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<unsigned>(v)), "n"(kCoders)
+      : "memory");
+  return r != 0;
 }
 
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) encode_kernel(EncodeParams p) {
@@ -354,8 +363,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) encode_kernel(EncodePara
     S.q_retired = 0;
     S.freed = 0;
     S.coders_done = 0;
-    S.abort = 0;
-    S.load_fail = 0;
     S.e0 = p.base >= 0 ? p.base : __ldcg(&p.ctrl->e0);
   }
   __syncthreads();
@@ -364,7 +371,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) encode_kernel(EncodePara
     return;
   }
 
-  Producer P;                            // coding thread 0 only
+  Ring R;                                // every coding thread's copy
+  bool failed = false;                   // this thread gave up a bounded wait
   unsigned pending = 0, parity = 0;      // coding thread 0: loads in flight per stage, next parity
   unsigned next_ticket = 0;              // coding thread 0: the ticket for the next free stage
   if (tid == 0) {
@@ -391,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) encode_kernel(EncodePara
     if (c >= p.N) break;
     if (!mbar_wait(&S.mbar[s], (it / kStages) & 1, kWaitLimit)) {
       set_error(p.status, ZC_ERR_TIMEOUT);
-      S.load_fail = 1;  // acted on by thread 0 before [E]
+      failed = true;  // the CTA stops at [C]
     }
     if (tid == 0) {
       pending &= ~(1u << s);
@@ -434,25 +442,24 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) encode_kernel(EncodePara
     unsigned base[kSlices];
     const unsigned k = chunk_ranks_bar1<kCoders>(cnt, base, S.scan);
     const unsigned esc_bytes = static_cast<unsigned>(pad16(3ull * k));
-    unsigned gap = 0;
-    if (tid == 0) {
-      if (c != p.stall_chunk) st_relaxed_u64(&p.flags[c], kFlagAggregate | esc_bytes);  // publish early
-      unsigned where = 0;
-      if (S.load_fail || c == p.stall_chunk || !ring_alloc(S, P, p, esc_bytes, &where, &gap)) {
-        S.abort = 1;  // (the stall test hook: this list is never resolved)
-        where = 0;
-      }
-      S.esc_off = where;
-    }
-    bar_coders();  // [E] the list has a place in the ring
-    if (!S.abort) {  // positions and exponents, in rank order (S.abort is the same for all)
+    // The list's place in the ring: every coding thread works it out from its own copy of the
+    // ring state and waits (bounded) for the room itself, so no barrier is needed before the
+    // list is written.  A thread that gives up stops the CTA at [C].
+    unsigned where, gap;
+    ring_place(R, esc_bytes, &where, &gap);
+    if (tid == 0 && c != p.stall_chunk) st_relaxed_u64(&p.flags[c], kFlagAggregate | esc_bytes);  // publish early
+    bool stop = failed || c == p.stall_chunk;  // (the stall test hook: this list is never resolved)
+    if (!stop && !ring_room(S, R, gap + esc_bytes, p)) stop = true;
+    R.made += gap + esc_bytes;
+    R.head = where + esc_bytes;
+    if (!__any_sync(0xFFFFFFFFu, stop)) {  // positions and exponents, in rank order
       // Two ways to write a warp's escapes, chosen by the most escapes any of its lanes holds
       // over all its slices (M).  Sparse (M < kCombinedMax): each lane walks one mask of all its
       // slices, M passes in all.  Dense, per slice: each lane enters its escapes' offsets (within
       // the warp's 256 values of the slice) in the warp's table, a short loop with no loads;
       // then lane x writes the warp's x-th escape, so one pass covers 32 escapes with
       // consecutive stores.  Shared memory is addressed with 32-bit shared-window addresses.
-      const uint32_t esc = smem_u32(S.ring) + S.esc_off;
+      const uint32_t esc = smem_u32(S.ring) + where;
       const uint32_t xin = smem_u32(S.xin[s]);
       unsigned mine = 0;
 #pragma unroll
@@ -501,16 +508,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) encode_kernel(EncodePara
       }
       if (tid < esc_bytes - 3 * k) sts_u8(esc + 3 * k + tid, 0);  // zero padding, < 16 bytes
     }
-    bar_coders();  // [C] the list is complete in the ring; stage s is free again
-    if (S.abort) break;
+    if (bar_coders_or(stop)) break;  // [C] the list is complete in the ring; stage s is free again
+    ++R.pushed;
     if (tid == 0) {
-      const unsigned qi = P.pushed % kQueue;
+      const unsigned qi = (R.pushed - 1) % kQueue;
       S.q_chunk[qi] = c;
-      S.q_off[qi] = S.esc_off;
+      S.q_off[qi] = where;
       S.q_size[qi] = esc_bytes;
       S.q_gap[qi] = gap;
       __threadfence_block();
-      S.q_pushed = ++P.pushed;
+      S.q_pushed = R.pushed;
       // The next ticket was taken a chunk ago, so its round trip is already over; the one
       // after it is taken now and used a chunk later.
       S.ticket[s] = next_ticket;
