@@ -6,11 +6,14 @@
 // reconstruction is exact (first technique); decompression kernels with aligned global and
 // shared memory access (second technique).
 //
-// GB300 design.  One 128-thread CTA per chunk, many CTAs per SM: fixed parts sit at places that
-// follow from n and the offset table locates every escape list, so there is no inter-CTA
-// dependency.  Warp 0 reads the header and the chunk's two escape offsets in one round trip and
-// checks them; the fixed part (5,632 B) and the escape list (at most 12,288 B) then arrive in
-// shared memory by two bulk async copies (TMA engine, one mbarrier).  A thread holds 4 slices
+// GB300 design.  One 128-thread CTA per chunk, sixteen CTAs per SM (32 registers, under 10 KB of
+// shared memory each): fixed parts sit at places that follow from n and the offset table
+// locates every escape list, so there is no inter-CTA dependency.  Warp 0 reads the header and
+// the chunk's two escape offsets in one round trip and checks them; the fixed part (5,632 B)
+// and, when it is at most 4 KB (about 1,360 escapes, a third of the chunk), the escape list then
+// arrive in shared memory by bulk async copies (TMA engine, one mbarrier).  A larger list is
+// read where it lies in the stream: sizing the staging buffer for the worst case (12 KB) would
+// cost a quarter of the CTAs per SM for every chunk.  A thread holds 4 slices
 // of 8 values; per slice it takes its 24 code bits and 8 sign|mantissa bytes from shared
 // memory, builds two values per 32-bit word with a few integer ops, and writes one coalesced
 // 16-byte store, escaped values with a placeholder exponent.  Then the threads walk the escape
@@ -24,6 +27,8 @@ namespace zc {
 namespace {
 
 constexpr int kThreads = kChunkThreads;  // 128
+constexpr int kCtasPerSm = 16;           // 2048 threads per SM: 32 registers and < 14 KB each
+constexpr unsigned kEscSmemBytes = 4096; // escape lists up to this size are staged in shared memory
 constexpr unsigned kWaitLimit = 1u << 22;   // mbarrier polls before giving up
 
 struct DecodeParams {
@@ -36,15 +41,16 @@ struct DecodeParams {
 
 struct __align__(128) DecodeSmem {
   uint4 fixed[kFullFixedBytes / 16];
-  uint4 esc[kMaxEscapeBytes / 16];
+  uint4 esc[kEscSmemBytes / 16];
   uint64_t mbar;
   unsigned escapes;  // code-7 count of the chunk, summed by the warps
   int ok;
   int e0;
   unsigned esc_bytes;
+  unsigned long long esc_off;
 };
 
-__global__ void __launch_bounds__(kThreads) decode_kernel(DecodeParams p) {
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(DecodeParams p) {
   __shared__ DecodeSmem S;
   const unsigned tid = threadIdx.x, lane = tid & 31;
   const uint64_t c = blockIdx.x;
@@ -85,9 +91,11 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeParams p) {
         const unsigned fbytes = static_cast<unsigned>(fixed_bytes(m));
         mbar_init(&S.mbar, 1);
         fence_mbar_init();
-        mbar_arrive_expect_tx(&S.mbar, fbytes + S.esc_bytes);
+        const unsigned staged = S.esc_bytes <= kEscSmemBytes ? S.esc_bytes : 0u;
+        mbar_arrive_expect_tx(&S.mbar, fbytes + staged);
         bulk_load(S.fixed, p.in + fixed_offset(p.n, c), fbytes, &S.mbar);
-        if (S.esc_bytes) bulk_load(S.esc, p.in + off0, S.esc_bytes, &S.mbar);
+        if (staged) bulk_load(S.esc, p.in + off0, staged, &S.mbar);
+        S.esc_off = off0;
       }
     }
   }
@@ -108,7 +116,9 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeParams p) {
   const unsigned smbytes = full ? kChunk : static_cast<unsigned>(pad16(m));
   const uint8_t* codes = reinterpret_cast<const uint8_t*>(S.fixed);
   const uint8_t* smp = codes + cbytes;
-  const uint8_t* esc = reinterpret_cast<const uint8_t*>(S.esc);
+  // A list larger than the staging buffer is read where it lies in the stream (its range was
+  // checked against the offset table and the stream length above).
+  const uint8_t* esc = S.esc_bytes <= kEscSmemBytes ? reinterpret_cast<const uint8_t*>(S.esc) : p.in + S.esc_off;
   const uint32_t e0_field = static_cast<uint32_t>(e0) * (128u * 0x00010001u);  // e0 << 7 in both halves
   uint16_t* dst = p.out + first;
 
@@ -155,17 +165,36 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeParams p) {
   bool corrupt = pad16(3ull * k) != S.esc_bytes;
   if (!corrupt) {
     const uint16_t* pos_list = reinterpret_cast<const uint16_t*>(esc);
-    for (unsigned i = tid; i < k; i += kThreads) {
-      const unsigned pos = pos_list[i], E = esc[2 * k + i];
+    auto patch = [&](unsigned i, unsigned pos, unsigned E, unsigned prev) {
       const unsigned pb = 3 * pos;
       const unsigned code = pos < m ? ((codes[pb >> 3] | (codes[(pb >> 3) + 1] << 8)) >> (pb & 7)) & 7u : 0u;
-      if (code != 7u || (i > 0 && pos <= pos_list[i - 1]) ||
+      if (code != 7u || (i > 0 && pos <= prev) ||
           (E >= static_cast<unsigned>(e0) && E <= static_cast<unsigned>(e0) + 6)) {
         corrupt = true;
-        continue;
+        return;
       }
       const unsigned sm = smp[pos];
       dst[pos] = static_cast<uint16_t>(((sm & 0x80u) << 8) | (E << 7) | (sm & 0x7Fu));
+    };
+    if (S.esc_bytes <= kEscSmemBytes) {  // staged in shared memory
+      for (unsigned i = tid; i < k; i += kThreads) patch(i, pos_list[i], esc[2 * k + i], i ? pos_list[i - 1] : 0u);
+    } else {  // in the stream: batches of kBatch entries per thread, every load issued first
+      constexpr int kBatch = 4;
+      for (unsigned i0 = 0; i0 < k; i0 += kBatch * kThreads) {
+        unsigned pv[kBatch], ev[kBatch], qv[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          const unsigned i = i0 + u * kThreads + tid;
+          pv[u] = i < k ? __ldg(pos_list + i) : 0u;
+          ev[u] = i < k ? __ldg(esc + 2 * k + i) : 0u;
+          qv[u] = (i < k && i > 0) ? __ldg(pos_list + i - 1) : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          const unsigned i = i0 + u * kThreads + tid;
+          if (i < k) patch(i, pv[u], ev[u], qv[u]);
+        }
+      }
     }
   }
 
