@@ -67,6 +67,10 @@ cudaError_t device_info(DeviceInfo* info) {
     if (err != cudaSuccess) return err;
     err = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status), g_status);
     if (err != cudaSuccess) return err;
+    err = stats_occupancy(&d.stats_per_sm);
+    if (err != cudaSuccess) return err;
+    err = encode_occupancy(&d.encode_per_sm);
+    if (err != cudaSuccess) return err;
     g_devices[dev] = d;
     g_device_ready[dev] = true;
   }

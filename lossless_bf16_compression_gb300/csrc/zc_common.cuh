@@ -361,10 +361,15 @@ __device__ __forceinline__ unsigned chunk_ranks_named(const unsigned (&cnt)[4], 
 
 struct DeviceInfo {
   int sm_count;
-  int* status;  // device address of the library's status word on this device
+  int* status;        // device address of the library's status word on this device
+  int stats_per_sm;   // resident CTAs per SM of the statistics and encode kernels, found once
+  int encode_per_sm;  // per device (host-side launch work stays small for small tensors)
 };
 
 cudaError_t device_info(DeviceInfo* info);  // defined in zc_api.cu
+cudaError_t stats_occupancy(int* per_sm);   // defined in zc_stats.cu
+cudaError_t encode_occupancy(int* per_sm);  // defined in zc_encode.cu; also sets the kernel's
+                                            // dynamic shared memory size, for the current device
 
 void timing_begin(int kernel_id, cudaStream_t stream);  // no-ops unless timing is enabled
 void timing_end(cudaStream_t stream);

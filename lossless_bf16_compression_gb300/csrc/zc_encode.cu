@@ -553,6 +553,13 @@ __global__ void empty_stream_kernel(uint8_t* out, int base, Control* ctrl, unsig
 
 }  // namespace
 
+cudaError_t encode_occupancy(int* per_sm) {
+  const int smem = static_cast<int>(sizeof(EncodeSmem));
+  cudaError_t err = cudaFuncSetAttribute(encode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (err != cudaSuccess) return err;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, encode_kernel, kThreads, smem);
+}
+
 cudaError_t launch_encode(const uint16_t* in, uint64_t n, int base, uint8_t* out,
                           unsigned long long* out_bytes, const DeviceInfo& dev, cudaStream_t stream,
                           uint64_t stall_chunk, unsigned spin_limit) {
@@ -577,11 +584,7 @@ cudaError_t launch_encode(const uint16_t* in, uint64_t n, int base, uint8_t* out
   p.spin_limit = spin_limit;
 
   const int smem = static_cast<int>(sizeof(EncodeSmem));
-  cudaError_t err = cudaFuncSetAttribute(encode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (err != cudaSuccess) return err;
-  int per_sm = 0;
-  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, encode_kernel, kThreads, smem);
-  if (err != cudaSuccess) return err;
+  const int per_sm = dev.encode_per_sm;
   uint64_t grid = static_cast<uint64_t>(per_sm > 0 ? per_sm : 1) * dev.sm_count;
   if (grid > p.N + 1) grid = p.N + 1;  // block 0 scans, the others code
   if (grid < 2) grid = 2;
@@ -612,11 +615,7 @@ cudaError_t launch_encode_ws(const uint16_t* in, uint64_t n, int base, uint8_t* 
   p.stall_chunk = ~uint64_t(0);
   p.spin_limit = 1u << 20;
   const int smem = static_cast<int>(sizeof(EncodeSmem));
-  cudaError_t err = cudaFuncSetAttribute(encode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (err != cudaSuccess) return err;
-  int per_sm = 0;
-  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, encode_kernel, kThreads, smem);
-  if (err != cudaSuccess) return err;
+  const int per_sm = dev.encode_per_sm;
   uint64_t grid = static_cast<uint64_t>(per_sm > 0 ? per_sm : 1) * dev.sm_count;
   if (grid > p.N + 1) grid = p.N + 1;  // block 0 scans, the others code
   if (grid < 2) grid = 2;

@@ -360,6 +360,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) stats_kernel(StatsParams
 
 }  // namespace
 
+cudaError_t stats_occupancy(int* per_sm) {
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, stats_kernel, kThreads, 0);
+}
+
 cudaError_t launch_stats(const uint16_t* in, uint64_t n, uint8_t* out, const DeviceInfo& dev,
                          cudaStream_t stream) {
   uint8_t* ws = out + workspace_offset(n);
@@ -371,9 +375,7 @@ cudaError_t launch_stats(const uint16_t* in, uint64_t n, uint8_t* out, const Dev
   p.status = dev.status;
   const uint64_t nv = n >> 3;
   const uint64_t blocks_needed = (nv + kVecPerWarpBlock * kWarps - 1) / (kVecPerWarpBlock * kWarps);
-  int per_sm = 0;
-  cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, stats_kernel, kThreads, 0);
-  if (err != cudaSuccess) return err;
+  const int per_sm = dev.stats_per_sm;
   uint64_t grid = static_cast<uint64_t>(per_sm > 0 ? per_sm : 1) * dev.sm_count;  // one wave
   if (grid > blocks_needed) grid = blocks_needed;
   if (grid < 1) grid = 1;
@@ -394,9 +396,7 @@ cudaError_t launch_stats_ws(const uint16_t* in, uint64_t n, uint8_t* ws, const D
   p.status = dev.status;
   const uint64_t nv = n >> 3;
   const uint64_t blocks_needed = (nv + kVecPerWarpBlock * kWarps - 1) / (kVecPerWarpBlock * kWarps);
-  int per_sm = 0;
-  cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, stats_kernel, kThreads, 0);
-  if (err != cudaSuccess) return err;
+  const int per_sm = dev.stats_per_sm;
   uint64_t grid = static_cast<uint64_t>(per_sm > 0 ? per_sm : 1) * dev.sm_count;
   if (grid > blocks_needed) grid = blocks_needed;
   if (grid < 1) grid = 1;
