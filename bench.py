@@ -305,24 +305,52 @@ def run_ours(args, rank, world, local):
     comp_ms = avg.get("stats", 0.0) + avg.get("encode", 0.0)
     dec_ms = avg.get("decode", 0.0)
 
-    # end to end through the C ABI: pinned host input -> device, compress, decompress, -> host
+    # End to end through the C ABI: every step copies its input from pinned host memory, runs
+    # zc_compress + zc_decompress, and copies the decoded tensor back to pinned host memory.
+    # Consecutive steps overlap on three streams with two sets of buffers, as a data pipeline
+    # would run: step i's copy back (device to host) runs while step i+1's input is copied in
+    # (host to device); the two directions use separate copy engines.
     xh = torch.from_numpy(x.view(np.int16)).pin_memory()
-    yh = torch.empty(n, dtype=torch.int16).pin_memory()
+    yh = [torch.empty(n, dtype=torch.int16).pin_memory() for _ in range(2)]
+    xd2, out2, dec2, ob2 = [xd, torch.empty_like(xd)], [out, torch.empty_like(out)], \
+        [dec, torch.empty_like(dec)], [ob, torch.zeros_like(ob)]
+    s_in, s_codec, s_out = (torch.cuda.Stream(device) for _ in range(3))
+    in_done, codec_done, out_done = ([torch.cuda.Event() for _ in range(2)] for _ in range(3))
+
+    def e2e_step(i):
+        b = i % 2
+        if i >= 2:
+            s_in.wait_event(codec_done[b])  # step i-2's compress has read xd2[b]
+        with torch.cuda.stream(s_in):
+            xd2[b].copy_(xh, non_blocking=True)
+        in_done[b].record(s_in)
+        s_codec.wait_event(in_done[b])
+        if i >= 2:
+            s_codec.wait_event(out_done[b])  # step i-2's decoded tensor has left dec2[b]
+        rc = zc.zc_compress(xd2[b].data_ptr(), n, zc.ZC_BASE_AUTO, out2[b].data_ptr(), ob2[b].data_ptr(),
+                            s_codec.cuda_stream)
+        rc |= zc.zc_decompress(out2[b].data_ptr(), dec2[b].data_ptr(), n, s_codec.cuda_stream)
+        if rc:
+            raise RuntimeError(f"codec call failed: {rc}")
+        codec_done[b].record(s_codec)
+        s_out.wait_event(codec_done[b])
+        with torch.cuda.stream(s_out):
+            yh[b].copy_(dec2[b], non_blocking=True)
+        out_done[b].record(s_out)
+
     e2e_steps = max(3, min(args.steps, 50))
-    es = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
-    ee = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
-    for i in range(e2e_steps + 2):
-        flush_l2()
-        if i >= 2:
-            es[i - 2].record(stream)
-        xd.copy_(xh, non_blocking=True)
-        step()
-        yh.copy_(dec, non_blocking=True)
-        if i >= 2:
-            ee[i - 2].record(stream)
+    for i in range(4):  # warm-up
+        e2e_step(i)
     torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(sum(s.elapsed_time(e) for s, e in zip(es, ee)) / e2e_steps, dist, device)
-    ok = ok and torch.equal(yh, xh) and zc.zc_status(sh, 1) == zc.ZC_OK
+    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e_start.record(s_in)
+    for i in range(4, 4 + e2e_steps):
+        e2e_step(i)
+    e_end.record(s_out)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e_start.elapsed_time(e_end) / e2e_steps, dist, device)
+    last = (4 + e2e_steps - 1) % 2
+    ok = ok and torch.equal(yh[last], xh) and zc.zc_status(s_codec.cuda_stream, 1) == zc.ZC_OK
 
     if rank != 0:
         return
@@ -355,7 +383,8 @@ def run_ours(args, rank, world, local):
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "algorithmic_bytes": alg[dominant], "traffic": profiled_traffic(dominant, args.workload)},
         "e2e": {"value": round(2 * n * world / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
-                "h2d_bytes_per_step": 2 * n, "d2h_bytes_per_step": 2 * n},
+                "h2d_bytes_per_step": 2 * n, "d2h_bytes_per_step": 2 * n,
+                "pipeline": "consecutive steps overlap on 3 streams, 2 buffer sets; no L2 flush"},
         "gpu_launches": len(records),
         "clocks": clk,
         "verified": bool(ok),
