@@ -120,6 +120,54 @@ def test_random_bit_flips_match_oracle_verdict(sample):
     assert accepted > 50 and rejected > 50
 
 
+@pytest.fixture(scope="module")
+def dense_sample():
+    """Random bit patterns: nearly every value escapes, so each chunk's escape list (about 12 KB)
+    is larger than the decoder's staging buffer and is checked where it lies in the stream."""
+    x = workloads.random_patterns(2 * 4096 + 50, 91)
+    return x, oracle.compress(x)
+
+
+def test_large_escape_lists_corruptions_are_reported(dense_sample):
+    x, s = dense_sample
+    n = x.size
+    cap = zc.zc_max_compressed_bytes(n)
+    off0, off1 = escape_offset(s, 0), escape_offset(s, 1)
+    assert off1 - off0 > 4096, "the list must exceed the staging buffer"
+    e0 = int(s[7])
+    E = (x[:4096].astype(np.int64) >> 7) & 0xFF
+    k0 = int(((E < e0) | (E > e0 + 6)).sum())
+    assert off1 - off0 == (3 * k0 + 15) // 16 * 16
+    st, vals = gpu_decompress_bytes(s, n, cap)
+    assert st == zc.ZC_OK and np.array_equal(vals, x)
+    muts = {
+        "first_position": (off0, s[off0] ^ 0x01),
+        "last_position": (off0 + 2 * (k0 - 1), s[off0 + 2 * (k0 - 1)] ^ 0x04),
+        "last_exponent_in_window": (off0 + 3 * k0 - 1, e0),
+        "middle_exponent_in_window": (off0 + 2 * k0 + k0 // 2, e0 + 3),
+    }
+    if (3 * k0) % 16:
+        muts["padding"] = (off0 + 3 * k0, 0x01)
+    for name, (pos, val) in muts.items():
+        t = s.copy()
+        t[pos] = np.uint8(val)
+        ost, _ = oracle_status(t, n, cap)
+        assert ost != oracle.OK, f"{name}: the oracle accepts it, the mutation is not a corruption"
+        st, _ = gpu_decompress_bytes(t, n, cap)
+        assert st == zc.ZC_ERR_CORRUPT, f"{name}: status {zc.ERROR_NAMES.get(st, st)}"
+    rng = np.random.default_rng(8)
+    for _ in range(60):  # flips inside the list: the GPU's verdict is the oracle's
+        t = s.copy()
+        pos = int(rng.integers(off0, off1))
+        t[pos] ^= np.uint8(1 << int(rng.integers(0, 8)))
+        ost, ovals = oracle_status(t, n, cap)
+        st, gvals = gpu_decompress_bytes(t, n, cap)
+        if ost == oracle.OK:
+            assert st == zc.ZC_OK and np.array_equal(gvals, ovals), f"flip at {pos}"
+        else:
+            assert st != zc.ZC_OK, f"flip at {pos}: GPU accepts an invalid stream"
+
+
 def test_valid_stream_and_wrong_n(sample):
     x, s = sample
     cap = zc.zc_max_compressed_bytes(N_VALUES)
