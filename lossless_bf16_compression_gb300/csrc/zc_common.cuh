@@ -59,7 +59,7 @@ __host__ __device__ inline uint64_t max_stream_bytes(uint64_t n) {
 //
 // [ws + 0,    ws + 256)            Control block
 // [ws + 256,  ws + 256 + 16 KiB)   per-CTA partials of the statistics pass
-// [ws + 16640, ...)                look-back state, one u64 per chunk
+// [ws + 16640, ...)                scan state, one u64 per chunk
 constexpr int kStatsMaxCtas = 1024;
 constexpr uint64_t kWsControlBytes = 256;
 constexpr uint64_t kWsPartialsBytes = 16ull * kStatsMaxCtas;
@@ -84,7 +84,7 @@ __host__ __device__ constexpr uint64_t workspace_bytes(uint64_t n) {
   return kWsControlBytes + kWsPartialsBytes + 8 * num_chunks(n);
 }
 
-// Look-back state word: bits 62..63 status, bits 0..61 value.
+// Scan state word of a chunk: bits 62..63 status, bits 0..61 value.
 constexpr unsigned long long kFlagAggregate = 1ull << 62;   // value = this chunk's record size
 constexpr unsigned long long kFlagInclusive = 2ull << 62;   // value = sizes up to and including it
 constexpr unsigned long long kFlagValueMask = (1ull << 62) - 1;

@@ -2,7 +2,7 @@
 
 Corrupt streams are made on the host; the decoder must report them through zc_status (and
 agree with the oracle on which streams are invalid) while reading only inside the buffer.
-The look-back wait is made to run out by a chunk that never publishes; the call must report
+The scan's wait is made to run out by a chunk that never publishes; the call must report
 ZC_ERR_TIMEOUT and leave the context usable.  Canary bytes around every buffer must survive.
 """
 import ctypes
@@ -186,7 +186,7 @@ def test_empty_stream():
 
 
 @pytest.mark.parametrize("stalled", [0, 1, 17])
-def test_lookback_wait_is_bounded(stalled):
+def test_scan_wait_is_bounded(stalled):
     x = workloads.sweep(18)  # 64 chunks
     xd = to_device(x)
     cap = zc.zc_max_compressed_bytes(x.size)
