@@ -117,8 +117,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(DecodePara
   const uint8_t* codes = reinterpret_cast<const uint8_t*>(S.fixed);
   const uint8_t* smp = codes + cbytes;
   // A list larger than the staging buffer is read where it lies in the stream (its range was
-  // checked against the offset table and the stream length above).
-  const uint8_t* esc = S.esc_bytes <= kEscSmemBytes ? reinterpret_cast<const uint8_t*>(S.esc) : p.in + S.esc_off;
+  // checked against the offset table and the stream length above).  The two cases keep apart
+  // so that every access has one known state space.
+  const bool staged = S.esc_bytes <= kEscSmemBytes;
+  const uint8_t* esc_s = reinterpret_cast<const uint8_t*>(S.esc);
+  const uint8_t* esc_g = p.in + S.esc_off;
   const uint32_t e0_field = static_cast<uint32_t>(e0) * (128u * 0x00010001u);  // e0 << 7 in both halves
   uint16_t* dst = p.out + first;
 
@@ -164,7 +167,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(DecodePara
   const unsigned k = S.escapes;
   bool corrupt = pad16(3ull * k) != S.esc_bytes;
   if (!corrupt) {
-    const uint16_t* pos_list = reinterpret_cast<const uint16_t*>(esc);
     auto patch = [&](unsigned i, unsigned pos, unsigned E, unsigned prev) {
       const unsigned pb = 3 * pos;
       const unsigned code = pos < m ? ((codes[pb >> 3] | (codes[(pb >> 3) + 1] << 8)) >> (pb & 7)) & 7u : 0u;
@@ -176,9 +178,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(DecodePara
       const unsigned sm = smp[pos];
       dst[pos] = static_cast<uint16_t>(((sm & 0x80u) << 8) | (E << 7) | (sm & 0x7Fu));
     };
-    if (S.esc_bytes <= kEscSmemBytes) {  // staged in shared memory
-      for (unsigned i = tid; i < k; i += kThreads) patch(i, pos_list[i], esc[2 * k + i], i ? pos_list[i - 1] : 0u);
-    } else {  // in the stream: batches of kBatch entries per thread, every load issued first
+    if (staged) {  // in shared memory
+      const uint16_t* pos_list = reinterpret_cast<const uint16_t*>(esc_s);
+      for (unsigned i = tid; i < k; i += kThreads) patch(i, pos_list[i], esc_s[2 * k + i], i ? pos_list[i - 1] : 0u);
+    } else {
+      const uint16_t* pos_list = reinterpret_cast<const uint16_t*>(esc_g);  // in the stream: batches of kBatch entries per thread, every load issued first
       constexpr int kBatch = 4;
       for (unsigned i0 = 0; i0 < k; i0 += kBatch * kThreads) {
         unsigned pv[kBatch], ev[kBatch], qv[kBatch];
@@ -186,7 +190,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(DecodePara
         for (int u = 0; u < kBatch; ++u) {
           const unsigned i = i0 + u * kThreads + tid;
           pv[u] = i < k ? __ldg(pos_list + i) : 0u;
-          ev[u] = i < k ? __ldg(esc + 2 * k + i) : 0u;
+          ev[u] = i < k ? __ldg(esc_g + 2 * k + i) : 0u;
           qv[u] = (i < k && i > 0) ? __ldg(pos_list + i - 1) : 0u;
         }
 #pragma unroll
@@ -200,7 +204,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(DecodePara
 
   // zero padding: the escape list always, code bits and sign|mantissa bytes of a partial chunk
   const unsigned epad = corrupt ? 0u : S.esc_bytes - 3 * k;  // < 16
-  if (tid < epad) corrupt |= esc[3 * k + tid] != 0;
+  if (tid < epad) corrupt |= (staged ? esc_s[3 * k + tid] : __ldg(esc_g + 3 * k + tid)) != 0;
   if (!full) {
     if (tid < smbytes - m) corrupt |= smp[m + tid] != 0;
     const unsigned bit = 3 * m + tid;  // at most 127 padding bits

@@ -91,24 +91,6 @@ __device__ __forceinline__ unsigned compact8(unsigned m) {
   return (m | (m >> 8)) & 0xFFu;
 }
 
-// Shared-memory accesses by 32-bit shared-window address.
-__device__ __forceinline__ void sts_u8(uint32_t a, unsigned v) {
-  asm volatile("st.shared.u8 [%0], %1;" ::"r"(a), "h"(static_cast<unsigned short>(v)) : "memory");
-}
-__device__ __forceinline__ void sts_u16(uint32_t a, unsigned v) {
-  asm volatile("st.shared.u16 [%0], %1;" ::"r"(a), "h"(static_cast<unsigned short>(v)) : "memory");
-}
-__device__ __forceinline__ unsigned lds_u8(uint32_t a) {
-  unsigned short v;
-  asm volatile("ld.shared.u8 %0, [%1];" : "=h"(v) : "r"(a) : "memory");
-  return v;
-}
-__device__ __forceinline__ unsigned lds_u16(uint32_t a) {
-  unsigned short v;
-  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a) : "memory");
-  return v;
-}
-
 __device__ __forceinline__ void bar_coders() { asm volatile("bar.sync 1, %0;" ::"n"(kCoders) : "memory"); }
 
 // Coding thread 0: start the bulk copy of chunk c into stage s (a ragged tail, < 16 bytes, by
