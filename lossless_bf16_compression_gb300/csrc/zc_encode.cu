@@ -345,7 +345,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) encode_kernel(EncodePara
     S.q_retired = 0;
     S.freed = 0;
     S.coders_done = 0;
-    S.e0 = p.base >= 0 ? p.base : __ldcg(&p.ctrl->e0);
   }
   __syncthreads();
   if (warp == kCoders / 32) {  // the retiring warp
@@ -369,6 +368,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) encode_kernel(EncodePara
       }
     }
     next_ticket = atomicAdd(&p.ctrl->encode_ticket, 1u);
+    // e0 last.  In auto mode this kernel may start while the statistics kernel is finishing
+    // (a programmatic dependent launch): the tickets and input copies above do not depend on
+    // it, e0 does, so wait for that kernel's completion and writes first.
+    if (p.base < 0) asm volatile("griddepcontrol.wait;" ::: "memory");
+    S.e0 = p.base >= 0 ? p.base : __ldcg(&p.ctrl->e0);
   }
   bar_coders();
   const int e0 = S.e0;
@@ -571,6 +575,24 @@ cudaError_t launch_encode(const uint16_t* in, uint64_t n, int base, uint8_t* out
   if (grid > p.N + 1) grid = p.N + 1;  // block 0 scans, the others code
   if (grid < 2) grid = 2;
   timing_begin(ZC_KERNEL_ENCODE, stream);
+  if (base < 0) {
+    // After our own statistics kernel: let this kernel start as that one finishes (it reads
+    // e0 only after griddepcontrol.wait).  Not after a caller's kernel, which may still be
+    // writing the input.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t err = cudaLaunchKernelEx(&cfg, encode_kernel, p);
+    timing_end(stream);
+    return err;
+  }
   encode_kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(p);
   timing_end(stream);
   return cudaGetLastError();

@@ -246,6 +246,8 @@ __device__ __noinline__ double exact_sum_of_squares(const uint16_t* x, uint64_t 
 }
 
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) stats_kernel(StatsParams p) {
+  // The encode kernel that follows may start now (it waits for this kernel before it reads e0).
+  asm volatile("griddepcontrol.launch_dependents;");
   __shared__ double red_sum[kWarps];
   __shared__ unsigned long long red_nf[kWarps];
   __shared__ unsigned long long bins[kWarps * 256];
