@@ -246,144 +246,7 @@ __device__ __forceinline__ uint32_t pack_codes8(const uint32_t (&c2)[4]) {
   return v;
 }
 
-// Write a warp's 32 consecutive 24-bit code groups (lane L's group at byte 3 L of `dst`) as 24
-// aligned 32-bit words, skipping words at or past `limit` bytes.  All lanes must call it.
-__device__ __forceinline__ void store_code_groups(uint8_t* dst, uint32_t bits, unsigned limit) {
-  const unsigned lane = threadIdx.x & 31;
-  const unsigned w = lane < 24 ? lane : 23;
-  const unsigned l0 = (4 * w) / 3, off = 32 * w - 24 * l0;  // off in {0, 8, 16}
-  const uint32_t a = __shfl_sync(0xFFFFFFFFu, bits, l0);
-  const uint32_t b = __shfl_sync(0xFFFFFFFFu, bits, l0 + 1);
-  const uint32_t word = (a >> off) | (b << (24 - off));
-  if (lane < 24 && 4 * lane < limit) reinterpret_cast<uint32_t*>(dst)[lane] = word;
-}
-
-// ------------------------------------------------------------------ block scan (128 threads)
-constexpr int kChunkThreads = 128;
-
-// Barrier over the CTA's first 128 threads only (named barrier 1), for kernels that run an
-// extra warp on other work.
-__device__ __forceinline__ void bar_chunk() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
-__device__ __forceinline__ bool bar_chunk_or(bool v) {
-  unsigned r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 q, %1, 0;\n\t"
-      "bar.red.or.pred p, 1, 128, q;\n\tselp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(r)
-      : "r"(static_cast<unsigned>(v))
-      : "memory");
-  return r != 0;
-}
-
-template <bool kNamedBarrier>
-__device__ __forceinline__ unsigned chunk_ranks_impl(const unsigned (&cnt)[4], unsigned (&base)[4],
-                                                     unsigned* scratch) {
-  const unsigned lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  unsigned p0 = cnt[0] | (cnt[1] << 16), p1 = cnt[2] | (cnt[3] << 16);
-  const unsigned own0 = p0, own1 = p1;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const unsigned a = __shfl_up_sync(0xFFFFFFFFu, p0, o);
-    const unsigned b = __shfl_up_sync(0xFFFFFFFFu, p1, o);
-    if (lane >= (unsigned)o) {
-      p0 += a;
-      p1 += b;
-    }
-  }
-  if (lane == 31) {
-    scratch[2 * warp] = p0;
-    scratch[2 * warp + 1] = p1;
-  }
-  if (kNamedBarrier) bar_chunk(); else __syncthreads();
-  const unsigned ex0 = p0 - own0, ex1 = p1 - own1;
-  unsigned before[4] = {0, 0, 0, 0}, total[4] = {0, 0, 0, 0};
-#pragma unroll
-  for (int w = 0; w < kChunkThreads / 32; ++w) {
-    const unsigned s0 = scratch[2 * w], s1 = scratch[2 * w + 1];
-    const unsigned t[4] = {s0 & 0xFFFFu, s0 >> 16, s1 & 0xFFFFu, s1 >> 16};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      total[q] += t[q];
-      if ((unsigned)w < warp) before[q] += t[q];
-    }
-  }
-  const unsigned ex[4] = {ex0 & 0xFFFFu, ex0 >> 16, ex1 & 0xFFFFu, ex1 >> 16};
-  unsigned run = 0;
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    base[q] = run + before[q] + ex[q];
-    run += total[q];
-  }
-  return run;
-}
-
-// kT threads, kS = 4096 / (8 kT) slices: chunk value v = 8 kT q + 8 t + j is held by thread t
-// (q = 0..kS-1, j = 0..7); escapes are ordered by (q, t, j).  Given each thread's per-slice
-// escape counts, return each slice's first rank and the chunk total.  Counts travel two to a
-// word (16-bit fields), so the cross-warp sums are plain adds.  Uses named barrier 1 over the
-// CTA's first kT threads; `scratch` holds kT / 32 * kS / 2 words (a multiple of 4).
-template <int kT>
-__device__ __forceinline__ unsigned chunk_ranks_bar1(const unsigned (&cnt)[kChunk / (8 * kT)],
-                                                     unsigned (&base)[kChunk / (8 * kT)], unsigned* scratch) {
-  constexpr int kS = kChunk / (8 * kT), kP = kS / 2, kW = kT / 32, kWords = kW * kP;
-  static_assert(kS % 2 == 0 && kWords % 4 == 0, "two counters per word, whole 16-byte reads");
-  const unsigned lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  unsigned pk[kP], own[kP];
-#pragma unroll
-  for (int i = 0; i < kP; ++i) own[i] = pk[i] = cnt[2 * i] | (cnt[2 * i + 1] << 16);
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-#pragma unroll
-    for (int i = 0; i < kP; ++i) {
-      const unsigned t = __shfl_up_sync(0xFFFFFFFFu, pk[i], o);
-      if (lane >= (unsigned)o) pk[i] += t;
-    }
-  }
-  if (lane == 31) {
-#pragma unroll
-    for (int i = 0; i < kP; ++i) scratch[kW * i + warp] = pk[i];  // pair-major: [pair][warp]
-  }
-  asm volatile("bar.sync 1, %0;" ::"n"(kT) : "memory");
-  unsigned tot[kP], bef[kP];
-#pragma unroll
-  for (int i = 0; i < kP; ++i) {
-    tot[i] = 0;
-    bef[i] = 0;
-  }
-#pragma unroll
-  for (int v = 0; v < kWords / 4; ++v) {
-    const uint4 t4 = reinterpret_cast<const uint4*>(scratch)[v];
-    const unsigned t[4] = {t4.x, t4.y, t4.z, t4.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int i = (4 * v + e) / kW, w = (4 * v + e) % kW;
-      tot[i] += t[e];
-      bef[i] += (unsigned)w < warp ? t[e] : 0u;
-    }
-  }
-  unsigned run = 0;
-#pragma unroll
-  for (int i = 0; i < kP; ++i) {
-    const unsigned ex = pk[i] - own[i] + bef[i];  // both fields: ranks before this thread, in this warp pair
-    base[2 * i] = run + (ex & 0xFFFFu);
-    run += tot[i] & 0xFFFFu;
-    base[2 * i + 1] = run + (ex >> 16);
-    run += tot[i] >> 16;
-  }
-  return run;
-}
-
-// Chunk value v = 1024 q + 8 t + j is held by thread t (slice q = 0..3, j = 0..7).  In
-// ascending position order the escapes are ordered by (q, t, j).  Given each thread's
-// per-slice counts, return each slice's first rank and the chunk total.  `scratch` holds
-// 8 words of shared memory.  Contains one barrier over the chunk's 128 threads.
-__device__ __forceinline__ unsigned chunk_ranks(const unsigned (&cnt)[4], unsigned (&base)[4], unsigned* scratch) {
-  return chunk_ranks_impl<false>(cnt, base, scratch);
-}
-__device__ __forceinline__ unsigned chunk_ranks_named(const unsigned (&cnt)[4], unsigned (&base)[4],
-                                                      unsigned* scratch) {
-  return chunk_ranks_impl<true>(cnt, base, scratch);
-}
+constexpr int kChunkThreads = 128;  // threads of a decode CTA, one chunk each
 
 // ------------------------------------------------------------------ launchers (host side)
 

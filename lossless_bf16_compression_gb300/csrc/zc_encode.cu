@@ -14,11 +14,12 @@
 // ticket (ticket order = chunk order).  Inputs (8 KiB per chunk) arrive by bulk async copies
 // (TMA engine, mbarrier completion) into two stages, so the next chunk's copy is in flight
 // while a chunk is coded (deeper pipelines measured slower: every stage holds a ticket, and
-// held tickets lengthen the tail); a coding thread holds 4 slices of 8 values and codes two
-// values per 32-bit word with packed 16-bit arithmetic.  The fixed part of
-// a chunk has a place that follows from n, so it goes straight from registers to HBM: 8-byte
-// stores of sign|mantissa bytes and, per warp, 24 coalesced 32-bit words of codes assembled
-// with two shuffles.  Only the escape list waits for the device-wide scan: each chunk publishes
+// held tickets lengthen the tail); a coding thread holds 32 consecutive values and codes two
+// values per 32-bit word with packed 16-bit arithmetic.  The fixed part of a chunk has a place
+// that follows from n, so it goes straight from registers to HBM: per thread two 16-byte
+// stores of sign|mantissa bytes and three 32-bit words of codes.  Holding consecutive values
+// makes a thread's escapes consecutive in the list, so each thread writes its own with one
+// bit scan, two stores and one load per escape.  Only the escape list waits for the device-wide scan: each chunk publishes
 // its list size in a per-chunk state word as soon as its escape count is known, and the
 // scanner's four warps walk the state words in order, 1024 per round trip, turning every run
 // of published sizes into inclusive offsets (a chained scan with one scanning block, after
@@ -31,16 +32,15 @@
 namespace zc {
 namespace {
 
-constexpr int kCoders = 128;               // coding threads
-constexpr int kSlices = kChunk / (8 * kCoders);  // slices of 8 values per coding thread
+constexpr int kCoders = 128;               // coding threads, 32 values each
+static_assert(32 * kCoders == kChunk, "a coding thread holds 32 consecutive values");
 constexpr int kThreads = kCoders + 32;     // + the retiring warp (the scanner in block 0)
 constexpr int kCtasPerSm = 5;
 constexpr int kStages = 2;                 // input chunks in flight per CTA
 constexpr unsigned kInBytes = 2 * kChunk;
 constexpr unsigned kRingBytes = 24 * 1024; // escape-list ring per CTA (two worst-case lists)
 constexpr unsigned kQueue = 64;            // escape lists waiting, at most
-constexpr unsigned kCombinedMax = 16;      // escapes per lane from which a warp writes them together
-static_assert(kSlices == 4, "the combined escape mask holds four slices of 8");
+constexpr unsigned kDenseMin = 16;         // escapes per lane from which a warp takes the dense loop
 constexpr unsigned kWaitLimit = 1u << 22;  // mbarrier polls before giving up
 constexpr int kScanPerLane = 8;            // state words per scanner lane per round trip
 constexpr int kCoderWarps = kCoders / 32;
@@ -73,10 +73,7 @@ struct __align__(128) EncodeSmem {
   volatile unsigned q_retired;  // entries written out and read back from the ring (consumer)
   volatile unsigned freed;      // ring bytes given back, gaps included (consumer)
   volatile int coders_done;     // no more entries will come
-  __align__(16) unsigned scan[kCoders / 32 * kSlices / 2];
-  // Per coding warp: the warp's escapes of one slice in rank order, each as its value's offset in
-  // the warp's 256 values of that slice.
-  uint8_t esc_at[kCoderWarps][256];
+  __align__(16) unsigned scan[kCoderWarps];  // per coding warp: its escape count
   // scanner (block 0): per round parity, each warp's ready count and sum, and the status word
   unsigned long long scan_sum[2][kCoderWarps];
   unsigned scan_ready[2][kCoderWarps];
@@ -92,6 +89,33 @@ __device__ __forceinline__ unsigned compact8(unsigned m) {
 }
 
 __device__ __forceinline__ void bar_coders() { asm volatile("bar.sync 1, %0;" ::"n"(kCoders) : "memory"); }
+
+// Index of the highest set bit of a nonzero word.
+__device__ __forceinline__ unsigned msb_index(unsigned x) {
+  unsigned b;
+  asm("bfind.u32 %0, %1;" : "=r"(b) : "r"(x));
+  return b;
+}
+
+// The coding threads' escape counts in thread order (= position order): this thread's first
+// rank (the exclusive prefix) and the chunk total.  One barrier over the coding threads [R];
+// `scratch` holds one word per coding warp, read as one 16-byte word.
+__device__ __forceinline__ unsigned chunk_rank(unsigned cnt, unsigned* first, unsigned* scratch) {
+  static_assert(kCoderWarps == 4, "one 16-byte read of the warp totals");
+  const unsigned lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  unsigned x = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned t = __shfl_up_sync(0xFFFFFFFFu, x, o);
+    if (lane >= static_cast<unsigned>(o)) x += t;
+  }
+  if (lane == 31) scratch[warp] = x;
+  bar_coders();
+  const uint4 tw = *reinterpret_cast<const uint4*>(scratch);
+  const unsigned before = (warp > 0 ? tw.x : 0u) + (warp > 1 ? tw.y : 0u) + (warp > 2 ? tw.z : 0u);
+  *first = before + x - cnt;
+  return tw.x + tw.y + tw.z + tw.w;
+}
 
 // Coding thread 0: start the bulk copy of chunk c into stage s (a ragged tail, < 16 bytes, by
 // plain loads).
@@ -335,7 +359,7 @@ __device__ __forceinline__ bool bar_coders_or(bool v) {
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) encode_kernel(EncodeParams p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   EncodeSmem& S = *reinterpret_cast<EncodeSmem*>(smem_raw);
-  const unsigned tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const unsigned tid = threadIdx.x, warp = tid >> 5;
   if (blockIdx.x == 0) {  // block 0: the scanner
     if (warp < kCoderWarps) scanner(S, p.flags, p.N, p.status, p.spin_limit);
     return;
@@ -399,34 +423,46 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) encode_kernel(EncodePara
     const unsigned smbytes = full ? kChunk : static_cast<unsigned>(pad16(m));
     uint8_t* fixed = p.out + R0 + c * static_cast<uint64_t>(kFullFixedBytes);
 
-    unsigned cnt[kSlices], msk[kSlices];
+    // Thread t codes values 32t .. 32t+31, four groups of 8: its codes are the 12 bytes at 12t
+    // of the code section, its sign|mantissa bytes the 32 at 32t of the plane, and its escapes
+    // take consecutive ranks.
+    const unsigned v0 = 32 * tid;
+    uint32_t g[4];     // 24-bit code groups
+    uint32_t sm[8];    // sign|mantissa bytes, four per word
+    unsigned m32 = 0;  // escape flags: bit b for value v0 + b
 #pragma unroll
-    for (int q = 0; q < kSlices; ++q) {
-      const uint4 xv = S.xin[s][kCoders * q + tid];
+    for (int q = 0; q < 4; ++q) {
+      const uint4 xv = S.xin[s][4 * tid + q];
       uint32_t w[4] = {xv.x, xv.y, xv.z, xv.w};
-      const unsigned v0 = 8 * kCoders * q + 8 * tid;
       uint32_t c2[4];
 #pragma unroll
       for (int i = 0; i < 4; ++i) c2[i] = codes_x2(w[i], neg_e0x2);
       if (!full) {  // values past m: code 0, byte 0, no escape
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const uint32_t keep = (v0 + 2 * i < m ? 0x0000FFFFu : 0u) | (v0 + 2 * i + 1 < m ? 0xFFFF0000u : 0u);
+          const unsigned v = v0 + 8 * q + 2 * i;
+          const uint32_t keep = (v < m ? 0x0000FFFFu : 0u) | (v + 1 < m ? 0xFFFF0000u : 0u);
           c2[i] &= keep;
           w[i] &= keep;
         }
       }
-      const uint2 smv = make_uint2(sign_mantissa_x4(w[0], w[1]), sign_mantissa_x4(w[2], w[3]));
-      if (full || v0 < smbytes) *reinterpret_cast<uint2*>(fixed + cbytes + v0) = smv;
-      const uint32_t bits = pack_codes8(c2);
-      const unsigned wbase = 3 * (kCoders * q + 32 * warp);  // this warp's 96 code bytes
-      store_code_groups(fixed + wbase, bits, cbytes > wbase ? cbytes - wbase : 0);
-      msk[q] = bits & (bits >> 1) & (bits >> 2) & 0x249249u;  // code 7: bit 3j for value j
-      cnt[q] = __popc(msk[q]);
+      sm[2 * q] = sign_mantissa_x4(w[0], w[1]);
+      sm[2 * q + 1] = sign_mantissa_x4(w[2], w[3]);
+      g[q] = pack_codes8(c2);
+      m32 |= compact8(g[q] & (g[q] >> 1) & (g[q] >> 2) & 0x249249u) << (8 * q);  // code 7
     }
+    uint8_t* const smp = fixed + cbytes + v0;
+    if (full || v0 < smbytes) *reinterpret_cast<uint4*>(smp) = make_uint4(sm[0], sm[1], sm[2], sm[3]);
+    if (full || v0 + 16 < smbytes) *reinterpret_cast<uint4*>(smp + 16) = make_uint4(sm[4], sm[5], sm[6], sm[7]);
+    const uint32_t cw[3] = {g[0] | (g[1] << 24), (g[1] >> 8) | (g[2] << 16), (g[2] >> 16) | (g[3] << 8)};
+    uint32_t* const cp = reinterpret_cast<uint32_t*>(fixed + 12 * tid);
+#pragma unroll
+    for (int i = 0; i < 3; ++i)
+      if (full || 12 * tid + 4 * i < cbytes) cp[i] = cw[i];
+    const unsigned cnt = __popc(m32);
 
-    unsigned base[kSlices];
-    const unsigned k = chunk_ranks_bar1<kCoders>(cnt, base, S.scan);
+    unsigned base;
+    const unsigned k = chunk_rank(cnt, &base, S.scan);  // [R]
     const unsigned esc_bytes = static_cast<unsigned>(pad16(3ull * k));
     // The list's place in the ring: every coding thread works it out from its own copy of the
     // ring state and waits (bounded) for the room itself, so no barrier is needed before the
@@ -439,57 +475,36 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) encode_kernel(EncodePara
     R.made += gap + esc_bytes;
     R.head = where + esc_bytes;
     if (!__any_sync(0xFFFFFFFFu, stop)) {  // positions and exponents, in rank order
-      // Two ways to write a warp's escapes, chosen by the most escapes any of its lanes holds
-      // over all its slices (M).  Sparse (M < kCombinedMax): each lane walks one mask of all its
-      // slices, M passes in all.  Dense, per slice: each lane enters its escapes' offsets (within
-      // the warp's 256 values of the slice) in the warp's table, a short loop with no loads;
-      // then lane x writes the warp's x-th escape, so one pass covers 32 escapes with
-      // consecutive stores.  Shared memory is addressed with 32-bit shared-window addresses.
+      // Each thread writes its own escapes; the exponent is read back from the staged input.
+      // Shared memory is addressed with 32-bit shared-window addresses.
       const uint32_t esc = smem_u32(S.ring) + where;
-      const uint32_t xin = smem_u32(S.xin[s]);
-      unsigned mine = 0;
-#pragma unroll
-      for (int q = 0; q < kSlices; ++q) mine += cnt[q];
-      if (__reduce_max_sync(0xFFFFFFFFu, mine) < kCombinedMax) {
-        unsigned m32 = 0, adj[kSlices], before = 0;  // rank of a lane's t-th escape: adj[q] + t
-#pragma unroll
-        for (int q = 0; q < kSlices; ++q) {
-          m32 |= compact8(msk[q]) << (8 * q);
-          adj[q] = base[q] - before;
-          before += cnt[q];
-        }
-        unsigned t = 0;
-        while (m32) {
-          const unsigned b = __ffs(m32) - 1;
-          m32 &= m32 - 1;
-          const unsigned q = b >> 3;
-          const unsigned pos = 8 * kCoders * q + 8 * tid + (b & 7);
-          const unsigned r = pick4(adj, q) + t++;
-          sts_u16(esc + 2 * r, pos);
-          sts_u8(esc + 2 * k + r, lds_u16(xin + 2 * pos) >> 7);
+      const uint32_t xv = smem_u32(&S.xin[s][4 * tid]);
+      if (__reduce_max_sync(0xFFFFFFFFu, cnt) < kDenseMin) {
+        // Highest value first: ranks base + cnt - 1 down to base.
+        uint32_t at16 = esc + 2 * (base + cnt), at8 = esc + 2 * k + base + cnt;  // one past the last
+        unsigned mm = m32;
+        while (mm) {
+          const unsigned b = msb_index(mm);
+          mm ^= 1u << b;
+          at16 -= 2;
+          at8 -= 1;
+          sts_u16(at16, v0 + b);
+          sts_u8(at8, lds_u16(xv + 2 * b) >> 7);
         }
       } else {
-#pragma unroll
-        for (int q = 0; q < kSlices; ++q) {
-          const unsigned first = 8 * kCoders * q + 256 * warp;  // the warp's values in slice q
-          unsigned mk = msk[q];
-          const unsigned wfirst = __shfl_sync(0xFFFFFFFFu, base[q], 0);  // lane 0: the warp's first rank
-          const unsigned wcnt = __shfl_sync(0xFFFFFFFFu, base[q] + cnt[q], 31) - wfirst;
-          const uint32_t at = smem_u32(&S.esc_at[warp][0]);
-          unsigned r = base[q] - wfirst;
-          while (mk) {
-            const unsigned j = ((__ffs(mk) - 1) * 11u) >> 5;  // bit 3j -> j, exact for j < 8
-            mk &= mk - 1;
-            sts_u8(at + r++, 8 * lane + j);
-          }
-          __syncwarp();
-          for (unsigned x = lane; x < wcnt; x += 32) {
-            const unsigned pos = first + lds_u8(at + x);
-            const unsigned rr = wfirst + x;
-            sts_u16(esc + 2 * rr, pos);
-            sts_u8(esc + 2 * k + rr, lds_u16(xin + 2 * pos) >> 7);
-          }
-          __syncwarp();  // the table is reused by the next slice
+        // Dense: in the loop above the lanes' values and ranks would lie 32 apart and meet in
+        // the same shared-memory banks.  So lane L takes its escapes from value L - 1 downwards
+        // (modulo 32), its flags rotated right by L, and ranks each one by counting its flags
+        // below it.
+        const unsigned rot = tid & 31;
+        unsigned mm = __funnelshift_r(m32, m32, rot);  // value b at bit (b - rot) mod 32
+        while (mm) {
+          const unsigned bp = msb_index(mm);
+          mm ^= 1u << bp;
+          const unsigned b = (bp + rot) & 31;
+          const unsigned r = base + __popc(m32 & ((1u << b) - 1u));
+          sts_u16(esc + 2 * r, v0 + b);
+          sts_u8(esc + 2 * k + r, lds_u16(xv + 2 * b) >> 7);
         }
       }
       if (tid < esc_bytes - 3 * k) sts_u8(esc + 3 * k + tid, 0);  // zero padding, < 16 bytes
