@@ -1,5 +1,5 @@
-// zc_common.cuh -- layout arithmetic, workspace, PTX wrappers and the block scan shared by the
-// sm_103a kernels of the lossless BF16 exponent codec.
+// zc_common.cuh -- layout arithmetic, workspace, PTX wrappers and value-level helpers shared by
+// the sm_103a kernels of the lossless BF16 exponent codec.
 //
 // Method: ZipCCL (SIGCOMM scribe notes), "Key idea and contribution": exponent coding with a
 // window taken from the standard deviation (first technique) and GPU kernels with a

@@ -11,15 +11,17 @@
 // block has four coding warps and one retiring warp, so that each chunk's fixed costs (waits,
 // ranks, barriers) are paid by 128 threads and five chunks are in flight per SM (measured
 // faster than eight coding warps at four CTAs per SM).  Chunks are handed out by an atomic
-// ticket (ticket order = chunk order).  Inputs (8 KiB per chunk) arrive by bulk async copies
-// (TMA engine, mbarrier completion) into two stages, so the next chunk's copy is in flight
-// while a chunk is coded (deeper pipelines measured slower: every stage holds a ticket, and
-// held tickets lengthen the tail); a coding thread holds 32 consecutive values and codes two
-// values per 32-bit word with packed 16-bit arithmetic.  The fixed part of a chunk has a place
-// that follows from n, so it goes straight from registers to HBM: per thread two 16-byte
-// stores of sign|mantissa bytes and three 32-bit words of codes.  Holding consecutive values
-// makes a thread's escapes consecutive in the list, so each thread writes its own with one
-// bit scan, two stores and one load per escape.  Only the escape list waits for the device-wide scan: each chunk publishes
+// ticket (ticket order = chunk order).  Inputs (8 KiB per chunk) arrive by tiled async copies
+// (TMA engine, one box of a tensor map per chunk, mbarrier completion) into two stages, so the
+// next chunk's copy is in flight while a chunk is coded (deeper pipelines measured slower:
+// every stage holds a ticket, and held tickets lengthen the tail).  A coding thread holds 32
+// consecutive values and codes two values per 32-bit word with packed 16-bit arithmetic; the
+// copies use the 128-byte swizzle, so its four 16-byte reads of its own 64 bytes are free of
+// bank conflicts.  The fixed part of a chunk has a place that follows from n, so it goes
+// straight from registers to HBM: per thread two 16-byte stores of sign|mantissa bytes and
+// three 32-bit words of codes.  Holding consecutive values makes a thread's escapes
+// consecutive in the list, so each thread writes its own with one bit scan, two stores and one
+// load per escape.  Only the escape list waits for the device-wide scan: each chunk publishes
 // its list size in a per-chunk state word as soon as its escape count is known, and the
 // scanner's four warps walk the state words in order, 1024 per round trip, turning every run
 // of published sizes into inclusive offsets (a chained scan with one scanning block, after
@@ -27,6 +29,12 @@
 // where a waiting list costs only its own bytes; the retiring warp polls up to 32 waiting lists
 // per round trip and copies resolved ones out with 16-byte stores, so coding never waits for
 // the scan unless the ring is full.  Every wait is bounded.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cstring>
+#include <mutex>
+
 #include "zc_common.cuh"
 
 namespace zc {
@@ -58,6 +66,7 @@ struct EncodeParams {
   int* status;
   uint64_t stall_chunk;
   unsigned spin_limit;
+  uint64_t full_chunks;  // n / 4096: chunks that come by one tiled copy each
 };
 
 struct __align__(128) EncodeSmem {
@@ -117,18 +126,19 @@ __device__ __forceinline__ unsigned chunk_rank(unsigned cnt, unsigned* first, un
   return tw.x + tw.y + tw.z + tw.w;
 }
 
-// Coding thread 0: start the bulk copy of chunk c into stage s (a ragged tail, < 16 bytes, by
-// plain loads).
-__device__ void issue_load(EncodeSmem& S, int s, uint64_t c, const EncodeParams& p) {
-  const uint64_t first = c * kChunk;
-  const unsigned m = chunk_values(p.n, c);
-  const unsigned bytes = 2 * m, bulk = bytes & ~15u;
-  uint8_t* dst = reinterpret_cast<uint8_t*>(S.xin[s]);
-  for (unsigned b = bulk; b < bytes; b += 2) *reinterpret_cast<uint16_t*>(dst + b) = p.in[first + b / 2];
-  if (bulk) {
-    fence_proxy_async_smem();
-    mbar_arrive_expect_tx(&S.mbar[s], bulk);
-    bulk_load(dst, p.in + first, bulk, &S.mbar[s]);
+// Coding thread 0: start the copy of chunk c into stage s.  A full chunk is one box of the
+// input's tensor map, written to shared memory with the 128-byte swizzle (16-byte unit u of
+// 128-byte row r lands at unit u ^ (r % 8)), so that each coding thread's four 16-byte reads of
+// its own 64 bytes meet no bank twice.  The ragged last chunk comes without a copy: every coding
+// thread fetches its own values.
+__device__ void issue_load(EncodeSmem& S, int s, uint64_t c, const EncodeParams& p, const CUtensorMap* map) {
+  if (c < p.full_chunks) {
+    mbar_arrive_expect_tx(&S.mbar[s], kInBytes);
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+        "[%5];" ::"r"(smem_u32(S.xin[s])),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(0), "r"(static_cast<int>(c)), "r"(smem_u32(&S.mbar[s]))
+        : "memory");
   } else {
     mbar_arrive(&S.mbar[s]);
   }
@@ -356,9 +366,11 @@ __device__ __forceinline__ bool bar_coders_or(bool v) {
   return r != 0;
 }
 
-__global__ void __launch_bounds__(kThreads, kCtasPerSm) encode_kernel(EncodeParams p) {
-  extern __shared__ __align__(128) unsigned char smem_raw[];
-  EncodeSmem& S = *reinterpret_cast<EncodeSmem*>(smem_raw);
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
+    encode_kernel(const EncodeParams p, const __grid_constant__ CUtensorMap in_map) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  // The stages start on a 1024-byte boundary of the shared window (the period of the swizzle).
+  EncodeSmem& S = *reinterpret_cast<EncodeSmem*>(smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
   const unsigned tid = threadIdx.x, warp = tid >> 5;
   if (blockIdx.x == 0) {  // block 0: the scanner
     if (warp < kCoderWarps) scanner(S, p.flags, p.N, p.status, p.spin_limit);
@@ -387,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) encode_kernel(EncodePara
       const unsigned c = atomicAdd(&p.ctrl->encode_ticket, 1u);
       S.ticket[s] = c;
       if (c < p.N) {
-        issue_load(S, s, c, p);
+        issue_load(S, s, c, p, &in_map);
         pending |= 1u << s;
       }
     }
@@ -402,6 +414,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) encode_kernel(EncodePara
   const int e0 = S.e0;
   const uint32_t neg_e0x2 = ((0x10000u - static_cast<unsigned>(e0)) & 0xFFFFu) * 0x00010001u;
   const uint64_t R0 = records_base(p.n);
+  // This thread's 64 bytes in a stage: logical 16-byte unit q (values v0 + 8q ..) of row tid / 2
+  // sits at byte offset sw ^ 16q.
+  const unsigned sw = 128 * (tid >> 1) + 16 * ((4 * (tid & 1)) ^ ((tid >> 1) & 7));
 
   for (unsigned it = 0;; ++it) {
     const int s = it % kStages;
@@ -427,12 +442,25 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) encode_kernel(EncodePara
     // of the code section, its sign|mantissa bytes the 32 at 32t of the plane, and its escapes
     // take consecutive ranks.
     const unsigned v0 = 32 * tid;
+    if (!full) {  // the ragged last chunk came without a copy: fetch this thread's values
+      const uint16_t* src = p.in + c * kChunk;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint32_t w4[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const unsigned v = v0 + 8 * q + 2 * i;
+          w4[i] = (v < m ? static_cast<uint32_t>(src[v]) : 0u) | (v + 1 < m ? static_cast<uint32_t>(src[v + 1]) << 16 : 0u);
+        }
+        S.xin[s][(sw ^ (16 * q)) / 16] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+      }
+    }
     uint32_t g[4];     // 24-bit code groups
     uint32_t sm[8];    // sign|mantissa bytes, four per word
     unsigned m32 = 0;  // escape flags: bit b for value v0 + b
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
-      const uint4 xv = S.xin[s][4 * tid + q];
+      const uint4 xv = S.xin[s][(sw ^ (16 * q)) / 16];
       uint32_t w[4] = {xv.x, xv.y, xv.z, xv.w};
       uint32_t c2[4];
 #pragma unroll
@@ -478,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) encode_kernel(EncodePara
       // Each thread writes its own escapes; the exponent is read back from the staged input.
       // Shared memory is addressed with 32-bit shared-window addresses.
       const uint32_t esc = smem_u32(S.ring) + where;
-      const uint32_t xv = smem_u32(&S.xin[s][4 * tid]);
+      const uint32_t xs = smem_u32(S.xin[s]);  // value v0 + b at byte xs + (sw ^ (2b & 0x3E))
       if (__reduce_max_sync(0xFFFFFFFFu, cnt) < kDenseMin) {
         // Highest value first: ranks base + cnt - 1 down to base.
         uint32_t at16 = esc + 2 * (base + cnt), at8 = esc + 2 * k + base + cnt;  // one past the last
@@ -489,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) encode_kernel(EncodePara
           at16 -= 2;
           at8 -= 1;
           sts_u16(at16, v0 + b);
-          sts_u8(at8, lds_u16(xv + 2 * b) >> 7);
+          sts_u8(at8, lds_u16(xs + (sw ^ ((2 * b) & 0x3Eu))) >> 7);
         }
       } else {
         // Dense: in the loop above the lanes' values and ranks would lie 32 apart and meet in
@@ -504,7 +532,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) encode_kernel(EncodePara
           const unsigned b = (bp + rot) & 31;
           const unsigned r = base + __popc(m32 & ((1u << b) - 1u));
           sts_u16(esc + 2 * r, v0 + b);
-          sts_u8(esc + 2 * k + r, lds_u16(xv + 2 * b) >> 7);
+          sts_u8(esc + 2 * k + r, lds_u16(xs + (sw ^ ((2 * b) & 0x3Eu))) >> 7);
         }
       }
       if (tid < esc_bytes - 3 * k) sts_u8(esc + 3 * k + tid, 0);  // zero padding, < 16 bytes
@@ -523,7 +551,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) encode_kernel(EncodePara
       // after it is taken now and used a chunk later.
       S.ticket[s] = next_ticket;
       if (next_ticket < p.N) {
-        issue_load(S, s, next_ticket, p);
+        issue_load(S, s, next_ticket, p, &in_map);
         pending |= 1u << s;
         next_ticket = atomicAdd(&p.ctrl->encode_ticket, 1u);
       }
@@ -552,10 +580,50 @@ __global__ void empty_stream_kernel(uint8_t* out, int base, Control* ctrl, unsig
   if (out_bytes) *out_bytes = 48;
 }
 
+// Dynamic shared memory of the encode kernel: the layout plus room to align it to 1024 bytes.
+constexpr int kEncodeSmemBytes = static_cast<int>(sizeof(EncodeSmem)) + 1024;
+static_assert(kEncodeSmemBytes <= 233472 / kCtasPerSm - 1024, "kCtasPerSm CTAs fit an SM's shared memory");
+
+// The driver's tensor-map encoder, looked up once through the runtime (so the library needs no
+// link to the driver library).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+// The input's full chunks as a 3-D tensor of u16, {64, 64, n / 4096} (a chunk is 64 rows of 128
+// bytes), one chunk per box, written to shared memory with the 128-byte swizzle.  With no full
+// chunk the map is left zeroed and never used.
+cudaError_t input_map(const uint16_t* in, uint64_t n, CUtensorMap* map) {
+  std::memset(map, 0, sizeof *map);
+  const uint64_t full = n / kChunk;
+  if (full == 0) return cudaSuccess;
+  const PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (encode == nullptr) return cudaErrorNotSupported;
+  const cuuint64_t dims[3] = {64, 64, full};
+  const cuuint64_t strides[2] = {128, 2 * kChunk};  // bytes, of dimensions 1 and 2
+  const cuuint32_t box[3] = {64, 64, 1};
+  const cuuint32_t unit[3] = {1, 1, 1};
+  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<uint16_t*>(in), dims, strides, box,
+                            unit, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 }  // namespace
 
 cudaError_t encode_occupancy(int* per_sm) {
-  const int smem = static_cast<int>(sizeof(EncodeSmem));
+  const int smem = kEncodeSmemBytes;
   cudaError_t err = cudaFuncSetAttribute(encode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, encode_kernel, kThreads, smem);
@@ -570,7 +638,6 @@ cudaError_t launch_encode(const uint16_t* in, uint64_t n, int base, uint8_t* out
     empty_stream_kernel<<<1, 1, 0, stream>>>(out, base, ctrl, out_bytes);
     return cudaGetLastError();
   }
-  static_assert(sizeof(EncodeSmem) <= 227 * 1024, "shared memory");
   EncodeParams p;
   p.in = in;
   p.n = n;
@@ -583,8 +650,12 @@ cudaError_t launch_encode(const uint16_t* in, uint64_t n, int base, uint8_t* out
   p.status = dev.status;
   p.stall_chunk = stall_chunk;
   p.spin_limit = spin_limit;
+  p.full_chunks = n / kChunk;
+  CUtensorMap map;
+  cudaError_t err = input_map(in, n, &map);
+  if (err != cudaSuccess) return err;
 
-  const int smem = static_cast<int>(sizeof(EncodeSmem));
+  const int smem = kEncodeSmemBytes;
   const int per_sm = dev.encode_per_sm;
   uint64_t grid = static_cast<uint64_t>(per_sm > 0 ? per_sm : 1) * dev.sm_count;
   if (grid > p.N + 1) grid = p.N + 1;  // block 0 scans, the others code
@@ -604,11 +675,11 @@ cudaError_t launch_encode(const uint16_t* in, uint64_t n, int base, uint8_t* out
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t err = cudaLaunchKernelEx(&cfg, encode_kernel, p);
+    err = cudaLaunchKernelEx(&cfg, encode_kernel, p, map);
     timing_end(stream);
     return err;
   }
-  encode_kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(p);
+  encode_kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(p, map);
   timing_end(stream);
   return cudaGetLastError();
 }
@@ -633,13 +704,17 @@ cudaError_t launch_encode_ws(const uint16_t* in, uint64_t n, int base, uint8_t* 
   p.status = dev.status;
   p.stall_chunk = ~uint64_t(0);
   p.spin_limit = 1u << 20;
-  const int smem = static_cast<int>(sizeof(EncodeSmem));
+  p.full_chunks = n / kChunk;
+  CUtensorMap map;
+  const cudaError_t err = input_map(in, n, &map);
+  if (err != cudaSuccess) return err;
+  const int smem = kEncodeSmemBytes;
   const int per_sm = dev.encode_per_sm;
   uint64_t grid = static_cast<uint64_t>(per_sm > 0 ? per_sm : 1) * dev.sm_count;
   if (grid > p.N + 1) grid = p.N + 1;  // block 0 scans, the others code
   if (grid < 2) grid = 2;
   timing_begin(ZC_KERNEL_ENCODE, stream);
-  encode_kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(p);
+  encode_kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(p, map);
   timing_end(stream);
   return cudaGetLastError();
 }
