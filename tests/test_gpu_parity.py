@@ -150,6 +150,29 @@ def test_deterministic_and_concurrent_streams():
         assert out[:total].cpu().numpy().tobytes() == oracle.compress(x).tobytes()
 
 
+@pytest.mark.parametrize("n", [4095, 3 * 4096, 3 * 4096 + 5])
+def test_buffers_at_16_byte_offsets(n):
+    """Input, stream and output buffers that start 16 bytes past an allocation's start (the
+    alignment the C ABI asks for, below what the caching allocator hands out)."""
+    x = mixed(n, 70 + n)
+    pad = np.zeros(8, dtype=np.uint16)
+    xd = to_device(np.concatenate([pad, x]))[8:]
+    assert xd.data_ptr() % 256 == 16
+    cap = zc.zc_max_compressed_bytes(n)
+    out_all = torch.zeros(cap + 16, dtype=torch.uint8, device="cuda")
+    out = out_all[16:]
+    zc.status(reset=True)
+    _, ob = zc.compress(xd, out=out)
+    total = int(ob.item())
+    assert zc.status(reset=True) == zc.ZC_OK
+    assert out[:total].cpu().numpy().tobytes() == oracle.compress(x).tobytes()
+    back_all = torch.zeros(n + 8, dtype=torch.int16, device="cuda")
+    zc.decompress(out, n, out=back_all[8:])
+    assert zc.status(reset=True) == zc.ZC_OK
+    assert np.array_equal(back_all[8:].cpu().numpy().view(np.uint16), x)
+    assert not back_all[:8].any()
+
+
 def test_out_bytes_in_host_memory():
     import ctypes
 
