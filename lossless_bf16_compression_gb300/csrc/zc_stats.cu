@@ -9,10 +9,11 @@
 //
 // GB300 design.  The pass is HBM-bound (it reads 2n bytes), and GB300's fp64 rate is far below
 // what one fp64 operation per value would need, so values are summed in fp32 blocks of 64 with
-// four FFMA chains, and only block sums go to fp64.  A block whose plain fp32 sum leaves the
-// safe range is redone with its values scaled by a power of two from its largest magnitude,
-// so no bit pattern of the BF16 range overflows or loses the block's sum to underflow; only
-// blocks holding Inf or NaN take a careful path that skips them.  Every block sum carries a relative error below 2^-18 (at most 17 roundings, or
+// four FFMA chains, and only block sums go to fp64.  Each block's largest magnitude decides
+// whether its plain fp32 sum is safe; when a lane's is not, its warp sums with every value
+// scaled by a power of two from that magnitude (1 in lanes that need none), so no bit pattern
+// of the BF16 range overflows or loses the block's sum to underflow and the warp runs one
+// loop; only blocks holding Inf or NaN take a careful path that skips them.  Every block sum carries a relative error below 2^-18 (at most 17 roundings, or
 // 64 on the careful path), so the grid total S_est
 // satisfies |S_est - S| < 2^-17 S.  The last CTA evaluates the rule at S_est (1 -+ 2^-16),
 // rounded outward; when both ends give the same e0 (all but ~4e-5 of random tensors) that e0
@@ -99,14 +100,10 @@ __device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
   return d;
 }
 
-// A block whose plain fp32 sum may have overflowed, lost precision to underflow or met Inf/NaN,
-// reloaded from memory (so that the fast path's registers need not survive the call).  Every
-// value is scaled by a power of two taken from the block's largest magnitude, so that no square
-// overflows and the largest lies in [2^-16, 16).  Bit patterns with the sign cleared order like
-// magnitudes, so one packed 16-bit max finds the largest.  Blocks holding Inf or NaN take the
-// careful path.
-__device__ __noinline__ double scaled_block_at(const uint4* in, uint64_t wb, uint64_t nv, unsigned lane,
-                                               unsigned* nonfinite) {
+// A block holding Inf or NaN, reloaded from memory (so that the fast path's registers need not
+// survive the call) and summed by the careful path.
+__device__ __noinline__ double careful_block_at(const uint4* in, uint64_t wb, uint64_t nv, unsigned lane,
+                                                unsigned* nonfinite) {
   uint32_t w[32];
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
@@ -117,20 +114,46 @@ __device__ __noinline__ double scaled_block_at(const uint4* in, uint64_t wb, uin
     w[4 * j + 2] = v.z;
     w[4 * j + 3] = v.w;
   }
+  return careful_block(w, nonfinite);
+}
+
+// Block sum of 64 values.  Bit patterns with the sign cleared order like magnitudes, so one
+// packed 16-bit max finds the block's largest, and it decides, per warp, between the plain sum
+// (every lane's largest biased exponent in [87, 187): no square reaches 2^122 and the block sum
+// is at least 2^-80, so the 64 squares, 17 roundings, stay within 2^-19 of the exact sum) and a
+// sum with every lane's values scaled by 2^(126 - Es), Es = E clamped to [1, 252] (1 for lanes
+// that need no scaling), which puts the largest magnitude in [2^-8, 4): no square overflows and
+// what underflows is under 2^-120 of the block sum.  The decision is one warp vote, so a warp runs one of the two loops.
+// Blocks holding Inf or NaN take the careful path.
+__device__ __forceinline__ void block_sum(const uint32_t (&w)[32], const uint4* in, uint64_t wb, uint64_t nv,
+                                          unsigned lane, double* acc, unsigned* nonfinite) {
   uint32_t mx = 0;
 #pragma unroll
   for (int i = 0; i < 32; ++i) mx = max_u16x2(mx, w[i] & 0x7FFF7FFFu);
   const unsigned m = max(mx & 0xFFFFu, mx >> 16);
-  if (m >= 0x7F80u) return careful_block(w, nonfinite);  // Inf or NaN in the block
-  if (m == 0) return 0.0;                                  // zeros only
-  // The largest value lies in [2^(E-127), 2^(E-126)), E its biased exponent (1 for subnormals,
-  // whose largest is at least 2^-133).  Scale by 2^(126-Es), Es = min(E, 252), a normal float:
-  // the scaled values stay below 4 and the largest is at least 2^-8.  A scaled value loses bits
-  // only below 2^-142, so every square the sum keeps is exact, and what underflows is under
-  // 2^-120 of the block sum.
-  const int Es = min(max(static_cast<int>(m >> 7), 1), 252);
-  const float sc = __int_as_float((253 - Es) << 23);
+  const unsigned E = m >> 7;
+  const bool nonfin = m >= 0x7F80u;
+  const bool odd = m != 0 && (E >= 187u || E < 87u);
   float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+  if (!__any_sync(0xFFFFFFFFu, nonfin || odd)) {
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) {
+      const float l0 = __uint_as_float(w[i] << 16), h0 = __uint_as_float(w[i] & 0xFFFF0000u);
+      const float l1 = __uint_as_float(w[i + 1] << 16), h1 = __uint_as_float(w[i + 1] & 0xFFFF0000u);
+      a0 = fmaf(l0, l0, a0);
+      a1 = fmaf(h0, h0, a1);
+      a2 = fmaf(l1, l1, a2);
+      a3 = fmaf(h1, h1, a3);
+    }
+    *acc += static_cast<double>((a0 + a1) + (a2 + a3));
+    return;
+  }
+  if (nonfin) {
+    *acc += careful_block_at(in, wb, nv, lane, nonfinite);
+    return;
+  }
+  const int Es = odd ? min(max(static_cast<int>(E), 1), 252) : 126;
+  const float sc = __int_as_float((253 - Es) << 23);
 #pragma unroll
   for (int i = 0; i < 32; i += 2) {
     const float l0 = __uint_as_float(w[i] << 16) * sc, h0 = __uint_as_float(w[i] & 0xFFFF0000u) * sc;
@@ -141,30 +164,7 @@ __device__ __noinline__ double scaled_block_at(const uint4* in, uint64_t wb, uin
     a3 = fmaf(h1, h1, a3);
   }
   const float blk = (a0 + a1) + (a2 + a3);
-  return static_cast<double>(blk) * __longlong_as_double(static_cast<long long>(1023 + 2 * Es - 252) << 52);
-}
-
-// Fast block sum: the squares of 64 values in four fp32 FFMA chains.
-__device__ __forceinline__ void block_sum(const uint32_t (&w)[32], const uint4* in, uint64_t wb, uint64_t nv,
-                                          unsigned lane, double* acc, unsigned* nonfinite) {
-  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll
-  for (int i = 0; i < 32; i += 2) {
-    const float l0 = __uint_as_float(w[i] << 16), h0 = __uint_as_float(w[i] & 0xFFFF0000u);
-    const float l1 = __uint_as_float(w[i + 1] << 16), h1 = __uint_as_float(w[i + 1] & 0xFFFF0000u);
-    a0 = fmaf(l0, l0, a0);
-    a1 = fmaf(h0, h0, a1);
-    a2 = fmaf(l1, l1, a2);
-    a3 = fmaf(h1, h1, a3);
-  }
-  const float blk = (a0 + a1) + (a2 + a3);
-  // NaN/Inf inputs, fp32 overflow and blocks that may have lost precision to subnormal
-  // partial sums all fail this test and are redone scaled.
-  if (blk >= 0x1p-100f && blk < 0x1p120f) {
-    *acc += static_cast<double>(blk);
-  } else {
-    *acc += scaled_block_at(in, wb, nv, lane, nonfinite);
-  }
+  *acc += static_cast<double>(blk) * __longlong_as_double(static_cast<long long>(1023 + 2 * Es - 252) << 52);
 }
 
 struct StatsParams {
