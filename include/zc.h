@@ -6,26 +6,32 @@
  * "Key idea and contribution", first technique: the frequent-exponent window is taken
  * directly from the tensor's standard deviation (no histogram, no sort), in-window exponents
  * are stored in 3 bits instead of 8, out-of-window exponents keep their full 8 bits in a
- * separate list so that reconstruction is exact, and sign and mantissa travel unchanged --
- * about 11 bits per value instead of 16.  The second technique of the same section
+ * separate store so that reconstruction is exact, and sign and mantissa travel unchanged --
+ * about 11 bits per value instead of 16.  The separate store of a chunk is a list of
+ * (position, exponent) pairs, or, when more than a third of the chunk escapes, a plane of all
+ * its exponents, whichever is smaller (the same section's third technique switches to the
+ * uncompressed form where coding does not pay).  The second technique of the same section
  * (kernels tuned for the GPU: a layout shaped by the communication, aligned global and shared
  * memory access, data movement pipelined with compute) is what the
  * kernels behind these calls implement for sm_103a.
  *
- * Stream format "ZCB1", version 2 (little-endian, every section zero-padded to 16 bytes):
- *   header    32 B  "ZCB1", u16 version = 2, u8 log2(chunk) = 12, u8 e0, u64 n, u64 N,
+ * Stream format "ZCB1", version 3 (little-endian, every section zero-padded to 16 bytes):
+ *   header    32 B  "ZCB1", u16 version = 3, u8 log2(chunk) = 12, u8 e0, u64 n, u64 N,
  *                   u64 total_bytes                      (N = ceil(n / 4096) chunks)
- *   offsets   u64[N+1]: absolute byte offset of each chunk's escape list; offsets[N] =
+ *   offsets   u64[N+1]: absolute byte offset of each chunk's escape section; offsets[N] =
  *             total_bytes.  Zero padding to R0 = pad16(32 + 8 (N+1)).
  *   fixed     for chunk c (m values), at R0 + 5632 c: 3-bit codes, code i at bits [3i, 3i+3)
  *             least significant bit first (pad16(ceil(3m/8)) B), then one sign|mantissa byte
  *             per value, (x >> 8 & 0x80) | (x & 0x7F) (pad16(m) B).  The place of every fixed
  *             part follows from n alone (a layout shaped by the communication: it can be sent
  *             before any size is exchanged).
- *   escapes   after the last fixed part, in chunk order: for a chunk with k escapes, u16
- *             positions then u8 full exponents in ascending position order (pad16(3k) B).
+ *   escapes   after the last fixed part, in chunk order, one section per chunk.  For a chunk
+ *             of m values with k escapes (k = the number of code-7 values): if 3k <= m, u16
+ *             positions then u8 full exponents in ascending position order (pad16(3k) B);
+ *             otherwise the u8 exponents of all m values in value order (pad16(m) B).
  *   Code c < 7 means exponent e0 + c; code 7 means "escape".  e0 is in [0, 249].
- * A full chunk without escapes costs 5632 B for 4096 values: 11 bits per value.
+ * A full chunk without escapes costs 5632 B for 4096 values: 11 bits per value.  A full chunk
+ * costs at most 9728 B (a plane): 19 bits per value.
  *
  * All entry points are host functions.  Pointers called "device" may be any address the GPU
  * can dereference (cudaMalloc, managed, or mapped pinned memory).  Every call is
@@ -60,8 +66,8 @@ typedef struct CUstream_st* cudaStream_t; /* the CUDA runtime's own stream handl
 /* ------------------------------------------------------------------ sizes */
 
 /* Bytes the caller must provide at `out` for zc_compress of n values: the worst-case stream
- * (every value escaping, 17,920 B per full chunk, plus header and offset table) followed by
- * the call's workspace (scan state, 8 B per chunk, and a 16.25 KiB control block).
+ * (9,728 B per full chunk: its fixed part and an exponent plane, plus header and offset table)
+ * followed by the call's workspace (scan state, 8 B per chunk, and a 16.25 KiB control block).
  * Pure host function; makes no CUDA call.  Returns 0 when n > ZC_MAX_N. */
 size_t zc_max_compressed_bytes(size_t n);
 

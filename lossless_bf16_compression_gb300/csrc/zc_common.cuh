@@ -14,20 +14,22 @@
 
 namespace zc {
 
-// ------------------------------------------------------------------ stream layout ("ZCB1" v2)
+// ------------------------------------------------------------------ stream layout ("ZCB1" v3)
 //
-// header (32 B) | u64 escape offsets [N+1] | zero pad to 16 | fixed parts | escape lists
+// header (32 B) | u64 escape offsets [N+1] | zero pad to 16 | fixed parts | escape sections
 // The fixed part of chunk c (3-bit codes, then the sign|mantissa plane) starts at
 // records_base(n) + c * kFullFixedBytes, so its place follows from n alone; only the escape
-// lists (u16 positions, u8 exponents, zero pad) are placed by the scan.
+// sections are placed by the scan.  A chunk of m values with k escapes keeps them as a list (u16
+// positions, u8 exponents, zero pad) when 3k <= m, else as a plane of all m exponents (zero
+// pad): whichever is smaller, chosen from k, which the codes give.
 constexpr int kChunk = 4096;                       // values per chunk
 constexpr int kHeaderBytes = 32;                   // stream header
 constexpr int kFullCodeBytes = 3 * kChunk / 8;     // 1536: 3-bit codes of a full chunk
 constexpr int kFullFixedBytes = kFullCodeBytes + kChunk;  // 5632: fixed part of a full chunk
-constexpr int kMaxEscapeBytes = 3 * kChunk;        // 12288: every value escapes
+constexpr int kMaxEscapeBytes = kChunk;            // 4096: an exponent plane, the largest section
 constexpr int kE0Max = 249;
-constexpr unsigned long long kMagicWord =          // bytes 0..6 of the header: "ZCB1", v2, 12
-    0x5Aull | (0x43ull << 8) | (0x42ull << 16) | (0x31ull << 24) | (2ull << 32) | (12ull << 48);
+constexpr unsigned long long kMagicWord =          // bytes 0..6 of the header: "ZCB1", v3, 12
+    0x5Aull | (0x43ull << 8) | (0x42ull << 16) | (0x31ull << 24) | (3ull << 32) | (12ull << 48);
 
 __host__ __device__ constexpr uint64_t pad16(uint64_t v) { return (v + 15u) & ~uint64_t(15); }
 __host__ __device__ constexpr uint64_t num_chunks(uint64_t n) { return (n + kChunk - 1) / kChunk; }
@@ -50,9 +52,14 @@ __host__ __device__ inline uint64_t escape_base(uint64_t n) {
   const uint64_t N = num_chunks(n);
   return N ? fixed_offset(n, N - 1) + fixed_bytes(chunk_values(n, N - 1)) : records_base(n);
 }
+// Escape section of a chunk of m values with k escapes: a list when 3k <= m, else a plane.
+__host__ __device__ inline bool exponent_plane(unsigned m, unsigned k) { return 3 * k > m; }
+__host__ __device__ inline unsigned escape_section_bytes(unsigned m, unsigned k) {
+  return static_cast<unsigned>(exponent_plane(m, k) ? pad16(m) : pad16(3ull * k));
+}
 __host__ __device__ inline uint64_t max_stream_bytes(uint64_t n) {
   const uint64_t rem = n % kChunk;
-  return escape_base(n) + (n / kChunk) * kMaxEscapeBytes + pad16(3 * rem);
+  return escape_base(n) + (n / kChunk) * kMaxEscapeBytes + pad16(rem);
 }
 
 // ------------------------------------------------------------------ workspace (tail of `out`)
@@ -210,6 +217,9 @@ __device__ __forceinline__ unsigned lds_u32(uint32_t a) {
   unsigned v;
   asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
   return v;
+}
+__device__ __forceinline__ void sts_v2(uint32_t a, uint32_t x, uint32_t y) {
+  asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(a), "r"(x), "r"(y) : "memory");
 }
 __device__ __forceinline__ uint2 lds_v2(uint32_t a) {
   uint2 v;

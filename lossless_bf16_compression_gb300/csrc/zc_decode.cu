@@ -2,25 +2,25 @@
 // exponents, rebuild the BF16 bit patterns, and validate the stream as it goes.
 //
 // Method: ZipCCL (SIGCOMM scribe notes), "Key idea and contribution": in-window exponents are
-// e0 + code, out-of-window exponents come from the separate full-exponent list, so the
-// reconstruction is exact (first technique); decompression kernels with aligned global and
-// shared memory access (second technique).
+// e0 + code, out-of-window exponents come from the separate store of full exponents (a list of
+// (position, exponent) pairs, or a plane of every exponent when more than a third of the chunk
+// escapes), so the reconstruction is exact (first technique); decompression kernels with
+// aligned global and shared memory access (second technique).
 //
 // GB300 design.  One 128-thread CTA per chunk, sixteen CTAs per SM (32 registers, under 10 KB of
 // shared memory each): fixed parts sit at places that follow from n and the offset table
-// locates every escape list, so there is no inter-CTA dependency.  Warp 0 reads the header and
-// the chunk's two escape offsets in one round trip and checks them; the fixed part (5,632 B)
-// and, when it is at most 4 KB (about 1,360 escapes, a third of the chunk), the escape list then
-// arrive in shared memory by bulk async copies (TMA engine, one mbarrier).  A larger list is
-// read where it lies in the stream: sizing the staging buffer for the worst case (12 KB) would
-// cost a quarter of the CTAs per SM for every chunk.  A thread holds 4 slices
-// of 8 values; per slice it takes its 24 code bits and 8 sign|mantissa bytes from shared
-// memory, builds two values per 32-bit word with a few integer ops, and writes one coalesced
-// 16-byte store, escaped values with a placeholder exponent.  Then the threads walk the escape
-// list together, one entry each, check it against the codes and patch the value, so escape
-// work is proportional to the number of escapes rather than to the busiest lane.  Every offset
-// and size is checked before it is used, so a corrupt stream sets an error instead of steering
-// a read outside [0, total_bytes).
+// locates every escape section, so there is no inter-CTA dependency.  Warp 0 reads the header
+// and the chunk's two escape offsets in one round trip and checks them; the fixed part (5,632 B)
+// and the escape section (at most 4 KB, the size of a plane) then arrive in shared memory by
+// bulk async copies (TMA engine, one mbarrier).  A thread holds 4 slices of 8 values; per slice
+// it takes its 24 code bits and 8 sign|mantissa bytes from shared memory, builds two values per
+// 32-bit word with a few integer ops, and writes one coalesced 16-byte store, escaped values
+// with a placeholder exponent.  Then, for a list, the threads walk it together, one entry each,
+// check it against the codes and patch the value, so escape work is proportional to the number
+// of escapes rather than to the busiest lane; for a plane, each thread rebuilds its values from
+// the plane and checks every exponent against its code.  Every offset and size is checked
+// before it is used, so a corrupt stream sets an error instead of steering a read outside
+// [0, total_bytes).
 #include "zc_common.cuh"
 
 namespace zc {
@@ -28,7 +28,8 @@ namespace {
 
 constexpr int kThreads = kChunkThreads;  // 128
 constexpr int kCtasPerSm = 16;           // 2048 threads per SM: 32 registers and < 14 KB each
-constexpr unsigned kEscSmemBytes = 4096; // escape lists up to this size are staged in shared memory
+constexpr unsigned kEscSmemBytes = 4096; // a chunk's escape section, staged in shared memory
+static_assert(kEscSmemBytes >= kMaxEscapeBytes, "every escape section fits the staging buffer");
 constexpr unsigned kWaitLimit = 1u << 22;   // mbarrier polls before giving up
 
 struct DecodeParams {
@@ -47,8 +48,44 @@ struct __align__(128) DecodeSmem {
   int ok;
   int e0;
   unsigned esc_bytes;
-  unsigned long long esc_off;
 };
+
+// A chunk whose escapes are kept as a plane: this thread's values again, each exponent from the
+// plane, each checked against its code (the same thread wrote the placeholders, so its stores
+// land after them).  Kept out of line, off the path of chunks with a list.  False if an
+// exponent disagrees with its code.
+__device__ __noinline__ bool rebuild_from_plane(const uint8_t* codes, const uint8_t* smp, const uint8_t* plane,
+                                                uint16_t* dst, unsigned m, int e0) {
+  const unsigned tid = threadIdx.x;
+  const bool full = m == kChunk;
+  bool ok = true;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const unsigned g = 128 * q + tid, v0 = 8 * g;
+    if (!full && v0 >= m) continue;
+    const unsigned b = 3 * g;
+    const uint32_t* cw = reinterpret_cast<const uint32_t*>(codes + (b & ~3u));
+    const uint32_t bits = __funnelshift_r(cw[0], cw[1], 8 * (b & 3));
+    const uint2 sm = *reinterpret_cast<const uint2*>(smp + v0);
+    const uint2 ex = *reinterpret_cast<const uint2*>(plane + v0);
+    uint32_t x[4];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const unsigned E = ((j < 4 ? ex.x : ex.y) >> (8 * (j & 3))) & 0xFFu;
+      const unsigned s8 = ((j < 4 ? sm.x : sm.y) >> (8 * (j & 3))) & 0xFFu;
+      const unsigned d = E - static_cast<unsigned>(e0);
+      if ((full || v0 + j < m) && (d <= 6u ? d : 7u) != ((bits >> (3 * j)) & 7u)) ok = false;
+      const uint32_t val = ((s8 & 0x80u) << 8) | (E << 7) | (s8 & 0x7Fu);
+      x[j >> 1] = (j & 1) ? (x[j >> 1] | (val << 16)) : val;
+    }
+    if (full || v0 + 8 <= m) {
+      *reinterpret_cast<uint4*>(dst + v0) = make_uint4(x[0], x[1], x[2], x[3]);
+    } else {
+      for (unsigned j = 0; v0 + j < m; ++j) dst[v0 + j] = static_cast<uint16_t>(pick4(x, j >> 1) >> (16 * (j & 1)));
+    }
+  }
+  return ok;
+}
 
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(DecodeParams p) {
   __shared__ DecodeSmem S;
@@ -80,7 +117,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(DecodePara
       else if ((c == 0 && off0 != E0) || (p.N == 0 && total != E0) || (p.N > 0 && c == p.N - 1 && off1 != total))
         bad = ZC_ERR_CORRUPT;
       else if (c < p.N && (off0 < E0 || off1 > total || off1 < off0 || ((off0 | off1) & 15) ||
-                           off1 - off0 > pad16(3ull * m)))
+                           off1 - off0 > pad16(m)))  // an escape section is at most a plane
         bad = ZC_ERR_CORRUPT;
       if (bad) set_error(p.status, bad);
       S.ok = !bad && c < p.N;
@@ -91,11 +128,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(DecodePara
         const unsigned fbytes = static_cast<unsigned>(fixed_bytes(m));
         mbar_init(&S.mbar, 1);
         fence_mbar_init();
-        const unsigned staged = S.esc_bytes <= kEscSmemBytes ? S.esc_bytes : 0u;
-        mbar_arrive_expect_tx(&S.mbar, fbytes + staged);
+        mbar_arrive_expect_tx(&S.mbar, fbytes + S.esc_bytes);
         bulk_load(S.fixed, p.in + fixed_offset(p.n, c), fbytes, &S.mbar);
-        if (staged) bulk_load(S.esc, p.in + off0, staged, &S.mbar);
-        S.esc_off = off0;
+        if (S.esc_bytes) bulk_load(S.esc, p.in + off0, S.esc_bytes, &S.mbar);
       }
     }
   }
@@ -116,12 +151,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(DecodePara
   const unsigned smbytes = full ? kChunk : static_cast<unsigned>(pad16(m));
   const uint8_t* codes = reinterpret_cast<const uint8_t*>(S.fixed);
   const uint8_t* smp = codes + cbytes;
-  // A list larger than the staging buffer is read where it lies in the stream (its range was
-  // checked against the offset table and the stream length above).  The two cases keep apart
-  // so that every access has one known state space.
-  const bool staged = S.esc_bytes <= kEscSmemBytes;
   const uint8_t* esc_s = reinterpret_cast<const uint8_t*>(S.esc);
-  const uint8_t* esc_g = p.in + S.esc_off;
   const uint32_t e0_field = static_cast<uint32_t>(e0) * (128u * 0x00010001u);  // e0 << 7 in both halves
   uint16_t* dst = p.out + first;
 
@@ -161,12 +191,18 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(DecodePara
   if (lane == 0) atomicAdd(&S.escapes, mine);
   __syncthreads();  // every placeholder is written and the chunk's escape count is known
 
-  // Escapes: entry i of the list patches value pos[i].  Positions strictly increasing, below m,
-  // each holding code 7, with as many entries as code-7 values: the list names exactly the
-  // escaped values, so the stream is canonical.
+  // Escapes.  k, the code-7 count, decides the section's form (a list when 3k <= m, else a
+  // plane of every exponent) and so its size.  A list must name exactly the escaped values:
+  // positions strictly increasing, below m, each holding code 7, each exponent outside the
+  // window.  A plane must agree with the codes everywhere.  Either way the stream is canonical.
   const unsigned k = S.escapes;
-  bool corrupt = pad16(3ull * k) != S.esc_bytes;
-  if (!corrupt) {
+  const bool plane = exponent_plane(m, k);
+  bool corrupt = escape_section_bytes(m, k) != S.esc_bytes;
+  if (!corrupt && plane) {
+    corrupt = !rebuild_from_plane(codes, smp, esc_s, dst, m, e0);
+  } else if (!corrupt) {
+    // A list: the threads walk it together, one entry each, check each entry against the codes
+    // and the entry before it, and patch the value.
     auto patch = [&](unsigned i, unsigned pos, unsigned E, unsigned prev) {
       const unsigned pb = 3 * pos;
       const unsigned code = pos < m ? ((codes[pb >> 3] | (codes[(pb >> 3) + 1] << 8)) >> (pb & 7)) & 7u : 0u;
@@ -178,33 +214,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(DecodePara
       const unsigned sm = smp[pos];
       dst[pos] = static_cast<uint16_t>(((sm & 0x80u) << 8) | (E << 7) | (sm & 0x7Fu));
     };
-    if (staged) {  // in shared memory
-      const uint16_t* pos_list = reinterpret_cast<const uint16_t*>(esc_s);
-      for (unsigned i = tid; i < k; i += kThreads) patch(i, pos_list[i], esc_s[2 * k + i], i ? pos_list[i - 1] : 0u);
-    } else {
-      const uint16_t* pos_list = reinterpret_cast<const uint16_t*>(esc_g);  // in the stream: batches of kBatch entries per thread, every load issued first
-      constexpr int kBatch = 4;
-      for (unsigned i0 = 0; i0 < k; i0 += kBatch * kThreads) {
-        unsigned pv[kBatch], ev[kBatch], qv[kBatch];
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-          const unsigned i = i0 + u * kThreads + tid;
-          pv[u] = i < k ? __ldg(pos_list + i) : 0u;
-          ev[u] = i < k ? __ldg(esc_g + 2 * k + i) : 0u;
-          qv[u] = (i < k && i > 0) ? __ldg(pos_list + i - 1) : 0u;
-        }
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-          const unsigned i = i0 + u * kThreads + tid;
-          if (i < k) patch(i, pv[u], ev[u], qv[u]);
-        }
-      }
-    }
+    const uint16_t* pos_list = reinterpret_cast<const uint16_t*>(esc_s);
+    for (unsigned i = tid; i < k; i += kThreads) patch(i, pos_list[i], esc_s[2 * k + i], i ? pos_list[i - 1] : 0u);
   }
 
-  // zero padding: the escape list always, code bits and sign|mantissa bytes of a partial chunk
-  const unsigned epad = corrupt ? 0u : S.esc_bytes - 3 * k;  // < 16
-  if (tid < epad) corrupt |= (staged ? esc_s[3 * k + tid] : __ldg(esc_g + 3 * k + tid)) != 0;
+  // zero padding: the escape section always, code bits and sign|mantissa bytes of a partial chunk
+  const unsigned used = plane ? m : 3 * k;
+  const unsigned epad = corrupt ? 0u : S.esc_bytes - used;  // < 16
+  if (tid < epad) corrupt |= esc_s[used + tid] != 0;
   if (!full) {
     if (tid < smbytes - m) corrupt |= smp[m + tid] != 0;
     const unsigned bit = 3 * m + tid;  // at most 127 padding bits

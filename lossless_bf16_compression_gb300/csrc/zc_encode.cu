@@ -46,7 +46,7 @@ constexpr int kThreads = kCoders + 32;     // + the retiring warp (the scanner i
 constexpr int kCtasPerSm = 5;
 constexpr int kStages = 2;                 // input chunks in flight per CTA
 constexpr unsigned kInBytes = 2 * kChunk;
-constexpr unsigned kRingBytes = 24 * 1024; // escape-list ring per CTA (two worst-case lists)
+constexpr unsigned kRingBytes = 24 * 1024; // escape-section ring per CTA (six of the largest, 4 KB each)
 constexpr unsigned kQueue = 64;            // escape lists waiting, at most
 constexpr unsigned kDenseMin = 16;         // escapes per lane from which a warp takes the dense loop
 constexpr unsigned kWaitLimit = 1u << 22;  // mbarrier polls before giving up
@@ -355,6 +355,20 @@ __device__ bool ring_room(const EncodeSmem& S, const Ring& R, unsigned bytes, co
   return true;
 }
 
+// An exponent plane: this thread's 32 exponent bytes at `dst` (shared window; byte v0 of the
+// section), read back from the staged input (values past m are zero there, so the section's
+// padding comes out zero); `room` bytes of the section lie at or past dst.  Out of line, off
+// the path of chunks with a list.
+__device__ __noinline__ void write_plane(const uint4* stage, unsigned sw, uint32_t dst, unsigned room) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const uint4 xv = stage[(sw ^ (16 * q)) / 16];
+    const uint32_t lo = prmt((xv.x >> 7) & 0x00FF00FFu, (xv.y >> 7) & 0x00FF00FFu, 0x6420);
+    const uint32_t hi = prmt((xv.z >> 7) & 0x00FF00FFu, (xv.w >> 7) & 0x00FF00FFu, 0x6420);
+    if (8u * q < room) sts_v2(dst + 8 * q, lo, hi);
+  }
+}
+
 __device__ __forceinline__ bool bar_coders_or(bool v) {
   unsigned r;
   asm volatile(
@@ -491,7 +505,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 
     unsigned base;
     const unsigned k = chunk_rank(cnt, &base, S.scan);  // [R]
-    const unsigned esc_bytes = static_cast<unsigned>(pad16(3ull * k));
+    // The escape section: a list when 3k <= m, else a plane (the same in every coding thread).
+    const bool plane = 3 * k > m;
+    const unsigned esc_bytes = plane ? ((m + 15u) & ~15u) : ((3 * k + 15u) & ~15u);
     // The list's place in the ring: every coding thread works it out from its own copy of the
     // ring state and waits (bounded) for the room itself, so no barrier is needed before the
     // list is written.  A thread that gives up stops the CTA at [C].
@@ -502,7 +518,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     if (!stop && !ring_room(S, R, gap + esc_bytes, p)) stop = true;
     R.made += gap + esc_bytes;
     R.head = where + esc_bytes;
-    if (!__any_sync(0xFFFFFFFFu, stop)) {  // positions and exponents, in rank order
+    if (__any_sync(0xFFFFFFFFu, stop)) {
+      // nothing to write: the CTA stops at [C]
+    } else if (plane) {
+      write_plane(S.xin[s], sw, smem_u32(S.ring) + where + v0, v0 < esc_bytes ? esc_bytes - v0 : 0u);
+    } else {  // positions and exponents, in rank order
       // Each thread writes its own escapes; the exponent is read back from the staged input.
       // Shared memory is addressed with 32-bit shared-window addresses.
       const uint32_t esc = smem_u32(S.ring) + where;

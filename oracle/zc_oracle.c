@@ -29,6 +29,13 @@
  *       only the variable escape lists are compacted, behind a table of their offsets.
  *       32-byte header, u64 escape-offset table, fixed parts in chunk order, escape lists in
  *       chunk order; every section padded with zeros to 16 bytes; little-endian.
+ *   R6  the separate store of a chunk's infrequent exponents (first technique: they keep their
+ *       complete information apart from the codes) takes whichever of two lossless forms is
+ *       smaller, in the spirit of the third technique's switch to the native path where
+ *       compression does not pay: with k escapes among m values, a list of k (u16 position,
+ *       u8 exponent) pairs when 3k <= m, else the chunk's m exponent bytes in value order (an
+ *       exponent plane).  The form follows from k, which the codes give, so the stream needs
+ *       no flag; the codes are the same in both forms.  Format version 3.
  */
 #include "zc_oracle.h"
 
@@ -38,7 +45,7 @@
 
 #define CHUNK 4096u
 #define HEADER_BYTES 32u
-#define FORMAT_VERSION 2u
+#define FORMAT_VERSION 3u
 #define LOG2_CHUNK 12u
 #define E0_MAX 249
 #define WINDOW 7
@@ -84,8 +91,15 @@ uint64_t zco_records_base(uint64_t n) {
 /* Fixed part of a chunk of m values: 3-bit code section, then the sign|mantissa plane. */
 static uint64_t fixed_bytes(uint64_t m) { return pad16((3u * m + 7u) / 8u) + pad16(m); }
 
-/* Bytes a chunk of m values with k escapes contributes: its fixed part and its escape list. */
-uint64_t zco_record_bytes(uint64_t m, uint64_t k) { return fixed_bytes(m) + pad16(3u * k); }
+/* R6: a chunk keeps its escapes as a list of k (position, exponent) pairs when 3k <= m, else as
+ * a plane of all m exponents. */
+static int exponent_plane(uint64_t m, uint64_t k) { return 3u * k > m; }
+
+/* Size of a chunk's escape section (list or plane), zero-padded to 16 bytes. */
+static uint64_t escape_bytes(uint64_t m, uint64_t k) { return exponent_plane(m, k) ? pad16(m) : pad16(3u * k); }
+
+/* Bytes a chunk of m values with k escapes contributes: its fixed part and its escape section. */
+uint64_t zco_record_bytes(uint64_t m, uint64_t k) { return fixed_bytes(m) + escape_bytes(m, k); }
 
 /* Where chunk c's fixed part starts: every earlier chunk is full. */
 static uint64_t fixed_offset(uint64_t n, uint64_t c) { return zco_records_base(n) + c * fixed_bytes(CHUNK); }
@@ -99,7 +113,7 @@ static uint64_t escape_base(uint64_t n) {
 uint64_t zco_max_stream_bytes(uint64_t n) {
   uint64_t total = escape_base(n);
   uint64_t N = zco_num_chunks(n);
-  for (uint64_t c = 0; c < N; ++c) total += pad16(3u * chunk_len(n, c)); /* every value escapes */
+  for (uint64_t c = 0; c < N; ++c) total += pad16(chunk_len(n, c)); /* a plane: the largest section */
   return total;
 }
 
@@ -225,7 +239,7 @@ int64_t zco_compress(const uint16_t* x, uint64_t n, int base_or_auto, uint8_t* o
   for (uint64_t c = 0; c < N; ++c) {
     uint64_t m = chunk_len(n, c), k = 0;
     for (uint64_t i = 0; i < m; ++i) k += exponent_code(bf16_exponent(x[c * CHUNK + i]), e0) == 7u;
-    total += pad16(3u * k);
+    total += escape_bytes(m, k);
   }
   if (out == NULL || total > cap) return -ZCO_ERR_CAPACITY;
   memset(out, 0, (size_t)total);
@@ -253,6 +267,7 @@ int64_t zco_compress(const uint16_t* x, uint64_t n, int base_or_auto, uint8_t* o
 
     uint64_t k = 0;
     for (uint64_t i = 0; i < m; ++i) k += exponent_code(bf16_exponent(xc[i]), e0) == 7u;
+    const int plane = exponent_plane(m, k);
 
     uint64_t r = 0;
     for (uint64_t i = 0; i < m; ++i) {
@@ -261,13 +276,15 @@ int64_t zco_compress(const uint16_t* x, uint64_t n, int base_or_auto, uint8_t* o
       for (unsigned b = 0; b < 3; ++b)
         if ((code >> b) & 1u) set_bit(codes, 3u * i + b); /* code i at bits [3i, 3i+3) */
       sm[i] = (uint8_t)((bf16_sign(xc[i]) << 7) | bf16_mantissa(xc[i]));
-      if (code == 7u) {
+      if (plane) {
+        esc[i] = (uint8_t)E; /* every exponent, in value order */
+      } else if (code == 7u) {
         put_u16(esc + 2u * r, (uint16_t)i); /* positions, ascending */
         esc[2u * k + r] = (uint8_t)E;       /* full exponents, same order */
         r += 1;
       }
     }
-    esc_pos += pad16(3u * k);
+    esc_pos += escape_bytes(m, k);
   }
   put_u64(out + HEADER_BYTES + 8u * N, esc_pos);
   return (int64_t)total;
@@ -308,7 +325,9 @@ int zco_decompress(const uint8_t* in, uint64_t in_bytes, uint16_t* out, uint64_t
     uint64_t k = 0; /* the escape count follows from the codes */
     for (uint64_t i = 0; i < m; ++i)
       k += (get_bit(codes, 3u * i) & get_bit(codes, 3u * i + 1) & get_bit(codes, 3u * i + 2));
-    if (esc_pos + pad16(3u * k) > total) return ZCO_ERR_CORRUPT;
+    const int plane = exponent_plane(m, k);
+    const uint64_t section = escape_bytes(m, k);
+    if (esc_pos + section > total) return ZCO_ERR_CORRUPT;
     const uint8_t* esc = in + esc_pos;
 
     uint64_t r = 0;
@@ -316,7 +335,10 @@ int zco_decompress(const uint8_t* in, uint64_t in_bytes, uint16_t* out, uint64_t
       unsigned code = get_bit(codes, 3u * i) | (get_bit(codes, 3u * i + 1) << 1) |
                       (get_bit(codes, 3u * i + 2) << 2);
       unsigned E;
-      if (code < 7u) {
+      if (plane) {
+        E = esc[i];
+        if (exponent_code(E, e0) != code) return ZCO_ERR_CORRUPT; /* the plane must agree with the codes */
+      } else if (code < 7u) {
         E = (unsigned)e0 + code;
       } else {
         if (get_u16(esc + 2u * r) != i) return ZCO_ERR_CORRUPT; /* positions ascending, exact */
@@ -329,8 +351,9 @@ int zco_decompress(const uint8_t* in, uint64_t in_bytes, uint16_t* out, uint64_t
     for (uint64_t b = 3u * m; b < 8u * code_bytes; ++b)
       if (get_bit(codes, b)) return ZCO_ERR_CORRUPT;
     if (!all_zero(sm + m, pad16(m) - m)) return ZCO_ERR_CORRUPT;
-    if (!all_zero(esc + 3u * k, pad16(3u * k) - 3u * k)) return ZCO_ERR_CORRUPT;
-    esc_pos += pad16(3u * k);
+    const uint64_t used = plane ? m : 3u * k;
+    if (!all_zero(esc + used, section - used)) return ZCO_ERR_CORRUPT;
+    esc_pos += section;
   }
   if (get_u64(in + HEADER_BYTES + 8u * N) != esc_pos || esc_pos != total) return ZCO_ERR_CORRUPT;
   return ZCO_OK;

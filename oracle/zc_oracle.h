@@ -42,7 +42,8 @@ extern "C" {
 
 /* Layout helpers (pure).  records_base: start of the fixed-part region (after the header and
  * the escape-offset table); record_bytes: what a chunk of m values with k escapes adds to the
- * stream (its fixed part plus its escape list). */
+ * stream (its fixed part plus its escape section: a list of k pairs, or all m exponents when
+ * 3k > m). */
 uint64_t zco_num_chunks(uint64_t n);
 uint64_t zco_records_base(uint64_t n);
 uint64_t zco_record_bytes(uint64_t m, uint64_t k);

@@ -25,11 +25,22 @@ def load_golden(name):
     return fields
 
 
-@pytest.fixture(scope="session")
-def golden_tiny():
+def _golden_stream(name):
     import numpy as np
 
-    g = load_golden("tiny_stream.txt")
+    g = load_golden(name)
     values = np.array([int(v, 16) for v in " ".join(g["values"]).split()], dtype=np.uint16)
     stream = np.frombuffer(bytes.fromhex("".join(g["stream"])), dtype=np.uint8)
     return int(g["e0"][0]), values, stream
+
+
+@pytest.fixture(scope="session")
+def golden_tiny():
+    """Five values whose two escapes are kept as an exponent plane (3k > m)."""
+    return _golden_stream("tiny_stream.txt")
+
+
+@pytest.fixture(scope="session")
+def golden_tiny_list():
+    """Seven values whose two escapes are kept as a (position, exponent) list (3k <= m)."""
+    return _golden_stream("tiny_list_stream.txt")

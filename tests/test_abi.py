@@ -45,8 +45,8 @@ def test_max_stream_bytes_closed_form_large(lib):
     N = (n + 4095) // 4096
     rem = n % 4096
     pad16 = lambda v: (v + 15) // 16 * 16  # noqa: E731
-    # header + table, then per chunk the fixed part and a full escape list (every value escapes)
-    want = pad16(32 + 8 * (N + 1)) + (n // 4096) * (5632 + 12288) + pad16((3 * rem + 7) // 8) + pad16(rem) + pad16(3 * rem)
+    # header + table, then per chunk the fixed part and an exponent plane (the largest escape section)
+    want = pad16(32 + 8 * (N + 1)) + (n // 4096) * (5632 + 4096) + pad16((3 * rem + 7) // 8) + pad16(rem) + pad16(rem)
     assert zc.zc_max_stream_bytes(n) == want
 
 

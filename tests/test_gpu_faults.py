@@ -29,10 +29,16 @@ def _gpu():
 
 @pytest.fixture(scope="module")
 def sample():
+    """N(0, 0.02^2) with 300 random bit patterns, coded with the window of the Gaussian part
+    (e0 = 116), so that every chunk keeps its escapes as a list.  (In auto mode the random
+    patterns' huge values pull e0 up to 243 and every chunk keeps a plane instead.)"""
     rng = np.random.default_rng(42)
     x = workloads.fp32_to_bf16_bits((rng.standard_normal(N_VALUES) * 0.02).astype(np.float32))
     x[rng.choice(N_VALUES, 300, replace=False)] = workloads.random_patterns(300, 43)
-    return x, oracle.compress(x)
+    s = oracle.compress(x, 116)
+    N = (N_VALUES + 4095) // 4096
+    assert all(escape_offset(s, c + 1) - escape_offset(s, c) < 1024 for c in range(N)), "lists expected"
+    return x, s
 
 
 def u64_at(s, off, v):
@@ -122,32 +128,34 @@ def test_random_bit_flips_match_oracle_verdict(sample):
 
 @pytest.fixture(scope="module")
 def dense_sample():
-    """Random bit patterns: nearly every value escapes, so each chunk's escape list (about 12 KB)
-    is larger than the decoder's staging buffer and is checked where it lies in the stream."""
+    """Random bit patterns: nearly every value escapes, so every chunk keeps its escapes as an
+    exponent plane (one byte per value) rather than a list of (position, exponent) pairs."""
     x = workloads.random_patterns(2 * 4096 + 50, 91)
     return x, oracle.compress(x)
 
 
-def test_large_escape_lists_corruptions_are_reported(dense_sample):
+def test_plane_corruptions_are_reported(dense_sample):
     x, s = dense_sample
     n = x.size
+    N = (n + 4095) // 4096
     cap = zc.zc_max_compressed_bytes(n)
     off0, off1 = escape_offset(s, 0), escape_offset(s, 1)
-    assert off1 - off0 > 4096, "the list must exceed the staging buffer"
+    assert off1 - off0 == 4096, "chunk 0 keeps a plane"
     e0 = int(s[7])
     E = (x[:4096].astype(np.int64) >> 7) & 0xFF
-    k0 = int(((E < e0) | (E > e0 + 6)).sum())
-    assert off1 - off0 == (3 * k0 + 15) // 16 * 16
+    inside = np.flatnonzero((E >= e0) & (E <= e0 + 6))
+    outside = np.flatnonzero((E < e0) | (E > e0 + 6))
+    assert inside.size > 0 and outside.size > 0
     st, vals = gpu_decompress_bytes(s, n, cap)
     assert st == zc.ZC_OK and np.array_equal(vals, x)
+    R0 = (32 + 8 * (N + 1) + 15) // 16 * 16
+    i_in, i_out = int(inside[0]), int(outside[-1])
+    last_off = escape_offset(s, N - 1)  # the last chunk's 50 values: a plane of pad16(50) = 64 bytes
     muts = {
-        "first_position": (off0, s[off0] ^ 0x01),
-        "last_position": (off0 + 2 * (k0 - 1), s[off0 + 2 * (k0 - 1)] ^ 0x04),
-        "last_exponent_in_window": (off0 + 3 * k0 - 1, e0),
-        "middle_exponent_in_window": (off0 + 2 * k0 + k0 // 2, e0 + 3),
+        "escaped_exponent_into_window": (off0 + i_out, e0 + 2),
+        "in_window_exponent_changed": (off0 + i_in, (int(E[i_in]) + 1) & 0xFF if E[i_in] < e0 + 6 else e0),
+        "last_plane_padding": (last_off + 50 + 3, 0x01),
     }
-    if (3 * k0) % 16:
-        muts["padding"] = (off0 + 3 * k0, 0x01)
     for name, (pos, val) in muts.items():
         t = s.copy()
         t[pos] = np.uint8(val)
@@ -155,10 +163,17 @@ def test_large_escape_lists_corruptions_are_reported(dense_sample):
         assert ost != oracle.OK, f"{name}: the oracle accepts it, the mutation is not a corruption"
         st, _ = gpu_decompress_bytes(t, n, cap)
         assert st == zc.ZC_ERR_CORRUPT, f"{name}: status {zc.ERROR_NAMES.get(st, st)}"
+    # an escaped value's exponent moved to another out-of-window exponent is a valid stream of
+    # another tensor: both sides must accept it and agree on the values
+    t = s.copy()
+    t[off0 + i_out] = np.uint8(0 if E[i_out] != 0 else 1)
+    ost, ovals = oracle_status(t, n, cap)
+    st, gvals = gpu_decompress_bytes(t, n, cap)
+    assert ost == oracle.OK and st == zc.ZC_OK and np.array_equal(gvals, ovals)
     rng = np.random.default_rng(8)
-    for _ in range(60):  # flips inside the list: the GPU's verdict is the oracle's
+    for _ in range(60):  # flips in chunk 0's codes and plane: the GPU's verdict is the oracle's
         t = s.copy()
-        pos = int(rng.integers(off0, off1))
+        pos = int(rng.choice([rng.integers(R0, R0 + 1536), rng.integers(off0, off1)]))
         t[pos] ^= np.uint8(1 << int(rng.integers(0, 8)))
         ost, ovals = oracle_status(t, n, cap)
         st, gvals = gpu_decompress_bytes(t, n, cap)

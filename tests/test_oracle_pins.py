@@ -29,6 +29,12 @@ def bf16_to_float(bits):
         return b.view(np.float32).astype(np.float64)
 
 
+def escape_section(m, k):
+    """Bytes of a chunk's escape section: a list of k (u16, u8) pairs, or a plane of all m
+    exponents when 3k > m; zero-padded to 16."""
+    return pad16(m) if 3 * k > m else pad16(3 * k)
+
+
 def closed_form_size(x, e0):
     """Stream length from the size formula, with escapes counted by a per-chunk histogram."""
     n = x.size
@@ -39,11 +45,36 @@ def closed_form_size(x, e0):
     for c in range(N):
         m = min(CHUNK, n - c * CHUNK)
         k = int(escape[c * CHUNK:c * CHUNK + m].sum())
-        total += pad16((3 * m + 7) // 8) + pad16(m) + pad16(3 * k)
+        total += pad16((3 * m + 7) // 8) + pad16(m) + escape_section(m, k)
     return total
 
 
 # ----------------------------------------------------------------------------- golden
+
+
+def test_golden_list_stream_matches_hand_derivation(golden_tiny_list):
+    e0, values, stream = golden_tiny_list
+    got = oracle.compress(values, e0)
+    assert got.tobytes() == stream.tobytes()
+    st, back = oracle.decompress(stream, values.size)
+    assert st == oracle.OK and np.array_equal(back, values)
+
+
+def test_list_or_plane_at_the_boundary():
+    """3k <= m keeps a list, 3k > m a plane, whichever is smaller; the codes are the same."""
+    e0 = 127
+    inside, outside = 0x3F80, 0x0000  # exponents 127 (code 0) and 0 (an escape)
+    for m in range(1, 40):
+        for k in range(0, m + 1):
+            x = np.array([outside] * k + [inside] * (m - k), np.uint16)
+            s = oracle.compress(x, e0)
+            section = len(s) - (48 + pad16((3 * m + 7) // 8) + pad16(m))
+            assert section == (pad16(m) if 3 * k > m else pad16(3 * k)), (m, k)
+            assert section == min(pad16(m), pad16(3 * k))
+            if 3 * k > m:  # a plane: one exponent byte per value, in value order
+                assert s[-section:][:m].tolist() == [0] * k + [127] * (m - k)
+            st, back = oracle.decompress(s, m)
+            assert st == oracle.OK and np.array_equal(back, x)
 
 
 def test_golden_stream_matches_hand_derivation(golden_tiny):
@@ -300,20 +331,45 @@ def test_decoder_accepts_only_canonical_streams(golden_tiny):
     _bijection_under_flips(oracle.compress(x), x.size)
 
 
+def test_decoder_accepts_only_canonical_list_streams(golden_tiny_list):
+    e0, values, stream = golden_tiny_list
+    assert _bijection_under_flips(stream, values.size) > 0
+
+
 def test_decoder_rejections(golden_tiny):
+    """The plane form (five values, two escapes)."""
     e0, values, stream = golden_tiny
     assert oracle.decompress(stream, 6)[0] == oracle.ERR_SIZE_MISMATCH
     assert oracle.decompress(stream[:-16], 5)[0] == oracle.ERR_CORRUPT  # truncated
     t = stream.copy(); t[0] = 0  # magic  # noqa: E702
     assert oracle.decompress(t, 5)[0] == oracle.ERR_CORRUPT
+    t = stream.copy(); t[4] = 2  # the list-only version  # noqa: E702
+    assert oracle.decompress(t, 5)[0] == oracle.ERR_CORRUPT
     t = stream.copy(); t[7] = 250  # base out of range  # noqa: E702
     assert oracle.decompress(t, 5)[0] == oracle.ERR_CORRUPT
-    t = stream.copy(); t[80 + 6] = 1  # nonzero escape padding (after 2+2+1+1 bytes)  # noqa: E702
+    t = stream.copy(); t[80 + 6] = 1  # nonzero plane padding (after 5 bytes)  # noqa: E702
     assert oracle.decompress(t, 5)[0] == oracle.ERR_CORRUPT
+    t = stream.copy(); t[80 + 4] = 130  # escaped value's exponent inside the window  # noqa: E702
+    assert oracle.decompress(t, 5)[0] == oracle.ERR_CORRUPT
+    t = stream.copy(); t[80 + 1] = 129  # in-window value's exponent other than e0 + code  # noqa: E702
+    assert oracle.decompress(t, 5)[0] == oracle.ERR_CORRUPT
+    t = stream.copy(); t[48] |= 0x07  # code 0 -> 7: the plane holds 127, inside the window  # noqa: E702
+    assert oracle.decompress(t, 5)[0] == oracle.ERR_CORRUPT
+
+
+def test_decoder_rejections_list(golden_tiny_list):
+    """The list form (seven values, two escapes)."""
+    e0, values, stream = golden_tiny_list
+    t = stream.copy(); t[80] = 3  # first position names an in-window value  # noqa: E702
+    assert oracle.decompress(t, 7)[0] == oracle.ERR_CORRUPT
+    t = stream.copy(); t[82] = 2  # positions not increasing  # noqa: E702
+    assert oracle.decompress(t, 7)[0] == oracle.ERR_CORRUPT
     t = stream.copy(); t[80 + 4] = 130  # escape exponent inside the window  # noqa: E702
-    assert oracle.decompress(t, 5)[0] == oracle.ERR_CORRUPT
+    assert oracle.decompress(t, 7)[0] == oracle.ERR_CORRUPT
+    t = stream.copy(); t[80 + 6] = 1  # nonzero list padding (after 2+2+1+1 bytes)  # noqa: E702
+    assert oracle.decompress(t, 7)[0] == oracle.ERR_CORRUPT
     t = stream.copy(); t[48] |= 0x07  # code 0 -> 7: one more escape than the list holds  # noqa: E702
-    assert oracle.decompress(t, 5)[0] == oracle.ERR_CORRUPT
+    assert oracle.decompress(t, 7)[0] == oracle.ERR_CORRUPT
 
 
 # ----------------------------------------------------------------------------- statistics
