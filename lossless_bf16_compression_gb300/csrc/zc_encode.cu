@@ -46,7 +46,11 @@ constexpr int kThreads = kCoders + 32;     // + the retiring warp (the scanner i
 constexpr int kCtasPerSm = 5;
 constexpr int kStages = 2;                 // input chunks in flight per CTA
 constexpr unsigned kInBytes = 2 * kChunk;
-constexpr unsigned kRingBytes = 24 * 1024; // escape-section ring per CTA (six of the largest, 4 KB each)
+// Escape-section ring per CTA: four of the largest (a 4 KB plane).  Measured against 20 and
+// 24 KB: 16 KB coded the low-escape tensors about 4% faster (the five CTAs' shared memory then
+// fits a smaller carveout) and the escape-heavy ones 2-16% slower, where the ring fills.
+constexpr unsigned kRingBytes = 16 * 1024;
+static_assert(kRingBytes >= 2 * kMaxEscapeBytes, "a section placed after a skipped gap always fits a drained ring");
 constexpr unsigned kQueue = 64;            // escape lists waiting, at most
 constexpr unsigned kDenseMin = 16;         // escapes per lane from which a warp takes the dense loop
 constexpr unsigned kWaitLimit = 1u << 22;  // mbarrier polls before giving up
