@@ -4,7 +4,7 @@
 // window from the standard deviation, 3-bit codes, separate full exponents):
 //   1. clear the workspace in the tail of `out` (one memset on `stream`);
 //   2. statistics kernel (auto mode only): sum of squares, non-finite count, e0;
-//   3. encode kernel: codes, sign|mantissa plane, escape lists, the single-pass chunk scan,
+//   3. encode kernel: codes, sign|mantissa plane, escape sections, the single-pass chunk scan,
 //      the offset table and the lists compacted behind it.
 // zc_decompress is one decode kernel.  No call synchronizes except zc_status, and
 // zc_compress when `out_bytes` is pageable host memory.

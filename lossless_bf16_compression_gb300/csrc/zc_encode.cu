@@ -51,7 +51,7 @@ constexpr unsigned kInBytes = 2 * kChunk;
 // fits a smaller carveout) and the escape-heavy ones 2-16% slower, where the ring fills.
 constexpr unsigned kRingBytes = 16 * 1024;
 static_assert(kRingBytes >= 2 * kMaxEscapeBytes, "a section placed after a skipped gap always fits a drained ring");
-constexpr unsigned kQueue = 64;            // escape lists waiting, at most
+constexpr unsigned kQueue = 64;            // escape sections waiting, at most
 constexpr unsigned kDenseMin = 16;         // escapes per lane from which a warp takes the dense loop
 constexpr unsigned kWaitLimit = 1u << 22;  // mbarrier polls before giving up
 constexpr int kScanPerLane = 8;            // state words per scanner lane per round trip
@@ -233,7 +233,7 @@ __device__ __noinline__ void scanner(EncodeSmem& S, unsigned long long* flags, u
   }
 }
 
-// The retiring warp: copy escape lists out in chunk order as the scanner resolves them, fill in
+// The retiring warp: copy escape sections out in chunk order as the scanner resolves them, fill in
 // the offset table (and the header fields that belong to the first and last chunk), and give
 // the ring space back.  Lists and their places are 16-byte aligned, so the whole warp copies
 // each one with 16-byte loads and stores: plain stores, so the coding threads need no proxy

@@ -22,12 +22,12 @@
  *       f(u) = f(2u) for f(t) = P(|Z| < t) + P(|Z| >= 128 t), Z ~ N(0,1).  For a Gaussian
  *       of standard deviation sigma this picks the 7-binade window with the fewest expected
  *       escapes.  It is evaluated as floor(ilogb(q*c^2)/2) + 127.
- *   R5  byte layout ("ZCB1", version 2), read from the data layout shaped by the
+ *   R5  byte layout ("ZCB1", version 3), read from the data layout shaped by the
  *       communication in the second technique and the compress / exchange sizes / send workflow (Figure 5(b),
  *       Design-1): every chunk's fixed-size part (3-bit codes, then the sign|mantissa plane) sits
  *       at an offset that follows from n alone, so it can be sent before any size is known;
- *       only the variable escape lists are compacted, behind a table of their offsets.
- *       32-byte header, u64 escape-offset table, fixed parts in chunk order, escape lists in
+ *       only the variable escape sections (R6) are compacted, behind a table of their offsets.
+ *       32-byte header, u64 escape-offset table, fixed parts in chunk order, escape sections in
  *       chunk order; every section padded with zeros to 16 bytes; little-endian.
  *   R6  the separate store of a chunk's infrequent exponents (first technique: they keep their
  *       complete information apart from the codes) takes whichever of two lossless forms is
