@@ -46,10 +46,11 @@ constexpr int kThreads = kCoders + 32;     // + the retiring warp (the scanner i
 constexpr int kCtasPerSm = 5;
 constexpr int kStages = 2;                 // input chunks in flight per CTA
 constexpr unsigned kInBytes = 2 * kChunk;
-// Escape-section ring per CTA: four of the largest (a 4 KB plane).  Measured against 20 and
-// 24 KB: 16 KB coded the low-escape tensors about 4% faster (the five CTAs' shared memory then
-// fits a smaller carveout) and the escape-heavy ones 2-16% slower, where the ring fills.
-constexpr unsigned kRingBytes = 16 * 1024;
+// Escape-section ring per CTA: four and a half of the largest (a 4 KB plane).  Measured against
+// 16, 20 and 24 KB: up to 18 KB the five CTAs' shared memory fits a smaller carveout, and the
+// low-escape tensors coded about 4% faster than with 20 or 24 KB; 18 KB keeps that and gives the
+// escape-heavy tensors, where the ring fills, 2% more than 16 KB.
+constexpr unsigned kRingBytes = 18 * 1024;
 static_assert(kRingBytes >= 2 * kMaxEscapeBytes, "a section placed after a skipped gap always fits a drained ring");
 constexpr unsigned kQueue = 64;            // escape sections waiting, at most
 constexpr unsigned kDenseMin = 16;         // escapes per lane from which a warp takes the dense loop
