@@ -15,12 +15,13 @@
 // bulk async copies (TMA engine, one mbarrier).  A thread holds 4 slices of 8 values; per slice
 // it takes its 24 code bits and 8 sign|mantissa bytes from shared memory, builds two values per
 // 32-bit word with a few integer ops, and writes one coalesced 16-byte store, escaped values
-// with a placeholder exponent.  Then, for a list, the threads walk it together, one entry each,
-// check it against the codes and patch the value, so escape work is proportional to the number
-// of escapes rather than to the busiest lane; for a plane, each thread rebuilds its values from
-// the plane and checks every exponent against its code.  Every offset and size is checked
-// before it is used, so a corrupt stream sets an error instead of steering a read outside
-// [0, total_bytes).
+// with a placeholder exponent.  Then the threads walk a list together, one entry each, check it
+// against the codes and patch the value, so escape work is proportional to the number of
+// escapes rather than to the busiest lane.  A section of a plane's size is built from instead
+// in the same single pass (sign|mantissa bytes plus the plane's exponents, each checked against
+// its code), and again from the codes in the rare case that the count shows a list of that size.
+// Every offset and size is checked before it is used, so a corrupt stream sets an error instead
+// of steering a read outside [0, total_bytes).
 #include "zc_common.cuh"
 
 namespace zc {
