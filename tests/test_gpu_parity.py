@@ -83,6 +83,26 @@ def test_escape_free_and_all_escape():
     check_parity(np.zeros(n, np.uint16))      # all zeros: e0 = 0, exponent 0 is in the window
 
 
+@pytest.mark.parametrize("k", [1361, 1365, 1366, 2048])
+def test_full_chunks_at_the_list_plane_boundary(k):
+    """Full chunks with k escapes.  Up to 1365 escapes (3k <= 4096) they keep a list.  From
+    1361 on, that list pads to 4096 bytes, the size of a plane, so the decoder builds from it
+    as a plane first and must rebuild the values from the codes.  From 1366 on they keep a
+    plane."""
+    rng = np.random.default_rng(k)
+    chunks = []
+    for _ in range(3):
+        x = np.full(4096, 0x3F80, np.uint16)  # 1.0: exponent 127, in the window for e0 = 127
+        x |= rng.integers(0, 128, 4096).astype(np.uint16)  # random mantissas
+        pos = rng.choice(4096, k, replace=False)
+        x[pos] = rng.integers(0, 0x0100, k).astype(np.uint16)  # exponents 0 and 1: escapes
+        chunks.append(x)
+    x = np.concatenate(chunks)
+    s = check_parity(x, 127)
+    section = (4096 if 3 * k > 4096 else (3 * k + 15) // 16 * 16)
+    assert s.size == oracle.records_base(x.size) + 3 * (5632 + section)
+
+
 def test_special_tensors():
     check_parity(np.full(9000, 0x7FC0, np.uint16))           # only NaN: no finite value
     check_parity(np.full(9000, 0x3F80, np.uint16))           # constant 1.0
