@@ -1,20 +1,33 @@
 #!/usr/bin/env python3
 """Benchmark: lossless BF16 exponent codec on GB300, one JSON line on stdout.
 
-A step is one pass of the whole hot path over one synthetic buffer: zc_compress in auto mode
-(statistics pass, window base, encode + single-pass chunk scan) followed by zc_decompress, on
-the 4096 x 14336 FSDP gradient-bucket workload resident in HBM.  The L2 cache is flushed
-between steps, outside the timed region: a 256 MiB buffer is written and then read back, so
-the cache holds none of the step's data and no dirty lines whose write-back the next kernel
-would pay for.  Each step is timed with CUDA events on the stream the library launches on.
-A second pass of the same K steps brackets every library kernel with CUDA events (for the
-per-kernel durations behind `roofline`); those events cost the GPU about 2 us each, so `value`
-comes from the first pass, which has none.
+A step is one pass of the whole hot path over one synthetic buffer resident in HBM:
+zc_compress in auto mode (statistics pass, window base, encode + single-pass chunk scan)
+followed by zc_decompress.  The default workload is the largest single-GPU configuration,
+2^29 N(0, 1) BF16 values (1 GiB).  The L2 cache is flushed between steps, outside the timed
+region: a 256 MiB buffer is written and then read back, so the cache holds none of the step's
+data and no dirty lines whose write-back the next kernel would pay for.  Steps are timed with
+CUDA events on the stream the library launches on.
 
-value = BF16 input bytes (2n) of all ranks per second of compress+decompress.
+value = BF16 input bytes (2n) of all ranks per second of compress + decompress.
+
+The same line also carries, for the default workload:
+  compress / decompress    each operation timed on its own (an event between the two calls):
+                           GB/s of BF16 input, algorithmic bytes (4n + C and C + 2n) per second
+                           and their fraction of the measured HBM copy bandwidth;
+  roofline                 the dominant kernel, from a pass with CUDA events around every
+                           library kernel;
+  e2e, cpu_baseline        the step through the C ABI with host buffers, and the oracle on the
+                           host cores on a bounded sample;
+and unless --no-extras:
+  configs                  the same compress / decompress figures for every configuration of at
+                           least 64M values (MoE activations, the adversarial tensor, N(0, 1) at
+                           2^26 .. 2^29), L2 flushed between steps;
+  sweep                    latency and GB/s per size for N(0, 1) buffers of 2^15 .. 2^29 values,
+                           each compressed and decompressed 100 times back to back on one stream.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
-                  [--profile]
+                  [--no-extras] [--profile]
 
 --impl reference times the plain C oracle on the host cores (one core) on a bounded sample of
 the same workload.  With N > 1 (torchrun), every rank runs its own replica: the codec has no
@@ -37,7 +50,11 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "compress+decompress GB/s on BF16 input (% of HBM peak); compression ratio"
-DEFAULT_WORKLOAD = "grad_bucket_4096x14336"
+DEFAULT_WORKLOAD = "sweep_2^29"
+# configurations of at least 64M values: the target of the roofline fractions
+TARGET_CONFIGS = ["moe_a2a_16384x7168", "adversarial_256m", "sweep_2^26", "sweep_2^27", "sweep_2^28", "sweep_2^29"]
+SWEEP_SIZES = list(range(15, 30))  # 2^15 .. 2^29 values (64 KiB .. 1 GiB)
+SWEEP_REPS = 100
 L2_FLUSH_BYTES = 256 << 20
 KERNEL_NAMES = {1: "stats", 2: "encode", 3: "decode"}
 KERNEL_SOURCES = {"stats": "zc_stats.cu", "encode": "zc_encode.cu", "decode": "zc_decode.cu"}
@@ -84,24 +101,26 @@ def barrier(dist):
 
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+    """nvidia-smi samples of SM clock and throttle reasons while the timed regions run."""
 
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
     REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    PERIOD_MS = 20
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
         self.lines: list[str] = []
         self.marks: list[float] = []
+        self.windows: list[tuple[float, float]] = []
 
     def start(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
-                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", str(self.PERIOD_MS)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (FileNotFoundError, OSError):
             self.proc = None
             return
@@ -117,7 +136,8 @@ class ClockSampler:
             self.marks.append(time.time())
 
     def window(self, t0: float, t1: float):
-        self.t0, self.t1 = t0, t1
+        """A timed region, by host wall clock (its GPU work was synchronized at both ends)."""
+        self.windows.append((t0, t1))
 
     def stop(self):
         if self.proc is None:
@@ -128,21 +148,21 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        rows = []
-        for line, t in zip(self.lines, self.marks):
-            if getattr(self, "t0", 0) - 0.06 <= t <= getattr(self, "t1", 1e18) + 0.06:
-                rows.append([c.strip() for c in line.split(",")])
+        slack = 1.5 * self.PERIOD_MS / 1e3
+        rows = [[c.strip() for c in line.split(",")] for line, t in zip(self.lines, self.marks)
+                if any(a - slack <= t <= b + slack for a, b in self.windows)]
         if not rows:
             rows = [[c.strip() for c in line.split(",")] for line in self.lines[-3:]]
-        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        sm = [float(r[1]) for r in rows if len(r) > 2 and r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if len(r) > 2 and r[2].replace(".", "").isdigit()]
         reasons = set()
         for r in rows:
             for name, v in zip(self.REASONS, r[5:9]):
                 if v.lower() == "active":
                     reasons.add(name)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "samples": len(rows)}
+                "reasons": sorted(reasons), "samples": len(rows),
+                "timed_s": round(sum(b - a for a, b in self.windows), 3)}
 
 
 # ---------------------------------------------------------------------------- helpers
@@ -167,42 +187,160 @@ def source_sha(kernel: str) -> str:
 
 
 def profiled_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on this exact
-    kernel source; None otherwise."""
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on this exact kernel
+    source: (bytes, workload it was taken on).  A capture on a smaller N(0, 1) sweep size is
+    scaled to this one by the number of values (the traffic of these kernels grows in proportion
+    to n at these sizes).  (None, None) when there is none."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
-        return None
+        return None, None
     want = source_sha(kernel)
+    scaled = (None, None)
     with open(path) as f:
         for line in f:
             parts = line.split()
-            if len(parts) >= 4 and not line.startswith("#") and parts[0] == kernel and parts[1] == workload \
-                    and parts[2] == want:
-                return int(parts[3])
-    return None
+            if len(parts) < 4 or line.startswith("#") or parts[0] != kernel or parts[2] != want:
+                continue
+            if parts[1] == workload:
+                return int(parts[3]), workload
+            if parts[1].startswith("sweep_2^") and workload.startswith("sweep_2^"):
+                k0, k1 = int(parts[1][8:]), int(workload[8:])
+                scaled = (int(parts[3]) << (k1 - k0) if k1 >= k0 else int(parts[3]) >> (k0 - k1), parts[1])
+    return scaled
 
 
 def cpu_baseline(x, budget_s: float = 10.0):
-    """The oracle, as it stands, single-threaded on this host, on whole-buffer round trips
-    repeated until `budget_s` seconds have passed (at least one)."""
+    """The oracle, as it stands, single-threaded on this host, on a round trip of the first M
+    values of the workload, M sized from a 2^20-value probe so the round trip takes about
+    `budget_s` seconds."""
     import oracle
 
     oracle.build()
-    reps, t_total = 0, 0.0
-    while reps == 0 or t_total < budget_s:
-        t0 = time.perf_counter()
-        s = oracle.compress(x)
-        st, _ = oracle.decompress(s, x.size)
-        t_total += time.perf_counter() - t0
-        reps += 1
-        if st != oracle.OK:
-            raise RuntimeError("oracle round trip failed")
-    return {"value": round(2 * x.size * reps / t_total / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"{reps} x whole-buffer round trip ({x.size} values, {t_total:.1f} s), "
-                      f"host {os.uname().machine}, {os.cpu_count()} cores available"}
+    probe = x[: 1 << 20]
+    t0 = time.perf_counter()
+    oracle.decompress(oracle.compress(probe), probe.size)
+    per_value = (time.perf_counter() - t0) / probe.size
+    m = int(min(x.size, max(1 << 20, budget_s / per_value)))
+    sample = x[:m]
+    t0 = time.perf_counter()
+    s = oracle.compress(sample)
+    st, _ = oracle.decompress(s, m)
+    dt = time.perf_counter() - t0
+    if st != oracle.OK:
+        raise RuntimeError("oracle round trip failed")
+    return {"value": round(2 * m / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"one round trip of the first {m} of {x.size} values ({dt:.1f} s), "
+                      f"host {os.uname().machine}, {os.cpu_count()} cores available, 1 used"}
 
 
 # ---------------------------------------------------------------------------- our arm
+
+
+class Codec:
+    """Device buffers sized for up to `n_max` values and the library calls of one step."""
+
+    def __init__(self, zc, torch, device, n_max):
+        self.zc, self.torch, self.device = zc, torch, device
+        self.xd = torch.empty(n_max, dtype=torch.int16, device=device)
+        self.out = torch.empty(zc.zc_max_compressed_bytes(n_max), dtype=torch.uint8, device=device)
+        self.dec = torch.empty(n_max, dtype=torch.int16, device=device)
+        self.ob = torch.zeros(1, dtype=torch.int64, device=device)
+        self.flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+        self.stream = torch.cuda.current_stream(device)
+        self.sh = self.stream.cuda_stream
+        self.n = 0
+
+    def load(self, x):
+        import numpy as np
+
+        self.n = x.size
+        self.xd[:self.n].copy_(self.torch.from_numpy(x.view(np.int16)))
+        self.dec[:self.n].zero_()
+
+    def flush_l2(self):
+        self.flush.zero_()  # evict everything: 2x the L2 capacity
+        self.flush.view(self.torch.int32).sum()  # then read it back, leaving only clean lines
+
+    def compress(self):
+        rc = self.zc.zc_compress(self.xd.data_ptr(), self.n, self.zc.ZC_BASE_AUTO, self.out.data_ptr(),
+                                 self.ob.data_ptr(), self.sh)
+        if rc:
+            raise RuntimeError(f"zc_compress failed: {rc}")
+
+    def decompress(self):
+        rc = self.zc.zc_decompress(self.out.data_ptr(), self.dec.data_ptr(), self.n, self.sh)
+        if rc:
+            raise RuntimeError(f"zc_decompress failed: {rc}")
+
+    def verified(self) -> bool:
+        st = self.zc.zc_status(self.sh, 1)
+        return st == self.zc.ZC_OK and bool(self.torch.equal(self.dec[:self.n], self.xd[:self.n]))
+
+    def stream_bytes(self) -> int:
+        return int(self.ob.item())
+
+    def e0(self) -> int:
+        return int(self.out[7].item())
+
+    def flushed_steps(self, steps, split, clocks=None, dist=None):
+        """`steps` steps, L2 flushed before each outside its events.  split=False: one event pair
+        per step (start, end); split=True: an event between compress and decompress as well.
+        Returns per-step milliseconds: (compress+decompress,) or (compress, decompress)."""
+        torch = self.torch
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3 if split else 2)] for _ in range(steps)]
+        barrier(dist)
+        torch.cuda.synchronize()
+        t0 = time.time()
+        for e in ev:
+            self.flush_l2()
+            e[0].record(self.stream)
+            self.compress()
+            if split:
+                e[1].record(self.stream)
+            self.decompress()
+            e[-1].record(self.stream)
+        torch.cuda.synchronize()
+        barrier(dist)
+        if clocks:
+            clocks.window(t0, time.time())
+        if split:
+            return [e[0].elapsed_time(e[1]) for e in ev], [e[1].elapsed_time(e[2]) for e in ev]
+        return ([e[0].elapsed_time(e[1]) for e in ev],)
+
+    def back_to_back(self, reps, clocks=None):
+        """`reps` compress+decompress round trips back to back on one stream (no flush), then
+        `reps` compresses alone and `reps` decompresses alone: mean ms of each."""
+        torch = self.torch
+        t = []
+        t_wall = time.time()
+        for what in ("round_trip", "compress", "decompress"):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            a.record(self.stream)
+            for _ in range(reps):
+                if what != "decompress":
+                    self.compress()
+                if what != "compress":
+                    self.decompress()
+            b.record(self.stream)
+            torch.cuda.synchronize()
+            t.append(a.elapsed_time(b) / reps)
+        if clocks:
+            clocks.window(t_wall, time.time())
+        return t
+
+
+def op_figures(n, C, comp_ms, dec_ms, peak):
+    """Compress and decompress figures of one workload from their mean times."""
+    return {
+        "n": n, "stream_bytes": C, "compression_ratio": round(2 * n / C, 4),
+        "compress": {"us": round(comp_ms * 1e3, 2), "gbs_input": round(2 * n / comp_ms / 1e6, 1),
+                     "gbs_algorithmic": round((4 * n + C) / comp_ms / 1e6, 1),
+                     "frac_of_peak": round((4 * n + C) / comp_ms / 1e6 / peak, 4)},
+        "decompress": {"us": round(dec_ms * 1e3, 2), "gbs_input": round(2 * n / dec_ms / 1e6, 1),
+                       "gbs_algorithmic": round((C + 2 * n) / dec_ms / 1e6, 1),
+                       "frac_of_peak": round((C + 2 * n) / dec_ms / 1e6 / peak, 4)},
+    }
 
 
 def run_ours(args, rank, world, local):
@@ -222,104 +360,99 @@ def run_ours(args, rank, world, local):
         zbuild.build()
     barrier(dist)
     zc.lib()
+    peak, peak_kind = measured_peaks()
 
     x = workloads.make(args.workload)
     n = x.size
-    xd = torch.from_numpy(x.view(np.int16)).to(device)
-    cap = zc.zc_max_compressed_bytes(n)
-    out = torch.empty(cap, dtype=torch.uint8, device=device)
-    dec = torch.empty(n, dtype=torch.int16, device=device)
-    ob = torch.zeros(1, dtype=torch.int64, device=device)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
-
-    def flush_l2():
-        flush.zero_()  # evict everything: 2x the L2 capacity
-        flush.view(torch.int32).sum()  # then read it back, leaving only clean lines behind
-    stream = torch.cuda.current_stream(device)
-    sh = stream.cuda_stream
-    xp, op, dp, obp = xd.data_ptr(), out.data_ptr(), dec.data_ptr(), ob.data_ptr()
+    extras = not args.no_extras and world == 1 and not args.profile
+    n_max = max(n, 1 << 29) if extras else n
+    cd = Codec(zc, torch, device, n_max)
+    cd.load(x)
 
     def step():
-        rc = zc.zc_compress(xp, n, zc.ZC_BASE_AUTO, op, obp, sh)
-        rc |= zc.zc_decompress(op, dp, n, sh)
-        if rc:
-            raise RuntimeError(f"codec call failed: {rc}")
+        cd.compress()
+        cd.decompress()
 
-    zc.zc_status(sh, 1)
+    zc.zc_status(cd.sh, 1)
     for _ in range(args.warmup):
-        flush_l2()
+        cd.flush_l2()
         step()
     torch.cuda.synchronize()
     if args.profile:  # the plain step loop only, for profiler captures: no timing extras
         for _ in range(args.steps):
-            flush_l2()
+            cd.flush_l2()
             step()
         torch.cuda.synchronize()
-        st = zc.zc_status(sh, 1)
-        ok = st == zc.ZC_OK and torch.equal(dec, xd)
+        ok = cd.verified()
         if rank == 0:
-            print(json.dumps({"profile_run": args.workload, "n": n, "steps": args.steps, "verified": bool(ok)}))
+            print(json.dumps({"profile_run": args.workload, "n": n, "steps": args.steps, "verified": ok}))
         if not ok:
             raise SystemExit("profile run self-check failed")
         return
 
-    def timed_steps(kernel_events):
-        """K steps, L2 flushed before each (outside its events); per-kernel CUDA events too when
-        asked (each event record costs the GPU about 2 us, so they stay out of the pass that
-        gives `value`)."""
-        starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-        ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-        if kernel_events:
-            zc.zc_timing_collect()
-            zc.zc_timing_enable(1)
-        barrier(dist)
-        torch.cuda.synchronize()
-        t0 = time.time()
-        for i in range(args.steps):
-            flush_l2()
-            starts[i].record(stream)
-            step()
-            ends[i].record(stream)
-        torch.cuda.synchronize()
-        barrier(dist)
-        t1 = time.time()
-        recs = []
-        if kernel_events:
-            zc.zc_timing_enable(0)
-            recs = zc.zc_timing_collect(1 << 20)
-        return [s.elapsed_time(e) for s, e in zip(starts, ends)], recs, t0, t1
-
-    # pass 1: the steps that give `value`, with the clock record
     clocks = ClockSampler(local) if not args.no_clocks else None
     if clocks:
         clocks.start()
-    step_ms, _, t_wall0, t_wall1 = timed_steps(kernel_events=False)
-    clk = None
-    if clocks:
-        clocks.window(t_wall0, t_wall1)
-        clk = clocks.stop()
-    # pass 2: the same number of steps with every library kernel bracketed by CUDA events on its
-    # stream, for per-kernel durations (the roofline) and the launch count
-    _, records, _, _ = timed_steps(kernel_events=True)
-
+    # pass 1: the steps that give `value` (one event pair per step)
+    (step_ms,) = cd.flushed_steps(args.steps, split=False, clocks=clocks, dist=dist)
     total_ms = max_over_ranks(sum(step_ms), dist, device)
-    st = zc.zc_status(sh, 1)
-    ok = st == zc.ZC_OK and torch.equal(dec, xd)
-    total_bytes = int(ob.item())
-    e0 = int(out[7].item())
+    # pass 2: compress and decompress timed apart (an event between the two calls)
+    comp, dec = cd.flushed_steps(args.steps, split=True, clocks=clocks, dist=dist)
+    comp_ms, dec_ms = sum(comp) / len(comp), sum(dec) / len(dec)
+    # pass 3: every library kernel bracketed by CUDA events on its stream, for per-kernel
+    # durations (the roofline) and the launch count; those events cost the GPU about 2 us each
+    # and break the overlap of the statistics and encode kernels, so no other figure uses them
+    zc.zc_timing_collect()
+    zc.zc_timing_enable(1)
+    cd.flushed_steps(args.steps, split=False, clocks=clocks, dist=dist)
+    zc.zc_timing_enable(0)
+    records = zc.zc_timing_collect(1 << 20)
+    ok = cd.verified()
+    C = cd.stream_bytes()
+    e0 = cd.e0()
 
-    # per-kernel device time over the timed region
     per = {}
     for kid, ms in records:
         per.setdefault(KERNEL_NAMES.get(kid, str(kid)), []).append(ms)
     avg = {k: sum(v) / len(v) for k, v in per.items()}
-    C = total_bytes
     alg = {"stats": 2 * n, "encode": 2 * n + C, "decode": C + 2 * n}
     dominant = max(avg, key=lambda k: avg[k] * len(per[k]))
-    peak, peak_kind = measured_peaks()
     achieved = alg[dominant] / (avg[dominant] * 1e-3) / 1e9
-    comp_ms = avg.get("stats", 0.0) + avg.get("encode", 0.0)
-    dec_ms = avg.get("decode", 0.0)
+    traffic, traffic_from = profiled_traffic(dominant, args.workload)
+
+    # per-configuration figures and the small-message sweep (rank 0 of a single-GPU run)
+    configs, sweep = {}, {}
+    if extras:
+        head = {"compress_ms": comp_ms, "decompress_ms": dec_ms, "C": C, "e0": e0, "ok": ok}
+        for k in SWEEP_SIZES:
+            name = f"sweep_2^{k}"
+            cd.load(x if name == args.workload else workloads.make(name))
+            m = cd.n
+            for _ in range(3):
+                step()
+            bt = cd.back_to_back(SWEEP_REPS, clocks=clocks)
+            sweep[name] = {"n": m, "round_trip_us": round(bt[0] * 1e3, 2), "compress_us": round(bt[1] * 1e3, 2),
+                           "decompress_us": round(bt[2] * 1e3, 2),
+                           "gbs_input": round(2 * m / bt[0] / 1e6, 1), "verified": cd.verified()}
+            if name in TARGET_CONFIGS:
+                if name == args.workload:
+                    c_ms, d_ms, Cc, ee, okc = head["compress_ms"], head["decompress_ms"], head["C"], head["e0"], ok
+                else:
+                    c, d = cd.flushed_steps(args.steps, split=True, clocks=clocks)
+                    c_ms, d_ms, Cc, ee, okc = sum(c) / len(c), sum(d) / len(d), cd.stream_bytes(), cd.e0(), \
+                        cd.verified()
+                configs[name] = {**op_figures(m, Cc, c_ms, d_ms, peak), "e0": ee, "verified": okc}
+        for name in TARGET_CONFIGS:
+            if name in configs:
+                continue
+            cd.load(x if name == args.workload else workloads.make(name))
+            for _ in range(3):
+                step()
+            c, d = cd.flushed_steps(args.steps, split=True, clocks=clocks)
+            configs[name] = {**op_figures(cd.n, cd.stream_bytes(), sum(c) / len(c), sum(d) / len(d), peak),
+                             "e0": cd.e0(), "verified": cd.verified()}
+        cd.load(x)
+    clk = clocks.stop() if clocks else None
 
     # End to end through the C ABI: every step copies its input from pinned host memory, runs
     # zc_compress + zc_decompress, and copies the decoded tensor back to pinned host memory.
@@ -328,8 +461,10 @@ def run_ours(args, rank, world, local):
     # (host to device); the two directions use separate copy engines.
     xh = torch.from_numpy(x.view(np.int16)).pin_memory()
     yh = [torch.empty(n, dtype=torch.int16).pin_memory() for _ in range(2)]
-    xd2, out2, dec2, ob2 = [xd, torch.empty_like(xd)], [out, torch.empty_like(out)], \
-        [dec, torch.empty_like(dec)], [ob, torch.zeros_like(ob)]
+    xd2 = [cd.xd[:n], torch.empty(n, dtype=torch.int16, device=device)]
+    out2 = [cd.out, torch.empty(zc.zc_max_compressed_bytes(n), dtype=torch.uint8, device=device)]
+    dec2 = [cd.dec[:n], torch.empty(n, dtype=torch.int16, device=device)]
+    ob2 = [cd.ob, torch.zeros_like(cd.ob)]
     s_in, s_codec, s_out = (torch.cuda.Stream(device) for _ in range(3))
     in_done, codec_done, out_done = ([torch.cuda.Event() for _ in range(2)] for _ in range(3))
 
@@ -372,6 +507,7 @@ def run_ours(args, rank, world, local):
         return
     ms_per_step = total_ms / args.steps
     value = 2 * n * world / (ms_per_step * 1e-3) / 1e9
+    head = op_figures(n, C, comp_ms, dec_ms, peak)
     line = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -387,31 +523,38 @@ def run_ours(args, rank, world, local):
         "data": "synthetic",
         "config": {"workload": args.workload, "n": n, "chunk": 4096, "base": "auto",
                    "l2": "flushed between steps (256 MiB write + read, outside the timed region)",
-                   "kernel_times": "a second pass of K steps with CUDA events around each launch "
-                                   "(they add about 14 us per step, so value comes from a pass without them)",
+                   "passes": "value: K steps with one event pair each; compress/decompress: K more steps with "
+                             "an event between the two calls; kernel_us and roofline: K more steps with events "
+                             "around every library kernel",
                    "parallelism": f"{world} independent replicas"},
-        "compression_ratio": round(2 * n / C, 4),
+        "compression_ratio": head["compression_ratio"],
         "stream_bytes": C,
         "e0": e0,
-        "compress_gbs": round(2 * n / (comp_ms * 1e-3) / 1e9, 2) if comp_ms else None,
-        "decompress_gbs": round(2 * n / (dec_ms * 1e-3) / 1e9, 2) if dec_ms else None,
+        "compress": head["compress"],
+        "decompress": head["decompress"],
         "kernel_us": {k: round(v * 1e3, 2) for k, v in avg.items()},
         "hbm_frac_by_kernel": {k: round(alg[k] / (avg[k] * 1e-3) / 1e9 / peak, 4) for k in avg},
         "roofline": {"bound": "hbm", "kernel": dominant, "achieved": round(achieved, 1), "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "algorithmic_bytes": alg[dominant], "traffic": profiled_traffic(dominant, args.workload)},
+                     "algorithmic_bytes": alg[dominant], "traffic": traffic,
+                     "traffic_from": traffic_from},
         "e2e": {"value": round(2 * n * world / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": 2 * n, "d2h_bytes_per_step": 2 * n,
                 "pipeline": "consecutive steps overlap on 3 streams, 2 buffer sets; no L2 flush"},
-        "gpu_launches": len(records),  # library kernels launched in K steps (pass 2; pass 1 is identical)
+        "gpu_launches": len(records),  # library kernels launched in the K steps of pass 3
         "clocks": clk,
         "verified": bool(ok),
     }
+    if configs:
+        line["configs"] = configs
+    if sweep:
+        line["sweep"] = sweep
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(x)
     print(json.dumps(line), flush=True)
-    if not ok:
-        raise SystemExit("bench self-check failed: the round trip was not exact")
+    bad = [k for k, v in {**configs, **sweep}.items() if not v["verified"]]
+    if not ok or bad:
+        raise SystemExit(f"bench self-check failed: the round trip was not exact ({bad or args.workload})")
 
 
 # ---------------------------------------------------------------------------- reference arm
@@ -466,6 +609,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the per-configuration figures and the size sweep")
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--profile", action="store_true",
                     help="run warm-up + steps of the bare step loop (for ncu), print no bench line")

@@ -89,7 +89,10 @@ size_t zc_max_stream_bytes(size_t n);
  *                 `in`.  The stream is written from out[0]; the bytes past *out_bytes,
  *                 including the workspace tail, are unspecified afterwards.  The library keeps
  *                 no per-call state outside `out`, so calls on different streams with
- *                 different buffers may run concurrently.
+ *                 different buffers may run concurrently.  The encode kernel's CTAs wait on
+ *                 one another (bounded) only for work that a CTA already running has taken,
+ *                 so a concurrent kernel that delays some of them slows the call but does not
+ *                 make it fail.
  *   out_bytes     receives the stream length.  Device, managed or pinned host memory is
  *                 written by the last kernel (asynchronously).  Pageable host memory is also
  *                 accepted: the call then copies the length back and synchronizes `stream`.
@@ -102,10 +105,14 @@ int zc_compress(const void* in, size_t n, int base_or_auto, void* out, size_t* o
 /* ------------------------------------------------------------------ decompress */
 
 /* Decompress a "ZCB1" stream back into n BF16 bit patterns (the exact input of compress).
- *   in      device, 16-byte aligned; must hold the stream's total_bytes (header bytes 24..31)
- *           readable bytes.  The kernel checks every offset and size against the header, the
- *           largest stream n values can produce and each record's own sizes, and reads only
- *           inside [0, total_bytes).
+ *   in      device, 16-byte aligned.  The kernel first reads the 32-byte header and checks it
+ *           against n: magic, version, base, n, N, and the start of the escape region (a
+ *           function of n alone) <= total_bytes (header bytes 24..31) <= the largest stream n
+ *           values can produce.  Only after that check
+ *           does it read further, and every later read lies inside [0, total_bytes): offsets and
+ *           section sizes are checked against the header and against each other before use.
+ *           So `in` must hold max(32, total_bytes) readable bytes; a wrong n or a short
+ *           total_bytes is reported, never read past.
  *   out     device, n x u16, 16-byte aligned, must not overlap `in`.
  *   n       the number of values the caller expects; a stream holding another n sets
  *           ZC_ERR_SIZE_MISMATCH.

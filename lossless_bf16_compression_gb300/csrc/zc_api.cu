@@ -20,21 +20,14 @@ namespace {
 __device__ int g_status;  // first device-side error since the last reset, per device
 
 constexpr int kMaxDevices = 64;
-constexpr unsigned kDefaultSpinLimit = 1u << 20;
 
 std::mutex g_mutex;
 DeviceInfo g_devices[kMaxDevices];
 bool g_device_ready[kMaxDevices];
 
-struct TimingRecord {
-  int kernel;
-  cudaEvent_t start, stop;
-};
 bool g_timing = false;
 std::vector<TimingRecord> g_records;
 std::vector<cudaEvent_t> g_event_pool;
-TimingRecord g_open;
-bool g_open_valid = false;
 
 cudaEvent_t take_event() {
   if (!g_event_pool.empty()) {
@@ -79,22 +72,29 @@ cudaError_t device_info(DeviceInfo* info) {
   return cudaSuccess;
 }
 
-void timing_begin(int kernel_id, cudaStream_t stream) {
+TimingRecord timing_begin(int kernel_id, cudaStream_t stream) {
+  TimingRecord rec;
   std::lock_guard<std::mutex> lock(g_mutex);
-  if (!g_timing) return;
-  g_open.kernel = kernel_id;
-  g_open.start = take_event();
-  g_open.stop = take_event();
-  g_open_valid = g_open.start && g_open.stop;
-  if (g_open_valid) cudaEventRecord(g_open.start, stream);
+  if (!g_timing) return rec;
+  rec.kernel = kernel_id;
+  rec.start = take_event();
+  rec.stop = take_event();
+  if (rec.start && rec.stop) {
+    cudaEventRecord(rec.start, stream);
+  } else {  // no events: record nothing for this kernel
+    if (rec.start) g_event_pool.push_back(rec.start);
+    if (rec.stop) g_event_pool.push_back(rec.stop);
+    rec.start = rec.stop = nullptr;
+  }
+  return rec;
 }
 
-void timing_end(cudaStream_t stream) {
+void timing_end(TimingRecord& rec, cudaStream_t stream) {
+  if (rec.start == nullptr) return;
   std::lock_guard<std::mutex> lock(g_mutex);
-  if (!g_timing || !g_open_valid) return;
-  cudaEventRecord(g_open.stop, stream);
-  g_records.push_back(g_open);
-  g_open_valid = false;
+  cudaEventRecord(rec.stop, stream);
+  g_records.push_back(rec);
+  rec.start = rec.stop = nullptr;
 }
 
 }  // namespace zc
@@ -125,17 +125,17 @@ int compress_impl(const void* in, size_t n, int base, void* out, size_t* out_byt
   if (!pageable) len_ptr = static_cast<unsigned long long*>(attr.devicePointer);
 
   uint8_t* o = static_cast<uint8_t*>(out);
-  const uint64_t ws = workspace_offset(n);
-  if (cudaMemsetAsync(o + ws, 0, workspace_bytes(n), stream) != cudaSuccess) return ZC_ERR_CUDA;
+  uint8_t* ws = o + workspace_offset(n);
+  if (cudaMemsetAsync(ws, 0, workspace_bytes(n), stream) != cudaSuccess) return ZC_ERR_CUDA;
   const uint16_t* x = static_cast<const uint16_t*>(in);
   if (n > 0 && base == ZC_BASE_AUTO) {
-    if (launch_stats(x, n, o, dev, stream) != cudaSuccess) return ZC_ERR_CUDA;
+    if (launch_stats(x, n, ws, dev, stream) != cudaSuccess) return ZC_ERR_CUDA;
   }
-  if (launch_encode(x, n, base, o, len_ptr, dev, stream, stall_chunk, spin_limit) != cudaSuccess)
+  if (launch_encode(x, n, base, o, len_ptr, ws, dev, stream, stall_chunk, spin_limit) != cudaSuccess)
     return ZC_ERR_CUDA;
   if (pageable) {
     unsigned long long total = 0;
-    const Control* ctrl = reinterpret_cast<const Control*>(o + ws);
+    const Control* ctrl = reinterpret_cast<const Control*>(ws);
     if (cudaMemcpyAsync(&total, &ctrl->total, sizeof total, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
       return ZC_ERR_CUDA;
     if (cudaStreamSynchronize(stream) != cudaSuccess) return ZC_ERR_CUDA;

@@ -77,6 +77,7 @@ struct Control {
   int e0;                   // window base chosen by the statistics pass
   unsigned exact_path;      // 1 when the statistics pass needed its exact fallback
   unsigned long long total; // stream length, for the pageable out_bytes path
+  unsigned role_ticket;     // encoder CTAs in start order: the first one to start scans
 };
 
 struct StatsPartial {
@@ -272,20 +273,24 @@ cudaError_t stats_occupancy(int* per_sm);   // defined in zc_stats.cu
 cudaError_t encode_occupancy(int* per_sm);  // defined in zc_encode.cu; also sets the kernel's
                                             // dynamic shared memory size, for the current device
 
-void timing_begin(int kernel_id, cudaStream_t stream);  // no-ops unless timing is enabled
-void timing_end(cudaStream_t stream);
+// CUDA events around one library kernel on its stream; inert unless timing is enabled.  The
+// open record lives with the caller, so concurrent host threads never pair each other's events.
+struct TimingRecord {
+  int kernel = 0;
+  cudaEvent_t start = nullptr, stop = nullptr;
+};
+TimingRecord timing_begin(int kernel_id, cudaStream_t stream);
+void timing_end(TimingRecord& rec, cudaStream_t stream);
 
-cudaError_t launch_stats(const uint16_t* in, uint64_t n, uint8_t* out, const DeviceInfo& dev,
-                         cudaStream_t stream);
-cudaError_t launch_encode(const uint16_t* in, uint64_t n, int base, uint8_t* out,
-                          unsigned long long* out_bytes, const DeviceInfo& dev, cudaStream_t stream,
-                          uint64_t stall_chunk, unsigned spin_limit);
+// The launches.  `ws` is the call's workspace (workspace_bytes(n) bytes, cleared): the tail of
+// `out` for zc_compress, the library's static array for zc_compress_static_scratch.
+cudaError_t launch_stats(const uint16_t* in, uint64_t n, uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream);
+cudaError_t launch_encode(const uint16_t* in, uint64_t n, int base, uint8_t* out, unsigned long long* out_bytes,
+                          uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream, uint64_t stall_chunk,
+                          unsigned spin_limit);
 cudaError_t launch_decode(const uint8_t* in, uint16_t* out, uint64_t n, const DeviceInfo& dev,
                           cudaStream_t stream);
-// The same statistics and encode launches with the workspace at `ws` (workspace_bytes(n) bytes)
-// instead of the tail of `out`.
-cudaError_t launch_stats_ws(const uint16_t* in, uint64_t n, uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream);
-cudaError_t launch_encode_ws(const uint16_t* in, uint64_t n, int base, uint8_t* out, unsigned long long* out_bytes,
-                             uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream);
+
+constexpr unsigned kDefaultSpinLimit = 1u << 20;  // polls of a bounded wait in the encoder
 
 }  // namespace zc

@@ -9,8 +9,8 @@
 //
 // GB300 design.  One 128-thread CTA per chunk, sixteen CTAs per SM (32 registers, under 10 KB of
 // shared memory each): fixed parts sit at places that follow from n and the offset table
-// locates every escape section, so there is no inter-CTA dependency.  Warp 0 reads the header
-// and the chunk's two escape offsets in one round trip and checks them; the fixed part (5,632 B)
+// locates every escape section, so there is no inter-CTA dependency.  Warp 0 reads and checks
+// the header, then reads and checks the chunk's two escape offsets; the fixed part (5,632 B)
 // and the escape section (at most 4 KB, the size of a plane) then arrive in shared memory by
 // bulk async copies (TMA engine, one mbarrier).  A thread holds 4 slices of 8 values; per slice
 // it takes its 24 code bits and 8 sign|mantissa bytes from shared memory, builds two values per
@@ -99,29 +99,36 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(DecodePara
   const unsigned m = c < p.N ? chunk_values(p.n, c) : 0;
 
   if (tid < 32) {
-    // lanes 0..6 fetch header words, the chunk's two escape offsets and the table's zero pad
+    // Two round trips.  Lanes 0..3 fetch the 32-byte header, and lane 0 checks it against the
+    // caller's n: magic, version, base, n, N, and escape_base(n) <= total_bytes <= the largest
+    // stream n values can produce.  Only then do lanes 4..6 fetch the chunk's two escape offsets
+    // and the table's zero pad; they lie below records_base(n) <= escape_base(n) <= total_bytes,
+    // so a wrong n or a short total_bytes never steers a read past the stream.
     const unsigned long long* w = reinterpret_cast<const unsigned long long*>(p.in);
     const uint64_t R0 = records_base(p.n), E0 = escape_base(p.n);
     const bool has_pad = kHeaderBytes + 8 * (p.N + 1) < R0;
+    const unsigned long long hv = lane < 4 ? w[lane] : 0ull;
+    const unsigned long long h0 = __shfl_sync(0xFFFFFFFFu, hv, 0), h1 = __shfl_sync(0xFFFFFFFFu, hv, 1);
+    const unsigned long long h2 = __shfl_sync(0xFFFFFFFFu, hv, 2), total = __shfl_sync(0xFFFFFFFFu, hv, 3);
+    const int e0 = static_cast<int>(h0 >> 56);
+    int bad = 0;
+    if ((h0 & 0x00FFFFFFFFFFFFFFull) != kMagicWord || e0 > kE0Max) bad = ZC_ERR_CORRUPT;
+    else if (h1 != p.n) bad = ZC_ERR_SIZE_MISMATCH;
+    else if (h2 != p.N || total < E0 || total > max_stream_bytes(p.n)) bad = ZC_ERR_CORRUPT;
     unsigned long long v = 0;
-    if (lane < 4) v = w[lane];
-    else if (lane == 4) v = w[4 + c];
-    else if (lane == 5 && c < p.N) v = w[5 + c];
-    else if (lane == 6 && has_pad && (c == 0 || c + 1 >= p.N)) v = w[5 + p.N];
-    const unsigned long long h0 = __shfl_sync(0xFFFFFFFFu, v, 0), h1 = __shfl_sync(0xFFFFFFFFu, v, 1);
-    const unsigned long long h2 = __shfl_sync(0xFFFFFFFFu, v, 2), total = __shfl_sync(0xFFFFFFFFu, v, 3);
+    if (!bad) {  // the same in every lane
+      if (lane == 4) v = w[4 + c];
+      else if (lane == 5 && c < p.N) v = w[5 + c];
+      else if (lane == 6 && has_pad && (c == 0 || c + 1 >= p.N)) v = w[5 + p.N];
+    }
     const unsigned long long off0 = __shfl_sync(0xFFFFFFFFu, v, 4), off1 = __shfl_sync(0xFFFFFFFFu, v, 5);
     const unsigned long long pad = __shfl_sync(0xFFFFFFFFu, v, 6);
     if (lane == 0) {
-      int bad = 0;
-      const int e0 = static_cast<int>(h0 >> 56);
-      if ((h0 & 0x00FFFFFFFFFFFFFFull) != kMagicWord || e0 > kE0Max) bad = ZC_ERR_CORRUPT;
-      else if (h1 != p.n) bad = ZC_ERR_SIZE_MISMATCH;
-      else if (h2 != p.N || total < E0 || total > max_stream_bytes(p.n) || pad != 0) bad = ZC_ERR_CORRUPT;
-      else if ((c == 0 && off0 != E0) || (p.N == 0 && total != E0) || (p.N > 0 && c == p.N - 1 && off1 != total))
-        bad = ZC_ERR_CORRUPT;
-      else if (c < p.N && (off0 < E0 || off1 > total || off1 < off0 || ((off0 | off1) & 15) ||
-                           off1 - off0 > pad16(m)))  // an escape section is at most a plane
+      if (bad == 0 &&
+          (pad != 0 || (c == 0 && off0 != E0) || (p.N == 0 && total != E0) ||
+           (p.N > 0 && c == p.N - 1 && off1 != total) ||
+           (c < p.N && (off0 < E0 || off1 > total || off1 < off0 || ((off0 | off1) & 15) ||
+                        off1 - off0 > pad16(m)))))  // an escape section is at most a plane
         bad = ZC_ERR_CORRUPT;
       if (bad) set_error(p.status, bad);
       S.ok = !bad && c < p.N;
@@ -192,7 +199,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(DecodePara
       }
       mine += __popc(e);
     }
-    return mine;
     return mine;
   };
   // A section of a plane's size (pad16(m) bytes) is a plane unless it is a list whose padded size
@@ -267,9 +273,9 @@ cudaError_t launch_decode(const uint8_t* in, uint16_t* out, uint64_t n, const De
   p.N = num_chunks(n);
   p.status = dev.status;
   const uint64_t grid = p.N ? p.N : 1;  // n = 0: one CTA checks the header
-  timing_begin(ZC_KERNEL_DECODE, stream);
+  TimingRecord t = timing_begin(ZC_KERNEL_DECODE, stream);
   decode_kernel<<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(p);
-  timing_end(stream);
+  timing_end(t, stream);
   return cudaGetLastError();
 }
 

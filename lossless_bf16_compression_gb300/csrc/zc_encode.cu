@@ -7,8 +7,8 @@
 // technique); the kernels lay data out for the communication step, align their global and
 // shared memory accesses, and overlap data movement with the coding (second technique).
 //
-// GB300 design.  A persistent grid, five CTAs per SM.  Block 0 is the scanner; every other
-// block has four coding warps and one retiring warp, so that each chunk's fixed costs (waits,
+// GB300 design.  A persistent grid, five CTAs per SM.  The first CTA to start is the scanner;
+// every other CTA has four coding warps and one retiring warp, so that each chunk's fixed costs (waits,
 // ranks, barriers) are paid by 128 threads and five chunks are in flight per SM (measured
 // faster than eight coding warps at four CTAs per SM).  Chunks are handed out by an atomic
 // ticket (ticket order = chunk order).  Inputs (8 KiB per chunk) arrive by tiled async copies
@@ -42,7 +42,7 @@ namespace {
 
 constexpr int kCoders = 128;               // coding threads, 32 values each
 static_assert(32 * kCoders == kChunk, "a coding thread holds 32 consecutive values");
-constexpr int kThreads = kCoders + 32;     // + the retiring warp (the scanner in block 0)
+constexpr int kThreads = kCoders + 32;     // + the retiring warp (idle in the scanning CTA)
 constexpr int kCtasPerSm = 5;
 constexpr int kStages = 2;                 // input chunks in flight per CTA
 constexpr unsigned kInBytes = 2 * kChunk;
@@ -88,11 +88,12 @@ struct __align__(128) EncodeSmem {
   volatile unsigned freed;      // ring bytes given back, gaps included (consumer)
   volatile int coders_done;     // no more entries will come
   __align__(16) unsigned scan[kCoderWarps];  // per coding warp: its escape count
-  // scanner (block 0): per round parity, each warp's ready count and sum, and the status word
+  // scanner: per round parity, each warp's ready count and sum, and the status word
   unsigned long long scan_sum[2][kCoderWarps];
   unsigned scan_ready[2][kCoderWarps];
   int scan_bad[2];
   int e0;
+  unsigned role;  // 0: this CTA scans; otherwise it codes
 };
 
 // The 8 code-7 flags of a slice (bit 3j for value j) as bits 0..7.
@@ -149,7 +150,7 @@ __device__ void issue_load(EncodeSmem& S, int s, uint64_t c, const EncodeParams&
   }
 }
 
-// The scanner (block 0, its kCoderWarps first warps): resolve chunks in order.  Each round, warp w reads state
+// The scanner (the first CTA to start, its kCoderWarps first warps): resolve chunks in order.  Each round, warp w reads state
 // words frontier + 256 w .. + 255; the published sizes before the first unpublished word (over
 // all warps, in order) become inclusive offsets.  One barrier per round exchanges the warps'
 // ready counts and sums (double-buffered by round parity, so one barrier suffices).
@@ -391,17 +392,21 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   // The stages start on a 1024-byte boundary of the shared window (the period of the swizzle).
   EncodeSmem& S = *reinterpret_cast<EncodeSmem*>(smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
   const unsigned tid = threadIdx.x, warp = tid >> 5;
-  if (blockIdx.x == 0) {  // block 0: the scanner
-    if (warp < kCoderWarps) scanner(S, p.flags, p.N, p.status, p.spin_limit);
-    return;
-  }
   if (tid == 0) {
+    // The first CTA to start is the scanner.  Every other CTA waits, bounded, only on work the
+    // scanner or a CTA that is already running will do (chunks are handed out at run time), so
+    // the call finishes whether or not all CTAs are resident at once.
+    S.role = atomicAdd(&p.ctrl->role_ticket, 1u);
     S.q_pushed = 0;
     S.q_retired = 0;
     S.freed = 0;
     S.coders_done = 0;
   }
   __syncthreads();
+  if (S.role == 0) {
+    if (warp < kCoderWarps) scanner(S, p.flags, p.N, p.status, p.spin_limit);
+    return;
+  }
   if (warp == kCoders / 32) {  // the retiring warp
     retirer(S, p);
     return;
@@ -654,10 +659,9 @@ cudaError_t encode_occupancy(int* per_sm) {
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, encode_kernel, kThreads, smem);
 }
 
-cudaError_t launch_encode(const uint16_t* in, uint64_t n, int base, uint8_t* out,
-                          unsigned long long* out_bytes, const DeviceInfo& dev, cudaStream_t stream,
-                          uint64_t stall_chunk, unsigned spin_limit) {
-  uint8_t* ws = out + workspace_offset(n);
+cudaError_t launch_encode(const uint16_t* in, uint64_t n, int base, uint8_t* out, unsigned long long* out_bytes,
+                          uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream, uint64_t stall_chunk,
+                          unsigned spin_limit) {
   Control* ctrl = reinterpret_cast<Control*>(ws);
   if (n == 0) {
     empty_stream_kernel<<<1, 1, 0, stream>>>(out, base, ctrl, out_bytes);
@@ -683,65 +687,25 @@ cudaError_t launch_encode(const uint16_t* in, uint64_t n, int base, uint8_t* out
   const int smem = kEncodeSmemBytes;
   const int per_sm = dev.encode_per_sm;
   uint64_t grid = static_cast<uint64_t>(per_sm > 0 ? per_sm : 1) * dev.sm_count;
-  if (grid > p.N + 1) grid = p.N + 1;  // block 0 scans, the others code
+  if (grid > p.N + 1) grid = p.N + 1;  // one CTA scans, the others code
   if (grid < 2) grid = 2;
-  timing_begin(ZC_KERNEL_ENCODE, stream);
-  if (base < 0) {
-    // After our own statistics kernel: let this kernel start as that one finishes (it reads
-    // e0 only after griddepcontrol.wait).  Not after a caller's kernel, which may still be
-    // writing the input.
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(grid));
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    err = cudaLaunchKernelEx(&cfg, encode_kernel, p, map);
-    timing_end(stream);
-    return err;
-  }
-  encode_kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(p, map);
-  timing_end(stream);
-  return cudaGetLastError();
-}
-
-// Same launch with the workspace at `ws` instead of the tail of `out`.
-cudaError_t launch_encode_ws(const uint16_t* in, uint64_t n, int base, uint8_t* out, unsigned long long* out_bytes,
-                             uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream) {
-  Control* ctrl = reinterpret_cast<Control*>(ws);
-  if (n == 0) {
-    empty_stream_kernel<<<1, 1, 0, stream>>>(out, base, ctrl, out_bytes);
-    return cudaGetLastError();
-  }
-  EncodeParams p;
-  p.in = in;
-  p.n = n;
-  p.N = num_chunks(n);
-  p.out = out;
-  p.ctrl = ctrl;
-  p.flags = reinterpret_cast<unsigned long long*>(ws + kWsControlBytes + kWsPartialsBytes);
-  p.out_bytes = out_bytes;
-  p.base = base;
-  p.status = dev.status;
-  p.stall_chunk = ~uint64_t(0);
-  p.spin_limit = 1u << 20;
-  p.full_chunks = n / kChunk;
-  CUtensorMap map;
-  const cudaError_t err = input_map(in, n, &map);
-  if (err != cudaSuccess) return err;
-  const int smem = kEncodeSmemBytes;
-  const int per_sm = dev.encode_per_sm;
-  uint64_t grid = static_cast<uint64_t>(per_sm > 0 ? per_sm : 1) * dev.sm_count;
-  if (grid > p.N + 1) grid = p.N + 1;  // block 0 scans, the others code
-  if (grid < 2) grid = 2;
-  timing_begin(ZC_KERNEL_ENCODE, stream);
-  encode_kernel<<<static_cast<unsigned>(grid), kThreads, smem, stream>>>(p, map);
-  timing_end(stream);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  // After our own statistics kernel (auto mode): let this kernel start as that one finishes (it
+  // reads e0 only after griddepcontrol.wait).  Not after a caller's kernel, which may still be
+  // writing the input.
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = base < 0 ? 1 : 0;
+  TimingRecord t = timing_begin(ZC_KERNEL_ENCODE, stream);
+  err = cudaLaunchKernelEx(&cfg, encode_kernel, p, map);
+  timing_end(t, stream);
+  return err;
 }
 
 }  // namespace zc

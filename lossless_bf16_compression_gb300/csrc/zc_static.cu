@@ -80,9 +80,10 @@ extern "C" int zc_compress_static_scratch(const void* in, size_t n, int base_or_
   const uint16_t* x = static_cast<const uint16_t*>(in);
   uint8_t* o = static_cast<uint8_t*>(out);
   if (n > 0 && base_or_auto == ZC_BASE_AUTO) {
-    if (launch_stats_ws(x, n, ws, dev, stream) != cudaSuccess) return ZC_ERR_CUDA;
+    if (launch_stats(x, n, ws, dev, stream) != cudaSuccess) return ZC_ERR_CUDA;
   }
-  if (launch_encode_ws(x, n, base_or_auto, o, len_ptr, ws, dev, stream) != cudaSuccess) return ZC_ERR_CUDA;
+  if (launch_encode(x, n, base_or_auto, o, len_ptr, ws, dev, stream, ~uint64_t(0), kDefaultSpinLimit) != cudaSuccess)
+    return ZC_ERR_CUDA;
   if (pageable) {
     unsigned long long total = 0;
     const Control* ctrl = reinterpret_cast<const Control*>(ws);

@@ -366,9 +366,7 @@ cudaError_t stats_occupancy(int* per_sm) {
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, stats_kernel, kThreads, 0);
 }
 
-cudaError_t launch_stats(const uint16_t* in, uint64_t n, uint8_t* out, const DeviceInfo& dev,
-                         cudaStream_t stream) {
-  uint8_t* ws = out + workspace_offset(n);
+cudaError_t launch_stats(const uint16_t* in, uint64_t n, uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream) {
   StatsParams p;
   p.in = reinterpret_cast<const uint4*>(in);
   p.n = n;
@@ -382,30 +380,9 @@ cudaError_t launch_stats(const uint16_t* in, uint64_t n, uint8_t* out, const Dev
   if (grid > blocks_needed) grid = blocks_needed;
   if (grid < 1) grid = 1;
   if (grid > kStatsMaxCtas) grid = kStatsMaxCtas;
-  timing_begin(ZC_KERNEL_STATS, stream);
+  TimingRecord t = timing_begin(ZC_KERNEL_STATS, stream);
   stats_kernel<<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(p);
-  timing_end(stream);
-  return cudaGetLastError();
-}
-
-// Same launch with the workspace at `ws` instead of the tail of `out`.
-cudaError_t launch_stats_ws(const uint16_t* in, uint64_t n, uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream) {
-  StatsParams p;
-  p.in = reinterpret_cast<const uint4*>(in);
-  p.n = n;
-  p.ctrl = reinterpret_cast<Control*>(ws);
-  p.partials = reinterpret_cast<StatsPartial*>(ws + kWsControlBytes);
-  p.status = dev.status;
-  const uint64_t nv = n >> 3;
-  const uint64_t blocks_needed = (nv + kVecPerWarpBlock * kWarps - 1) / (kVecPerWarpBlock * kWarps);
-  const int per_sm = dev.stats_per_sm;
-  uint64_t grid = static_cast<uint64_t>(per_sm > 0 ? per_sm : 1) * dev.sm_count;
-  if (grid > blocks_needed) grid = blocks_needed;
-  if (grid < 1) grid = 1;
-  if (grid > kStatsMaxCtas) grid = kStatsMaxCtas;
-  timing_begin(ZC_KERNEL_STATS, stream);
-  stats_kernel<<<static_cast<unsigned>(grid), kThreads, 0, stream>>>(p);
-  timing_end(stream);
+  timing_end(t, stream);
   return cudaGetLastError();
 }
 

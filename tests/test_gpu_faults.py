@@ -192,6 +192,40 @@ def test_valid_stream_and_wrong_n(sample):
     assert st == zc.ZC_ERR_SIZE_MISMATCH
 
 
+def test_valid_small_stream_with_much_larger_n(sample):
+    """A caller's n far above the stream's: the header check reports it before any read that
+    depends on n.  The stream sits at the start of a zeroed buffer large enough for every read
+    a decoder could make for the larger n, so this test cannot fault whatever the kernel does."""
+    x, s = sample
+    big = 64 * 4096 + 5
+    st, _ = gpu_decompress_bytes(s, big, zc.zc_max_compressed_bytes(big))
+    assert st == zc.ZC_ERR_SIZE_MISMATCH
+    st, _ = gpu_decompress_bytes(s, 0, zc.zc_max_compressed_bytes(big))
+    assert st == zc.ZC_ERR_SIZE_MISMATCH
+
+
+@pytest.mark.parametrize("total", [0, 16, 48, 64])
+def test_total_below_the_fixed_region(sample, total):
+    """A header whose total_bytes ends before the fixed parts (below records_base(n), or below the
+    start of the escape region) is corrupt.  The stream is cut to total_bytes bytes and followed
+    by a 4 KiB guard band inside the same allocation; the decoder reports ZC_ERR_CORRUPT and
+    writes nothing."""
+    x, s = sample
+    G = 4096
+    t = u64_at(s, 24, total)[:max(total, 32)]
+    ost, _ = oracle_status(t, N_VALUES, t.size)
+    assert ost == oracle.ERR_CORRUPT
+    buf = torch.full((t.size + G,), 0xA5, dtype=torch.uint8, device="cuda")
+    buf[:t.size] = torch.from_numpy(t.copy())
+    out = torch.full((N_VALUES + 16,), 0x5A5A, dtype=torch.int16, device="cuda")
+    s_ = torch.cuda.current_stream().cuda_stream
+    zc.status(reset=True)
+    assert zc.zc_decompress(buf.data_ptr(), out.data_ptr(), N_VALUES, s_) == zc.ZC_OK
+    assert zc.zc_status(s_, 1) == zc.ZC_ERR_CORRUPT
+    assert bool((out == 0x5A5A).all()), "the decoder wrote values from a corrupt stream"
+    assert bool((buf[t.size:] == 0xA5).all())
+
+
 def test_empty_stream():
     s = oracle.compress(np.zeros(0, np.uint16))
     st, _ = gpu_decompress_bytes(s, 0, 64)

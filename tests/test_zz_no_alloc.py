@@ -5,14 +5,17 @@ worst-case stream size, and that must not call cudaMalloc on its progress path (
 synchronize the device, and it is not allowed during stream capture) cannot give zc_compress the
 extra workspace it keeps in the tail of `out`.  The static-scratch entry point takes its
 workspace from a fixed array inside the library instead.  These checks run it through the C ABI
-and require its streams to equal zc_compress's streams byte for byte, on calls made one after
-the other (the shared array must not carry anything over), and its size limit to be enforced.
+and require its streams to equal the oracle's byte for byte on calls made one after the other
+(the shared array must not carry anything over), the device's free memory to stay the same
+across those calls, its writes to stay inside zc_max_stream_bytes(n) bytes of `out`, and its
+size limit to be enforced.
 """
 import ctypes
 
 import numpy as np
 import pytest
 
+import oracle
 from lossless_bf16_compression_gb300 import binding as zc
 from lossless_bf16_compression_gb300 import workloads
 
@@ -35,46 +38,67 @@ def _inputs():
     return a, b
 
 
-def _reference_stream(x):
-    """The stream zc_compress writes for x (its `out` includes the workspace tail)."""
-    out, ob = zc.compress(to_device(x))
-    torch.cuda.synchronize()
-    return out[:int(ob.item())].cpu().numpy()
-
-
-def test_static_scratch_matches_compress_on_consecutive_calls():
+def _static_call(xd, n, base, out, ob_ptr):
     s = torch.cuda.current_stream().cuda_stream
+    rc = zc.zc_compress_static_scratch(xd.data_ptr(), n, base, out.data_ptr(), ob_ptr, s)
+    torch.cuda.synchronize()
+    return rc, zc.zc_status(s, 1)
+
+
+def test_static_scratch_matches_oracle_on_consecutive_calls():
+    inputs = _inputs()
+    wants = [oracle.compress(x) for x in inputs]
+    devs = [to_device(x) for x in inputs]
+    outs = [torch.full((zc.zc_max_stream_bytes(x.size),), 0xEE, dtype=torch.uint8, device="cuda") for x in inputs]
+    obs = [torch.zeros(1, dtype=torch.int64, device="cuda") for _ in inputs]
+    backs = [torch.empty(x.size, dtype=torch.int16, device="cuda") for x in inputs]
     zc.status(reset=True)
-    for x in _inputs():  # two calls in a row through the shared array
-        want = _reference_stream(x)
-        xd = to_device(x)
-        out = torch.full((zc.zc_max_stream_bytes(x.size),), 0xEE, dtype=torch.uint8, device="cuda")
-        ob = torch.zeros(1, dtype=torch.int64, device="cuda")
-        assert zc.zc_compress_static_scratch(xd.data_ptr(), x.size, zc.ZC_BASE_AUTO, out.data_ptr(),
-                                             ob.data_ptr(), s) == zc.ZC_OK
-        assert zc.zc_status(s, 1) == zc.ZC_OK
+    # a first call loads the library's kernels (and with them its device arrays) on this device
+    assert _static_call(devs[1], inputs[1].size, zc.ZC_BASE_AUTO, outs[1], obs[1].data_ptr()) == (zc.ZC_OK, zc.ZC_OK)
+    for x, xd, out, ob, want in zip(inputs, devs, outs, obs, wants):  # two calls in a row
+        free_before = torch.cuda.mem_get_info()[0]
+        assert _static_call(xd, x.size, zc.ZC_BASE_AUTO, out, ob.data_ptr()) == (zc.ZC_OK, zc.ZC_OK)
+        assert torch.cuda.mem_get_info()[0] == free_before, "the call changed the device's free memory"
         total = int(ob.item())
         assert total == want.size
         assert out[:total].cpu().numpy().tobytes() == want.tobytes()
-        back = zc.decompress(out, x.size)
+    for x, out, back in zip(inputs, outs, backs):
+        zc.decompress(out, x.size, out=back)
         assert zc.status(reset=True) == zc.ZC_OK
         assert np.array_equal(back.cpu().numpy().view(np.uint16), x)
 
 
 def test_static_scratch_supplied_base_and_host_length():
     x = _inputs()[0]
-    s = torch.cuda.current_stream().cuda_stream
+    want = oracle.compress(x, 116)
     xd = to_device(x)
     out = torch.empty(zc.zc_max_stream_bytes(x.size), dtype=torch.uint8, device="cuda")
     length = ctypes.c_uint64(0)  # pageable host memory: the call copies the length back
-    e0 = int(_reference_stream(x)[7])
     zc.status(reset=True)
-    assert zc.zc_compress_static_scratch(xd.data_ptr(), x.size, e0, out.data_ptr(), ctypes.addressof(length),
-                                         s) == zc.ZC_OK
-    assert zc.zc_status(s, 1) == zc.ZC_OK
-    want = _reference_stream(x)
+    assert _static_call(xd, x.size, 116, out, ctypes.addressof(length)) == (zc.ZC_OK, zc.ZC_OK)
     assert length.value == want.size
     assert out[:want.size].cpu().numpy().tobytes() == want.tobytes()
+
+
+@pytest.mark.parametrize("n", [2 * 4096 + 50, 3 * 4096])
+def test_static_scratch_stays_inside_its_stream_bound(n):
+    """All-escape random patterns reach the largest stream n values can give (every chunk keeps a
+    plane of exponents); 4 KiB of 0xA5 right before `out` and right after zc_max_stream_bytes(n)
+    bytes of it must survive."""
+    G = 4096
+    x = workloads.random_patterns(n, 600 + n)
+    want = oracle.compress(x)
+    cap = zc.zc_max_stream_bytes(n)
+    buf = torch.full((G + cap + G,), 0xA5, dtype=torch.uint8, device="cuda")
+    out = buf[G:G + cap]
+    ob = torch.zeros(1, dtype=torch.int64, device="cuda")
+    zc.status(reset=True)
+    assert _static_call(to_device(x), n, zc.ZC_BASE_AUTO, out, ob.data_ptr()) == (zc.ZC_OK, zc.ZC_OK)
+    h = buf.cpu().numpy()
+    assert np.all(h[:G] == 0xA5) and np.all(h[G + cap:] == 0xA5), "a guard band was written"
+    total = int(ob.item())
+    assert total == want.size
+    assert h[G:G + total].tobytes() == want.tobytes()
 
 
 def test_static_scratch_rejects_sizes_beyond_its_limit():
