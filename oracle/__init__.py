@@ -5,7 +5,8 @@ imports this package; only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-b
 of ``bench.py`` do.  The C source (``zc_oracle.c``) shares nothing with the CUDA library.
 
 Method: ZipCCL (SIGCOMM scribe notes), "Key idea and contribution", first technique --
-exponent coding with a window taken from the tensor's standard deviation.
+exponent coding with a window taken from the tensor's standard deviation -- and the third
+technique's switch to the native form where coding does not pay.
 """
 from __future__ import annotations
 
@@ -51,7 +52,7 @@ def _load():
             build()
             lib = ctypes.CDLL(_LIB_PATH)
             u64, i64, c_int, p = ctypes.c_uint64, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
-            for name in ("zco_num_chunks", "zco_records_base", "zco_max_stream_bytes"):
+            for name in ("zco_num_chunks", "zco_records_base", "zco_max_stream_bytes", "zco_raw_stream_bytes"):
                 getattr(lib, name).argtypes = [u64]
                 getattr(lib, name).restype = u64
             lib.zco_record_bytes.argtypes = [u64, u64]
@@ -93,6 +94,10 @@ def record_bytes(m: int, k: int) -> int:
 
 def max_stream_bytes(n: int) -> int:
     return int(_load().zco_max_stream_bytes(n))
+
+
+def raw_stream_bytes(n: int) -> int:
+    return int(_load().zco_raw_stream_bytes(n))
 
 
 def window_constant() -> float:

@@ -22,7 +22,7 @@
  *       f(u) = f(2u) for f(t) = P(|Z| < t) + P(|Z| >= 128 t), Z ~ N(0,1).  For a Gaussian
  *       of standard deviation sigma this picks the 7-binade window with the fewest expected
  *       escapes.  It is evaluated as floor(ilogb(q*c^2)/2) + 127.
- *   R5  byte layout ("ZCB1", version 3), read from the data layout shaped by the
+ *   R5  byte layout of the coded form ("ZCB1", version 4), read from the data layout shaped by the
  *       communication in the second technique and the compress / exchange sizes / send workflow (Figure 5(b),
  *       Design-1): every chunk's fixed-size part (3-bit codes, then the sign|mantissa plane) sits
  *       at an offset that follows from n alone, so it can be sent before any size is known;
@@ -35,7 +35,15 @@
  *       compression does not pay: with k escapes among m values, a list of k (u16 position,
  *       u8 exponent) pairs when 3k <= m, else the chunk's m exponent bytes in value order (an
  *       exponent plane).  The form follows from k, which the codes give, so the stream needs
- *       no flag; the codes are the same in both forms.  Format version 3.
+ *       no flag; the codes are the same in both forms.
+ *   R7  stream form: the third technique also switches a whole transfer between the compressed
+ *       path and the native one, by the benefit of compressing.  A tensor whose coded stream
+ *       (R5, R6) would be longer than its native form -- the 32-byte header followed by the n
+ *       values as they are, zero-padded to 16 bytes -- is stored in that native ("raw") form:
+ *       header byte 6 (the chunk size field) is 0, N is 0, and the values follow the header as
+ *       little-endian u16.  Ties keep the coded form.  The decoder checks a raw stream's bytes
+ *       (header, length, padding) but does not recompute whether the coded form would have been
+ *       shorter.  Format version 4.
  */
 #include "zc_oracle.h"
 
@@ -45,8 +53,9 @@
 
 #define CHUNK 4096u
 #define HEADER_BYTES 32u
-#define FORMAT_VERSION 3u
+#define FORMAT_VERSION 4u
 #define LOG2_CHUNK 12u
+#define RAW_FORM 0u /* header byte 6 of a raw stream (R7) */
 #define E0_MAX 249
 #define WINDOW 7
 
@@ -110,12 +119,14 @@ static uint64_t escape_base(uint64_t n) {
   return N ? fixed_offset(n, N - 1) + fixed_bytes(chunk_len(n, N - 1)) : zco_records_base(n);
 }
 
-uint64_t zco_max_stream_bytes(uint64_t n) {
-  uint64_t total = escape_base(n);
-  uint64_t N = zco_num_chunks(n);
-  for (uint64_t c = 0; c < N; ++c) total += pad16(chunk_len(n, c)); /* a plane: the largest section */
-  return total;
-}
+/* Length of the coded form (R5, R6) of x under e0. */
+static uint64_t coded_bytes(const uint16_t* x, uint64_t n, int e0);
+
+/* Length of the raw form (R7): header, n values, zero padding. */
+uint64_t zco_raw_stream_bytes(uint64_t n) { return HEADER_BYTES + pad16(2u * n); }
+
+/* Every stream is at most as long as the raw form (R7). */
+uint64_t zco_max_stream_bytes(uint64_t n) { return zco_raw_stream_bytes(n); }
 
 double zco_window_constant(void) { return WINDOW_C2; }
 
@@ -227,35 +238,51 @@ static unsigned exponent_code(unsigned E, int e0) {
 static void set_bit(uint8_t* base, uint64_t bit) { base[bit / 8] |= (uint8_t)(1u << (bit % 8)); }
 static unsigned get_bit(const uint8_t* base, uint64_t bit) { return (base[bit / 8] >> (bit % 8)) & 1u; }
 
-int64_t zco_compress(const uint16_t* x, uint64_t n, int base_or_auto, uint8_t* out, uint64_t cap) {
-  if (base_or_auto < -1 || base_or_auto > E0_MAX) return -ZCO_ERR_INVALID_ARG;
-  if (n > 0 && (x == NULL || out == NULL)) return -ZCO_ERR_INVALID_ARG;
-  int e0 = base_or_auto == -1 ? zco_choose_e0(x, n) : base_or_auto;
-
-  uint64_t N = zco_num_chunks(n);
-
-  /* First pass: escape-list sizes, so that the capacity check happens before any write. */
+static uint64_t coded_bytes(const uint16_t* x, uint64_t n, int e0) {
   uint64_t total = escape_base(n);
-  for (uint64_t c = 0; c < N; ++c) {
+  for (uint64_t c = 0; c < zco_num_chunks(n); ++c) {
     uint64_t m = chunk_len(n, c), k = 0;
     for (uint64_t i = 0; i < m; ++i) k += exponent_code(bf16_exponent(x[c * CHUNK + i]), e0) == 7u;
     total += escape_bytes(m, k);
   }
-  if (out == NULL || total > cap) return -ZCO_ERR_CAPACITY;
-  memset(out, 0, (size_t)total);
+  return total;
+}
 
-  /* Stream header. */
+static void put_header(uint8_t* out, unsigned form, int e0, uint64_t n, uint64_t N, uint64_t total) {
   out[0] = 'Z';
   out[1] = 'C';
   out[2] = 'B';
   out[3] = '1';
   put_u16(out + 4, FORMAT_VERSION);
-  out[6] = LOG2_CHUNK;
+  out[6] = (uint8_t)form;
   out[7] = (uint8_t)e0;
   put_u64(out + 8, n);
   put_u64(out + 16, N);
   put_u64(out + 24, total);
+}
 
+int64_t zco_compress(const uint16_t* x, uint64_t n, int base_or_auto, uint8_t* out, uint64_t cap) {
+  if (base_or_auto < -1 || base_or_auto > E0_MAX) return -ZCO_ERR_INVALID_ARG;
+  if (n > 0 && (x == NULL || out == NULL)) return -ZCO_ERR_INVALID_ARG;
+  int e0 = base_or_auto == -1 ? zco_choose_e0(x, n) : base_or_auto;
+
+  /* First pass: the coded length, so that the form (R7) and the capacity are settled before
+   * any write. */
+  const uint64_t coded = coded_bytes(x, n, e0);
+  const uint64_t raw = zco_raw_stream_bytes(n);
+  const int raw_form = coded > raw; /* R7: ties keep the coded form */
+  const uint64_t total = raw_form ? raw : coded;
+  if (out == NULL || total > cap) return -ZCO_ERR_CAPACITY;
+  memset(out, 0, (size_t)total);
+
+  if (raw_form) { /* R7: the native form */
+    put_header(out, RAW_FORM, e0, n, 0, total);
+    for (uint64_t i = 0; i < n; ++i) put_u16(out + HEADER_BYTES + 2u * i, x[i]);
+    return (int64_t)total;
+  }
+
+  uint64_t N = zco_num_chunks(n);
+  put_header(out, LOG2_CHUNK, e0, n, N, total);
   uint64_t esc_pos = escape_base(n);
   for (uint64_t c = 0; c < N; ++c) {
     const uint16_t* xc = x + c * CHUNK;
@@ -302,15 +329,24 @@ int zco_decompress(const uint8_t* in, uint64_t in_bytes, uint16_t* out, uint64_t
   if (in == NULL || (n > 0 && out == NULL)) return ZCO_ERR_INVALID_ARG;
   if (in_bytes < HEADER_BYTES) return ZCO_ERR_CORRUPT;
   if (in[0] != 'Z' || in[1] != 'C' || in[2] != 'B' || in[3] != '1') return ZCO_ERR_CORRUPT;
-  if (get_u16(in + 4) != FORMAT_VERSION || in[6] != LOG2_CHUNK) return ZCO_ERR_CORRUPT;
+  if (get_u16(in + 4) != FORMAT_VERSION || (in[6] != LOG2_CHUNK && in[6] != RAW_FORM)) return ZCO_ERR_CORRUPT;
   int e0 = in[7];
   if (e0 > E0_MAX) return ZCO_ERR_CORRUPT;
   if (get_u64(in + 8) != n) return ZCO_ERR_SIZE_MISMATCH;
+  uint64_t total = get_u64(in + 24);
+
+  if (in[6] == RAW_FORM) { /* R7: header, the values as they are, zero padding */
+    if (get_u64(in + 16) != 0 || total != zco_raw_stream_bytes(n) || total > in_bytes) return ZCO_ERR_CORRUPT;
+    for (uint64_t i = 0; i < n; ++i) out[i] = get_u16(in + HEADER_BYTES + 2u * i);
+    if (!all_zero(in + HEADER_BYTES + 2u * n, total - HEADER_BYTES - 2u * n)) return ZCO_ERR_CORRUPT;
+    return ZCO_OK;
+  }
+
   uint64_t N = zco_num_chunks(n);
   if (get_u64(in + 16) != N) return ZCO_ERR_CORRUPT;
-  uint64_t total = get_u64(in + 24);
   uint64_t base = zco_records_base(n);
-  if (total > in_bytes || total > zco_max_stream_bytes(n) || total < escape_base(n)) return ZCO_ERR_CORRUPT;
+  /* a coded stream is never longer than the raw form (R7), nor shorter than its fixed parts */
+  if (total > in_bytes || total > zco_raw_stream_bytes(n) || total < escape_base(n)) return ZCO_ERR_CORRUPT;
   if (!all_zero(in + HEADER_BYTES + 8u * (N + 1), base - (HEADER_BYTES + 8u * (N + 1))))
     return ZCO_ERR_CORRUPT;
 

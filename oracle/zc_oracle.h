@@ -11,7 +11,8 @@
  * contribution", first technique (theoretically grounded exponent coding): a window of
  * frequent exponents is taken directly from the tensor's standard deviation, in-window
  * exponents are stored in 3 bits, out-of-window exponents are kept whole in a separate
- * list, and sign and mantissa travel unchanged, for roughly 11 bits per value.  The page
+ * list, and sign and mantissa travel unchanged, for roughly 11 bits per value; where that
+ * coding does not pay, the tensor travels in its native form (third technique).  The page
  * fixes neither the window rule's constant nor a byte layout; the readings used here are
  * stated beside each function in zc_oracle.c.
  *
@@ -20,8 +21,9 @@
  *       against math.fsum; window rule checked against a Gaussian escape-rate argmin; the
  *       constant re-derived with mpmath).
  *   zco_compress / zco_decompress -- pinned against the format readings (hand-derived
- *       stream fixture, closed-form size, exhaustive round trips, bijection under byte
- *       flips); the byte layout itself has no counterpart on the pages.
+ *       stream fixtures of the coded form with a list and with a plane, and of the raw form;
+ *       closed-form size; exhaustive round trips; bijection under byte flips); the byte
+ *       layout itself has no counterpart on the pages.
  */
 #ifndef ZC_ORACLE_H
 #define ZC_ORACLE_H
@@ -47,7 +49,8 @@ extern "C" {
 uint64_t zco_num_chunks(uint64_t n);
 uint64_t zco_records_base(uint64_t n);
 uint64_t zco_record_bytes(uint64_t m, uint64_t k);
-uint64_t zco_max_stream_bytes(uint64_t n);
+uint64_t zco_max_stream_bytes(uint64_t n); /* the longest stream: the raw form's length */
+uint64_t zco_raw_stream_bytes(uint64_t n); /* 32-byte header + n values, zero-padded to 16 */
 
 /* The constant c^2 of the window rule (fp64). */
 double zco_window_constant(void);
@@ -64,7 +67,8 @@ int zco_choose_e0(const uint16_t* x, uint64_t n);
 
 /* Compress n BF16 bit patterns.  base_or_auto is -1 (choose e0 from the data) or a base in
  * [0, 249].  Writes the stream to out (capacity cap bytes) and returns its length, or a
- * negative status (-ZCO_ERR_...). */
+ * negative status (-ZCO_ERR_...).  The stream is the coded form, or the raw form when the
+ * coded one would be longer. */
 int64_t zco_compress(const uint16_t* x, uint64_t n, int base_or_auto, uint8_t* out, uint64_t cap);
 
 /* Decompress a stream of in_bytes bytes into n BF16 bit patterns.  Returns ZCO_OK, or

@@ -25,22 +25,39 @@ def load_golden(name):
     return fields
 
 
-def _golden_stream(name):
+def golden_stream(name):
+    """(e0, values, stream) of a fixture.  'values' lists hex BF16 patterns, 'hex*count' for a run;
+    the stream is 'length' bytes, zero except for the 'bytes OFFSET' lines (hex, spaces allowed)."""
     import numpy as np
 
     g = load_golden(name)
-    values = np.array([int(v, 16) for v in " ".join(g["values"]).split()], dtype=np.uint16)
-    stream = np.frombuffer(bytes.fromhex("".join(g["stream"])), dtype=np.uint8)
-    return int(g["e0"][0]), values, stream
+    vals = []
+    for tok in " ".join(g["values"]).split():
+        v, _, count = tok.partition("*")
+        vals += [int(v, 16)] * (int(count) if count else 1)
+    stream = np.zeros(int(g["length"][0]), dtype=np.uint8)
+    for key, lines in g.items():
+        if key.startswith("bytes "):
+            off = int(key.split()[1])
+            data = bytes.fromhex("".join(lines).replace(" ", ""))
+            assert off + len(data) <= stream.size, (name, key)
+            stream[off:off + len(data)] = np.frombuffer(data, np.uint8)
+    return int(g["e0"][0]), np.array(vals, dtype=np.uint16), stream
 
 
 @pytest.fixture(scope="session")
-def golden_tiny():
-    """Five values whose two escapes are kept as an exponent plane (3k > m)."""
-    return _golden_stream("tiny_stream.txt")
+def golden_raw():
+    """Five values stored in the raw form (their coded form would be longer)."""
+    return golden_stream("tiny_raw_stream.txt")
 
 
 @pytest.fixture(scope="session")
-def golden_tiny_list():
-    """Seven values whose two escapes are kept as a (position, exponent) list (3k <= m)."""
-    return _golden_stream("tiny_list_stream.txt")
+def golden_plane():
+    """Two chunks (4096 + 5 values); chunk 1 keeps its two escapes as an exponent plane."""
+    return golden_stream("two_chunk_plane_stream.txt")
+
+
+@pytest.fixture(scope="session")
+def golden_list():
+    """Two chunks (4096 + 7 values); both keep their escapes as (position, exponent) lists."""
+    return golden_stream("two_chunk_list_stream.txt")

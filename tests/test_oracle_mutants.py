@@ -15,7 +15,7 @@ import subprocess
 import numpy as np
 import pytest
 
-from conftest import ROOT, load_golden
+from conftest import ROOT, golden_stream
 
 SRC = os.path.join(ROOT, "oracle", "zc_oracle.c")
 C2 = float.fromhex("0x1.79a1e790e0f01p-10")
@@ -39,9 +39,18 @@ MUTANTS = {
                                    "        esc[r] = (uint8_t)E;"),
     "offset_table_shifted": ("    put_u64(out + HEADER_BYTES + 8u * c, esc_pos);",
                              "    put_u64(out + HEADER_BYTES + 8u * c, esc_pos + 16u);"),
-    "max_stream_lists_only": ("  for (uint64_t c = 0; c < N; ++c) total += pad16(chunk_len(n, c)); /* a plane: the largest section */",
-                              "  for (uint64_t c = 0; c < N; ++c) total += pad16(3u * chunk_len(n, c));"),
-    "version_2": ("#define FORMAT_VERSION 3u", "#define FORMAT_VERSION 2u"),
+    "version_3": ("#define FORMAT_VERSION 4u", "#define FORMAT_VERSION 3u"),
+    "raw_rule_ge": ("  const int raw_form = coded > raw; /* R7: ties keep the coded form */",
+                    "  const int raw_form = coded >= raw;"),
+    "raw_never": ("  const int raw_form = coded > raw; /* R7: ties keep the coded form */",
+                  "  const int raw_form = 0; (void)raw;"),
+    "raw_values_byte_swapped": ("    for (uint64_t i = 0; i < n; ++i) put_u16(out + HEADER_BYTES + 2u * i, x[i]);",
+                                "    for (uint64_t i = 0; i < n; ++i) put_u16(out + HEADER_BYTES + 2u * i, (uint16_t)((x[i] << 8) | (x[i] >> 8)));"),
+    "raw_unpadded": ("uint64_t zco_raw_stream_bytes(uint64_t n) { return HEADER_BYTES + pad16(2u * n); }",
+                     "uint64_t zco_raw_stream_bytes(uint64_t n) { return HEADER_BYTES + 2u * n; }"),
+    "raw_form_marker": ("#define RAW_FORM 0u /* header byte 6 of a raw stream (R7) */", "#define RAW_FORM 1u"),
+    "coded_length_unbounded": ("  if (total > in_bytes || total > zco_raw_stream_bytes(n) || total < escape_base(n)) return ZCO_ERR_CORRUPT;",
+                               "  if (total > in_bytes || total < escape_base(n)) return ZCO_ERR_CORRUPT;"),
     "floor_half_truncates": ("static int floor_half(int v) { return v >= 0 ? v / 2 : -((-v + 1) / 2); }",
                              "static int floor_half(int v) { return v / 2; }"),
     "constant_typo": ("static const double WINDOW_C2 = 0x1.79a1e790e0f01p-10;",
@@ -109,6 +118,7 @@ def bf16_value(b):
 
 
 def size_formula(x, e0):
+    """The coded form's length from the size formula, or the raw form's when that is shorter."""
     n = x.size
     N = (n + 4095) // 4096
     E = (x.astype(np.int64) >> 7) & 0xFF
@@ -118,7 +128,16 @@ def size_formula(x, e0):
         m = min(4096, n - 4096 * c)
         k = int(esc[4096 * c:4096 * c + m].sum())
         total += pad16((3 * m + 7) // 8) + pad16(m) + (pad16(m) if 3 * k > m else pad16(3 * k))
-    return total
+    return min(total, 32 + pad16(2 * n))
+
+
+# The coded form of the five values of tiny_raw_stream.txt under e0 = 127, worked out by hand
+# there (96 bytes: header, table, codes, sign|mantissa plane, an exponent plane).  It is longer
+# than the raw form (48 bytes), so no encoder writes it and the decoder must reject it.
+NONCANONICAL_CODED = bytes.fromhex(
+    "5a43423104000c7f0500000000000000" "01000000000000006000000000000000"
+    "50000000000000006000000000000000" "c87d0000000000000000000000000000"
+    "00a00048410000000000000000000000" "7f800085ff0000000000000000000000")
 
 
 def window_rule_for_constant(v, n):
@@ -131,21 +150,24 @@ def window_rule_for_constant(v, n):
 def checks(o):
     """Names of the independent checks that fail for this oracle build."""
     failed = []
-    for fixture in ("tiny_stream.txt", "tiny_list_stream.txt"):
-        g = load_golden(fixture)
-        vals = np.array([int(v, 16) for v in " ".join(g["values"]).split()], np.uint16)
-        want = np.frombuffer(bytes.fromhex("".join(g["stream"])), np.uint8).copy()
-        got = o.compress(vals, int(g["e0"][0]))
+    for fixture in ("tiny_raw_stream.txt", "two_chunk_plane_stream.txt", "two_chunk_list_stream.txt"):
+        e0, vals, want = golden_stream(fixture)
+        got = o.compress(vals, e0)
         if got is None or got.tobytes() != want.tobytes():
             failed.append(f"golden {fixture}")
         st, back = o.decompress(want, vals.size)
         if st != 0 or not np.array_equal(back, vals):
             failed.append(f"golden decode {fixture}")
-    g = load_golden("tiny_stream.txt")  # a plane byte moved into the window must be rejected
-    bad = np.frombuffer(bytes.fromhex("".join(g["stream"])), np.uint8).copy()
-    bad[80 + 1] = 129
-    if o.decompress(bad, 5)[0] == 0:
+    e0, vals, bad = golden_stream("two_chunk_plane_stream.txt")  # a plane byte moved into the window
+    bad[5744 + 1] = 129
+    if o.decompress(bad, vals.size)[0] == 0:
         failed.append("plane corruption accepted")
+    if o.decompress(np.frombuffer(NONCANONICAL_CODED, np.uint8).copy(), 5)[0] == 0:
+        failed.append("coded stream longer than the raw form accepted")
+    tie = np.full(37, 0x3F80, np.uint16)  # coded: 48 + 16 + 48 = 112 bytes; raw: 32 + 80 = 112
+    s = o.compress(tie, 127)
+    if s is None or len(s) != 112 or s[6] != 12:
+        failed.append("a tie keeps the coded form")
     rng = np.random.default_rng(11)
     samples = [rng.integers(0, 1 << 16, 5000).astype(np.uint16),
                rng.integers(0, 0x0100, 3000).astype(np.uint16),  # subnormals and zeros
@@ -173,26 +195,23 @@ def checks(o):
             failed.append("round trip")
             break
     for n in (1, 5000, 12345):
-        N = (n + 4095) // 4096
-        rem = n % 4096
-        want = pad16(32 + 8 * (N + 1)) + (n // 4096) * (5632 + 4096) + (
-            pad16((3 * rem + 7) // 8) + pad16(rem) + pad16(rem) if rem else 0)
-        if o.lib.zco_max_stream_bytes(n) != want:
+        if o.lib.zco_max_stream_bytes(n) != 32 + pad16(2 * n):
             failed.append("worst-case size")
             break
     for m in range(1, 24):  # the list-or-plane boundary, both sides of 3k = m
         for k in (m // 3, m // 3 + 1):
             if k > m:
                 continue
-            # k zeros (exponent 0, escapes for e0 = 127) then 1.0s (exponent 127, code 0)
-            x = np.array([0x0000] * k + [0x3F80] * (m - k), np.uint16)
+            # a chunk of 1.0s keeps the coded form; then k zeros (exponent 0, escapes for
+            # e0 = 127) and 1.0s (exponent 127, code 0)
+            x = np.array([0x3F80] * 4096 + [0x0000] * k + [0x3F80] * (m - k), np.uint16)
             if 3 * k > m:  # a plane: every exponent in value order
                 section = bytes([0] * k + [127] * (m - k))
             else:  # a list: u16 positions 0..k-1, then k exponent bytes 0
                 section = b"".join(i.to_bytes(2, "little") for i in range(k)) + bytes(k)
             section += bytes(pad16(len(section)) - len(section))
             s = o.compress(x, 127)
-            ok = s is not None and len(s) == size_formula(x, 127) and o.decompress(s, m)[0] == 0
+            ok = s is not None and len(s) == size_formula(x, 127) and o.decompress(s, x.size)[0] == 0
             if not ok or (section and s[len(s) - len(section):].tobytes() != section):
                 failed.append("list/plane boundary")
                 break

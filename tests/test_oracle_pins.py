@@ -35,8 +35,8 @@ def escape_section(m, k):
     return pad16(m) if 3 * k > m else pad16(3 * k)
 
 
-def closed_form_size(x, e0):
-    """Stream length from the size formula, with escapes counted by a per-chunk histogram."""
+def coded_size(x, e0):
+    """Length of the coded form from the size formula, escapes counted per chunk."""
     n = x.size
     N = (n + CHUNK - 1) // CHUNK
     E = (x.astype(np.int64) >> 7) & 0xFF
@@ -49,11 +49,22 @@ def closed_form_size(x, e0):
     return total
 
 
+def raw_size(n):
+    """The raw form: 32-byte header, then the n values, zero-padded to 16 bytes."""
+    return 32 + pad16(2 * n)
+
+
+def closed_form_size(x, e0):
+    """Stream length: the coded form, or the raw form when the coded one is longer."""
+    return min(coded_size(x, e0), raw_size(x.size))
+
+
 # ----------------------------------------------------------------------------- golden
 
 
-def test_golden_list_stream_matches_hand_derivation(golden_tiny_list):
-    e0, values, stream = golden_tiny_list
+@pytest.mark.parametrize("fixture", ["golden_raw", "golden_plane", "golden_list"])
+def test_golden_streams_match_hand_derivation(fixture, request):
+    e0, values, stream = request.getfixturevalue(fixture)
     got = oracle.compress(values, e0)
     assert got.tobytes() == stream.tobytes()
     st, back = oracle.decompress(stream, values.size)
@@ -61,29 +72,50 @@ def test_golden_list_stream_matches_hand_derivation(golden_tiny_list):
 
 
 def test_list_or_plane_at_the_boundary():
-    """3k <= m keeps a list, 3k > m a plane, whichever is smaller; the codes are the same."""
+    """3k <= m keeps a list, 3k > m a plane, whichever is smaller; the codes are the same.  A
+    first chunk of 4096 in-window values keeps the stream in the coded form."""
     e0 = 127
     inside, outside = 0x3F80, 0x0000  # exponents 127 (code 0) and 0 (an escape)
+    head = [inside] * CHUNK
     for m in range(1, 40):
         for k in range(0, m + 1):
-            x = np.array([outside] * k + [inside] * (m - k), np.uint16)
+            x = np.array(head + [outside] * k + [inside] * (m - k), np.uint16)
             s = oracle.compress(x, e0)
-            section = len(s) - (48 + pad16((3 * m + 7) // 8) + pad16(m))
+            fixed_end = pad16(32 + 8 * 3) + 5632 + pad16((3 * m + 7) // 8) + pad16(m)
+            section = len(s) - fixed_end
             assert section == (pad16(m) if 3 * k > m else pad16(3 * k)), (m, k)
             assert section == min(pad16(m), pad16(3 * k))
             if 3 * k > m:  # a plane: one exponent byte per value, in value order
                 assert s[-section:][:m].tolist() == [0] * k + [127] * (m - k)
-            st, back = oracle.decompress(s, m)
+            st, back = oracle.decompress(s, CHUNK + m)
             assert st == oracle.OK and np.array_equal(back, x)
 
 
-def test_golden_stream_matches_hand_derivation(golden_tiny):
-    e0, values, stream = golden_tiny
-    got = oracle.compress(values, e0)
-    assert got.tobytes() == stream.tobytes()
-    st, back = oracle.decompress(stream, values.size)
-    assert st == oracle.OK
-    assert np.array_equal(back, values)
+def test_raw_form_exactly_when_the_coded_form_is_longer():
+    """The native form is chosen exactly when the coded form would be longer than the 32-byte
+    header plus the values; ties keep the coded form."""
+    rng = np.random.default_rng(21)
+    seen = {True: 0, False: 0}
+    for n in [1, 2, 7, 37, 38, 100, 171, 600, 4095, 4096, 4097, 9000]:
+        for frac in (0.0, 0.01, 0.05, 0.2, 0.3, 0.5, 1.0):
+            e = rng.integers(120, 127, n)  # in the window of e0 = 120
+            x = ((rng.integers(0, 2, n) << 15) | (e << 7) | rng.integers(0, 128, n)).astype(np.uint16)
+            esc = rng.random(n) < frac
+            x[esc] = rng.integers(0, 0x0100, int(esc.sum())).astype(np.uint16)  # exponents 0, 1
+            s = oracle.compress(x, 120)
+            raw = coded_size(x, 120) > raw_size(n)
+            seen[raw] += 1
+            assert len(s) == (raw_size(n) if raw else coded_size(x, 120)), (n, frac)
+            assert (s[6] == 0) == raw  # byte 6: 0 for the raw form, 12 for the coded one
+            if raw:
+                assert s[32:32 + 2 * n].tobytes() == x.tobytes()  # the values as they are
+            st, back = oracle.decompress(s, n)
+            assert st == oracle.OK and np.array_equal(back, x)
+    assert seen[True] > 10 and seen[False] > 10
+    # a tie: 37 in-window values cost 48 + 16 + 48 = 112 bytes either way -> coded
+    x = np.full(37, 0x3F80, np.uint16)
+    assert coded_size(x, 127) == raw_size(37) == 112
+    assert oracle.compress(x, 127)[6] == 12
 
 
 # ----------------------------------------------------------------------------- window rule
@@ -256,13 +288,12 @@ def test_all_patterns_round_trip_every_base():
 
 
 def test_every_pattern_as_single_value():
+    """One value: the coded form takes at least 48 + 16 + 16 bytes, the raw form 48."""
     x = workloads.all_patterns()
     for b in x:
         one = np.array([b], np.uint16)
         s = oracle.compress(one)
-        E = (int(b) >> 7) & 0xFF
-        k = 0 if s[7] <= E <= s[7] + 6 else 1
-        assert len(s) == 48 + 16 + 16 + 16 * k  # header+table, codes, byte plane, escapes
+        assert len(s) == 48 and s[6] == 0 and s[32:34].tobytes() == one.tobytes()
         st, back = oracle.decompress(s, 1)
         assert st == oracle.OK and back[0] == b
 
@@ -308,68 +339,107 @@ def test_brute_force_triples():
 # ----------------------------------------------------------------------------- canonical form
 
 
-def _bijection_under_flips(stream, n):
+def _bijection_under_flips(stream, n, positions=None):
+    """Every single-bit flip is rejected, or decodes to values whose stream is the flipped one.
+    The one exception the format allows: a raw stream is accepted for values whose coded form
+    is shorter (the decoder does not recompute the form choice)."""
     accepted = 0
-    for pos in range(len(stream)):
+    for pos in (range(len(stream)) if positions is None else positions):
         for bit in range(8):
             t = stream.copy()
             t[pos] ^= 1 << bit
             st, back = oracle.decompress(t, n)
             if st == oracle.OK:
-                # an accepted stream must be exactly what the encoder writes for its content
-                assert oracle.compress(back, int(t[7])).tobytes() == t.tobytes(), (pos, bit)
+                again = oracle.compress(back, int(t[7]))
+                if t[6] == 0 and again[6] != 0:
+                    assert len(again) <= len(t), (pos, bit)
+                else:
+                    assert again.tobytes() == t.tobytes(), (pos, bit)
                 accepted += 1
     return accepted
 
 
-def test_decoder_accepts_only_canonical_streams(golden_tiny):
-    e0, values, stream = golden_tiny
-    accepted = _bijection_under_flips(stream, values.size)
-    assert accepted > 0  # flips of sign/mantissa bits or in-window codes stay valid
+def _interesting_positions(stream):
+    """Header, table, chunk 1's fixed part, the escape region, and every 61st byte of chunk 0."""
+    return sorted(set(range(64)) | set(range(0, 5696, 61)) | {1599} | set(range(5696, len(stream))))
+
+
+def test_decoder_accepts_only_canonical_streams(golden_raw, golden_plane, golden_list):
+    for e0, values, stream in (golden_raw, golden_plane, golden_list):
+        pos = None if stream.size < 100 else _interesting_positions(stream)
+        assert _bijection_under_flips(stream, values.size, pos) > 0
     rng = np.random.default_rng(3)
-    x = workloads.fp32_to_bf16_bits(rng.standard_normal(37).astype(np.float32))
-    _bijection_under_flips(oracle.compress(x), x.size)
+    x = workloads.fp32_to_bf16_bits(rng.standard_normal(300).astype(np.float32))
+    s = oracle.compress(x)
+    assert s[6] == 12
+    _bijection_under_flips(s, x.size)
 
 
-def test_decoder_accepts_only_canonical_list_streams(golden_tiny_list):
-    e0, values, stream = golden_tiny_list
-    assert _bijection_under_flips(stream, values.size) > 0
+def test_decoder_rejections_plane(golden_plane):
+    """The plane form (chunk 1: five values, two escapes; its section at 5744)."""
+    e0, values, stream = golden_plane
+    n = values.size
+    assert oracle.decompress(stream, n + 1)[0] == oracle.ERR_SIZE_MISMATCH
+    assert oracle.decompress(stream[:-16], n)[0] == oracle.ERR_CORRUPT  # truncated
+    for pos, val in [(0, 0),          # magic
+                     (4, 3),          # version 3
+                     (6, 11),         # another chunk size
+                     (7, 250),        # base out of range
+                     (5744 + 6, 1),   # nonzero plane padding (after 5 bytes)
+                     (5744 + 4, 130),  # an escaped value's exponent inside the window
+                     (5744 + 1, 129),  # an in-window value's exponent other than e0 + code
+                     (5696, 0xCF)]:   # code 0 -> 7: the plane holds 127, inside the window
+        t = stream.copy()
+        t[pos] = val
+        assert oracle.decompress(t, n)[0] == oracle.ERR_CORRUPT, (pos, val)
 
 
-def test_decoder_rejections(golden_tiny):
-    """The plane form (five values, two escapes)."""
-    e0, values, stream = golden_tiny
+def test_decoder_rejections_list(golden_list):
+    """The list form (chunk 0: one escape, its section at 5728; chunk 1: two, at 5744)."""
+    e0, values, stream = golden_list
+    n = values.size
+    for pos, val in [(5744, 3),       # first position names an in-window value
+                     (5746, 2),       # positions not increasing
+                     (5744 + 4, 130),  # escape exponent inside the window
+                     (5744 + 6, 1),   # nonzero list padding (after 2 + 2 + 1 + 1 bytes)
+                     (5696, 0xCF),    # code 0 -> 7: three escapes, the section must be a plane
+                     (5728, 0xFE),    # chunk 0's escape names value 4094 (code 0)
+                     (1599, 0x60),    # chunk 0's escape loses its code 7
+                     (40, 0x71)]:     # chunk 1's escape offset moved
+        t = stream.copy()
+        t[pos] = val
+        assert oracle.decompress(t, n)[0] == oracle.ERR_CORRUPT, (pos, val)
+
+
+def test_decoder_rejections_raw(golden_raw):
+    """The raw form: byte 6 = 0, N = 0, total = 32 + pad16(2n), zero padding."""
+    e0, values, stream = golden_raw
     assert oracle.decompress(stream, 6)[0] == oracle.ERR_SIZE_MISMATCH
     assert oracle.decompress(stream[:-16], 5)[0] == oracle.ERR_CORRUPT  # truncated
-    t = stream.copy(); t[0] = 0  # magic  # noqa: E702
-    assert oracle.decompress(t, 5)[0] == oracle.ERR_CORRUPT
-    t = stream.copy(); t[4] = 2  # the list-only version  # noqa: E702
-    assert oracle.decompress(t, 5)[0] == oracle.ERR_CORRUPT
-    t = stream.copy(); t[7] = 250  # base out of range  # noqa: E702
-    assert oracle.decompress(t, 5)[0] == oracle.ERR_CORRUPT
-    t = stream.copy(); t[80 + 6] = 1  # nonzero plane padding (after 5 bytes)  # noqa: E702
-    assert oracle.decompress(t, 5)[0] == oracle.ERR_CORRUPT
-    t = stream.copy(); t[80 + 4] = 130  # escaped value's exponent inside the window  # noqa: E702
-    assert oracle.decompress(t, 5)[0] == oracle.ERR_CORRUPT
-    t = stream.copy(); t[80 + 1] = 129  # in-window value's exponent other than e0 + code  # noqa: E702
-    assert oracle.decompress(t, 5)[0] == oracle.ERR_CORRUPT
-    t = stream.copy(); t[48] |= 0x07  # code 0 -> 7: the plane holds 127, inside the window  # noqa: E702
-    assert oracle.decompress(t, 5)[0] == oracle.ERR_CORRUPT
+    for pos, val in [(6, 12),   # read as a coded stream: N = 0 is not ceil(5/4096)
+                     (16, 1),   # N = 1 in a raw stream
+                     (24, 64),  # total is not 48
+                     (42, 1),   # nonzero padding after the 10 value bytes
+                     (4, 3),    # version 3
+                     (7, 250)]:  # base out of range
+        t = stream.copy()
+        t[pos] = val
+        assert oracle.decompress(t, 5)[0] == oracle.ERR_CORRUPT, (pos, val)
 
 
-def test_decoder_rejections_list(golden_tiny_list):
-    """The list form (seven values, two escapes)."""
-    e0, values, stream = golden_tiny_list
-    t = stream.copy(); t[80] = 3  # first position names an in-window value  # noqa: E702
-    assert oracle.decompress(t, 7)[0] == oracle.ERR_CORRUPT
-    t = stream.copy(); t[82] = 2  # positions not increasing  # noqa: E702
-    assert oracle.decompress(t, 7)[0] == oracle.ERR_CORRUPT
-    t = stream.copy(); t[80 + 4] = 130  # escape exponent inside the window  # noqa: E702
-    assert oracle.decompress(t, 7)[0] == oracle.ERR_CORRUPT
-    t = stream.copy(); t[80 + 6] = 1  # nonzero list padding (after 2+2+1+1 bytes)  # noqa: E702
-    assert oracle.decompress(t, 7)[0] == oracle.ERR_CORRUPT
-    t = stream.copy(); t[48] |= 0x07  # code 0 -> 7: one more escape than the list holds  # noqa: E702
-    assert oracle.decompress(t, 7)[0] == oracle.ERR_CORRUPT
+def test_raw_stream_of_a_compressible_tensor_is_accepted(golden_plane):
+    """The decoder checks a raw stream's bytes but does not recompute the form choice: the raw
+    form of a tensor whose coded form is shorter still decodes to its values."""
+    e0, values, stream = golden_plane
+    n = values.size
+    raw = np.zeros(raw_size(n), np.uint8)
+    raw[:4] = np.frombuffer(b"ZCB1", np.uint8)
+    raw[4], raw[7] = 4, e0
+    raw[8:16] = np.frombuffer(np.uint64(n).tobytes(), np.uint8)
+    raw[24:32] = np.frombuffer(np.uint64(raw.size).tobytes(), np.uint8)
+    raw[32:32 + 2 * n] = np.frombuffer(values.tobytes(), np.uint8)
+    st, back = oracle.decompress(raw, n)
+    assert st == oracle.OK and np.array_equal(back, values)
 
 
 # ----------------------------------------------------------------------------- statistics
