@@ -15,9 +15,10 @@
  * memory access, data movement pipelined with compute) is what the
  * kernels behind these calls implement for sm_103a.
  *
- * Stream format "ZCB1", version 3 (little-endian, every section zero-padded to 16 bytes):
- *   header    32 B  "ZCB1", u16 version = 3, u8 log2(chunk) = 12, u8 e0, u64 n, u64 N,
- *                   u64 total_bytes                      (N = ceil(n / 4096) chunks)
+ * Stream format "ZCB1", version 4 (little-endian, every section zero-padded to 16 bytes):
+ *   header    32 B  "ZCB1", u16 version = 4, u8 form, u8 e0, u64 n, u64 N, u64 total_bytes.
+ *             form = 12 (log2 of the chunk size) for the coded form, 0 for the raw form.
+ * Coded form (N = ceil(n / 4096) chunks):
  *   offsets   u64[N+1]: absolute byte offset of each chunk's escape section; offsets[N] =
  *             total_bytes.  Zero padding to R0 = pad16(32 + 8 (N+1)).
  *   fixed     for chunk c (m values), at R0 + 5632 c: 3-bit codes, code i at bits [3i, 3i+3)
@@ -30,8 +31,13 @@
  *             positions then u8 full exponents in ascending position order (pad16(3k) B);
  *             otherwise the u8 exponents of all m values in value order (pad16(m) B).
  *   Code c < 7 means exponent e0 + c; code 7 means "escape".  e0 is in [0, 249].
- * A full chunk without escapes costs 5632 B for 4096 values: 11 bits per value.  A full chunk
- * costs at most 9728 B (a plane): 19 bits per value.
+ * Raw form (N = 0): the n values as they are (2n B), zero padding; total_bytes =
+ *   32 + pad16(2n).  A tensor whose coded form would be longer than its raw form is stored raw
+ *   (the same section's third technique switches a transfer to the native path where
+ *   compressing does not pay); ties keep the coded form.  So no stream is longer than its
+ *   values plus 32 bytes (and 15 of padding).
+ * A full chunk without escapes costs 5632 B for 4096 values: 11 bits per value.  A full coded
+ * chunk costs at most 9728 B (a plane), but a coded stream is never longer than the raw form.
  *
  * All entry points are host functions.  Pointers called "device" may be any address the GPU
  * can dereference (cudaMalloc, managed, or mapped pinned memory).  Every call is
@@ -65,20 +71,23 @@ typedef struct CUstream_st* cudaStream_t; /* the CUDA runtime's own stream handl
 
 /* ------------------------------------------------------------------ sizes */
 
-/* Bytes the caller must provide at `out` for zc_compress of n values: the worst-case stream
- * (9,728 B per full chunk: its fixed part and an exponent plane, plus header and offset table)
- * followed by the call's workspace (scan state, 8 B per chunk, and a 16.25 KiB control block).
- * Pure host function; makes no CUDA call.  Returns 0 when n > ZC_MAX_N. */
+/* Bytes the caller must provide at `out` for zc_compress of n values: zc_max_stream_bytes(n),
+ * rounded up to 256, followed by the call's workspace (scan state, 8 B per chunk, and a
+ * 16.25 KiB control block).  Pure host function; makes no CUDA call.  Returns 0 when
+ * n > ZC_MAX_N. */
 size_t zc_max_compressed_bytes(size_t n);
 
-/* Worst-case stream length alone (no workspace).  Pure host function. */
+/* Bytes of `out` that the stream may occupy while it is written: the larger of the raw form's
+ * length, 32 + pad16(2n) (no stream is longer), and the end of the coded fixed parts, which
+ * are written before the form is known (larger only for n below about 100).  Pure host
+ * function.  Returns 0 when n > ZC_MAX_N. */
 size_t zc_max_stream_bytes(size_t n);
 
 /* ------------------------------------------------------------------ compress */
 
 /* Compress n BF16 values (raw bit patterns) into one "ZCB1" stream.
  *   in            device, n x u16, 16-byte aligned, read only.
- *   n             number of values, 0 <= n <= ZC_MAX_N.  n = 0 gives a 48-byte stream.
+ *   n             number of values, 0 <= n <= ZC_MAX_N.  n = 0 gives a 32-byte (raw) stream.
  *   base_or_auto  ZC_BASE_AUTO: e0 = floor(log2(sigma * c)) + 127 clamped to [0, 249], with
  *                 sigma the root mean square of the finite values and c^2 =
  *                 0x1.79a1e790e0f01p-10 (the window with the fewest expected escapes for a
@@ -86,8 +95,10 @@ size_t zc_max_stream_bytes(size_t n);
  *                 histogram or sort).  0..249: use that e0.  The stream depends only on
  *                 (input bits, e0): both modes give identical bytes for the same e0.
  *   out           device, zc_max_compressed_bytes(n) bytes, 16-byte aligned, must not overlap
- *                 `in`.  The stream is written from out[0]; the bytes past *out_bytes,
- *                 including the workspace tail, are unspecified afterwards.  The library keeps
+ *                 `in`.  The stream is written from out[0]: the coded form, or the raw form
+ *                 when that is shorter (decided on the device after the scan, so no host
+ *                 synchronization); the bytes past *out_bytes, including the workspace tail,
+ *                 are unspecified afterwards.  The library keeps
  *                 no per-call state outside `out`, so calls on different streams with
  *                 different buffers may run concurrently.  The encode kernel's CTAs wait on
  *                 one another (bounded) only for work that a CTA already running has taken,
@@ -116,9 +127,11 @@ int zc_compress(const void* in, size_t n, int base_or_auto, void* out, size_t* o
  *   out     device, n x u16, 16-byte aligned, must not overlap `in`.
  *   n       the number of values the caller expects; a stream holding another n sets
  *           ZC_ERR_SIZE_MISMATCH.
- * Any stream the encoder could not have written (bad magic, version, base, offsets, sizes,
- * escape positions or exponents, nonzero padding) sets ZC_ERR_CORRUPT; `out` is then
- * unspecified.  Device-side errors are read with zc_status. */
+ * Any stream the encoder could not have written (bad magic, version, form, base, offsets,
+ * sizes, escape positions or exponents, nonzero padding, a coded stream longer than the raw
+ * form) sets ZC_ERR_CORRUPT; `out` is then unspecified.  A raw stream is checked byte for byte
+ * (header, length, padding), but whether its coded form would have been shorter is not
+ * recomputed.  Device-side errors are read with zc_status. */
 int zc_decompress(const void* in, void* out, size_t n, cudaStream_t stream);
 
 /* ------------------------------------------------------------------ status */
@@ -133,6 +146,7 @@ int zc_status(cudaStream_t stream, int reset);
 #define ZC_KERNEL_STATS 1
 #define ZC_KERNEL_ENCODE 2
 #define ZC_KERNEL_DECODE 3
+#define ZC_KERNEL_RAW 4    /* the step that rewrites a stream in the raw form when that is shorter */
 
 /* enable != 0: bracket every kernel the library launches from now on with CUDA events on the
  * kernel's own stream.  enable == 0: stop recording.  Returns ZC_OK or ZC_ERR_CUDA. */
@@ -153,7 +167,8 @@ int zc_timing_collect(int* kernel_ids, float* ms, int max);
  * not call cudaMalloc on its progress path.  The paper has no counterpart: it is an interface
  * for such callers.
  * Arguments, stream and results are those of zc_compress, except:
- *   - `out` needs only zc_max_stream_bytes(n) bytes: the call's workspace lives in a
+ *   - `out` needs only zc_max_stream_bytes(n) bytes (about the size of the input): the
+ *     call's workspace lives in a
  *     file-scope 2 MiB device array of the library instead of the tail of `out`.  That array
  *     exists on every GPU that loads the library until the process exits.
  *   - n > ZC_STATIC_SCRATCH_MAX_N returns ZC_ERR_INVALID_ARG.

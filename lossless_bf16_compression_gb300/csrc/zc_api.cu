@@ -5,7 +5,10 @@
 //   1. clear the workspace in the tail of `out` (one memset on `stream`);
 //   2. statistics kernel (auto mode only): sum of squares, non-finite count, e0;
 //   3. encode kernel: codes, sign|mantissa plane, escape sections, the single-pass chunk scan,
-//      the offset table and the lists compacted behind it.
+//      the offset table and the lists compacted behind it;
+//   4. raw-form step (third technique: the native path where compressing does not pay): when
+//      the coded stream came out longer than the header plus the values, the stream is
+//      rewritten in that raw form; otherwise the kernel returns at once.
 // zc_decompress is one decode kernel.  No call synchronizes except zc_status, and
 // zc_compress when `out_bytes` is pageable host memory.
 #include <cstring>
@@ -133,6 +136,7 @@ int compress_impl(const void* in, size_t n, int base, void* out, size_t* out_byt
   }
   if (launch_encode(x, n, base, o, len_ptr, ws, dev, stream, stall_chunk, spin_limit) != cudaSuccess)
     return ZC_ERR_CUDA;
+  if (launch_raw_form(x, n, base, o, len_ptr, ws, dev, stream) != cudaSuccess) return ZC_ERR_CUDA;
   if (pageable) {
     unsigned long long total = 0;
     const Control* ctrl = reinterpret_cast<const Control*>(ws);

@@ -14,22 +14,27 @@
 
 namespace zc {
 
-// ------------------------------------------------------------------ stream layout ("ZCB1" v3)
+// ------------------------------------------------------------------ stream layout ("ZCB1" v4)
 //
+// Coded form (header byte 6 = 12):
 // header (32 B) | u64 escape offsets [N+1] | zero pad to 16 | fixed parts | escape sections
 // The fixed part of chunk c (3-bit codes, then the sign|mantissa plane) starts at
 // records_base(n) + c * kFullFixedBytes, so its place follows from n alone; only the escape
 // sections are placed by the scan.  A chunk of m values with k escapes keeps them as a list (u16
 // positions, u8 exponents, zero pad) when 3k <= m, else as a plane of all m exponents (zero
 // pad): whichever is smaller, chosen from k, which the codes give.
+// Raw form (header byte 6 = 0, N = 0): header (32 B) | the n values | zero pad to 16.  A tensor
+// whose coded form would be longer than its raw form is stored raw (ties keep the coded form).
 constexpr int kChunk = 4096;                       // values per chunk
 constexpr int kHeaderBytes = 32;                   // stream header
 constexpr int kFullCodeBytes = 3 * kChunk / 8;     // 1536: 3-bit codes of a full chunk
 constexpr int kFullFixedBytes = kFullCodeBytes + kChunk;  // 5632: fixed part of a full chunk
 constexpr int kMaxEscapeBytes = kChunk;            // 4096: an exponent plane, the largest section
 constexpr int kE0Max = 249;
-constexpr unsigned long long kMagicWord =          // bytes 0..6 of the header: "ZCB1", v3, 12
-    0x5Aull | (0x43ull << 8) | (0x42ull << 16) | (0x31ull << 24) | (3ull << 32) | (12ull << 48);
+constexpr unsigned long long kRawMagicWord =       // bytes 0..6 of a raw header: "ZCB1", v4, 0
+    0x5Aull | (0x43ull << 8) | (0x42ull << 16) | (0x31ull << 24) | (4ull << 32);
+constexpr unsigned long long kMagicWord =          // bytes 0..6 of a coded header: "ZCB1", v4, 12
+    kRawMagicWord | (12ull << 48);
 
 __host__ __device__ constexpr uint64_t pad16(uint64_t v) { return (v + 15u) & ~uint64_t(15); }
 __host__ __device__ constexpr uint64_t num_chunks(uint64_t n) { return (n + kChunk - 1) / kChunk; }
@@ -57,9 +62,14 @@ __host__ __device__ inline bool exponent_plane(unsigned m, unsigned k) { return 
 __host__ __device__ inline unsigned escape_section_bytes(unsigned m, unsigned k) {
   return static_cast<unsigned>(exponent_plane(m, k) ? pad16(m) : pad16(3ull * k));
 }
+// Length of the raw form: the header, the n values, zero padding.
+__host__ __device__ constexpr uint64_t raw_stream_bytes(uint64_t n) { return kHeaderBytes + pad16(2 * n); }
+// Bytes of `out` that a call may write: the stream is at most raw_stream_bytes(n) long, and the
+// coded fixed parts, written before the form is known, end at escape_base(n).  (Escape sections
+// that would end past raw_stream_bytes(n) are never written: the stream is then raw.)
 __host__ __device__ inline uint64_t max_stream_bytes(uint64_t n) {
-  const uint64_t rem = n % kChunk;
-  return escape_base(n) + (n / kChunk) * kMaxEscapeBytes + pad16(rem);
+  const uint64_t e = escape_base(n), r = raw_stream_bytes(n);
+  return e > r ? e : r;
 }
 
 // ------------------------------------------------------------------ workspace (tail of `out`)
@@ -290,6 +300,10 @@ cudaError_t launch_encode(const uint16_t* in, uint64_t n, int base, uint8_t* out
                           unsigned spin_limit);
 cudaError_t launch_decode(const uint8_t* in, uint16_t* out, uint64_t n, const DeviceInfo& dev,
                           cudaStream_t stream);
+// After the encode kernel: when the coded stream came out longer than the raw form, rewrite the
+// stream in the raw form (header, the n values, zero padding); otherwise return at once.
+cudaError_t launch_raw_form(const uint16_t* in, uint64_t n, int base, uint8_t* out, unsigned long long* out_bytes,
+                            uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream);
 
 constexpr unsigned kDefaultSpinLimit = 1u << 20;  // polls of a bounded wait in the encoder
 

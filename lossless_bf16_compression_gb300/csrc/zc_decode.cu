@@ -20,8 +20,10 @@
 // escapes rather than to the busiest lane.  A section of a plane's size is built from instead
 // in the same single pass (sign|mantissa bytes plus the plane's exponents, each checked against
 // its code), and again from the codes in the rare case that the count shows a list of that size.
-// Every offset and size is checked before it is used, so a corrupt stream sets an error instead
-// of steering a read outside [0, total_bytes).
+// A raw stream (the values after the header, when coding did not pay: third technique) is
+// copied with 16-byte loads and stores, one chunk's worth per CTA.  Every offset and size is
+// checked before it is used, so a corrupt stream sets an error instead of steering a read
+// outside [0, total_bytes).
 #include "zc_common.cuh"
 
 namespace zc {
@@ -47,9 +49,32 @@ struct __align__(128) DecodeSmem {
   uint64_t mbar;
   unsigned escapes;  // code-7 count of the chunk, summed by the warps
   int ok;
+  int raw;  // the stream is in the raw form
   int e0;
   unsigned esc_bytes;
 };
+
+// A raw stream: chunk c's values are bytes [32 + 8192 c, 32 + 8192 c + 2m) of the stream, copied
+// with 16-byte loads and stores.  The last vector of the stream also holds its zero padding,
+// which is checked.  Every read lies inside [0, 32 + pad16(2n)) = [0, total_bytes).
+__device__ __noinline__ void raw_chunk(const uint8_t* in, uint16_t* out, int* status, uint64_t c, unsigned m) {
+  const uint4* src = reinterpret_cast<const uint4*>(in + kHeaderBytes) + c * (kChunk / 8);
+  uint4* dst = reinterpret_cast<uint4*>(out + c * kChunk);
+  const unsigned whole = m / 8;  // whole vectors of this chunk
+  for (unsigned i = threadIdx.x; i < whole; i += kChunkThreads) dst[i] = __ldcs(src + i);
+  if (m % 8 && threadIdx.x == 0) {  // the stream's last vector: m % 8 values, then zero padding
+    const uint4 v = src[whole];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint16_t* tail = out + c * kChunk + 8 * whole;
+    bool bad = false;
+    for (unsigned i = 0; i < 8; ++i) {
+      const uint16_t x = static_cast<uint16_t>(w[i >> 1] >> (16 * (i & 1)));
+      if (i < m % 8) tail[i] = x;
+      else bad |= x != 0;
+    }
+    if (bad) set_error(status, ZC_ERR_CORRUPT);
+  }
+}
 
 // A chunk whose escape section has the size of a plane: this thread's values built straight
 // from the plane's exponents, each exponent checked against its value's code.  Returns this
@@ -99,24 +124,27 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(DecodePara
   const unsigned m = c < p.N ? chunk_values(p.n, c) : 0;
 
   if (tid < 32) {
-    // Two round trips.  Lanes 0..3 fetch the 32-byte header, and lane 0 checks it against the
-    // caller's n: magic, version, base, n, N, and escape_base(n) <= total_bytes <= the largest
-    // stream n values can produce.  Only then do lanes 4..6 fetch the chunk's two escape offsets
-    // and the table's zero pad; they lie below records_base(n) <= escape_base(n) <= total_bytes,
-    // so a wrong n or a short total_bytes never steers a read past the stream.
+    // Lanes 0..3 fetch the 32-byte header, and every lane checks it against the caller's n:
+    // magic, version, form, base, n, N, and total_bytes -- for the coded form between the start
+    // of the escape region and the raw form's length, for the raw form exactly that length.  Only
+    // then, and only for the coded form, do lanes 4..6 fetch the chunk's two escape offsets and
+    // the table's zero pad; they lie below records_base(n) <= escape_base(n) <= total_bytes, so a
+    // wrong n or a short total_bytes never steers a read past the stream.
     const unsigned long long* w = reinterpret_cast<const unsigned long long*>(p.in);
-    const uint64_t R0 = records_base(p.n), E0 = escape_base(p.n);
+    const uint64_t R0 = records_base(p.n), E0 = escape_base(p.n), RAW = raw_stream_bytes(p.n);
     const bool has_pad = kHeaderBytes + 8 * (p.N + 1) < R0;
     const unsigned long long hv = lane < 4 ? w[lane] : 0ull;
     const unsigned long long h0 = __shfl_sync(0xFFFFFFFFu, hv, 0), h1 = __shfl_sync(0xFFFFFFFFu, hv, 1);
     const unsigned long long h2 = __shfl_sync(0xFFFFFFFFu, hv, 2), total = __shfl_sync(0xFFFFFFFFu, hv, 3);
     const int e0 = static_cast<int>(h0 >> 56);
+    const unsigned long long head = h0 & 0x00FFFFFFFFFFFFFFull;  // bytes 0..6
+    const bool raw = head == kRawMagicWord;
     int bad = 0;
-    if ((h0 & 0x00FFFFFFFFFFFFFFull) != kMagicWord || e0 > kE0Max) bad = ZC_ERR_CORRUPT;
+    if ((head != kMagicWord && !raw) || e0 > kE0Max) bad = ZC_ERR_CORRUPT;
     else if (h1 != p.n) bad = ZC_ERR_SIZE_MISMATCH;
-    else if (h2 != p.N || total < E0 || total > max_stream_bytes(p.n)) bad = ZC_ERR_CORRUPT;
+    else if (raw ? (h2 != 0 || total != RAW) : (h2 != p.N || total < E0 || total > RAW)) bad = ZC_ERR_CORRUPT;
     unsigned long long v = 0;
-    if (!bad) {  // the same in every lane
+    if (!bad && !raw) {  // the same in every lane
       if (lane == 4) v = w[4 + c];
       else if (lane == 5 && c < p.N) v = w[5 + c];
       else if (lane == 6 && has_pad && (c == 0 || c + 1 >= p.N)) v = w[5 + p.N];
@@ -124,7 +152,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(DecodePara
     const unsigned long long off0 = __shfl_sync(0xFFFFFFFFu, v, 4), off1 = __shfl_sync(0xFFFFFFFFu, v, 5);
     const unsigned long long pad = __shfl_sync(0xFFFFFFFFu, v, 6);
     if (lane == 0) {
-      if (bad == 0 &&
+      if (bad == 0 && !raw &&
           (pad != 0 || (c == 0 && off0 != E0) || (p.N == 0 && total != E0) ||
            (p.N > 0 && c == p.N - 1 && off1 != total) ||
            (c < p.N && (off0 < E0 || off1 > total || off1 < off0 || ((off0 | off1) & 15) ||
@@ -132,10 +160,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(DecodePara
         bad = ZC_ERR_CORRUPT;
       if (bad) set_error(p.status, bad);
       S.ok = !bad && c < p.N;
+      S.raw = raw;
       S.e0 = e0;
       S.escapes = 0;
       S.esc_bytes = static_cast<unsigned>(off1 - off0);
-      if (S.ok) {
+      if (S.ok && !raw) {
         const unsigned fbytes = static_cast<unsigned>(fixed_bytes(m));
         mbar_init(&S.mbar, 1);
         fence_mbar_init();
@@ -147,6 +176,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) decode_kernel(DecodePara
   }
   __syncthreads();
   if (!S.ok) return;
+  if (S.raw) {  // the values follow the header as they are
+    raw_chunk(p.in, p.out, p.status, c, m);
+    return;
+  }
   // every thread polls; the CTA acts on one shared answer
   if (__syncthreads_or(!mbar_wait(&S.mbar, 0, kWaitLimit))) {
     if (tid == 0) {

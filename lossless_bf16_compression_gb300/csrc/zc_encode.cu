@@ -244,6 +244,8 @@ __device__ __noinline__ void scanner(EncodeSmem& S, unsigned long long* flags, u
 __device__ void retirer(EncodeSmem& S, const EncodeParams& p) {
   const unsigned lane = threadIdx.x & 31;
   const uint64_t E0 = escape_base(p.n);
+  // A section ending past the raw form's length means the stream will be raw: it is not written.
+  const uint64_t room = raw_stream_bytes(p.n) > E0 ? raw_stream_bytes(p.n) - E0 : 0;
   unsigned long long* table = reinterpret_cast<unsigned long long*>(p.out + kHeaderBytes);
   unsigned retired = 0, freed = 0, spins = 0, backoff = 64;
   for (;;) {
@@ -286,6 +288,7 @@ __device__ void retirer(EncodeSmem& S, const EncodeParams& p) {
     backoff = 64;
     for (unsigned t = 0; t < run; ++t) {  // the lists, in order, each by the whole warp
       const unsigned long long ft = __shfl_sync(0xFFFFFFFFu, f, t);
+      if ((ft & kFlagValueMask) > room) break;  // this one and all later ones: the stream is raw
       const unsigned it = (retired + t) % kQueue;
       const unsigned size = S.q_size[it];
       const uint4* src = S.ring + S.q_off[it] / 16;
@@ -391,6 +394,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // The stages start on a 1024-byte boundary of the shared window (the period of the swizzle).
   EncodeSmem& S = *reinterpret_cast<EncodeSmem*>(smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
+  // The step that follows (the raw-form check) may be scheduled now: it waits for this kernel's
+  // completion before it reads anything.
+  asm volatile("griddepcontrol.launch_dependents;");
   const unsigned tid = threadIdx.x, warp = tid >> 5;
   if (tid == 0) {
     // The first CTA to start is the scanner.  Every other CTA waits, bounded, only on work the
@@ -596,18 +602,58 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   }
 }
 
-// n = 0: the stream is the header, offsets[0] = 48 and 8 bytes of padding.
+// n = 0: the raw form (32 bytes, the header alone) is shorter than the coded one (48 bytes).
 __global__ void empty_stream_kernel(uint8_t* out, int base, Control* ctrl, unsigned long long* out_bytes) {
   unsigned long long* w = reinterpret_cast<unsigned long long*>(out);
   const int e0 = base >= 0 ? base : 0;  // no finite value: e0 = 0
-  w[0] = kMagicWord | (static_cast<unsigned long long>(e0) << 56);
+  w[0] = kRawMagicWord | (static_cast<unsigned long long>(e0) << 56);
   w[1] = 0;
   w[2] = 0;
-  w[3] = 48;
-  w[4] = 48;
-  w[5] = 0;
-  ctrl->total = 48;
-  if (out_bytes) *out_bytes = 48;
+  w[3] = kHeaderBytes;
+  ctrl->total = kHeaderBytes;
+  if (out_bytes) *out_bytes = kHeaderBytes;
+}
+
+// After the encode kernel, as a programmatic dependent launch: when the coded stream is longer
+// than the raw form, the stream becomes the raw form -- the header (byte 6 = 0, N = 0), the n
+// values as they are (16-byte copies), zero padding -- and its length is reported again.
+// Otherwise every CTA returns after one load.
+constexpr int kRawThreads = 256;
+constexpr int kRawVecPerThread = 4;
+
+__global__ void __launch_bounds__(kRawThreads) raw_form_kernel(const uint16_t* in, uint64_t n, int base, uint8_t* out,
+                                                               Control* ctrl, unsigned long long* out_bytes) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the encode kernel and its writes are done
+  const unsigned long long raw = raw_stream_bytes(n);
+  if (__ldcg(&ctrl->total) <= raw) return;
+  const uint4* src = reinterpret_cast<const uint4*>(in);
+  uint4* dst = reinterpret_cast<uint4*>(out + kHeaderBytes);
+  const uint64_t nvec = n / 8;  // whole 16-byte vectors of values
+  const uint64_t stride = static_cast<uint64_t>(gridDim.x) * kRawThreads;
+  for (uint64_t i = static_cast<uint64_t>(blockIdx.x) * kRawThreads + threadIdx.x; i < nvec; i += stride * kRawVecPerThread) {
+    uint4 v[kRawVecPerThread];
+#pragma unroll
+    for (int j = 0; j < kRawVecPerThread; ++j)
+      if (i + j * stride < nvec) v[j] = __ldcs(src + i + j * stride);
+#pragma unroll
+    for (int j = 0; j < kRawVecPerThread; ++j)
+      if (i + j * stride < nvec) __stcs(dst + i + j * stride, v[j]);
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    if (n % 8) {  // the last values and the zero padding: one 16-byte vector
+      uint32_t w[4] = {0, 0, 0, 0};
+      for (unsigned i = 0; i < n % 8; ++i) w[i >> 1] |= static_cast<uint32_t>(in[8 * nvec + i]) << (16 * (i & 1));
+      dst[nvec] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    const unsigned long long e0 = base >= 0 ? static_cast<unsigned>(base) : static_cast<unsigned>(__ldcg(&ctrl->e0));
+    unsigned long long* hdr = reinterpret_cast<unsigned long long*>(out);
+    hdr[0] = kRawMagicWord | (e0 << 56);
+    hdr[1] = n;
+    hdr[2] = 0;
+    hdr[3] = raw;
+    ctrl->total = raw;
+    if (out_bytes) *out_bytes = raw;
+  }
 }
 
 // Dynamic shared memory of the encode kernel: the layout plus room to align it to 1024 bytes.
@@ -704,6 +750,30 @@ cudaError_t launch_encode(const uint16_t* in, uint64_t n, int base, uint8_t* out
   cfg.numAttrs = base < 0 ? 1 : 0;
   TimingRecord t = timing_begin(ZC_KERNEL_ENCODE, stream);
   err = cudaLaunchKernelEx(&cfg, encode_kernel, p, map);
+  timing_end(t, stream);
+  return err;
+}
+
+cudaError_t launch_raw_form(const uint16_t* in, uint64_t n, int base, uint8_t* out, unsigned long long* out_bytes,
+                            uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream) {
+  if (n == 0) return cudaSuccess;  // the empty stream is written raw by the encode step
+  const uint64_t nvec = n / 8;
+  uint64_t grid = (nvec + kRawThreads * kRawVecPerThread - 1) / (kRawThreads * kRawVecPerThread);
+  const uint64_t cap = 4ull * dev.sm_count;
+  if (grid > cap) grid = cap;
+  if (grid < 1) grid = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kRawThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // after our own encode kernel
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  TimingRecord t = timing_begin(ZC_KERNEL_RAW, stream);
+  const cudaError_t err = cudaLaunchKernelEx(&cfg, raw_form_kernel, in, n, base, out,
+                                             reinterpret_cast<Control*>(ws), out_bytes);
   timing_end(t, stream);
   return err;
 }

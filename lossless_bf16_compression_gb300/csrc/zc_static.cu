@@ -84,6 +84,7 @@ extern "C" int zc_compress_static_scratch(const void* in, size_t n, int base_or_
   }
   if (launch_encode(x, n, base_or_auto, o, len_ptr, ws, dev, stream, ~uint64_t(0), kDefaultSpinLimit) != cudaSuccess)
     return ZC_ERR_CUDA;
+  if (launch_raw_form(x, n, base_or_auto, o, len_ptr, ws, dev, stream) != cudaSuccess) return ZC_ERR_CUDA;
   if (pageable) {
     unsigned long long total = 0;
     const Control* ctrl = reinterpret_cast<const Control*>(ws);

@@ -33,21 +33,32 @@ def test_every_declared_symbol_is_exported(lib):
     assert sorted(zc.exported_symbols()) == names
 
 
+def _pad16(v):
+    return (v + 15) // 16 * 16
+
+
+def _fixed_region_end(n):
+    """End of the coded form's fixed parts: header, table, then 5632 B per full chunk."""
+    N = (n + 4095) // 4096
+    rem = n % 4096
+    return _pad16(32 + 8 * (N + 1)) + (n // 4096) * 5632 + (_pad16((3 * rem + 7) // 8) + _pad16(rem) if rem else 0)
+
+
 def test_max_stream_bytes_matches_oracle(lib):
-    for n in [0, 1, 7, 8, 4095, 4096, 4097, 10 ** 6, 58_720_256, 117_440_512, 268_435_456, 1 << 29]:
-        assert zc.zc_max_stream_bytes(n) == oracle.max_stream_bytes(n)
+    """Room for the stream: the longest stream (the raw form, the oracle's bound) or the coded
+    fixed parts, whichever ends later."""
+    for n in [0, 1, 7, 8, 50, 100, 4095, 4096, 4097, 10 ** 6, 58_720_256, 117_440_512, 268_435_456, 1 << 29]:
+        assert oracle.max_stream_bytes(n) == oracle.raw_stream_bytes(n) == 32 + _pad16(2 * n)
+        assert zc.zc_max_stream_bytes(n) == max(oracle.max_stream_bytes(n), _fixed_region_end(n))
         N = (n + 4095) // 4096
         assert zc.zc_max_compressed_bytes(n) >= zc.zc_max_stream_bytes(n) + 8 * N
+    assert zc.zc_max_stream_bytes(1) == 80 > oracle.max_stream_bytes(1) == 48  # tiny n: the fixed parts
+    assert zc.zc_max_stream_bytes(1000) == oracle.max_stream_bytes(1000)
 
 
 def test_max_stream_bytes_closed_form_large(lib):
     n = (1 << 40) - 3
-    N = (n + 4095) // 4096
-    rem = n % 4096
-    pad16 = lambda v: (v + 15) // 16 * 16  # noqa: E731
-    # header + table, then per chunk the fixed part and an exponent plane (the largest escape section)
-    want = pad16(32 + 8 * (N + 1)) + (n // 4096) * (5632 + 4096) + pad16((3 * rem + 7) // 8) + pad16(rem) + pad16(rem)
-    assert zc.zc_max_stream_bytes(n) == want
+    assert zc.zc_max_stream_bytes(n) == 32 + _pad16(2 * n)
 
 
 def test_sizes_beyond_limit(lib):

@@ -126,12 +126,23 @@ def test_random_bit_flips_match_oracle_verdict(sample):
     assert accepted > 50 and rejected > 50
 
 
+PLANE_CHUNKS = (6, 7)  # chunks of random bit patterns among escape-free ones
+
+
 @pytest.fixture(scope="module")
 def dense_sample():
-    """Random bit patterns: nearly every value escapes, so every chunk keeps its escapes as an
-    exponent plane (one byte per value) rather than a list of (position, exponent) pairs."""
-    x = workloads.random_patterns(2 * 4096 + 50, 91)
-    return x, oracle.compress(x)
+    """Six escape-free chunks (exponents 127..133, in the window of e0 = 127), two chunks and 50
+    values of random bit patterns: nearly every value of the last three escapes, so they keep
+    their escapes as exponent planes (one byte per value) rather than lists, and the clean
+    chunks keep the stream in the coded form."""
+    rng = np.random.default_rng(91)
+    clean = 6 * 4096
+    e = rng.integers(127, 134, clean)
+    head = ((rng.integers(0, 2, clean) << 15) | (e << 7) | rng.integers(0, 128, clean)).astype(np.uint16)
+    x = np.concatenate([head, workloads.random_patterns(2 * 4096 + 50, 91)])
+    s = oracle.compress(x, 127)
+    assert s[6] == 12
+    return x, s
 
 
 def test_plane_corruptions_are_reported(dense_sample):
@@ -139,16 +150,18 @@ def test_plane_corruptions_are_reported(dense_sample):
     n = x.size
     N = (n + 4095) // 4096
     cap = zc.zc_max_compressed_bytes(n)
-    off0, off1 = escape_offset(s, 0), escape_offset(s, 1)
-    assert off1 - off0 == 4096, "chunk 0 keeps a plane"
+    c0 = PLANE_CHUNKS[0]
+    off0, off1 = escape_offset(s, c0), escape_offset(s, c0 + 1)
+    assert off1 - off0 == 4096, "the first random chunk keeps a plane"
     e0 = int(s[7])
-    E = (x[:4096].astype(np.int64) >> 7) & 0xFF
+    E = (x[4096 * c0:4096 * (c0 + 1)].astype(np.int64) >> 7) & 0xFF
     inside = np.flatnonzero((E >= e0) & (E <= e0 + 6))
     outside = np.flatnonzero((E < e0) | (E > e0 + 6))
     assert inside.size > 0 and outside.size > 0
     st, vals = gpu_decompress_bytes(s, n, cap)
     assert st == zc.ZC_OK and np.array_equal(vals, x)
     R0 = (32 + 8 * (N + 1) + 15) // 16 * 16
+    codes0 = R0 + 5632 * c0
     i_in, i_out = int(inside[0]), int(outside[-1])
     last_off = escape_offset(s, N - 1)  # the last chunk's 50 values: a plane of pad16(50) = 64 bytes
     muts = {
@@ -171,9 +184,9 @@ def test_plane_corruptions_are_reported(dense_sample):
     st, gvals = gpu_decompress_bytes(t, n, cap)
     assert ost == oracle.OK and st == zc.ZC_OK and np.array_equal(gvals, ovals)
     rng = np.random.default_rng(8)
-    for _ in range(60):  # flips in chunk 0's codes and plane: the GPU's verdict is the oracle's
+    for _ in range(60):  # flips in the plane chunk's codes and plane: the GPU's verdict is the oracle's
         t = s.copy()
-        pos = int(rng.choice([rng.integers(R0, R0 + 1536), rng.integers(off0, off1)]))
+        pos = int(rng.choice([rng.integers(codes0, codes0 + 1536), rng.integers(off0, off1)]))
         t[pos] ^= np.uint8(1 << int(rng.integers(0, 8)))
         ost, ovals = oracle_status(t, n, cap)
         st, gvals = gpu_decompress_bytes(t, n, cap)
@@ -181,6 +194,44 @@ def test_plane_corruptions_are_reported(dense_sample):
             assert st == zc.ZC_OK and np.array_equal(gvals, ovals), f"flip at {pos}"
         else:
             assert st != zc.ZC_OK, f"flip at {pos}: GPU accepts an invalid stream"
+
+
+@pytest.fixture(scope="module")
+def raw_sample():
+    """Random bit patterns: the coded form would be longer, so the stream is in the raw form."""
+    x = workloads.random_patterns(3 * 4096 + 77, 92)
+    s = oracle.compress(x)
+    assert s[6] == 0 and s.size == 32 + (2 * x.size + 15) // 16 * 16
+    return x, s
+
+
+def test_raw_corruptions_are_reported(raw_sample):
+    x, s = raw_sample
+    n = x.size
+    cap = zc.zc_max_compressed_bytes(n)
+    st, vals = gpu_decompress_bytes(s, n, cap)
+    assert st == zc.ZC_OK and np.array_equal(vals, x)
+    muts = {"form_12": (6, 12), "form_1": (6, 1), "version": (4, 3), "base_250": (7, 250), "N_1": (16, 1),
+            "total": (24, s[24] ^ 0x10), "padding": (32 + 2 * n + 1, 0x01), "magic": (1, 0)}
+    for name, (pos, val) in muts.items():
+        t = s.copy()
+        t[pos] = np.uint8(val)
+        ost, _ = oracle_status(t, n, cap)
+        assert ost == oracle.ERR_CORRUPT, f"{name}: the oracle accepts it"
+        st, _ = gpu_decompress_bytes(t, n, cap)
+        assert st == zc.ZC_ERR_CORRUPT, f"{name}: status {zc.ERROR_NAMES.get(st, st)}"
+    st, _ = gpu_decompress_bytes(s, n + 1, zc.zc_max_compressed_bytes(n + 1))
+    assert st == zc.ZC_ERR_SIZE_MISMATCH
+    rng = np.random.default_rng(9)
+    for _ in range(100):  # flips anywhere in a raw stream: the GPU's verdict and values are the oracle's
+        t = s.copy()
+        pos = int(rng.integers(0, s.size))
+        t[pos] ^= np.uint8(1 << int(rng.integers(0, 8)))
+        ost, ovals = oracle_status(t, n, cap)
+        st, gvals = gpu_decompress_bytes(t, n, cap)
+        assert (st == zc.ZC_OK) == (ost == oracle.OK), f"flip at {pos}"
+        if st == zc.ZC_OK:
+            assert np.array_equal(gvals, ovals), f"flip at {pos}"
 
 
 def test_valid_stream_and_wrong_n(sample):

@@ -88,19 +88,42 @@ def test_full_chunks_at_the_list_plane_boundary(k):
     """Full chunks with k escapes.  Up to 1365 escapes (3k <= 4096) they keep a list.  From
     1361 on, that list pads to 4096 bytes, the size of a plane, so the decoder builds from it
     as a plane first and must rebuild the values from the codes.  From 1366 on they keep a
-    plane."""
+    plane.  Seven escape-free chunks after them keep the stream in the coded form."""
     rng = np.random.default_rng(k)
     chunks = []
-    for _ in range(3):
+    for j in range(10):
         x = np.full(4096, 0x3F80, np.uint16)  # 1.0: exponent 127, in the window for e0 = 127
         x |= rng.integers(0, 128, 4096).astype(np.uint16)  # random mantissas
-        pos = rng.choice(4096, k, replace=False)
-        x[pos] = rng.integers(0, 0x0100, k).astype(np.uint16)  # exponents 0 and 1: escapes
+        if j < 3:
+            pos = rng.choice(4096, k, replace=False)
+            x[pos] = rng.integers(0, 0x0100, k).astype(np.uint16)  # exponents 0 and 1: escapes
         chunks.append(x)
     x = np.concatenate(chunks)
     s = check_parity(x, 127)
     section = (4096 if 3 * k > 4096 else (3 * k + 15) // 16 * 16)
-    assert s.size == oracle.records_base(x.size) + 3 * (5632 + section)
+    assert s[6] == 12 and s.size == oracle.records_base(x.size) + 3 * (5632 + section) + 7 * 5632
+
+
+@pytest.mark.parametrize("n", [0, 1, 5, 37, 38, 4095, 4097, 3 * 4096 + 3, 100_000])
+def test_raw_form(n):
+    """Tensors whose coded form would be longer come out in the raw form: the header, then the
+    values as they are.  Random bit patterns escape almost everywhere; tiny tensors pay more
+    for the coded header and table than they save."""
+    x = workloads.random_patterns(n, 500 + n)
+    s = check_parity(x)
+    assert s[6] == 0 and s.size == 32 + (2 * n + 15) // 16 * 16
+    assert s[32:32 + 2 * n].tobytes() == x.tobytes()
+
+
+def test_raw_and_coded_at_the_tie():
+    """37 values of 1.0 under e0 = 127 cost 112 bytes either way: the coded form is kept; one
+    escape more tips the stream into the raw form."""
+    x = np.full(37, 0x3F80, np.uint16)
+    s = check_parity(x, 127)
+    assert s.size == 112 and s[6] == 12
+    x[5] = 0
+    s = check_parity(x, 127)
+    assert s.size == 112 and s[6] == 0
 
 
 def test_special_tensors():

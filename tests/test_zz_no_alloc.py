@@ -82,9 +82,9 @@ def test_static_scratch_supplied_base_and_host_length():
 
 @pytest.mark.parametrize("n", [2 * 4096 + 50, 3 * 4096])
 def test_static_scratch_stays_inside_its_stream_bound(n):
-    """All-escape random patterns reach the largest stream n values can give (every chunk keeps a
-    plane of exponents); 4 KiB of 0xA5 right before `out` and right after zc_max_stream_bytes(n)
-    bytes of it must survive."""
+    """Random bit patterns give the longest stream n values can give (the raw form, after the
+    coded form was written and found longer); 4 KiB of 0xA5 right before `out` and right after
+    zc_max_stream_bytes(n) bytes of it must survive."""
     G = 4096
     x = workloads.random_patterns(n, 600 + n)
     want = oracle.compress(x)
@@ -97,7 +97,7 @@ def test_static_scratch_stays_inside_its_stream_bound(n):
     h = buf.cpu().numpy()
     assert np.all(h[:G] == 0xA5) and np.all(h[G + cap:] == 0xA5), "a guard band was written"
     total = int(ob.item())
-    assert total == want.size
+    assert total == want.size == cap
     assert h[G:G + total].tobytes() == want.tobytes()
 
 
