@@ -245,11 +245,12 @@ __device__ __forceinline__ uint32_t pick4(const uint32_t (&a)[4], unsigned i) {
   return i < 2 ? (i == 0 ? a[0] : a[1]) : (i == 2 ? a[2] : a[3]);
 }
 
-// Codes of two BF16 values (halves of w): e - e0 when 0 <= e - e0 <= 6, else 7.
-// neg_e0x2 holds (65536 - e0) in both halves, so the add wraps out-of-window values high.
-__device__ __forceinline__ uint32_t codes_x2(uint32_t w, uint32_t neg_e0x2) {
-  const uint32_t e2 = (w >> 7) & 0x00FF00FFu;
-  return min_u16x2(add_u16x2(e2, neg_e0x2), 0x00070007u);
+// Codes of two BF16 values (halves of w), each shifted left by 7: e - e0 when 0 <= e - e0 <= 6,
+// else 7.  kadd holds (256 - e0) << 7 in both halves: the masked exponent field plus it stays
+// below 2^16, and bits 7..14 of the sum are (e - e0) mod 256, which is at least 7 whenever
+// e < e0 because e0 <= 249.  Three logic/add operations and one packed 16-bit minimum.
+__device__ __forceinline__ uint32_t codes7_x2(uint32_t w, uint32_t kadd) {
+  return min_u16x2(((w & 0x7F807F80u) + kadd) & 0x7F807F80u, 0x03800380u);
 }
 
 // Sign|mantissa bytes of the four values in (w0, w1): (x >> 8 & 0x80) | (x & 0x7F).
@@ -259,12 +260,14 @@ __device__ __forceinline__ uint32_t sign_mantissa_x4(uint32_t w0, uint32_t w1) {
   return (hi & 0x80808080u) | (lo & 0x7F7F7F7Fu);
 }
 
-// 24-bit little-endian bitstream of 8 codes: code j at bits [3j, 3j+3).
-__device__ __forceinline__ uint32_t pack_codes8(const uint32_t (&c2)[4]) {
-  uint32_t v = 0;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) v |= ((c2[i] | (c2[i] >> 13)) & 0x3Fu) << (6 * i);
-  return v;
+// 24-bit little-endian bitstream of the 8 codes in four words of codes7_x2: code j at bits
+// [3j, 3j+3).  In t = w0 + (w1 << 6) the codes of values 0, 2 sit at bits 7, 13 and those of
+// values 1, 3 at bits 23, 29, so two shifts and a masked merge put all four in place.
+__device__ __forceinline__ uint32_t pack_codes8(const uint32_t (&c7)[4]) {
+  const uint32_t t01 = c7[0] + (c7[1] << 6), t23 = c7[2] + (c7[3] << 6);
+  const uint32_t g01 = ((t01 >> 7) & 0x1C7u) | (t01 >> 20);
+  const uint32_t g23 = ((t23 >> 7) & 0x1C7u) | (t23 >> 20);
+  return g01 + (g23 << 12);
 }
 
 constexpr int kChunkThreads = 128;  // threads of a decode CTA, one chunk each

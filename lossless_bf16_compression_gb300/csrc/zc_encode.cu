@@ -36,6 +36,7 @@
 #include <mutex>
 
 #include "zc_common.cuh"
+#include "zc_ring.h"
 
 namespace zc {
 namespace {
@@ -52,6 +53,7 @@ constexpr unsigned kInBytes = 2 * kChunk;
 // escape-heavy tensors, where the ring fills, 2% more than 16 KB.
 constexpr unsigned kRingBytes = 18 * 1024;
 static_assert(kRingBytes >= 2 * kMaxEscapeBytes, "a section placed after a skipped gap always fits a drained ring");
+static_assert(kRingBytes % 16 == 0, "sections and their places are 16-byte aligned");
 constexpr unsigned kQueue = 64;            // escape sections waiting, at most
 constexpr unsigned kDenseMin = 16;         // escapes per lane from which a warp takes the dense loop
 constexpr unsigned kWaitLimit = 1u << 22;  // mbarrier polls before giving up
@@ -340,19 +342,11 @@ struct Ring {
   unsigned head = 0;    // ring offset where the next list may start
 };
 
-__device__ __forceinline__ void ring_place(Ring& R, unsigned need, unsigned* where, unsigned* gap) {
-  // head is the ring offset of `made`; a list that ended exactly at the end leaves it at
-  // kRingBytes, which is offset 0.  With head below kRingBytes, where + need <= kRingBytes.
-  if (R.head >= kRingBytes) R.head = 0;
-  *gap = (need && R.head + need > kRingBytes) ? kRingBytes - R.head : 0u;
-  *where = *gap ? 0u : R.head;
-}
-
-// Wait (bounded) until the retiring warp has freed room for `bytes` more ring bytes and a queue
-// slot.  False after an error or a timeout.
-__device__ bool ring_room(const EncodeSmem& S, const Ring& R, unsigned bytes, const EncodeParams& p) {
+// Wait (bounded) until the retiring warp has freed room for a section of `need` bytes after a
+// `gap` (ring_fits) and a queue slot.  False after an error or a timeout.
+__device__ bool ring_room(const EncodeSmem& S, const Ring& R, unsigned gap, unsigned need, const EncodeParams& p) {
   unsigned spins = 0, backoff = 64;
-  while (R.pushed - S.q_retired >= kQueue || R.made + bytes - S.freed > kRingBytes) {
+  while (R.pushed - S.q_retired >= kQueue || !ring_fits(R.made - S.freed, gap, need, kRingBytes)) {
     if (read_status(p.status) != 0) return false;
     if (++spins > p.spin_limit) {
       set_error(p.status, ZC_ERR_TIMEOUT);
@@ -442,7 +436,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   }
   bar_coders();
   const int e0 = S.e0;
-  const uint32_t neg_e0x2 = ((0x10000u - static_cast<unsigned>(e0)) & 0xFFFFu) * 0x00010001u;
+  const uint32_t kadd = ((256u - static_cast<unsigned>(e0)) << 7) * 0x00010001u;
   const uint64_t R0 = records_base(p.n);
   // This thread's 64 bytes in a stage: logical 16-byte unit q (values v0 + 8q ..) of row tid / 2
   // sits at byte offset sw ^ 16q.
@@ -485,29 +479,29 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         S.xin[s][(sw ^ (16 * q)) / 16] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
       }
     }
-    uint32_t g[4];     // 24-bit code groups
-    uint32_t sm[8];    // sign|mantissa bytes, four per word
-    unsigned m32 = 0;  // escape flags: bit b for value v0 + b
+    uint32_t g[4];   // 24-bit code groups
+    uint32_t sm[8];  // sign|mantissa bytes, four per word
+    uint32_t e[4];   // code-7 flags: bit 3j of e[q] for value v0 + 8q + j
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const uint4 xv = S.xin[s][(sw ^ (16 * q)) / 16];
       uint32_t w[4] = {xv.x, xv.y, xv.z, xv.w};
-      uint32_t c2[4];
+      uint32_t c7[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) c2[i] = codes_x2(w[i], neg_e0x2);
+      for (int i = 0; i < 4; ++i) c7[i] = codes7_x2(w[i], kadd);
       if (!full) {  // values past m: code 0, byte 0, no escape
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const unsigned v = v0 + 8 * q + 2 * i;
           const uint32_t keep = (v < m ? 0x0000FFFFu : 0u) | (v + 1 < m ? 0xFFFF0000u : 0u);
-          c2[i] &= keep;
+          c7[i] &= keep;
           w[i] &= keep;
         }
       }
       sm[2 * q] = sign_mantissa_x4(w[0], w[1]);
       sm[2 * q + 1] = sign_mantissa_x4(w[2], w[3]);
-      g[q] = pack_codes8(c2);
-      m32 |= compact8(g[q] & (g[q] >> 1) & (g[q] >> 2) & 0x249249u) << (8 * q);  // code 7
+      g[q] = pack_codes8(c7);
+      e[q] = g[q] & (g[q] >> 1) & (g[q] >> 2) & 0x249249u;  // code 7
     }
     uint8_t* const smp = fixed + cbytes + v0;
     if (full || v0 < smbytes) *reinterpret_cast<uint4*>(smp) = make_uint4(sm[0], sm[1], sm[2], sm[3]);
@@ -517,7 +511,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 #pragma unroll
     for (int i = 0; i < 3; ++i)
       if (full || 12 * tid + 4 * i < cbytes) cp[i] = cw[i];
-    const unsigned cnt = __popc(m32);
+    const unsigned cnt = __popc(e[0]) + __popc(e[1]) + __popc(e[2]) + __popc(e[3]);
 
     unsigned base;
     const unsigned k = chunk_rank(cnt, &base, S.scan);  // [R]
@@ -528,10 +522,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     // ring state and waits (bounded) for the room itself, so no barrier is needed before the
     // list is written.  A thread that gives up stops the CTA at [C].
     unsigned where, gap;
-    ring_place(R, esc_bytes, &where, &gap);
+    ring_place(R.head, esc_bytes, kRingBytes, &where, &gap);
     if (tid == 0 && c != p.stall_chunk) st_relaxed_u64(&p.flags[c], kFlagAggregate | esc_bytes);  // publish early
     bool stop = failed || c == p.stall_chunk;  // (the stall test hook: this list is never resolved)
-    if (!stop && !ring_room(S, R, gap + esc_bytes, p)) stop = true;
+    if (!stop && !ring_room(S, R, gap, esc_bytes, p)) stop = true;
     R.made += gap + esc_bytes;
     R.head = where + esc_bytes;
     if (__any_sync(0xFFFFFFFFu, stop)) {
@@ -543,6 +537,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       // Shared memory is addressed with 32-bit shared-window addresses.
       const uint32_t esc = smem_u32(S.ring) + where;
       const uint32_t xs = smem_u32(S.xin[s]);  // value v0 + b at byte xs + (sw ^ (2b & 0x3E))
+      unsigned m32 = 0;  // the flags compacted: value v0 + b at bit b
+#pragma unroll
+      for (int q = 0; q < 4; ++q) m32 |= compact8(e[q]) << (8 * q);
       if (__reduce_max_sync(0xFFFFFFFFu, cnt) < kDenseMin) {
         // Highest value first: ranks base + cnt - 1 down to base.
         uint32_t at16 = esc + 2 * (base + cnt), at8 = esc + 2 * k + base + cnt;  // one past the last
