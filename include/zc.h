@@ -134,6 +134,33 @@ int zc_compress(const void* in, size_t n, int base_or_auto, void* out, size_t* o
  * recomputed.  Device-side errors are read with zc_status. */
 int zc_decompress(const void* in, void* out, size_t n, cudaStream_t stream);
 
+/* ------------------------------------------------------------------ loopback pipeline */
+
+/* Bytes the caller must provide at `out` for zc_loopback of n values: the longest coded form
+ * (every chunk with a plane of exponents, 9,728 B per full chunk), since the loopback writes every
+ * escape section before the stream's form is chosen, rounded up to 256, then the workspace.
+ * Pure host function.  Returns 0 when n > ZC_MAX_N. */
+size_t zc_loopback_bytes(size_t n);
+
+/* Compress n values into a stream and decompress that stream into `values`, in one launch, as a
+ * sender and a receiver on one GPU would: a chunk is decoded as soon as its own bytes are in the
+ * stream -- its fixed part (whose place follows from n) and its escape section (once the
+ * device-wide scan has placed it and it has been written) -- while later chunks are still being
+ * coded.  This is the compress -> exchange sizes -> send -> decompress workflow of the same page
+ * (Figure 5(b), Design-1) and UCCL-Zip's split-send pipeline (data transmissible as early as
+ * possible, compression overlapped with the transfer), with the transfer taken out: the decoder
+ * reads the stream where the encoder wrote it.
+ *   in, n, base_or_auto, out_bytes, stream   as for zc_compress.
+ *   out     device, zc_loopback_bytes(n) bytes, 16-byte aligned, not overlapping `in` or
+ *           `values`; afterwards it holds the same stream zc_compress writes (the raw form when
+ *           that is shorter, which is decided after the decoding, from the coded form).
+ *   values  device, n x u16, 16-byte aligned: receives the decoded values, equal to `in`.
+ * Returns ZC_OK or a host-side error code; device-side errors (a stream section that fails the
+ * decoder's checks: ZC_ERR_CORRUPT; a bounded wait that ran out: ZC_ERR_TIMEOUT) are read with
+ * zc_status.  The pages have no counterpart of this entry point as an interface. */
+int zc_loopback(const void* in, size_t n, int base_or_auto, void* out, size_t* out_bytes, void* values,
+                cudaStream_t stream);
+
 /* ------------------------------------------------------------------ status */
 
 /* Synchronize `stream`, then return the first device-side error recorded on the current
@@ -191,6 +218,13 @@ int zc_compress_static_scratch(const void* in, size_t n, int base_or_auto, void*
 int zc_compress_stall_test(const void* in, size_t n, int base_or_auto, void* out,
                            size_t* out_bytes, cudaStream_t stream, size_t stalled_chunk,
                            unsigned spin_limit);
+
+/* zc_loopback with the same planted stall as zc_compress_stall_test: chunk `stalled_chunk` never
+ * publishes its escape-section size, so neither the scan nor the chunks' decoding can pass it;
+ * the waits run out after about `spin_limit` polls and zc_status reports ZC_ERR_TIMEOUT.  No
+ * counterpart on the pages. */
+int zc_loopback_stall_test(const void* in, size_t n, int base_or_auto, void* out, size_t* out_bytes, void* values,
+                           cudaStream_t stream, size_t stalled_chunk, unsigned spin_limit);
 
 #ifdef __cplusplus
 }

@@ -52,6 +52,12 @@ _SIG = {
     "zc_compress_stall_test": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int,
                                               ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                                               ctypes.c_size_t, ctypes.c_uint]),
+    "zc_loopback_bytes": (ctypes.c_size_t, [ctypes.c_size_t]),
+    "zc_loopback": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p,
+                                   ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
+    "zc_loopback_stall_test": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_void_p,
+                                              ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                              ctypes.c_size_t, ctypes.c_uint]),
 }
 
 _lock = threading.Lock()
@@ -133,6 +139,21 @@ def zc_compress_stall_test(in_ptr: int, n: int, base_or_auto: int, out_ptr: int,
                                             stalled_chunk, spin_limit))
 
 
+def zc_loopback_bytes(n: int) -> int:
+    return int(lib().zc_loopback_bytes(n))
+
+
+def zc_loopback(in_ptr: int, n: int, base_or_auto: int, out_ptr: int, out_bytes_ptr: int, values_ptr: int,
+                stream: int) -> int:
+    return int(lib().zc_loopback(in_ptr, n, base_or_auto, out_ptr, out_bytes_ptr, values_ptr, stream))
+
+
+def zc_loopback_stall_test(in_ptr: int, n: int, base_or_auto: int, out_ptr: int, out_bytes_ptr: int,
+                           values_ptr: int, stream: int, stalled_chunk: int, spin_limit: int) -> int:
+    return int(lib().zc_loopback_stall_test(in_ptr, n, base_or_auto, out_ptr, out_bytes_ptr, values_ptr, stream,
+                                            stalled_chunk, spin_limit))
+
+
 # ------------------------------------------------------------------ torch conveniences
 
 
@@ -178,6 +199,26 @@ def decompress(stream_bytes, n: int, stream=None, out=None):
         out = torch.empty(n, dtype=torch.int16, device=stream_bytes.device)
     _check(zc_decompress(stream_bytes.data_ptr(), out.data_ptr(), n, _stream_handle(stream)), "zc_decompress")
     return out
+
+
+def loopback(x, base: int = ZC_BASE_AUTO, stream=None):
+    """Compress a CUDA tensor of BF16 values and decode the stream in the same launch.
+
+    Returns (out, out_bytes, values): the stream at the start of ``out`` (uint8, capacity
+    zc_loopback_bytes(n)), its length (1-element int64 CUDA tensor) and the decoded values
+    (int16 CUDA tensor)."""
+    import torch
+
+    if not x.is_cuda or x.element_size() != 2:
+        raise TypeError("loopback expects a CUDA tensor of 16-bit values")
+    x = x.contiguous()
+    n = x.numel()
+    out = torch.empty(zc_loopback_bytes(n), dtype=torch.uint8, device=x.device)
+    out_bytes = torch.zeros(1, dtype=torch.int64, device=x.device)
+    values = torch.empty(max(n, 1), dtype=torch.int16, device=x.device)[:n]
+    _check(zc_loopback(x.data_ptr(), n, base, out.data_ptr(), out_bytes.data_ptr(), values.data_ptr(),
+                       _stream_handle(stream)), "zc_loopback")
+    return out, out_bytes, values
 
 
 def status(stream=None, reset: bool = False) -> int:

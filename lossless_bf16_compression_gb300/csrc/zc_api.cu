@@ -106,13 +106,22 @@ using namespace zc;
 
 namespace {
 
+// The workspace's place in `out`: after the longest stream the call may write (the loopback
+// writes every escape section of the coded form before the form is chosen).
+uint64_t workspace_at(uint64_t n, bool loopback) {
+  return loopback ? (max_coded_bytes(n) + 255) & ~uint64_t(255) : workspace_offset(n);
+}
+
 int compress_impl(const void* in, size_t n, int base, void* out, size_t* out_bytes, cudaStream_t stream,
-                  uint64_t stall_chunk, unsigned spin_limit) {
+                  uint64_t stall_chunk, unsigned spin_limit, void* values = nullptr) {
   if (n > ZC_MAX_N || base < ZC_BASE_AUTO || base > kE0Max) return ZC_ERR_INVALID_ARG;
   if (out == nullptr || out_bytes == nullptr || (n > 0 && in == nullptr)) return ZC_ERR_INVALID_ARG;
   if (!aligned(in, 16) || !aligned(out, 16) || !aligned(out_bytes, 8)) return ZC_ERR_MISALIGNED;
-  const size_t cap = zc_max_compressed_bytes(n);
+  const bool loopback = values != nullptr;
+  if (loopback && !aligned(values, 16)) return ZC_ERR_MISALIGNED;
+  const size_t cap = loopback ? zc_loopback_bytes(n) : zc_max_compressed_bytes(n);
   if (overlap(in, 2 * n, out, cap)) return ZC_ERR_INVALID_ARG;
+  if (loopback && (overlap(values, 2 * n, out, cap) || overlap(values, 2 * n, in, 2 * n))) return ZC_ERR_INVALID_ARG;
 
   DeviceInfo dev;
   if (device_info(&dev) != cudaSuccess) return ZC_ERR_CUDA;
@@ -128,13 +137,14 @@ int compress_impl(const void* in, size_t n, int base, void* out, size_t* out_byt
   if (!pageable) len_ptr = static_cast<unsigned long long*>(attr.devicePointer);
 
   uint8_t* o = static_cast<uint8_t*>(out);
-  uint8_t* ws = o + workspace_offset(n);
+  uint8_t* ws = o + workspace_at(n, loopback);
   if (cudaMemsetAsync(ws, 0, workspace_bytes(n), stream) != cudaSuccess) return ZC_ERR_CUDA;
   const uint16_t* x = static_cast<const uint16_t*>(in);
   if (n > 0 && base == ZC_BASE_AUTO) {
     if (launch_stats(x, n, ws, dev, stream) != cudaSuccess) return ZC_ERR_CUDA;
   }
-  if (launch_encode(x, n, base, o, len_ptr, ws, dev, stream, stall_chunk, spin_limit) != cudaSuccess)
+  if (launch_encode(x, n, base, o, len_ptr, ws, dev, stream, stall_chunk, spin_limit,
+                    static_cast<uint16_t*>(values)) != cudaSuccess)
     return ZC_ERR_CUDA;
   if (launch_raw_form(x, n, base, o, len_ptr, ws, dev, stream) != cudaSuccess) return ZC_ERR_CUDA;
   if (pageable) {
@@ -169,6 +179,24 @@ int zc_compress(const void* in, size_t n, int base_or_auto, void* out, size_t* o
 int zc_compress_stall_test(const void* in, size_t n, int base_or_auto, void* out, size_t* out_bytes,
                            cudaStream_t stream, size_t stalled_chunk, unsigned spin_limit) {
   return compress_impl(in, n, base_or_auto, out, out_bytes, stream, stalled_chunk, spin_limit);
+}
+
+size_t zc_loopback_bytes(size_t n) {
+  if (n > ZC_MAX_N) return 0;
+  return static_cast<size_t>(workspace_at(n, true) + workspace_bytes(n));
+}
+
+int zc_loopback(const void* in, size_t n, int base_or_auto, void* out, size_t* out_bytes, void* values,
+                cudaStream_t stream) {
+  if (values == nullptr && n > 0) return ZC_ERR_INVALID_ARG;
+  return compress_impl(in, n, base_or_auto, out, out_bytes, stream, ~uint64_t(0), kDefaultSpinLimit,
+                       n > 0 ? values : nullptr);
+}
+
+int zc_loopback_stall_test(const void* in, size_t n, int base_or_auto, void* out, size_t* out_bytes, void* values,
+                           cudaStream_t stream, size_t stalled_chunk, unsigned spin_limit) {
+  if (values == nullptr || n == 0) return ZC_ERR_INVALID_ARG;
+  return compress_impl(in, n, base_or_auto, out, out_bytes, stream, stalled_chunk, spin_limit, values);
 }
 
 int zc_decompress(const void* in, void* out, size_t n, cudaStream_t stream) {

@@ -71,6 +71,11 @@ __host__ __device__ inline uint64_t max_stream_bytes(uint64_t n) {
   const uint64_t e = escape_base(n), r = raw_stream_bytes(n);
   return e > r ? e : r;
 }
+// The longest coded form (every chunk keeps a plane of exponents): the room the loopback needs,
+// since it writes every escape section before the form is chosen.
+__host__ __device__ inline uint64_t max_coded_bytes(uint64_t n) {
+  return escape_base(n) + (n / kChunk) * kMaxEscapeBytes + pad16(n % kChunk);
+}
 
 // ------------------------------------------------------------------ workspace (tail of `out`)
 //
@@ -88,6 +93,7 @@ struct Control {
   unsigned exact_path;      // 1 when the statistics pass needed its exact fallback
   unsigned long long total; // stream length, for the pageable out_bytes path
   unsigned role_ticket;     // encoder CTAs in start order: the first one to start scans
+  unsigned decode_ticket;   // loopback: next chunk to decode
 };
 
 struct StatsPartial {
@@ -105,6 +111,7 @@ __host__ __device__ constexpr uint64_t workspace_bytes(uint64_t n) {
 // Scan state word of a chunk: bits 62..63 status, bits 0..61 value.
 constexpr unsigned long long kFlagAggregate = 1ull << 62;   // value = this chunk's record size
 constexpr unsigned long long kFlagInclusive = 2ull << 62;   // value = sizes up to and including it
+constexpr unsigned long long kFlagCopied = 3ull << 62;      // inclusive, and the section is written (loopback)
 constexpr unsigned long long kFlagValueMask = (1ull << 62) - 1;
 
 // ------------------------------------------------------------------ errors
@@ -300,7 +307,7 @@ void timing_end(TimingRecord& rec, cudaStream_t stream);
 cudaError_t launch_stats(const uint16_t* in, uint64_t n, uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream);
 cudaError_t launch_encode(const uint16_t* in, uint64_t n, int base, uint8_t* out, unsigned long long* out_bytes,
                           uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream, uint64_t stall_chunk,
-                          unsigned spin_limit);
+                          unsigned spin_limit, uint16_t* loopback_values = nullptr);
 cudaError_t launch_decode(const uint8_t* in, uint16_t* out, uint64_t n, const DeviceInfo& dev,
                           cudaStream_t stream);
 // After the encode kernel: when the coded stream came out longer than the raw form, rewrite the

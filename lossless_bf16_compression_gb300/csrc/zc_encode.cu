@@ -36,6 +36,7 @@
 #include <mutex>
 
 #include "zc_common.cuh"
+#include "zc_decode_core.cuh"
 #include "zc_ring.h"
 
 namespace zc {
@@ -58,6 +59,15 @@ constexpr unsigned kQueue = 64;            // escape sections waiting, at most
 constexpr unsigned kDenseMin = 16;         // escapes per lane from which a warp takes the dense loop
 constexpr unsigned kWaitLimit = 1u << 22;  // mbarrier polls before giving up
 constexpr int kScanPerLane = 8;            // state words per scanner lane per round trip
+#ifndef ZC_LOOPBACK_CYCLE
+#define ZC_LOOPBACK_CYCLE 5
+#endif
+#ifndef ZC_LOOPBACK_DECODERS
+#define ZC_LOOPBACK_DECODERS 2
+#endif
+constexpr unsigned kLoopbackCycle = ZC_LOOPBACK_CYCLE;      // loopback: of every kLoopbackCycle CTAs (by
+constexpr unsigned kLoopbackDecoders = ZC_LOOPBACK_DECODERS;  // start order), this many only decode
+static_assert(kLoopbackDecoders < kLoopbackCycle - 1, "the first CTA after the scanner codes");
 constexpr int kCoderWarps = kCoders / 32;
 constexpr unsigned kScanPerWarp = 32 * kScanPerLane;
 
@@ -74,6 +84,7 @@ struct EncodeParams {
   uint64_t stall_chunk;
   unsigned spin_limit;
   uint64_t full_chunks;  // n / 4096: chunks that come by one tiled copy each
+  uint16_t* values;      // loopback: the decoded values (n x u16); null for compression alone
 };
 
 struct __align__(128) EncodeSmem {
@@ -95,7 +106,15 @@ struct __align__(128) EncodeSmem {
   unsigned scan_ready[2][kCoderWarps];
   int scan_bad[2];
   int e0;
-  unsigned role;  // 0: this CTA scans; otherwise it codes
+  unsigned role;  // 0: this CTA scans; otherwise it codes (and, in the loopback, decodes)
+  // loopback decoding: the chunk, its escape section and the code-7 count
+  unsigned dchunk;
+  unsigned long long doff;
+  unsigned dsize;
+  int dok;
+  unsigned descapes;
+  unsigned slot_chunk[2], slot_size[2];  // a decoding-only CTA's two slots
+  int slot_ok[2];
 };
 
 // The 8 code-7 flags of a slice (bit 3j for value j) as bits 0..7.
@@ -246,8 +265,9 @@ __device__ __noinline__ void scanner(EncodeSmem& S, unsigned long long* flags, u
 __device__ void retirer(EncodeSmem& S, const EncodeParams& p) {
   const unsigned lane = threadIdx.x & 31;
   const uint64_t E0 = escape_base(p.n);
-  // A section ending past the raw form's length means the stream will be raw: it is not written.
-  const uint64_t room = raw_stream_bytes(p.n) > E0 ? raw_stream_bytes(p.n) - E0 : 0;
+  // A section ending past the raw form's length means the stream will be raw: it is not written
+  // (except in the loopback, which decodes every section of the coded form).
+  const uint64_t room = p.values ? ~0ull : raw_stream_bytes(p.n) > E0 ? raw_stream_bytes(p.n) - E0 : 0;
   unsigned long long* table = reinterpret_cast<unsigned long long*>(p.out + kHeaderBytes);
   unsigned retired = 0, freed = 0, spins = 0, backoff = 64;
   for (;;) {
@@ -319,6 +339,16 @@ __device__ void retirer(EncodeSmem& S, const EncodeParams& p) {
       }
       give_back = S.q_gap[i] + size;
     }
+    if (p.values) {
+      // Loopback: the sections and offsets above are written; mark each chunk copied, so that a
+      // decoding CTA may take it (the fence orders the warp's stores, and the coding threads'
+      // fixed parts that reached this warp through the queue, before the mark).
+      __syncwarp();
+      if (lane < run) {
+        __threadfence();
+        st_relaxed_u64(&p.flags[S.q_chunk[i]], kFlagCopied | (f & kFlagValueMask));
+      }
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) give_back += __shfl_xor_sync(0xFFFFFFFFu, give_back, o);
     retired += run;
@@ -383,6 +413,176 @@ __device__ __forceinline__ bool bar_coders_or(bool v) {
   return r != 0;
 }
 
+// Loopback, the 128 coding threads of a CTA: decode chunks in ticket order as their escape
+// sections reach the stream (the split-send pipeline: a chunk is transmissible, and here
+// decoded, as soon as its own bytes are in place, while later chunks are still being coded).
+// Each chunk waits (bounded, thread 0) for its copied mark, then its fixed part and escape
+// section are read back from the stream into the free input stages and decoded with the decode
+// kernel's own code.
+struct LoopbackArgs {  // what the loopback decoding needs, passed in registers
+  const uint8_t* stream;
+  uint16_t* values;
+  unsigned long long* flags;
+  Control* ctrl;
+  int* status;
+  uint64_t n, N;
+  unsigned spin_limit;
+};
+
+__device__ __noinline__ void loopback_decode(EncodeSmem& S, const uint8_t* stream, uint16_t* values,
+                                             unsigned long long* flags, Control* ctrl, int* status, uint64_t n,
+                                             uint64_t N, unsigned spin_limit) {
+  const LoopbackArgs p{stream, values, flags, ctrl, status, n, N, spin_limit};
+  const unsigned tid = threadIdx.x;
+  const uint64_t E0 = escape_base(p.n), R0 = records_base(p.n);
+  uint4* const fixed = S.xin[0];
+  uint4* const esc = S.xin[1];
+  for (;;) {
+    if (tid == 0) {
+      const unsigned d = atomicAdd(&p.ctrl->decode_ticket, 1u);
+      int ok = d < p.N;
+      if (ok) {
+        unsigned spins = 0, backoff = 64;
+        unsigned long long f;
+        while (((f = ld_relaxed_u64(&p.flags[d])) >> 62) != 3) {
+          if (read_status(p.status) != 0 || ++spins > p.spin_limit) {
+            if (spins > p.spin_limit) set_error(p.status, ZC_ERR_TIMEOUT);
+            ok = 0;
+            break;
+          }
+          __nanosleep(backoff);
+          backoff = backoff < 512 ? backoff * 2 : 512;
+        }
+        if (ok) {
+          // chunk d - 1 is resolved (the scan runs in order): its value ends the sections before d
+          const unsigned long long prev = d ? (ld_relaxed_u64(&p.flags[d - 1]) & kFlagValueMask) : 0ull;
+          __threadfence();  // acquire: the chunk's bytes are visible from here on
+          S.doff = E0 + prev;
+          S.dsize = static_cast<unsigned>((f & kFlagValueMask) - prev);
+        }
+      }
+      S.dchunk = d;
+      S.dok = ok;
+      S.descapes = 0;
+    }
+    bar_coders();
+    if (!S.dok) break;
+    const unsigned d = S.dchunk, m = chunk_values(p.n, d), size = S.dsize;
+    const unsigned fb = static_cast<unsigned>(fixed_bytes(m));
+    const uint4* gf = reinterpret_cast<const uint4*>(p.stream + R0 + static_cast<uint64_t>(d) * kFullFixedBytes);
+    const uint4* ge = reinterpret_cast<const uint4*>(p.stream + S.doff);
+    for (unsigned i = tid; i < fb / 16; i += kCoders) fixed[i] = __ldcg(gf + i);
+    for (unsigned i = tid; i < size / 16; i += kCoders) esc[i] = __ldcg(ge + i);
+    bar_coders();
+    decode_chunk(fixed, esc, &S.descapes, p.values + static_cast<uint64_t>(d) * kChunk, m, S.e0, size, p.status,
+                 tid, [] { bar_coders(); });
+    bar_coders();  // the stages are read before the next chunk is staged
+  }
+}
+
+// Thread 0: take the next chunk to decode and wait (bounded) for its copied mark.  Returns false
+// when no chunk is left or after an error or a timeout; otherwise *off and *size give its escape
+// section, and its bytes are visible to this thread's later reads (acquire).
+__device__ bool claim_decode(const LoopbackArgs& p, uint64_t E0, unsigned* d, unsigned long long* off,
+                             unsigned* size) {
+  *d = atomicAdd(&p.ctrl->decode_ticket, 1u);
+  if (*d >= p.N) return false;
+  unsigned spins = 0, backoff = 64;
+  unsigned long long f;
+  while (((f = ld_relaxed_u64(&p.flags[*d])) >> 62) != 3) {
+    if (read_status(p.status) != 0) return false;
+    if (++spins > p.spin_limit) {
+      set_error(p.status, ZC_ERR_TIMEOUT);
+      return false;
+    }
+    __nanosleep(backoff);
+    backoff = backoff < 512 ? backoff * 2 : 512;
+  }
+  // chunk d - 1 is resolved (the scan runs in order): its value ends the sections before d
+  const unsigned long long prev = *d ? (ld_relaxed_u64(&p.flags[*d - 1]) & kFlagValueMask) : 0ull;
+  __threadfence();
+  *off = E0 + prev;
+  *size = static_cast<unsigned>((f & kFlagValueMask) - prev);
+  return true;
+}
+
+// Loopback, a CTA that only decodes: two slots, each a chunk's fixed part (in an input stage) and
+// escape section (in the ring, unused here), filled by bulk async copies; the next chunk's copies
+// are in flight while a chunk is decoded.
+__device__ __noinline__ void loopback_decode_only(EncodeSmem& S, const uint8_t* stream, uint16_t* values,
+                                                  unsigned long long* flags, Control* ctrl, int* status, uint64_t n,
+                                                  uint64_t N, unsigned spin_limit) {
+  const LoopbackArgs p{stream, values, flags, ctrl, status, n, N, spin_limit};
+  const unsigned tid = threadIdx.x;
+  const uint64_t E0 = escape_base(p.n), R0 = records_base(p.n);
+  // slot j: fixed part in input stage j, escape section in the ring at 4096 j
+  auto fixed_of = [&](int j) { return S.xin[0] + j * (kInBytes / 16); };
+  auto esc_of = [&](int j) { return S.ring + j * (kMaxEscapeBytes / 16); };
+  // thread 0: claim a chunk and start its copies into slot j
+  auto fill = [&](int j) {
+    unsigned d = 0, size = 0;
+    unsigned long long off = 0;
+    const bool ok = claim_decode(p, E0, &d, &off, &size);
+    S.slot_chunk[j] = d;
+    S.slot_size[j] = size;
+    S.slot_ok[j] = ok;
+    if (ok) {
+      const unsigned fb = static_cast<unsigned>(fixed_bytes(chunk_values(p.n, d)));
+      asm volatile("fence.proxy.async.global;" ::: "memory");  // the acquired bytes, for the copy engine
+      mbar_arrive_expect_tx(&S.mbar[j], fb + size);
+      bulk_load(fixed_of(j), p.stream + R0 + static_cast<uint64_t>(d) * kFullFixedBytes, fb, &S.mbar[j]);
+      if (size) bulk_load(esc_of(j), p.stream + off, size, &S.mbar[j]);
+    }
+  };
+  if (tid == 0) {
+    for (int j = 0; j < 2; ++j) mbar_init(&S.mbar[j], 1);
+    fence_mbar_init();
+    fill(0);
+    fill(1);
+  }
+  bar_coders();
+  unsigned parity = 0;
+  for (int j = 0;; j ^= 1) {
+    if (!S.slot_ok[j]) break;
+    // every thread polls; all act on one shared answer
+    const bool arrived = mbar_wait(&S.mbar[j], (parity >> j) & 1u, kWaitLimit);
+    parity ^= 1u << j;
+    if (bar_coders_or(!arrived)) {
+      if (tid == 0) {  // never leave a copy in flight (bounded again)
+        set_error(p.status, ZC_ERR_TIMEOUT);
+        mbar_wait(&S.mbar[j], ((parity >> j) & 1u) ^ 1u, kWaitLimit);
+        if (S.slot_ok[j ^ 1]) mbar_wait(&S.mbar[j ^ 1], (parity >> (j ^ 1)) & 1u, kWaitLimit);
+      }
+      return;
+    }
+    const unsigned d = S.slot_chunk[j];
+    if (tid == 0) S.descapes = 0;
+    bar_coders();
+    decode_chunk(fixed_of(j), esc_of(j), &S.descapes, p.values + static_cast<uint64_t>(d) * kChunk, chunk_values(p.n, d),
+                 S.e0, S.slot_size[j], p.status, tid, [] { bar_coders(); });
+    bar_coders();  // slot j is read: refill it
+    if (tid == 0) fill(j);
+    bar_coders();
+  }
+  // the other slot may still hold a claimed chunk whose copies are in flight: decode it too
+  const int k = S.slot_ok[0] ? 0 : (S.slot_ok[1] ? 1 : -1);
+  if (k >= 0) {
+    const bool arrived = mbar_wait(&S.mbar[k], (parity >> k) & 1u, kWaitLimit);
+    if (bar_coders_or(!arrived)) {
+      if (tid == 0) {
+        set_error(p.status, ZC_ERR_TIMEOUT);
+        mbar_wait(&S.mbar[k], (parity >> k) & 1u, kWaitLimit);  // never leave a copy in flight
+      }
+      return;
+    }
+    if (tid == 0) S.descapes = 0;
+    bar_coders();
+    const unsigned d = S.slot_chunk[k];
+    decode_chunk(fixed_of(k), esc_of(k), &S.descapes, p.values + static_cast<uint64_t>(d) * kChunk, chunk_values(p.n, d),
+                 S.e0, S.slot_size[k], p.status, tid, [] { bar_coders(); });
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     encode_kernel(const EncodeParams p, const __grid_constant__ CUtensorMap in_map) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -407,8 +607,20 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     if (warp < kCoderWarps) scanner(S, p.flags, p.N, p.status, p.spin_limit);
     return;
   }
+  // Loopback: kLoopbackDecoders CTAs in every kLoopbackCycle decode from the start; the others
+  // code, then decode too.
+  const bool decode_only = p.values != nullptr && S.role % kLoopbackCycle >= kLoopbackCycle - kLoopbackDecoders;
   if (warp == kCoders / 32) {  // the retiring warp
-    retirer(S, p);
+    if (!decode_only) retirer(S, p);
+    return;
+  }
+  if (decode_only) {
+    if (tid == 0) {
+      if (p.base < 0) asm volatile("griddepcontrol.wait;" ::: "memory");
+      S.e0 = p.base >= 0 ? p.base : __ldcg(&p.ctrl->e0);
+    }
+    bar_coders();
+    loopback_decode_only(S, p.out, p.values, p.flags, p.ctrl, p.status, p.n, p.N, p.spin_limit);
     return;
   }
 
@@ -597,6 +809,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     for (int s = 0; s < kStages; ++s)  // never leave a copy in flight
       if (pending & (1u << s)) mbar_wait(&S.mbar[s], (parity >> s) & 1u, kWaitLimit);
   }
+  if (p.values) {  // loopback: no chunk left to code, so decode (the stages are free now)
+    bar_coders();
+    loopback_decode(S, p.out, p.values, p.flags, p.ctrl, p.status, p.n, p.N, p.spin_limit);
+  }
 }
 
 // n = 0: the raw form (32 bytes, the header alone) is shorter than the coded one (48 bytes).
@@ -704,7 +920,7 @@ cudaError_t encode_occupancy(int* per_sm) {
 
 cudaError_t launch_encode(const uint16_t* in, uint64_t n, int base, uint8_t* out, unsigned long long* out_bytes,
                           uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream, uint64_t stall_chunk,
-                          unsigned spin_limit) {
+                          unsigned spin_limit, uint16_t* loopback_values) {
   Control* ctrl = reinterpret_cast<Control*>(ws);
   if (n == 0) {
     empty_stream_kernel<<<1, 1, 0, stream>>>(out, base, ctrl, out_bytes);
@@ -723,6 +939,7 @@ cudaError_t launch_encode(const uint16_t* in, uint64_t n, int base, uint8_t* out
   p.stall_chunk = stall_chunk;
   p.spin_limit = spin_limit;
   p.full_chunks = n / kChunk;
+  p.values = loopback_values;
   CUtensorMap map;
   cudaError_t err = input_map(in, n, &map);
   if (err != cudaSuccess) return err;
