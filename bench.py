@@ -24,7 +24,9 @@ and unless --no-extras:
                            least 64M values (MoE activations, the adversarial tensor, N(0, 1) at
                            2^26 .. 2^29), L2 flushed between steps;
   sweep                    latency and GB/s per size for N(0, 1) buffers of 2^15 .. 2^29 values,
-                           each compressed and decompressed 100 times back to back on one stream.
+                           each compressed and decompressed 100 times back to back on one stream;
+                           up to 2^22 values also the same 100 round trips replayed from a CUDA graph
+                           (the device's time without the host's per-call cost).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
                   [--no-extras] [--profile]
@@ -56,9 +58,9 @@ TARGET_CONFIGS = ["moe_a2a_16384x7168", "adversarial_256m", "sweep_2^26", "sweep
 SWEEP_SIZES = list(range(15, 30))  # 2^15 .. 2^29 values (64 KiB .. 1 GiB)
 SWEEP_REPS = 100
 L2_FLUSH_BYTES = 256 << 20
-KERNEL_NAMES = {1: "stats", 2: "encode", 3: "decode", 4: "raw_form"}
+KERNEL_NAMES = {1: "stats", 2: "encode", 3: "decode", 4: "raw_form", 5: "small", 6: "exact"}
 KERNEL_SOURCES = {"stats": "zc_stats.cu", "encode": "zc_encode.cu", "decode": "zc_decode.cu",
-                  "raw_form": "zc_encode.cu"}
+                  "raw_form": "zc_encode.cu", "small": "zc_small.cu", "exact": "zc_stats.cu"}
 
 
 # ---------------------------------------------------------------------------- ranks
@@ -308,6 +310,36 @@ class Codec:
             return [e[0].elapsed_time(e[1]) for e in ev], [e[1].elapsed_time(e[2]) for e in ev]
         return ([e[0].elapsed_time(e[1]) for e in ev],)
 
+    def replayed(self, reps):
+        """The same `reps` round trips captured once in a CUDA graph and replayed: mean ms per round
+        trip without the host's per-call cost (None when the calls cannot be captured)."""
+        torch = self.torch
+        try:
+            side = torch.cuda.Stream(self.device)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(side):
+                sh = side.cuda_stream
+                with torch.cuda.graph(g, stream=side):
+                    for _ in range(reps):
+                        self.zc.zc_compress(self.xd.data_ptr(), self.n, self.zc.ZC_BASE_AUTO, self.out.data_ptr(),
+                                            self.ob.data_ptr(), sh)
+                        self.zc.zc_decompress(self.out.data_ptr(), self.dec.data_ptr(), self.n, sh)
+            self.dec[:self.n].zero_()
+            g.replay()
+            torch.cuda.synchronize()
+            if not self.verified():  # the replay must really have run the codec
+                return None
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(self.stream)
+            g.replay()
+            b.record(self.stream)
+            torch.cuda.synchronize()
+            del g
+            return a.elapsed_time(b) / reps
+        except Exception:  # noqa: BLE001 -- capture is optional; the plain numbers stand
+            torch.cuda.synchronize()
+            return None
+
     def back_to_back(self, reps, clocks=None):
         """`reps` compress+decompress round trips back to back on one stream (no flush), then
         `reps` compresses alone and `reps` decompresses alone: mean ms of each."""
@@ -479,6 +511,10 @@ def run_ours(args, rank, world, local):
             sweep[name] = {"n": m, "round_trip_us": round(bt[0] * 1e3, 2), "compress_us": round(bt[1] * 1e3, 2),
                            "decompress_us": round(bt[2] * 1e3, 2),
                            "gbs_input": round(2 * m / bt[0] / 1e6, 1), "verified": cd.verified()}
+            if k <= 22:  # small messages: the device's own time per round trip, without host calls
+                rp = cd.replayed(SWEEP_REPS)
+                sweep[name]["graph_round_trip_us"] = round(rp * 1e3, 2) if rp else None
+                sweep[name]["verified"] = sweep[name]["verified"] and cd.verified()
             if name in TARGET_CONFIGS:
                 if name == args.workload:
                     c_ms, d_ms, Cc, ee, okc = head["compress_ms"], head["decompress_ms"], head["C"], head["e0"], ok

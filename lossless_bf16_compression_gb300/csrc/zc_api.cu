@@ -68,6 +68,8 @@ cudaError_t device_info(DeviceInfo* info) {
     if (err != cudaSuccess) return err;
     err = encode_occupancy(&d.encode_per_sm);
     if (err != cudaSuccess) return err;
+    err = small_setup();
+    if (err != cudaSuccess) return err;
     g_devices[dev] = d;
     g_device_ready[dev] = true;
   }
@@ -112,6 +114,26 @@ uint64_t workspace_at(uint64_t n, bool loopback) {
   return loopback ? (max_coded_bytes(n) + 255) & ~uint64_t(255) : workspace_offset(n);
 }
 
+}  // namespace
+
+namespace zc {
+
+// A pageable length: copy it back from the control block and wait for it.
+int finish_length(bool pageable, uint8_t* ws, size_t* out_bytes, cudaStream_t stream) {
+  if (!pageable) return ZC_OK;
+  unsigned long long total = 0;
+  const Control* ctrl = reinterpret_cast<const Control*>(ws);
+  if (cudaMemcpyAsync(&total, &ctrl->total, sizeof total, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+    return ZC_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return ZC_ERR_CUDA;
+  *out_bytes = static_cast<size_t>(total);
+  return ZC_OK;
+}
+
+}  // namespace zc
+
+namespace {
+
 int compress_impl(const void* in, size_t n, int base, void* out, size_t* out_bytes, cudaStream_t stream,
                   uint64_t stall_chunk, unsigned spin_limit, void* values = nullptr) {
   if (n > ZC_MAX_N || base < ZC_BASE_AUTO || base > kE0Max) return ZC_ERR_INVALID_ARG;
@@ -138,24 +160,22 @@ int compress_impl(const void* in, size_t n, int base, void* out, size_t* out_byt
 
   uint8_t* o = static_cast<uint8_t*>(out);
   uint8_t* ws = o + workspace_at(n, loopback);
-  if (cudaMemsetAsync(ws, 0, workspace_bytes(n), stream) != cudaSuccess) return ZC_ERR_CUDA;
   const uint16_t* x = static_cast<const uint16_t*>(in);
+  if (n > 0 && n <= small_max_values() && !loopback && stall_chunk == ~uint64_t(0)) {
+    // a small tensor: one launch, no workspace to clear
+    if (launch_small(x, n, base, o, len_ptr, ws, dev, stream) != cudaSuccess) return ZC_ERR_CUDA;
+    return finish_length(pageable, ws, out_bytes, stream);
+  }
+  if (cudaMemsetAsync(ws, 0, workspace_bytes(n), stream) != cudaSuccess) return ZC_ERR_CUDA;
   if (n > 0 && base == ZC_BASE_AUTO) {
     if (launch_stats(x, n, ws, dev, stream) != cudaSuccess) return ZC_ERR_CUDA;
+    if (launch_exact(x, n, ws, dev, stream) != cudaSuccess) return ZC_ERR_CUDA;
   }
   if (launch_encode(x, n, base, o, len_ptr, ws, dev, stream, stall_chunk, spin_limit,
                     static_cast<uint16_t*>(values)) != cudaSuccess)
     return ZC_ERR_CUDA;
   if (launch_raw_form(x, n, base, o, len_ptr, ws, dev, stream) != cudaSuccess) return ZC_ERR_CUDA;
-  if (pageable) {
-    unsigned long long total = 0;
-    const Control* ctrl = reinterpret_cast<const Control*>(ws);
-    if (cudaMemcpyAsync(&total, &ctrl->total, sizeof total, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
-      return ZC_ERR_CUDA;
-    if (cudaStreamSynchronize(stream) != cudaSuccess) return ZC_ERR_CUDA;
-    *out_bytes = static_cast<size_t>(total);
-  }
-  return ZC_OK;
+  return finish_length(pageable, ws, out_bytes, stream);
 }
 
 }  // namespace

@@ -80,11 +80,14 @@ __host__ __device__ inline uint64_t max_coded_bytes(uint64_t n) {
 // ------------------------------------------------------------------ workspace (tail of `out`)
 //
 // [ws + 0,    ws + 256)            Control block
-// [ws + 256,  ws + 256 + 16 KiB)   per-CTA partials of the statistics pass
+// [ws + 256,  ws + 256 + 14 KiB)   per-CTA partials of the statistics pass
+// [.., ws + 256 + 16 KiB)          exact fallback: per-exponent sums of sig^2, 256 x u64
 // [ws + 16640, ...)                scan state, one u64 per chunk
-constexpr int kStatsMaxCtas = 1024;
+constexpr int kStatsMaxCtas = 896;
 constexpr uint64_t kWsControlBytes = 256;
-constexpr uint64_t kWsPartialsBytes = 16ull * kStatsMaxCtas;
+constexpr uint64_t kWsExactBinsOffset = kWsControlBytes + 16ull * kStatsMaxCtas;
+constexpr uint64_t kWsPartialsBytes = 16ull * kStatsMaxCtas + 8 * 256;  // partials and exact bins
+static_assert(kWsPartialsBytes == 16384, "the workspace layout is unchanged");
 
 struct Control {
   unsigned encode_ticket;   // next chunk to hand out (encoder)
@@ -94,6 +97,9 @@ struct Control {
   unsigned long long total; // stream length, for the pageable out_bytes path
   unsigned role_ticket;     // encoder CTAs in start order: the first one to start scans
   unsigned decode_ticket;   // loopback: next chunk to decode
+  unsigned exact_done;      // CTAs of the exact fallback that have finished
+  unsigned long long n_finite;  // finite values, for the exact fallback
+  unsigned long long exact_pieces[4];  // exact fallback: 32-bit pieces of the window sums
 };
 
 struct StatsPartial {
@@ -305,6 +311,10 @@ void timing_end(TimingRecord& rec, cudaStream_t stream);
 // The launches.  `ws` is the call's workspace (workspace_bytes(n) bytes, cleared): the tail of
 // `out` for zc_compress, the library's static array for zc_compress_static_scratch.
 cudaError_t launch_stats(const uint16_t* in, uint64_t n, uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream);
+// After the statistics kernel (auto mode): when its estimate could not settle e0, the exact sum
+// of squares over the whole grid (per-exponent integer sums) decides it; otherwise the kernel
+// returns at once.
+cudaError_t launch_exact(const uint16_t* in, uint64_t n, uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream);
 cudaError_t launch_encode(const uint16_t* in, uint64_t n, int base, uint8_t* out, unsigned long long* out_bytes,
                           uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream, uint64_t stall_chunk,
                           unsigned spin_limit, uint16_t* loopback_values = nullptr);
@@ -314,6 +324,17 @@ cudaError_t launch_decode(const uint8_t* in, uint16_t* out, uint64_t n, const De
 // stream in the raw form (header, the n values, zero padding); otherwise return at once.
 cudaError_t launch_raw_form(const uint16_t* in, uint64_t n, int base, uint8_t* out, unsigned long long* out_bytes,
                             uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream);
+
+// Small tensors (up to small_max_values() = 131072 values): the whole compression in one cluster launch,
+// with no workspace beyond the control block's e0, exact-path flag and length.
+cudaError_t small_setup();  // per device: the kernel's dynamic shared memory size
+uint64_t small_max_values();
+cudaError_t launch_small(const uint16_t* in, uint64_t n, int base, uint8_t* out, unsigned long long* out_bytes,
+                         uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream);
+
+// After the launches of a compression: when the caller's length is pageable host memory, copy
+// it back from the control block and synchronize the stream.  Returns a ZC_ status.
+int finish_length(bool pageable, uint8_t* ws, size_t* out_bytes, cudaStream_t stream);
 
 constexpr unsigned kDefaultSpinLimit = 1u << 20;  // polls of a bounded wait in the encoder
 

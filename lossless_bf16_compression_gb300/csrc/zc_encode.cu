@@ -35,6 +35,7 @@
 #include <cstring>
 #include <mutex>
 
+#include "zc_code_core.cuh"
 #include "zc_common.cuh"
 #include "zc_decode_core.cuh"
 #include "zc_ring.h"
@@ -117,21 +118,7 @@ struct __align__(128) EncodeSmem {
   int slot_ok[2];
 };
 
-// The 8 code-7 flags of a slice (bit 3j for value j) as bits 0..7.
-__device__ __forceinline__ unsigned compact8(unsigned m) {
-  m = (m | (m >> 2)) & 0x0C30C3u;
-  m = (m | (m >> 4)) & 0x00F00Fu;
-  return (m | (m >> 8)) & 0xFFu;
-}
-
 __device__ __forceinline__ void bar_coders() { asm volatile("bar.sync 1, %0;" ::"n"(kCoders) : "memory"); }
-
-// Index of the highest set bit of a nonzero word.
-__device__ __forceinline__ unsigned msb_index(unsigned x) {
-  unsigned b;
-  asm("bfind.u32 %0, %1;" : "=r"(b) : "r"(x));
-  return b;
-}
 
 // The coding threads' escape counts in thread order (= position order): this thread's first
 // rank (the exclusive prefix) and the chunk total.  One barrier over the coding threads [R];
@@ -691,39 +678,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         S.xin[s][(sw ^ (16 * q)) / 16] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
       }
     }
-    uint32_t g[4];   // 24-bit code groups
-    uint32_t sm[8];  // sign|mantissa bytes, four per word
-    uint32_t e[4];   // code-7 flags: bit 3j of e[q] for value v0 + 8q + j
+    uint4 xv[4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const uint4 xv = S.xin[s][(sw ^ (16 * q)) / 16];
-      uint32_t w[4] = {xv.x, xv.y, xv.z, xv.w};
-      uint32_t c7[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) c7[i] = codes7_x2(w[i], kadd);
-      if (!full) {  // values past m: code 0, byte 0, no escape
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const unsigned v = v0 + 8 * q + 2 * i;
-          const uint32_t keep = (v < m ? 0x0000FFFFu : 0u) | (v + 1 < m ? 0xFFFF0000u : 0u);
-          c7[i] &= keep;
-          w[i] &= keep;
-        }
-      }
-      sm[2 * q] = sign_mantissa_x4(w[0], w[1]);
-      sm[2 * q + 1] = sign_mantissa_x4(w[2], w[3]);
-      g[q] = pack_codes8(c7);
-      e[q] = g[q] & (g[q] >> 1) & (g[q] >> 2) & 0x249249u;  // code 7
-    }
-    uint8_t* const smp = fixed + cbytes + v0;
-    if (full || v0 < smbytes) *reinterpret_cast<uint4*>(smp) = make_uint4(sm[0], sm[1], sm[2], sm[3]);
-    if (full || v0 + 16 < smbytes) *reinterpret_cast<uint4*>(smp + 16) = make_uint4(sm[4], sm[5], sm[6], sm[7]);
-    const uint32_t cw[3] = {g[0] | (g[1] << 24), (g[1] >> 8) | (g[2] << 16), (g[2] >> 16) | (g[3] << 8)};
-    uint32_t* const cp = reinterpret_cast<uint32_t*>(fixed + 12 * tid);
-#pragma unroll
-    for (int i = 0; i < 3; ++i)
-      if (full || 12 * tid + 4 * i < cbytes) cp[i] = cw[i];
-    const unsigned cnt = __popc(e[0]) + __popc(e[1]) + __popc(e[2]) + __popc(e[3]);
+    for (int q = 0; q < 4; ++q) xv[q] = S.xin[s][(sw ^ (16 * q)) / 16];
+    Coded32 kd;
+    code32(xv, kadd, v0, m, full, kd);
+    store_fixed32(fixed, cbytes, smbytes, v0, full, kd);
+    const unsigned cnt = __popc(kd.e[0]) + __popc(kd.e[1]) + __popc(kd.e[2]) + __popc(kd.e[3]);
 
     unsigned base;
     const unsigned k = chunk_rank(cnt, &base, S.scan);  // [R]
@@ -751,35 +712,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       const uint32_t xs = smem_u32(S.xin[s]);  // value v0 + b at byte xs + (sw ^ (2b & 0x3E))
       unsigned m32 = 0;  // the flags compacted: value v0 + b at bit b
 #pragma unroll
-      for (int q = 0; q < 4; ++q) m32 |= compact8(e[q]) << (8 * q);
-      if (__reduce_max_sync(0xFFFFFFFFu, cnt) < kDenseMin) {
-        // Highest value first: ranks base + cnt - 1 down to base.
-        uint32_t at16 = esc + 2 * (base + cnt), at8 = esc + 2 * k + base + cnt;  // one past the last
-        unsigned mm = m32;
-        while (mm) {
-          const unsigned b = msb_index(mm);
-          mm ^= 1u << b;
-          at16 -= 2;
-          at8 -= 1;
-          sts_u16(at16, v0 + b);
-          sts_u8(at8, lds_u16(xs + (sw ^ ((2 * b) & 0x3Eu))) >> 7);
-        }
-      } else {
-        // Dense: in the loop above the lanes' values and ranks would lie 32 apart and meet in
-        // the same shared-memory banks.  So lane L takes its escapes from value L - 1 downwards
-        // (modulo 32), its flags rotated right by L, and ranks each one by counting its flags
-        // below it.
-        const unsigned rot = tid & 31;
-        unsigned mm = __funnelshift_r(m32, m32, rot);  // value b at bit (b - rot) mod 32
-        while (mm) {
-          const unsigned bp = msb_index(mm);
-          mm ^= 1u << bp;
-          const unsigned b = (bp + rot) & 31;
-          const unsigned r = base + __popc(m32 & ((1u << b) - 1u));
-          sts_u16(esc + 2 * r, v0 + b);
-          sts_u8(esc + 2 * k + r, lds_u16(xs + (sw ^ ((2 * b) & 0x3Eu))) >> 7);
-        }
-      }
+      for (int q = 0; q < 4; ++q) m32 |= compact8(kd.e[q]) << (8 * q);
+      write_list32(m32, cnt, v0, base, k, esc, __reduce_max_sync(0xFFFFFFFFu, cnt) >= kDenseMin,
+                   [&](unsigned b) { return lds_u16(xs + (sw ^ ((2 * b) & 0x3Eu))) >> 7; });
       if (tid < esc_bytes - 3 * k) sts_u8(esc + 3 * k + tid, 0);  // zero padding, < 16 bytes
     }
     if (bar_coders_or(stop)) break;  // [C] the list is complete in the ring; stage s is free again

@@ -76,22 +76,19 @@ extern "C" int zc_compress_static_scratch(const void* in, size_t n, int base_or_
   const bool pageable = attr.type == cudaMemoryTypeUnregistered || attr.devicePointer == nullptr;
   unsigned long long* len_ptr = pageable ? nullptr : static_cast<unsigned long long*>(attr.devicePointer);
 
-  if (cudaMemsetAsync(ws, 0, workspace_bytes(n), stream) != cudaSuccess) return ZC_ERR_CUDA;
   const uint16_t* x = static_cast<const uint16_t*>(in);
   uint8_t* o = static_cast<uint8_t*>(out);
+  if (n > 0 && n <= small_max_values()) {  // a small tensor: one launch, nothing to clear
+    if (launch_small(x, n, base_or_auto, o, len_ptr, ws, dev, stream) != cudaSuccess) return ZC_ERR_CUDA;
+    return finish_length(pageable, ws, out_bytes, stream);
+  }
+  if (cudaMemsetAsync(ws, 0, workspace_bytes(n), stream) != cudaSuccess) return ZC_ERR_CUDA;
   if (n > 0 && base_or_auto == ZC_BASE_AUTO) {
     if (launch_stats(x, n, ws, dev, stream) != cudaSuccess) return ZC_ERR_CUDA;
+    if (launch_exact(x, n, ws, dev, stream) != cudaSuccess) return ZC_ERR_CUDA;
   }
   if (launch_encode(x, n, base_or_auto, o, len_ptr, ws, dev, stream, ~uint64_t(0), kDefaultSpinLimit) != cudaSuccess)
     return ZC_ERR_CUDA;
   if (launch_raw_form(x, n, base_or_auto, o, len_ptr, ws, dev, stream) != cudaSuccess) return ZC_ERR_CUDA;
-  if (pageable) {
-    unsigned long long total = 0;
-    const Control* ctrl = reinterpret_cast<const Control*>(ws);
-    if (cudaMemcpyAsync(&total, &ctrl->total, sizeof total, cudaMemcpyDeviceToHost, stream) != cudaSuccess)
-      return ZC_ERR_CUDA;
-    if (cudaStreamSynchronize(stream) != cudaSuccess) return ZC_ERR_CUDA;
-    *out_bytes = static_cast<size_t>(total);
-  }
-  return ZC_OK;
+  return finish_length(pageable, ws, out_bytes, stream);
 }

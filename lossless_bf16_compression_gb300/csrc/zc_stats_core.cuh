@@ -1,0 +1,245 @@
+// zc_stats_core.cuh -- the arithmetic of the window base e0, shared by the statistics kernel and
+// the small-tensor kernel: fp32 block sums of squares with a rigorous error bound, the window rule,
+// and the exact fallback (per-exponent integer sums rounded once to fp64).
+//
+// Method: ZipCCL (SIGCOMM scribe notes), "Key idea and contribution", first technique: the
+// window of frequent exponents is taken from the tensor's standard deviation alone, with no
+// histogram and no sort.  e0 = floor(log2(sigma * c)) + 127 clamped to [0, 249], sigma^2 = S / n_f,
+// where S is the exact sum of squares rounded once to fp64 and c^2 = 0x1.79a1e790e0f01p-10 (the
+// base whose 7-binade window has the fewest expected escapes under a Gaussian).
+//
+// Every block sum of 64 values carries a relative error below 2^-18 (at most 17 roundings, or 64
+// on the careful path), so a total over blocks lies within 2^-17 of the exact sum; decide_e0 then
+// settles e0 exactly for all but ~4e-5 of random tensors, and the exact fallback decides the rest.
+#pragma once
+
+#include "zc_common.cuh"
+
+namespace zc {
+namespace {
+
+constexpr double kWindowC2 = 0x1.79a1e790e0f01p-10;
+
+// floor(log2(y)) for a positive finite double, from its bit pattern.
+__device__ __forceinline__ int ilogb_pos(double y) {
+  const unsigned long long b = static_cast<unsigned long long>(__double_as_longlong(y));
+  const int ex = static_cast<int>((b >> 52) & 0x7FF);
+  if (ex != 0) return ex - 1023;
+  const unsigned long long mant = b & ((1ull << 52) - 1);
+  return (63 - __clzll(static_cast<long long>(mant))) - 1074;
+}
+
+__device__ __forceinline__ int floor_half(int v) { return v >= 0 ? v / 2 : -((-v + 1) / 2); }
+
+// The window rule at a given fp64 sum of squares.
+__device__ int select_e0(double S, unsigned long long n_f) {
+  if (n_f == 0 || S == 0.0) return 0;
+  const double q = __ddiv_rn(S, static_cast<double>(n_f));
+  const double y = __dmul_rn(q, kWindowC2);
+  int e = floor_half(ilogb_pos(y)) + 127;
+  return e < 0 ? 0 : (e > kE0Max ? kE0Max : e);
+}
+
+// Careful block sum for 64 values (32 words): skips Inf/NaN, and scales every square by
+// 4^-(Emax'-E') relative to the largest exponent present, so no fp32 overflow or underflow
+// matters.  Returns the fp64 value of the block sum and adds the non-finite count.
+__device__ __forceinline__ double careful_block(const uint32_t (&w)[32], unsigned* nonfinite) {
+  int emax = 0;
+  unsigned nf = 0;
+#pragma unroll
+  for (int i = 0; i < 64; ++i) {
+    const uint32_t x = (w[i >> 1] >> (16 * (i & 1))) & 0xFFFFu;
+    const int E = (x >> 7) & 0xFF;
+    if (E == 255) {
+      ++nf;
+    } else if (x & 0x7FFFu) {
+      emax = max(emax, max(E, 1));
+    }
+  }
+  *nonfinite += nf;
+  if (emax == 0) return 0.0;  // only zeros (and non-finite values)
+  float s = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 64; ++i) {
+    const uint32_t x = (w[i >> 1] >> (16 * (i & 1))) & 0xFFFFu;
+    const int E = (x >> 7) & 0xFF;
+    if (E == 255 || (x & 0x7FFFu) == 0) continue;
+    const int sig = E ? 128 + static_cast<int>(x & 0x7F) : static_cast<int>(x & 0x7F);
+    const int d2 = 2 * (emax - max(E, 1));
+    if (d2 > 126) continue;  // below 2^-110 of the block's largest square
+    s = fmaf(static_cast<float>(sig * sig), __int_as_float((127 - d2) << 23), s);
+  }
+  // The block sum is s * 2^(2 emax - 268); emax in [1, 254] keeps the scale a normal double.
+  const double scale = __longlong_as_double(static_cast<long long>(755 + 2 * emax) << 52);
+  return static_cast<double>(s) * scale;
+}
+
+// The last n % 8 values, zero-padded (a zero adds nothing and is not counted as non-finite).
+__device__ __noinline__ double tail_block(const uint16_t* tail, unsigned count, unsigned* nonfinite) {
+  uint32_t w[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) w[i] = 0;
+  for (unsigned i = 0; i < count; ++i) w[i >> 1] |= static_cast<uint32_t>(tail[i]) << (16 * (i & 1));
+  return careful_block(w, nonfinite);
+}
+
+__device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// A block holding Inf or NaN, reloaded from memory (so that the fast path's registers need not
+// survive the call) and summed by the careful path.
+__device__ __noinline__ double careful_block_at(const uint4* in, uint64_t wb, uint64_t nv, unsigned lane,
+                                                unsigned* nonfinite) {
+  uint32_t w[32];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint64_t idx = wb + 32 * j + lane;
+    const uint4 v = idx < nv ? __ldg(in + idx) : make_uint4(0, 0, 0, 0);
+    w[4 * j] = v.x;
+    w[4 * j + 1] = v.y;
+    w[4 * j + 2] = v.z;
+    w[4 * j + 3] = v.w;
+  }
+  return careful_block(w, nonfinite);
+}
+
+// Block sum of 64 values (this lane's block; `careful` sums a block holding Inf or NaN).  Bit patterns with the sign cleared order like magnitudes, so one
+// packed 16-bit max finds the block's largest, and it decides, per warp, between the plain sum
+// (every lane's largest biased exponent in [87, 187): no square reaches 2^122 and the block sum
+// is at least 2^-80, so the 64 squares, 17 roundings, stay within 2^-19 of the exact sum) and a
+// sum with every lane's values scaled by 2^(126 - Es), Es = E clamped to [1, 252] (1 for lanes
+// that need no scaling), which puts the largest magnitude in [2^-8, 4): no square overflows and
+// what underflows is under 2^-120 of the block sum.  The decision is one warp vote, so a warp runs one of the two loops.
+// Blocks holding Inf or NaN take the careful path.
+template <typename Careful>
+__device__ __forceinline__ void block_sum_with(const uint32_t (&w)[32], double* acc, Careful careful) {
+  uint32_t mx = 0;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) mx = max_u16x2(mx, w[i] & 0x7FFF7FFFu);
+  const unsigned m = max(mx & 0xFFFFu, mx >> 16);
+  const unsigned E = m >> 7;
+  const bool nonfin = m >= 0x7F80u;
+  const bool odd = m != 0 && (E >= 187u || E < 87u);
+  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+  if (!__any_sync(0xFFFFFFFFu, nonfin || odd)) {
+#pragma unroll
+    for (int i = 0; i < 32; i += 2) {
+      const float l0 = __uint_as_float(w[i] << 16), h0 = __uint_as_float(w[i] & 0xFFFF0000u);
+      const float l1 = __uint_as_float(w[i + 1] << 16), h1 = __uint_as_float(w[i + 1] & 0xFFFF0000u);
+      a0 = fmaf(l0, l0, a0);
+      a1 = fmaf(h0, h0, a1);
+      a2 = fmaf(l1, l1, a2);
+      a3 = fmaf(h1, h1, a3);
+    }
+    *acc += static_cast<double>((a0 + a1) + (a2 + a3));
+    return;
+  }
+  if (nonfin) {
+    *acc += careful();
+    return;
+  }
+  const int Es = odd ? min(max(static_cast<int>(E), 1), 252) : 126;
+  const float sc = __int_as_float((253 - Es) << 23);
+#pragma unroll
+  for (int i = 0; i < 32; i += 2) {
+    const float l0 = __uint_as_float(w[i] << 16) * sc, h0 = __uint_as_float(w[i] & 0xFFFF0000u) * sc;
+    const float l1 = __uint_as_float(w[i + 1] << 16) * sc, h1 = __uint_as_float(w[i + 1] & 0xFFFF0000u) * sc;
+    a0 = fmaf(l0, l0, a0);
+    a1 = fmaf(h0, h0, a1);
+    a2 = fmaf(l1, l1, a2);
+    a3 = fmaf(h1, h1, a3);
+  }
+  const float blk = (a0 + a1) + (a2 + a3);
+  *acc += static_cast<double>(blk) * __longlong_as_double(static_cast<long long>(1023 + 2 * Es - 252) << 52);
+}
+
+// The same for the statistics kernel, whose careful path reloads the block from memory.
+__device__ __forceinline__ void block_sum(const uint32_t (&w)[32], const uint4* in, uint64_t wb, uint64_t nv,
+                                          unsigned lane, double* acc, unsigned* nonfinite) {
+  block_sum_with(w, acc, [&] { return careful_block_at(in, wb, nv, lane, nonfinite); });
+}
+
+// The window rule at an fp64 estimate S_est of the sum of squares that lies within 2^-17 of the
+// exact sum: evaluated at S_est (1 -+ 2^-16), rounded outward, both ends give the exact e0 when
+// they agree (the rule is monotone in S).  Returns false when they do not: the exact sum decides.
+__device__ __forceinline__ bool decide_e0(double S_est, unsigned long long n_f, int* e0) {
+  *e0 = 0;
+  if (n_f == 0 || S_est == 0.0) return true;
+  const double lo = __dmul_rd(S_est, 1.0 - 0x1p-16);
+  const double hi = __dmul_ru(S_est, 1.0 + 0x1p-16);
+  const int elo = select_e0(lo, n_f), ehi = select_e0(hi, n_f);
+  *e0 = elo;
+  return elo == ehi;
+}
+
+// Per-exponent integer sums of sig^2 of the finite values x[i], i = start, start + stride, ..
+// < count, added into bins[E] (shared, 256 words; E = 0 and 1 share bin 1).
+__device__ __forceinline__ void add_exponent_sums(const uint16_t* x, uint64_t count, uint64_t start, uint64_t stride,
+                                                  unsigned long long* bins) {
+  for (uint64_t i = start; i < count; i += stride) {
+    const unsigned v = x[i];
+    const unsigned E = (v >> 7) & 0xFF;
+    if (E == 255 || (v & 0x7FFF) == 0) continue;
+    const unsigned sig = E ? 128 + (v & 0x7F) : (v & 0x7F);
+    atomicAdd(bins + (E ? E : 1), static_cast<unsigned long long>(sig * sig));
+  }
+}
+
+// Add t * 2^s (t < 2^64, s + 64 < 576) into a 576-bit integer.
+__device__ __forceinline__ void add_shifted_576(unsigned long long (&limb)[9], unsigned long long t, int s) {
+  if (t == 0) return;
+  const int li = s >> 6, sh = s & 63;
+  const unsigned long long add[2] = {t << sh, sh ? t >> (64 - sh) : 0ull};
+  unsigned long long carry = 0;
+  for (int j = li; j < 9; ++j) {
+    const unsigned long long a = (j - li < 2 ? add[j - li] : 0ull);
+    const unsigned long long before = limb[j];
+    unsigned long long sum = before + a;
+    unsigned long long c1 = sum < before;
+    sum += carry;
+    c1 += sum < carry;
+    limb[j] = sum;
+    carry = c1;
+    if (j - li >= 1 && carry == 0) break;
+  }
+}
+
+// The 576-bit integer sum_E T_E 2^(2E-2) (= S 2^266) of per-exponent sums T_E (each below 2^56),
+// plus, when `pieces` is given, sum_k pieces[k] 2^(32k + 2 Eb - 2) (window sums relative to the
+// exponent Eb), rounded once to fp64, nearest-even: the exact sum of squares S rounded correctly.
+// One thread.
+__device__ __noinline__ double exact_from_bins(const unsigned long long* bins,
+                                               const unsigned long long* pieces = nullptr, int Eb = 1) {
+  unsigned long long limb[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};
+  for (int e = 1; e < 255; ++e) add_shifted_576(limb, bins[e], 2 * e - 2);
+  if (pieces)
+    for (int k = 0; k < 4; ++k) add_shifted_576(limb, pieces[k], 32 * k + 2 * Eb - 2);
+  int top = -1;
+  for (int j = 8; j >= 0 && top < 0; --j)
+    if (limb[j]) top = 64 * j + 63 - __clzll(static_cast<long long>(limb[j]));
+  if (top < 0) return 0.0;
+  auto bit = [&](int i) -> unsigned long long { return (limb[i >> 6] >> (i & 63)) & 1ull; };
+  int shift = top > 52 ? top - 52 : 0;
+  unsigned long long M = 0;
+  for (int b = top; b >= shift; --b) M = (M << 1) | bit(b);
+  if (shift > 0) {
+    const unsigned long long half = bit(shift - 1);
+    bool sticky = false;
+    for (int b = shift - 2; b >= 0 && !sticky; --b) sticky = bit(b) != 0;
+    if (half && (sticky || (M & 1ull))) {
+      ++M;
+      if (M == (1ull << 53)) {
+        M >>= 1;
+        ++shift;
+      }
+    }
+  }
+  // M * 2^(shift - 266): M < 2^53 and the exponent stays inside the normal range.
+  return static_cast<double>(M) * __longlong_as_double(static_cast<long long>(1023 + shift - 266) << 52);
+}
+
+}  // namespace
+}  // namespace zc

@@ -170,6 +170,20 @@ def test_auto_base_at_binade_boundaries(k4, rel):
     check_parity(x)
 
 
+@pytest.mark.parametrize("n,k4", [((1 << 20) + 3, -8), (1 << 26, -3)])
+def test_auto_base_at_binade_boundaries_large(n, k4):
+    """Boundary tensors beyond the small-tensor path: the exact sum runs over the whole grid (a
+    follow-on kernel gated by the statistics pass's verdict) and must agree with the oracle."""
+    x = _near_boundary_tensor(k4, n, 200 + k4, 1e-9)
+    st, out, total = gpu_compress(x)
+    assert st == zc.ZC_OK
+    stream = out[:total].cpu().numpy()
+    assert stream[7] == oracle.choose_e0(x)
+    ws = (zc.zc_max_stream_bytes(x.size) + 255) // 256 * 256
+    assert int(out[ws + 12:ws + 16].cpu().numpy().view(np.uint32)[0]) == 1, "the exact fallback did not run"
+    check_parity(x)
+
+
 def test_supplied_base_matches_auto_stream():
     x = mixed(50_000, 4)
     s_auto = check_parity(x, -1)
