@@ -181,10 +181,13 @@ def measured_peaks():
 
 
 def source_sha(kernel: str) -> str:
-    path = os.path.join(ROOT, "lossless_bf16_compression_gb300", "csrc", KERNEL_SOURCES[kernel])
+    """Hash of the kernel's source file and every header of the library (the kernels share code
+    through them), so that profiled counters are used only for the exact source they came from."""
+    csrc = os.path.join(ROOT, "lossless_bf16_compression_gb300", "csrc")
     h = hashlib.sha256()
-    for p in (path, os.path.join(ROOT, "lossless_bf16_compression_gb300", "csrc", "zc_common.cuh")):
-        with open(p, "rb") as f:
+    files = [KERNEL_SOURCES[kernel]] + sorted(f for f in os.listdir(csrc) if f.endswith((".cuh", ".h")))
+    for name in files:
+        with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
