@@ -58,9 +58,9 @@ TARGET_CONFIGS = ["moe_a2a_16384x7168", "adversarial_256m", "sweep_2^26", "sweep
 SWEEP_SIZES = list(range(15, 30))  # 2^15 .. 2^29 values (64 KiB .. 1 GiB)
 SWEEP_REPS = 100
 L2_FLUSH_BYTES = 256 << 20
-KERNEL_NAMES = {1: "stats", 2: "encode", 3: "decode", 4: "raw_form", 5: "small", 6: "exact"}
+KERNEL_NAMES = {1: "stats", 2: "encode", 3: "decode", 4: "raw_form", 5: "small", 6: "decide"}
 KERNEL_SOURCES = {"stats": "zc_stats.cu", "encode": "zc_encode.cu", "decode": "zc_decode.cu",
-                  "raw_form": "zc_encode.cu", "small": "zc_small.cu", "exact": "zc_stats.cu"}
+                  "raw_form": "zc_encode.cu", "small": "zc_small.cu", "decide": "zc_stats.cu"}
 
 
 # ---------------------------------------------------------------------------- ranks
@@ -493,9 +493,14 @@ def run_ours(args, rank, world, local):
         per.setdefault(KERNEL_NAMES.get(kid, str(kid)), []).append(ms)
     avg = {k: sum(v) / len(v) for k, v in per.items()}
     raw_stream = C == 32 + (2 * n + 15) // 16 * 16 and int(cd.out[6].item()) == 0
-    # the raw-form step moves bytes only when the stream comes out raw: it then reads the values
-    # and writes them behind the header
-    alg = {"stats": 2 * n, "encode": 2 * n + C, "decode": C + 2 * n, "raw_form": 4 * n if raw_stream else 0}
+    # A raw stream is written by one of two kernels, each reading the values and writing them
+    # behind the header: the decide kernel's raw pass when the statistics pass predicted it (the
+    # encode kernel then returns at once and moves nothing), else the raw-form step after coding.
+    raw_by = None
+    if raw_stream:
+        raw_by = "decide" if avg.get("decide", 0) > avg.get("raw_form", 0) else "raw_form"
+    alg = {"stats": 2 * n, "encode": 0 if raw_by == "decide" else 2 * n + C, "decode": C + 2 * n,
+           "raw_form": 4 * n if raw_by == "raw_form" else 0, "decide": 4 * n if raw_by == "decide" else 0}
     dominant = max((k for k in avg if alg.get(k)), key=lambda k: avg[k] * len(per[k]))
     achieved = alg[dominant] / (avg[dominant] * 1e-3) / 1e9
     traffic, traffic_from = profiled_traffic(dominant, args.workload)
@@ -623,6 +628,7 @@ def run_ours(args, rank, world, local):
         "kernel_us": {k: round(v * 1e3, 2) for k, v in avg.items()},
         "hbm_frac_by_kernel": {k: round(alg[k] / (avg[k] * 1e-3) / 1e9 / peak, 4) for k in avg if alg.get(k)},
         "stream_form": "raw" if raw_stream else "coded",
+        "raw_written_by": raw_by,
         "roofline": {"bound": "hbm", "kernel": dominant, "achieved": round(achieved, 1), "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "algorithmic_bytes": alg[dominant], "traffic": traffic,

@@ -7,6 +7,7 @@
 // with compute (second technique).
 #pragma once
 
+#include <cstddef>
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -80,14 +81,16 @@ __host__ __device__ inline uint64_t max_coded_bytes(uint64_t n) {
 // ------------------------------------------------------------------ workspace (tail of `out`)
 //
 // [ws + 0,    ws + 256)            Control block
-// [ws + 256,  ws + 256 + 14 KiB)   per-CTA partials of the statistics pass
-// [.., ws + 256 + 16 KiB)          exact fallback: per-exponent sums of sig^2, 256 x u64
+// [ws + 256,  ws + 256 + 12 KiB)   per-CTA partials of the statistics pass
+// [.., ws + 256 + 14 KiB)          exact fallback: per-exponent sums of sig^2, 256 x u64
+// [.., ws + 256 + 16 KiB)          exponent sample of the statistics pass, 256 x u64 counts
 // [ws + 16640, ...)                scan state, one u64 per chunk
-constexpr int kStatsMaxCtas = 896;
+constexpr int kStatsMaxCtas = 768;
 constexpr uint64_t kWsControlBytes = 256;
 constexpr uint64_t kWsExactBinsOffset = kWsControlBytes + 16ull * kStatsMaxCtas;
-constexpr uint64_t kWsPartialsBytes = 16ull * kStatsMaxCtas + 8 * 256;  // partials and exact bins
-static_assert(kWsPartialsBytes == 16384, "the workspace layout is unchanged");
+constexpr uint64_t kWsSampleOffset = kWsExactBinsOffset + 8 * 256;
+constexpr uint64_t kWsPartialsBytes = 16ull * kStatsMaxCtas + 8 * 256 + 8 * 256;  // partials, bins, sample
+static_assert(kWsPartialsBytes == 16384, "the workspace is 16,640 bytes plus 8 per chunk");
 
 struct Control {
   unsigned encode_ticket;   // next chunk to hand out (encoder)
@@ -100,7 +103,15 @@ struct Control {
   unsigned exact_done;      // CTAs of the exact fallback that have finished
   unsigned long long n_finite;  // finite values, for the exact fallback
   unsigned long long exact_pieces[4];  // exact fallback: 32-bit pieces of the window sums
+  unsigned raw_predicted;   // 1: the statistics pass's exponent sample predicts a raw stream
+  unsigned raw_done;        // 1: the raw pass found the coded form longer and wrote the raw form
+  unsigned raw_pass_done;   // CTAs of the raw pass that have finished
+  unsigned long long raw_escape_bytes;  // raw pass: the escape sections' bytes, summed
 };
+static_assert(sizeof(Control) <= kWsControlBytes, "the control block fits its place");
+static_assert(offsetof(Control, exact_path) == 12 && offsetof(Control, raw_predicted) == 80 &&
+                  offsetof(Control, raw_done) == 84,
+              "the tests read these words of the control block at these offsets");
 
 struct StatsPartial {
   double sum;               // fp64 sum of block sums of squares
@@ -290,12 +301,13 @@ constexpr int kChunkThreads = 128;  // threads of a decode CTA, one chunk each
 struct DeviceInfo {
   int sm_count;
   int* status;        // device address of the library's status word on this device
-  int stats_per_sm;   // resident CTAs per SM of the statistics and encode kernels, found once
-  int encode_per_sm;  // per device (host-side launch work stays small for small tensors)
+  int stats_per_sm;   // resident CTAs per SM of the statistics, decide and encode kernels, found
+  int decide_per_sm;  // once per device (host-side launch work stays small for small tensors)
+  int encode_per_sm;
 };
 
 cudaError_t device_info(DeviceInfo* info);  // defined in zc_api.cu
-cudaError_t stats_occupancy(int* per_sm);   // defined in zc_stats.cu
+cudaError_t stats_occupancy(int* stats_per_sm, int* decide_per_sm);  // defined in zc_stats.cu
 cudaError_t encode_occupancy(int* per_sm);  // defined in zc_encode.cu; also sets the kernel's
                                             // dynamic shared memory size, for the current device
 
@@ -310,11 +322,18 @@ void timing_end(TimingRecord& rec, cudaStream_t stream);
 
 // The launches.  `ws` is the call's workspace (workspace_bytes(n) bytes, cleared): the tail of
 // `out` for zc_compress, the library's static array for zc_compress_static_scratch.
-cudaError_t launch_stats(const uint16_t* in, uint64_t n, uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream);
-// After the statistics kernel (auto mode): when its estimate could not settle e0, the exact sum
-// of squares over the whole grid (per-exponent integer sums) decides it; otherwise the kernel
-// returns at once.
-cudaError_t launch_exact(const uint16_t* in, uint64_t n, uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream);
+// predict_raw: also sample the exponents and, when the sample predicts that the coded stream
+// will be longer than the raw form, have the decide kernel take the raw pass.
+cudaError_t launch_stats(const uint16_t* in, uint64_t n, uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream,
+                         bool predict_raw);
+// After the statistics kernel (auto mode), one of: when its estimate could not settle e0, the
+// exact sum of squares over the whole grid (per-exponent integer sums) decides it; when its
+// sample predicted a raw stream, the raw pass counts every chunk's escapes (the coded form's
+// exact length) while it copies the values to their place in the raw form, and keeps the raw
+// form when the coded one is longer (the encode kernel then returns at once); otherwise the
+// kernel returns at once.
+cudaError_t launch_decide(const uint16_t* in, uint64_t n, uint8_t* out, unsigned long long* out_bytes, uint8_t* ws,
+                          const DeviceInfo& dev, cudaStream_t stream);
 cudaError_t launch_encode(const uint16_t* in, uint64_t n, int base, uint8_t* out, unsigned long long* out_bytes,
                           uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream, uint64_t stall_chunk,
                           unsigned spin_limit, uint16_t* loopback_values = nullptr);

@@ -107,6 +107,7 @@ struct __align__(128) EncodeSmem {
   unsigned scan_ready[2][kCoderWarps];
   int scan_bad[2];
   int e0;
+  int skip;       // the raw pass already wrote the stream in the raw form: nothing to code
   unsigned role;  // 0: this CTA scans; otherwise it codes (and, in the loopback, decodes)
   // loopback decoding: the chunk, its escape section and the code-7 count
   unsigned dchunk;
@@ -588,10 +589,21 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     S.q_retired = 0;
     S.freed = 0;
     S.coders_done = 0;
+    S.skip = 0;
   }
   __syncthreads();
   if (S.role == 0) {
-    if (warp < kCoderWarps) scanner(S, p.flags, p.N, p.status, p.spin_limit);
+    if (warp < kCoderWarps) {
+      if (p.base < 0) {  // auto mode: the decide kernel may have written the raw form already
+        if (tid == 0) {
+          asm volatile("griddepcontrol.wait;" ::: "memory");
+          S.skip = static_cast<int>(__ldcg(&p.ctrl->raw_done));
+        }
+        bar_coders();
+        if (S.skip) return;
+      }
+      scanner(S, p.flags, p.N, p.status, p.spin_limit);
+    }
     return;
   }
   // Loopback: kLoopbackDecoders CTAs in every kLoopbackCycle decode from the start; the others
@@ -632,16 +644,18 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     // it, e0 does, so wait for that kernel's completion and writes first.
     if (p.base < 0) asm volatile("griddepcontrol.wait;" ::: "memory");
     S.e0 = p.base >= 0 ? p.base : __ldcg(&p.ctrl->e0);
+    S.skip = p.base >= 0 ? 0 : static_cast<int>(__ldcg(&p.ctrl->raw_done));
   }
   bar_coders();
   const int e0 = S.e0;
+  const bool skip = S.skip != 0;  // the stream is already in the raw form: drain the copies and leave
   const uint32_t kadd = ((256u - static_cast<unsigned>(e0)) << 7) * 0x00010001u;
   const uint64_t R0 = records_base(p.n);
   // This thread's 64 bytes in a stage: logical 16-byte unit q (values v0 + 8q ..) of row tid / 2
   // sits at byte offset sw ^ 16q.
   const unsigned sw = 128 * (tid >> 1) + 16 * ((4 * (tid & 1)) ^ ((tid >> 1) & 7));
 
-  for (unsigned it = 0;; ++it) {
+  for (unsigned it = 0; !skip; ++it) {
     const int s = it % kStages;
     const unsigned c = S.ticket[s];  // set at least one barrier ago
     if (c >= p.N) break;

@@ -124,7 +124,7 @@ __global__ void __launch_bounds__(kSmallThreads) small_kernel(const uint16_t* in
         w[4 * k + 2] = v.z;
         w[4 * k + 3] = v.w;
       }
-      block_sum_with(w, &acc, [&] { return careful_block(w, &nonfinite); });
+      block_sum(w, &acc, &nonfinite);
     }
     unsigned long long nf = nonfinite;
 #pragma unroll

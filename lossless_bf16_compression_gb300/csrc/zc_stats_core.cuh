@@ -9,8 +9,9 @@
 // base whose 7-binade window has the fewest expected escapes under a Gaussian).
 //
 // Every block sum of 64 values carries a relative error below 2^-18 (at most 17 roundings, or 64
-// on the careful path), so a total over blocks lies within 2^-17 of the exact sum; decide_e0 then
-// settles e0 exactly for all but ~4e-5 of random tensors, and the exact fallback decides the rest.
+// for the last n % 8 values, summed one by one), so a total over blocks lies within 2^-17 of the
+// exact sum; decide_e0 then settles e0 exactly for all but ~4e-5 of random tensors, and the exact
+// fallback decides the rest.
 #pragma once
 
 #include "zc_common.cuh"
@@ -40,7 +41,7 @@ __device__ int select_e0(double S, unsigned long long n_f) {
   return e < 0 ? 0 : (e > kE0Max ? kE0Max : e);
 }
 
-// Careful block sum for 64 values (32 words): skips Inf/NaN, and scales every square by
+// Careful block sum for 64 values (32 words), one by one (the last n % 8 values): skips Inf/NaN, and scales every square by
 // 4^-(Emax'-E') relative to the largest exponent present, so no fp32 overflow or underflow
 // matters.  Returns the fp64 value of the block sum and adds the non-finite count.
 __device__ __forceinline__ double careful_block(const uint32_t (&w)[32], unsigned* nonfinite) {
@@ -89,42 +90,24 @@ __device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
   return d;
 }
 
-// A block holding Inf or NaN, reloaded from memory (so that the fast path's registers need not
-// survive the call) and summed by the careful path.
-__device__ __noinline__ double careful_block_at(const uint4* in, uint64_t wb, uint64_t nv, unsigned lane,
-                                                unsigned* nonfinite) {
-  uint32_t w[32];
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const uint64_t idx = wb + 32 * j + lane;
-    const uint4 v = idx < nv ? __ldg(in + idx) : make_uint4(0, 0, 0, 0);
-    w[4 * j] = v.x;
-    w[4 * j + 1] = v.y;
-    w[4 * j + 2] = v.z;
-    w[4 * j + 3] = v.w;
-  }
-  return careful_block(w, nonfinite);
-}
-
-// Block sum of 64 values (this lane's block; `careful` sums a block holding Inf or NaN).  Bit patterns with the sign cleared order like magnitudes, so one
-// packed 16-bit max finds the block's largest, and it decides, per warp, between the plain sum
-// (every lane's largest biased exponent in [87, 187): no square reaches 2^122 and the block sum
-// is at least 2^-80, so the 64 squares, 17 roundings, stay within 2^-19 of the exact sum) and a
-// sum with every lane's values scaled by 2^(126 - Es), Es = E clamped to [1, 252] (1 for lanes
-// that need no scaling), which puts the largest magnitude in [2^-8, 4): no square overflows and
-// what underflows is under 2^-120 of the block sum.  The decision is one warp vote, so a warp runs one of the two loops.
-// Blocks holding Inf or NaN take the careful path.
-template <typename Careful>
-__device__ __forceinline__ void block_sum_with(const uint32_t (&w)[32], double* acc, Careful careful) {
+// Block sum of 64 values (this lane's block, 32 words; `w` is consumed).  Bit patterns with the
+// sign cleared order like magnitudes, so one packed 16-bit max finds the block's largest, and it
+// decides, per warp, between the plain sum (every lane's largest biased exponent in [87, 187): no
+// square reaches 2^122 and the block sum is at least 2^-80, so the 64 squares, 17 roundings, stay
+// within 2^-19 of the exact sum) and a sum with every lane's values scaled by 2^(126 - Es), Es = E
+// clamped to [1, 252] (1 for lanes that need no scaling), which puts the largest magnitude in
+// [2^-8, 4): no square overflows and what underflows is under 2^-120 of the block sum.  The
+// decision is one warp vote, so a warp runs one of the two loops.  A lane whose block holds Inf
+// or NaN (its largest pattern is at or above 0x7F80) first counts them and clears them to zero,
+// which adds nothing to the sum, and takes the largest of the rest; its warp then sums scaled.
+__device__ __forceinline__ void block_sum(uint32_t (&w)[32], double* acc, unsigned* nonfinite) {
   uint32_t mx = 0;
 #pragma unroll
   for (int i = 0; i < 32; ++i) mx = max_u16x2(mx, w[i] & 0x7FFF7FFFu);
-  const unsigned m = max(mx & 0xFFFFu, mx >> 16);
-  const unsigned E = m >> 7;
-  const bool nonfin = m >= 0x7F80u;
-  const bool odd = m != 0 && (E >= 187u || E < 87u);
+  unsigned m = max(mx & 0xFFFFu, mx >> 16);
+  bool odd = m != 0 && (m >> 7 >= 187u || m >> 7 < 87u);  // Inf and NaN included (E = 255)
   float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-  if (!__any_sync(0xFFFFFFFFu, nonfin || odd)) {
+  if (!__any_sync(0xFFFFFFFFu, odd)) {
 #pragma unroll
     for (int i = 0; i < 32; i += 2) {
       const float l0 = __uint_as_float(w[i] << 16), h0 = __uint_as_float(w[i] & 0xFFFF0000u);
@@ -137,11 +120,23 @@ __device__ __forceinline__ void block_sum_with(const uint32_t (&w)[32], double* 
     *acc += static_cast<double>((a0 + a1) + (a2 + a3));
     return;
   }
-  if (nonfin) {
-    *acc += careful();
-    return;
+  if (m >= 0x7F80u) {
+    // A 16-bit magnitude a is at or above 0x7F80 exactly when a + 0x80 reaches bit 15 (a <= 0x7FFF,
+    // so nothing carries into the other half).
+    unsigned nf = 0;
+    mx = 0;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const uint32_t t = ((w[i] & 0x7FFF7FFFu) + 0x00800080u) & 0x80008000u;  // bit 15 of each non-finite half
+      nf += __popc(t);
+      w[i] &= ~(t | (t - (t >> 15)));  // clear those halves
+      mx = max_u16x2(mx, w[i] & 0x7FFF7FFFu);
+    }
+    *nonfinite += nf;
+    m = max(mx & 0xFFFFu, mx >> 16);
+    odd = m != 0 && (m >> 7 >= 187u || m >> 7 < 87u);
   }
-  const int Es = odd ? min(max(static_cast<int>(E), 1), 252) : 126;
+  const int Es = odd ? min(max(static_cast<int>(m >> 7), 1), 252) : 126;
   const float sc = __int_as_float((253 - Es) << 23);
 #pragma unroll
   for (int i = 0; i < 32; i += 2) {
@@ -154,12 +149,6 @@ __device__ __forceinline__ void block_sum_with(const uint32_t (&w)[32], double* 
   }
   const float blk = (a0 + a1) + (a2 + a3);
   *acc += static_cast<double>(blk) * __longlong_as_double(static_cast<long long>(1023 + 2 * Es - 252) << 52);
-}
-
-// The same for the statistics kernel, whose careful path reloads the block from memory.
-__device__ __forceinline__ void block_sum(const uint32_t (&w)[32], const uint4* in, uint64_t wb, uint64_t nv,
-                                          unsigned lane, double* acc, unsigned* nonfinite) {
-  block_sum_with(w, acc, [&] { return careful_block_at(in, wb, nv, lane, nonfinite); });
 }
 
 // The window rule at an fp64 estimate S_est of the sum of squares that lies within 2^-17 of the

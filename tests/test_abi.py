@@ -33,6 +33,20 @@ def test_every_declared_symbol_is_exported(lib):
     assert sorted(zc.exported_symbols()) == names
 
 
+def test_binding_constants_match_the_header():
+    """Every numeric #define of include/zc.h that the binding names has the header's value."""
+    text = re.sub(r"/\*.*?\*/", "", open(os.path.join(ROOT, "include", "zc.h")).read(), flags=re.S)
+    defines = {k: int(v, 0) for k, v in re.findall(r"^#define\s+(ZC_\w+)\s+\(?(-?\w+)\)?\s*$", text, flags=re.M)
+               if re.fullmatch(r"-?(0x[0-9a-fA-F]+|\d+)[uUlL]*", v) and not v.endswith(("u", "U", "l", "L"))}
+    assert {"ZC_OK", "ZC_ERR_TIMEOUT", "ZC_KERNEL_DECIDE", "ZC_BASE_AUTO"} <= set(defines)
+    for name, value in defines.items():
+        if hasattr(zc, name):
+            assert getattr(zc, name) == value, name
+    for name in ("ZC_KERNEL_STATS", "ZC_KERNEL_ENCODE", "ZC_KERNEL_DECODE", "ZC_KERNEL_RAW", "ZC_KERNEL_SMALL",
+                 "ZC_KERNEL_DECIDE"):
+        assert getattr(zc, name) == defines[name]
+
+
 def _pad16(v):
     return (v + 15) // 16 * 16
 

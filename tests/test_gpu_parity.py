@@ -133,6 +133,21 @@ def test_special_tensors():
     check_parity(workloads.random_patterns(70_000, 5))
 
 
+@pytest.mark.parametrize("case", ["mixed_1pct", "nan_every_64th", "all_patterns_x4"])
+def test_nonfinite_blocks_beyond_the_small_path(case):
+    """Blocks of 64 values holding Inf or NaN clear and count them inside the vectorized sum (the
+    statistics kernel of the multi-launch path): e0 and the stream must still equal the oracle's."""
+    if case == "mixed_1pct":
+        x = mixed(2_000_003, 41, sigma=1.0, frac=0.01)
+    elif case == "nan_every_64th":
+        x = workloads.sweep(21).copy()
+        x[::64] = 0x7FC1
+        x[5::4096] = 0xFF80  # -Inf
+    else:
+        x = np.concatenate([np.tile(workloads.all_patterns(), 4), workloads.all_patterns()[:1234]])
+    check_parity(x)
+
+
 def _near_boundary_tensor(k4, n, seed, rel):
     """A tensor whose sum of squares is within ~1e-15 of (1 + rel) 4**k4 n / c^2, i.e. whose
     mean square times c^2 sits `rel` away from a switching point of the window rule."""
