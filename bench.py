@@ -58,9 +58,9 @@ TARGET_CONFIGS = ["moe_a2a_16384x7168", "adversarial_256m", "sweep_2^26", "sweep
 SWEEP_SIZES = list(range(15, 30))  # 2^15 .. 2^29 values (64 KiB .. 1 GiB)
 SWEEP_REPS = 100
 L2_FLUSH_BYTES = 256 << 20
-KERNEL_NAMES = {1: "stats", 2: "encode", 3: "decode", 4: "raw_form", 5: "small", 6: "decide"}
+KERNEL_NAMES = {1: "stats", 2: "encode", 3: "decode", 4: "raw_form", 5: "small"}
 KERNEL_SOURCES = {"stats": "zc_stats.cu", "encode": "zc_encode.cu", "decode": "zc_decode.cu",
-                  "raw_form": "zc_encode.cu", "small": "zc_small.cu", "decide": "zc_stats.cu"}
+                  "raw_form": "zc_encode.cu", "small": "zc_small.cu"}
 
 
 # ---------------------------------------------------------------------------- ranks
@@ -493,14 +493,15 @@ def run_ours(args, rank, world, local):
         per.setdefault(KERNEL_NAMES.get(kid, str(kid)), []).append(ms)
     avg = {k: sum(v) / len(v) for k, v in per.items()}
     raw_stream = C == 32 + (2 * n + 15) // 16 * 16 and int(cd.out[6].item()) == 0
-    # A raw stream is written by one of two kernels, each reading the values and writing them
-    # behind the header: the decide kernel's raw pass when the statistics pass predicted it (the
-    # encode kernel then returns at once and moves nothing), else the raw-form step after coding.
-    raw_by = None
-    if raw_stream:
-        raw_by = "decide" if avg.get("decide", 0) > avg.get("raw_form", 0) else "raw_form"
-    alg = {"stats": 2 * n, "encode": 0 if raw_by == "decide" else 2 * n + C, "decode": C + 2 * n,
-           "raw_form": 4 * n if raw_by == "raw_form" else 0, "decide": 4 * n if raw_by == "decide" else 0}
+    # A raw stream is written by one of two steps, each reading the values and writing them
+    # behind the header: the encode kernel's raw pass when the statistics pass predicted it
+    # (nothing is coded then; the control block at the head of the workspace says so), else the
+    # raw-form step after coding.
+    ws = (zc.zc_max_stream_bytes(n) + 255) // 256 * 256
+    raw_pass = raw_stream and int(cd.out[ws + 84:ws + 88].cpu().numpy().view(np.uint32)[0]) == 1
+    raw_by = ("encode (raw pass)" if raw_pass else "raw_form") if raw_stream else None
+    alg = {"stats": 2 * n, "encode": 4 * n if raw_pass else 2 * n + C, "decode": C + 2 * n,
+           "raw_form": 4 * n if raw_stream and not raw_pass else 0}
     dominant = max((k for k in avg if alg.get(k)), key=lambda k: avg[k] * len(per[k]))
     achieved = alg[dominant] / (avg[dominant] * 1e-3) / 1e9
     traffic, traffic_from = profiled_traffic(dominant, args.workload)

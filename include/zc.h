@@ -96,9 +96,12 @@ size_t zc_max_stream_bytes(size_t n);
  *                 (input bits, e0): both modes give identical bytes for the same e0.
  *   out           device, zc_max_compressed_bytes(n) bytes, 16-byte aligned, must not overlap
  *                 `in`.  The stream is written from out[0]: the coded form, or the raw form
- *                 when that is shorter (decided on the device after the scan, so no host
- *                 synchronization); the bytes past *out_bytes, including the workspace tail,
- *                 are unspecified afterwards.  The library keeps
+ *                 when that is shorter.  The form is decided on the device from the coded
+ *                 form's exact length, with no host synchronization: after the encoder's scan,
+ *                 or, in auto mode when an exponent sample of the statistics pass predicts a
+ *                 raw stream, by a pass that counts every chunk's escapes while it copies the
+ *                 values to the raw form (the encoder then has nothing to do).  The bytes past
+ *                 *out_bytes, including the workspace tail, are unspecified afterwards.  The library keeps
  *                 no per-call state outside `out`, so calls on different streams with
  *                 different buffers may run concurrently.  The encode kernel's CTAs wait on
  *                 one another (bounded) only for work that a CTA already running has taken,
@@ -175,8 +178,6 @@ int zc_status(cudaStream_t stream, int reset);
 #define ZC_KERNEL_DECODE 3
 #define ZC_KERNEL_RAW 4    /* the step that rewrites a stream in the raw form when that is shorter */
 #define ZC_KERNEL_SMALL 5  /* the single launch that compresses a tensor of up to 32 chunks */
-#define ZC_KERNEL_DECIDE 6 /* after the statistics pass: the exact sum of squares when that pass cannot
-                              settle e0, or the raw pass when its exponent sample predicts a raw stream */
 
 /* enable != 0: bracket every kernel the library launches from now on with CUDA events on the
  * kernel's own stream.  enable == 0: stop recording.  Returns ZC_OK or ZC_ERR_CUDA. */

@@ -64,7 +64,7 @@ cudaError_t device_info(DeviceInfo* info) {
     if (err != cudaSuccess) return err;
     err = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status), g_status);
     if (err != cudaSuccess) return err;
-    err = stats_occupancy(&d.stats_per_sm, &d.decide_per_sm);
+    err = stats_occupancy(&d.stats_per_sm);
     if (err != cudaSuccess) return err;
     err = encode_occupancy(&d.encode_per_sm);
     if (err != cudaSuccess) return err;
@@ -172,7 +172,6 @@ int compress_impl(const void* in, size_t n, int base, void* out, size_t* out_byt
     // the raw pass.
     const bool predict_raw = !loopback && stall_chunk == ~uint64_t(0);
     if (launch_stats(x, n, ws, dev, stream, predict_raw) != cudaSuccess) return ZC_ERR_CUDA;
-    if (launch_decide(x, n, o, len_ptr, ws, dev, stream) != cudaSuccess) return ZC_ERR_CUDA;
   }
   if (launch_encode(x, n, base, o, len_ptr, ws, dev, stream, stall_chunk, spin_limit,
                     static_cast<uint16_t*>(values)) != cudaSuccess)

@@ -100,12 +100,13 @@ struct Control {
   unsigned long long total; // stream length, for the pageable out_bytes path
   unsigned role_ticket;     // encoder CTAs in start order: the first one to start scans
   unsigned decode_ticket;   // loopback: next chunk to decode
-  unsigned exact_done;      // CTAs of the exact fallback that have finished
+  unsigned first_ticket;    // the encoder's first phase: next chunk to take
   unsigned long long n_finite;  // finite values, for the exact fallback
   unsigned long long exact_pieces[4];  // exact fallback: 32-bit pieces of the window sums
   unsigned raw_predicted;   // 1: the statistics pass's exponent sample predicts a raw stream
   unsigned raw_done;        // 1: the raw pass found the coded form longer and wrote the raw form
-  unsigned raw_pass_done;   // CTAs of the raw pass that have finished
+  unsigned first_done;      // the encoder's first phase: chunks finished
+  unsigned first_ready;     // the encoder's first phase: e0 and the stream form are final
   unsigned long long raw_escape_bytes;  // raw pass: the escape sections' bytes, summed
 };
 static_assert(sizeof(Control) <= kWsControlBytes, "the control block fits its place");
@@ -213,6 +214,14 @@ __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long
 __device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
   asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_u32(unsigned* p, unsigned v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 
 // Packed 16-bit lane arithmetic (two BF16 values per 32-bit word).
 __device__ __forceinline__ uint32_t add_u16x2(uint32_t a, uint32_t b) {
@@ -301,13 +310,12 @@ constexpr int kChunkThreads = 128;  // threads of a decode CTA, one chunk each
 struct DeviceInfo {
   int sm_count;
   int* status;        // device address of the library's status word on this device
-  int stats_per_sm;   // resident CTAs per SM of the statistics, decide and encode kernels, found
-  int decide_per_sm;  // once per device (host-side launch work stays small for small tensors)
-  int encode_per_sm;
+  int stats_per_sm;   // resident CTAs per SM of the statistics and encode kernels, found once
+  int encode_per_sm;  // per device (host-side launch work stays small for small tensors)
 };
 
 cudaError_t device_info(DeviceInfo* info);  // defined in zc_api.cu
-cudaError_t stats_occupancy(int* stats_per_sm, int* decide_per_sm);  // defined in zc_stats.cu
+cudaError_t stats_occupancy(int* per_sm);   // defined in zc_stats.cu
 cudaError_t encode_occupancy(int* per_sm);  // defined in zc_encode.cu; also sets the kernel's
                                             // dynamic shared memory size, for the current device
 
@@ -323,17 +331,9 @@ void timing_end(TimingRecord& rec, cudaStream_t stream);
 // The launches.  `ws` is the call's workspace (workspace_bytes(n) bytes, cleared): the tail of
 // `out` for zc_compress, the library's static array for zc_compress_static_scratch.
 // predict_raw: also sample the exponents and, when the sample predicts that the coded stream
-// will be longer than the raw form, have the decide kernel take the raw pass.
+// will be longer than the raw form, have the encode kernel take the raw pass first.
 cudaError_t launch_stats(const uint16_t* in, uint64_t n, uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream,
                          bool predict_raw);
-// After the statistics kernel (auto mode), one of: when its estimate could not settle e0, the
-// exact sum of squares over the whole grid (per-exponent integer sums) decides it; when its
-// sample predicted a raw stream, the raw pass counts every chunk's escapes (the coded form's
-// exact length) while it copies the values to their place in the raw form, and keeps the raw
-// form when the coded one is longer (the encode kernel then returns at once); otherwise the
-// kernel returns at once.
-cudaError_t launch_decide(const uint16_t* in, uint64_t n, uint8_t* out, unsigned long long* out_bytes, uint8_t* ws,
-                          const DeviceInfo& dev, cudaStream_t stream);
 cudaError_t launch_encode(const uint16_t* in, uint64_t n, int base, uint8_t* out, unsigned long long* out_bytes,
                           uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream, uint64_t stall_chunk,
                           unsigned spin_limit, uint16_t* loopback_values = nullptr);

@@ -39,6 +39,7 @@
 #include "zc_common.cuh"
 #include "zc_decode_core.cuh"
 #include "zc_ring.h"
+#include "zc_stats_core.cuh"
 
 namespace zc {
 namespace {
@@ -107,7 +108,10 @@ struct __align__(128) EncodeSmem {
   unsigned scan_ready[2][kCoderWarps];
   int scan_bad[2];
   int e0;
-  int skip;       // the raw pass already wrote the stream in the raw form: nothing to code
+  int skip;       // nothing to code: the raw pass wrote the stream, or the first phase failed
+  int kind;       // the first phase's job: 0 none, 1 the exact e0, 2 the raw pass
+  int first_ok;   // the first phase ended with its result published
+  int first_last; // this CTA finished the first phase's last chunk
   unsigned role;  // 0: this CTA scans; otherwise it codes (and, in the loopback, decodes)
   // loopback decoding: the chunk, its escape section and the code-7 count
   unsigned dchunk;
@@ -390,6 +394,242 @@ __device__ __noinline__ void write_plane(const uint4* stage, unsigned sw, uint32
   }
 }
 
+// ------------------------------------------------------------------ the first phase
+//
+// In auto mode the statistics pass may leave one of two jobs, done here before any chunk is
+// coded.  Their chunks are handed out by a ticket of their own, a batch of four to a warp; each
+// CTA adds its results and the number of chunks it finished to the control block, and the CTA
+// whose count completes N finishes the job and publishes it (first_ready, a release store); the
+// others wait for that, bounded.  A CTA waits only on chunks that a running CTA has taken, so the phase needs
+// no CTA to be resident at any particular time.
+//  - Exact e0 (kind 1), when the statistics pass's estimate could not settle it: every thread sums
+//    sig^2 4^d exactly in a 128-bit integer over a 24-binade window from Eb (around the typical
+//    value, anchored on the estimate's e0; a term is below 2^62, so 2^66 of them fit); values
+//    outside the window add sig^2 to their exponent's bin in shared memory.  The finisher rounds
+//    the 576-bit total of the grid's bins and window sums once to fp64 and picks e0
+//    (exact_from_bins, select_e0).
+//  - Raw pass (kind 2), when the statistics pass's exponent sample predicted a raw stream (the
+//    third technique: the native path when coding does not pay): every value is copied to its
+//    place in the raw form and every chunk's escapes are counted under e0 exactly as the coding
+//    counts them, giving its escape section's size.  The finisher compares the coded form's
+//    exact length with the raw form's; when the coded one is longer it completes the raw form
+//    (header, length) and marks the stream done, so nothing is coded.  Otherwise (ties included)
+//    the coding writes the coded form over the copy.
+constexpr int kExactWindow = 24;
+constexpr int kFirstVecPerLane = kChunk / 8 / 32;  // 16 vectors of a chunk per lane
+constexpr unsigned kFirstBatch = 4;                // chunks a warp takes per ticket
+
+// Ask for `bytes` (a multiple of 16) at a 16-byte aligned global address to be brought into L2.
+__device__ __forceinline__ void prefetch_l2(const void* p, unsigned bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// Escapes among the two values of w outside `keep`'s cleared halves (codes7_x2 gives exactly
+// 7 << 7 for an escape, and 7 << 7 + 0x80 reaches bit 10).
+__device__ __forceinline__ unsigned escapes_x2(uint32_t w, uint32_t kadd, uint32_t keep = 0xFFFFFFFFu) {
+  return __popc(((codes7_x2(w, kadd) & keep) + 0x00800080u) & 0x04000400u);
+}
+
+// Raw pass, one warp: chunk c's values copied behind the 32-byte header (the last vector of the
+// stream completed with zeros); returns the chunk's escape-section bytes in every lane.
+__device__ unsigned raw_chunk(const uint16_t* x, uint64_t n, uint64_t c, uint32_t kadd, uint8_t* out) {
+  const unsigned lane = threadIdx.x & 31;
+  const uint4* src = reinterpret_cast<const uint4*>(x);
+  uint4* dst = reinterpret_cast<uint4*>(out + kHeaderBytes);
+  const uint64_t nv = n / 8;
+  unsigned esc = 0, m = kChunk;
+  if (c < n / kChunk) {
+#pragma unroll 1
+    for (int h = 0; h < 2; ++h) {  // two halves of 8 vectors per lane
+      const uint64_t b = c * (kChunk / 8) + 32 * (kFirstVecPerLane / 2) * h + lane;
+      uint4 v[kFirstVecPerLane / 2];
+#pragma unroll
+      for (int j = 0; j < kFirstVecPerLane / 2; ++j) v[j] = __ldcs(src + b + 32 * j);
+#pragma unroll
+      for (int j = 0; j < kFirstVecPerLane / 2; ++j) {
+        __stcs(dst + b + 32 * j, v[j]);
+        esc += escapes_x2(v[j].x, kadd) + escapes_x2(v[j].y, kadd) + escapes_x2(v[j].z, kadd) +
+               escapes_x2(v[j].w, kadd);
+      }
+    }
+  } else {  // the ragged last chunk: its m values
+    m = static_cast<unsigned>(n - c * kChunk);
+    for (unsigned i = lane; i < (m + 7) / 8; i += 32) {
+      const uint64_t g = c * (kChunk / 8) + i;
+      uint32_t w[4];
+      if (g < nv) {
+        const uint4 t = __ldcs(src + g);
+        w[0] = t.x, w[1] = t.y, w[2] = t.z, w[3] = t.w;
+      } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint64_t v = 8 * g + 2 * q;
+          w[q] = (v < n ? static_cast<uint32_t>(x[v]) : 0u) | (v + 1 < n ? static_cast<uint32_t>(x[v + 1]) << 16 : 0u);
+        }
+      }
+      __stcs(dst + g, make_uint4(w[0], w[1], w[2], w[3]));
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const unsigned v = 8 * i + 2 * q;
+        esc += escapes_x2(w[q], kadd, (v < m ? 0x0000FFFFu : 0u) | (v + 1 < m ? 0xFFFF0000u : 0u));
+      }
+    }
+  }
+  const unsigned k = __reduce_add_sync(0xFFFFFFFFu, esc);
+  return 3 * k <= m ? static_cast<unsigned>(pad16(3 * k)) : static_cast<unsigned>(pad16(m));
+}
+
+// Exact sums, one warp: chunk c's values (zeros past n add nothing).
+__device__ void exact_chunk(const uint16_t* x, uint64_t n, uint64_t c, int Eb, unsigned long long& lo,
+                            unsigned long long& hi, unsigned long long* bins) {
+  const unsigned lane = threadIdx.x & 31;
+  auto add = [&](unsigned b) {
+    const unsigned E = (b >> 7) & 0xFF;
+    if (E == 255 || (b & 0x7FFF) == 0) return;
+    const unsigned Ep = E ? E : 1, sig = E ? 128 + (b & 0x7F) : (b & 0x7F);
+    const unsigned d = Ep - static_cast<unsigned>(Eb);
+    if (d < static_cast<unsigned>(kExactWindow)) {
+      const unsigned long long t = static_cast<unsigned long long>(sig * sig) << (2 * d);
+      lo += t;
+      hi += lo < t;
+    } else {
+      atomicAdd(bins + Ep, static_cast<unsigned long long>(sig * sig));
+    }
+  };
+  const uint4* src = reinterpret_cast<const uint4*>(x);
+  const uint64_t nv = n / 8, first = c * (kChunk / 8);
+  const uint64_t end = first + kChunk / 8 < nv ? first + kChunk / 8 : nv;  // whole vectors of the chunk
+  constexpr int kUnroll = 4;
+  for (uint64_t g = first + lane; g < end; g += 32 * kUnroll) {
+    uint4 v[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) v[u] = g + 32 * u < end ? __ldcs(src + g + 32 * u) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+      for (int j = 0; j < 8; ++j) add((w[j >> 1] >> (16 * (j & 1))) & 0xFFFFu);
+    }
+  }
+  if (c == (n - 1) / kChunk && lane < n % 8) add(x[8 * nv + lane]);  // the last n % 8 values
+}
+
+// Bounded wait (one thread) for the first phase's result.  False after an error or a timeout.
+__device__ bool wait_first_ready(Control* ctrl, int* status, unsigned spin_limit) {
+  unsigned spins = 0, backoff = 64;
+  while (ld_acquire_u32(&ctrl->first_ready) == 0) {
+    if (read_status(status) != 0) return false;
+    if (++spins > spin_limit) {
+      set_error(status, ZC_ERR_TIMEOUT);
+      return false;
+    }
+    __nanosleep(backoff);
+    backoff = backoff < 512 ? backoff * 2 : 512;
+  }
+  return true;
+}
+
+// The first phase, by the 128 coding threads of a CTA.  Returns (in every thread) whether the
+// result is published; e0 and the stream form are then final in the control block.
+__device__ __noinline__ bool first_phase(EncodeSmem& S, const uint16_t* x, uint64_t n, uint64_t N, uint8_t* out,
+                                         unsigned long long* out_bytes, Control* ctrl, unsigned long long* gbins,
+                                         int* status, unsigned spin_limit, int kind) {
+  const unsigned tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  unsigned long long* bins = reinterpret_cast<unsigned long long*>(S.ring);  // exact: this CTA's bins
+  unsigned long long* pieces = S.scan_sum[1];                               // exact: its window sums
+  if (kind == 1) {
+    for (unsigned i = tid; i < 256; i += kCoders) bins[i] = 0;
+    if (tid < 4) pieces[tid] = 0;
+  }
+  bar_coders();
+  const int e0 = __ldcg(&ctrl->e0);
+  const uint32_t kadd = ((256u - static_cast<unsigned>(e0)) << 7) * 0x00010001u;
+  int Eb = e0 - 12;  // e0 + 5 is about the typical exponent of a Gaussian tensor
+  Eb = Eb < 1 ? 1 : (Eb > 254 - kExactWindow ? 254 - kExactWindow : Eb);
+  unsigned long long lo = 0, hi = 0, bytes = 0;
+  unsigned mine = 0;  // chunks this warp finished
+  for (;;) {
+    // A batch of chunks per ticket (fewer atomics on the one counter), brought into L2 at once
+    // (the whole chunks: one bulk prefetch each), then read from there.
+    unsigned c0 = 0;
+    if (lane == 0) c0 = atomicAdd(&ctrl->first_ticket, kFirstBatch);
+    c0 = __shfl_sync(0xFFFFFFFFu, c0, 0);
+    if (c0 >= N) break;
+    const unsigned cend = c0 + kFirstBatch < N ? c0 + kFirstBatch : static_cast<unsigned>(N);
+    if (lane < cend - c0 && c0 + lane < n / kChunk) prefetch_l2(x + static_cast<uint64_t>(c0 + lane) * kChunk, 2 * kChunk);
+    for (unsigned c = c0; c < cend; ++c) {
+      if (kind == 2)
+        bytes += raw_chunk(x, n, c, kadd, out);
+      else
+        exact_chunk(x, n, c, Eb, lo, hi, bins);
+      ++mine;
+    }
+  }
+  if (kind == 1) {  // the window sums in 32-bit pieces, over the warp, then the CTA
+    unsigned long long pc[4] = {lo & 0xFFFFFFFFull, lo >> 32, hi & 0xFFFFFFFFull, hi >> 32};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) pc[k] += __shfl_xor_sync(0xFFFFFFFFu, pc[k], o);
+      if (lane == 0 && pc[k]) atomicAdd(pieces + k, pc[k]);
+    }
+  }
+  if (lane == 0) {
+    S.scan_sum[0][warp] = bytes;
+    S.scan_ready[0][warp] = mine;
+  }
+  bar_coders();
+  // The CTA's results into the grid's, each thread's made visible (fence) before the CTA reports
+  // its chunks; the report that completes N makes this CTA the finisher.
+  if (kind == 1) {
+    for (unsigned i = tid; i < 256; i += kCoders)
+      if (bins[i]) atomicAdd(gbins + i, bins[i]);
+    if (tid < 4 && pieces[tid]) atomicAdd(&ctrl->exact_pieces[tid], pieces[tid]);
+  } else if (tid == 0) {
+    unsigned long long sum = 0;
+    for (int w = 0; w < kCoderWarps; ++w) sum += S.scan_sum[0][w];
+    if (sum) atomicAdd(&ctrl->raw_escape_bytes, sum);
+  }
+  __threadfence();
+  bar_coders();
+  if (tid == 0) {
+    unsigned count = 0;
+    for (int w = 0; w < kCoderWarps; ++w) count += S.scan_ready[0][w];
+    S.first_last = count != 0 && atomicAdd(&ctrl->first_done, count) == N - count;
+    if (S.first_last) __threadfence();  // acquire: every CTA's results are visible from here on
+  }
+  bar_coders();
+  if (S.first_last) {
+    if (kind == 1) {
+      for (unsigned i = tid; i < 256; i += kCoders) bins[i] = __ldcg(gbins + i);
+      if (tid < 4) pieces[tid] = __ldcg(&ctrl->exact_pieces[tid]);
+      bar_coders();
+      if (tid == 0) ctrl->e0 = select_e0(exact_from_bins(bins, pieces, Eb), __ldcg(&ctrl->n_finite));
+    } else if (tid == 0) {
+      const unsigned long long coded = escape_base(n) + __ldcg(&ctrl->raw_escape_bytes), raw = raw_stream_bytes(n);
+      if (coded > raw) {
+        unsigned long long* hdr = reinterpret_cast<unsigned long long*>(out);
+        hdr[0] = kRawMagicWord | (static_cast<unsigned long long>(e0) << 56);
+        hdr[1] = n;
+        hdr[2] = 0;
+        hdr[3] = raw;
+        ctrl->total = raw;
+        if (out_bytes) *out_bytes = raw;
+        ctrl->raw_done = 1;
+      }
+    }
+    if (tid == 0) {
+      __threadfence();
+      st_release_u32(&ctrl->first_ready, 1u);
+      S.first_ok = 1;
+    }
+  } else if (tid == 0) {
+    S.first_ok = wait_first_ready(ctrl, status, spin_limit) ? 1 : 0;
+  }
+  bar_coders();
+  return S.first_ok != 0;
+}
+
 __device__ __forceinline__ bool bar_coders_or(bool v) {
   unsigned r;
   asm volatile(
@@ -399,6 +639,24 @@ __device__ __forceinline__ bool bar_coders_or(bool v) {
       : "r"(static_cast<unsigned>(v)), "n"(kCoders)
       : "memory");
   return r != 0;
+}
+
+// The escape section of a chunk marked copied (state word f, read before an acquire fence): its
+// offset from the offset table (written by the same retiring lane before its fence and the mark,
+// so visible after the acquire; the state word of the chunk before it comes from another lane of
+// the scanner and may not be), its end from f.  Every size is checked before anything is read by
+// it: a section that does not fit its place sets ZC_ERR_CORRUPT and returns false.
+__device__ bool copied_section(const uint8_t* stream, int* status, uint64_t E0, unsigned d, unsigned long long f,
+                               unsigned long long* off, unsigned* size) {
+  const unsigned long long end = E0 + (f & kFlagValueMask);
+  const unsigned long long o = __ldcg(reinterpret_cast<const unsigned long long*>(stream + kHeaderBytes) + d);
+  if (o < E0 || o > end || end - o > kMaxEscapeBytes || ((end - o) & 15u) != 0) {
+    set_error(status, ZC_ERR_CORRUPT);
+    return false;
+  }
+  *off = o;
+  *size = static_cast<unsigned>(end - o);
+  return true;
 }
 
 // Loopback, the 128 coding threads of a CTA: decode chunks in ticket order as their escape
@@ -442,11 +700,12 @@ __device__ __noinline__ void loopback_decode(EncodeSmem& S, const uint8_t* strea
           backoff = backoff < 512 ? backoff * 2 : 512;
         }
         if (ok) {
-          // chunk d - 1 is resolved (the scan runs in order): its value ends the sections before d
-          const unsigned long long prev = d ? (ld_relaxed_u64(&p.flags[d - 1]) & kFlagValueMask) : 0ull;
-          __threadfence();  // acquire: the chunk's bytes are visible from here on
-          S.doff = E0 + prev;
-          S.dsize = static_cast<unsigned>((f & kFlagValueMask) - prev);
+          __threadfence();  // acquire: the chunk's bytes and its offset are visible from here on
+          unsigned long long off = 0;
+          unsigned size = 0;
+          ok = copied_section(p.stream, p.status, E0, d, f, &off, &size);
+          S.doff = off;
+          S.dsize = size;
         }
       }
       S.dchunk = d;
@@ -486,12 +745,8 @@ __device__ bool claim_decode(const LoopbackArgs& p, uint64_t E0, unsigned* d, un
     __nanosleep(backoff);
     backoff = backoff < 512 ? backoff * 2 : 512;
   }
-  // chunk d - 1 is resolved (the scan runs in order): its value ends the sections before d
-  const unsigned long long prev = *d ? (ld_relaxed_u64(&p.flags[*d - 1]) & kFlagValueMask) : 0ull;
-  __threadfence();
-  *off = E0 + prev;
-  *size = static_cast<unsigned>((f & kFlagValueMask) - prev);
-  return true;
+  __threadfence();  // acquire: the chunk's bytes and its offset are visible from here on
+  return copied_section(p.stream, p.status, E0, *d, f, off, size);
 }
 
 // Loopback, a CTA that only decodes: two slots, each a chunk's fixed part (in an input stage) and
@@ -594,10 +849,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   __syncthreads();
   if (S.role == 0) {
     if (warp < kCoderWarps) {
-      if (p.base < 0) {  // auto mode: the decide kernel may have written the raw form already
+      if (p.base < 0) {  // auto mode: wait for the first phase, if there is one (it may leave the raw form)
         if (tid == 0) {
           asm volatile("griddepcontrol.wait;" ::: "memory");
-          S.skip = static_cast<int>(__ldcg(&p.ctrl->raw_done));
+          bool ok = true;
+          if (__ldcg(&p.ctrl->exact_path) != 0 || __ldcg(&p.ctrl->raw_predicted) != 0)
+            ok = wait_first_ready(p.ctrl, p.status, p.spin_limit);
+          S.skip = !ok || __ldcg(&p.ctrl->raw_done) != 0;
         }
         bar_coders();
         if (S.skip) return;
@@ -613,11 +871,18 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     if (!decode_only) retirer(S, p);
     return;
   }
-  if (decode_only) {
+  if (decode_only) {  // (the loopback never takes the raw pass; the exact e0 it may need)
     if (tid == 0) {
       if (p.base < 0) asm volatile("griddepcontrol.wait;" ::: "memory");
-      S.e0 = p.base >= 0 ? p.base : __ldcg(&p.ctrl->e0);
+      S.kind = p.base < 0 && __ldcg(&p.ctrl->exact_path) != 0 ? 1 : 0;
     }
+    bar_coders();
+    if (S.kind &&
+        !first_phase(S, p.in, p.n, p.N, p.out, p.out_bytes, p.ctrl,
+                     reinterpret_cast<unsigned long long*>(reinterpret_cast<uint8_t*>(p.ctrl) + kWsExactBinsOffset),
+                     p.status, p.spin_limit, S.kind))
+      return;
+    if (tid == 0) S.e0 = p.base >= 0 ? p.base : __ldcg(&p.ctrl->e0);
     bar_coders();
     loopback_decode_only(S, p.out, p.values, p.flags, p.ctrl, p.status, p.n, p.N, p.spin_limit);
     return;
@@ -643,12 +908,24 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     // (a programmatic dependent launch): the tickets and input copies above do not depend on
     // it, e0 does, so wait for that kernel's completion and writes first.
     if (p.base < 0) asm volatile("griddepcontrol.wait;" ::: "memory");
+    S.kind = p.base >= 0                           ? 0
+             : __ldcg(&p.ctrl->exact_path) != 0    ? 1
+             : __ldcg(&p.ctrl->raw_predicted) != 0 ? 2
+                                                   : 0;
+  }
+  bar_coders();
+  const bool first_ok =
+      S.kind == 0 ||
+      first_phase(S, p.in, p.n, p.N, p.out, p.out_bytes, p.ctrl,
+                  reinterpret_cast<unsigned long long*>(reinterpret_cast<uint8_t*>(p.ctrl) + kWsExactBinsOffset),
+                  p.status, p.spin_limit, S.kind);
+  if (tid == 0) {
     S.e0 = p.base >= 0 ? p.base : __ldcg(&p.ctrl->e0);
-    S.skip = p.base >= 0 ? 0 : static_cast<int>(__ldcg(&p.ctrl->raw_done));
+    S.skip = !first_ok || (p.base < 0 && __ldcg(&p.ctrl->raw_done) != 0);
   }
   bar_coders();
   const int e0 = S.e0;
-  const bool skip = S.skip != 0;  // the stream is already in the raw form: drain the copies and leave
+  const bool skip = S.skip != 0;  // nothing to code (raw form written, or a failed wait): drain the copies and leave
   const uint32_t kadd = ((256u - static_cast<unsigned>(e0)) << 7) * 0x00010001u;
   const uint64_t R0 = records_base(p.n);
   // This thread's 64 bytes in a stage: logical 16-byte unit q (values v0 + 8q ..) of row tid / 2

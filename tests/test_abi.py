@@ -38,12 +38,11 @@ def test_binding_constants_match_the_header():
     text = re.sub(r"/\*.*?\*/", "", open(os.path.join(ROOT, "include", "zc.h")).read(), flags=re.S)
     defines = {k: int(v, 0) for k, v in re.findall(r"^#define\s+(ZC_\w+)\s+\(?(-?\w+)\)?\s*$", text, flags=re.M)
                if re.fullmatch(r"-?(0x[0-9a-fA-F]+|\d+)[uUlL]*", v) and not v.endswith(("u", "U", "l", "L"))}
-    assert {"ZC_OK", "ZC_ERR_TIMEOUT", "ZC_KERNEL_DECIDE", "ZC_BASE_AUTO"} <= set(defines)
+    assert {"ZC_OK", "ZC_ERR_TIMEOUT", "ZC_KERNEL_SMALL", "ZC_BASE_AUTO"} <= set(defines)
     for name, value in defines.items():
         if hasattr(zc, name):
             assert getattr(zc, name) == value, name
-    for name in ("ZC_KERNEL_STATS", "ZC_KERNEL_ENCODE", "ZC_KERNEL_DECODE", "ZC_KERNEL_RAW", "ZC_KERNEL_SMALL",
-                 "ZC_KERNEL_DECIDE"):
+    for name in ("ZC_KERNEL_STATS", "ZC_KERNEL_ENCODE", "ZC_KERNEL_DECODE", "ZC_KERNEL_RAW", "ZC_KERNEL_SMALL"):
         assert getattr(zc, name) == defines[name]
 
 

@@ -65,6 +65,16 @@ def test_sweep(k):
     check_loopback(workloads.sweep(k))
 
 
+def test_exact_e0_in_the_loopback():
+    """A tensor on a switching point of the window rule: the encode kernel's first phase settles
+    e0 exactly before any CTA codes or decodes (the decoding-only CTAs take part too)."""
+    from test_gpu_parity import _near_boundary_tensor
+
+    x = _near_boundary_tensor(-8, (1 << 20) + 3, 192, 1e-9)
+    s = check_loopback(x)
+    assert s[7] == oracle.choose_e0(x)
+
+
 @pytest.mark.parametrize("stalled", [0, 37])
 def test_decode_wait_is_bounded(stalled):
     x = workloads.sweep(18)  # 64 chunks

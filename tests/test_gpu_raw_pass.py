@@ -1,8 +1,8 @@
 """The raw pass, against the oracle, through the C ABI.
 
-In auto mode the statistics pass also counts the exponents of a sample (two values in every 64)
+In auto mode the statistics pass also counts the exponents of a sample (two values in every 256)
 and predicts the coded stream's length from the sample's share of escapes.  When the prediction
-is clearly past the raw form's length, the decide kernel counts every chunk's escapes exactly
+is clearly past the raw form's length, the encode kernel first counts every chunk's escapes exactly
 while it copies the values to their place in the raw form, and keeps the form that the rule
 gives: the raw form when the coded one is longer, else (ties included) the coded form, which the
 encode kernel then writes over the copy.  A prediction only picks the route, so every stream
