@@ -47,14 +47,20 @@ namespace {
 constexpr int kCoders = 128;               // coding threads, 32 values each
 static_assert(32 * kCoders == kChunk, "a coding thread holds 32 consecutive values");
 constexpr int kThreads = kCoders + 32;     // + the retiring warp (idle in the scanning CTA)
-constexpr int kCtasPerSm = 5;
+#ifndef ZC_ENCODE_CTAS_PER_SM
+#define ZC_ENCODE_CTAS_PER_SM 5
+#endif
+#ifndef ZC_ENCODE_RING_KB
+#define ZC_ENCODE_RING_KB 18
+#endif
+constexpr int kCtasPerSm = ZC_ENCODE_CTAS_PER_SM;
 constexpr int kStages = 2;                 // input chunks in flight per CTA
 constexpr unsigned kInBytes = 2 * kChunk;
 // Escape-section ring per CTA: four and a half of the largest (a 4 KB plane).  Measured against
 // 16, 20 and 24 KB: up to 18 KB the five CTAs' shared memory fits a smaller carveout, and the
 // low-escape tensors coded about 4% faster than with 20 or 24 KB; 18 KB keeps that and gives the
 // escape-heavy tensors, where the ring fills, 2% more than 16 KB.
-constexpr unsigned kRingBytes = 18 * 1024;
+constexpr unsigned kRingBytes = ZC_ENCODE_RING_KB * 1024;
 static_assert(kRingBytes >= 2 * kMaxEscapeBytes, "a section placed after a skipped gap always fits a drained ring");
 static_assert(kRingBytes % 16 == 0, "sections and their places are 16-byte aligned");
 constexpr unsigned kQueue = 64;            // escape sections waiting, at most
