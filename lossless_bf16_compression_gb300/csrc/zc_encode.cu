@@ -169,10 +169,11 @@ __device__ void issue_load(EncodeSmem& S, int s, uint64_t c, const EncodeParams&
   }
 }
 
-// The scanner (the first CTA to start, its kCoderWarps first warps): resolve chunks in order.  Each round, warp w reads state
-// words frontier + 256 w .. + 255; the published sizes before the first unpublished word (over
-// all warps, in order) become inclusive offsets.  One barrier per round exchanges the warps'
-// ready counts and sums (double-buffered by round parity, so one barrier suffices).
+// The scanner (the first CTA to start, its kCoderWarps first warps): resolve chunks in order.
+// Each round, warp w reads state words frontier + 256 w .. + 255; the published sizes before
+// the first unpublished word (over all warps, in order) become inclusive offsets.  One barrier
+// per round exchanges the warps' ready counts and sums (double-buffered by round parity, so one
+// barrier suffices).
 __device__ __noinline__ void scanner(EncodeSmem& S, unsigned long long* flags, uint64_t N, int* status,
                                      unsigned spin_limit) {
   const unsigned lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -403,7 +404,7 @@ __device__ __noinline__ void write_plane(const uint4* stage, unsigned sw, uint32
 // ------------------------------------------------------------------ the first phase
 //
 // In auto mode the statistics pass may leave one of two jobs, done here before any chunk is
-// coded.  Their chunks are handed out by a ticket of their own, a batch of four to a warp; each
+// coded.  Their chunks are handed out by a ticket of their own, in batches to a warp; each
 // CTA adds its results and the number of chunks it finished to the control block, and the CTA
 // whose count completes N finishes the job and publishes it (first_ready, a release store); the
 // others wait for that, bounded.  A CTA waits only on chunks that a running CTA has taken, so the phase needs
@@ -423,7 +424,7 @@ __device__ __noinline__ void write_plane(const uint4* stage, unsigned sw, uint32
 //    the coding writes the coded form over the copy.
 constexpr int kExactWindow = 24;
 constexpr int kFirstVecPerLane = kChunk / 8 / 32;  // 16 vectors of a chunk per lane
-constexpr unsigned kFirstBatch = 4;                // chunks a warp takes per ticket
+constexpr unsigned kFirstBatch = 8;                // chunks a warp takes per ticket, at most
 
 // Ask for `bytes` (a multiple of 16) at a 16-byte aligned global address to be brought into L2.
 __device__ __forceinline__ void prefetch_l2(const void* p, unsigned bytes) {
@@ -554,16 +555,26 @@ __device__ __noinline__ bool first_phase(EncodeSmem& S, const uint16_t* x, uint6
   Eb = Eb < 1 ? 1 : (Eb > 254 - kExactWindow ? 254 - kExactWindow : Eb);
   unsigned long long lo = 0, hi = 0, bytes = 0;
   unsigned mine = 0;  // chunks this warp finished
+  // Batches of chunks per ticket (fewer atomics on the one counter): about a quarter of what is
+  // left per warp, so the batches shrink to one chunk as the tickets run out and the last ones
+  // end together.  Each chunk is brought into L2 by one bulk prefetch two chunks ahead.
+  const uint64_t warps = static_cast<uint64_t>(gridDim.x) * kCoderWarps;
+  unsigned seen = 0;  // the ticket counter as this warp last saw it
   for (;;) {
-    // A batch of chunks per ticket (fewer atomics on the one counter), brought into L2 at once
-    // (the whole chunks: one bulk prefetch each), then read from there.
+    const uint64_t left = N > seen ? N - seen : 0;
+    const unsigned batch = left > 4 * kFirstBatch * warps ? kFirstBatch
+                                                          : static_cast<unsigned>(left / (4 * warps)) + 1;
     unsigned c0 = 0;
-    if (lane == 0) c0 = atomicAdd(&ctrl->first_ticket, kFirstBatch);
+    if (lane == 0) c0 = atomicAdd(&ctrl->first_ticket, batch);
     c0 = __shfl_sync(0xFFFFFFFFu, c0, 0);
     if (c0 >= N) break;
-    const unsigned cend = c0 + kFirstBatch < N ? c0 + kFirstBatch : static_cast<unsigned>(N);
-    if (lane < cend - c0 && c0 + lane < n / kChunk) prefetch_l2(x + static_cast<uint64_t>(c0 + lane) * kChunk, 2 * kChunk);
+    seen = c0 + batch;
+    const unsigned cend = c0 + batch < N ? c0 + batch : static_cast<unsigned>(N);
+    const uint64_t full = n / kChunk;  // whole chunks: 8 KiB each, 16-byte aligned
+    auto prefetch = [&](uint64_t c) { prefetch_l2(x + c * kChunk, 2 * kChunk); };
+    if (lane < 2 && c0 + lane < cend && c0 + lane < full) prefetch(c0 + lane);
     for (unsigned c = c0; c < cend; ++c) {
+      if (lane == 0 && c + 2 < cend && c + 2 < full) prefetch(c + 2);
       if (kind == 2)
         bytes += raw_chunk(x, n, c, kadd, out);
       else

@@ -15,9 +15,10 @@
 // of the BF16 range overflows or loses the block's sum to underflow and the warp runs one
 // loop; a lane whose block holds Inf or NaN clears and counts them first (they add nothing).
 // Every block sum carries a relative error below 2^-18 (at most 17 roundings, or 64 for the last
-// n % 8 values, summed one by one), so the grid total S_est satisfies |S_est - S| < 2^-17 S.  The last CTA evaluates the rule at S_est (1 -+ 2^-16),
-// rounded outward; when both ends give the same e0 (all but ~4e-5 of random tensors) that e0
-// is exactly the one the correctly rounded S gives, because the rule is monotone in S.
+// n % 8 values, summed one by one), so the grid total S_est satisfies |S_est - S| < 2^-17 S.
+// The last CTA evaluates the rule at S_est (1 -+ 2^-16), rounded outward; when both ends give
+// the same e0 (all but ~4e-5 of random tensors) that e0 is exactly the one the correctly
+// rounded S gives, because the rule is monotone in S.
 // Otherwise the encode kernel's first phase recomputes S exactly with per-exponent integer sums
 // over the whole grid.
 //

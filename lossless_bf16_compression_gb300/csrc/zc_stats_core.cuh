@@ -41,9 +41,10 @@ __device__ int select_e0(double S, unsigned long long n_f) {
   return e < 0 ? 0 : (e > kE0Max ? kE0Max : e);
 }
 
-// Careful block sum for 64 values (32 words), one by one (the last n % 8 values): skips Inf/NaN, and scales every square by
-// 4^-(Emax'-E') relative to the largest exponent present, so no fp32 overflow or underflow
-// matters.  Returns the fp64 value of the block sum and adds the non-finite count.
+// Careful block sum for 64 values (32 words), one by one (used for the last n % 8 values): skips
+// Inf/NaN, and scales every square by 4^-(Emax'-E') relative to the largest exponent present, so
+// no fp32 overflow or underflow matters.  Returns the fp64 value of the block sum and adds the
+// non-finite count.
 __device__ __forceinline__ double careful_block(const uint32_t (&w)[32], unsigned* nonfinite) {
   int emax = 0;
   unsigned nf = 0;

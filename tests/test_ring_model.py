@@ -49,8 +49,10 @@ def ring(tmp_path_factory):
 
 
 def encoder_ring_bytes():
+    """The ring size the encoder is built with by default (ZC_ENCODE_RING_KB KiB)."""
     text = open(os.path.join(CSRC, "zc_encode.cu")).read()
-    return int(eval(re.search(r"constexpr unsigned kRingBytes = ([0-9 *]+);", text).group(1)))
+    assert re.search(r"constexpr unsigned kRingBytes = ZC_ENCODE_RING_KB \* 1024;", text)
+    return 1024 * int(re.search(r"#define ZC_ENCODE_RING_KB (\d+)", text).group(1))
 
 
 def test_edge_cases(ring):
