@@ -312,6 +312,7 @@ struct DeviceInfo {
   int* status;        // device address of the library's status word on this device
   int stats_per_sm;   // resident CTAs per SM of the statistics and encode kernels, found once
   int encode_per_sm;  // per device (host-side launch work stays small for small tensors)
+  int small_ctas;     // the small-tensor kernel's largest cluster on this device (16, else 8)
 };
 
 cudaError_t device_info(DeviceInfo* info);  // defined in zc_api.cu
@@ -344,10 +345,11 @@ cudaError_t launch_decode(const uint8_t* in, uint16_t* out, uint64_t n, const De
 cudaError_t launch_raw_form(const uint16_t* in, uint64_t n, int base, uint8_t* out, unsigned long long* out_bytes,
                             uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream);
 
-// Small tensors (up to small_max_values() = 131072 values): the whole compression in one cluster launch,
-// with no workspace beyond the control block's e0, exact-path flag and length.
-cudaError_t small_setup();  // per device: the kernel's dynamic shared memory size
-uint64_t small_max_values();
+// Small tensors (up to small_max_values(dev) = 262,144 values, or 131,072 where 16-CTA clusters
+// cannot be scheduled): the whole compression in one cluster launch, with no workspace beyond the
+// control block's e0, exact-path flag and length.
+cudaError_t small_setup(int* max_ctas);  // per device: shared memory size, largest cluster
+uint64_t small_max_values(const DeviceInfo& dev);
 cudaError_t launch_small(const uint16_t* in, uint64_t n, int base, uint8_t* out, unsigned long long* out_bytes,
                          uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream);
 

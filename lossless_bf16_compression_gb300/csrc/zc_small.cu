@@ -1,4 +1,4 @@
-// zc_small.cu -- compression of a small tensor (up to 32 chunks of 4096 values) in one launch of
+// zc_small.cu -- compression of a small tensor (up to 64 chunks of 4096 values) in one launch of
 // one thread-block cluster: no workspace, no memset, no tensor map, no second kernel.
 //
 // Method: ZipCCL (SIGCOMM scribe notes), "Key idea and contribution": the window base from the
@@ -8,7 +8,7 @@
 // (general-purpose compressors can be slower than sending the data as it is); here a small
 // tensor costs one launch.
 //
-// GB300 design.  C = min(N, 8) CTAs of 128 threads form one cluster; CTA r holds chunks r, r + C,
+// GB300 design.  C = min(N, 16) CTAs of 128 threads form one cluster; CTA r holds chunks r, r + C,
 // ... in shared memory (up to four: 32 KiB of input, their fixed parts and escape sections, about
 // 70 KB).  The input arrives by bulk async copies.  Each CTA sums its squares in the same fp32
 // blocks with the same error bound as the statistics kernel; after a cluster barrier every CTA
@@ -29,7 +29,14 @@ namespace cg = cooperative_groups;
 namespace zc {
 namespace {
 
-constexpr unsigned kSmallCtas = 8;      // CTAs of the cluster, at most (a portable cluster size)
+#ifndef ZC_SMALL_CTAS
+#define ZC_SMALL_CTAS 16
+#endif
+// CTAs of the cluster, at most: 16 (a non-portable cluster size, taken when the device can
+// schedule such a cluster of this kernel), else 8 (the portable size).
+constexpr unsigned kSmallCtas = ZC_SMALL_CTAS;
+constexpr unsigned kSmallPortableCtas = 8;
+static_assert(kSmallCtas >= kSmallPortableCtas && kSmallCtas <= 16, "a cluster of 8 to 16 CTAs");
 constexpr unsigned kSmallPerCta = 4;    // chunks per CTA, at most (more are faster on the big path)
 constexpr int kSmallThreads = 128;      // a chunk's coding threads, 32 values each
 static_assert(32 * kSmallThreads == kChunk, "a thread codes 32 consecutive values of a chunk");
@@ -297,17 +304,45 @@ __global__ void __launch_bounds__(kSmallThreads) small_kernel(const uint16_t* in
 
 }  // namespace
 
-cudaError_t small_setup() {
-  return cudaFuncSetAttribute(small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(sizeof(SmallSmem)));
+cudaError_t small_setup(int* max_ctas) {
+  cudaError_t err = cudaFuncSetAttribute(small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(sizeof(SmallSmem)));
+  if (err != cudaSuccess) return err;
+  *max_ctas = static_cast<int>(kSmallPortableCtas);
+  if (kSmallCtas > kSmallPortableCtas) {
+    err = cudaFuncSetAttribute(small_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (err != cudaSuccess) {
+      cudaGetLastError();
+      return cudaSuccess;  // the portable size then
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kSmallCtas);
+    cfg.blockDim = dim3(kSmallThreads);
+    cfg.dynamicSmemBytes = sizeof(SmallSmem);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kSmallCtas;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, small_kernel, &cfg) == cudaSuccess && clusters > 0)
+      *max_ctas = static_cast<int>(kSmallCtas);
+    cudaGetLastError();
+  }
+  return cudaSuccess;
 }
 
-uint64_t small_max_values() { return static_cast<uint64_t>(kSmallCtas) * kSmallPerCta * kChunk; }
+uint64_t small_max_values(const DeviceInfo& dev) {
+  return static_cast<uint64_t>(dev.small_ctas) * kSmallPerCta * kChunk;
+}
 
 cudaError_t launch_small(const uint16_t* in, uint64_t n, int base, uint8_t* out, unsigned long long* out_bytes,
                          uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream) {
   const uint64_t N = num_chunks(n);
-  const unsigned C = static_cast<unsigned>(N < kSmallCtas ? N : kSmallCtas);
+  const unsigned cmax = static_cast<unsigned>(dev.small_ctas);
+  const unsigned C = static_cast<unsigned>(N < cmax ? N : cmax);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(C);
   cfg.blockDim = dim3(kSmallThreads);

@@ -78,7 +78,7 @@ extern "C" int zc_compress_static_scratch(const void* in, size_t n, int base_or_
 
   const uint16_t* x = static_cast<const uint16_t*>(in);
   uint8_t* o = static_cast<uint8_t*>(out);
-  if (n > 0 && n <= small_max_values()) {  // a small tensor: one launch, nothing to clear
+  if (n > 0 && n <= small_max_values(dev)) {  // a small tensor: one launch, nothing to clear
     if (launch_small(x, n, base_or_auto, o, len_ptr, ws, dev, stream) != cudaSuccess) return ZC_ERR_CUDA;
     return finish_length(pageable, ws, out_bytes, stream);
   }

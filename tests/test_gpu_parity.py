@@ -207,7 +207,9 @@ def test_supplied_base_matches_auto_stream():
 
 
 def test_deterministic_and_concurrent_streams():
-    xs = [mixed(200_000 + 17 * i, 20 + i) for i in range(4)]
+    """Four compressions on four streams at once: two on the single-launch path for small
+    tensors, two on the multi-launch path."""
+    xs = [mixed((200_000 if i % 2 else 600_000) + 17 * i, 20 + i) for i in range(4)]
     devs = [to_device(x) for x in xs]
     streams = [torch.cuda.Stream() for _ in xs]
     outs = []

@@ -80,12 +80,12 @@ def test_static_scratch_supplied_base_and_host_length():
     assert out[:want.size].cpu().numpy().tobytes() == want.tobytes()
 
 
-@pytest.mark.parametrize("n", [2 * 4096 + 50, 3 * 4096, 40 * 4096 + 50])
+@pytest.mark.parametrize("n", [2 * 4096 + 50, 3 * 4096, 40 * 4096 + 50, 70 * 4096 + 50])
 def test_static_scratch_stays_inside_its_stream_bound(n):
     """Random bit patterns give the longest stream n values can give (the raw form: written after
-    the coded form was found longer by the single-launch path for up to 32 chunks, and by the
-    raw pass beyond); 4 KiB of 0xA5 right before `out` and right after zc_max_stream_bytes(n)
-    bytes of it must survive."""
+    the coded form was found longer by the single-launch path for small tensors, and by the raw
+    pass beyond); 4 KiB of 0xA5 right before `out` and right after zc_max_stream_bytes(n) bytes
+    of it must survive."""
     G = 4096
     x = workloads.random_patterns(n, 600 + n)
     want = oracle.compress(x)
