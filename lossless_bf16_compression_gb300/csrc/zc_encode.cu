@@ -53,6 +53,9 @@ constexpr int kThreads = kCoders + 32;     // + the retiring warp (idle in the s
 #ifndef ZC_ENCODE_RING_KB
 #define ZC_ENCODE_RING_KB 18
 #endif
+#ifndef ZC_ENCODE_PREFETCH
+#define ZC_ENCODE_PREFETCH 1
+#endif
 constexpr int kCtasPerSm = ZC_ENCODE_CTAS_PER_SM;
 constexpr int kStages = 2;                 // input chunks in flight per CTA
 constexpr unsigned kInBytes = 2 * kChunk;
@@ -149,6 +152,11 @@ __device__ __forceinline__ unsigned chunk_rank(unsigned cnt, unsigned* first, un
   const unsigned before = (warp > 0 ? tw.x : 0u) + (warp > 1 ? tw.y : 0u) + (warp > 2 ? tw.z : 0u);
   *first = before + x - cnt;
   return tw.x + tw.y + tw.z + tw.w;
+}
+
+// Ask for `bytes` (a multiple of 16) at a 16-byte aligned global address to be brought into L2.
+__device__ __forceinline__ void prefetch_l2(const void* p, unsigned bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
 // Coding thread 0: start the copy of chunk c into stage s.  A full chunk is one box of the
@@ -426,10 +434,6 @@ constexpr int kExactWindow = 24;
 constexpr int kFirstVecPerLane = kChunk / 8 / 32;  // 16 vectors of a chunk per lane
 constexpr unsigned kFirstBatch = 8;                // chunks a warp takes per ticket, at most
 
-// Ask for `bytes` (a multiple of 16) at a 16-byte aligned global address to be brought into L2.
-__device__ __forceinline__ void prefetch_l2(const void* p, unsigned bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
 
 // Escapes among the two values of w outside `keep`'s cleared halves (codes7_x2 gives exactly
 // 7 << 7 for an escape, and 7 << 7 + 0x80 reaches bit 10).
@@ -960,6 +964,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     if (tid == 0) {
       pending &= ~(1u << s);
       parity ^= 1u << s;
+      // The next ticket's chunk, whose tiled copy starts when this chunk is done, is brought into
+      // L2 now: a third chunk in flight per CTA without a third stage or another held ticket
+      // (taking a ticket earlier to prefetch two ahead measured slower).
+      if (ZC_ENCODE_PREFETCH && next_ticket < p.full_chunks)
+        prefetch_l2(p.in + static_cast<uint64_t>(next_ticket) * kChunk, 2 * kChunk);
     }
 
     // ---- code the chunk: the fixed part goes straight to its place in the stream
