@@ -983,7 +983,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     // take consecutive ranks.
     const unsigned v0 = 32 * tid;
     if (!full) {  // the ragged last chunk came without a copy: fetch this thread's values
-      const uint16_t* src = p.in + c * kChunk;
+      const uint16_t* src = p.in + static_cast<uint64_t>(c) * kChunk;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         uint32_t w4[4];
