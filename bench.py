@@ -58,9 +58,9 @@ TARGET_CONFIGS = ["moe_a2a_16384x7168", "adversarial_256m", "sweep_2^26", "sweep
 SWEEP_SIZES = list(range(15, 30))  # 2^15 .. 2^29 values (64 KiB .. 1 GiB)
 SWEEP_REPS = 100
 L2_FLUSH_BYTES = 256 << 20
-KERNEL_NAMES = {1: "stats", 2: "encode", 3: "decode", 4: "raw_form", 5: "small"}
+KERNEL_NAMES = {1: "stats", 2: "encode", 3: "decode", 4: "raw_form", 5: "small", 6: "medium"}
 KERNEL_SOURCES = {"stats": "zc_stats.cu", "encode": "zc_encode.cu", "decode": "zc_decode.cu",
-                  "raw_form": "zc_encode.cu", "small": "zc_small.cu"}
+                  "raw_form": "zc_encode.cu", "small": "zc_small.cu", "medium": "zc_small.cu"}
 
 
 # ---------------------------------------------------------------------------- ranks

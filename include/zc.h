@@ -178,6 +178,7 @@ int zc_status(cudaStream_t stream, int reset);
 #define ZC_KERNEL_DECODE 3
 #define ZC_KERNEL_RAW 4    /* the step that rewrites a stream in the raw form when that is shorter */
 #define ZC_KERNEL_SMALL 5  /* the single launch that compresses a tensor of up to 64 chunks */
+#define ZC_KERNEL_MEDIUM 6 /* the single cooperative launch that compresses a medium tensor */
 
 /* enable != 0: bracket every kernel the library launches from now on with CUDA events on the
  * kernel's own stream.  enable == 0: stop recording.  Returns ZC_OK or ZC_ERR_CUDA. */

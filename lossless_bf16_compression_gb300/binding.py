@@ -28,6 +28,7 @@ ZC_KERNEL_ENCODE = 2
 ZC_KERNEL_DECODE = 3
 ZC_KERNEL_RAW = 4
 ZC_KERNEL_SMALL = 5
+ZC_KERNEL_MEDIUM = 6
 
 ERROR_NAMES = {
     ZC_OK: "ZC_OK",

@@ -68,7 +68,7 @@ cudaError_t device_info(DeviceInfo* info) {
     if (err != cudaSuccess) return err;
     err = encode_occupancy(&d.encode_per_sm);
     if (err != cudaSuccess) return err;
-    err = small_setup(&d.small_ctas);
+    err = small_setup(&d.small_ctas, &d.medium_ctas);
     if (err != cudaSuccess) return err;
     g_devices[dev] = d;
     g_device_ready[dev] = true;
@@ -161,9 +161,14 @@ int compress_impl(const void* in, size_t n, int base, void* out, size_t* out_byt
   uint8_t* o = static_cast<uint8_t*>(out);
   uint8_t* ws = o + workspace_at(n, loopback);
   const uint16_t* x = static_cast<const uint16_t*>(in);
-  if (n > 0 && n <= small_max_values(dev) && !loopback && stall_chunk == ~uint64_t(0)) {
-    // a small tensor: one launch, no workspace to clear
-    if (launch_small(x, n, base, o, len_ptr, ws, dev, stream) != cudaSuccess) return ZC_ERR_CUDA;
+  if (n > 0 && n <= medium_max_values(dev) && !loopback && stall_chunk == ~uint64_t(0)) {
+    // a small or medium tensor: one launch
+    // (the medium kernel's barrier counter is in the control block: cleared first)
+    const bool small = n <= small_max_values(dev);
+    if (!small && cudaMemsetAsync(ws, 0, kWsControlBytes, stream) != cudaSuccess) return ZC_ERR_CUDA;
+    const cudaError_t err = small ? launch_small(x, n, base, o, len_ptr, ws, dev, stream)
+                                  : launch_medium(x, n, base, o, len_ptr, ws, dev, stream);
+    if (err != cudaSuccess) return ZC_ERR_CUDA;
     return finish_length(pageable, ws, out_bytes, stream);
   }
   if (cudaMemsetAsync(ws, 0, workspace_bytes(n), stream) != cudaSuccess) return ZC_ERR_CUDA;

@@ -108,6 +108,7 @@ struct Control {
   unsigned first_done;      // the encoder's first phase: chunks finished
   unsigned first_ready;     // the encoder's first phase: e0 and the stream form are final
   unsigned long long raw_escape_bytes;  // raw pass: the escape sections' bytes, summed
+  unsigned grid_arrivals;   // the medium kernel's grid barriers: CTAs arrived so far
 };
 static_assert(sizeof(Control) <= kWsControlBytes, "the control block fits its place");
 static_assert(offsetof(Control, exact_path) == 12 && offsetof(Control, raw_predicted) == 80 &&
@@ -313,6 +314,7 @@ struct DeviceInfo {
   int stats_per_sm;   // resident CTAs per SM of the statistics and encode kernels, found once
   int encode_per_sm;  // per device (host-side launch work stays small for small tensors)
   int small_ctas;     // the small-tensor kernel's largest cluster on this device (16, else 8)
+  int medium_ctas;    // CTAs of the medium-tensor kernel's cooperative grid (0: none)
 };
 
 cudaError_t device_info(DeviceInfo* info);  // defined in zc_api.cu
@@ -345,11 +347,17 @@ cudaError_t launch_decode(const uint8_t* in, uint16_t* out, uint64_t n, const De
 cudaError_t launch_raw_form(const uint16_t* in, uint64_t n, int base, uint8_t* out, unsigned long long* out_bytes,
                             uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream);
 
-// Small tensors (up to small_max_values(dev) = 262,144 values, or 131,072 where 16-CTA clusters
-// cannot be scheduled): the whole compression in one cluster launch, with no workspace beyond the
-// control block's e0, exact-path flag and length.
-cudaError_t small_setup(int* max_ctas);  // per device: shared memory size, largest cluster
+// Small and medium tensors: the whole compression in one launch with every CTA resident, up to
+// four chunks per CTA -- one thread-block cluster up to small_max_values(dev) (262,144 values, or
+// 131,072 where 16-CTA clusters cannot be scheduled), one cooperative grid up to
+// medium_max_values(dev).  The small path uses no workspace beyond the control block's e0,
+// exact-path flag and length; the medium path needs only its control block cleared (its
+// barriers' counter): its other workspace slots are each written before they are read.
+cudaError_t small_setup(int* small_ctas, int* medium_ctas);  // per device
 uint64_t small_max_values(const DeviceInfo& dev);
+uint64_t medium_max_values(const DeviceInfo& dev);
+cudaError_t launch_medium(const uint16_t* in, uint64_t n, int base, uint8_t* out, unsigned long long* out_bytes,
+                          uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream);
 cudaError_t launch_small(const uint16_t* in, uint64_t n, int base, uint8_t* out, unsigned long long* out_bytes,
                          uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream);
 

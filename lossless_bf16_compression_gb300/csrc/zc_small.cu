@@ -1,23 +1,35 @@
-// zc_small.cu -- compression of a small tensor (up to 64 chunks of 4096 values) in one launch of
-// one thread-block cluster: no workspace, no memset, no tensor map, no second kernel.
+// zc_small.cu -- compression of a small or medium tensor in one launch, with every CTA resident
+// at once: one thread-block cluster for up to 64 chunks of 4096 values, or one cooperative grid
+// for up to four chunks per resident CTA.  No tensor map, no second kernel.
 //
 // Method: ZipCCL (SIGCOMM scribe notes), "Key idea and contribution": the window base from the
 // tensor's standard deviation, 3-bit codes with the full exponents of the others kept apart
 // (first technique), and the native form where coding does not pay (third technique).  The
 // overhead of a compressor on small messages is what the page calls its performance cliff
-// (general-purpose compressors can be slower than sending the data as it is); here a small
+// (general-purpose compressors can be slower than sending the data as it is); here such a
 // tensor costs one launch.
 //
-// GB300 design.  C = min(N, 16) CTAs of 128 threads form one cluster; CTA r holds chunks r, r + C,
-// ... in shared memory (up to four: 32 KiB of input, their fixed parts and escape sections, about
-// 70 KB).  The input arrives by bulk async copies.  Each CTA sums its squares in the same fp32
-// blocks with the same error bound as the statistics kernel; after a cluster barrier every CTA
-// reads all partials through distributed shared memory, in rank order, so all settle the same e0
-// (and, when the bound straddles a switching point, the same exact per-exponent sums).  The CTAs
-// code their chunks into shared memory, exchange the sections' sizes the same way, and write
-// either the coded stream (fixed parts, sections at their scanned offsets, table, header) or the
-// raw form.  Every cluster barrier is the hardware's; the one wait that polls (the copies'
-// mbarrier) is bounded.
+// GB300 design.  G CTAs of 128 threads; CTA r holds chunks r J .. r J + J - 1 (J = ceil(N / G),
+// at most four) in shared memory: 32 KiB of input and their escape sections.  The input arrives
+// by bulk async copies.  Each CTA sums its squares in the same fp32 blocks with the same error
+// bound as the statistics kernel and publishes its partial; after a barrier over all CTAs every
+// CTA combines all partials in one fixed order, so all settle the same e0 (and, when the bound
+// straddles a switching point, the same exact per-exponent sums).  The CTAs code their chunks
+// (escape sections into shared memory; fixed parts too in a cluster, so that its barriers wait
+// for no global store, or straight to their places in `out` in a grid), publish the sections'
+// sizes, and after another barrier each finds its sections' offsets and the stream's length,
+// then writes the coded form (fixed parts, sections, offset table, header) or the raw form (the
+// values from shared memory, over anything written before the barrier).
+//  - Cluster (up to 16 CTAs, 64 chunks): partials, bins and sizes are read from the other CTAs'
+//    shared memory (distributed shared memory); the barriers are the cluster's, in hardware.
+//  - Cooperative grid (as many CTAs as the device holds at once, launched cooperatively so that
+//    all are resident): partials, bins and sizes go through the call's workspace (slots each CTA
+//    writes before the barrier; the exact path's bins are cleared by CTA 0 before the first
+//    barrier); the barriers count arrivals in the control block, cleared before the launch, and
+//    their waits are bounded.
+// Every CTA takes part in every barrier (a CTA whose copies did not arrive goes on with zeros
+// and sets the error); every wait that polls (the copies' mbarrier, the grid barriers) is
+// bounded, and a grid barrier that fails stops the CTAs (the cluster's never fail).
 #include <cooperative_groups.h>
 
 #include "zc_code_core.cuh"
@@ -37,60 +49,193 @@ namespace {
 constexpr unsigned kSmallCtas = ZC_SMALL_CTAS;
 constexpr unsigned kSmallPortableCtas = 8;
 static_assert(kSmallCtas >= kSmallPortableCtas && kSmallCtas <= 16, "a cluster of 8 to 16 CTAs");
-constexpr unsigned kSmallPerCta = 4;    // chunks per CTA, at most (more are faster on the big path)
+constexpr unsigned kPerCta = 4;         // chunks per CTA, at most
 constexpr int kSmallThreads = 128;      // a chunk's coding threads, 32 values each
 static_assert(32 * kSmallThreads == kChunk, "a thread codes 32 consecutive values of a chunk");
 constexpr unsigned kSmallWaitLimit = 1u << 22;
-
-struct __align__(128) SmallSmem {
-  uint4 x[kSmallPerCta][kChunk / 8];                 // inputs, 8 KiB per chunk (zero past m)
-  uint4 fixed[kSmallPerCta][kFullFixedBytes / 16];   // fixed parts: codes, then sign|mantissa
-  uint4 sec[kSmallPerCta][kMaxEscapeBytes / 16];     // escape sections
-  unsigned long long bins[256];                      // exact fallback: this CTA's exponent sums
-  unsigned long long allbins[256];                   // ... and the cluster's
-  unsigned long long offset[kSmallCtas * kSmallPerCta];  // every chunk's section offset (stream)
-  unsigned size[kSmallCtas * kSmallPerCta];          // every chunk's section bytes
-  uint64_t mbar;
-  double wsum[kSmallThreads / 32];
-  unsigned long long wnf[kSmallThreads / 32];
-  double cta_sum;
-  unsigned long long cta_nonfinite;
-  unsigned long long total;
-  unsigned scan[kSmallThreads / 32];
-  unsigned my_size[kSmallPerCta];
-  int e0;
-  int need_exact;
-  int ok;
-};
+constexpr int kWarpsPerCta = kSmallThreads / 32;
 
 __device__ __forceinline__ void bar_cta() { __syncthreads(); }
 
-__global__ void __launch_bounds__(kSmallThreads) small_kernel(const uint16_t* in, uint64_t n, int base,
-                                                               uint8_t* out, unsigned long long* out_bytes,
-                                                               Control* ctrl, int* status) {
-  extern __shared__ __align__(128) unsigned char smem_raw[];
-  SmallSmem& S = *reinterpret_cast<SmallSmem*>(smem_raw);
-  cg::cluster_group cluster = cg::this_cluster();
-  const unsigned C = cluster.num_blocks(), r = cluster.block_rank();
+struct __align__(128) ResidentSmem {
+  uint4 x[kPerCta][kChunk / 8];                 // inputs, 8 KiB per chunk (zero past m)
+  uint4 sec[kPerCta][kMaxEscapeBytes / 16];     // escape sections
+  unsigned long long bins[256];                 // exact fallback: this CTA's exponent sums, then all
+  uint64_t mbar;
+  double wsum[kWarpsPerCta];
+  unsigned long long wnf[kWarpsPerCta];
+  unsigned long long wbefore[kWarpsPerCta], wtotal[kWarpsPerCta];
+  double cta_sum;
+  unsigned long long cta_nonfinite;
+  unsigned long long offset[kPerCta];          // this CTA's sections' offsets in the stream
+  unsigned long long total;
+  unsigned long long n_finite;
+  unsigned scan[kWarpsPerCta];
+  unsigned my_size[kPerCta];
+  int e0;
+  int need_exact;
+  int ok;
+  // last: the fixed parts, kept here until the stream's form is known (cluster launches only; the
+  // grid launch stores them in place at once and does not allocate this)
+  uint4 fixed[kPerCta][kFullFixedBytes / 16];
+};
+constexpr size_t kGridSmemBytes = offsetof(ResidentSmem, fixed);
+
+// The exchange between the CTAs of a cluster: distributed shared memory, cluster barriers.
+struct ClusterExchange {
+  cg::cluster_group cl = cg::this_cluster();
+  __device__ unsigned ctas() const { return cl.num_blocks(); }
+  __device__ unsigned rank() const { return cl.block_rank(); }
+  __device__ bool sync() {  // a hardware barrier: always passed
+    cl.sync();
+    return true;
+  }
+  __device__ void put_partial(ResidentSmem& S, double s, unsigned long long nf) {
+    S.cta_sum = s;
+    S.cta_nonfinite = nf;
+  }
+  __device__ void get_partial(ResidentSmem& S, unsigned q, double* s, unsigned long long* nf) {
+    *s = *cl.map_shared_rank(&S.cta_sum, q);
+    *nf = *cl.map_shared_rank(&S.cta_nonfinite, q);
+  }
+  // exact path: the CTA's bins are in S.bins; every CTA adds up all of them (after a barrier)
+  __device__ void share_bins(ResidentSmem&) {}
+  __device__ unsigned long long all_bins(ResidentSmem& S, unsigned e) {
+    unsigned long long t = 0;
+    for (unsigned q = 0; q < ctas(); ++q) t += cl.map_shared_rank(S.bins, q)[e];
+    return t;
+  }
+  __device__ void put_size(ResidentSmem& S, unsigned j, uint64_t, unsigned size) { S.my_size[j] = size; }
+  __device__ unsigned get_size(ResidentSmem& S, uint64_t c, unsigned J) {
+    return cl.map_shared_rank(S.my_size, static_cast<unsigned>(c / J))[c % J];
+  }
+  static constexpr bool kKeepFixed = true;  // no store to global memory before the last barrier
+  __device__ void finish() {  // no CTA leaves while another may read its shared memory: order no memory
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.aligned;" ::: "memory");
+  }
+};
+
+// A barrier over the CTAs of a cooperative grid (all resident at once), bounded: *arrivals was
+// cleared before the launch, and barrier k (k = 1, 2, ..) is passed when it reaches k G.  A wait
+// that runs out sets ZC_ERR_TIMEOUT.  Returns, the same in every thread of the CTA, whether the
+// barrier was passed with no error recorded; after an error the CTAs stop waiting and the caller
+// stops (the call has failed and reports it), so no CTA is left spinning and nothing is written
+// from data that may be missing.
+__device__ bool grid_barrier(unsigned* arrivals, unsigned target, int* status, unsigned spin_limit) {
+  __shared__ int barrier_ok;
+  bar_cta();
+  if (threadIdx.x == 0) {
+    __threadfence();  // this CTA's writes, before its arrival
+    atomicAdd(arrivals, 1u);
+    unsigned spins = 0, backoff = 32;
+    bool ok = true;
+    while (ld_acquire_u32(arrivals) < target) {
+      if (read_status(status) != 0 || ++spins > spin_limit) {
+        if (spins > spin_limit) set_error(status, ZC_ERR_TIMEOUT);
+        ok = false;
+        break;
+      }
+      __nanosleep(backoff);
+      backoff = backoff < 256 ? backoff * 2 : 256;
+    }
+    __threadfence();  // the other CTAs' writes, from here on
+    barrier_ok = ok && read_status(status) == 0;
+  }
+  bar_cta();
+  return barrier_ok != 0;
+}
+
+// The exchange between the CTAs of a cooperative grid: the call's workspace, bounded barriers.
+struct GridExchange {
+  StatsPartial* partials;        // one per CTA
+  unsigned long long* bins;      // 256, cleared by CTA 0 before the first barrier
+  unsigned* sizes;               // one per chunk
+  unsigned* arrivals;            // the barriers' counter, cleared before the launch
+  int* status;
+  unsigned passed = 0;           // barriers passed so far
+  __device__ unsigned ctas() const { return gridDim.x; }
+  __device__ unsigned rank() const { return blockIdx.x; }
+  __device__ bool sync() { return grid_barrier(arrivals, ++passed * gridDim.x, status, kDefaultSpinLimit); }
+  __device__ void put_partial(ResidentSmem&, double s, unsigned long long nf) {
+    partials[blockIdx.x].sum = s;
+    partials[blockIdx.x].nonfinite = nf;
+  }
+  __device__ void get_partial(ResidentSmem&, unsigned q, double* s, unsigned long long* nf) {
+    *s = __ldcg(&partials[q].sum);
+    *nf = __ldcg(&partials[q].nonfinite);
+  }
+  __device__ void share_bins(ResidentSmem& S) {
+    for (unsigned e = threadIdx.x; e < 256; e += kSmallThreads)
+      if (S.bins[e]) atomicAdd(bins + e, S.bins[e]);
+  }
+  __device__ unsigned long long all_bins(ResidentSmem&, unsigned e) { return __ldcg(bins + e); }
+  __device__ void put_size(ResidentSmem&, unsigned, uint64_t c, unsigned size) { sizes[c] = size; }
+  __device__ unsigned get_size(ResidentSmem&, uint64_t c, unsigned) { return __ldcg(sizes + c); }
+  static constexpr bool kKeepFixed = false;  // fixed parts stored in place while coding
+  __device__ void finish() {}
+};
+
+// Sum over a warp in a fixed order (a butterfly tree), in every lane.
+template <typename T>
+__device__ T warp_sum(T v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  return v;
+}
+
+// Sum over the CTA's threads in a fixed order (warp tree, then warps in order), in every thread.
+template <typename T>
+__device__ T cta_sum(T v, T* scratch) {
+  v = warp_sum(v);
+  if ((threadIdx.x & 31) == 0) scratch[threadIdx.x >> 5] = v;
+  bar_cta();
+  T t = 0;
+#pragma unroll
+  for (int i = 0; i < kWarpsPerCta; ++i) t += scratch[i];
+  bar_cta();
+  return t;
+}
+
+// f(i, a, b) adds term i to the pair (a, b) for i < count; the pairs are summed in a fixed order,
+// valid in thread 0: by warp 0 alone (no CTA barrier) when count <= 32 * per_lane, else by the
+// whole CTA.
+template <typename A, typename B, typename F>
+__device__ void fixed_sum2(uint64_t count, unsigned per_lane, A* sa, B* sb, A* a, B* b, F f) {
+  const bool wide = count > 32ull * per_lane;
+  const unsigned step = wide ? kSmallThreads : 32;
+  A va = 0;
+  B vb = 0;
+  if (wide || threadIdx.x < 32)
+    for (uint64_t i = threadIdx.x; i < count; i += step) f(i, va, vb);
+  *a = wide ? cta_sum(va, sa) : warp_sum(va);
+  *b = wide ? cta_sum(vb, sb) : warp_sum(vb);
+}
+
+template <typename Exchange>
+__device__ void compress_resident(Exchange& X, ResidentSmem& S, const uint16_t* in, uint64_t n, int base,
+                                  uint8_t* out, unsigned long long* out_bytes, Control* ctrl, int* status) {
+  const unsigned G = X.ctas(), r = X.rank();
   const unsigned tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint64_t N = num_chunks(n);
-  const unsigned J = N > r ? static_cast<unsigned>((N - r + C - 1) / C) : 0u;  // chunks r + C j, j < J
+  const unsigned J = static_cast<unsigned>((N + G - 1) / G);  // chunks per CTA
+  const uint64_t first = static_cast<uint64_t>(r) * J;        // this CTA's chunks: first .. first + mine - 1
+  const unsigned mine = first < N ? static_cast<unsigned>(N - first < J ? N - first : J) : 0u;
+  const uint64_t R0 = records_base(n), E0 = escape_base(n);
 
   // ---- the input: whole 16-byte vectors by bulk async copies, the ragged tail and zeros by threads
   if (tid == 0) {
     mbar_init(&S.mbar, 1);
     fence_mbar_init();
     unsigned bytes = 0;
-    for (unsigned j = 0; j < J; ++j) bytes += (2 * chunk_values(n, r + C * j)) & ~15u;
+    for (unsigned j = 0; j < mine; ++j) bytes += (2 * chunk_values(n, first + j)) & ~15u;
     mbar_arrive_expect_tx(&S.mbar, bytes);
-    for (unsigned j = 0; j < J; ++j) {
-      const uint64_t c = r + C * j;
-      const unsigned vb = (2 * chunk_values(n, c)) & ~15u;
-      if (vb) bulk_load(S.x[j], in + c * kChunk, vb, &S.mbar);
+    for (unsigned j = 0; j < mine; ++j) {
+      const unsigned vb = (2 * chunk_values(n, first + j)) & ~15u;
+      if (vb) bulk_load(S.x[j], in + (first + j) * kChunk, vb, &S.mbar);
     }
   }
-  for (unsigned j = 0; j < J; ++j) {
-    const uint64_t c = r + C * j;
+  for (unsigned j = 0; j < mine; ++j) {
+    const uint64_t c = first + j;
     const unsigned m = chunk_values(n, c);
     if (m == kChunk) continue;
     for (unsigned i = tid; i < kChunk / 8; i += kSmallThreads) {
@@ -112,14 +257,14 @@ __global__ void __launch_bounds__(kSmallThreads) small_kernel(const uint16_t* in
   }
   bar_cta();
   if (!S.ok && tid == 0) mbar_wait(&S.mbar, 0, kSmallWaitLimit);  // never leave a copy in flight
-  // (a CTA whose copies did not arrive still takes part in every cluster barrier below, with zeros)
+  // (a CTA whose copies did not arrive still takes part in every barrier below, with zeros)
 
   // ---- the window base
   int e0 = base;
   if (base < 0) {
     double acc = 0.0;
     unsigned nonfinite = 0;
-    const unsigned B = 64 * J;  // blocks of 64 values of this CTA's chunks (zeros past m add nothing)
+    const unsigned B = 64 * mine;  // blocks of 64 values of this CTA's chunks (zeros past m add nothing)
     for (unsigned b0 = 0; b0 < B; b0 += kSmallThreads) {
       const unsigned b = b0 + tid;
       uint32_t w[32];
@@ -147,55 +292,61 @@ __global__ void __launch_bounds__(kSmallThreads) small_kernel(const uint16_t* in
     if (tid == 0) {
       double s = 0.0;
       unsigned long long c = 0;
-      for (int i = 0; i < kSmallThreads / 32; ++i) {
+      for (int i = 0; i < kWarpsPerCta; ++i) {
         s += S.wsum[i];
         c += S.wnf[i];
       }
-      S.cta_sum = s;
-      S.cta_nonfinite = c;
+      X.put_partial(S, s, c);
     }
-    cluster.sync();
-    if (tid == 0) {  // every CTA combines the partials in rank order: the same e0 everywhere
-      double s = 0.0;
-      unsigned long long nf_all = 0;
-      for (unsigned q = 0; q < C; ++q) {
-        s += *cluster.map_shared_rank(&S.cta_sum, q);
-        nf_all += *cluster.map_shared_rank(&S.cta_nonfinite, q);
-      }
+    if (!X.sync()) return;
+    // Every CTA combines the partials in the same fixed order (thread t takes CTAs t, t + 32 or
+    // t + 128, .., then a fixed tree), so every CTA settles the same e0.
+    double s = 0.0;
+    unsigned long long nf_all = 0;
+    fixed_sum2(G, 1, S.wsum, S.wnf, &s, &nf_all, [&](uint64_t q, double& a, unsigned long long& b) {
+      double sq;
+      unsigned long long nq;
+      X.get_partial(S, static_cast<unsigned>(q), &sq, &nq);
+      a += sq;
+      b += nq;
+    });
+    if (tid == 0) {
       int e = 0;
       S.need_exact = decide_e0(s, n - nf_all, &e) ? 0 : 1;
       S.e0 = e;
-      S.total = n - nf_all;  // the finite count, kept for the exact path
+      S.n_finite = n - nf_all;  // for the exact path
     }
     bar_cta();
-    if (S.need_exact) {  // the same in every CTA: exact per-exponent sums over the cluster
+    if (S.need_exact) {  // the same in every CTA: exact per-exponent sums over all CTAs
       for (unsigned e = tid; e < 256; e += kSmallThreads) S.bins[e] = 0;
       bar_cta();
-      for (unsigned j = 0; j < J; ++j)
-        add_exponent_sums(reinterpret_cast<const uint16_t*>(S.x[j]), chunk_values(n, r + C * j), tid, kSmallThreads,
+      for (unsigned j = 0; j < mine; ++j)
+        add_exponent_sums(reinterpret_cast<const uint16_t*>(S.x[j]), chunk_values(n, first + j), tid, kSmallThreads,
                           S.bins);
-      cluster.sync();
-      for (unsigned e = tid; e < 256; e += kSmallThreads) {
-        unsigned long long t = 0;
-        for (unsigned q = 0; q < C; ++q) t += cluster.map_shared_rank(S.bins, q)[e];
-        S.allbins[e] = t;
-      }
       bar_cta();
-      if (tid == 0) S.e0 = select_e0(exact_from_bins(S.allbins), S.total);
-      cluster.sync();  // no CTA overwrites its bins while another one reads them
+      X.share_bins(S);
+      if (!X.sync()) return;
+      unsigned long long t[2] = {0, 0};
+      for (unsigned e = tid, i = 0; e < 256; e += kSmallThreads, ++i) t[i] = X.all_bins(S, e);
+      if (!X.sync()) return;  // every CTA has read the others' bins before any overwrites its own
+      for (unsigned e = tid, i = 0; e < 256; e += kSmallThreads, ++i) S.bins[e] = t[i];
+      bar_cta();
+      if (tid == 0) S.e0 = select_e0(exact_from_bins(S.bins), S.n_finite);
+      bar_cta();
     }
     e0 = S.e0;
-    if (r == 0 && tid == 0 && ctrl) {
+    if (r == 0 && tid == 0) {
       ctrl->e0 = e0;
       ctrl->exact_path = S.need_exact;
     }
   }
 
-  // ---- code this CTA's chunks into shared memory
+  // ---- code this CTA's chunks: fixed parts to their places, escape sections into shared memory
   const uint32_t kadd = ((256u - static_cast<unsigned>(e0)) << 7) * 0x00010001u;
   const unsigned v0 = 32 * tid;
-  for (unsigned j = 0; j < J; ++j) {
-    const unsigned m = chunk_values(n, r + C * j);
+  for (unsigned j = 0; j < mine; ++j) {
+    const uint64_t c = first + j;
+    const unsigned m = chunk_values(n, c);
     const bool full = m == kChunk;
     const unsigned cbytes = full ? kFullCodeBytes : static_cast<unsigned>(code_section_bytes(m));
     const unsigned smbytes = full ? kChunk : static_cast<unsigned>(pad16(m));
@@ -205,7 +356,8 @@ __global__ void __launch_bounds__(kSmallThreads) small_kernel(const uint16_t* in
     Coded32 kd;
     code32(xv, kadd, v0, m, full, kd);
     // (a ragged chunk's threads past m store zero codes and bytes: the sections' padding)
-    store_fixed32(reinterpret_cast<uint8_t*>(S.fixed[j]), cbytes, smbytes, v0, full, kd);
+    store_fixed32(Exchange::kKeepFixed ? reinterpret_cast<uint8_t*>(S.fixed[j]) : out + R0 + c * kFullFixedBytes,
+                  cbytes, smbytes, v0, full, kd);
     const unsigned cnt = __popc(kd.e[0]) + __popc(kd.e[1]) + __popc(kd.e[2]) + __popc(kd.e[3]);
     // ranks: a warp scan of the counts, then the warps' totals
     unsigned x = cnt;
@@ -218,7 +370,7 @@ __global__ void __launch_bounds__(kSmallThreads) small_kernel(const uint16_t* in
     bar_cta();
     unsigned before = 0, k = 0;
 #pragma unroll
-    for (int i = 0; i < kSmallThreads / 32; ++i) {
+    for (int i = 0; i < kWarpsPerCta; ++i) {
       before += i < static_cast<int>(warp) ? S.scan[i] : 0u;
       k += S.scan[i];
     }
@@ -241,28 +393,34 @@ __global__ void __launch_bounds__(kSmallThreads) small_kernel(const uint16_t* in
                    [&](unsigned b) { return lds_u16(xs + 2 * (v0 + b)) >> 7; });
       if (tid < esc_bytes - 3 * k) sts_u8(sec + 3 * k + tid, 0);  // zero padding, < 16 bytes
     }
-    if (tid == 0) S.my_size[j] = esc_bytes;
+    if (tid == 0) {
+      S.my_size[j] = esc_bytes;
+      X.put_size(S, j, c, esc_bytes);
+    }
     bar_cta();  // S.scan is free for the next chunk
   }
 
-  // ---- the sections' offsets: every chunk's size from its CTA, in chunk order
-  cluster.sync();
-  const uint64_t E0 = escape_base(n), R0 = records_base(n);
-  for (unsigned c = tid; c < N; c += kSmallThreads) S.size[c] = cluster.map_shared_rank(S.my_size, c % C)[c / C];
-  bar_cta();
+  // ---- the sections' offsets: the sizes of the chunks before this CTA's, and the stream's length
+  if (!X.sync()) return;
+  unsigned long long bef = 0, tot = 0;  // the sizes of the chunks before this CTA's, of all
+  fixed_sum2(N, 2, S.wbefore, S.wtotal, &bef, &tot, [&](uint64_t c, unsigned long long& a, unsigned long long& b) {
+    const unsigned long long sz = X.get_size(S, c, J);
+    a += c < first ? sz : 0ull;
+    b += sz;
+  });
   if (tid == 0) {
-    unsigned long long at = E0;
-    for (unsigned c = 0; c < N; ++c) {
-      S.offset[c] = at;
-      at += S.size[c];
+    unsigned long long at = E0 + bef;
+    for (unsigned j = 0; j < mine; ++j) {
+      S.offset[j] = at;
+      at += S.my_size[j];
     }
-    S.total = at;
+    S.total = E0 + tot;
   }
   bar_cta();
   const unsigned long long coded = S.total, raw = raw_stream_bytes(n);
   if (coded > raw) {  // the raw form: the header, the values as they are, zero padding
-    for (unsigned j = 0; j < J; ++j) {
-      const uint64_t c = r + C * j;
+    for (unsigned j = 0; j < mine; ++j) {
+      const uint64_t c = first + j;
       const unsigned vecs = (2 * chunk_values(n, c) + 15) / 16;  // the last one carries the padding
       uint4* dst = reinterpret_cast<uint4*>(out + kHeaderBytes + c * 2 * kChunk);
       for (unsigned i = tid; i < vecs; i += kSmallThreads) dst[i] = S.x[j][i];
@@ -273,19 +431,20 @@ __global__ void __launch_bounds__(kSmallThreads) small_kernel(const uint16_t* in
       hdr[1] = n;
       hdr[2] = 0;
       hdr[3] = raw;
-      if (ctrl) ctrl->total = raw;
+      ctrl->total = raw;
       if (out_bytes) *out_bytes = raw;
     }
-  } else {  // the coded form: fixed parts, escape sections, offset table, header
+  } else {  // the coded form: (fixed parts,) escape sections, offset table, header
     unsigned long long* table = reinterpret_cast<unsigned long long*>(out + kHeaderBytes);
-    for (unsigned j = 0; j < J; ++j) {
-      const uint64_t c = r + C * j;
-      const unsigned fb = static_cast<unsigned>(fixed_bytes(chunk_values(n, c))) / 16;
-      uint4* df = reinterpret_cast<uint4*>(out + R0 + c * kFullFixedBytes);
-      for (unsigned i = tid; i < fb; i += kSmallThreads) df[i] = S.fixed[j][i];
-      uint4* ds = reinterpret_cast<uint4*>(out + S.offset[c]);
-      for (unsigned i = tid; i < S.size[c] / 16; i += kSmallThreads) ds[i] = S.sec[j][i];
-      if (tid == 0) table[c] = S.offset[c];
+    for (unsigned j = 0; j < mine; ++j) {
+      if (Exchange::kKeepFixed) {
+        const unsigned fb = static_cast<unsigned>(fixed_bytes(chunk_values(n, first + j))) / 16;
+        uint4* df = reinterpret_cast<uint4*>(out + R0 + (first + j) * kFullFixedBytes);
+        for (unsigned i = tid; i < fb; i += kSmallThreads) df[i] = S.fixed[j][i];
+      }
+      uint4* ds = reinterpret_cast<uint4*>(out + S.offset[j]);
+      for (unsigned i = tid; i < S.my_size[j] / 16; i += kSmallThreads) ds[i] = S.sec[j][i];
+      if (tid == 0) table[first + j] = S.offset[j];
     }
     if (r == 0 && tid == 0) {
       unsigned long long* hdr = reinterpret_cast<unsigned long long*>(out);
@@ -295,20 +454,60 @@ __global__ void __launch_bounds__(kSmallThreads) small_kernel(const uint16_t* in
       hdr[3] = coded;
       table[N] = coded;
       if (kHeaderBytes + 8 * (N + 1) < R0) table[N + 1] = 0;  // zero pad
-      if (ctrl) ctrl->total = coded;
+      ctrl->total = coded;
       if (out_bytes) *out_bytes = coded;
     }
   }
-  cluster.sync();  // no CTA leaves while another one may still read its shared memory
+  X.finish();
+}
+
+__global__ void __launch_bounds__(kSmallThreads) small_kernel(const uint16_t* in, uint64_t n, int base,
+                                                               uint8_t* out, unsigned long long* out_bytes,
+                                                               Control* ctrl, int* status) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  ClusterExchange X;
+  compress_resident(X, *reinterpret_cast<ResidentSmem*>(smem_raw), in, n, base, out, out_bytes, ctrl, status);
+}
+
+__global__ void __launch_bounds__(kSmallThreads) medium_kernel(const uint16_t* in, uint64_t n, int base,
+                                                                uint8_t* out, unsigned long long* out_bytes,
+                                                                uint8_t* ws, int* status) {
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  GridExchange X;
+  X.partials = reinterpret_cast<StatsPartial*>(ws + kWsControlBytes);
+  X.bins = reinterpret_cast<unsigned long long*>(ws + kWsExactBinsOffset);
+  X.sizes = reinterpret_cast<unsigned*>(ws + kWsControlBytes + kWsPartialsBytes);
+  X.arrivals = &reinterpret_cast<Control*>(ws)->grid_arrivals;
+  X.status = status;
+  if (blockIdx.x == 0)  // before the first barrier; only the exact path adds to them, after it
+    for (unsigned e = threadIdx.x; e < 256; e += kSmallThreads) X.bins[e] = 0;
+  compress_resident(X, *reinterpret_cast<ResidentSmem*>(smem_raw), in, n, base, out, out_bytes,
+                    reinterpret_cast<Control*>(ws), status);
 }
 
 }  // namespace
 
-cudaError_t small_setup(int* max_ctas) {
-  cudaError_t err = cudaFuncSetAttribute(small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(sizeof(SmallSmem)));
+cudaError_t small_setup(int* small_ctas, int* medium_ctas) {
+  const int smem = static_cast<int>(sizeof(ResidentSmem));
+  cudaError_t err = cudaFuncSetAttribute(small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
-  *max_ctas = static_cast<int>(kSmallPortableCtas);
+  err = cudaFuncSetAttribute(medium_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kGridSmemBytes));
+  if (err != cudaSuccess) return err;
+  // the cooperative grid: every CTA resident at once, and one statistics partial slot each
+  int dev = 0, sms = 0, per_sm = 0, coop = 0;
+  err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (err != cudaSuccess) return err;
+  err = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
+  if (err != cudaSuccess) return err;
+  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, medium_kernel, kSmallThreads, kGridSmemBytes);
+  if (err != cudaSuccess) return err;
+  const int grid = coop ? per_sm * sms : 0;
+  *medium_ctas = grid < kStatsMaxCtas ? grid : kStatsMaxCtas;
+
+  *small_ctas = static_cast<int>(kSmallPortableCtas);
   if (kSmallCtas > kSmallPortableCtas) {
     err = cudaFuncSetAttribute(small_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (err != cudaSuccess) {
@@ -318,7 +517,7 @@ cudaError_t small_setup(int* max_ctas) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(kSmallCtas);
     cfg.blockDim = dim3(kSmallThreads);
-    cfg.dynamicSmemBytes = sizeof(SmallSmem);
+    cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = kSmallCtas;
@@ -328,25 +527,29 @@ cudaError_t small_setup(int* max_ctas) {
     cfg.numAttrs = 1;
     int clusters = 0;
     if (cudaOccupancyMaxActiveClusters(&clusters, small_kernel, &cfg) == cudaSuccess && clusters > 0)
-      *max_ctas = static_cast<int>(kSmallCtas);
+      *small_ctas = static_cast<int>(kSmallCtas);
     cudaGetLastError();
   }
   return cudaSuccess;
 }
 
 uint64_t small_max_values(const DeviceInfo& dev) {
-  return static_cast<uint64_t>(dev.small_ctas) * kSmallPerCta * kChunk;
+  return static_cast<uint64_t>(dev.small_ctas) * kPerCta * kChunk;
+}
+
+uint64_t medium_max_values(const DeviceInfo& dev) {
+  return static_cast<uint64_t>(dev.medium_ctas) * kPerCta * kChunk;
 }
 
 cudaError_t launch_small(const uint16_t* in, uint64_t n, int base, uint8_t* out, unsigned long long* out_bytes,
                          uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream) {
   const uint64_t N = num_chunks(n);
   const unsigned cmax = static_cast<unsigned>(dev.small_ctas);
-  const unsigned C = static_cast<unsigned>(N < cmax ? N : cmax);
+  const unsigned C = static_cast<unsigned>(N < cmax ? N : cmax);  // then J = ceil(N / C) <= 4
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(C);
   cfg.blockDim = dim3(kSmallThreads);
-  cfg.dynamicSmemBytes = sizeof(SmallSmem);
+  cfg.dynamicSmemBytes = sizeof(ResidentSmem);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -358,6 +561,28 @@ cudaError_t launch_small(const uint16_t* in, uint64_t n, int base, uint8_t* out,
   TimingRecord t = timing_begin(ZC_KERNEL_SMALL, stream);
   const cudaError_t err = cudaLaunchKernelEx(&cfg, small_kernel, in, n, base, out, out_bytes,
                                              reinterpret_cast<Control*>(ws), dev.status);
+  timing_end(t, stream);
+  return err;
+}
+
+cudaError_t launch_medium(const uint16_t* in, uint64_t n, int base, uint8_t* out, unsigned long long* out_bytes,
+                          uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream) {
+  // one chunk per CTA while the device holds that many CTAs, else up to four
+  const uint64_t N = num_chunks(n), gmax = static_cast<uint64_t>(dev.medium_ctas);
+  const uint64_t J = (N + gmax - 1) / gmax;
+  const unsigned G = static_cast<unsigned>((N + J - 1) / J);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(G);
+  cfg.blockDim = dim3(kSmallThreads);
+  cfg.dynamicSmemBytes = kGridSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;  // every CTA resident at once: the grid barriers
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  TimingRecord t = timing_begin(ZC_KERNEL_MEDIUM, stream);
+  const cudaError_t err = cudaLaunchKernelEx(&cfg, medium_kernel, in, n, base, out, out_bytes, ws, dev.status);
   timing_end(t, stream);
   return err;
 }

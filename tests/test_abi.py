@@ -42,7 +42,8 @@ def test_binding_constants_match_the_header():
     for name, value in defines.items():
         if hasattr(zc, name):
             assert getattr(zc, name) == value, name
-    for name in ("ZC_KERNEL_STATS", "ZC_KERNEL_ENCODE", "ZC_KERNEL_DECODE", "ZC_KERNEL_RAW", "ZC_KERNEL_SMALL"):
+    for name in ("ZC_KERNEL_STATS", "ZC_KERNEL_ENCODE", "ZC_KERNEL_DECODE", "ZC_KERNEL_RAW", "ZC_KERNEL_SMALL",
+                 "ZC_KERNEL_MEDIUM"):
         assert getattr(zc, name) == defines[name]
 
 

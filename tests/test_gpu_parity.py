@@ -126,6 +126,24 @@ def test_raw_and_coded_at_the_tie():
     assert s.size == 112 and s[6] == 0
 
 
+@pytest.mark.parametrize("n", [64 * 4096 + 1, 100_003 * 3, 1 << 20, 4 * (1 << 20) + 77, 2432 * 4096, 2432 * 4096 + 1])
+@pytest.mark.parametrize("base", [-1, 122])
+def test_single_cooperative_launch(n, base):
+    """Sizes past the cluster launch: up to four chunks per CTA of one cooperative grid (2432
+    chunks on a GB300: 608 resident CTAs), then, one value more, the multi-launch path."""
+    check_parity(mixed(n, 500 + n % 1000, sigma=1.0, frac=0.02), base)
+
+
+@pytest.mark.parametrize("n", [300_001, 5_000_000])
+def test_single_cooperative_launch_raw_and_special(n):
+    """The raw form and non-finite blocks on the cooperative-grid path."""
+    s = check_parity(workloads.random_patterns(n, 61))
+    assert s[6] == 0
+    x = workloads.sweep(20)[: n % (1 << 20)].copy() if n < (1 << 20) else np.tile(workloads.sweep(20), 5)[:n].copy()
+    x[::97] = 0x7FC0
+    check_parity(x)
+
+
 def test_special_tensors():
     check_parity(np.full(9000, 0x7FC0, np.uint16))           # only NaN: no finite value
     check_parity(np.full(9000, 0x3F80, np.uint16))           # constant 1.0
@@ -187,8 +205,9 @@ def test_auto_base_at_binade_boundaries(k4, rel):
 
 @pytest.mark.parametrize("n,k4", [((1 << 20) + 3, -8), (1 << 26, -3)])
 def test_auto_base_at_binade_boundaries_large(n, k4):
-    """Boundary tensors beyond the small-tensor path: the exact sum runs over the whole grid (a
-    follow-on kernel gated by the statistics pass's verdict) and must agree with the oracle."""
+    """Boundary tensors beyond the cluster launch: the exact sum runs over the whole grid (in the
+    cooperative-grid launch at 2^20 + 3 values, in the encode kernel's first phase at 2^26) and
+    must agree with the oracle."""
     x = _near_boundary_tensor(k4, n, 200 + k4, 1e-9)
     st, out, total = gpu_compress(x)
     assert st == zc.ZC_OK
