@@ -412,11 +412,11 @@ __device__ __noinline__ void write_plane(const uint4* stage, unsigned sw, uint32
 // ------------------------------------------------------------------ the first phase
 //
 // In auto mode the statistics pass may leave one of two jobs, done here before any chunk is
-// coded.  Their chunks are handed out by a ticket of their own, in batches to a warp; each
-// CTA adds its results and the number of chunks it finished to the control block, and the CTA
-// whose count completes N finishes the job and publishes it (first_ready, a release store); the
-// others wait for that, bounded.  A CTA waits only on chunks that a running CTA has taken, so the phase needs
-// no CTA to be resident at any particular time.
+// coded.  Their chunks are handed out by a ticket of their own, in batches to a warp; each CTA
+// adds its results and the number of chunks it finished to the control block, and the CTA whose
+// count completes N finishes the job and publishes it (first_ready, a release store); the others
+// wait for that, bounded.  A CTA waits only on chunks that a running CTA has taken, so the phase
+// needs no CTA to be resident at any particular time.
 //  - Exact e0 (kind 1), when the statistics pass's estimate could not settle it: every thread sums
 //    sig^2 4^d exactly in a 128-bit integer over a 24-binade window from Eb (around the typical
 //    value, anchored on the estimate's e0; a term is below 2^62, so 2^66 of them fit); values
@@ -433,7 +433,6 @@ __device__ __noinline__ void write_plane(const uint4* stage, unsigned sw, uint32
 constexpr int kExactWindow = 24;
 constexpr int kFirstVecPerLane = kChunk / 8 / 32;  // 16 vectors of a chunk per lane
 constexpr unsigned kFirstBatch = 8;                // chunks a warp takes per ticket, at most
-
 
 // Escapes among the two values of w outside `keep`'s cleared halves (codes7_x2 gives exactly
 // 7 << 7 for an escape, and 7 << 7 + 0x80 reaches bit 10).
@@ -822,8 +821,8 @@ __device__ __noinline__ void loopback_decode_only(EncodeSmem& S, const uint8_t* 
     const unsigned d = S.slot_chunk[j];
     if (tid == 0) S.descapes = 0;
     bar_coders();
-    decode_chunk(fixed_of(j), esc_of(j), &S.descapes, p.values + static_cast<uint64_t>(d) * kChunk, chunk_values(p.n, d),
-                 S.e0, S.slot_size[j], p.status, tid, [] { bar_coders(); });
+    decode_chunk(fixed_of(j), esc_of(j), &S.descapes, p.values + static_cast<uint64_t>(d) * kChunk,
+                 chunk_values(p.n, d), S.e0, S.slot_size[j], p.status, tid, [] { bar_coders(); });
     bar_coders();  // slot j is read: refill it
     if (tid == 0) fill(j);
     bar_coders();
@@ -842,8 +841,8 @@ __device__ __noinline__ void loopback_decode_only(EncodeSmem& S, const uint8_t* 
     if (tid == 0) S.descapes = 0;
     bar_coders();
     const unsigned d = S.slot_chunk[k];
-    decode_chunk(fixed_of(k), esc_of(k), &S.descapes, p.values + static_cast<uint64_t>(d) * kChunk, chunk_values(p.n, d),
-                 S.e0, S.slot_size[k], p.status, tid, [] { bar_coders(); });
+    decode_chunk(fixed_of(k), esc_of(k), &S.descapes, p.values + static_cast<uint64_t>(d) * kChunk,
+                 chunk_values(p.n, d), S.e0, S.slot_size[k], p.status, tid, [] { bar_coders(); });
   }
 }
 
@@ -990,7 +989,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const unsigned v = v0 + 8 * q + 2 * i;
-          w4[i] = (v < m ? static_cast<uint32_t>(src[v]) : 0u) | (v + 1 < m ? static_cast<uint32_t>(src[v + 1]) << 16 : 0u);
+          w4[i] = (v < m ? static_cast<uint32_t>(src[v]) : 0u) |
+                  (v + 1 < m ? static_cast<uint32_t>(src[v + 1]) << 16 : 0u);
         }
         S.xin[s][(sw ^ (16 * q)) / 16] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
       }
@@ -1095,7 +1095,8 @@ __global__ void __launch_bounds__(kRawThreads) raw_form_kernel(const uint16_t* i
   uint4* dst = reinterpret_cast<uint4*>(out + kHeaderBytes);
   const uint64_t nvec = n / 8;  // whole 16-byte vectors of values
   const uint64_t stride = static_cast<uint64_t>(gridDim.x) * kRawThreads;
-  for (uint64_t i = static_cast<uint64_t>(blockIdx.x) * kRawThreads + threadIdx.x; i < nvec; i += stride * kRawVecPerThread) {
+  for (uint64_t i = static_cast<uint64_t>(blockIdx.x) * kRawThreads + threadIdx.x; i < nvec;
+       i += stride * kRawVecPerThread) {
     uint4 v[kRawVecPerThread];
 #pragma unroll
     for (int j = 0; j < kRawVecPerThread; ++j)
