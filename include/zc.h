@@ -97,14 +97,18 @@ size_t zc_max_stream_bytes(size_t n);
  *   out           device, zc_max_compressed_bytes(n) bytes, 16-byte aligned, must not overlap
  *                 `in`.  The stream is written from out[0]: the coded form, or the raw form
  *                 when that is shorter.  The form is decided on the device from the coded
- *                 form's exact length, with no host synchronization: after the encoder's scan,
- *                 or, in auto mode when an exponent sample of the statistics pass predicts a
- *                 raw stream, by a pass that counts every chunk's escapes while it copies the
- *                 values to the raw form (the encoder then has nothing to do).  The bytes past
- *                 *out_bytes, including the workspace tail, are unspecified afterwards.  The library keeps
- *                 no per-call state outside `out`, so calls on different streams with
- *                 different buffers may run concurrently.  The encode kernel's CTAs wait on
- *                 one another (bounded) only for work that a CTA already running has taken,
+ *                 form's exact length, with no host synchronization.  A tensor of up to 2^25
+ *                 values compresses in one launch (a thread-block cluster or a cooperative
+ *                 grid, every CTA resident from the start), which knows every chunk's escape
+ *                 count before it writes a section.  A larger one runs a statistics kernel and
+ *                 an encode kernel: the form is decided after the encoder's scan, or, in auto
+ *                 mode when an exponent sample of the statistics pass predicts a raw stream,
+ *                 by a pass that counts every chunk's escapes while it copies the values to
+ *                 the raw form (the encoder then has nothing to do).  The bytes past
+ *                 *out_bytes, including the workspace tail, are unspecified afterwards.  The
+ *                 library keeps no per-call state outside `out`, so calls on different streams
+ *                 with different buffers may run concurrently.  The encode kernel's CTAs wait
+ *                 on one another (bounded) only for work that a CTA already running has taken,
  *                 so a concurrent kernel that delays some of them slows the call but does not
  *                 make it fail.
  *   out_bytes     receives the stream length.  Device, managed or pinned host memory is
@@ -179,6 +183,7 @@ int zc_status(cudaStream_t stream, int reset);
 #define ZC_KERNEL_RAW 4    /* the step that rewrites a stream in the raw form when that is shorter */
 #define ZC_KERNEL_SMALL 5  /* the single launch that compresses a tensor of up to 64 chunks */
 #define ZC_KERNEL_MEDIUM 6 /* the single cooperative launch that compresses a medium tensor */
+#define ZC_KERNEL_FUSED 7  /* the single cooperative launch for a tensor of up to 2^25 values */
 
 /* enable != 0: bracket every kernel the library launches from now on with CUDA events on the
  * kernel's own stream.  enable == 0: stop recording.  Returns ZC_OK or ZC_ERR_CUDA. */

@@ -29,6 +29,7 @@ ZC_KERNEL_DECODE = 3
 ZC_KERNEL_RAW = 4
 ZC_KERNEL_SMALL = 5
 ZC_KERNEL_MEDIUM = 6
+ZC_KERNEL_FUSED = 7
 
 ERROR_NAMES = {
     ZC_OK: "ZC_OK",

@@ -16,7 +16,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libzc.so")
-SOURCES = ["zc_api.cu", "zc_stats.cu", "zc_encode.cu", "zc_decode.cu", "zc_static.cu", "zc_small.cu"]
+SOURCES = ["zc_api.cu", "zc_stats.cu", "zc_encode.cu", "zc_decode.cu", "zc_static.cu", "zc_small.cu", "zc_fused.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr", f"-I{INCLUDE}", f"-I{CSRC}"]

@@ -70,6 +70,8 @@ cudaError_t device_info(DeviceInfo* info) {
     if (err != cudaSuccess) return err;
     err = small_setup(&d.small_ctas, &d.medium_ctas);
     if (err != cudaSuccess) return err;
+    err = fused_setup(&d.fused_ctas);
+    if (err != cudaSuccess) return err;
     g_devices[dev] = d;
     g_device_ready[dev] = true;
   }
@@ -119,6 +121,20 @@ uint64_t workspace_at(uint64_t n, bool loopback) {
 namespace zc {
 
 // A pageable length: copy it back from the control block and wait for it.
+bool single_launch(uint64_t n, const DeviceInfo& dev) {
+  return n <= medium_max_values(dev) || n <= fused_max_values(dev);
+}
+
+cudaError_t launch_one(const uint16_t* in, uint64_t n, int base, uint8_t* out, unsigned long long* out_bytes,
+                       uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream) {
+  if (n <= small_max_values(dev)) return launch_small(in, n, base, out, out_bytes, ws, dev, stream);
+  // the grid kernels' barrier counter is in the control block: cleared first
+  const cudaError_t err = cudaMemsetAsync(ws, 0, kWsControlBytes, stream);
+  if (err != cudaSuccess) return err;
+  if (n <= medium_max_values(dev)) return launch_medium(in, n, base, out, out_bytes, ws, dev, stream);
+  return launch_fused(in, n, base, out, out_bytes, ws, dev, stream);
+}
+
 int finish_length(bool pageable, uint8_t* ws, size_t* out_bytes, cudaStream_t stream) {
   if (!pageable) return ZC_OK;
   unsigned long long total = 0;
@@ -161,14 +177,8 @@ int compress_impl(const void* in, size_t n, int base, void* out, size_t* out_byt
   uint8_t* o = static_cast<uint8_t*>(out);
   uint8_t* ws = o + workspace_at(n, loopback);
   const uint16_t* x = static_cast<const uint16_t*>(in);
-  if (n > 0 && n <= medium_max_values(dev) && !loopback && stall_chunk == ~uint64_t(0)) {
-    // a small or medium tensor: one launch
-    // (the medium kernel's barrier counter is in the control block: cleared first)
-    const bool small = n <= small_max_values(dev);
-    if (!small && cudaMemsetAsync(ws, 0, kWsControlBytes, stream) != cudaSuccess) return ZC_ERR_CUDA;
-    const cudaError_t err = small ? launch_small(x, n, base, o, len_ptr, ws, dev, stream)
-                                  : launch_medium(x, n, base, o, len_ptr, ws, dev, stream);
-    if (err != cudaSuccess) return ZC_ERR_CUDA;
+  if (n > 0 && !loopback && stall_chunk == ~uint64_t(0) && single_launch(n, dev)) {
+    if (launch_one(x, n, base, o, len_ptr, ws, dev, stream) != cudaSuccess) return ZC_ERR_CUDA;
     return finish_length(pageable, ws, out_bytes, stream);
   }
   if (cudaMemsetAsync(ws, 0, workspace_bytes(n), stream) != cudaSuccess) return ZC_ERR_CUDA;

@@ -108,7 +108,11 @@ struct Control {
   unsigned first_done;      // the encoder's first phase: chunks finished
   unsigned first_ready;     // the encoder's first phase: e0 and the stream form are final
   unsigned long long raw_escape_bytes;  // raw pass: the escape sections' bytes, summed
-  unsigned grid_arrivals;   // the medium kernel's grid barriers: CTAs arrived so far
+  unsigned grid_arrivals;   // the grid kernels' barriers: CTAs arrived so far
+  unsigned grid_release;    // the L2-resident kernel: the last barrier its last CTA released
+  int grid_e0;              // ... the window base, and 1 when the exact sums must decide it
+  unsigned grid_exact;
+  unsigned long long grid_escape_bytes;  // ... the escape sections' bytes, all chunks
 };
 static_assert(sizeof(Control) <= kWsControlBytes, "the control block fits its place");
 static_assert(offsetof(Control, exact_path) == 12 && offsetof(Control, raw_predicted) == 80 &&
@@ -315,6 +319,7 @@ struct DeviceInfo {
   int encode_per_sm;  // per device (host-side launch work stays small for small tensors)
   int small_ctas;     // the small-tensor kernel's largest cluster on this device (16, else 8)
   int medium_ctas;    // CTAs of the medium-tensor kernel's cooperative grid (0: none)
+  int fused_ctas;     // CTAs of the L2-resident kernel's cooperative grid (0: none)
 };
 
 cudaError_t device_info(DeviceInfo* info);  // defined in zc_api.cu
@@ -360,6 +365,21 @@ cudaError_t launch_medium(const uint16_t* in, uint64_t n, int base, uint8_t* out
                           uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream);
 cudaError_t launch_small(const uint16_t* in, uint64_t n, int base, uint8_t* out, unsigned long long* out_bytes,
                          uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream);
+
+// Tensors above the medium size that the L2 nearly holds: one cooperative launch that reads the
+// input three times (statistics from HBM; an exact escape count per chunk and the coding, mostly
+// from the L2) and writes every part of the stream straight to its place.  Needs the control block
+// cleared; its other workspace slots are each written before they are read.
+cudaError_t fused_setup(int* fused_ctas);  // per device
+uint64_t fused_max_values(const DeviceInfo& dev);
+cudaError_t launch_fused(const uint16_t* in, uint64_t n, int base, uint8_t* out, unsigned long long* out_bytes,
+                         uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream);
+
+// Whether a tensor of n values (n > 0) compresses in one launch, and that launch (the small,
+// medium or L2-resident kernel, with the control block cleared for the grid kernels).
+bool single_launch(uint64_t n, const DeviceInfo& dev);
+cudaError_t launch_one(const uint16_t* in, uint64_t n, int base, uint8_t* out, unsigned long long* out_bytes,
+                       uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream);
 
 // After the launches of a compression: when the caller's length is pageable host memory, copy
 // it back from the control block and synchronize the stream.  Returns a ZC_ status.

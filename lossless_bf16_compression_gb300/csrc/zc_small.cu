@@ -12,21 +12,25 @@
 // GB300 design.  G CTAs of 128 threads; CTA r holds chunks r J .. r J + J - 1 (J = ceil(N / G),
 // at most four) in shared memory: 32 KiB of input and their escape sections.  The input arrives
 // by bulk async copies.  Each CTA sums its squares in the same fp32 blocks with the same error
-// bound as the statistics kernel and publishes its partial; after a barrier over all CTAs every
-// CTA combines all partials in one fixed order, so all settle the same e0 (and, when the bound
-// straddles a switching point, the same exact per-exponent sums).  The CTAs code their chunks
-// (escape sections into shared memory; fixed parts too in a cluster, so that its barriers wait
-// for no global store, or straight to their places in `out` in a grid), publish the sections'
-// sizes, and after another barrier each finds its sections' offsets and the stream's length,
-// then writes the coded form (fixed parts, sections, offset table, header) or the raw form (the
+// bound as the statistics kernel and publishes its partial; after a barrier the partials are
+// combined in one fixed order, so that one e0 is settled for all (and, when the bound straddles a
+// switching point, the exact per-exponent sums decide it).  The CTAs code their chunks (escape
+// sections into shared memory; fixed parts too in a cluster, so that its barriers wait for no
+// global store, or straight to their places in `out` in a grid), publish the sections' sizes,
+// and after another barrier each knows its sections' offsets and the stream's length, then
+// writes the coded form (fixed parts, sections, offset table, header) or the raw form (the
 // values from shared memory, over anything written before the barrier).
-//  - Cluster (up to 16 CTAs, 64 chunks): partials, bins and sizes are read from the other CTAs'
-//    shared memory (distributed shared memory); the barriers are the cluster's, in hardware.
+//  - Cluster (up to 16 CTAs, 64 chunks): every CTA reads the partials and sizes from the other
+//    CTAs' shared memory (distributed shared memory) and combines them itself; the barriers are
+//    the cluster's, in hardware.
 //  - Cooperative grid (as many CTAs as the device holds at once, launched cooperatively so that
-//    all are resident): partials, bins and sizes go through the call's workspace (slots each CTA
-//    writes before the barrier; the exact path's bins are cleared by CTA 0 before the first
-//    barrier); the barriers count arrivals in the control block, cleared before the launch, and
-//    their waits are bounded.
+//    all are resident): partials, bins and per-CTA totals go through the call's workspace (slots
+//    each CTA writes before the barrier; the exact path's bins are cleared by CTA 0 before the
+//    first barrier).  The barriers count arrivals in the control block, cleared before the
+//    launch; at the two main ones the last CTA to arrive does the combining -- the sum of the
+//    partials and the window rule, the scan of the CTAs' totals into offsets -- and releases the
+//    others, so it is done once instead of by every CTA from every other CTA's slots.  The waits
+//    are bounded.
 // Every CTA takes part in every barrier (a CTA whose copies did not arrive goes on with zeros
 // and sets the error); every wait that polls (the copies' mbarrier, the grid barriers) is
 // bounded, and a grid barrier that fails stops the CTAs (the cluster's never fail).
@@ -34,6 +38,7 @@
 
 #include "zc_code_core.cuh"
 #include "zc_common.cuh"
+#include "zc_grid.cuh"
 #include "zc_stats_core.cuh"
 
 namespace cg = cooperative_groups;
@@ -50,12 +55,10 @@ constexpr unsigned kSmallCtas = ZC_SMALL_CTAS;
 constexpr unsigned kSmallPortableCtas = 8;
 static_assert(kSmallCtas >= kSmallPortableCtas && kSmallCtas <= 16, "a cluster of 8 to 16 CTAs");
 constexpr unsigned kPerCta = 4;         // chunks per CTA, at most
-constexpr int kSmallThreads = 128;      // a chunk's coding threads, 32 values each
+constexpr int kSmallThreads = kResidentThreads;
 static_assert(32 * kSmallThreads == kChunk, "a thread codes 32 consecutive values of a chunk");
 constexpr unsigned kSmallWaitLimit = 1u << 22;
-constexpr int kWarpsPerCta = kSmallThreads / 32;
-
-__device__ __forceinline__ void bar_cta() { __syncthreads(); }
+constexpr int kWarpsPerCta = kResidentWarps;
 
 struct __align__(128) ResidentSmem {
   uint4 x[kPerCta][kChunk / 8];                 // inputs, 8 KiB per chunk (zero past m)
@@ -105,9 +108,39 @@ struct ClusterExchange {
     for (unsigned q = 0; q < ctas(); ++q) t += cl.map_shared_rank(S.bins, q)[e];
     return t;
   }
-  __device__ void put_size(ResidentSmem& S, unsigned j, uint64_t, unsigned size) { S.my_size[j] = size; }
-  __device__ unsigned get_size(ResidentSmem& S, uint64_t c, unsigned J) {
-    return cl.map_shared_rank(S.my_size, static_cast<unsigned>(c / J))[c % J];
+  // Every CTA combines the partials in the same fixed order (thread t takes CTAs t, t + 32, ..,
+  // then a fixed tree), so every CTA settles the same e0.
+  __device__ bool settle(ResidentSmem& S, double s_cta, unsigned long long nf_cta, uint64_t n) {
+    if (threadIdx.x == 0) put_partial(S, s_cta, nf_cta);
+    sync();
+    double s = 0.0;
+    unsigned long long nf_all = 0;
+    fixed_sum2(ctas(), 1, S.wsum, S.wnf, &s, &nf_all, [&](uint64_t q, double& a, unsigned long long& b) {
+      double sq;
+      unsigned long long nq;
+      get_partial(S, static_cast<unsigned>(q), &sq, &nq);
+      a += sq;
+      b += nq;
+    });
+    if (threadIdx.x == 0) {
+      int e = 0;
+      S.need_exact = decide_e0(s, n - nf_all, &e) ? 0 : 1;
+      S.e0 = e;
+      S.n_finite = n - nf_all;  // for the exact path
+    }
+    bar_cta();
+    return true;
+  }
+  // The sizes of the chunks before this CTA's and of all, read from the CTAs' shared memory.
+  __device__ bool offsets(ResidentSmem& S, uint64_t first, unsigned, unsigned J, uint64_t N, unsigned long long* bef,
+                          unsigned long long* tot) {
+    sync();
+    fixed_sum2(N, 2, S.wbefore, S.wtotal, bef, tot, [&](uint64_t c, unsigned long long& a, unsigned long long& b) {
+      const unsigned long long sz = cl.map_shared_rank(S.my_size, static_cast<unsigned>(c / J))[c % J];
+      a += c < first ? sz : 0ull;
+      b += sz;
+    });
+    return true;
   }
   static constexpr bool kKeepFixed = true;  // no store to global memory before the last barrier
   __device__ void finish() {  // no CTA leaves while another may read its shared memory: order no memory
@@ -115,42 +148,13 @@ struct ClusterExchange {
   }
 };
 
-// A barrier over the CTAs of a cooperative grid (all resident at once), bounded: *arrivals was
-// cleared before the launch, and barrier k (k = 1, 2, ..) is passed when it reaches k G.  A wait
-// that runs out sets ZC_ERR_TIMEOUT.  Returns, the same in every thread of the CTA, whether the
-// barrier was passed with no error recorded; after an error the CTAs stop waiting and the caller
-// stops (the call has failed and reports it), so no CTA is left spinning and nothing is written
-// from data that may be missing.
-__device__ bool grid_barrier(unsigned* arrivals, unsigned target, int* status, unsigned spin_limit) {
-  __shared__ int barrier_ok;
-  bar_cta();
-  if (threadIdx.x == 0) {
-    __threadfence();  // this CTA's writes, before its arrival
-    atomicAdd(arrivals, 1u);
-    unsigned spins = 0, backoff = 32;
-    bool ok = true;
-    while (ld_acquire_u32(arrivals) < target) {
-      if (read_status(status) != 0 || ++spins > spin_limit) {
-        if (spins > spin_limit) set_error(status, ZC_ERR_TIMEOUT);
-        ok = false;
-        break;
-      }
-      __nanosleep(backoff);
-      backoff = backoff < 256 ? backoff * 2 : 256;
-    }
-    __threadfence();  // the other CTAs' writes, from here on
-    barrier_ok = ok && read_status(status) == 0;
-  }
-  bar_cta();
-  return barrier_ok != 0;
-}
-
 // The exchange between the CTAs of a cooperative grid: the call's workspace, bounded barriers.
 struct GridExchange {
   StatsPartial* partials;        // one per CTA
   unsigned long long* bins;      // 256, cleared by CTA 0 before the first barrier
-  unsigned* sizes;               // one per chunk
-  unsigned* arrivals;            // the barriers' counter, cleared before the launch
+  unsigned long long* totals;    // one per CTA (the scan-state slots, G <= N): escape bytes, then offsets
+  Control* ctrl;                 // the barriers' counter and release word (cleared before the launch)
+  unsigned* arrivals;
   int* status;
   unsigned passed = 0;           // barriers passed so far
   __device__ unsigned ctas() const { return gridDim.x; }
@@ -169,47 +173,42 @@ struct GridExchange {
       if (S.bins[e]) atomicAdd(bins + e, S.bins[e]);
   }
   __device__ unsigned long long all_bins(ResidentSmem&, unsigned e) { return __ldcg(bins + e); }
-  __device__ void put_size(ResidentSmem&, unsigned, uint64_t c, unsigned size) { sizes[c] = size; }
-  __device__ unsigned get_size(ResidentSmem&, uint64_t c, unsigned) { return __ldcg(sizes + c); }
+  // The last CTA to arrive adds the partials up and settles e0 for all (settle_e0_work).
+  __device__ bool settle(ResidentSmem& S, double s_cta, unsigned long long nf_cta, uint64_t n) {
+    if (threadIdx.x == 0) put_partial(S, s_cta, nf_cta);
+    ++passed;
+    if (!grid_barrier_last(arrivals, passed * gridDim.x, &ctrl->grid_release, passed, status, kDefaultSpinLimit,
+                           [&] { settle_e0_work(partials, gridDim.x, n, ctrl, S.wsum, S.wnf); }))
+      return false;
+    if (threadIdx.x == 0) {
+      S.e0 = __ldcg(&ctrl->grid_e0);
+      S.need_exact = static_cast<int>(__ldcg(&ctrl->grid_exact));
+      S.n_finite = __ldcg(&ctrl->n_finite);
+    }
+    bar_cta();
+    return true;
+  }
+  // Each CTA's escape bytes; the last CTA to arrive turns them into offsets (scan_totals_work).
+  __device__ bool offsets(ResidentSmem& S, uint64_t, unsigned mine, unsigned, uint64_t, unsigned long long* bef,
+                          unsigned long long* tot) {
+    if (threadIdx.x == 0) {
+      unsigned long long t = 0;
+      for (unsigned j = 0; j < mine; ++j) t += S.my_size[j];
+      totals[blockIdx.x] = t;
+    }
+    ++passed;
+    if (!grid_barrier_last(arrivals, passed * gridDim.x, &ctrl->grid_release, passed, status, kDefaultSpinLimit,
+                           [&] { scan_totals_work(totals, gridDim.x, ctrl, S.wbefore); }))
+      return false;
+    if (threadIdx.x == 0) {
+      *bef = __ldcg(totals + blockIdx.x);
+      *tot = __ldcg(&ctrl->grid_escape_bytes);
+    }
+    return true;
+  }
   static constexpr bool kKeepFixed = false;  // fixed parts stored in place while coding
   __device__ void finish() {}
 };
-
-// Sum over a warp in a fixed order (a butterfly tree), in every lane.
-template <typename T>
-__device__ T warp_sum(T v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-  return v;
-}
-
-// Sum over the CTA's threads in a fixed order (warp tree, then warps in order), in every thread.
-template <typename T>
-__device__ T cta_sum(T v, T* scratch) {
-  v = warp_sum(v);
-  if ((threadIdx.x & 31) == 0) scratch[threadIdx.x >> 5] = v;
-  bar_cta();
-  T t = 0;
-#pragma unroll
-  for (int i = 0; i < kWarpsPerCta; ++i) t += scratch[i];
-  bar_cta();
-  return t;
-}
-
-// f(i, a, b) adds term i to the pair (a, b) for i < count; the pairs are summed in a fixed order,
-// valid in thread 0: by warp 0 alone (no CTA barrier) when count <= 32 * per_lane, else by the
-// whole CTA.
-template <typename A, typename B, typename F>
-__device__ void fixed_sum2(uint64_t count, unsigned per_lane, A* sa, B* sb, A* a, B* b, F f) {
-  const bool wide = count > 32ull * per_lane;
-  const unsigned step = wide ? kSmallThreads : 32;
-  A va = 0;
-  B vb = 0;
-  if (wide || threadIdx.x < 32)
-    for (uint64_t i = threadIdx.x; i < count; i += step) f(i, va, vb);
-  *a = wide ? cta_sum(va, sa) : warp_sum(va);
-  *b = wide ? cta_sum(vb, sb) : warp_sum(vb);
-}
 
 template <typename Exchange>
 __device__ void compress_resident(Exchange& X, ResidentSmem& S, const uint16_t* in, uint64_t n, int base,
@@ -289,34 +288,14 @@ __device__ void compress_resident(Exchange& X, ResidentSmem& S, const uint16_t* 
       S.wnf[warp] = nf;
     }
     bar_cta();
-    if (tid == 0) {
-      double s = 0.0;
-      unsigned long long c = 0;
+    double s_cta = 0.0;  // (thread 0)
+    unsigned long long nf_cta = 0;
+    if (tid == 0)
       for (int i = 0; i < kWarpsPerCta; ++i) {
-        s += S.wsum[i];
-        c += S.wnf[i];
+        s_cta += S.wsum[i];
+        nf_cta += S.wnf[i];
       }
-      X.put_partial(S, s, c);
-    }
-    if (!X.sync()) return;
-    // Every CTA combines the partials in the same fixed order (thread t takes CTAs t, t + 32 or
-    // t + 128, .., then a fixed tree), so every CTA settles the same e0.
-    double s = 0.0;
-    unsigned long long nf_all = 0;
-    fixed_sum2(G, 1, S.wsum, S.wnf, &s, &nf_all, [&](uint64_t q, double& a, unsigned long long& b) {
-      double sq;
-      unsigned long long nq;
-      X.get_partial(S, static_cast<unsigned>(q), &sq, &nq);
-      a += sq;
-      b += nq;
-    });
-    if (tid == 0) {
-      int e = 0;
-      S.need_exact = decide_e0(s, n - nf_all, &e) ? 0 : 1;
-      S.e0 = e;
-      S.n_finite = n - nf_all;  // for the exact path
-    }
-    bar_cta();
+    if (!X.settle(S, s_cta, nf_cta, n)) return;  // S.e0, S.need_exact, S.n_finite
     if (S.need_exact) {  // the same in every CTA: exact per-exponent sums over all CTAs
       for (unsigned e = tid; e < 256; e += kSmallThreads) S.bins[e] = 0;
       bar_cta();
@@ -393,21 +372,13 @@ __device__ void compress_resident(Exchange& X, ResidentSmem& S, const uint16_t* 
                    [&](unsigned b) { return lds_u16(xs + 2 * (v0 + b)) >> 7; });
       if (tid < esc_bytes - 3 * k) sts_u8(sec + 3 * k + tid, 0);  // zero padding, < 16 bytes
     }
-    if (tid == 0) {
-      S.my_size[j] = esc_bytes;
-      X.put_size(S, j, c, esc_bytes);
-    }
+    if (tid == 0) S.my_size[j] = esc_bytes;
     bar_cta();  // S.scan is free for the next chunk
   }
 
   // ---- the sections' offsets: the sizes of the chunks before this CTA's, and the stream's length
-  if (!X.sync()) return;
-  unsigned long long bef = 0, tot = 0;  // the sizes of the chunks before this CTA's, of all
-  fixed_sum2(N, 2, S.wbefore, S.wtotal, &bef, &tot, [&](uint64_t c, unsigned long long& a, unsigned long long& b) {
-    const unsigned long long sz = X.get_size(S, c, J);
-    a += c < first ? sz : 0ull;
-    b += sz;
-  });
+  unsigned long long bef = 0, tot = 0;  // (thread 0)
+  if (!X.offsets(S, first, mine, J, N, &bef, &tot)) return;
   if (tid == 0) {
     unsigned long long at = E0 + bef;
     for (unsigned j = 0; j < mine; ++j) {
@@ -476,8 +447,9 @@ __global__ void __launch_bounds__(kSmallThreads) medium_kernel(const uint16_t* i
   GridExchange X;
   X.partials = reinterpret_cast<StatsPartial*>(ws + kWsControlBytes);
   X.bins = reinterpret_cast<unsigned long long*>(ws + kWsExactBinsOffset);
-  X.sizes = reinterpret_cast<unsigned*>(ws + kWsControlBytes + kWsPartialsBytes);
-  X.arrivals = &reinterpret_cast<Control*>(ws)->grid_arrivals;
+  X.totals = reinterpret_cast<unsigned long long*>(ws + kWsControlBytes + kWsPartialsBytes);
+  X.ctrl = reinterpret_cast<Control*>(ws);
+  X.arrivals = &X.ctrl->grid_arrivals;
   X.status = status;
   if (blockIdx.x == 0)  // before the first barrier; only the exact path adds to them, after it
     for (unsigned e = threadIdx.x; e < 256; e += kSmallThreads) X.bins[e] = 0;

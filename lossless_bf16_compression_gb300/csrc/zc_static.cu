@@ -78,13 +78,8 @@ extern "C" int zc_compress_static_scratch(const void* in, size_t n, int base_or_
 
   const uint16_t* x = static_cast<const uint16_t*>(in);
   uint8_t* o = static_cast<uint8_t*>(out);
-  if (n > 0 && n <= medium_max_values(dev)) {  // a small or medium tensor: one launch
-    // (the medium kernel's barrier counter is in the control block: cleared first)
-    const bool small = n <= small_max_values(dev);
-    if (!small && cudaMemsetAsync(ws, 0, kWsControlBytes, stream) != cudaSuccess) return ZC_ERR_CUDA;
-    const cudaError_t err = small ? launch_small(x, n, base_or_auto, o, len_ptr, ws, dev, stream)
-                                  : launch_medium(x, n, base_or_auto, o, len_ptr, ws, dev, stream);
-    if (err != cudaSuccess) return ZC_ERR_CUDA;
+  if (n > 0 && single_launch(n, dev)) {
+    if (launch_one(x, n, base_or_auto, o, len_ptr, ws, dev, stream) != cudaSuccess) return ZC_ERR_CUDA;
     return finish_length(pageable, ws, out_bytes, stream);
   }
   if (cudaMemsetAsync(ws, 0, workspace_bytes(n), stream) != cudaSuccess) return ZC_ERR_CUDA;

@@ -61,7 +61,7 @@ def tiny(rng, k):
     return ((rng.integers(0, 2, k) << 15) | (20 << 7) | rng.integers(0, 128, k)).astype(np.uint16)
 
 
-def planes_and_list(planes, list_k, extra=0, chunks=4100, tail=0, seed=7):
+def planes_and_list(planes, list_k, extra=0, chunks=16400, tail=0, seed=7):
     """`planes` chunks of escapes only (each keeps a 4096-byte plane), then one chunk with
     list_k escapes, one with `extra`, the rest (and a ragged tail of `tail` values) with none."""
     rng = np.random.default_rng(seed)
@@ -77,8 +77,9 @@ def planes_and_list(planes, list_k, extra=0, chunks=4100, tail=0, seed=7):
     return np.concatenate(parts)
 
 
-# (tensors beyond the single-launch paths, which decide the form after coding in shared memory)
-@pytest.mark.parametrize("n", [16_800_001, (1 << 24) + 77, 4200 * 4096, 4200 * 4096 + 8, 30_000_001])
+# (tensors beyond the single-launch paths -- 2^26 values on a GB300 -- which decide the form from
+# exact sizes before writing)
+@pytest.mark.parametrize("n", [(1 << 26) + 1, (1 << 26) + 77, 16500 * 4096, 16500 * 4096 + 8, 70_000_001])
 def test_random_patterns_take_the_raw_pass(n):
     x = workloads.random_patterns(n, 900 + n % 1000)
     s, route = compress_and_route(x)
@@ -95,24 +96,24 @@ def test_gaussian_tensor_is_not_predicted_raw():
 
 
 def test_prediction_raw_but_coded_is_shorter():
-    """1300 of 4100 chunks escape everywhere and keep planes (one byte per value): the sample
+    """5200 of 16400 chunks escape everywhere and keep planes (one byte per value): the sample
     sees ~32% escapes, which at three bytes each would make the coded stream longer, but the
     planes make it shorter.  The exact count keeps the coded form."""
-    x = planes_and_list(1300, 100, tail=1000)
+    x = planes_and_list(5200, 100, tail=1000)
     s, route = compress_and_route(x)
     assert route == (1, 0), "the sample did not predict a raw stream, or the raw form was kept"
     assert s[6] == 12 and s.size < raw_bytes(x.size)
 
 
 def test_tie_after_the_raw_pass_keeps_the_coded_form():
-    """2554 plane chunks and one list of 662 escapes (1986 bytes, padded to 2000) make the coded
-    stream exactly as long as the raw form (33,587,232 bytes): the coded form is kept.  One
+    """10217 plane chunks and one list of 1317 escapes (3951 bytes, padded to 3952) make the coded
+    stream exactly as long as the raw form (134,348,832 bytes): the coded form is kept.  One
     escape more, in another chunk, makes it 16 bytes longer: the raw form."""
-    x = planes_and_list(2554, 662)
+    x = planes_and_list(10217, 1317)
     s, route = compress_and_route(x)
     assert route == (1, 0)
     assert s[6] == 12 and s.size == raw_bytes(x.size)
-    x = planes_and_list(2554, 662, extra=1)
+    x = planes_and_list(10217, 1317, extra=1)
     s, route = compress_and_route(x)
     assert route == (1, 1)
     assert s[6] == 0 and s.size == raw_bytes(x.size)
@@ -121,7 +122,7 @@ def test_tie_after_the_raw_pass_keeps_the_coded_form():
 def test_supplied_base_takes_no_prediction():
     """With e0 supplied there is no statistics pass: a raw stream comes from the raw-form step
     after coding, and it is the same stream."""
-    x = workloads.random_patterns(17_000_003, 31)
+    x = workloads.random_patterns(67_200_003, 31)
     s, route = compress_and_route(x, base=int(oracle.choose_e0(x)))
     assert route == (0, 0)
     assert s[6] == 0
@@ -133,7 +134,7 @@ def test_raw_pass_length_on_the_host():
     """The length reaches pageable host memory through the control block as well."""
     import ctypes
 
-    x = workloads.random_patterns(17_000_000, 77)
+    x = workloads.random_patterns(67_200_000, 77)
     xd = torch.from_numpy(x.view(np.int16)).cuda()
     out = torch.empty(zc.zc_max_compressed_bytes(x.size), dtype=torch.uint8, device="cuda")
     length = ctypes.c_uint64(0)
