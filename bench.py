@@ -58,10 +58,12 @@ TARGET_CONFIGS = ["moe_a2a_16384x7168", "adversarial_256m", "sweep_2^26", "sweep
 SWEEP_SIZES = list(range(15, 30))  # 2^15 .. 2^29 values (64 KiB .. 1 GiB)
 SWEEP_REPS = 100
 L2_FLUSH_BYTES = 256 << 20
-KERNEL_NAMES = {1: "stats", 2: "encode", 3: "decode", 4: "raw_form", 5: "small", 6: "medium", 7: "fused"}
+KERNEL_NAMES = {1: "stats", 2: "encode", 3: "decode", 4: "raw_form", 5: "small", 6: "medium", 7: "fused",
+                8: "sample", 9: "encode_spec", 10: "reset"}
 KERNEL_SOURCES = {"stats": "zc_stats.cu", "encode": "zc_encode.cu", "decode": "zc_decode.cu",
                   "raw_form": "zc_encode.cu", "small": "zc_small.cu", "medium": "zc_small.cu",
-                  "fused": "zc_fused.cu"}
+                  "fused": "zc_fused.cu", "sample": "zc_stats.cu", "encode_spec": "zc_encode.cu",
+                  "reset": "zc_encode.cu"}
 
 
 # ---------------------------------------------------------------------------- ranks
@@ -502,7 +504,7 @@ def run_ours(args, rank, world, local):
     raw_pass = raw_stream and int(cd.out[ws + 84:ws + 88].cpu().numpy().view(np.uint32)[0]) == 1
     raw_by = ("encode (raw pass)" if raw_pass else "raw_form") if raw_stream else None
     alg = {"stats": 2 * n, "encode": 4 * n if raw_pass else 2 * n + C, "decode": C + 2 * n,
-           "raw_form": 4 * n if raw_stream and not raw_pass else 0, "fused": 4 * n + C}
+           "raw_form": 4 * n if raw_stream and not raw_pass else 0, "fused": 4 * n + C, "encode_spec": 2 * n + C}
     dominant = max((k for k in avg if alg.get(k)), key=lambda k: avg[k] * len(per[k]))
     achieved = alg[dominant] / (avg[dominant] * 1e-3) / 1e9
     traffic, traffic_from = profiled_traffic(dominant, args.workload)

@@ -81,6 +81,12 @@ constexpr unsigned kLoopbackDecoders = ZC_LOOPBACK_DECODERS;  // start order), t
 static_assert(kLoopbackDecoders < kLoopbackCycle - 1, "the first CTA after the scanner codes");
 constexpr int kCoderWarps = kCoders / 32;
 constexpr unsigned kScanPerWarp = 32 * kScanPerLane;
+// Launch modes.  kPlain: e0 supplied, or (auto) read from the statistics kernel before it.
+// kSpeculative: code with the sample pass's e0 and sum the squares while coding; the CTA whose
+// chunks complete the count checks that e0 against the exact rule on the whole tensor's sum and
+// sets the fallback word when it differs (or cannot be settled).  kGated: after the speculative
+// path; runs as kPlain (auto) only when the fallback word is set, else returns at once.
+constexpr int kPlain = 0, kSpeculative = 1, kGated = 2;
 
 struct EncodeParams {
   const uint16_t* in;
@@ -96,6 +102,8 @@ struct EncodeParams {
   unsigned spin_limit;
   uint64_t full_chunks;  // n / 4096: chunks that come by one tiled copy each
   uint16_t* values;      // loopback: the decoded values (n x u16); null for compression alone
+  int mode;              // kPlain, kSpeculative or kGated
+  StatsPartial* partials;  // speculative: one slot per CTA for its sums
 };
 
 struct __align__(128) EncodeSmem {
@@ -130,6 +138,11 @@ struct __align__(128) EncodeSmem {
   unsigned descapes;
   unsigned slot_chunk[2], slot_size[2];  // a decoding-only CTA's two slots
   int slot_ok[2];
+  // speculative: the coding warps' sums, and whether this CTA completed the chunk count
+  double spec_sum[kCoderWarps];
+  unsigned long long spec_nf[kCoderWarps], spec_values[kCoderWarps], spec_inside[kCoderWarps];
+  int spec_last;
+  int e_end[2];
 };
 
 __device__ __forceinline__ void bar_coders() { asm volatile("bar.sync 1, %0;" ::"n"(kCoders) : "memory"); }
@@ -846,6 +859,141 @@ __device__ __noinline__ void loopback_decode_only(EncodeSmem& S, const uint8_t* 
   }
 }
 
+// Speculative mode: one coding thread's share of a chunk's sum of squares, its 32 values (xv) as
+// one block.  With e0 in [kFastE0Min, kFastE0Max] (`fast`), the values inside the window have
+// magnitudes in [2^-40, 2^61), so their squares are normal fp32 numbers, and the block is summed
+// plainly: bf16 -> fp32 by a shift or a mask, squares by packed fp32x2 FMAs into four partial
+// sums (at most 11 roundings, relative error below 2^-19 while nothing underflows).  An escape can
+// overflow (the sum is then not finite, as it is for Inf and NaN inputs): such a lane's block goes
+// through block_sum, the careful sum.  An escape can also underflow, losing at most 2^-150 per
+// operation; against a sum of squares of which half the values lie inside the window (each
+// square at least 2^-80), that is below 2^-66 of it -- so the CTA checks that half of its values
+// were inside the window (spec_verdict), and otherwise the guess is not trusted.  Outside that
+// range of e0 every block goes through block_sum.
+constexpr int kFastE0Min = 87, kFastE0Max = 180;
+
+__device__ __forceinline__ unsigned long long fma_f32x2(unsigned long long a, unsigned long long b,
+                                                        unsigned long long c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+__device__ __forceinline__ void spec_square_sum(const uint4 (&xv)[4], bool fast, double* acc, unsigned* nonfinite) {
+  const uint32_t w[16] = {xv[0].x, xv[0].y, xv[0].z, xv[0].w, xv[1].x, xv[1].y, xv[1].z, xv[1].w,
+                          xv[2].x, xv[2].y, xv[2].z, xv[2].w, xv[3].x, xv[3].y, xv[3].z, xv[3].w};
+  bool redo = !fast;
+  if (fast) {
+    unsigned long long a = 0, b = 0;  // two fp32x2 accumulators: four partial sums
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const unsigned long long x =
+          static_cast<unsigned long long>(w[i] << 16) | (static_cast<unsigned long long>(w[i] & 0xFFFF0000u) << 32);
+      if (i & 1) b = fma_f32x2(x, x, b);
+      else a = fma_f32x2(x, x, a);
+    }
+    const float s = (__uint_as_float(static_cast<uint32_t>(a)) + __uint_as_float(static_cast<uint32_t>(a >> 32))) +
+                    (__uint_as_float(static_cast<uint32_t>(b)) + __uint_as_float(static_cast<uint32_t>(b >> 32)));
+    redo = !isfinite(s);
+    if (!redo) *acc += static_cast<double>(s);
+  }
+  if (__any_sync(0xFFFFFFFFu, redo)) {  // block_sum's vote needs every lane: the others add zeros
+    uint32_t z[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) z[i] = redo ? w[i] : 0u;
+    block_sum(z, acc, nonfinite);
+  }
+}
+
+// Speculative mode, the coding threads of a CTA after its last chunk: the CTA's sums go to its
+// slot, and its chunks to the count.  The CTA whose chunks complete the count (an acquire-release
+// add tells it; every other coding CTA has published its slot before its own add) sums all the
+// slots, applies the rule exactly as the statistics kernel does (decide_e0, one end per thread),
+// and sets the fallback word unless the rule settles the e0 the chunks were coded with.  A CTA
+// that took no chunk publishes nothing.  Slots are per CTA, cleared with the workspace.
+__device__ __noinline__ void spec_verdict(EncodeSmem& S, const EncodeParams& p, int e0, double acc,
+                                          unsigned nonfinite, unsigned chunks, bool fast,
+                                          unsigned long long values, unsigned long long inside) {
+  const unsigned tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  unsigned long long nf = nonfinite;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+    nf += __shfl_xor_sync(0xFFFFFFFFu, nf, o);
+    values += __shfl_xor_sync(0xFFFFFFFFu, values, o);
+    inside += __shfl_xor_sync(0xFFFFFFFFu, inside, o);
+  }
+  if (lane == 0) {
+    S.spec_sum[warp] = acc;
+    S.spec_nf[warp] = nf;
+    S.spec_values[warp] = values;
+    S.spec_inside[warp] = inside;
+  }
+  bar_coders();
+  if (tid == 0) {
+    S.spec_last = 0;
+    if (chunks != 0) {
+      double s = 0.0;
+      unsigned long long c = 0, v = 0, in = 0;
+      for (int i = 0; i < kCoderWarps; ++i) {
+        s += S.spec_sum[i];
+        c += S.spec_nf[i];
+        v += S.spec_values[i];
+        in += S.spec_inside[i];
+      }
+      // The plain fp32 squares are within the bound only for a CTA with at least half of its
+      // values inside the window (spec_square_sum); otherwise the guess is not trusted.
+      if (fast && 2 * in < v) p.ctrl->spec_untrusted = 1u;
+      p.partials[blockIdx.x].sum = s;
+      p.partials[blockIdx.x].nonfinite = c;
+      unsigned old;
+      asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;"
+                   : "=r"(old)
+                   : "l"(&p.ctrl->spec_chunks), "r"(chunks)
+                   : "memory");
+      S.spec_last = old + chunks == p.N;
+    }
+  }
+  bar_coders();
+  if (!S.spec_last) return;
+  double a = 0.0;
+  unsigned long long b = 0;
+  for (unsigned q = tid; q < gridDim.x; q += kCoders) {
+    a += __ldcg(&p.partials[q].sum);
+    b += __ldcg(&p.partials[q].nonfinite);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    a += __shfl_xor_sync(0xFFFFFFFFu, a, o);
+    b += __shfl_xor_sync(0xFFFFFFFFu, b, o);
+  }
+  bar_coders();  // the slots of this CTA's warps are free again
+  if (lane == 0) {
+    S.spec_sum[warp] = a;
+    S.spec_nf[warp] = b;
+  }
+  bar_coders();
+  if (tid < 2) {
+    double S_all = 0.0;
+    unsigned long long nf_all = 0;
+    for (int i = 0; i < kCoderWarps; ++i) {
+      S_all += S.spec_sum[i];
+      nf_all += S.spec_nf[i];
+    }
+    const unsigned long long n_f = p.n - nf_all;
+    int e = 0;
+    if (n_f != 0 && S_all != 0.0)
+      e = select_e0(tid == 0 ? __dmul_rd(S_all, 1.0 - 0x1p-16) : __dmul_ru(S_all, 1.0 + 0x1p-16), n_f);
+    const int e_hi = __shfl_sync(0x3u, e, 1);
+    if (tid == 0) {
+      const bool held = e == e_hi && e == e0 && __ldcg(&p.ctrl->spec_untrusted) == 0;
+      p.ctrl->e0 = e0;
+      p.ctrl->n_finite = n_f;
+      if (!held) p.ctrl->fallback = 1u;
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     encode_kernel(const EncodeParams p, const __grid_constant__ CUtensorMap in_map) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -855,6 +1003,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   // completion before it reads anything.
   asm volatile("griddepcontrol.launch_dependents;");
   const unsigned tid = threadIdx.x, warp = tid >> 5;
+  if (p.mode == kGated) {
+    // After the speculative path: wait for the steps before (the speculative coding pass, the
+    // reset, the statistics kernel) and run only when the speculation fell back.
+    if (tid == 0) {
+      asm volatile("griddepcontrol.wait;" ::: "memory");
+      S.skip = __ldcg(&p.ctrl->fallback) == 0;
+    }
+    __syncthreads();
+    if (S.skip) return;
+  }
   if (tid == 0) {
     // The first CTA to start is the scanner.  Every other CTA waits, bounded, only on work the
     // scanner or a CTA that is already running will do (chunks are handed out at run time), so
@@ -873,9 +1031,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         if (tid == 0) {
           asm volatile("griddepcontrol.wait;" ::: "memory");
           bool ok = true;
-          if (__ldcg(&p.ctrl->exact_path) != 0 || __ldcg(&p.ctrl->raw_predicted) != 0)
-            ok = wait_first_ready(p.ctrl, p.status, p.spin_limit);
-          S.skip = !ok || __ldcg(&p.ctrl->raw_done) != 0;
+          if (p.mode == kSpeculative) {  // the sample pass may have turned the speculation off
+            S.skip = __ldcg(&p.ctrl->fallback) != 0;
+          } else {
+            if (__ldcg(&p.ctrl->exact_path) != 0 || __ldcg(&p.ctrl->raw_predicted) != 0)
+              ok = wait_first_ready(p.ctrl, p.status, p.spin_limit);
+            S.skip = !ok || __ldcg(&p.ctrl->raw_done) != 0;
+          }
         }
         bar_coders();
         if (S.skip) return;
@@ -928,7 +1090,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     // (a programmatic dependent launch): the tickets and input copies above do not depend on
     // it, e0 does, so wait for that kernel's completion and writes first.
     if (p.base < 0) asm volatile("griddepcontrol.wait;" ::: "memory");
-    S.kind = p.base >= 0                           ? 0
+    S.kind = p.base >= 0 || p.mode == kSpeculative ? 0
              : __ldcg(&p.ctrl->exact_path) != 0    ? 1
              : __ldcg(&p.ctrl->raw_predicted) != 0 ? 2
                                                    : 0;
@@ -940,12 +1102,23 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                   reinterpret_cast<unsigned long long*>(reinterpret_cast<uint8_t*>(p.ctrl) + kWsExactBinsOffset),
                   p.status, p.spin_limit, S.kind);
   if (tid == 0) {
-    S.e0 = p.base >= 0 ? p.base : __ldcg(&p.ctrl->e0);
-    S.skip = !first_ok || (p.base < 0 && __ldcg(&p.ctrl->raw_done) != 0);
+    if (p.mode == kSpeculative) {  // the sample's e0; off when the sample pass turned the speculation off
+      S.e0 = __ldcg(&p.ctrl->e0_guess);
+      S.skip = __ldcg(&p.ctrl->fallback) != 0;
+    } else {
+      S.e0 = p.base >= 0 ? p.base : __ldcg(&p.ctrl->e0);
+      S.skip = !first_ok || (p.base < 0 && __ldcg(&p.ctrl->raw_done) != 0);
+    }
   }
   bar_coders();
   const int e0 = S.e0;
   const bool skip = S.skip != 0;  // nothing to code (raw form written, or a failed wait): drain the copies and leave
+  const bool speculative = p.mode == kSpeculative;
+  const bool spec_fast = e0 >= kFastE0Min && e0 <= kFastE0Max;  // the plain fp32 squares (spec_square_sum)
+  double spec_acc = 0.0;          // speculative: this thread's sum of squares (fp32 blocks of 32 values)
+  unsigned spec_nonfinite = 0;    // ... and its Inf and NaN
+  unsigned spec_chunks = 0;       // ... and the chunks this CTA coded
+  unsigned long long spec_values = 0, spec_inside = 0;  // ... its values, and those inside the window
   const uint32_t kadd = ((256u - static_cast<unsigned>(e0)) << 7) * 0x00010001u;
   const uint64_t R0 = records_base(p.n);
   // This thread's 64 bytes in a stage: logical 16-byte unit q (values v0 + 8q ..) of row tid / 2
@@ -998,10 +1171,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     uint4 xv[4];
 #pragma unroll
     for (int q = 0; q < 4; ++q) xv[q] = S.xin[s][(sw ^ (16 * q)) / 16];
+    if (speculative) spec_square_sum(xv, spec_fast, &spec_acc, &spec_nonfinite);
     Coded32 kd;
     code32(xv, kadd, v0, m, full, kd);
     store_fixed32(fixed, cbytes, smbytes, v0, full, kd);
     const unsigned cnt = __popc(kd.e[0]) + __popc(kd.e[1]) + __popc(kd.e[2]) + __popc(kd.e[3]);
+    if (speculative) {  // this thread's values, and those inside the window
+      const unsigned mine = full ? 32u : (m > v0 ? min(m - v0, 32u) : 0u);
+      spec_values += mine;
+      spec_inside += mine - cnt;
+    }
 
     unsigned base;
     const unsigned k = chunk_rank(cnt, &base, S.scan);  // [R]
@@ -1036,6 +1215,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     }
     if (bar_coders_or(stop)) break;  // [C] the list is complete in the ring; stage s is free again
     ++R.pushed;
+    ++spec_chunks;
     if (tid == 0) {
       const unsigned qi = (R.pushed - 1) % kQueue;
       S.q_chunk[qi] = c;
@@ -1061,6 +1241,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     for (int s = 0; s < kStages; ++s)  // never leave a copy in flight
       if (pending & (1u << s)) mbar_wait(&S.mbar[s], (parity >> s) & 1u, kWaitLimit);
   }
+  if (speculative && !skip)
+    spec_verdict(S, p, e0, spec_acc, spec_nonfinite, spec_chunks, spec_fast, spec_values, spec_inside);
   if (p.values) {  // loopback: no chunk left to code, so decode (the stages are free now)
     bar_coders();
     loopback_decode(S, p.out, p.values, p.flags, p.ctrl, p.status, p.n, p.N, p.spin_limit);
@@ -1122,6 +1304,24 @@ __global__ void __launch_bounds__(kRawThreads) raw_form_kernel(const uint16_t* i
   }
 }
 
+// After the speculative coding pass, as a programmatic dependent launch: when the guess did not
+// hold, the workspace goes back to zero (all but the control block's last 16 bytes, which hold the
+// fallback word) for the statistics and encode kernels that follow; otherwise every CTA returns.
+constexpr int kResetThreads = 256;
+
+__global__ void __launch_bounds__(kResetThreads) reset_kernel(uint8_t* ws, uint64_t bytes) {
+  asm volatile("griddepcontrol.launch_dependents;");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (__ldcg(&reinterpret_cast<const Control*>(ws)->fallback) == 0) return;
+  uint4* w = reinterpret_cast<uint4*>(ws);
+  const uint64_t keep = (kWsControlBytes - 16) / 16;  // the vector holding the fallback word
+  const uint64_t stride = static_cast<uint64_t>(gridDim.x) * kResetThreads;
+  for (uint64_t i = static_cast<uint64_t>(blockIdx.x) * kResetThreads + threadIdx.x; i < bytes / 16; i += stride)
+    if (i != keep) w[i] = make_uint4(0, 0, 0, 0);
+  if (blockIdx.x == 0 && threadIdx.x == 0 && (bytes & 15))  // an odd chunk count's last scan-state word
+    *reinterpret_cast<unsigned long long*>(ws + (bytes & ~uint64_t(15))) = 0;
+}
+
 // Dynamic shared memory of the encode kernel: the layout plus room to align it to 1024 bytes.
 constexpr int kEncodeSmemBytes = static_cast<int>(sizeof(EncodeSmem)) + 1024;
 static_assert(kEncodeSmemBytes <= 233472 / kCtasPerSm - 1024, "kCtasPerSm CTAs fit an SM's shared memory");
@@ -1173,7 +1373,7 @@ cudaError_t encode_occupancy(int* per_sm) {
 
 cudaError_t launch_encode(const uint16_t* in, uint64_t n, int base, uint8_t* out, unsigned long long* out_bytes,
                           uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream, uint64_t stall_chunk,
-                          unsigned spin_limit, uint16_t* loopback_values) {
+                          unsigned spin_limit, uint16_t* loopback_values, int mode) {
   Control* ctrl = reinterpret_cast<Control*>(ws);
   if (n == 0) {
     empty_stream_kernel<<<1, 1, 0, stream>>>(out, base, ctrl, out_bytes);
@@ -1193,6 +1393,8 @@ cudaError_t launch_encode(const uint16_t* in, uint64_t n, int base, uint8_t* out
   p.spin_limit = spin_limit;
   p.full_chunks = n / kChunk;
   p.values = loopback_values;
+  p.mode = mode;
+  p.partials = reinterpret_cast<StatsPartial*>(ws + kWsControlBytes);
   CUtensorMap map;
   cudaError_t err = input_map(in, n, &map);
   if (err != cudaSuccess) return err;
@@ -1202,6 +1404,7 @@ cudaError_t launch_encode(const uint16_t* in, uint64_t n, int base, uint8_t* out
   uint64_t grid = static_cast<uint64_t>(per_sm > 0 ? per_sm : 1) * dev.sm_count;
   if (grid > p.N + 1) grid = p.N + 1;  // one CTA scans, the others code
   if (grid < 2) grid = 2;
+  if (grid > kStatsMaxCtas) grid = kStatsMaxCtas;  // a statistics slot per CTA (speculative mode)
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
   cfg.blockDim = dim3(kThreads);
@@ -1215,8 +1418,29 @@ cudaError_t launch_encode(const uint16_t* in, uint64_t n, int base, uint8_t* out
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = base < 0 ? 1 : 0;
-  TimingRecord t = timing_begin(ZC_KERNEL_ENCODE, stream);
+  TimingRecord t = timing_begin(mode == kSpeculative ? ZC_KERNEL_ENCODE_SPEC : ZC_KERNEL_ENCODE, stream);
   err = cudaLaunchKernelEx(&cfg, encode_kernel, p, map);
+  timing_end(t, stream);
+  return err;
+}
+
+cudaError_t launch_reset(uint64_t n, uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream) {
+  static_assert(workspace_bytes(0) % 16 == 0 && kWsControlBytes % 16 == 0, "whole vectors, but for the last word");
+  const uint64_t bytes = workspace_bytes(n);
+  uint64_t grid = (bytes / 16 + kResetThreads - 1) / kResetThreads;
+  const uint64_t cap = 2ull * dev.sm_count;
+  if (grid > cap) grid = cap;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kResetThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // after our own encode kernel
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  TimingRecord t = timing_begin(ZC_KERNEL_RESET, stream);
+  const cudaError_t err = cudaLaunchKernelEx(&cfg, reset_kernel, ws, bytes);
   timing_end(t, stream);
   return err;
 }
@@ -1242,6 +1466,24 @@ cudaError_t launch_raw_form(const uint16_t* in, uint64_t n, int base, uint8_t* o
   const cudaError_t err = cudaLaunchKernelEx(&cfg, raw_form_kernel, in, n, base, out,
                                              reinterpret_cast<Control*>(ws), out_bytes);
   timing_end(t, stream);
+  return err;
+}
+
+// The speculative path, after the workspace is cleared: the sample pass, the speculative coding
+// pass, then -- each a programmatic dependent launch that returns at once unless the fallback
+// word is set -- the reset, the statistics kernel, the encode kernel; then the raw-form step.
+cudaError_t launch_speculative(const uint16_t* in, uint64_t n, uint8_t* out, unsigned long long* out_bytes,
+                               uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream) {
+  cudaError_t err = launch_sample(in, n, ws, stream);
+  if (err == cudaSuccess)
+    err = launch_encode(in, n, ZC_BASE_AUTO, out, out_bytes, ws, dev, stream, ~uint64_t(0), kDefaultSpinLimit,
+                        nullptr, kSpeculative);
+  if (err == cudaSuccess) err = launch_reset(n, ws, dev, stream);
+  if (err == cudaSuccess) err = launch_stats(in, n, ws, dev, stream, true, true);
+  if (err == cudaSuccess)
+    err = launch_encode(in, n, ZC_BASE_AUTO, out, out_bytes, ws, dev, stream, ~uint64_t(0), kDefaultSpinLimit,
+                        nullptr, kGated);
+  if (err == cudaSuccess) err = launch_raw_form(in, n, ZC_BASE_AUTO, out, out_bytes, ws, dev, stream);
   return err;
 }
 

@@ -91,26 +91,29 @@ __device__ __forceinline__ uint32_t max_u16x2(uint32_t a, uint32_t b) {
   return d;
 }
 
-// Block sum of 64 values (this lane's block, 32 words; `w` is consumed).  Bit patterns with the
-// sign cleared order like magnitudes, so one packed 16-bit max finds the block's largest, and it
-// decides, per warp, between the plain sum (every lane's largest biased exponent in [87, 187): no
-// square reaches 2^122 and the block sum is at least 2^-80, so the 64 squares, 17 roundings, stay
-// within 2^-19 of the exact sum) and a sum with every lane's values scaled by 2^(126 - Es), Es = E
-// clamped to [1, 252] (1 for lanes that need no scaling), which puts the largest magnitude in
-// [2^-8, 4): no square overflows and what underflows is under 2^-120 of the block sum.  The
-// decision is one warp vote, so a warp runs one of the two loops.  A lane whose block holds Inf
-// or NaN (its largest pattern is at or above 0x7F80) first counts them and clears them to zero,
-// which adds nothing to the sum, and takes the largest of the rest; its warp then sums scaled.
-__device__ __forceinline__ void block_sum(uint32_t (&w)[32], double* acc, unsigned* nonfinite) {
+// Block sum of 2W values (this lane's block, W = 32 or 16 words; `w` is consumed).  Bit
+// patterns with the sign cleared order like magnitudes, so one packed 16-bit max finds the
+// block's largest, and it decides, per warp, between the plain sum (every lane's largest biased
+// exponent in [87, 187): no square reaches 2^122 and the block sum is at least 2^-80, so the at
+// most 64 squares, at most 17 roundings, stay within 2^-19 of the exact sum) and a sum with every
+// lane's values scaled by 2^(126 - Es), Es = E clamped to [1, 252] (1 for lanes that need no
+// scaling), which puts the largest magnitude in [2^-8, 4): no square overflows and what
+// underflows is under 2^-120 of the block sum.  The decision is one warp vote, so a warp runs one
+// of the two loops (every lane of the warp must call).  A lane whose block holds Inf or NaN (its
+// largest pattern is at or above 0x7F80) first counts them and clears them to zero, which adds
+// nothing to the sum, and takes the largest of the rest; its warp then sums scaled.
+template <int W>
+__device__ __forceinline__ void block_sum(uint32_t (&w)[W], double* acc, unsigned* nonfinite) {
+  static_assert(W == 32 || W == 16, "blocks of 64 or 32 values");
   uint32_t mx = 0;
 #pragma unroll
-  for (int i = 0; i < 32; ++i) mx = max_u16x2(mx, w[i] & 0x7FFF7FFFu);
+  for (int i = 0; i < W; ++i) mx = max_u16x2(mx, w[i] & 0x7FFF7FFFu);
   unsigned m = max(mx & 0xFFFFu, mx >> 16);
   bool odd = m != 0 && (m >> 7 >= 187u || m >> 7 < 87u);  // Inf and NaN included (E = 255)
   float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
   if (!__any_sync(0xFFFFFFFFu, odd)) {
 #pragma unroll
-    for (int i = 0; i < 32; i += 2) {
+    for (int i = 0; i < W; i += 2) {
       const float l0 = __uint_as_float(w[i] << 16), h0 = __uint_as_float(w[i] & 0xFFFF0000u);
       const float l1 = __uint_as_float(w[i + 1] << 16), h1 = __uint_as_float(w[i + 1] & 0xFFFF0000u);
       a0 = fmaf(l0, l0, a0);
@@ -127,7 +130,7 @@ __device__ __forceinline__ void block_sum(uint32_t (&w)[32], double* acc, unsign
     unsigned nf = 0;
     mx = 0;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
+    for (int i = 0; i < W; ++i) {
       const uint32_t t = ((w[i] & 0x7FFF7FFFu) + 0x00800080u) & 0x80008000u;  // bit 15 of each non-finite half
       nf += __popc(t);
       w[i] &= ~(t | (t - (t >> 15)));  // clear those halves
@@ -140,7 +143,7 @@ __device__ __forceinline__ void block_sum(uint32_t (&w)[32], double* acc, unsign
   const int Es = odd ? min(max(static_cast<int>(m >> 7), 1), 252) : 126;
   const float sc = __int_as_float((253 - Es) << 23);
 #pragma unroll
-  for (int i = 0; i < 32; i += 2) {
+  for (int i = 0; i < W; i += 2) {
     const float l0 = __uint_as_float(w[i] << 16) * sc, h0 = __uint_as_float(w[i] & 0xFFFF0000u) * sc;
     const float l1 = __uint_as_float(w[i + 1] << 16) * sc, h1 = __uint_as_float(w[i + 1] & 0xFFFF0000u) * sc;
     a0 = fmaf(l0, l0, a0);

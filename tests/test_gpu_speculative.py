@@ -1,0 +1,160 @@
+"""The speculative path (auto mode, tensors above the single-launch sizes), against the oracle,
+through the C ABI.
+
+A sample pass takes one 16-byte vector of every full chunk -- the vector (37 c + 11) mod 512 of
+chunk c -- and guesses e0 from it; the encode kernel codes with the guess while it sums the
+squares of every value exactly as the statistics kernel does, and the CTA whose chunks complete
+the count applies the rule to the whole tensor's sum.  When the rule settles the guessed e0 the
+stream is final; otherwise (or when the sample is not confident) the fallback word is set and
+the statistics and encode kernels redo the job.  Every stream must equal the oracle's byte for
+byte whichever way it went; the fallback word (the control block's bytes 240..243, at the start
+of the workspace in the tail of `out`) tells which way that was.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from lossless_bf16_compression_gb300 import binding as zc
+from lossless_bf16_compression_gb300 import workloads
+
+from gpu_helpers import require_gpu, to_device
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+SINGLE_MAX = 1 << 25  # the largest tensor that compresses in one launch on a GB300
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    require_gpu()
+
+
+def ctrl_word(out, n, offset):
+    ws = (zc.zc_max_stream_bytes(n) + 255) // 256 * 256
+    return int(out[ws + offset:ws + offset + 4].cpu().numpy().view(np.uint32)[0])
+
+
+def compress_checked(x, base=-1):
+    """(stream, kernels run, fallback word): the stream equal to the oracle's, decoded back."""
+    xd = to_device(x)
+    zc.zc_timing_enable(1)
+    zc.zc_timing_collect()
+    try:
+        zc.status(reset=True)
+        out, ob = zc.compress(xd, base)
+        st = zc.status(reset=True)
+        kernels = [k for k, _ in zc.zc_timing_collect()]
+    finally:
+        zc.zc_timing_enable(0)
+    assert st == zc.ZC_OK, zc.ERROR_NAMES.get(st, st)
+    total = int(ob.item())
+    stream = out[:total].cpu().numpy()
+    want = oracle.compress(x, base)
+    assert stream[7] == want[7], f"e0 {stream[7]} vs oracle {want[7]}"
+    assert stream.size == want.size, f"length {stream.size} vs oracle {want.size}"
+    if stream.tobytes() != want.tobytes():
+        diff = np.flatnonzero(stream != want)
+        pytest.fail(f"stream differs from the oracle at {diff.size} bytes, first at {diff[0]}")
+    back = zc.decompress(out, x.size)
+    assert zc.status(reset=True) == zc.ZC_OK
+    assert bool(torch.equal(back, xd))
+    return stream, kernels, ctrl_word(out, x.size, 240)
+
+
+def sampled_positions(n):
+    """Start of the sampled vector of every full chunk."""
+    c = np.arange(n // 4096, dtype=np.int64)
+    return 4096 * c + 8 * ((37 * c + 11) % 512)
+
+
+def gaussian(n, seed, sigma=1.0):
+    rng = np.random.default_rng(seed)
+    return workloads.fp32_to_bf16_bits((rng.standard_normal(n) * sigma).astype(np.float32))
+
+
+SPEC_KERNELS = [zc.ZC_KERNEL_SAMPLE, zc.ZC_KERNEL_ENCODE_SPEC, zc.ZC_KERNEL_RESET, zc.ZC_KERNEL_STATS,
+                zc.ZC_KERNEL_ENCODE, zc.ZC_KERNEL_RAW]
+
+
+@pytest.mark.parametrize("n", [SINGLE_MAX + 1, SINGLE_MAX + 3 * 4096 + 5, 40_000_001, 3 * SINGLE_MAX])
+def test_guess_holds(n):
+    s, kernels, fallback = compress_checked(gaussian(n, n % 1000))
+    assert kernels == SPEC_KERNELS
+    assert fallback == 0 and s[6] == 12 and s[7] == 122
+
+
+def test_gradient_bucket_is_not_speculated():
+    """0.1% of the values are 100x the rest and make most of the sum of squares: a sample of one
+    value in 512 estimates it with a relative standard error of about 14%, too wide around the
+    tensor's e0 (114; the sample's own is 113), so the sample pass turns the speculation off."""
+    x = workloads.make("grad_bucket_4096x14336")
+    s, _, fallback = compress_checked(x)
+    assert fallback == 1 and s[6] == 12 and s[7] == 114
+
+
+def test_guess_wrong_falls_back_to_the_coded_form():
+    """The sampled vectors are scaled by 1/4: the sample's e0 is 120, the tensor's 122.  The coding
+    pass codes with 120, its own sums settle 122, and the statistics and encode kernels redo it."""
+    n = SINGLE_MAX + 4096 * 11 + 3
+    x = gaussian(n, 7).view(np.uint16).copy()
+    pos = sampled_positions(n)
+    idx = (pos[:, None] + np.arange(8)[None, :]).ravel()
+    v = (x[idx].astype(np.uint32) << 16).view(np.float32) * np.float32(0.25)
+    x[idx] = workloads.fp32_to_bf16_bits(v)
+    assert oracle.choose_e0(x) == 122
+    s, _, fallback = compress_checked(x)
+    assert fallback == 1 and s[6] == 12 and s[7] == 122
+
+
+def test_guess_wrong_falls_back_to_the_raw_form():
+    """One huge value outside the sample: the tensor's e0 is far above the sample's, almost every
+    value escapes, and the stream is raw."""
+    n = SINGLE_MAX + 77
+    x = gaussian(n, 8)
+    x[1] = workloads.fp32_to_bf16_bits(np.array([1e20], np.float32))[0]
+    s, _, fallback = compress_checked(x)
+    assert fallback == 1 and s[6] == 0
+
+
+def test_sample_not_confident_on_random_patterns():
+    """A sample that predicts a raw stream turns the speculation off before any coding."""
+    n = SINGLE_MAX + 4096
+    s, _, fallback = compress_checked(workloads.random_patterns(n, 3))
+    assert fallback == 1 and s[6] == 0
+
+
+def test_nonfinite_values_in_the_speculative_sums():
+    n = SINGLE_MAX + 999
+    x = gaussian(n, 9)
+    x[::97] = 0x7FC0   # NaN
+    x[5::4096] = 0xFF80  # -Inf
+    s, _, fallback = compress_checked(x)
+    assert fallback == 0 and s[6] == 12
+
+
+def test_supplied_base_takes_no_speculation():
+    x = gaussian(SINGLE_MAX + 5, 10)
+    s, kernels, _ = compress_checked(x, base=122)
+    assert kernels == [zc.ZC_KERNEL_ENCODE, zc.ZC_KERNEL_RAW]
+
+
+def test_static_scratch_entry_takes_the_speculative_path():
+    x = gaussian(SINGLE_MAX + 4096 + 1, 11)
+    xd = to_device(x)
+    out = torch.zeros(zc.zc_max_stream_bytes(x.size), dtype=torch.uint8, device="cuda")
+    ob = torch.zeros(1, dtype=torch.int64, device="cuda")
+    zc.zc_timing_enable(1)
+    zc.zc_timing_collect()
+    try:
+        zc.status(reset=True)
+        s = torch.cuda.current_stream().cuda_stream
+        assert zc.zc_compress_static_scratch(xd.data_ptr(), x.size, zc.ZC_BASE_AUTO, out.data_ptr(),
+                                             ob.data_ptr(), s) == 0
+        assert zc.status(reset=True) == zc.ZC_OK
+        kernels = [k for k, _ in zc.zc_timing_collect()]
+    finally:
+        zc.zc_timing_enable(0)
+    assert kernels == SPEC_KERNELS
+    total = int(ob.item())
+    assert out[:total].cpu().numpy().tobytes() == oracle.compress(x).tobytes()
