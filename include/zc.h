@@ -184,9 +184,9 @@ int zc_status(cudaStream_t stream, int reset);
 #define ZC_KERNEL_SMALL 5  /* the single launch that compresses a tensor of up to 64 chunks */
 #define ZC_KERNEL_MEDIUM 6 /* the single cooperative launch that compresses a medium tensor */
 #define ZC_KERNEL_FUSED 7  /* the single cooperative launch for a tensor of up to 2^25 values */
-#define ZC_KERNEL_SAMPLE 8 /* larger tensors, auto mode: the sample pass that guesses e0 */
-#define ZC_KERNEL_ENCODE_SPEC 9 /* ... the coding pass with the guessed e0, summing the squares */
-#define ZC_KERNEL_RESET 10 /* ... the reset of the workspace when the guess did not hold */
+#define ZC_KERNEL_REFIT_STATS 8  /* larger tensors, auto mode: the statistics pass after the
+                                    encode kernel's guess of e0 was not trusted or did not hold */
+#define ZC_KERNEL_REFIT_ENCODE 9 /* ... and the encode kernel again, after it */
 
 /* enable != 0: bracket every kernel the library launches from now on with CUDA events on the
  * kernel's own stream.  enable == 0: stop recording.  Returns ZC_OK or ZC_ERR_CUDA. */

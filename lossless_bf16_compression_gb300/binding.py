@@ -30,9 +30,8 @@ ZC_KERNEL_RAW = 4
 ZC_KERNEL_SMALL = 5
 ZC_KERNEL_MEDIUM = 6
 ZC_KERNEL_FUSED = 7
-ZC_KERNEL_SAMPLE = 8
-ZC_KERNEL_ENCODE_SPEC = 9
-ZC_KERNEL_RESET = 10
+ZC_KERNEL_REFIT_STATS = 8
+ZC_KERNEL_REFIT_ENCODE = 9
 
 ERROR_NAMES = {
     ZC_OK: "ZC_OK",

@@ -113,19 +113,16 @@ struct Control {
   int grid_e0;              // ... the window base, and 1 when the exact sums must decide it
   unsigned grid_exact;
   unsigned long long grid_escape_bytes;  // ... the escape sections' bytes, all chunks
-  // The speculative path: the sample pass's guess of e0 and its sums, and the coding pass's
-  // verdict on the guess.
-  double sample_sum;             // sum of squares of the sample's finite values
-  unsigned long long sample_finite;  // ... and their number
-  unsigned sample_done;          // sample CTAs finished
-  int e0_guess;                  // e0 of the sample, which the speculative coding pass uses
-  unsigned spec_chunks;          // chunks the speculative coding pass has coded and summed
-  unsigned spec_untrusted;       // 1: a CTA had fewer than half of its values inside the window
-  double sample_sum4;            // sum of fourth powers of the sample's finite values
-  unsigned reserved[18];
-  // 1: the speculation is off (the sample was not confident) or wrong (the coding pass's own
-  // sums settle another e0, or none): the pipeline of the statistics and encode kernels runs.
-  // Alone in the last 16 bytes, which the reset step keeps.
+  // The speculative encode kernel: its sums of squares and Inf/NaN counts (added by each CTA
+  // as it leaves), the chunks they cover, and a CTA's report that too few of its values were
+  // inside the window for its fast sums to be trusted.
+  double spec_sum;
+  unsigned long long spec_nonfinite;
+  unsigned spec_chunks;
+  unsigned spec_untrusted;
+  unsigned reserved[22];
+  // 1: the speculative encode kernel did not speculate (its sample was not confident) or found
+  // its guess wrong: the statistics and encode kernels after it do the job.
   unsigned fallback;
   unsigned fallback_pad[3];
 };
@@ -357,19 +354,19 @@ void timing_end(TimingRecord& rec, cudaStream_t stream);
 // `out` for zc_compress, the library's static array for zc_compress_static_scratch.
 // predict_raw: also sample the exponents and, when the sample predicts that the coded stream
 // will be longer than the raw form, have the encode kernel take the raw pass first.
-// gated: after the speculative path (below), run only when it fell back.
+// gated: after the speculative encode kernel (below), run only when it fell back.
 cudaError_t launch_stats(const uint16_t* in, uint64_t n, uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream,
                          bool predict_raw, bool gated = false);
-// mode: 0 plain, 1 speculative, 2 gated (the encode kernel's kPlain, kSpeculative, kGated).
+// mode: 0 plain, 1 speculative unless the sample was not confident, 2 only when the speculation
+// fell back (the encode kernel's kPlain, kSpeculative, kGated).
 cudaError_t launch_encode(const uint16_t* in, uint64_t n, int base, uint8_t* out, unsigned long long* out_bytes,
                           uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream, uint64_t stall_chunk,
                           unsigned spin_limit, uint16_t* loopback_values = nullptr, int mode = 0);
-// The speculative path (auto mode, tensors above the single-launch sizes): the sample pass guesses
-// e0; the encode kernel codes with it and checks it; when the guess did not hold (or the sample was
-// not confident) the reset step clears the workspace and the statistics and encode kernels, gated
-// on the fallback word, do the job as they do without the speculation.
-cudaError_t launch_sample(const uint16_t* in, uint64_t n, uint8_t* ws, cudaStream_t stream);
-cudaError_t launch_reset(uint64_t n, uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream);
+// The speculative path (auto mode, tensors above the single-launch sizes): the encode kernel
+// guesses e0 from a sample (every CTA the same guess), codes with it and checks it against the
+// whole tensor's sum of squares, which it takes as it codes; when the sample was not confident or
+// the guess did not hold, the statistics and encode kernels after it, gated on the fallback
+// word, do the job as they do without the speculation.
 cudaError_t launch_speculative(const uint16_t* in, uint64_t n, uint8_t* out, unsigned long long* out_bytes,
                                uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream);
 cudaError_t launch_decode(const uint8_t* in, uint16_t* out, uint64_t n, const DeviceInfo& dev,

@@ -82,11 +82,14 @@ static_assert(kLoopbackDecoders < kLoopbackCycle - 1, "the first CTA after the s
 constexpr int kCoderWarps = kCoders / 32;
 constexpr unsigned kScanPerWarp = 32 * kScanPerLane;
 // Launch modes.  kPlain: e0 supplied, or (auto) read from the statistics kernel before it.
-// kSpeculative: code with the sample pass's e0 and sum the squares while coding; the CTA whose
-// chunks complete the count checks that e0 against the exact rule on the whole tensor's sum and
-// sets the fallback word when it differs (or cannot be settled).  kGated: after the speculative
-// path; runs as kPlain (auto) only when the fallback word is set, else returns at once.
+// kSpeculative (auto, first after the workspace is cleared): every CTA takes the same sample and
+// guesses e0 from it (spec_guess); when the guess is confident, code with it and sum the squares
+// while coding -- the CTA whose chunks complete the count checks the guess against the exact
+// rule on the whole tensor's sum and sets the fallback word when it differs (or cannot be
+// settled); when it is not, set the fallback word and leave.  kGated: after the gated
+// statistics kernel; runs as kPlain (auto) only when the fallback word is set, else returns.
 constexpr int kPlain = 0, kSpeculative = 1, kGated = 2;
+static_assert(kPlain == 0, "launch_encode's default mode is kPlain");
 
 struct EncodeParams {
   const uint16_t* in;
@@ -103,7 +106,6 @@ struct EncodeParams {
   uint64_t full_chunks;  // n / 4096: chunks that come by one tiled copy each
   uint16_t* values;      // loopback: the decoded values (n x u16); null for compression alone
   int mode;              // kPlain, kSpeculative or kGated
-  StatsPartial* partials;  // speculative: one slot per CTA for its sums
 };
 
 struct __align__(128) EncodeSmem {
@@ -142,6 +144,13 @@ struct __align__(128) EncodeSmem {
   double spec_sum[kCoderWarps];
   unsigned long long spec_nf[kCoderWarps], spec_values[kCoderWarps], spec_inside[kCoderWarps];
   int spec_last;
+  int spec;       // this launch speculates (kSpeculative, and the sample was confident)
+  // the sample's per-warp sums (scaled by 2^(126 - Es)), finite counts and escapes under the guess
+  float g2[kCoderWarps], g4[kCoderWarps];
+  int gk[kCoderWarps];
+  unsigned gf[kCoderWarps], gesc[kCoderWarps];
+  int guess;
+  int confident;
   int e_end[2];
 };
 
@@ -905,12 +914,132 @@ __device__ __forceinline__ void spec_square_sum(const uint4 (&xv)[4], bool fast,
   }
 }
 
-// Speculative mode, the coding threads of a CTA after its last chunk: the CTA's sums go to its
-// slot, and its chunks to the count.  The CTA whose chunks complete the count (an acquire-release
-// add tells it; every other coding CTA has published its slot before its own add) sums all the
-// slots, applies the rule exactly as the statistics kernel does (decide_e0, one end per thread),
-// and sets the fallback word unless the rule settles the e0 the chunks were coded with.  A CTA
-// that took no chunk publishes nothing.  Slots are per CTA, cleared with the workspace.
+// Speculative mode, the coding threads of every CTA before anything else: the guess of e0 and
+// whether to trust it, from a fixed sample -- 512 chunks spread evenly over the tensor, chunk c
+// giving its vector (37 c + 11) mod 512 (8 values), four vectors per thread -- which every CTA
+// reads and reduces in the same order, so all reach the same guess and the same verdict without
+// a word between them (after the first CTA the sample comes from the L2).  Squares and fourth
+// powers in fp32, scaled by a power of two from the warp's largest magnitude; the rule's e0 at
+// the sample's mean square (in fp32, the binary exponent taken out first) and at that times
+// 1 -+ (4 r + 1/32), r the mean square's relative standard error estimated from the fourth
+// powers.  Confident when the three agree, the sample has a finite nonzero value, and the stream
+// the sample predicts under the guess (the fixed parts plus min(3p, 1) bytes per value, p its
+// share of escapes) is shorter than 0.95 of the raw form.  A tensor near a switching point, one
+// whose sum of squares a few large values dominate, and one that may come out raw go the safe
+// way.  Leaves S.guess and S.confident.
+#ifndef ZC_GUESS_VECTORS
+#define ZC_GUESS_VECTORS 4
+#endif
+constexpr int kGuessVectors = ZC_GUESS_VECTORS;  // sampled vectors per coding thread: 512 chunks, 4096 values
+
+__device__ __noinline__ void spec_guess(EncodeSmem& S, const EncodeParams& p) {
+  const unsigned tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint4* in = reinterpret_cast<const uint4*>(p.in);
+  const uint64_t full = p.full_chunks;
+  uint32_t w[4 * kGuessVectors];
+#pragma unroll
+  for (int h = 0; h < kGuessVectors; ++h) {  // all loads in flight at once
+    const uint64_t c = (static_cast<uint64_t>(tid + kCoders * h) * full) / (kCoders * kGuessVectors);
+    const uint4 v = __ldg(in + c * (kChunk / 8) + ((37 * c + 11) & (kChunk / 8 - 1)));
+    w[4 * h] = v.x;
+    w[4 * h + 1] = v.y;
+    w[4 * h + 2] = v.z;
+    w[4 * h + 3] = v.w;
+  }
+  constexpr int kVals = 8 * kGuessVectors;  // this thread's sampled values
+  unsigned mx = 0, nonfinite = 0;
+#pragma unroll
+  for (int i = 0; i < kVals; ++i) {
+    const unsigned a = (w[i >> 1] >> (16 * (i & 1))) & 0x7FFFu;
+    if (a >= 0x7F80u) ++nonfinite;
+    else mx = max(mx, a);
+  }
+  mx = __reduce_max_sync(0xFFFFFFFFu, mx);
+  const int Es = min(max(static_cast<int>(mx >> 7), 1), 252);
+  const float sc = __int_as_float((253 - Es) << 23);  // 2^(126 - Es)
+  float a2 = 0.f, a4 = 0.f, b2 = 0.f, b4 = 0.f;
+#pragma unroll
+  for (int i = 0; i < kVals; ++i) {
+    const uint32_t h = (w[i >> 1] >> (16 * (i & 1))) & 0xFFFFu;
+    const float x = (h & 0x7FFFu) >= 0x7F80u ? 0.f : __uint_as_float(h << 16) * sc;
+    const float x2 = x * x;
+    if (i & 1) {
+      b2 += x2;
+      b4 = fmaf(x2, x2, b4);
+    } else {
+      a2 += x2;
+      a4 = fmaf(x2, x2, a4);
+    }
+  }
+  float s2 = a2 + b2, s4 = a4 + b4;
+  unsigned fin = kVals - nonfinite;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    s2 += __shfl_xor_sync(0xFFFFFFFFu, s2, o);
+    s4 += __shfl_xor_sync(0xFFFFFFFFu, s4, o);
+    fin += __shfl_xor_sync(0xFFFFFFFFu, fin, o);
+  }
+  if (lane == 0) {
+    S.g2[warp] = s2;
+    S.g4[warp] = s4;
+    S.gk[warp] = Es - 126;
+    S.gf[warp] = fin;
+  }
+  bar_coders();
+  if (tid == 0) {
+    double Sd = 0.0, Qd = 0.0;  // the true sums: x^2 and x^4 times 2^(2k), 2^(4k)
+    unsigned m = 0;
+    for (int i = 0; i < kCoderWarps; ++i) {
+      Sd += static_cast<double>(S.g2[i]) * __longlong_as_double(static_cast<long long>(1023 + 2 * S.gk[i]) << 52);
+      Qd += static_cast<double>(S.g4[i]) * __longlong_as_double(static_cast<long long>(1023 + 4 * S.gk[i]) << 52);
+      m += S.gf[i];
+    }
+    int e_at[3] = {0, 0, 0};
+    bool conf = false;
+    if (m > 0 && Sd > 0.0) {
+      const int kS = ilogb_pos(Sd);  // Sd = Sn 2^kS, Sn in [1, 2)
+      const float Sn = static_cast<float>(Sd * __longlong_as_double(static_cast<long long>(1023 - kS) << 52));
+      const float Qn = static_cast<float>(Qd * __longlong_as_double(static_cast<long long>(1023 - 2 * kS) << 52));
+      const float fm = static_cast<float>(m);
+      const float d = fminf(1.0f / 32 + 4.0f * sqrtf(fmaxf(Qn / (Sn * Sn) * fm - 1.0f, 0.0f) / fm), 0.75f);
+      const float y = Sn / fm * static_cast<float>(kWindowC2);  // the rule's y, times 2^-kS
+#pragma unroll
+      for (int t = 0; t < 3; ++t) {
+        const float yt = y * (t == 0 ? 1.0f - d : t == 1 ? 1.0f : 1.0f + d);
+        const int e = floor_half(static_cast<int>((__float_as_uint(yt) >> 23) & 0xFF) - 127 + kS) + 127;
+        e_at[t] = e < 0 ? 0 : (e > kE0Max ? kE0Max : e);
+      }
+      conf = e_at[0] == e_at[1] && e_at[2] == e_at[1];
+    }
+    S.guess = e_at[1];
+    S.confident = conf;
+  }
+  bar_coders();
+  // the sample's escapes under the guess: the predicted stream must be clearly shorter than raw
+  const unsigned g = static_cast<unsigned>(S.guess);
+  unsigned esc = 0;
+#pragma unroll
+  for (int i = 0; i < kVals; ++i) esc += (((w[i >> 1] >> (16 * (i & 1) + 7)) & 0xFFu) - g) >= 7u;
+  esc = __reduce_add_sync(0xFFFFFFFFu, esc);
+  if (lane == 0) S.gesc[warp] = esc;
+  bar_coders();
+  if (tid == 0 && S.confident) {
+    unsigned e = 0;
+    for (int i = 0; i < kCoderWarps; ++i) e += S.gesc[i];
+    const float per_value = fminf(3.0f * static_cast<float>(e) / static_cast<float>(kVals * kCoders), 1.0f);
+    const double coded = static_cast<double>(escape_base(p.n)) + static_cast<double>(per_value) * static_cast<double>(p.n);
+    S.confident = coded < 0.95 * static_cast<double>(raw_stream_bytes(p.n));
+  }
+  bar_coders();
+}
+
+// Speculative mode, the coding threads of a CTA after its last chunk: the CTA's sums are added to
+// the control block's, and its chunks to the count.  The CTA whose chunks complete the count (an
+// acquire-release add tells it; every other coding CTA added its sums before its own count)
+// applies the rule to the total exactly as the statistics kernel does (decide_e0, one end per
+// thread), and sets the fallback word unless the rule settles the e0 the chunks were coded with.
+// The order of the additions varies from run to run; the rule's bound holds for every order, so
+// the e0 it settles does not.  A CTA that took no chunk adds nothing.
 __device__ __noinline__ void spec_verdict(EncodeSmem& S, const EncodeParams& p, int e0, double acc,
                                           unsigned nonfinite, unsigned chunks, bool fast,
                                           unsigned long long values, unsigned long long inside) {
@@ -944,8 +1073,8 @@ __device__ __noinline__ void spec_verdict(EncodeSmem& S, const EncodeParams& p, 
       // The plain fp32 squares are within the bound only for a CTA with at least half of its
       // values inside the window (spec_square_sum); otherwise the guess is not trusted.
       if (fast && 2 * in < v) p.ctrl->spec_untrusted = 1u;
-      p.partials[blockIdx.x].sum = s;
-      p.partials[blockIdx.x].nonfinite = c;
+      atomicAdd(&p.ctrl->spec_sum, s);
+      atomicAdd(&p.ctrl->spec_nonfinite, c);
       unsigned old;
       asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;"
                    : "=r"(old)
@@ -956,31 +1085,9 @@ __device__ __noinline__ void spec_verdict(EncodeSmem& S, const EncodeParams& p, 
   }
   bar_coders();
   if (!S.spec_last) return;
-  double a = 0.0;
-  unsigned long long b = 0;
-  for (unsigned q = tid; q < gridDim.x; q += kCoders) {
-    a += __ldcg(&p.partials[q].sum);
-    b += __ldcg(&p.partials[q].nonfinite);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    a += __shfl_xor_sync(0xFFFFFFFFu, a, o);
-    b += __shfl_xor_sync(0xFFFFFFFFu, b, o);
-  }
-  bar_coders();  // the slots of this CTA's warps are free again
-  if (lane == 0) {
-    S.spec_sum[warp] = a;
-    S.spec_nf[warp] = b;
-  }
-  bar_coders();
-  if (tid < 2) {
-    double S_all = 0.0;
-    unsigned long long nf_all = 0;
-    for (int i = 0; i < kCoderWarps; ++i) {
-      S_all += S.spec_sum[i];
-      nf_all += S.spec_nf[i];
-    }
-    const unsigned long long n_f = p.n - nf_all;
+  if (tid < 2) {  // every CTA's sums were added before its chunks were counted
+    const double S_all = __ldcg(&p.ctrl->spec_sum);
+    const unsigned long long n_f = p.n - __ldcg(&p.ctrl->spec_nonfinite);
     int e = 0;
     if (n_f != 0 && S_all != 0.0)
       e = select_e0(tid == 0 ? __dmul_rd(S_all, 1.0 - 0x1p-16) : __dmul_ru(S_all, 1.0 + 0x1p-16), n_f);
@@ -1004,8 +1111,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   asm volatile("griddepcontrol.launch_dependents;");
   const unsigned tid = threadIdx.x, warp = tid >> 5;
   if (p.mode == kGated) {
-    // After the speculative path: wait for the steps before (the speculative coding pass, the
-    // reset, the statistics kernel) and run only when the speculation fell back.
+    // After the speculative path: wait for the steps before (the speculative encode kernel, the
+    // gated statistics kernel) and run only when the speculation fell back.
     if (tid == 0) {
       asm volatile("griddepcontrol.wait;" ::: "memory");
       S.skip = __ldcg(&p.ctrl->fallback) == 0;
@@ -1023,21 +1130,21 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     S.freed = 0;
     S.coders_done = 0;
     S.skip = 0;
+    S.spec = 0;
   }
   __syncthreads();
   if (S.role == 0) {
     if (warp < kCoderWarps) {
-      if (p.base < 0) {  // auto mode: wait for the first phase, if there is one (it may leave the raw form)
+      if (p.mode == kSpeculative) {  // the same guess as the coding CTAs: nothing to scan without it
+        spec_guess(S, p);
+        if (!S.confident) return;
+      } else if (p.base < 0) {  // auto mode: wait for the first phase, if there is one (it may leave the raw form)
         if (tid == 0) {
           asm volatile("griddepcontrol.wait;" ::: "memory");
           bool ok = true;
-          if (p.mode == kSpeculative) {  // the sample pass may have turned the speculation off
-            S.skip = __ldcg(&p.ctrl->fallback) != 0;
-          } else {
-            if (__ldcg(&p.ctrl->exact_path) != 0 || __ldcg(&p.ctrl->raw_predicted) != 0)
-              ok = wait_first_ready(p.ctrl, p.status, p.spin_limit);
-            S.skip = !ok || __ldcg(&p.ctrl->raw_done) != 0;
-          }
+          if (__ldcg(&p.ctrl->exact_path) != 0 || __ldcg(&p.ctrl->raw_predicted) != 0)
+            ok = wait_first_ready(p.ctrl, p.status, p.spin_limit);
+          S.skip = !ok || __ldcg(&p.ctrl->raw_done) != 0;
         }
         bar_coders();
         if (S.skip) return;
@@ -1089,22 +1196,25 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     // e0 last.  In auto mode this kernel may start while the statistics kernel is finishing
     // (a programmatic dependent launch): the tickets and input copies above do not depend on
     // it, e0 does, so wait for that kernel's completion and writes first.
-    if (p.base < 0) asm volatile("griddepcontrol.wait;" ::: "memory");
+    if (p.base < 0 && p.mode != kSpeculative) asm volatile("griddepcontrol.wait;" ::: "memory");
     S.kind = p.base >= 0 || p.mode == kSpeculative ? 0
              : __ldcg(&p.ctrl->exact_path) != 0    ? 1
              : __ldcg(&p.ctrl->raw_predicted) != 0 ? 2
                                                    : 0;
   }
   bar_coders();
+  if (p.mode == kSpeculative) spec_guess(S, p);  // (meanwhile the first chunks arrive)
   const bool first_ok =
       S.kind == 0 ||
       first_phase(S, p.in, p.n, p.N, p.out, p.out_bytes, p.ctrl,
                   reinterpret_cast<unsigned long long*>(reinterpret_cast<uint8_t*>(p.ctrl) + kWsExactBinsOffset),
                   p.status, p.spin_limit, S.kind);
   if (tid == 0) {
-    if (p.mode == kSpeculative) {  // the sample's e0; off when the sample pass turned the speculation off
-      S.e0 = __ldcg(&p.ctrl->e0_guess);
-      S.skip = __ldcg(&p.ctrl->fallback) != 0;
+    if (p.mode == kSpeculative) {  // the sample's e0, if it is trusted; else the kernels after this one
+      S.spec = S.confident;
+      S.e0 = S.guess;
+      S.skip = !S.confident;
+      if (!S.confident) p.ctrl->fallback = 1u;
     } else {
       S.e0 = p.base >= 0 ? p.base : __ldcg(&p.ctrl->e0);
       S.skip = !first_ok || (p.base < 0 && __ldcg(&p.ctrl->raw_done) != 0);
@@ -1113,7 +1223,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   bar_coders();
   const int e0 = S.e0;
   const bool skip = S.skip != 0;  // nothing to code (raw form written, or a failed wait): drain the copies and leave
-  const bool speculative = p.mode == kSpeculative;
+  const bool speculative = S.spec != 0;
   const bool spec_fast = e0 >= kFastE0Min && e0 <= kFastE0Max;  // the plain fp32 squares (spec_square_sum)
   double spec_acc = 0.0;          // speculative: this thread's sum of squares (fp32 blocks of 32 values)
   unsigned spec_nonfinite = 0;    // ... and its Inf and NaN
@@ -1304,24 +1414,6 @@ __global__ void __launch_bounds__(kRawThreads) raw_form_kernel(const uint16_t* i
   }
 }
 
-// After the speculative coding pass, as a programmatic dependent launch: when the guess did not
-// hold, the workspace goes back to zero (all but the control block's last 16 bytes, which hold the
-// fallback word) for the statistics and encode kernels that follow; otherwise every CTA returns.
-constexpr int kResetThreads = 256;
-
-__global__ void __launch_bounds__(kResetThreads) reset_kernel(uint8_t* ws, uint64_t bytes) {
-  asm volatile("griddepcontrol.launch_dependents;");
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  if (__ldcg(&reinterpret_cast<const Control*>(ws)->fallback) == 0) return;
-  uint4* w = reinterpret_cast<uint4*>(ws);
-  const uint64_t keep = (kWsControlBytes - 16) / 16;  // the vector holding the fallback word
-  const uint64_t stride = static_cast<uint64_t>(gridDim.x) * kResetThreads;
-  for (uint64_t i = static_cast<uint64_t>(blockIdx.x) * kResetThreads + threadIdx.x; i < bytes / 16; i += stride)
-    if (i != keep) w[i] = make_uint4(0, 0, 0, 0);
-  if (blockIdx.x == 0 && threadIdx.x == 0 && (bytes & 15))  // an odd chunk count's last scan-state word
-    *reinterpret_cast<unsigned long long*>(ws + (bytes & ~uint64_t(15))) = 0;
-}
-
 // Dynamic shared memory of the encode kernel: the layout plus room to align it to 1024 bytes.
 constexpr int kEncodeSmemBytes = static_cast<int>(sizeof(EncodeSmem)) + 1024;
 static_assert(kEncodeSmemBytes <= 233472 / kCtasPerSm - 1024, "kCtasPerSm CTAs fit an SM's shared memory");
@@ -1394,7 +1486,6 @@ cudaError_t launch_encode(const uint16_t* in, uint64_t n, int base, uint8_t* out
   p.full_chunks = n / kChunk;
   p.values = loopback_values;
   p.mode = mode;
-  p.partials = reinterpret_cast<StatsPartial*>(ws + kWsControlBytes);
   CUtensorMap map;
   cudaError_t err = input_map(in, n, &map);
   if (err != cudaSuccess) return err;
@@ -1404,7 +1495,6 @@ cudaError_t launch_encode(const uint16_t* in, uint64_t n, int base, uint8_t* out
   uint64_t grid = static_cast<uint64_t>(per_sm > 0 ? per_sm : 1) * dev.sm_count;
   if (grid > p.N + 1) grid = p.N + 1;  // one CTA scans, the others code
   if (grid < 2) grid = 2;
-  if (grid > kStatsMaxCtas) grid = kStatsMaxCtas;  // a statistics slot per CTA (speculative mode)
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(grid));
   cfg.blockDim = dim3(kThreads);
@@ -1417,30 +1507,9 @@ cudaError_t launch_encode(const uint16_t* in, uint64_t n, int base, uint8_t* out
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = base < 0 ? 1 : 0;
-  TimingRecord t = timing_begin(mode == kSpeculative ? ZC_KERNEL_ENCODE_SPEC : ZC_KERNEL_ENCODE, stream);
+  cfg.numAttrs = base < 0 && mode != kSpeculative ? 1 : 0;  // (the speculative launch follows the memset)
+  TimingRecord t = timing_begin(mode == kGated ? ZC_KERNEL_REFIT_ENCODE : ZC_KERNEL_ENCODE, stream);
   err = cudaLaunchKernelEx(&cfg, encode_kernel, p, map);
-  timing_end(t, stream);
-  return err;
-}
-
-cudaError_t launch_reset(uint64_t n, uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream) {
-  static_assert(workspace_bytes(0) % 16 == 0 && kWsControlBytes % 16 == 0, "whole vectors, but for the last word");
-  const uint64_t bytes = workspace_bytes(n);
-  uint64_t grid = (bytes / 16 + kResetThreads - 1) / kResetThreads;
-  const uint64_t cap = 2ull * dev.sm_count;
-  if (grid > cap) grid = cap;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(grid));
-  cfg.blockDim = dim3(kResetThreads);
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // after our own encode kernel
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  TimingRecord t = timing_begin(ZC_KERNEL_RESET, stream);
-  const cudaError_t err = cudaLaunchKernelEx(&cfg, reset_kernel, ws, bytes);
   timing_end(t, stream);
   return err;
 }
@@ -1469,16 +1538,13 @@ cudaError_t launch_raw_form(const uint16_t* in, uint64_t n, int base, uint8_t* o
   return err;
 }
 
-// The speculative path, after the workspace is cleared: the sample pass, the speculative coding
-// pass, then -- each a programmatic dependent launch that returns at once unless the fallback
-// word is set -- the reset, the statistics kernel, the encode kernel; then the raw-form step.
+// The speculative path, after the workspace is cleared: the encode kernel, speculating; then --
+// each a programmatic dependent launch that returns at once unless the fallback word is set --
+// the statistics kernel and the encode kernel again; then the raw-form step.
 cudaError_t launch_speculative(const uint16_t* in, uint64_t n, uint8_t* out, unsigned long long* out_bytes,
                                uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream) {
-  cudaError_t err = launch_sample(in, n, ws, stream);
-  if (err == cudaSuccess)
-    err = launch_encode(in, n, ZC_BASE_AUTO, out, out_bytes, ws, dev, stream, ~uint64_t(0), kDefaultSpinLimit,
-                        nullptr, kSpeculative);
-  if (err == cudaSuccess) err = launch_reset(n, ws, dev, stream);
+  cudaError_t err = launch_encode(in, n, ZC_BASE_AUTO, out, out_bytes, ws, dev, stream, ~uint64_t(0),
+                                  kDefaultSpinLimit, nullptr, kSpeculative);
   if (err == cudaSuccess) err = launch_stats(in, n, ws, dev, stream, true, true);
   if (err == cudaSuccess)
     err = launch_encode(in, n, ZC_BASE_AUTO, out, out_bytes, ws, dev, stream, ~uint64_t(0), kDefaultSpinLimit,

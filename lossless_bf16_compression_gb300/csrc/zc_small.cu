@@ -164,10 +164,6 @@ struct GridExchange {
     partials[blockIdx.x].sum = s;
     partials[blockIdx.x].nonfinite = nf;
   }
-  __device__ void get_partial(ResidentSmem&, unsigned q, double* s, unsigned long long* nf) {
-    *s = __ldcg(&partials[q].sum);
-    *nf = __ldcg(&partials[q].nonfinite);
-  }
   __device__ void share_bins(ResidentSmem& S) {
     for (unsigned e = threadIdx.x; e < 256; e += kSmallThreads)
       if (S.bins[e]) atomicAdd(bins + e, S.bins[e]);

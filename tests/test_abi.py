@@ -43,7 +43,7 @@ def test_binding_constants_match_the_header():
         if hasattr(zc, name):
             assert getattr(zc, name) == value, name
     for name in ("ZC_KERNEL_STATS", "ZC_KERNEL_ENCODE", "ZC_KERNEL_DECODE", "ZC_KERNEL_RAW", "ZC_KERNEL_SMALL",
-                 "ZC_KERNEL_MEDIUM", "ZC_KERNEL_FUSED", "ZC_KERNEL_SAMPLE", "ZC_KERNEL_ENCODE_SPEC", "ZC_KERNEL_RESET"):
+                 "ZC_KERNEL_MEDIUM", "ZC_KERNEL_FUSED", "ZC_KERNEL_REFIT_STATS", "ZC_KERNEL_REFIT_ENCODE"):
         assert getattr(zc, name) == defines[name]
 
 

@@ -1,14 +1,15 @@
 """The speculative path (auto mode, tensors above the single-launch sizes), against the oracle,
 through the C ABI.
 
-A sample pass takes one 16-byte vector of every full chunk -- the vector (37 c + 11) mod 512 of
-chunk c -- and guesses e0 from it; the encode kernel codes with the guess while it sums the
-squares of every value exactly as the statistics kernel does, and the CTA whose chunks complete
-the count applies the rule to the whole tensor's sum.  When the rule settles the guessed e0 the
-stream is final; otherwise (or when the sample is not confident) the fallback word is set and
-the statistics and encode kernels redo the job.  Every stream must equal the oracle's byte for
-byte whichever way it went; the fallback word (the control block's bytes 240..243, at the start
-of the workspace in the tail of `out`) tells which way that was.
+Every CTA of the encode kernel reads the same sample -- 512 chunks spread evenly over the tensor,
+chunk c giving its 16-byte vector (37 c + 11) mod 512 -- and guesses e0 from it; when it trusts
+the guess it codes with it while summing the squares of every value exactly as the statistics
+kernel does, and the CTA whose chunks complete the count applies the rule to the whole tensor's
+sum.  When the rule settles the guessed e0 the stream is final; otherwise, or when the sample was
+not trusted, the fallback word is set and the statistics kernel and the encode kernel run again
+after it, as without the speculation.  Every stream must equal the oracle's byte for byte
+whichever way it went; the fallback word (bytes 240..243 of the control block at the start of the
+workspace, in the tail of `out`) tells which way that was.
 """
 import numpy as np
 import pytest
@@ -63,8 +64,9 @@ def compress_checked(x, base=-1):
 
 
 def sampled_positions(n):
-    """Start of the sampled vector of every full chunk."""
-    c = np.arange(n // 4096, dtype=np.int64)
+    """Start of every sampled vector."""
+    full = n // 4096
+    c = np.arange(512, dtype=np.int64) * full // 512
     return 4096 * c + 8 * ((37 * c + 11) % 512)
 
 
@@ -73,24 +75,23 @@ def gaussian(n, seed, sigma=1.0):
     return workloads.fp32_to_bf16_bits((rng.standard_normal(n) * sigma).astype(np.float32))
 
 
-SPEC_KERNELS = [zc.ZC_KERNEL_SAMPLE, zc.ZC_KERNEL_ENCODE_SPEC, zc.ZC_KERNEL_RESET, zc.ZC_KERNEL_STATS,
-                zc.ZC_KERNEL_ENCODE, zc.ZC_KERNEL_RAW]
+SPEC_KERNELS = [zc.ZC_KERNEL_ENCODE, zc.ZC_KERNEL_REFIT_STATS, zc.ZC_KERNEL_REFIT_ENCODE, zc.ZC_KERNEL_RAW]
 
 
 @pytest.mark.parametrize("n", [SINGLE_MAX + 1, SINGLE_MAX + 3 * 4096 + 5, 40_000_001, 3 * SINGLE_MAX])
 def test_guess_holds(n):
-    s, kernels, fallback = compress_checked(gaussian(n, n % 1000))
+    s, kernels, route = compress_checked(gaussian(n, n % 1000))
     assert kernels == SPEC_KERNELS
-    assert fallback == 0 and s[6] == 12 and s[7] == 122
+    assert route == 0 and s[6] == 12 and s[7] == 122
 
 
 def test_gradient_bucket_is_not_speculated():
-    """0.1% of the values are 100x the rest and make most of the sum of squares: a sample of one
-    value in 512 estimates it with a relative standard error of about 14%, too wide around the
-    tensor's e0 (114; the sample's own is 113), so the sample pass turns the speculation off."""
+    """0.1% of the values are 100x the rest and make most of the sum of squares: a sample of 4096
+    values estimates it far too loosely (relative standard error over 30%), so the encode kernel
+    does not speculate."""
     x = workloads.make("grad_bucket_4096x14336")
-    s, _, fallback = compress_checked(x)
-    assert fallback == 1 and s[6] == 12 and s[7] == 114
+    s, _, route = compress_checked(x)
+    assert route == 1 and s[6] == 12 and s[7] == 114
 
 
 def test_guess_wrong_falls_back_to_the_coded_form():
@@ -103,8 +104,8 @@ def test_guess_wrong_falls_back_to_the_coded_form():
     v = (x[idx].astype(np.uint32) << 16).view(np.float32) * np.float32(0.25)
     x[idx] = workloads.fp32_to_bf16_bits(v)
     assert oracle.choose_e0(x) == 122
-    s, _, fallback = compress_checked(x)
-    assert fallback == 1 and s[6] == 12 and s[7] == 122
+    s, _, route = compress_checked(x)
+    assert route == 1 and s[6] == 12 and s[7] == 122
 
 
 def test_guess_wrong_falls_back_to_the_raw_form():
@@ -113,15 +114,15 @@ def test_guess_wrong_falls_back_to_the_raw_form():
     n = SINGLE_MAX + 77
     x = gaussian(n, 8)
     x[1] = workloads.fp32_to_bf16_bits(np.array([1e20], np.float32))[0]
-    s, _, fallback = compress_checked(x)
-    assert fallback == 1 and s[6] == 0
+    s, _, route = compress_checked(x)
+    assert route == 1 and s[6] == 0
 
 
 def test_sample_not_confident_on_random_patterns():
-    """A sample that predicts a raw stream turns the speculation off before any coding."""
+    """A sample that predicts a raw stream keeps the encode kernel from speculating at all."""
     n = SINGLE_MAX + 4096
-    s, _, fallback = compress_checked(workloads.random_patterns(n, 3))
-    assert fallback == 1 and s[6] == 0
+    s, _, route = compress_checked(workloads.random_patterns(n, 3))
+    assert route == 1 and s[6] == 0
 
 
 def test_nonfinite_values_in_the_speculative_sums():
@@ -129,8 +130,8 @@ def test_nonfinite_values_in_the_speculative_sums():
     x = gaussian(n, 9)
     x[::97] = 0x7FC0   # NaN
     x[5::4096] = 0xFF80  # -Inf
-    s, _, fallback = compress_checked(x)
-    assert fallback == 0 and s[6] == 12
+    s, _, route = compress_checked(x)
+    assert route == 0 and s[6] == 12
 
 
 def test_supplied_base_takes_no_speculation():
