@@ -1111,12 +1111,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   asm volatile("griddepcontrol.launch_dependents;");
   const unsigned tid = threadIdx.x, warp = tid >> 5;
   if (p.mode == kGated) {
-    // After the speculative path: wait for the steps before (the speculative encode kernel, the
-    // gated statistics kernel) and run only when the speculation fell back.
-    if (tid == 0) {
-      asm volatile("griddepcontrol.wait;" ::: "memory");
-      S.skip = __ldcg(&p.ctrl->fallback) == 0;
-    }
+    // After the speculative path: run only when the speculation fell back.  This kernel starts
+    // only after every CTA of the gated statistics kernel before it has passed that kernel's
+    // wait for the speculative encode kernel (and cleared its share of the workspace), or has
+    // returned after it: the fallback word is final and visible by then.  When it is set, the
+    // tickets and first copies below go ahead while the statistics pass finishes, and e0 is read
+    // after griddepcontrol.wait, as after the statistics kernel alone.
+    if (tid == 0) S.skip = ld_acquire_u32(&p.ctrl->fallback) == 0;
     __syncthreads();
     if (S.skip) return;
   }

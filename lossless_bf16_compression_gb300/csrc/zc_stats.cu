@@ -201,7 +201,7 @@ __device__ void stats_settle(const StatsParams& p, unsigned ctas, StatsScratch& 
 
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) stats_kernel(StatsParams p) {
   // The encode kernel that follows may start now (it waits for this kernel before it reads e0).
-  asm volatile("griddepcontrol.launch_dependents;");
+  if (!p.gated) asm volatile("griddepcontrol.launch_dependents;");
   __shared__ StatsScratch T;
   __shared__ int go;
   if (p.gated) {
@@ -213,7 +213,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) stats_kernel(StatsParams
       go = __ldcg(&p.ctrl->fallback) != 0;
     }
     __syncthreads();
-    if (!go) return;
+    if (!go) return;  // the encode kernel after this one starts when this one is done
     if (blockIdx.x == 0) {
       if (threadIdx.x == 0) {
         Control& c = *p.ctrl;
@@ -229,6 +229,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) stats_kernel(StatsParams
     for (uint64_t i = static_cast<uint64_t>(blockIdx.x) * kThreads + threadIdx.x; i < p.flag_words;
          i += static_cast<uint64_t>(gridDim.x) * kThreads)
       p.flags[i] = 0;
+    // Only now may the encode kernel start: every CTA's share of the workspace is cleared and
+    // visible device-wide before that kernel can take a ticket (it reads e0 only after waiting
+    // for this kernel's completion).
+    __threadfence();
+    __syncthreads();
+    asm volatile("griddepcontrol.launch_dependents;");
   }
   stats_share(p, blockIdx.x, gridDim.x, T);
   if (threadIdx.x < 32) {  // warp 0's writes, then the completion ticket
