@@ -182,10 +182,11 @@ int compress_impl(const void* in, size_t n, int base, void* out, size_t* out_byt
     return finish_length(pageable, ws, out_bytes, stream);
   }
   if (cudaMemsetAsync(ws, 0, workspace_bytes(n), stream) != cudaSuccess) return ZC_ERR_CUDA;
-  if (n > 0 && base == ZC_BASE_AUTO && !loopback && stall_chunk == ~uint64_t(0)) {
+  if (base == ZC_BASE_AUTO && stall_chunk == ~uint64_t(0) && n / kChunk >= kSpecSampleChunks) {
     // auto mode: code with the e0 of a sample and check it (the statistics pass runs only when
-    // the check fails or the sample is not confident)
-    if (launch_speculative(x, n, o, len_ptr, ws, dev, stream) != cudaSuccess) return ZC_ERR_CUDA;
+    // the check fails or the sample is not confident); the loopback decodes on either pass
+    if (launch_speculative(x, n, o, len_ptr, ws, dev, stream, static_cast<uint16_t*>(values)) != cudaSuccess)
+      return ZC_ERR_CUDA;
     return finish_length(pageable, ws, out_bytes, stream);
   }
   if (n > 0 && base == ZC_BASE_AUTO) {

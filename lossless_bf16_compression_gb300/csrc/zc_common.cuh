@@ -350,6 +350,9 @@ struct TimingRecord {
 TimingRecord timing_begin(int kernel_id, cudaStream_t stream);
 void timing_end(TimingRecord& rec, cudaStream_t stream);
 
+// The speculative encode kernel samples one 16-byte vector from each of 512 full chunks spread
+// over the tensor: it runs only on tensors with at least that many full chunks.
+constexpr uint64_t kSpecSampleChunks = 512;
 // The launches.  `ws` is the call's workspace (workspace_bytes(n) bytes, cleared): the tail of
 // `out` for zc_compress, the library's static array for zc_compress_static_scratch.
 // predict_raw: also sample the exponents and, when the sample predicts that the coded stream
@@ -366,9 +369,11 @@ cudaError_t launch_encode(const uint16_t* in, uint64_t n, int base, uint8_t* out
 // guesses e0 from a sample (every CTA the same guess), codes with it and checks it against the
 // whole tensor's sum of squares, which it takes as it codes; when the sample was not confident or
 // the guess did not hold, the statistics and encode kernels after it, gated on the fallback
-// word, do the job as they do without the speculation.
+// word, do the job as they do without the speculation.  loopback_values: the loopback's decoded
+// values (both encode launches decode what they code), or null.
 cudaError_t launch_speculative(const uint16_t* in, uint64_t n, uint8_t* out, unsigned long long* out_bytes,
-                               uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream);
+                               uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream,
+                               uint16_t* loopback_values = nullptr);
 cudaError_t launch_decode(const uint8_t* in, uint16_t* out, uint64_t n, const DeviceInfo& dev,
                           cudaStream_t stream);
 // After the encode kernel: when the coded stream came out longer than the raw form, rewrite the

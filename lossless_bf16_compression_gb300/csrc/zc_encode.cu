@@ -1162,17 +1162,23 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     return;
   }
   if (decode_only) {  // (the loopback never takes the raw pass; the exact e0 it may need)
-    if (tid == 0) {
-      if (p.base < 0) asm volatile("griddepcontrol.wait;" ::: "memory");
-      S.kind = p.base < 0 && __ldcg(&p.ctrl->exact_path) != 0 ? 1 : 0;
+    if (p.mode == kSpeculative) {  // the coding CTAs' guess; no decoding without it
+      spec_guess(S, p);
+      if (!S.confident) return;
+      if (tid == 0) S.e0 = S.guess;
+    } else {
+      if (tid == 0) {
+        if (p.base < 0) asm volatile("griddepcontrol.wait;" ::: "memory");
+        S.kind = p.base < 0 && __ldcg(&p.ctrl->exact_path) != 0 ? 1 : 0;
+      }
+      bar_coders();
+      if (S.kind &&
+          !first_phase(S, p.in, p.n, p.N, p.out, p.out_bytes, p.ctrl,
+                       reinterpret_cast<unsigned long long*>(reinterpret_cast<uint8_t*>(p.ctrl) + kWsExactBinsOffset),
+                       p.status, p.spin_limit, S.kind))
+        return;
+      if (tid == 0) S.e0 = p.base >= 0 ? p.base : __ldcg(&p.ctrl->e0);
     }
-    bar_coders();
-    if (S.kind &&
-        !first_phase(S, p.in, p.n, p.N, p.out, p.out_bytes, p.ctrl,
-                     reinterpret_cast<unsigned long long*>(reinterpret_cast<uint8_t*>(p.ctrl) + kWsExactBinsOffset),
-                     p.status, p.spin_limit, S.kind))
-      return;
-    if (tid == 0) S.e0 = p.base >= 0 ? p.base : __ldcg(&p.ctrl->e0);
     bar_coders();
     loopback_decode_only(S, p.out, p.values, p.flags, p.ctrl, p.status, p.n, p.N, p.spin_limit);
     return;
@@ -1354,7 +1360,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   }
   if (speculative && !skip)
     spec_verdict(S, p, e0, spec_acc, spec_nonfinite, spec_chunks, spec_fast, spec_values, spec_inside);
-  if (p.values) {  // loopback: no chunk left to code, so decode (the stages are free now)
+  if (p.values && !skip) {  // loopback: no chunk left to code, so decode (the stages are free now)
     bar_coders();
     loopback_decode(S, p.out, p.values, p.flags, p.ctrl, p.status, p.n, p.N, p.spin_limit);
   }
@@ -1543,13 +1549,14 @@ cudaError_t launch_raw_form(const uint16_t* in, uint64_t n, int base, uint8_t* o
 // each a programmatic dependent launch that returns at once unless the fallback word is set --
 // the statistics kernel and the encode kernel again; then the raw-form step.
 cudaError_t launch_speculative(const uint16_t* in, uint64_t n, uint8_t* out, unsigned long long* out_bytes,
-                               uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream) {
+                               uint8_t* ws, const DeviceInfo& dev, cudaStream_t stream, uint16_t* loopback_values) {
   cudaError_t err = launch_encode(in, n, ZC_BASE_AUTO, out, out_bytes, ws, dev, stream, ~uint64_t(0),
-                                  kDefaultSpinLimit, nullptr, kSpeculative);
-  if (err == cudaSuccess) err = launch_stats(in, n, ws, dev, stream, true, true);
+                                  kDefaultSpinLimit, loopback_values, kSpeculative);
+  // (the loopback decodes the coded form: it never takes the raw pass, so no prediction)
+  if (err == cudaSuccess) err = launch_stats(in, n, ws, dev, stream, loopback_values == nullptr, true);
   if (err == cudaSuccess)
     err = launch_encode(in, n, ZC_BASE_AUTO, out, out_bytes, ws, dev, stream, ~uint64_t(0), kDefaultSpinLimit,
-                        nullptr, kGated);
+                        loopback_values, kGated);
   if (err == cudaSuccess) err = launch_raw_form(in, n, ZC_BASE_AUTO, out, out_bytes, ws, dev, stream);
   return err;
 }

@@ -83,10 +83,12 @@ extern "C" int zc_compress_static_scratch(const void* in, size_t n, int base_or_
     return finish_length(pageable, ws, out_bytes, stream);
   }
   if (cudaMemsetAsync(ws, 0, workspace_bytes(n), stream) != cudaSuccess) return ZC_ERR_CUDA;
-  if (n > 0 && base_or_auto == ZC_BASE_AUTO) {  // the speculative path, as zc_compress takes it
+  if (base_or_auto == ZC_BASE_AUTO && n / kChunk >= kSpecSampleChunks) {  // as zc_compress: speculative
     if (launch_speculative(x, n, o, len_ptr, ws, dev, stream) != cudaSuccess) return ZC_ERR_CUDA;
     return finish_length(pageable, ws, out_bytes, stream);
   }
+  if (n > 0 && base_or_auto == ZC_BASE_AUTO && launch_stats(x, n, ws, dev, stream, true) != cudaSuccess)
+    return ZC_ERR_CUDA;
   if (launch_encode(x, n, base_or_auto, o, len_ptr, ws, dev, stream, ~uint64_t(0), kDefaultSpinLimit) != cudaSuccess)
     return ZC_ERR_CUDA;
   if (launch_raw_form(x, n, base_or_auto, o, len_ptr, ws, dev, stream) != cudaSuccess) return ZC_ERR_CUDA;

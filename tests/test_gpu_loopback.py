@@ -75,6 +75,45 @@ def test_exact_e0_in_the_loopback():
     assert s[7] == oracle.choose_e0(x)
 
 
+def loopback_fallback_word(out, n):
+    """The fallback word of the loopback's control block (bytes 240..243; the workspace is the
+    last workspace-size bytes of the loopback's buffer)."""
+    ws_bytes = zc.zc_max_compressed_bytes(n) - (zc.zc_max_stream_bytes(n) + 255) // 256 * 256
+    at = zc.zc_loopback_bytes(n) - ws_bytes
+    return int(out[at + 240:at + 244].cpu().numpy().view(np.uint32)[0])
+
+
+def test_speculative_loopback_guess_holds():
+    """From 512 full chunks on, the loopback takes the speculative route: it codes and decodes
+    with the sample's e0, which the whole tensor's sums then confirm."""
+    x = workloads.sweep(23)
+    xd = to_device(x)
+    zc.status(reset=True)
+    out, ob, values = zc.loopback(xd)
+    assert zc.status(reset=True) == zc.ZC_OK
+    assert loopback_fallback_word(out, x.size) == 0
+    assert np.array_equal(values.cpu().numpy().view(np.uint16), x)
+    want = oracle.compress(x)
+    assert out[:int(ob.item())].cpu().numpy().tobytes() == want.tobytes()
+
+
+def test_speculative_loopback_falls_back():
+    """A sample that names the wrong e0 (120 for a tensor of 122): the chunks coded and decoded
+    with 120 are coded and decoded again after the statistics pass, and the final stream and
+    values are the oracle's and the input."""
+    from test_gpu_speculative import misleading_sample
+
+    x = misleading_sample((1 << 25) + 4096 * 3 + 9, 21)
+    xd = to_device(x)
+    zc.status(reset=True)
+    out, ob, values = zc.loopback(xd)
+    assert zc.status(reset=True) == zc.ZC_OK
+    assert loopback_fallback_word(out, x.size) == 1
+    assert np.array_equal(values.cpu().numpy().view(np.uint16), x)
+    want = oracle.compress(x)
+    assert out[:int(ob.item())].cpu().numpy().tobytes() == want.tobytes()
+
+
 @pytest.mark.parametrize("stalled", [0, 37])
 def test_decode_wait_is_bounded(stalled):
     x = workloads.sweep(18)  # 64 chunks

@@ -85,6 +85,18 @@ def test_guess_holds(n):
     assert route == 0 and s[6] == 12 and s[7] == 122
 
 
+@pytest.mark.parametrize("log2_sigma,e0", [(-46, 76), (-34.5, 87), (58.5, 180), (62, 184)])
+def test_guess_holds_at_every_scale(log2_sigma, e0):
+    """The speculative sums take the plain fp32 squares only for e0 in [87, 180], where the
+    window's squares are normal fp32 numbers; outside that range every block goes through the
+    careful (scaled) block sum.  Both ends of the plain range and a scale beyond each: the guess
+    holds and the stream is the oracle's."""
+    x = gaussian(SINGLE_MAX + 4096 * 5 + 11, 12, 2.0 ** log2_sigma)
+    s, kernels, route = compress_checked(x)
+    assert kernels == SPEC_KERNELS
+    assert route == 0 and s[6] == 12 and s[7] == e0
+
+
 def test_gradient_bucket_is_not_speculated():
     """0.1% of the values are 100x the rest and make most of the sum of squares: a sample of 4096
     values estimates it far too loosely (relative standard error over 30%), so the encode kernel
@@ -94,16 +106,22 @@ def test_gradient_bucket_is_not_speculated():
     assert route == 1 and s[6] == 12 and s[7] == 114
 
 
-def test_guess_wrong_falls_back_to_the_coded_form():
-    """The sampled vectors are scaled by 1/4: the sample's e0 is 120, the tensor's 122.  The coding
-    pass codes with 120, its own sums settle 122, and the statistics and encode kernels redo it."""
-    n = SINGLE_MAX + 4096 * 11 + 3
-    x = gaussian(n, 7).view(np.uint16).copy()
+def misleading_sample(n, seed):
+    """N(0, 1) values whose sampled vectors are scaled by 1/4: the sample's e0 is 120, the
+    tensor's 122."""
+    x = gaussian(n, seed).view(np.uint16).copy()
     pos = sampled_positions(n)
     idx = (pos[:, None] + np.arange(8)[None, :]).ravel()
     v = (x[idx].astype(np.uint32) << 16).view(np.float32) * np.float32(0.25)
     x[idx] = workloads.fp32_to_bf16_bits(v)
     assert oracle.choose_e0(x) == 122
+    return x
+
+
+def test_guess_wrong_falls_back_to_the_coded_form():
+    """The coding pass codes with the sample's 120, its own sums settle 122, and the statistics
+    and encode kernels redo it."""
+    x = misleading_sample(SINGLE_MAX + 4096 * 11 + 3, 7)
     s, _, route = compress_checked(x)
     assert route == 1 and s[6] == 12 and s[7] == 122
 
