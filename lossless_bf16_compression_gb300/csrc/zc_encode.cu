@@ -74,7 +74,7 @@ constexpr int kScanPerLane = 8;            // state words per scanner lane per r
 #define ZC_LOOPBACK_CYCLE 5
 #endif
 #ifndef ZC_LOOPBACK_DECODERS
-#define ZC_LOOPBACK_DECODERS 2
+#define ZC_LOOPBACK_DECODERS 1
 #endif
 constexpr unsigned kLoopbackCycle = ZC_LOOPBACK_CYCLE;      // loopback: of every kLoopbackCycle CTAs (by
 constexpr unsigned kLoopbackDecoders = ZC_LOOPBACK_DECODERS;  // start order), this many only decode
@@ -121,6 +121,7 @@ struct __align__(128) EncodeSmem {
   volatile unsigned q_retired;  // entries written out and read back from the ring (consumer)
   volatile unsigned freed;      // ring bytes given back, gaps included (consumer)
   volatile int coders_done;     // no more entries will come
+  volatile int retirer_done;    // the retiring warp has left: the ring is free
   __align__(16) unsigned scan[kCoderWarps];  // per coding warp: its escape count
   // scanner: per round parity, each warp's ready count and sum, and the status word
   unsigned long long scan_sum[2][kCoderWarps];
@@ -138,8 +139,9 @@ struct __align__(128) EncodeSmem {
   unsigned dsize;
   int dok;
   unsigned descapes;
-  unsigned slot_chunk[2], slot_size[2];  // a decoding-only CTA's two slots
+  unsigned slot_chunk[2], slot_size[2];  // a decoding CTA's two slots
   int slot_ok[2];
+  unsigned lb_parity;  // a coding CTA turned decoder: the stages' mbarrier phases to wait for next
   // speculative: the coding warps' sums, and whether this CTA completed the chunk count
   double spec_sum[kCoderWarps];
   unsigned long long spec_nf[kCoderWarps], spec_values[kCoderWarps], spec_inside[kCoderWarps];
@@ -389,6 +391,11 @@ __device__ void retirer(EncodeSmem& S, const EncodeParams& p) {
       S.q_retired = retired;
     }
     __syncwarp();
+  }
+  __syncwarp();  // every lane's copies out of the ring are done
+  if (lane == 0) {
+    __threadfence_block();
+    S.retirer_done = 1;
   }
 }
 
@@ -701,12 +708,11 @@ __device__ bool copied_section(const uint8_t* stream, int* status, uint64_t E0, 
   return true;
 }
 
-// Loopback, the 128 coding threads of a CTA: decode chunks in ticket order as their escape
-// sections reach the stream (the split-send pipeline: a chunk is transmissible, and here
-// decoded, as soon as its own bytes are in place, while later chunks are still being coded).
-// Each chunk waits (bounded, thread 0) for its copied mark, then its fixed part and escape
-// section are read back from the stream into the free input stages and decoded with the decode
-// kernel's own code.
+// Loopback decoding: chunks are decoded in ticket order as their escape sections reach the
+// stream (the split-send pipeline: a chunk is transmissible, and here decoded, as soon as its own
+// bytes are in place, while later chunks are still being coded).  Each chunk waits (bounded,
+// thread 0) for its copied mark, then its fixed part and escape section are read back from the
+// stream and decoded with the decode kernel's own code.
 struct LoopbackArgs {  // what the loopback decoding needs, passed in registers
   const uint8_t* stream;
   uint16_t* values;
@@ -716,58 +722,6 @@ struct LoopbackArgs {  // what the loopback decoding needs, passed in registers
   uint64_t n, N;
   unsigned spin_limit;
 };
-
-__device__ __noinline__ void loopback_decode(EncodeSmem& S, const uint8_t* stream, uint16_t* values,
-                                             unsigned long long* flags, Control* ctrl, int* status, uint64_t n,
-                                             uint64_t N, unsigned spin_limit) {
-  const LoopbackArgs p{stream, values, flags, ctrl, status, n, N, spin_limit};
-  const unsigned tid = threadIdx.x;
-  const uint64_t E0 = escape_base(p.n), R0 = records_base(p.n);
-  uint4* const fixed = S.xin[0];
-  uint4* const esc = S.xin[1];
-  for (;;) {
-    if (tid == 0) {
-      const unsigned d = atomicAdd(&p.ctrl->decode_ticket, 1u);
-      int ok = d < p.N;
-      if (ok) {
-        unsigned spins = 0, backoff = 64;
-        unsigned long long f;
-        while (((f = ld_relaxed_u64(&p.flags[d])) >> 62) != 3) {
-          if (read_status(p.status) != 0 || ++spins > p.spin_limit) {
-            if (spins > p.spin_limit) set_error(p.status, ZC_ERR_TIMEOUT);
-            ok = 0;
-            break;
-          }
-          __nanosleep(backoff);
-          backoff = backoff < 512 ? backoff * 2 : 512;
-        }
-        if (ok) {
-          __threadfence();  // acquire: the chunk's bytes and its offset are visible from here on
-          unsigned long long off = 0;
-          unsigned size = 0;
-          ok = copied_section(p.stream, p.status, E0, d, f, &off, &size);
-          S.doff = off;
-          S.dsize = size;
-        }
-      }
-      S.dchunk = d;
-      S.dok = ok;
-      S.descapes = 0;
-    }
-    bar_coders();
-    if (!S.dok) break;
-    const unsigned d = S.dchunk, m = chunk_values(p.n, d), size = S.dsize;
-    const unsigned fb = static_cast<unsigned>(fixed_bytes(m));
-    const uint4* gf = reinterpret_cast<const uint4*>(p.stream + R0 + static_cast<uint64_t>(d) * kFullFixedBytes);
-    const uint4* ge = reinterpret_cast<const uint4*>(p.stream + S.doff);
-    for (unsigned i = tid; i < fb / 16; i += kCoders) fixed[i] = __ldcg(gf + i);
-    for (unsigned i = tid; i < size / 16; i += kCoders) esc[i] = __ldcg(ge + i);
-    bar_coders();
-    decode_chunk(fixed, esc, &S.descapes, p.values + static_cast<uint64_t>(d) * kChunk, m, S.e0, size, p.status,
-                 tid, [] { bar_coders(); });
-    bar_coders();  // the stages are read before the next chunk is staged
-  }
-}
 
 // Thread 0: take the next chunk to decode and wait (bounded) for its copied mark.  Returns false
 // when no chunk is left or after an error or a timeout; otherwise *off and *size give its escape
@@ -791,12 +745,15 @@ __device__ bool claim_decode(const LoopbackArgs& p, uint64_t E0, unsigned* d, un
   return copied_section(p.stream, p.status, E0, *d, f, off, size);
 }
 
-// Loopback, a CTA that only decodes: two slots, each a chunk's fixed part (in an input stage) and
-// escape section (in the ring, unused here), filled by bulk async copies; the next chunk's copies
-// are in flight while a chunk is decoded.
-__device__ __noinline__ void loopback_decode_only(EncodeSmem& S, const uint8_t* stream, uint16_t* values,
-                                                  unsigned long long* flags, Control* ctrl, int* status, uint64_t n,
-                                                  uint64_t N, unsigned spin_limit) {
+// Loopback, the 128 coding threads of a CTA that decodes: two slots, each a chunk's fixed part
+// (in an input stage) and escape section (in the ring), filled by bulk async copies; the next
+// chunk's copies are in flight while a chunk is decoded.  A CTA that only decodes starts here
+// (fresh mbarriers); a coding CTA comes here once it has no chunk left to code and its retiring
+// warp has left (the ring is free), reusing the stages' mbarriers from the phases in
+// S.lb_parity (`reuse`).
+__device__ __noinline__ void loopback_decode_slots(EncodeSmem& S, const uint8_t* stream, uint16_t* values,
+                                                   unsigned long long* flags, Control* ctrl, int* status, uint64_t n,
+                                                   uint64_t N, unsigned spin_limit, bool reuse) {
   const LoopbackArgs p{stream, values, flags, ctrl, status, n, N, spin_limit};
   const unsigned tid = threadIdx.x;
   const uint64_t E0 = escape_base(p.n), R0 = records_base(p.n);
@@ -820,13 +777,15 @@ __device__ __noinline__ void loopback_decode_only(EncodeSmem& S, const uint8_t* 
     }
   };
   if (tid == 0) {
-    for (int j = 0; j < 2; ++j) mbar_init(&S.mbar[j], 1);
-    fence_mbar_init();
+    if (!reuse) {
+      for (int j = 0; j < 2; ++j) mbar_init(&S.mbar[j], 1);
+      fence_mbar_init();
+    }
     fill(0);
     fill(1);
   }
   bar_coders();
-  unsigned parity = 0;
+  unsigned parity = reuse ? S.lb_parity : 0u;
   for (int j = 0;; j ^= 1) {
     if (!S.slot_ok[j]) break;
     // every thread polls; all act on one shared answer
@@ -1130,6 +1089,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     S.q_retired = 0;
     S.freed = 0;
     S.coders_done = 0;
+    S.retirer_done = 0;
     S.skip = 0;
     S.spec = 0;
   }
@@ -1180,7 +1140,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       if (tid == 0) S.e0 = p.base >= 0 ? p.base : __ldcg(&p.ctrl->e0);
     }
     bar_coders();
-    loopback_decode_only(S, p.out, p.values, p.flags, p.ctrl, p.status, p.n, p.N, p.spin_limit);
+    loopback_decode_slots(S, p.out, p.values, p.flags, p.ctrl, p.status, p.n, p.N, p.spin_limit, false);
     return;
   }
 
@@ -1356,13 +1316,34 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     __threadfence_block();
     S.coders_done = 1;  // the retiring warp drains the queue and leaves
     for (int s = 0; s < kStages; ++s)  // never leave a copy in flight
-      if (pending & (1u << s)) mbar_wait(&S.mbar[s], (parity >> s) & 1u, kWaitLimit);
+      if (pending & (1u << s)) {
+        mbar_wait(&S.mbar[s], (parity >> s) & 1u, kWaitLimit);
+        parity ^= 1u << s;
+      }
+    S.lb_parity = parity;
   }
   if (speculative && !skip)
     spec_verdict(S, p, e0, spec_acc, spec_nonfinite, spec_chunks, spec_fast, spec_values, spec_inside);
-  if (p.values && !skip) {  // loopback: no chunk left to code, so decode (the stages are free now)
+  if (p.values && !skip) {
+    // Loopback: no chunk left to code, so decode.  The stages are free now, the ring once the
+    // retiring warp has written out the last sections and left (bounded wait).
+    if (tid == 0) {
+      unsigned spins = 0, backoff = 64;
+      S.dok = 1;
+      while (S.retirer_done == 0) {
+        if (read_status(p.status) != 0 || ++spins > p.spin_limit) {
+          if (spins > p.spin_limit) set_error(p.status, ZC_ERR_TIMEOUT);
+          S.dok = 0;
+          break;
+        }
+        __nanosleep(backoff);
+        backoff = backoff < 512 ? backoff * 2 : 512;
+      }
+      __threadfence_block();
+    }
     bar_coders();
-    loopback_decode(S, p.out, p.values, p.flags, p.ctrl, p.status, p.n, p.N, p.spin_limit);
+    if (S.dok)
+      loopback_decode_slots(S, p.out, p.values, p.flags, p.ctrl, p.status, p.n, p.N, p.spin_limit, true);
   }
 }
 
