@@ -995,8 +995,9 @@ __device__ __noinline__ void spec_guess(EncodeSmem& S, const EncodeParams& p) {
 // Speculative mode, the coding threads of a CTA after its last chunk: the CTA's sums are added to
 // the control block's, and its chunks to the count.  The CTA whose chunks complete the count (an
 // acquire-release add tells it; every other coding CTA added its sums before its own count)
-// applies the rule to the total exactly as the statistics kernel does (decide_e0, one end per
-// thread), and sets the fallback word unless the rule settles the e0 the chunks were coded with.
+// applies the rule to the total exactly as the statistics kernel does (decide_e0_pair: one end
+// per thread), and sets the fallback word unless the rule settles the e0 the chunks were coded
+// with.
 // The order of the additions varies from run to run; the rule's bound holds for every order, so
 // the e0 it settles does not.  A CTA that took no chunk adds nothing.
 __device__ __noinline__ void spec_verdict(EncodeSmem& S, const EncodeParams& p, int e0, double acc,

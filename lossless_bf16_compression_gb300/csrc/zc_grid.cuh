@@ -131,7 +131,7 @@ __device__ void fixed_sum2(uint64_t count, unsigned per_lane, A* sa, B* sb, A* a
 
 // Work for the last CTA of a grid barrier (all its threads): the CTAs' statistics partials
 // added up in one fixed order (thread t takes CTAs t, t + 128, ..; then a fixed tree), and the
-// window rule at both ends of the estimate's error interval, one end per thread (decide_e0): e0
+// window rule at both ends of the estimate's error interval, one end per thread (as decide_e0_pair): e0
 // is settled when they agree, else the exact sums must decide it.  Writes e0, the exact flag and
 // the finite count to the control block.  G <= kMaxGridCtas.
 constexpr unsigned kMaxGridCtas = 1024;

@@ -11,8 +11,9 @@
 //
 // GB300 design.  G CTAs of 128 threads; CTA r holds chunks r J .. r J + J - 1 (J = ceil(N / G),
 // at most four) in shared memory: 32 KiB of input and their escape sections.  The input arrives
-// by bulk async copies.  Each CTA sums its squares in the same fp32 blocks with the same error
-// bound as the statistics kernel and publishes its partial; after a barrier the partials are
+// by bulk async copies.  Each CTA sums its squares in fp32 blocks as the statistics kernel does
+// (of 32 values, one per thread and chunk, inside that kernel's error bound for its blocks of
+// 64) and publishes its partial; after a barrier the partials are
 // combined in one fixed order, so that one e0 is settled for all (and, when the bound straddles a
 // switching point, the exact per-exponent sums decide it).  The CTAs code their chunks (escape
 // sections into shared memory; fixed parts too in a cluster, so that its barriers wait for no
@@ -78,9 +79,14 @@ struct __align__(128) ResidentSmem {
   int e0;
   int need_exact;
   int ok;
-  // last: the fixed parts, kept here until the stream's form is known (cluster launches only; the
-  // grid launch stores them in place at once and does not allocate this)
+  // last, for cluster launches only (the grid launch does not allocate them): the fixed parts,
+  // kept here until the stream's form is known (the grid launch stores them in place at once),
+  // and every CTA's partial and sections' sizes, pushed here by their CTAs before the barrier
+  // that publishes them, so that they are read locally after it
   uint4 fixed[kPerCta][kFullFixedBytes / 16];
+  double all_sum[kSmallCtas];
+  unsigned long long all_nf[kSmallCtas];
+  unsigned all_size[kSmallCtas * kPerCta];
 };
 constexpr size_t kGridSmemBytes = offsetof(ResidentSmem, fixed);
 
@@ -97,10 +103,6 @@ struct ClusterExchange {
     S.cta_sum = s;
     S.cta_nonfinite = nf;
   }
-  __device__ void get_partial(ResidentSmem& S, unsigned q, double* s, unsigned long long* nf) {
-    *s = *cl.map_shared_rank(&S.cta_sum, q);
-    *nf = *cl.map_shared_rank(&S.cta_nonfinite, q);
-  }
   // exact path: the CTA's bins are in S.bins; every CTA adds up all of them (after a barrier)
   __device__ void share_bins(ResidentSmem&) {}
   __device__ unsigned long long all_bins(ResidentSmem& S, unsigned e) {
@@ -109,34 +111,47 @@ struct ClusterExchange {
     return t;
   }
   // Every CTA combines the partials in the same fixed order (thread t takes CTAs t, t + 32, ..,
-  // then a fixed tree), so every CTA settles the same e0.
+  // then a fixed tree), so every CTA settles the same e0.  Thread t pushes this CTA's partial to
+  // CTA t before the barrier; after it each CTA reads them from its own shared memory.
   __device__ bool settle(ResidentSmem& S, double s_cta, unsigned long long nf_cta, uint64_t n) {
     if (threadIdx.x == 0) put_partial(S, s_cta, nf_cta);
+    bar_cta();
+    const unsigned G = ctas(), r = rank();
+    if (threadIdx.x < G) {
+      cl.map_shared_rank(S.all_sum, threadIdx.x)[r] = S.cta_sum;
+      cl.map_shared_rank(S.all_nf, threadIdx.x)[r] = S.cta_nonfinite;
+    }
     sync();
     double s = 0.0;
     unsigned long long nf_all = 0;
-    fixed_sum2(ctas(), 1, S.wsum, S.wnf, &s, &nf_all, [&](uint64_t q, double& a, unsigned long long& b) {
-      double sq;
-      unsigned long long nq;
-      get_partial(S, static_cast<unsigned>(q), &sq, &nq);
-      a += sq;
-      b += nq;
+    fixed_sum2(G, 1, S.wsum, S.wnf, &s, &nf_all, [&](uint64_t q, double& a, unsigned long long& b) {
+      a += S.all_sum[q];
+      b += S.all_nf[q];
     });
-    if (threadIdx.x == 0) {
+    if (threadIdx.x < 2) {  // (warp 0's lanes all hold the sums) one end of the rule each
       int e = 0;
-      S.need_exact = decide_e0(s, n - nf_all, &e) ? 0 : 1;
-      S.e0 = e;
-      S.n_finite = n - nf_all;  // for the exact path
+      const bool settled = decide_e0_pair(s, n - nf_all, &e);
+      if (threadIdx.x == 0) {
+        S.need_exact = settled ? 0 : 1;
+        S.e0 = e;
+        S.n_finite = n - nf_all;  // for the exact path
+      }
     }
     bar_cta();
     return true;
   }
-  // The sizes of the chunks before this CTA's and of all, read from the CTAs' shared memory.
-  __device__ bool offsets(ResidentSmem& S, uint64_t first, unsigned, unsigned J, uint64_t N, unsigned long long* bef,
-                          unsigned long long* tot) {
+  // The sizes of the chunks before this CTA's and of all: thread t pushes this CTA's sizes to CTA
+  // t before the barrier (S.my_size is complete: the coding loop ends with a CTA barrier), and
+  // each CTA reads them from its own shared memory after it.
+  __device__ bool offsets(ResidentSmem& S, uint64_t first, unsigned mine, unsigned, uint64_t N,
+                          unsigned long long* bef, unsigned long long* tot) {
+    if (threadIdx.x < ctas()) {
+      unsigned* dst = cl.map_shared_rank(S.all_size, threadIdx.x);
+      for (unsigned j = 0; j < mine; ++j) dst[first + j] = S.my_size[j];
+    }
     sync();
     fixed_sum2(N, 2, S.wbefore, S.wtotal, bef, tot, [&](uint64_t c, unsigned long long& a, unsigned long long& b) {
-      const unsigned long long sz = cl.map_shared_rank(S.my_size, static_cast<unsigned>(c / J))[c % J];
+      const unsigned long long sz = S.all_size[c];
       a += c < first ? sz : 0ull;
       b += sz;
     });
@@ -259,13 +274,13 @@ __device__ void compress_resident(Exchange& X, ResidentSmem& S, const uint16_t* 
   if (base < 0) {
     double acc = 0.0;
     unsigned nonfinite = 0;
-    const unsigned B = 64 * mine;  // blocks of 64 values of this CTA's chunks (zeros past m add nothing)
+    const unsigned B = 128 * mine;  // blocks of 32 values of this CTA's chunks (zeros past m add nothing)
     for (unsigned b0 = 0; b0 < B; b0 += kSmallThreads) {
       const unsigned b = b0 + tid;
-      uint32_t w[32];
+      uint32_t w[16];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const uint4 v = b < B && S.ok ? S.x[b / 64][8 * (b % 64) + k] : make_uint4(0, 0, 0, 0);
+      for (int k = 0; k < 4; ++k) {
+        const uint4 v = b < B && S.ok ? S.x[b / 128][4 * (b % 128) + k] : make_uint4(0, 0, 0, 0);
         w[4 * k] = v.x;
         w[4 * k + 1] = v.y;
         w[4 * k + 2] = v.z;

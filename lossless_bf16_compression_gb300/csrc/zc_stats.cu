@@ -158,7 +158,7 @@ __device__ void stats_settle(const StatsParams& p, unsigned ctas, StatsScratch& 
     T.red_nf[warp] = c;
   }
   __syncthreads();
-  if (threadIdx.x == 0) {
+  if (threadIdx.x < 2) {  // both the same sums; one end of the rule each
     double S = 0.0;
     unsigned long long nonfin = 0;
     for (int i = 0; i < kWarps; ++i) {
@@ -167,11 +167,13 @@ __device__ void stats_settle(const StatsParams& p, unsigned ctas, StatsScratch& 
     }
     const unsigned long long n_f = p.n - nonfin;
     int e0 = 0;
-    const bool settled = decide_e0(S, n_f, &e0);
-    p.ctrl->e0 = e0;  // when not settled: the lower end's e0, the exact sums' window anchor
-    p.ctrl->n_finite = n_f;
-    p.ctrl->exact_path = settled ? 0u : 1u;  // the encode kernel's first phase decides then
-    T.settled_e0 = settled ? e0 : -1;
+    const bool settled = decide_e0_pair(S, n_f, &e0);
+    if (threadIdx.x == 0) {
+      p.ctrl->e0 = e0;  // when not settled: the lower end's e0, the exact sums' window anchor
+      p.ctrl->n_finite = n_f;
+      p.ctrl->exact_path = settled ? 0u : 1u;  // the encode kernel's first phase decides then
+      T.settled_e0 = settled ? e0 : -1;
+    }
   }
   __syncthreads();
   if (!p.predict) return;

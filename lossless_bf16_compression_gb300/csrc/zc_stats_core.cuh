@@ -10,8 +10,8 @@
 //
 // Every block sum of 64 values carries a relative error below 2^-18 (at most 17 roundings, or 64
 // for the last n % 8 values, summed one by one), so a total over blocks lies within 2^-17 of the
-// exact sum; decide_e0 then settles e0 exactly for all but ~4e-5 of random tensors, and the exact
-// fallback decides the rest.
+// exact sum; decide_e0_pair then settles e0 exactly for all but ~4e-5 of random tensors, and the
+// exact fallback decides the rest.
 #pragma once
 
 #include "zc_common.cuh"
@@ -158,14 +158,15 @@ __device__ __forceinline__ void block_sum(uint32_t (&w)[W], double* acc, unsigne
 // The window rule at an fp64 estimate S_est of the sum of squares that lies within 2^-17 of the
 // exact sum: evaluated at S_est (1 -+ 2^-16), rounded outward, both ends give the exact e0 when
 // they agree (the rule is monotone in S).  Returns false when they do not: the exact sum decides.
-__device__ __forceinline__ bool decide_e0(double S_est, unsigned long long n_f, int* e0) {
-  *e0 = 0;
-  if (n_f == 0 || S_est == 0.0) return true;
-  const double lo = __dmul_rd(S_est, 1.0 - 0x1p-16);
-  const double hi = __dmul_ru(S_est, 1.0 + 0x1p-16);
-  const int elo = select_e0(lo, n_f), ehi = select_e0(hi, n_f);
-  *e0 = elo;
-  return elo == ehi;
+// One end per lane: lanes 0 and 1 of a warp call it together, with the same S_est and n_f, and
+// both get the result (the fp64 division of each end runs in parallel); *e0 is the lower end's.
+__device__ __forceinline__ bool decide_e0_pair(double S_est, unsigned long long n_f, int* e0) {
+  int e = 0;
+  if (n_f != 0 && S_est != 0.0)
+    e = select_e0((threadIdx.x & 1) == 0 ? __dmul_rd(S_est, 1.0 - 0x1p-16) : __dmul_ru(S_est, 1.0 + 0x1p-16), n_f);
+  const int lo = __shfl_sync(0x3u, e, 0), hi = __shfl_sync(0x3u, e, 1);
+  *e0 = lo;
+  return lo == hi;
 }
 
 // Per-exponent integer sums of sig^2 of the finite values x[i], i = start, start + stride, ..
