@@ -120,7 +120,8 @@ struct Control {
   unsigned long long spec_nonfinite;
   unsigned spec_chunks;
   unsigned spec_untrusted;
-  unsigned reserved[22];
+  unsigned grid_guesses_held;  // the cooperative grid: 1 when every CTA coded with the settled e0
+  unsigned reserved[21];
   // 1: the speculative encode kernel did not speculate (its sample was not confident) or found
   // its guess wrong: the statistics and encode kernels after it do the job.
   unsigned fallback;

@@ -79,6 +79,8 @@ struct __align__(128) ResidentSmem {
   int e0;
   int need_exact;
   int ok;
+  int guess;      // the cooperative grid, auto mode: this CTA's own e0, coded with at once
+  int held;       // ... and whether every CTA's was the settled e0
   // last, for cluster launches only (the grid launch does not allocate them): the fixed parts,
   // kept here until the stream's form is known (the grid launch stores them in place at once),
   // and every CTA's partial and sections' sizes, pushed here by their CTAs before the barrier
@@ -89,6 +91,7 @@ struct __align__(128) ResidentSmem {
   unsigned all_size[kSmallCtas * kPerCta];
 };
 constexpr size_t kGridSmemBytes = offsetof(ResidentSmem, fixed);
+static_assert(kMaxGridCtas <= 8 * 256, "a cooperative grid's e0 per CTA fits the exponent-sample region");
 
 // The exchange between the CTAs of a cluster: distributed shared memory, cluster barriers.
 struct ClusterExchange {
@@ -110,21 +113,27 @@ struct ClusterExchange {
     for (unsigned q = 0; q < ctas(); ++q) t += cl.map_shared_rank(S.bins, q)[e];
     return t;
   }
-  // Every CTA combines the partials in the same fixed order (thread t takes CTAs t, t + 32, ..,
-  // then a fixed tree), so every CTA settles the same e0.  Thread t pushes this CTA's partial to
-  // CTA t before the barrier; after it each CTA reads them from its own shared memory.
-  __device__ bool settle(ResidentSmem& S, double s_cta, unsigned long long nf_cta, uint64_t n) {
-    if (threadIdx.x == 0) put_partial(S, s_cta, nf_cta);
-    bar_cta();
-    const unsigned G = ctas(), r = rank();
-    if (threadIdx.x < G) {
-      cl.map_shared_rank(S.all_sum, threadIdx.x)[r] = S.cta_sum;
-      cl.map_shared_rank(S.all_nf, threadIdx.x)[r] = S.cta_nonfinite;
+  // Thread t pushes this CTA's partial (put_partial, then a CTA barrier) or its sections' sizes
+  // (S.my_size, complete: the coding loop ends with a CTA barrier) to CTA t, before the barrier
+  // that publishes them; after it each CTA reads them from its own shared memory.
+  __device__ void push_partial(ResidentSmem& S) {
+    if (threadIdx.x < ctas()) {
+      cl.map_shared_rank(S.all_sum, threadIdx.x)[rank()] = S.cta_sum;
+      cl.map_shared_rank(S.all_nf, threadIdx.x)[rank()] = S.cta_nonfinite;
     }
-    sync();
+  }
+  __device__ void push_sizes(ResidentSmem& S, uint64_t first, unsigned mine) {
+    if (threadIdx.x < ctas()) {
+      unsigned* dst = cl.map_shared_rank(S.all_size, threadIdx.x);
+      for (unsigned j = 0; j < mine; ++j) dst[first + j] = S.my_size[j];
+    }
+  }
+  // Every CTA combines the partials in the same fixed order (thread t takes CTAs t, t + 32, ..,
+  // then a fixed tree), so every CTA settles the same e0: S.e0, S.need_exact, S.n_finite.
+  __device__ void settle_local(ResidentSmem& S, uint64_t n) {
     double s = 0.0;
     unsigned long long nf_all = 0;
-    fixed_sum2(G, 1, S.wsum, S.wnf, &s, &nf_all, [&](uint64_t q, double& a, unsigned long long& b) {
+    fixed_sum2(ctas(), 1, S.wsum, S.wnf, &s, &nf_all, [&](uint64_t q, double& a, unsigned long long& b) {
       a += S.all_sum[q];
       b += S.all_nf[q];
     });
@@ -138,24 +147,36 @@ struct ClusterExchange {
       }
     }
     bar_cta();
-    return true;
   }
-  // The sizes of the chunks before this CTA's and of all: thread t pushes this CTA's sizes to CTA
-  // t before the barrier (S.my_size is complete: the coding loop ends with a CTA barrier), and
-  // each CTA reads them from its own shared memory after it.
-  __device__ bool offsets(ResidentSmem& S, uint64_t first, unsigned mine, unsigned, uint64_t N,
-                          unsigned long long* bef, unsigned long long* tot) {
-    if (threadIdx.x < ctas()) {
-      unsigned* dst = cl.map_shared_rank(S.all_size, threadIdx.x);
-      for (unsigned j = 0; j < mine; ++j) dst[first + j] = S.my_size[j];
-    }
-    sync();
+  // The sizes of the chunks before this CTA's and of all, in thread 0.
+  __device__ void offsets_local(ResidentSmem& S, uint64_t first, uint64_t N, unsigned long long* bef,
+                                unsigned long long* tot) {
     fixed_sum2(N, 2, S.wbefore, S.wtotal, bef, tot, [&](uint64_t c, unsigned long long& a, unsigned long long& b) {
       const unsigned long long sz = S.all_size[c];
       a += c < first ? sz : 0ull;
       b += sz;
     });
+  }
+  __device__ bool settle(ResidentSmem& S, double s_cta, unsigned long long nf_cta, uint64_t n) {
+    if (threadIdx.x == 0) put_partial(S, s_cta, nf_cta);
+    bar_cta();
+    push_partial(S);
+    sync();
+    settle_local(S, n);
     return true;
+  }
+  __device__ bool offsets(ResidentSmem& S, uint64_t first, unsigned mine, unsigned, uint64_t N,
+                          unsigned long long* bef, unsigned long long* tot) {
+    push_sizes(S, first, mine);
+    sync();
+    offsets_local(S, first, N, bef, tot);
+    return true;
+  }
+  // Cluster barriers are cheap: e0 is settled before any chunk is coded.
+  static constexpr bool kSpeculate = false;
+  __device__ bool settle_offsets(ResidentSmem&, double, unsigned long long, uint64_t, uint64_t, unsigned, int,
+                                 unsigned long long*, unsigned long long*) {
+    return false;
   }
   static constexpr bool kKeepFixed = true;  // no store to global memory before the last barrier
   __device__ void finish() {  // no CTA leaves while another may read its shared memory: order no memory
@@ -168,6 +189,7 @@ struct GridExchange {
   StatsPartial* partials;        // one per CTA
   unsigned long long* bins;      // 256, cleared by CTA 0 before the first barrier
   unsigned long long* totals;    // one per CTA (the scan-state slots, G <= N): escape bytes, then offsets
+  unsigned char* guesses;        // one per CTA: the e0 it coded with first (auto mode)
   Control* ctrl;                 // the barriers' counter and release word (cleared before the launch)
   unsigned* arrivals;
   int* status;
@@ -215,6 +237,44 @@ struct GridExchange {
       *bef = __ldcg(totals + blockIdx.x);
       *tot = __ldcg(&ctrl->grid_escape_bytes);
     }
+    return true;
+  }
+  // Grid barriers are dear (a few microseconds each): each CTA codes at once with its own e0 (the
+  // rule at its own partial), and one barrier settles e0 and turns the sizes into offsets; when
+  // every CTA's own e0 was the settled one (S.held), that barrier did for both.
+  static constexpr bool kSpeculate = true;
+  __device__ bool settle_offsets(ResidentSmem& S, double s_cta, unsigned long long nf_cta, uint64_t n, uint64_t,
+                                 unsigned mine, int own_e0, unsigned long long* bef, unsigned long long* tot) {
+    if (threadIdx.x == 0) {
+      put_partial(S, s_cta, nf_cta);
+      guesses[blockIdx.x] = static_cast<unsigned char>(own_e0);
+      unsigned long long t = 0;
+      for (unsigned j = 0; j < mine; ++j) t += S.my_size[j];
+      totals[blockIdx.x] = t;
+    }
+    ++passed;
+    if (!grid_barrier_last(arrivals, passed * gridDim.x, &ctrl->grid_release, passed, status, kDefaultSpinLimit,
+                           [&] {
+                             settle_e0_work(partials, gridDim.x, n, ctrl, S.wsum, S.wnf);
+                             bar_cta();  // the settled e0, written by thread 0
+                             const unsigned e = static_cast<unsigned>(__ldcg(&ctrl->grid_e0));
+                             bool same = true;
+                             for (unsigned q = threadIdx.x; q < gridDim.x; q += kSmallThreads)
+                               same = same && __ldcg(guesses + q) == e;
+                             same = __syncthreads_and(same);
+                             if (threadIdx.x == 0) ctrl->grid_guesses_held = same ? 1u : 0u;
+                             scan_totals_work(totals, gridDim.x, ctrl, S.wbefore);
+                           }))
+      return false;
+    if (threadIdx.x == 0) {
+      S.e0 = __ldcg(&ctrl->grid_e0);
+      S.need_exact = static_cast<int>(__ldcg(&ctrl->grid_exact));
+      S.n_finite = __ldcg(&ctrl->n_finite);
+      S.held = !S.need_exact && __ldcg(&ctrl->grid_guesses_held) != 0;
+      *bef = __ldcg(totals + blockIdx.x);
+      *tot = __ldcg(&ctrl->grid_escape_bytes);
+    }
+    bar_cta();
     return true;
   }
   static constexpr bool kKeepFixed = false;  // fixed parts stored in place while coding
@@ -269,8 +329,15 @@ __device__ void compress_resident(Exchange& X, ResidentSmem& S, const uint16_t* 
   if (!S.ok && tid == 0) mbar_wait(&S.mbar, 0, kSmallWaitLimit);  // never leave a copy in flight
   // (a CTA whose copies did not arrive still takes part in every barrier below, with zeros)
 
-  // ---- the window base
+  // ---- the window base.  Auto mode: this CTA's partial sum of squares.  In a cooperative grid
+  // (Exchange::kSpeculate) the CTA codes at once with its own e0 -- the rule at its own partial --
+  // and the barrier that publishes the sections' sizes publishes the partials and those e0 too:
+  // when every CTA's was the settled e0, one barrier did for both; otherwise the chunks are coded
+  // again with the settled (or exact) e0.
   int e0 = base;
+  int guess = -1;
+  double s_cta = 0.0;  // (thread 0)
+  unsigned long long nf_cta = 0;
   if (base < 0) {
     double acc = 0.0;
     unsigned nonfinite = 0;
@@ -299,97 +366,125 @@ __device__ void compress_resident(Exchange& X, ResidentSmem& S, const uint16_t* 
       S.wnf[warp] = nf;
     }
     bar_cta();
-    double s_cta = 0.0;  // (thread 0)
-    unsigned long long nf_cta = 0;
     if (tid == 0)
       for (int i = 0; i < kWarpsPerCta; ++i) {
         s_cta += S.wsum[i];
         nf_cta += S.wnf[i];
       }
-    if (!X.settle(S, s_cta, nf_cta, n)) return;  // S.e0, S.need_exact, S.n_finite
-    if (S.need_exact) {  // the same in every CTA: exact per-exponent sums over all CTAs
-      for (unsigned e = tid; e < 256; e += kSmallThreads) S.bins[e] = 0;
+    if (Exchange::kSpeculate) {
+      if (tid == 0) {
+        unsigned long long values = 0;
+        for (unsigned j = 0; j < mine; ++j) values += chunk_values(n, first + j);
+        S.guess = select_e0(s_cta, values - nf_cta);
+      }
       bar_cta();
-      for (unsigned j = 0; j < mine; ++j)
-        add_exponent_sums(reinterpret_cast<const uint16_t*>(S.x[j]), chunk_values(n, first + j), tid, kSmallThreads,
-                          S.bins);
-      bar_cta();
-      X.share_bins(S);
-      if (!X.sync()) return;
-      unsigned long long t[2] = {0, 0};
-      for (unsigned e = tid, i = 0; e < 256; e += kSmallThreads, ++i) t[i] = X.all_bins(S, e);
-      if (!X.sync()) return;  // every CTA has read the others' bins before any overwrites its own
-      for (unsigned e = tid, i = 0; e < 256; e += kSmallThreads, ++i) S.bins[e] = t[i];
-      bar_cta();
-      if (tid == 0) S.e0 = select_e0(exact_from_bins(S.bins), S.n_finite);
-      bar_cta();
+      guess = S.guess;
     }
+  }
+
+  // The exact per-exponent sums over all CTAs, when the estimate cannot settle e0 (the same in
+  // every CTA): S.e0 from S.bins.
+  auto exact_e0 = [&]() -> bool {
+    for (unsigned e = tid; e < 256; e += kSmallThreads) S.bins[e] = 0;
+    bar_cta();
+    for (unsigned j = 0; j < mine; ++j)
+      add_exponent_sums(reinterpret_cast<const uint16_t*>(S.x[j]), chunk_values(n, first + j), tid, kSmallThreads,
+                        S.bins);
+    bar_cta();
+    X.share_bins(S);
+    if (!X.sync()) return false;
+    unsigned long long t[2] = {0, 0};
+    for (unsigned e = tid, i = 0; e < 256; e += kSmallThreads, ++i) t[i] = X.all_bins(S, e);
+    if (!X.sync()) return false;  // every CTA has read the others' bins before any overwrites its own
+    for (unsigned e = tid, i = 0; e < 256; e += kSmallThreads, ++i) S.bins[e] = t[i];
+    bar_cta();
+    if (tid == 0) S.e0 = select_e0(exact_from_bins(S.bins), S.n_finite);
+    bar_cta();
+    return true;
+  };
+
+  // ---- code this CTA's chunks with e: fixed parts to their places, escape sections into shared
+  // memory, their sizes to S.my_size
+  auto code_chunks = [&](int e) {
+    const uint32_t kadd = ((256u - static_cast<unsigned>(e)) << 7) * 0x00010001u;
+    const unsigned v0 = 32 * tid;
+    for (unsigned j = 0; j < mine; ++j) {
+      const uint64_t c = first + j;
+      const unsigned m = chunk_values(n, c);
+      const bool full = m == kChunk;
+      const unsigned cbytes = full ? kFullCodeBytes : static_cast<unsigned>(code_section_bytes(m));
+      const unsigned smbytes = full ? kChunk : static_cast<unsigned>(pad16(m));
+      uint4 xv[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) xv[q] = S.x[j][4 * tid + q];
+      Coded32 kd;
+      code32(xv, kadd, v0, m, full, kd);
+      // (a ragged chunk's threads past m store zero codes and bytes: the sections' padding)
+      store_fixed32(Exchange::kKeepFixed ? reinterpret_cast<uint8_t*>(S.fixed[j]) : out + R0 + c * kFullFixedBytes,
+                    cbytes, smbytes, v0, full, kd);
+      const unsigned cnt = __popc(kd.e[0]) + __popc(kd.e[1]) + __popc(kd.e[2]) + __popc(kd.e[3]);
+      // ranks: a warp scan of the counts, then the warps' totals
+      unsigned x = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned t = __shfl_up_sync(0xFFFFFFFFu, x, o);
+        if (lane >= static_cast<unsigned>(o)) x += t;
+      }
+      if (lane == 31) S.scan[warp] = x;
+      bar_cta();
+      unsigned before = 0, k = 0;
+#pragma unroll
+      for (int i = 0; i < kWarpsPerCta; ++i) {
+        before += i < static_cast<int>(warp) ? S.scan[i] : 0u;
+        k += S.scan[i];
+      }
+      const unsigned base_rank = before + x - cnt;
+      const bool plane = exponent_plane(m, k);
+      const unsigned esc_bytes = escape_section_bytes(m, k);
+      const uint32_t sec = smem_u32(S.sec[j]), xs = smem_u32(S.x[j]);
+      if (plane) {  // every exponent, in value order (values past m are zero: the padding)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t lo = prmt((xv[q].x >> 7) & 0x00FF00FFu, (xv[q].y >> 7) & 0x00FF00FFu, 0x6420);
+          const uint32_t hi = prmt((xv[q].z >> 7) & 0x00FF00FFu, (xv[q].w >> 7) & 0x00FF00FFu, 0x6420);
+          if (v0 + 8 * q < esc_bytes) sts_v2(sec + v0 + 8 * q, lo, hi);
+        }
+      } else {
+        unsigned m32 = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) m32 |= compact8(kd.e[q]) << (8 * q);
+        write_list32(m32, cnt, v0, base_rank, k, sec, false,
+                     [&](unsigned b) { return lds_u16(xs + 2 * (v0 + b)) >> 7; });
+        if (tid < esc_bytes - 3 * k) sts_u8(sec + 3 * k + tid, 0);  // zero padding, < 16 bytes
+      }
+      if (tid == 0) S.my_size[j] = esc_bytes;
+      bar_cta();  // S.scan is free for the next chunk
+    }
+  };
+
+  // ---- e0, the coding, and the sections' offsets: the sizes of the chunks before this CTA's,
+  // and the stream's length (thread 0)
+  unsigned long long bef = 0, tot = 0;
+  bool coded_with_e0 = false;
+  if (guess >= 0) {
+    code_chunks(guess);
+    if (!X.settle_offsets(S, s_cta, nf_cta, n, first, mine, guess, &bef, &tot)) return;
+    coded_with_e0 = S.held != 0;  // the same in every CTA
+  } else if (base < 0) {
+    if (!X.settle(S, s_cta, nf_cta, n)) return;  // S.e0, S.need_exact, S.n_finite
+  }
+  if (base < 0) {
+    if (!coded_with_e0 && S.need_exact && !exact_e0()) return;
     e0 = S.e0;
     if (r == 0 && tid == 0) {
       ctrl->e0 = e0;
       ctrl->exact_path = S.need_exact;
     }
   }
-
-  // ---- code this CTA's chunks: fixed parts to their places, escape sections into shared memory
-  const uint32_t kadd = ((256u - static_cast<unsigned>(e0)) << 7) * 0x00010001u;
-  const unsigned v0 = 32 * tid;
-  for (unsigned j = 0; j < mine; ++j) {
-    const uint64_t c = first + j;
-    const unsigned m = chunk_values(n, c);
-    const bool full = m == kChunk;
-    const unsigned cbytes = full ? kFullCodeBytes : static_cast<unsigned>(code_section_bytes(m));
-    const unsigned smbytes = full ? kChunk : static_cast<unsigned>(pad16(m));
-    uint4 xv[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) xv[q] = S.x[j][4 * tid + q];
-    Coded32 kd;
-    code32(xv, kadd, v0, m, full, kd);
-    // (a ragged chunk's threads past m store zero codes and bytes: the sections' padding)
-    store_fixed32(Exchange::kKeepFixed ? reinterpret_cast<uint8_t*>(S.fixed[j]) : out + R0 + c * kFullFixedBytes,
-                  cbytes, smbytes, v0, full, kd);
-    const unsigned cnt = __popc(kd.e[0]) + __popc(kd.e[1]) + __popc(kd.e[2]) + __popc(kd.e[3]);
-    // ranks: a warp scan of the counts, then the warps' totals
-    unsigned x = cnt;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const unsigned t = __shfl_up_sync(0xFFFFFFFFu, x, o);
-      if (lane >= static_cast<unsigned>(o)) x += t;
-    }
-    if (lane == 31) S.scan[warp] = x;
-    bar_cta();
-    unsigned before = 0, k = 0;
-#pragma unroll
-    for (int i = 0; i < kWarpsPerCta; ++i) {
-      before += i < static_cast<int>(warp) ? S.scan[i] : 0u;
-      k += S.scan[i];
-    }
-    const unsigned base_rank = before + x - cnt;
-    const bool plane = exponent_plane(m, k);
-    const unsigned esc_bytes = escape_section_bytes(m, k);
-    const uint32_t sec = smem_u32(S.sec[j]), xs = smem_u32(S.x[j]);
-    if (plane) {  // every exponent, in value order (values past m are zero: the padding)
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const uint32_t lo = prmt((xv[q].x >> 7) & 0x00FF00FFu, (xv[q].y >> 7) & 0x00FF00FFu, 0x6420);
-        const uint32_t hi = prmt((xv[q].z >> 7) & 0x00FF00FFu, (xv[q].w >> 7) & 0x00FF00FFu, 0x6420);
-        if (v0 + 8 * q < esc_bytes) sts_v2(sec + v0 + 8 * q, lo, hi);
-      }
-    } else {
-      unsigned m32 = 0;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) m32 |= compact8(kd.e[q]) << (8 * q);
-      write_list32(m32, cnt, v0, base_rank, k, sec, false,
-                   [&](unsigned b) { return lds_u16(xs + 2 * (v0 + b)) >> 7; });
-      if (tid < esc_bytes - 3 * k) sts_u8(sec + 3 * k + tid, 0);  // zero padding, < 16 bytes
-    }
-    if (tid == 0) S.my_size[j] = esc_bytes;
-    bar_cta();  // S.scan is free for the next chunk
+  if (!coded_with_e0) {
+    code_chunks(e0);
+    if (!X.offsets(S, first, mine, J, N, &bef, &tot)) return;
   }
-
-  // ---- the sections' offsets: the sizes of the chunks before this CTA's, and the stream's length
-  unsigned long long bef = 0, tot = 0;  // (thread 0)
-  if (!X.offsets(S, first, mine, J, N, &bef, &tot)) return;
   if (tid == 0) {
     unsigned long long at = E0 + bef;
     for (unsigned j = 0; j < mine; ++j) {
@@ -459,6 +554,7 @@ __global__ void __launch_bounds__(kSmallThreads) medium_kernel(const uint16_t* i
   X.partials = reinterpret_cast<StatsPartial*>(ws + kWsControlBytes);
   X.bins = reinterpret_cast<unsigned long long*>(ws + kWsExactBinsOffset);
   X.totals = reinterpret_cast<unsigned long long*>(ws + kWsControlBytes + kWsPartialsBytes);
+  X.guesses = ws + kWsSampleOffset;  // (the statistics kernel's exponent sample; unused here)
   X.ctrl = reinterpret_cast<Control*>(ws);
   X.arrivals = &X.ctrl->grid_arrivals;
   X.status = status;

@@ -169,6 +169,91 @@ __device__ __forceinline__ bool decide_e0_pair(double S_est, unsigned long long 
   return lo == hi;
 }
 
+// The speculative routes' guess of e0 from a sample, by a group of kThreads threads (whole warps)
+// each holding W words (2W values) of it, `vals` of them real (the rest zero, at the end).  Per
+// warp: squares and fourth powers in fp32, scaled by 2^(126 - Es) from the warp's largest finite
+// magnitude (so no power overflows); Inf and NaN are counted out.  Thread 0 combines the warps in
+// fp64 and evaluates the rule (in fp32, the binary exponent taken out first) at the sample's mean
+// square q and at q (1 -+ d), d = 1/32 + 4 r (at most 3/4), r the mean square's relative standard
+// error estimated from the fourth powers; *guess is the e0 at q, *confident whether the three
+// agree and the sample has a finite nonzero value.  For a guess only: no error bound is claimed,
+// and the group's every thread sees the same answer after bar().  g2, g4, gk, gf: per-warp scratch.
+template <int kThreads, int W, typename Bar>
+__device__ void guess_e0(const uint32_t (&w)[W], unsigned vals, float* g2, float* g4, int* gk, unsigned* gf,
+                         int* guess, int* confident, Bar bar) {
+  constexpr int kWarpsG = kThreads / 32;
+  const unsigned tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int kVals = 2 * W;
+  unsigned mx = 0, nonfinite = 0;
+#pragma unroll
+  for (int i = 0; i < kVals; ++i) {
+    const unsigned a = (w[i >> 1] >> (16 * (i & 1))) & 0x7FFFu;
+    if (a >= 0x7F80u) ++nonfinite;
+    else mx = max(mx, a);
+  }
+  mx = __reduce_max_sync(0xFFFFFFFFu, mx);
+  const int Es = min(max(static_cast<int>(mx >> 7), 1), 252);
+  const float sc = __int_as_float((253 - Es) << 23);  // 2^(126 - Es)
+  float a2 = 0.f, a4 = 0.f, b2 = 0.f, b4 = 0.f;
+#pragma unroll
+  for (int i = 0; i < kVals; ++i) {
+    const uint32_t h = (w[i >> 1] >> (16 * (i & 1))) & 0xFFFFu;
+    const float x = (h & 0x7FFFu) >= 0x7F80u ? 0.f : __uint_as_float(h << 16) * sc;
+    const float x2 = x * x;
+    if (i & 1) {
+      b2 += x2;
+      b4 = fmaf(x2, x2, b4);
+    } else {
+      a2 += x2;
+      a4 = fmaf(x2, x2, a4);
+    }
+  }
+  float s2 = a2 + b2, s4 = a4 + b4;
+  unsigned fin = vals - nonfinite;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    s2 += __shfl_xor_sync(0xFFFFFFFFu, s2, o);
+    s4 += __shfl_xor_sync(0xFFFFFFFFu, s4, o);
+    fin += __shfl_xor_sync(0xFFFFFFFFu, fin, o);
+  }
+  if (lane == 0) {
+    g2[warp] = s2;
+    g4[warp] = s4;
+    gk[warp] = Es - 126;
+    gf[warp] = fin;
+  }
+  bar();
+  if (tid == 0) {
+    double Sd = 0.0, Qd = 0.0;  // the true sums: x^2 and x^4 times 2^(2k), 2^(4k)
+    unsigned m = 0;
+    for (int i = 0; i < kWarpsG; ++i) {
+      Sd += static_cast<double>(g2[i]) * __longlong_as_double(static_cast<long long>(1023 + 2 * gk[i]) << 52);
+      Qd += static_cast<double>(g4[i]) * __longlong_as_double(static_cast<long long>(1023 + 4 * gk[i]) << 52);
+      m += gf[i];
+    }
+    int e_at[3] = {0, 0, 0};
+    bool conf = false;
+    if (m > 0 && Sd > 0.0) {
+      const int kS = ilogb_pos(Sd);  // Sd = Sn 2^kS, Sn in [1, 2)
+      const float Sn = static_cast<float>(Sd * __longlong_as_double(static_cast<long long>(1023 - kS) << 52));
+      const float Qn = static_cast<float>(Qd * __longlong_as_double(static_cast<long long>(1023 - 2 * kS) << 52));
+      const float fm = static_cast<float>(m);
+      const float d = fminf(1.0f / 32 + 4.0f * sqrtf(fmaxf(Qn / (Sn * Sn) * fm - 1.0f, 0.0f) / fm), 0.75f);
+      const float y = Sn / fm * static_cast<float>(kWindowC2);  // the rule's y, times 2^-kS
+#pragma unroll
+      for (int t = 0; t < 3; ++t) {
+        const float yt = y * (t == 0 ? 1.0f - d : t == 1 ? 1.0f : 1.0f + d);
+        const int e = floor_half(static_cast<int>((__float_as_uint(yt) >> 23) & 0xFF) - 127 + kS) + 127;
+        e_at[t] = e < 0 ? 0 : (e > kE0Max ? kE0Max : e);
+      }
+      conf = e_at[0] == e_at[1] && e_at[2] == e_at[1];
+    }
+    *guess = e_at[1];
+    *confident = conf;
+  }
+  bar();
+}
+
 // Per-exponent integer sums of sig^2 of the finite values x[i], i = start, start + stride, ..
 // < count, added into bins[E] (shared, 256 words; E = 0 and 1 share bin 1).
 __device__ __forceinline__ void add_exponent_sums(const uint16_t* x, uint64_t count, uint64_t start, uint64_t stride,

@@ -177,3 +177,23 @@ def test_static_scratch_entry_takes_the_speculative_path():
     assert kernels == SPEC_KERNELS
     total = int(ob.item())
     assert out[:total].cpu().numpy().tobytes() == oracle.compress(x).tobytes()
+
+
+@pytest.mark.parametrize("n", [3 * 4096 + 17, 40 * 4096 + 5, (1 << 21) + 4096 * 3 + 1, (1 << 23) + 9, (1 << 24) + 77])
+def test_single_launch_own_e0_differs(n):
+    """The cooperative grid codes each CTA's chunks at once with that CTA's own e0 (the rule at its
+    own partial) and settles the tensor's e0 at the barrier that also publishes the sections'
+    sizes.  Here the first half is N(0, 1) and the second N(0, 16^2): the halves' own e0 (122 and
+    126) both differ from the tensor's (125), so the chunks are coded again with 125.  (The
+    cluster and the L2-resident kernel settle e0 before coding: the same tensor as a check.)"""
+    x = np.concatenate([gaussian(n // 2, 51), gaussian(n - n // 2, 52, 16.0)])
+    assert oracle.choose_e0(x) == 125
+    s, _, _ = compress_checked(x)
+    assert s[6] == 12 and s[7] == 125
+
+
+@pytest.mark.parametrize("n", [1, 7, 8, 4096 * 2 + 3, 40 * 4096 + 5, (1 << 20) + 3, (1 << 23) + 9, (1 << 25) - 5])
+def test_single_launch_guess_holds(n):
+    """Tiny to 2^25 - 5 values (every single-launch kernel): the stream, e0 included, is the
+    oracle's."""
+    compress_checked(gaussian(n, 41 + n % 89))
