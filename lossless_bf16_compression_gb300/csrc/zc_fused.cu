@@ -9,13 +9,15 @@
 // GB300 design.  G CTAs of 128 threads, as many as the device holds at once, launched
 // cooperatively so that all are resident; CTA r owns the contiguous chunks r J .. r J + J - 1.
 //  1. Statistics: the statistics kernel's fp32 blocks of 64 values with the same error bound, one
-//     partial per CTA; the last CTA to reach the barrier adds them up in one fixed order and
-//     settles e0 for all -- or, when the bound straddles a switching point, the exact
-//     per-exponent sums decide it after one more such barrier.
-//  2. Count: one warp per chunk counts its escapes under e0 exactly as the coding does, giving
-//     the escape section's size; the last CTA to reach the barrier turns the CTAs' totals into
-//     their sections' offsets (an exclusive scan) and the stream's length, so the form is known
-//     before anything is written.
+//     partial per CTA, and the CTA's own e0 (the window rule at its own partial).
+//  2. Count: one warp per chunk counts its escapes exactly as the coding does, giving the escape
+//     section's size, under the CTA's own e0 in auto mode.  The last CTA to reach the barrier
+//     adds the partials up in one fixed order and settles e0 for all, checks every CTA's own e0
+//     against it, and turns the CTAs' totals into their sections' offsets (an exclusive scan)
+//     and the stream's length, so the form is known before anything is written.  When some
+//     CTA's own e0 was not the settled one -- or the bound straddles a switching point and the
+//     exact per-exponent sums decide e0 after one more barrier -- the chunks are counted again
+//     under e0 and another barrier places them.
 //  3. Write: each chunk comes into a ring of four shared-memory slots by a bulk async copy, three
 //     chunks ahead of the coding (the first three during the statistics pass); the CTA codes it
 //     (a thread's 32 consecutive values, code32) and stores its fixed part, its escape section
@@ -58,6 +60,8 @@ struct FusedSmem {
   unsigned scan[2][kResidentWarps];          // the coding pass: warps' escape counts, by chunk parity
   int e0;
   int need_exact;
+  int own;   // auto mode: this CTA's own e0 (the rule at its own partial), counted with at once
+  int held;  // ... and whether every CTA's was the settled e0
 };
 
 struct FusedParams {
@@ -125,7 +129,7 @@ __device__ __forceinline__ void issue_chunk(FusedSmem& S, const uint16_t* x, uin
   if (bytes) bulk_load(S.ring[s], x + c * kChunk, bytes, &S.mbar[s]);
 }
 
-__global__ void __launch_bounds__(kThreads, 5) fused_kernel(const FusedParams p) {
+__global__ void __launch_bounds__(kThreads, 6) fused_kernel(const FusedParams p) {
   __shared__ FusedSmem S;
   const unsigned G = gridDim.x, r = blockIdx.x;
   const unsigned tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -136,10 +140,12 @@ __global__ void __launch_bounds__(kThreads, 5) fused_kernel(const FusedParams p)
   const uint64_t R0 = records_base(n), E0 = escape_base(n);
   Control* ctrl = reinterpret_cast<Control*>(p.ws);
   unsigned long long* gbins = reinterpret_cast<unsigned long long*>(p.ws + kWsExactBinsOffset);
-  // In the scan-state slots (8 bytes per chunk; G <= N / 2): the CTAs' partial sums, then, once
-  // the last CTA has read them all, their escape bytes and offsets.
+  // The CTAs' partial sums in the scan-state slots (8 bytes per chunk; G <= N / 2); their escape
+  // bytes, then offsets, in the statistics kernel's partials region (8 bytes per CTA); in auto
+  // mode, the e0 each CTA counted with first in the exponent-sample region (a byte per CTA).
   StatsPartial* partials = reinterpret_cast<StatsPartial*>(p.ws + kWsControlBytes + kWsPartialsBytes);
-  unsigned long long* totals = reinterpret_cast<unsigned long long*>(p.ws + kWsControlBytes + kWsPartialsBytes);
+  unsigned long long* totals = reinterpret_cast<unsigned long long*>(p.ws + kWsControlBytes);
+  unsigned char* guesses = p.ws + kWsSampleOffset;
   unsigned barriers = 0;
   auto sync_last = [&](auto work) {
     ++barriers;
@@ -191,15 +197,60 @@ __global__ void __launch_bounds__(kThreads, 5) fused_kernel(const FusedParams p)
     if (tid == 0) {
       partials[r].sum = s;
       partials[r].nonfinite = nf;
+      const uint64_t end = (first + mine) * kChunk < n ? (first + mine) * kChunk : n;
+      S.own = select_e0(s, end - first * kChunk - nf);  // the rule at this CTA's own values
     }
-    // the last CTA adds the partials up in one fixed order and settles e0 for all
-    if (!sync_last([&] { settle_e0_work(partials, G, n, ctrl, S.wsum, S.wnf); }))
+    bar_cta();
+  }
+
+  // ---- 2. every chunk's escape-section size under e, exactly; this CTA's total.  The chunks in
+  // the reverse order of the first pass: the last ones read are the likeliest still in the L2.
+  auto count_pass = [&](int e) {
+    const uint32_t ka = ((256u - static_cast<unsigned>(e)) << 7) * 0x00010001u;
+    unsigned long long mytotal = 0;  // lane 0 of each warp
+    for (unsigned jj = warp; jj < mine; jj += kResidentWarps) {
+      const unsigned j = mine - 1 - jj;
+      const unsigned sz = count_chunk(p.in, n, first + j, ka);
+      if (lane == 0) {
+        S.size[j] = sz;
+        mytotal += sz;
+      }
+    }
+    if (lane == 0) S.wtot[warp] = mytotal;
+    bar_cta();
+    if (tid == 0) {
+      unsigned long long t = 0;
+      for (int w = 0; w < kResidentWarps; ++w) t += S.wtot[w];
+      totals[r] = t;
+    }
+  };
+
+  // Auto mode: count at once with this CTA's own e0; the barrier whose last CTA settles the
+  // tensor's e0 also checks every CTA's own e0 against it and turns the totals into offsets.  When
+  // every CTA's was the settled one, that barrier did for both (a grid barrier costs a few
+  // microseconds); otherwise the exact sums (when needed) and a second count and barrier follow.
+  bool counted = false;
+  if (p.base < 0) {
+    count_pass(S.own);
+    if (tid == 0) guesses[r] = static_cast<unsigned char>(S.own);
+    if (!sync_last([&] {
+          settle_e0_work(partials, G, n, ctrl, S.wsum, S.wnf);
+          bar_cta();  // the settled e0, written by thread 0
+          const unsigned e = static_cast<unsigned>(__ldcg(&ctrl->grid_e0));
+          bool same = true;
+          for (unsigned q = tid; q < G; q += kThreads) same = same && __ldcg(guesses + q) == e;
+          same = __syncthreads_and(same);
+          if (tid == 0) ctrl->grid_guesses_held = same ? 1u : 0u;
+          scan_totals_work(totals, G, ctrl, S.wtot);
+        }))
       return abandon(0, kAhead);
     if (tid == 0) {
       S.e0 = __ldcg(&ctrl->grid_e0);
       S.need_exact = static_cast<int>(__ldcg(&ctrl->grid_exact));
+      S.held = !S.need_exact && __ldcg(&ctrl->grid_guesses_held) != 0;
     }
     bar_cta();
+    counted = S.held != 0;
     if (S.need_exact) {  // the same in every CTA: exact per-exponent sums over the grid
       for (unsigned e = tid; e < 256; e += kThreads) S.bins[e] = 0;
       bar_cta();
@@ -224,28 +275,12 @@ __global__ void __launch_bounds__(kThreads, 5) fused_kernel(const FusedParams p)
     }
   }
   const uint32_t kadd = ((256u - static_cast<unsigned>(e0)) << 7) * 0x00010001u;
-
-  // ---- 2. every chunk's escape-section size, exactly; this CTA's total.  The chunks in the
-  // reverse order of the first pass: the last ones read are the likeliest still in the L2.
-  unsigned long long mytotal = 0;  // lane 0 of each warp
-  for (unsigned jj = warp; jj < mine; jj += kResidentWarps) {
-    const unsigned j = mine - 1 - jj;
-    const unsigned sz = count_chunk(p.in, n, first + j, kadd);
-    if (lane == 0) {
-      S.size[j] = sz;
-      mytotal += sz;
-    }
+  if (!counted) {
+    count_pass(e0);
+    // the last CTA turns the totals into offsets from the escape region (an exclusive scan)
+    if (!sync_last([&] { scan_totals_work(totals, G, ctrl, S.wtot); }))
+      return abandon(0, kAhead);
   }
-  if (lane == 0) S.wtot[warp] = mytotal;
-  bar_cta();
-  if (tid == 0) {
-    unsigned long long t = 0;
-    for (int w = 0; w < kResidentWarps; ++w) t += S.wtot[w];
-    totals[r] = t;
-  }
-  // the last CTA turns the totals into offsets from the escape region (an exclusive scan)
-  if (!sync_last([&] { scan_totals_work(totals, G, ctrl, S.wtot); }))
-    return abandon(0, kAhead);
   if (tid == 0) {
     unsigned long long at = E0 + __ldcg(totals + r);
     for (unsigned j = 0; j < mine; ++j) {
