@@ -100,11 +100,15 @@ size_t zc_max_stream_bytes(size_t n);
  *                 form's exact length, with no host synchronization.  A tensor of up to 2^25
  *                 values compresses in one launch (a thread-block cluster or a cooperative
  *                 grid, every CTA resident from the start), which knows every chunk's escape
- *                 count before it writes a section.  A larger one runs a statistics kernel and
- *                 an encode kernel: the form is decided after the encoder's scan, or, in auto
- *                 mode when an exponent sample of the statistics pass predicts a raw stream,
- *                 by a pass that counts every chunk's escapes while it copies the values to
- *                 the raw form (the encoder then has nothing to do).  The bytes past
+ *                 count before it writes a section.  A larger one runs the encode kernel; in
+ *                 auto mode that kernel first guesses e0 from a 4096-value sample, codes with
+ *                 the guess and checks it against the rule on the whole tensor's sum of
+ *                 squares, which it takes while coding (the input is read once).  When the
+ *                 sample is not trusted or the guess does not hold, a statistics kernel and the
+ *                 encode kernel run again after it (they return at once otherwise): the form is
+ *                 then decided after the encoder's scan, or, when an exponent sample of the
+ *                 statistics pass predicts a raw stream, by a pass that counts every chunk's
+ *                 escapes while it copies the values to the raw form.  The bytes past
  *                 *out_bytes, including the workspace tail, are unspecified afterwards.  The
  *                 library keeps no per-call state outside `out`, so calls on different streams
  *                 with different buffers may run concurrently.  The encode kernel's CTAs wait
