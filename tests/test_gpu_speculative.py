@@ -136,6 +136,27 @@ def test_guess_wrong_falls_back_to_the_raw_form():
     assert route == 1 and s[6] == 0
 
 
+def test_guess_holds_and_the_stream_is_raw():
+    """Outside the sampled vectors, value pairs (a, b) become (sqrt(a^2 + b^2), 0): the sum of
+    squares and the finite count barely move, so the sample's e0 (122) holds, but half of those
+    values are now zeros -- escapes below the window -- so the chunks keep exponent planes and the
+    coded form is longer than the raw one.  The stream must come out raw, as the oracle's."""
+    n = SINGLE_MAX + 4096 * 7 + 5
+    f = (gaussian(n, 61).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    sampled = np.zeros(n, bool)
+    sampled[(sampled_positions(n)[:, None] + np.arange(8)[None, :]).ravel()] = True
+    a, b = f[0:n - 1:2].copy(), f[1:n:2].copy()
+    pair = ~sampled[0:n - 1:2] & ~sampled[1:n:2]
+    a[pair] = np.sign(a[pair]) * np.sqrt(a[pair] ** 2 + b[pair] ** 2)
+    b[pair] = 0.0
+    f[0:n - 1:2], f[1:n:2] = a, b
+    x = workloads.fp32_to_bf16_bits(f.astype(np.float32))
+    assert oracle.choose_e0(x) == 122
+    s, kernels, route = compress_checked(x)
+    assert kernels == SPEC_KERNELS
+    assert route == 0 and s[6] == 0 and s[7] == 122
+
+
 def test_sample_not_confident_on_random_patterns():
     """A sample that predicts a raw stream keeps the encode kernel from speculating at all."""
     n = SINGLE_MAX + 4096
