@@ -233,16 +233,7 @@ __global__ void __launch_bounds__(kThreads, 6) fused_kernel(const FusedParams p)
   if (p.base < 0) {
     count_pass(S.own);
     if (tid == 0) guesses[r] = static_cast<unsigned char>(S.own);
-    if (!sync_last([&] {
-          settle_e0_work(partials, G, n, ctrl, S.wsum, S.wnf);
-          bar_cta();  // the settled e0, written by thread 0
-          const unsigned e = static_cast<unsigned>(__ldcg(&ctrl->grid_e0));
-          bool same = true;
-          for (unsigned q = tid; q < G; q += kThreads) same = same && __ldcg(guesses + q) == e;
-          same = __syncthreads_and(same);
-          if (tid == 0) ctrl->grid_guesses_held = same ? 1u : 0u;
-          scan_totals_work(totals, G, ctrl, S.wtot);
-        }))
+    if (!sync_last([&] { settle_scan_work(partials, guesses, totals, G, n, ctrl, S.wsum, S.wnf, S.wtot, &S.own); }))
       return abandon(0, kAhead);
     if (tid == 0) {
       S.e0 = __ldcg(&ctrl->grid_e0);

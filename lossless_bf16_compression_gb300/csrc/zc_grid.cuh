@@ -206,5 +206,87 @@ __device__ void scan_totals_work(unsigned long long* totals, unsigned G, Control
   if (tid == 0) ctrl->grid_escape_bytes = all;
 }
 
+// Work for the last CTA of the one barrier that both settles e0 and places the sections (all its
+// threads): what settle_e0_work and scan_totals_work do, plus the check of every CTA's own e0
+// (guesses[q], the e0 CTA q counted or coded with) against the settled one -- with every load
+// (partials, own e0, totals) issued at once, so the work costs one memory round trip, not three.
+// Writes e0, the exact flag, the finite count, whether every CTA's own e0 was the settled one,
+// the offsets (in place of the totals) and the sections' total to the control block.
+// G <= kMaxGridCtas; e_shared: one int of shared memory.
+__device__ void settle_scan_work(const StatsPartial* partials, const unsigned char* guesses,
+                                 unsigned long long* totals, unsigned G, uint64_t n, Control* ctrl, double* wsum,
+                                 unsigned long long* wnf, unsigned long long* wtot, int* e_shared) {
+  const unsigned tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const unsigned per = (G + kResidentThreads - 1) / kResidentThreads, lo = min(tid * per, G), hi = min(lo + per, G);
+  double v[kGridPerThread];
+  unsigned long long c[kGridPerThread], t[kGridPerThread];
+  unsigned g[kGridPerThread];
+#pragma unroll
+  for (unsigned i = 0; i < kGridPerThread; ++i) {  // all loads in flight at once
+    const unsigned q = tid + kResidentThreads * i;
+    v[i] = q < G ? __ldcg(&partials[q].sum) : 0.0;
+    c[i] = q < G ? __ldcg(&partials[q].nonfinite) : 0ull;
+    g[i] = q < G ? __ldcg(guesses + q) : 0u;
+    t[i] = lo + i < hi ? __ldcg(totals + lo + i) : 0ull;
+  }
+  // e0 from the partials, in one fixed order (as settle_e0_work)
+  double a = 0.0;
+  unsigned long long b = 0;
+#pragma unroll
+  for (unsigned i = 0; i < kGridPerThread; ++i) {
+    a += v[i];
+    b += c[i];
+  }
+  const double S_all = cta_sum(a, wsum);
+  const unsigned long long nf_all = cta_sum(b, wnf);
+  if (tid < 2) {
+    const unsigned long long n_f = n - nf_all;
+    int e = 0;
+    if (n_f != 0 && S_all != 0.0)
+      e = select_e0(tid == 0 ? __dmul_rd(S_all, 1.0 - 0x1p-16) : __dmul_ru(S_all, 1.0 + 0x1p-16), n_f);
+    const int e_hi = __shfl_sync(0x3u, e, 1);
+    if (tid == 0) {
+      ctrl->grid_e0 = e;
+      ctrl->grid_exact = e != e_hi ? 1u : 0u;
+      ctrl->n_finite = n_f;
+      *e_shared = e;
+    }
+  }
+  bar_cta();
+  // every CTA's own e0 against the settled one
+  const unsigned e = static_cast<unsigned>(*e_shared);
+  bool same = true;
+#pragma unroll
+  for (unsigned i = 0; i < kGridPerThread; ++i)
+    if (tid + kResidentThreads * i < G) same = same && g[i] == e;
+  same = __syncthreads_and(same);
+  if (tid == 0) ctrl->grid_guesses_held = same ? 1u : 0u;
+  // the totals' exclusive prefix sums (as scan_totals_work)
+  unsigned long long run = 0;
+#pragma unroll
+  for (unsigned i = 0; i < kGridPerThread; ++i) run += t[i];
+  unsigned long long x = run;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long u = __shfl_up_sync(0xFFFFFFFFu, x, o);
+    if (lane >= static_cast<unsigned>(o)) x += u;
+  }
+  if (lane == 31) wtot[warp] = x;
+  bar_cta();
+  unsigned long long at = x - run, all = 0;
+#pragma unroll
+  for (int w = 0; w < kResidentWarps; ++w) {
+    at += w < static_cast<int>(warp) ? wtot[w] : 0ull;
+    all += wtot[w];
+  }
+#pragma unroll
+  for (unsigned i = 0; i < kGridPerThread; ++i)
+    if (lo + i < hi) {
+      totals[lo + i] = at;
+      at += t[i];
+    }
+  if (tid == 0) ctrl->grid_escape_bytes = all;
+}
+
 }  // namespace
 }  // namespace zc

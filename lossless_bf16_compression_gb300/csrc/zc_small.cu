@@ -255,15 +255,8 @@ struct GridExchange {
     ++passed;
     if (!grid_barrier_last(arrivals, passed * gridDim.x, &ctrl->grid_release, passed, status, kDefaultSpinLimit,
                            [&] {
-                             settle_e0_work(partials, gridDim.x, n, ctrl, S.wsum, S.wnf);
-                             bar_cta();  // the settled e0, written by thread 0
-                             const unsigned e = static_cast<unsigned>(__ldcg(&ctrl->grid_e0));
-                             bool same = true;
-                             for (unsigned q = threadIdx.x; q < gridDim.x; q += kSmallThreads)
-                               same = same && __ldcg(guesses + q) == e;
-                             same = __syncthreads_and(same);
-                             if (threadIdx.x == 0) ctrl->grid_guesses_held = same ? 1u : 0u;
-                             scan_totals_work(totals, gridDim.x, ctrl, S.wbefore);
+                             settle_scan_work(partials, guesses, totals, gridDim.x, n, ctrl, S.wsum, S.wnf,
+                                              S.wbefore, &S.guess);
                            }))
       return false;
     if (threadIdx.x == 0) {
