@@ -198,7 +198,7 @@ __global__ void __launch_bounds__(kThreads, 6) fused_kernel(const FusedParams p)
       partials[r].sum = s;
       partials[r].nonfinite = nf;
       const uint64_t end = (first + mine) * kChunk < n ? (first + mine) * kChunk : n;
-      S.own = select_e0(s, end - first * kChunk - nf);  // the rule at this CTA's own values
+      S.own = rough_e0(s, end - first * kChunk - nf);  // the rule at this CTA's own values
     }
     bar_cta();
   }

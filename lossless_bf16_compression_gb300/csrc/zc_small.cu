@@ -368,7 +368,7 @@ __device__ void compress_resident(Exchange& X, ResidentSmem& S, const uint16_t* 
       if (tid == 0) {
         unsigned long long values = 0;
         for (unsigned j = 0; j < mine; ++j) values += chunk_values(n, first + j);
-        S.guess = select_e0(s_cta, values - nf_cta);
+        S.guess = rough_e0(s_cta, values - nf_cta);
       }
       bar_cta();
       guess = S.guess;

@@ -41,6 +41,18 @@ __device__ int select_e0(double S, unsigned long long n_f) {
   return e < 0 ? 0 : (e > kE0Max ? kE0Max : e);
 }
 
+// The window rule in fp32, for a guess only (the exact rule decides what is kept): the binary
+// exponent of S taken out first, so nothing overflows or underflows; a few fp32 operations
+// where select_e0's fp64 division takes far longer on this part.
+__device__ __forceinline__ int rough_e0(double S, unsigned long long n_f) {
+  if (n_f == 0 || !(S > 0.0)) return 0;
+  const int kS = ilogb_pos(S);  // S = Sn 2^kS, Sn in [1, 2)
+  const float Sn = static_cast<float>(S * __longlong_as_double(static_cast<long long>(1023 - kS) << 52));
+  const float y = Sn / static_cast<float>(n_f) * static_cast<float>(kWindowC2);  // the rule's y, times 2^-kS
+  const int e = floor_half(static_cast<int>((__float_as_uint(y) >> 23) & 0xFF) - 127 + kS) + 127;
+  return e < 0 ? 0 : (e > kE0Max ? kE0Max : e);
+}
+
 // Careful block sum for 64 values (32 words), one by one (used for the last n % 8 values): skips
 // Inf/NaN, and scales every square by 4^-(Emax'-E') relative to the largest exponent present, so
 // no fp32 overflow or underflow matters.  Returns the fp64 value of the block sum and adds the
