@@ -982,11 +982,9 @@ __device__ __noinline__ void spec_verdict(EncodeSmem& S, const EncodeParams& p, 
     const double S_all = __ldcg(&p.ctrl->spec_sum);
     const unsigned long long n_f = p.n - __ldcg(&p.ctrl->spec_nonfinite);
     int e = 0;
-    if (n_f != 0 && S_all != 0.0)
-      e = select_e0(tid == 0 ? __dmul_rd(S_all, 1.0 - 0x1p-16) : __dmul_ru(S_all, 1.0 + 0x1p-16), n_f);
-    const int e_hi = __shfl_sync(0x3u, e, 1);
+    const bool settled = decide_e0_pair(S_all, n_f, &e);
     if (tid == 0) {
-      const bool held = e == e_hi && e == e0 && __ldcg(&p.ctrl->spec_untrusted) == 0;
+      const bool held = settled && e == e0 && __ldcg(&p.ctrl->spec_untrusted) == 0;
       p.ctrl->e0 = e0;
       p.ctrl->n_finite = n_f;
       if (!held) p.ctrl->fallback = 1u;

@@ -160,12 +160,10 @@ __device__ void settle_e0_work(const StatsPartial* partials, unsigned G, uint64_
   if (tid < 2) {
     const unsigned long long n_f = n - nf_all;
     int e = 0;
-    if (n_f != 0 && S_all != 0.0)
-      e = select_e0(tid == 0 ? __dmul_rd(S_all, 1.0 - 0x1p-16) : __dmul_ru(S_all, 1.0 + 0x1p-16), n_f);
-    const int e_hi = __shfl_sync(0x3u, e, 1);
+    const bool settled = decide_e0_pair(S_all, n_f, &e);
     if (tid == 0) {
       ctrl->grid_e0 = e;
-      ctrl->grid_exact = e != e_hi ? 1u : 0u;
+      ctrl->grid_exact = settled ? 0u : 1u;
       ctrl->n_finite = n_f;
     }
   }
@@ -242,12 +240,10 @@ __device__ void settle_scan_work(const StatsPartial* partials, const unsigned ch
   if (tid < 2) {
     const unsigned long long n_f = n - nf_all;
     int e = 0;
-    if (n_f != 0 && S_all != 0.0)
-      e = select_e0(tid == 0 ? __dmul_rd(S_all, 1.0 - 0x1p-16) : __dmul_ru(S_all, 1.0 + 0x1p-16), n_f);
-    const int e_hi = __shfl_sync(0x3u, e, 1);
+    const bool settled = decide_e0_pair(S_all, n_f, &e);
     if (tid == 0) {
       ctrl->grid_e0 = e;
-      ctrl->grid_exact = e != e_hi ? 1u : 0u;
+      ctrl->grid_exact = settled ? 0u : 1u;
       ctrl->n_finite = n_f;
       *e_shared = e;
     }

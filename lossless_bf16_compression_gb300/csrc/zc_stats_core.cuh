@@ -167,15 +167,41 @@ __device__ __forceinline__ void block_sum(uint32_t (&w)[W], double* acc, unsigne
   *acc += static_cast<double>(blk) * __longlong_as_double(static_cast<long long>(1023 + 2 * Es - 252) << 52);
 }
 
+// The e0 both ends of decide_e0_pair's interval give, found in fp32 when it can be: with
+// Sn = S_est 2^-kS in [1, 2), y = Sn / n_f c^2 in fp32 is within 6 roundings (below 2^-21.4) of
+// its exact value, so y (1 -+ 2^-12) brackets the rule's fp64 y at S_est (1 -+ 2^-16) (each within
+// 2^-52 of exact) with room to spare; when both brackets fall in one bin of the rule (one power
+// of 4 of y), that bin's e0 is what the fp64 ends give.  Returns -1 otherwise (a bracket straddles
+// a switching point: the fp64 ends decide).
+__device__ __forceinline__ int settled_e0_fp32(double S_est, unsigned long long n_f) {
+  if (n_f == 0 || S_est == 0.0) return 0;  // as select_e0
+  const int kS = ilogb_pos(S_est);
+  const float Sn = static_cast<float>(S_est * __longlong_as_double(static_cast<long long>(1023 - kS) << 52));
+  const float y = Sn / static_cast<float>(n_f) * static_cast<float>(kWindowC2);  // the rule's y, times 2^-kS
+  int e[2];
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const float yt = y * (t == 0 ? 1.0f - 0x1p-12f : 1.0f + 0x1p-12f);
+    const int v = floor_half(static_cast<int>((__float_as_uint(yt) >> 23) & 0xFF) - 127 + kS) + 127;
+    e[t] = v < 0 ? 0 : (v > kE0Max ? kE0Max : v);
+  }
+  return e[0] == e[1] ? e[0] : -1;
+}
+
 // The window rule at an fp64 estimate S_est of the sum of squares that lies within 2^-17 of the
 // exact sum: evaluated at S_est (1 -+ 2^-16), rounded outward, both ends give the exact e0 when
 // they agree (the rule is monotone in S).  Returns false when they do not: the exact sum decides.
-// One end per lane: lanes 0 and 1 of a warp call it together, with the same S_est and n_f, and
-// both get the result (the fp64 division of each end runs in parallel); *e0 is the lower end's.
+// Lanes 0 and 1 of a warp call it together, with the same S_est and n_f, and both get the result;
+// *e0 is the lower end's.  Most estimates are settled by settled_e0_fp32; otherwise each lane
+// evaluates one end in fp64 (their divisions in parallel).
 __device__ __forceinline__ bool decide_e0_pair(double S_est, unsigned long long n_f, int* e0) {
-  int e = 0;
-  if (n_f != 0 && S_est != 0.0)
-    e = select_e0((threadIdx.x & 1) == 0 ? __dmul_rd(S_est, 1.0 - 0x1p-16) : __dmul_ru(S_est, 1.0 + 0x1p-16), n_f);
+  const int quick = settled_e0_fp32(S_est, n_f);
+  if (quick >= 0) {
+    *e0 = quick;
+    return true;
+  }
+  const int e =
+      select_e0((threadIdx.x & 1) == 0 ? __dmul_rd(S_est, 1.0 - 0x1p-16) : __dmul_ru(S_est, 1.0 + 0x1p-16), n_f);
   const int lo = __shfl_sync(0x3u, e, 0), hi = __shfl_sync(0x3u, e, 1);
   *e0 = lo;
   return lo == hi;
