@@ -218,6 +218,23 @@ def test_auto_base_at_binade_boundaries_large(n, k4):
     check_parity(x)
 
 
+@pytest.mark.parametrize("n,k4,rel", [(20_000, -8, 1e-4), (20_000, -3, -5e-5), ((1 << 20) + 3, -8, -1e-4),
+                                      ((1 << 24) + 5, -5, 5e-5), ((1 << 25) + 4096 * 2 + 7, -8, 1e-4)])
+def test_auto_base_near_binade_boundaries(n, k4, rel):
+    """Mean squares 5e-5 to 1e-4 from a switching point: closer than the margin of the quick fp32
+    check of the window rule (2^-12, about 2.4e-4), farther than the fp64 rule's interval (2^-16
+    plus the estimate's 2^-17): e0 is settled by the rule's two fp64 ends, with no exact sums, and
+    must be the oracle's -- in the cluster, the cooperative grid, the L2-resident kernel and the
+    statistics kernel."""
+    x = _near_boundary_tensor(k4, n, 300 + k4, rel)
+    st, out, total = gpu_compress(x)
+    assert st == zc.ZC_OK
+    assert out[7].item() == oracle.choose_e0(x)
+    ws = (zc.zc_max_stream_bytes(x.size) + 255) // 256 * 256
+    assert int(out[ws + 12:ws + 16].cpu().numpy().view(np.uint32)[0]) == 0, "the exact fallback ran"
+    check_parity(x)
+
+
 def test_supplied_base_matches_auto_stream():
     x = mixed(50_000, 4)
     s_auto = check_parity(x, -1)
