@@ -21,17 +21,20 @@
 // and after another barrier each knows its sections' offsets and the stream's length, then
 // writes the coded form (fixed parts, sections, offset table, header) or the raw form (the
 // values from shared memory, over anything written before the barrier).
-//  - Cluster (up to 16 CTAs, 64 chunks): every CTA reads the partials and sizes from the other
-//    CTAs' shared memory (distributed shared memory) and combines them itself; the barriers are
-//    the cluster's, in hardware.
+//  - Cluster (up to 16 CTAs, 64 chunks): before each barrier every CTA pushes its partial (or its
+//    sections' sizes) into every other CTA's shared memory (distributed shared memory), and each
+//    combines them itself after it; the barriers are the cluster's, in hardware.
 //  - Cooperative grid (as many CTAs as the device holds at once, launched cooperatively so that
-//    all are resident): partials, bins and per-CTA totals go through the call's workspace (slots
-//    each CTA writes before the barrier; the exact path's bins are cleared by CTA 0 before the
-//    first barrier).  The barriers count arrivals in the control block, cleared before the
-//    launch; at the two main ones the last CTA to arrive does the combining -- the sum of the
-//    partials and the window rule, the scan of the CTAs' totals into offsets -- and releases the
-//    others, so it is done once instead of by every CTA from every other CTA's slots.  The waits
-//    are bounded.
+//    all are resident): partials, bins, the CTAs' own e0 and per-CTA totals go through the
+//    call's workspace (slots each CTA writes before the barrier; the exact path's bins are
+//    cleared by CTA 0 before the first barrier).  The barriers count arrivals in the control
+//    block, cleared before the launch; the last CTA to arrive does the combining -- the sum of
+//    the partials and the window rule, the scan of the CTAs' totals into offsets -- and releases
+//    the others, so it is done once instead of by every CTA from every other CTA's slots.  A
+//    grid barrier costs microseconds, so in auto mode each CTA codes at once with its own e0
+//    (the rule at its own partial) and one barrier settles e0 and places the sections; when some
+//    CTA's own e0 was not the settled one, the chunks are coded again and a second barrier
+//    places them.  The waits are bounded.
 // Every CTA takes part in every barrier (a CTA whose copies did not arrive goes on with zeros
 // and sets the error); every wait that polls (the copies' mbarrier, the grid barriers) is
 // bounded, and a grid barrier that fails stops the CTAs (the cluster's never fail).
