@@ -219,3 +219,28 @@ def test_single_launch_guess_holds(n):
     """Tiny to 2^25 - 5 values (every single-launch kernel): the stream, e0 included, is the
     oracle's."""
     compress_checked(gaussian(n, 41 + n % 89))
+
+
+def test_concurrent_calls_on_two_streams():
+    """Two large tensors compressed at once on two streams, each with its own buffers: the
+    persistent encode kernels share the GPU, their CTAs wait only on work that running CTAs of
+    their own launch have taken, and each stream must be the oracle's (one speculates, the
+    other's sample is not trusted and takes the statistics route)."""
+    xs = [gaussian(SINGLE_MAX + 4096 * 3 + 5, 71), workloads.make("grad_bucket_4096x14336")]
+    devs = [to_device(x) for x in xs]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    torch.cuda.synchronize()
+    zc.status(reset=True)
+    outs = []
+    for xd, st in zip(devs, streams):
+        with torch.cuda.stream(st):
+            outs.append(zc.compress(xd, stream=st))
+    torch.cuda.synchronize()
+    assert zc.status(reset=True) == zc.ZC_OK
+    for x, xd, (out, ob) in zip(xs, devs, outs):
+        total = int(ob.item())
+        want = oracle.compress(x)
+        assert total == want.size and out[:total].cpu().numpy().tobytes() == want.tobytes()
+        back = zc.decompress(out, x.size)
+        assert zc.status(reset=True) == zc.ZC_OK
+        assert bool(torch.equal(back, xd))
