@@ -114,7 +114,10 @@ size_t zc_max_stream_bytes(size_t n);
  *                 with different buffers may run concurrently.  The encode kernel's CTAs wait
  *                 on one another (bounded) only for work that a CTA already running has taken,
  *                 so a concurrent kernel that delays some of them slows the call but does not
- *                 make it fail.
+ *                 make it fail.  The host picks the route from n and base_or_auto alone and
+ *                 the kernels reset their own state, so a call whose out_bytes is not pageable
+ *                 can be captured in a CUDA graph (after a first call on the device, which loads
+ *                 the kernels) and replayed on new contents of the same buffers.
  *   out_bytes     receives the stream length.  Device, managed or pinned host memory is
  *                 written by the last kernel (asynchronously).  Pageable host memory is also
  *                 accepted: the call then copies the length back and synchronizes `stream`.
