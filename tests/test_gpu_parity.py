@@ -166,13 +166,16 @@ def test_nonfinite_blocks_beyond_the_small_path(case):
     check_parity(x)
 
 
-def _near_boundary_tensor(k4, n, seed, rel):
+def _near_boundary_tensor(k4, n, seed, rel, zero_frac=0.0):
     """A tensor whose sum of squares is within ~1e-15 of (1 + rel) 4**k4 n / c^2, i.e. whose
-    mean square times c^2 sits `rel` away from a switching point of the window rule."""
+    mean square times c^2 sits `rel` away from a switching point of the window rule (with about
+    `zero_frac` of its values zero)."""
     rng = np.random.default_rng(seed)
     T = (4.0 ** k4) * n / oracle.window_constant() * (1.0 + rel)
     bulk = n - 48
     v = rng.standard_normal(bulk)
+    if zero_frac:
+        v[rng.random(bulk) < zero_frac] = 0.0
     v *= np.sqrt(T * (1 - 1e-3) / np.sum(v * v))
     x = workloads.fp32_to_bf16_bits(v.astype(np.float32))
     as_float = lambda b: float(np.array([int(b) << 16], np.uint32).view(np.float32)[0])  # noqa: E731
@@ -180,7 +183,8 @@ def _near_boundary_tensor(k4, n, seed, rel):
     R = T - float(np.sum(f * f))
     tail = []
     for _ in range(48):  # greedy: the largest BF16 whose square still fits in what is left
-        t = int(workloads.fp32_to_bf16_bits(np.array([np.sqrt(max(R, 0.0))], np.float32))[0])
+        r = min(np.sqrt(max(R, 0.0)), float(np.finfo(np.float32).max))  # (no overflow to Inf in the cast)
+        t = int(workloads.fp32_to_bf16_bits(np.array([r], np.float32))[0])
         while t > 0 and as_float(t) ** 2 > R:
             t -= 1
         tail.append(t)
@@ -203,12 +207,18 @@ def test_auto_base_at_binade_boundaries(k4, rel):
     check_parity(x)
 
 
-@pytest.mark.parametrize("n,k4", [((1 << 20) + 3, -8), (1 << 26, -3)])
-def test_auto_base_at_binade_boundaries_large(n, k4):
+@pytest.mark.parametrize("n,k4,zeros", [((1 << 20) + 3, -8, 0.0), (1 << 26, -3, 0.0),
+                                        ((1 << 25) + 3 * 4096 + 5, -114, 0.0),
+                                        ((1 << 25) + 3 * 4096 + 5, 118, 0.0),
+                                        ((1 << 25) + 4096 + 3, -8, 0.3)])
+def test_auto_base_at_binade_boundaries_large(n, k4, zeros):
     """Boundary tensors beyond the cluster launch: the exact sum runs over the whole grid (in the
-    cooperative-grid launch at 2^20 + 3 values, in the encode kernel's first phase at 2^26) and
-    must agree with the oracle."""
-    x = _near_boundary_tensor(k4, n, 200 + k4, 1e-9)
+    cooperative-grid launch at 2^20 + 3 values, in the encode kernel's first phase beyond 2^25)
+    and must agree with the oracle.  In the first phase, e0 = 13 puts the exact sums' 24-binade
+    window at its lowest anchor (exponent 1: subnormals inside it), e0 = 245 at its highest
+    (exponent 230), and a tensor with 30% zeros sends many values down the out-of-window path
+    that skips them."""
+    x = _near_boundary_tensor(k4, n, 200 + k4, 1e-9, zeros)
     st, out, total = gpu_compress(x)
     assert st == zc.ZC_OK
     stream = out[:total].cpu().numpy()
