@@ -459,7 +459,6 @@ __device__ __noinline__ void write_plane(const uint4* stage, unsigned sw, uint32
 //    exact length with the raw form's; when the coded one is longer it completes the raw form
 //    (header, length) and marks the stream done, so nothing is coded.  Otherwise (ties included)
 //    the coding writes the coded form over the copy.
-constexpr int kExactWindow = 24;
 constexpr int kFirstVecPerLane = kChunk / 8 / 32;  // 16 vectors of a chunk per lane
 constexpr unsigned kFirstBatch = 8;                // chunks a warp takes per ticket, at most
 
@@ -518,45 +517,14 @@ __device__ unsigned raw_chunk(const uint16_t* x, uint64_t n, uint64_t c, uint32_
   return 3 * k <= m ? static_cast<unsigned>(pad16(3 * k)) : static_cast<unsigned>(pad16(m));
 }
 
-// Exact sums, one warp: chunk c's values (zeros past n add nothing).  Two values of a word at a
-// time: their exponents (subnormals at 1) and d = E - Eb in 16-bit halves, clamped to the
-// window's width; a value inside the window adds (sig << d)^2 = sig^2 4^d (below 2^62, one
-// widening multiply) to a 96-bit sum of the chunk's terms kept in three 32-bit pieces with a
-// carry chain, folded into the 128-bit (lo, hi) at the chunk's end; a value outside has its sig
-// masked to 0 there and adds sig^2 to its exponent's bin instead (zeros and Inf/NaN add nothing).
-__device__ __forceinline__ void add96(unsigned& a0, unsigned& a1, unsigned& a2, unsigned long long t) {
-  asm("add.cc.u32 %0, %0, %3;\n\taddc.cc.u32 %1, %1, %4;\n\taddc.u32 %2, %2, 0;"
-      : "+r"(a0), "+r"(a1), "+r"(a2)
-      : "r"(static_cast<unsigned>(t)), "r"(static_cast<unsigned>(t >> 32)));
-}
-
+// Exact sums, one warp: chunk c's values (zeros past n add nothing), two at a time
+// (ExactWindow); the chunk's 96-bit window sum is folded into the thread's 128-bit (lo, hi) at
+// its end.
 __device__ void exact_chunk(const uint16_t* x, uint64_t n, uint64_t c, int Eb, unsigned long long& lo,
                             unsigned long long& hi, unsigned long long* bins) {
   const unsigned lane = threadIdx.x & 31;
-  auto to_bin = [&](unsigned b) {
-    const unsigned E = (b >> 7) & 0xFF;
-    if (E == 255 || (b & 0x7FFF) == 0) return;
-    const unsigned Ep = E ? E : 1, sig = E ? 128 + (b & 0x7F) : (b & 0x7F);
-    atomicAdd(bins + Ep, static_cast<unsigned long long>(sig * sig));
-  };
-  const uint32_t neg_eb = ((0x10000u - static_cast<unsigned>(Eb)) & 0xFFFFu) * 0x00010001u;
-  unsigned a0 = 0, a1 = 0, a2 = 0;
-  auto add_word = [&](uint32_t w) {
-    const uint32_t y = w & 0x7FFF7FFFu;  // magnitudes
-    const uint32_t Ep = max_u16x2((w >> 7) & 0x00FF00FFu, 0x00010001u);
-    const uint32_t d = min_u16x2(add_u16x2(Ep, neg_eb), kExactWindow * 0x00010001u);
-    // bit 15 of a half: d reached the window's width; of y + 0x7FFF: y is not zero (a zero is
-    // left inside: its sig below is 0)
-    const uint32_t outside = ((d + (0x8000u - kExactWindow) * 0x00010001u) & (y + 0x7FFF7FFFu) & 0x80008000u) >> 15;
-    // per half: y + 128 - 128 Ep = sig (128 + m for E >= 1, m for E = 0), in [0, 255]
-    const uint32_t sig = (y + 0x00800080u - (Ep << 7)) & ~(outside * 0xFFFFu);
-    const uint32_t u0 = (sig & 0xFFFFu) << (d & 0xFFFFu), u1 = (sig >> 16) << (d >> 16);  // < 2^31
-    add96(a0, a1, a2, static_cast<unsigned long long>(u0) * u0 + static_cast<unsigned long long>(u1) * u1);
-    if (outside) {
-      if (outside & 1u) to_bin(w & 0xFFFFu);
-      if (outside >> 16) to_bin(w >> 16);
-    }
-  };
+  ExactWindow ew(Eb);
+  auto add_word = [&](uint32_t w) { ew.add_word(w, bins); };
   const uint4* src = reinterpret_cast<const uint4*>(x);
   const uint64_t nv = n / 8, first = c * (kChunk / 8);
   const uint64_t end = first + kChunk / 8 < nv ? first + kChunk / 8 : nv;  // whole vectors of the chunk
@@ -575,9 +543,9 @@ __device__ void exact_chunk(const uint16_t* x, uint64_t n, uint64_t c, int Eb, u
   }
   if (c == (n - 1) / kChunk && lane < n % 8) add_word(x[8 * nv + lane]);  // the last n % 8 values
   // 128 terms per lane at most, each below 2^62: the chunk's sum fits in 96 bits
-  const unsigned long long s = (static_cast<unsigned long long>(a1) << 32) | a0;
+  const unsigned long long s = (static_cast<unsigned long long>(ew.a1) << 32) | ew.a0;
   lo += s;
-  hi += a2 + (lo < s);
+  hi += ew.a2 + (lo < s);
 }
 
 // Bounded wait (one thread) for the first phase's result.  False after an error or a timeout.

@@ -245,8 +245,8 @@ __global__ void __launch_bounds__(kThreads, 6) fused_kernel(const FusedParams p)
     if (S.need_exact) {  // the same in every CTA: exact per-exponent sums over the grid
       for (unsigned e = tid; e < 256; e += kThreads) S.bins[e] = 0;
       bar_cta();
-      add_exponent_sums(p.in + vb * 8, (ve - vb) * 8, tid, kThreads, S.bins);
-      if (first + mine == N && (n & 7)) add_exponent_sums(p.in + (nv << 3), n & 7, tid, kThreads, S.bins);
+      add_exponent_sums(p.in + vb * 8, (ve - vb) * 8, tid, kThreads, S.bins, S.own);
+      if (first + mine == N && (n & 7)) add_exponent_sums(p.in + (nv << 3), n & 7, tid, kThreads, S.bins, S.own);
       bar_cta();
       for (unsigned e = tid; e < 256; e += kThreads)
         if (S.bins[e]) atomicAdd(gbins + e, S.bins[e]);

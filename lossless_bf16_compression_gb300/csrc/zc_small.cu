@@ -385,7 +385,7 @@ __device__ void compress_resident(Exchange& X, ResidentSmem& S, const uint16_t* 
     bar_cta();
     for (unsigned j = 0; j < mine; ++j)
       add_exponent_sums(reinterpret_cast<const uint16_t*>(S.x[j]), chunk_values(n, first + j), tid, kSmallThreads,
-                        S.bins);
+                        S.bins, S.e0);
     bar_cta();
     X.share_bins(S);
     if (!X.sync()) return false;

@@ -292,16 +292,67 @@ __device__ void guess_e0(const uint32_t (&w)[W], unsigned vals, float* g2, float
   bar();
 }
 
-// Per-exponent integer sums of sig^2 of the finite values x[i], i = start, start + stride, ..
-// < count, added into bins[E] (shared, 256 words; E = 0 and 1 share bin 1).
-__device__ __forceinline__ void add_exponent_sums(const uint16_t* x, uint64_t count, uint64_t start, uint64_t stride,
-                                                  unsigned long long* bins) {
-  for (uint64_t i = start; i < count; i += stride) {
-    const unsigned v = x[i];
-    const unsigned E = (v >> 7) & 0xFF;
-    if (E == 255 || (v & 0x7FFF) == 0) continue;
-    const unsigned sig = E ? 128 + (v & 0x7F) : (v & 0x7F);
+// Exact sums of squares, one thread: sig^2 4^d, d = E - Eb, of the values whose exponent E
+// (subnormals at 1) lies in the window [Eb, Eb + 24), in a 96-bit integer (a0, a1, a2); a finite
+// nonzero value outside the window adds sig^2 to bins[E] instead (shared memory).  Two values of
+// a word at a time: E and d in packed 16-bit halves, d clamped to the window's width; sig as
+// y + 128 - 128 E from the magnitude y (128 + m for E >= 1, m for E = 0); the term as
+// (sig << d)^2 (below 2^62) by one widening multiply, added by a carry chain.  A value outside
+// the window has its sig masked to zero in that step and takes a branch to its bin; a zero stays
+// inside and adds nothing, and Inf/NaN (E = 255) are outside and skipped there.  No atomics on
+// the common path: a tensor's values share a handful of exponents, which per-value atomics on
+// their bins would serialise.
+constexpr int kExactWindow = 24;
+struct ExactWindow {
+  uint32_t neg_eb;  // -Eb in both halves
+  unsigned a0 = 0, a1 = 0, a2 = 0;
+  __device__ explicit ExactWindow(int Eb) : neg_eb(((0x10000u - static_cast<unsigned>(Eb)) & 0xFFFFu) * 0x00010001u) {}
+  __device__ __forceinline__ void add_word(uint32_t w, unsigned long long* bins) {
+    const uint32_t y = w & 0x7FFF7FFFu;
+    const uint32_t Ep = max_u16x2((w >> 7) & 0x00FF00FFu, 0x00010001u);
+    const uint32_t d = min_u16x2(add_u16x2(Ep, neg_eb), kExactWindow * 0x00010001u);
+    // bit 15 of a half: d reached the window's width, and y is not zero
+    const uint32_t outside = ((d + (0x8000u - kExactWindow) * 0x00010001u) & (y + 0x7FFF7FFFu) & 0x80008000u) >> 15;
+    const uint32_t sig = (y + 0x00800080u - (Ep << 7)) & ~(outside * 0xFFFFu);
+    const uint32_t u0 = (sig & 0xFFFFu) << (d & 0xFFFFu), u1 = (sig >> 16) << (d >> 16);  // < 2^31
+    const unsigned long long t = static_cast<unsigned long long>(u0) * u0 + static_cast<unsigned long long>(u1) * u1;
+    asm("add.cc.u32 %0, %0, %3;\n\taddc.cc.u32 %1, %1, %4;\n\taddc.u32 %2, %2, 0;"
+        : "+r"(a0), "+r"(a1), "+r"(a2)
+        : "r"(static_cast<unsigned>(t)), "r"(static_cast<unsigned>(t >> 32)));
+    if (outside) {
+      if (outside & 1u) to_bin(w & 0xFFFFu, bins);
+      if (outside >> 16) to_bin(w >> 16, bins);
+    }
+  }
+  __device__ static void to_bin(unsigned b, unsigned long long* bins) {
+    const unsigned E = (b >> 7) & 0xFF;
+    if (E == 255 || (b & 0x7FFF) == 0) return;
+    const unsigned sig = E ? 128 + (b & 0x7F) : (b & 0x7F);
     atomicAdd(bins + (E ? E : 1), static_cast<unsigned long long>(sig * sig));
+  }
+};
+
+// Per-exponent integer sums of sig^2 of the finite values x[0..count), the thread taking words
+// (value pairs) start, start + stride, .., added into bins[E] (shared, 256 words; E = 0 and 1
+// share bin 1; x 4-byte aligned).  Called by every thread of the CTA alike (warp reductions).
+// The values in the 24-binade window from Eb = anchor_e0 - 12 (around a Gaussian's typical
+// exponent; clamped to [1, 214]) are summed exactly in registers (ExactWindow); the thread's
+// 96-bit sum goes to the bins as six 16-bit pieces, each summed over the warp: piece j weighs
+// 2^(16 j) 4^(E - Eb), which is the weight of bin Eb + 8 j (bin e counts 4^e).  anchor_e0 only
+// steers speed: any value gives the same bins' total.
+__device__ __forceinline__ void add_exponent_sums(const uint16_t* x, uint64_t count, uint64_t start, uint64_t stride,
+                                                  unsigned long long* bins, int anchor_e0) {
+  int Eb = anchor_e0 - 12;
+  Eb = Eb < 1 ? 1 : (Eb > 214 ? 214 : Eb);
+  ExactWindow ew(Eb);
+  const uint32_t* w = reinterpret_cast<const uint32_t*>(x);
+  for (uint64_t i = start; i < count / 2; i += stride) ew.add_word(w[i], bins);
+  if ((count & 1) && start == 0) ew.add_word(x[count - 1], bins);  // an odd last value
+  const unsigned piece[6] = {ew.a0 & 0xFFFFu, ew.a0 >> 16, ew.a1 & 0xFFFFu, ew.a1 >> 16, ew.a2 & 0xFFFFu, ew.a2 >> 16};
+#pragma unroll
+  for (int j = 0; j < 6; ++j) {
+    const unsigned s = __reduce_add_sync(0xFFFFFFFFu, piece[j]);  // 32 pieces below 2^16
+    if ((threadIdx.x & 31) == 0 && s) atomicAdd(bins + Eb + 8 * j, static_cast<unsigned long long>(s));
   }
 }
 
